@@ -1,0 +1,90 @@
+// Shared helpers of the libmtp kernels: status plumbing, the per-file device
+// error word, bounded waits, bf16 conversion and small warp reductions.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/mtp.h"
+
+#define MTP_CUDA_TRY(expr)                                \
+  do {                                                    \
+    cudaError_t mtp_e_ = (expr);                          \
+    if (mtp_e_ != cudaSuccess) return MTP_ERR_CUDA;       \
+  } while (0)
+
+#define MTP_LAUNCH_CHECK()                                \
+  do {                                                    \
+    if (cudaPeekAtLastError() != cudaSuccess) {           \
+      (void)cudaGetLastError();                           \
+      return MTP_ERR_CUDA;                                \
+    }                                                     \
+  } while (0)
+
+// Each kernel file owns one device error word; mtp_check_errors ORs them.
+// `take` reads and clears it (the stream has been synchronised by then).
+#define MTP_DEFINE_ERROR_WORD(take_fn)                                        \
+  static __device__ unsigned int g_mtp_error_word = 0;                        \
+  unsigned int take_fn() {                                                    \
+    unsigned int v = 0, zero = 0;                                             \
+    if (cudaMemcpyFromSymbol(&v, g_mtp_error_word, sizeof(v)) != cudaSuccess) \
+      return 0xFFFFFFFFu;                                                     \
+    cudaMemcpyToSymbol(g_mtp_error_word, &zero, sizeof(zero));                \
+    return v;                                                                 \
+  }
+
+namespace mtp {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// A pipeline wait gives up after this long; a legitimate wait lasts microseconds.
+constexpr uint64_t kWaitLimitNs = 1500ull * 1000ull * 1000ull;
+
+__device__ __forceinline__ float bf16_to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ __nv_bfloat16 f32_to_bf16(float v) { return __float2bfloat16_rn(v); }
+
+template <typename T> __device__ __forceinline__ float load_f32(const T* p);
+template <> __device__ __forceinline__ float load_f32<float>(const float* p) { return *p; }
+template <> __device__ __forceinline__ float load_f32<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+// Inclusive prefix sum across the warp (lane order).
+__device__ __forceinline__ double warp_inclusive_scan(double v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    double n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+}  // namespace mtp

@@ -1,0 +1,624 @@
+// tcgen05 GEMM core for sm_103a: acc[M,N] = A[M,K] · B[N,K]^T, bf16 operands,
+// fp32 accumulation in tensor memory, fused epilogues.
+//
+// Persistent, warp-specialised CTA of 6 warps, one CTA per SM:
+//   warp 0     TMA producer: 128x64 A box and BNx64 B box (128-byte swizzle)
+//              per k-block into a STAGES-deep shared-memory ring (mbarriers
+//              with transaction counts).
+//   warp 1     allocates 2*BN TMEM columns; one thread issues
+//              tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16) four
+//              times per k-block and tcgen05.commit's the smem slot back to
+//              the producer; a whole tile's accumulator is committed to the
+//              epilogue.  Two accumulators alternate so the epilogue of tile
+//              i overlaps the MMAs of tile i+1.
+//   warps 2-5  epilogue: tcgen05.ld 32 lanes x 32 columns per load (warp w
+//              reads TMEM lanes 32*(w%4)..+31 = tile rows), applies the fused
+//              operation and stores bf16 rows (or CE partials).
+// Every mbarrier wait is bounded: after ~1.5 s it sets MTP_DEVERR_TIMEOUT,
+// raises a CTA abort flag and every role drains out; the producer then waits
+// (bounded) for its in-flight copies and warp 1 for its MMAs before freeing
+// TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "gemm_tc.cuh"
+
+MTP_DEFINE_ERROR_WORD(mtp_take_errors_gemm)
+
+namespace mtp {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle atom row
+constexpr int kThreads = 192;
+constexpr int kGroupM = 16;
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase of `parity` to complete; false on abort or timeout.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(&g_mtp_error_word, MTP_DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+// Teardown wait that ignores the abort flag (bounded by `limit_ns`).
+__device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// 32 consecutive fp32 columns of this thread's TMEM lane; the wait is part of
+// the same asm statement so no use of the registers can precede it.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor of a K-major bf16 tile stored as rows of
+// 128 bytes with the 128-byte swizzle (what TMA writes with
+// CU_TENSOR_MAP_SWIZZLE_128B): start address >> 4 (bits 0-13), leading byte
+// offset 16 B (unused for swizzled K-major), stride byte offset 1024 B
+// between 8-row groups (bits 32-45), descriptor version 1 (bit 46),
+// layout type 2 = 128-byte swizzle (bits 61-63).  The tile base is
+// 1024-byte aligned so the base-offset field stays 0.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+struct Args {
+  int M, N, K;
+  int seg_rows;
+  int tiles_m, tiles_n, nk;
+  __nv_bfloat16* out;
+  int ldo;
+  const __nv_bfloat16* resid;
+  int ldr;
+  const int32_t* pos;
+  const float2* rope;
+  int rope_len, rope_cols, head_dim;
+  const int32_t* labels;
+  float2* ce_part;
+  float* z_tgt;
+};
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
+  const int per_group = kGroupM * tiles_n;
+  const int group = t / per_group;
+  const int first_m = group * kGroupM;
+  const int gsz = min(tiles_m - first_m, kGroupM);
+  const int r = t - group * per_group;
+  tm = first_m + r % gsz;
+  tn = r / gsz;
+}
+
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&v)[32], int valid) {
+  if (valid >= 32) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      __nv_bfloat162 h[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
+      d4[q] = *reinterpret_cast<uint4*>(h);
+    }
+  } else {
+    for (int i = 0; i < valid; ++i) dst[i] = __float2bfloat16_rn(v[i]);
+  }
+}
+__device__ __forceinline__ void load_row32(const __nv_bfloat16* src, float (&v)[32], int valid) {
+  if (valid >= 32) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 u = s4[q];
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        v[8 * q + 2 * i] = f.x;
+        v[8 * q + 2 * i + 1] = f.y;
+      }
+    }
+  } else {
+    for (int i = 0; i < 32; ++i) v[i] = i < valid ? __bfloat162float(src[i]) : 0.0f;
+  }
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+               const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
+               const Args P) {
+  using C = Cfg<BN>;
+  constexpr int S = C::kStages;
+  constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
+  const uint32_t final_bar = bar0 + 8u * (2 * S + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 128);
+    }
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int ntiles = P.tiles_m * P.tiles_n;
+  const int nk = P.nk;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------ producer ------------------------------
+    int stage = 0;
+    uint32_t phase = 0;
+    bool issued[S];
+    uint32_t armed[S];
+#pragma unroll
+    for (int s = 0; s < S; ++s) { issued[s] = false; armed[s] = 0; }
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+      int tm, tn;
+      tile_coords(t, P.tiles_m, P.tiles_n, tm, tn);
+      const CUtensorMap* bmap = &tmB0;
+      int by;
+      if constexpr (EPI == EPI_SWIGLU) {
+        by = tn * (BN / 2);
+      } else {
+        const int n0 = tn * BN;
+        const int seg = n0 / P.seg_rows;
+        by = n0 - seg * P.seg_rows;
+        bmap = seg == 0 ? &tmB0 : (seg == 1 ? &tmB1 : &tmB2);
+      }
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+        const uint32_t sa = base + stage * C::kStageBytes;
+        const uint32_t sb = sa + C::kABytes;
+        mbar_expect_tx(full_bar(stage), C::kStageBytes);
+        tma_load_2d(sa, &tmA, kb * BK, tm * BM, full_bar(stage));
+        if constexpr (EPI == EPI_SWIGLU) {
+          tma_load_2d(sb, &tmB0, kb * BK, by, full_bar(stage));
+          tma_load_2d(sb + (BN / 2) * BK * 2, &tmB1, kb * BK, by, full_bar(stage));
+        } else {
+          tma_load_2d(sb, bmap, kb * BK, by, full_bar(stage));
+        }
+        issued[stage] = true;
+        armed[stage] = phase;
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (*abort_flag) {  // let every copy this thread started land before the CTA exits
+      for (int s = 0; s < S; ++s)
+        if (issued[s]) mbar_wait_drain(full_bar(s), armed[s], 20ull * 1000 * 1000);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------ MMA issuer ------------------------------
+    int stage = 0;
+    uint32_t phase = 0;
+    int local = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++local) {
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sa = base + stage * C::kStageBytes;
+        const uint64_t adesc = sdesc_sw128(sa);
+        const uint64_t bdesc = sdesc_sw128(sa + C::kABytes);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (kb | kk) != 0);
+        umma_commit(empty_bar(stage));
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+      if (ok) umma_commit(tfull_bar(acc));
+    }
+  } else if (warp >= 2) {
+    // ------------------------------ epilogue ------------------------------
+    const int quarter = warp & 3;
+    int local = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++local) {
+      int tm, tn;
+      tile_coords(t, P.tiles_m, P.tiles_n, tm, tn);
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
+      tc_fence_after();
+      const int row = tm * BM + quarter * 32 + lane;
+      const bool row_ok = row < P.M;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+
+      if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(taddr + c * 32, v);
+          const int col0 = tn * BN + c * 32;
+          if (row_ok && col0 < P.N) {
+            const int valid = min(32, P.N - col0);
+            if constexpr (EPI == EPI_RESID) {
+              float r[32];
+              load_row32(P.resid + static_cast<size_t>(row) * P.ldr + col0, r, valid);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] += r[i];
+            }
+            store_row32(P.out + static_cast<size_t>(row) * P.ldo + col0, v, valid);
+          }
+        }
+      } else if constexpr (EPI == EPI_ROPE) {
+        const int tile_col0 = tn * BN;
+        if (tile_col0 >= P.rope_cols) {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_ld32(taddr + c * 32, v);
+            const int col0 = tile_col0 + c * 32;
+            if (row_ok && col0 < P.N) store_row32(P.out + static_cast<size_t>(row) * P.ldo + col0, v, min(32, P.N - col0));
+          }
+        } else {
+          const int hd = P.head_dim, half = hd >> 1;
+          int p = row_ok ? P.pos[row] : 0;
+          if (p < 0 || p >= P.rope_len) {
+            if (row_ok) atomicOr(&g_mtp_error_word, MTP_DEVERR_TOKEN_RANGE);
+            p = min(max(p, 0), P.rope_len - 1);
+          }
+          const float2* tab = P.rope + static_cast<size_t>(p) * half;
+#pragma unroll 1
+          for (int h0 = 0; h0 < BN; h0 += hd) {
+#pragma unroll 1
+            for (int j = 0; j < half; j += 32) {
+              float x1[32], x2[32];
+              tmem_ld32(taddr + h0 + j, x1);
+              tmem_ld32(taddr + h0 + half + j, x2);
+              if (row_ok) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  const float2 cs = tab[j + i];
+                  const float a = x1[i], b = x2[i];
+                  x1[i] = a * cs.x - b * cs.y;
+                  x2[i] = b * cs.x + a * cs.y;
+                }
+                const int col = tile_col0 + h0 + j;
+                store_row32(P.out + static_cast<size_t>(row) * P.ldo + col, x1, 32);
+                store_row32(P.out + static_cast<size_t>(row) * P.ldo + col + half, x2, 32);
+              }
+            }
+          }
+        }
+      } else if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          float g[32], u[32];
+          tmem_ld32(taddr + c * 32, g);
+          tmem_ld32(taddr + BN / 2 + c * 32, u);
+          const int col0 = tn * (BN / 2) + c * 32;
+          if (row_ok && col0 < P.N) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) g[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
+            store_row32(P.out + static_cast<size_t>(row) * P.ldo + col0, g, min(32, P.N - col0));
+          }
+        }
+      } else if constexpr (EPI == EPI_CE) {
+        const int lab = row_ok ? P.labels[row] : -1;
+        float m_run = -INFINITY, s_run = 0.0f, zt = 0.0f;
+        bool has_t = false;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(taddr + c * 32, v);
+          const int col0 = tn * BN + c * 32;
+          const int valid = min(32, P.N - col0);
+          float cmax = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i < valid) cmax = fmaxf(cmax, v[i]);
+          const float m_new = fmaxf(m_run, cmax);
+          if (m_new != -INFINITY) {
+            float s = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < valid) s += __expf(v[i] - m_new);
+            s_run = s_run * __expf(m_run - m_new) + s;
+            m_run = m_new;
+          }
+          const int off = lab - col0;
+          if (off >= 0 && off < 32 && off < valid) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i == off) zt = v[i];
+            has_t = true;
+          }
+        }
+        if (row_ok) {
+          P.ce_part[static_cast<size_t>(row) * P.tiles_n + tn] = make_float2(m_run, s_run);
+          if (has_t) P.z_tgt[row] = zt;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    if (lane == 0) {  // every MMA this CTA issued has completed before TMEM is freed
+      umma_commit(final_bar);
+      mbar_wait_drain(final_bar, 0, 20ull * 1000 * 1000);
+    }
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D bf16 tensor [rows, cols] with row stride `ld` elements, box 64 x box_rows.
+bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int ld, int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+template <int BN, int EPI>
+mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
+  using C = Cfg<BN>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
+      return MTP_ERR_CUDA;
+    attr_done = true;
+  }
+  CUtensorMap ta, tb[3];
+  const int box_b = EPI == EPI_SWIGLU ? BN / 2 : BN;
+  if (!make_map(&ta, g.A, g.M, g.K, g.lda, BM)) return MTP_ERR_INVALID_ARG;
+  const int nmaps = EPI == EPI_SWIGLU ? 2 : g.nseg;
+  const int brows = EPI == EPI_SWIGLU ? g.N : g.seg_rows;
+  for (int i = 0; i < 3; ++i) {
+    const void* ptr = g.B[i < nmaps ? i : 0];
+    if (!make_map(&tb[i], ptr, brows, g.K, g.ldb, box_b)) return MTP_ERR_INVALID_ARG;
+  }
+  Args a{};
+  a.M = g.M;
+  a.N = g.N;
+  a.K = g.K;
+  a.seg_rows = g.seg_rows > 0 ? g.seg_rows : g.N;
+  a.tiles_m = (g.M + BM - 1) / BM;
+  a.tiles_n = (g.N + (EPI == EPI_SWIGLU ? BN / 2 : BN) - 1) / (EPI == EPI_SWIGLU ? BN / 2 : BN);
+  a.nk = (g.K + BK - 1) / BK;
+  a.out = g.out;
+  a.ldo = g.ldo;
+  a.resid = g.resid;
+  a.ldr = g.ldr;
+  a.pos = g.pos;
+  a.rope = g.rope;
+  a.rope_len = g.rope_len;
+  a.rope_cols = g.rope_cols;
+  a.head_dim = g.head_dim;
+  a.labels = g.labels;
+  a.ce_part = g.ce_part;
+  a.z_tgt = g.z_tgt;
+  const int ntiles = a.tiles_m * a.tiles_n;
+  const int grid = ntiles < num_sms() ? ntiles : num_sms();
+  gemm_tc_kernel<BN, EPI><<<grid, kThreads, C::kSmemBytes, stream>>>(ta, tb[0], tb[1], tb[2], a);
+  MTP_LAUNCH_CHECK();
+  return MTP_OK;
+}
+
+}  // namespace
+
+int gemm_ce_tile_n() { return 256; }
+
+mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream) {
+  if (g.M <= 0 || g.N <= 0 || g.K <= 0) return MTP_ERR_SHAPE;
+  if (!g.A || !g.B[0]) return MTP_ERR_INVALID_ARG;
+  if (g.K % 8 || g.lda % 8 || g.ldb % 8) return MTP_ERR_ALIGNMENT;
+  if (!aligned16(g.A)) return MTP_ERR_ALIGNMENT;
+  for (int i = 0; i < 3; ++i)
+    if (g.B[i] && !aligned16(g.B[i])) return MTP_ERR_ALIGNMENT;
+  if (g.epi != EPI_CE && (!g.out || g.ldo % 8 || !aligned16(g.out))) return MTP_ERR_ALIGNMENT;
+  if (!encoder()) return MTP_ERR_CUDA;
+  switch (g.epi) {
+    case EPI_STORE:
+    case EPI_RESID: {
+      if (g.epi == EPI_RESID && (!g.resid || g.ldr % 8 || !aligned16(g.resid))) return MTP_ERR_ALIGNMENT;
+      const int seg = g.seg_rows > 0 ? g.seg_rows : g.N;
+      if (g.nseg > 1 && seg % 128) return MTP_ERR_UNSUPPORTED;
+      const bool wide = (g.nseg == 1 || seg % 256 == 0);
+      if (g.epi == EPI_STORE) return wide ? launch<256, EPI_STORE>(g, stream) : launch<128, EPI_STORE>(g, stream);
+      return wide ? launch<256, EPI_RESID>(g, stream) : launch<128, EPI_RESID>(g, stream);
+    }
+    case EPI_ROPE: {
+      const int seg = g.seg_rows > 0 ? g.seg_rows : g.N;
+      if ((g.head_dim != 64 && g.head_dim != 128) || !g.pos || !g.rope || g.rope_len <= 0) return MTP_ERR_INVALID_ARG;
+      if (seg % 128 || g.rope_cols % 128) return MTP_ERR_UNSUPPORTED;
+      return (seg % 256 == 0 && g.rope_cols % 256 == 0) ? launch<256, EPI_ROPE>(g, stream)
+                                                         : launch<128, EPI_ROPE>(g, stream);
+    }
+    case EPI_SWIGLU:
+      if (!g.B[1] || !aligned16(g.B[1])) return MTP_ERR_INVALID_ARG;
+      return launch<256, EPI_SWIGLU>(g, stream);
+    case EPI_CE:
+      if (!g.labels || !g.ce_part || !g.z_tgt) return MTP_ERR_INVALID_ARG;
+      return launch<256, EPI_CE>(g, stream);
+    default:
+      return MTP_ERR_INVALID_ARG;
+  }
+}
+
+}  // namespace mtp
+
+extern "C" mtp_status mtp_gemm_bf16(int M, int N, int K, const void* A, const void* B, void* C,
+                                    cudaStream_t stream) {
+  if (!A || !B || !C) return MTP_ERR_INVALID_ARG;
+  mtp::GemmDesc g;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.A = static_cast<const __nv_bfloat16*>(A);
+  g.lda = K;
+  g.B[0] = static_cast<const __nv_bfloat16*>(B);
+  g.ldb = K;
+  g.nseg = 1;
+  g.seg_rows = N;
+  g.epi = mtp::EPI_STORE;
+  g.out = static_cast<__nv_bfloat16*>(C);
+  g.ldo = N;
+  return mtp::gemm_bf16_launch(g, stream);
+}

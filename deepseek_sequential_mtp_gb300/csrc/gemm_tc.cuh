@@ -1,0 +1,49 @@
+// Internal interface of the tcgen05 GEMM core (gemm_tc.cu) used by the chain.
+#pragma once
+
+#include "common.cuh"
+
+namespace mtp {
+
+enum GemmEpilogue : int {
+  EPI_STORE = 0,   // out = acc
+  EPI_RESID = 1,   // out = resid + acc
+  EPI_ROPE = 2,    // out = RoPE(acc) on columns < rope_cols, acc elsewhere
+  EPI_SWIGLU = 3,  // out[:, j] = silu(gate_j) * up_j; B = (gate, up) stacked per tile
+  EPI_CE = 4       // no output: per (row, vocab tile) online max / sum-exp and the label logit
+};
+
+// C-side description of one GEMM  acc[M, N] = A[M, K] · B[N, K]^T  (bf16 in,
+// fp32 accumulate).  B may be given as up to three row segments of
+// `seg_rows` rows each (q/k/v weights); for EPI_SWIGLU B[0] = gate [N, K]
+// and B[1] = up [N, K] and N counts output columns.
+struct GemmDesc {
+  int M = 0, N = 0, K = 0;
+  const __nv_bfloat16* A = nullptr;
+  int lda = 0;
+  const __nv_bfloat16* B[3] = {nullptr, nullptr, nullptr};
+  int ldb = 0;
+  int nseg = 1;
+  int seg_rows = 0;
+  int epi = EPI_STORE;
+  __nv_bfloat16* out = nullptr;
+  int ldo = 0;
+  const __nv_bfloat16* resid = nullptr;
+  int ldr = 0;
+  // RoPE: pos [M] in [0, rope_len), table [rope_len, head_dim/2] of (cos, sin)
+  const int32_t* pos = nullptr;
+  const float2* rope = nullptr;
+  int rope_len = 0, rope_cols = 0, head_dim = 0;
+  // CE: labels [M] (-1 = none); ce_part [M, n_vtiles] (max, sumexp); z_tgt [M]
+  const int32_t* labels = nullptr;
+  float2* ce_part = nullptr;
+  float* z_tgt = nullptr;
+};
+
+// Tile width along N the launcher will use for this descriptor (CE partial
+// buffers are sized by ceil(N / ce_tile_n)).
+int gemm_ce_tile_n();
+
+mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream);
+
+}  // namespace mtp

@@ -1,0 +1,246 @@
+"""Thin ctypes binding of libmtp (include/mtp.h).
+
+Argument marshalling only: every step of the hot path runs in the library's
+CUDA kernels.  PyTorch supplies device memory and the current stream.  The
+binding raises if the library is missing or a call returns an error; there
+is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmtp.so")
+
+MTP_F32, MTP_BF16 = 0, 1
+DEN = {"fixed": 0, "masked_mean": 1}
+VERIFY_STATUS = {0: "ok", 1: "invalid_draft", 2: "zero_residual", 3: "invalid_probs",
+                 4: "invalid_budget"}
+
+
+class MtpError(RuntimeError):
+    pass
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("d", ctypes.c_int),
+                ("n_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("ffn", ctypes.c_int),
+                ("V", ctypes.c_int), ("D", ctypes.c_int), ("eps", ctypes.c_float),
+                ("rope_base", ctypes.c_float), ("dtype", ctypes.c_int)]
+
+
+_PP = ctypes.POINTER(ctypes.c_void_p)
+_WEIGHT_LISTS = ("hnorm", "enorm", "eh_proj", "attn_norm", "wq", "wk", "wv", "wo",
+                 "ffn_norm", "w_gate", "w_up", "w_down")
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("embed", ctypes.c_void_p), ("head", ctypes.c_void_p),
+                ("out_norm", ctypes.c_void_p)] + [(k, _PP) for k in _WEIGHT_LISTS]
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libmtp.so (built by ``__graft_entry__.build()``); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise MtpError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, u64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t
+    lib.mtp_status_string.restype = ctypes.c_char_p
+    lib.mtp_status_string.argtypes = [i32]
+    lib.mtp_abi_version.restype = i32
+    lib.mtp_check_errors.restype = i32
+    lib.mtp_check_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+    lib.spec_verify.restype = i32
+    lib.spec_verify.argtypes = [i32, i32, i32, vp, vp, vp, u64, u64, vp, vp, vp, vp, vp, vp, vp]
+    lib.mtp_gemm_bf16.restype = i32
+    lib.mtp_gemm_bf16.argtypes = [i32, i32, i32, vp, vp, vp, vp]
+    lib.mtp_chain_workspace_bytes.restype = sz
+    lib.mtp_chain_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
+    lib.mtp_chain_forward.restype = i32
+    lib.mtp_chain_forward.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Weights),
+                                      vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.mtp_chain_loss.restype = i32
+    lib.mtp_chain_loss.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Weights),
+                                   vp, vp, vp, vp, ctypes.c_float, i32, i32,
+                                   vp, vp, vp, vp, vp, sz, vp]
+    _lib = lib
+    return lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        msg = load().mtp_status_string(status).decode()
+        raise MtpError(f"{what}: {msg} (status {status})")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype):
+    if not t.is_cuda:
+        raise MtpError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise MtpError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise MtpError(f"{name} must be contiguous")
+
+
+def check_errors(stream=None) -> int:
+    """Synchronise and return the device error bits (raises if any is set)."""
+    flags = ctypes.c_uint(0)
+    st = load().mtp_check_errors(_stream(stream), ctypes.byref(flags))
+    if st != 0:
+        raise MtpError(f"device error word 0x{flags.value:x} ({load().mtp_status_string(st).decode()})")
+    return flags.value
+
+
+# --------------------------------------------------------------------------
+# spec_verify
+# --------------------------------------------------------------------------
+def spec_verify(p: torch.Tensor, q: torch.Tensor, draft: torch.Tensor, seed: int, offset: int,
+                eos: Optional[torch.Tensor] = None, remaining: Optional[torch.Tensor] = None,
+                out: Optional[dict] = None, stream=None) -> dict:
+    """Exact speculative verification (include/mtp.h: spec_verify)."""
+    R, gamma = draft.shape
+    V = p.shape[-1]
+    _need(p, "p", torch.float32)
+    _need(q, "q", torch.float32)
+    _need(draft, "draft", torch.int32)
+    if p.shape != (R, gamma + 1, V) or q.shape != (R, gamma, V):
+        raise MtpError("p must be [R, gamma+1, V] and q [R, gamma, V]")
+    for name, t in (("eos", eos), ("remaining", remaining)):
+        if t is not None:
+            _need(t, name, torch.int32)
+    if out is None:
+        out = {k: torch.empty(R, dtype=torch.int32, device=p.device)
+               for k in ("accepted", "next_token", "n_emit", "status")}
+    st = load().spec_verify(R, gamma, V, _ptr(p), _ptr(q), _ptr(draft),
+                            int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                            _ptr(eos), _ptr(remaining), _ptr(out["accepted"]),
+                            _ptr(out["next_token"]), _ptr(out["n_emit"]), _ptr(out["status"]),
+                            _stream(stream))
+    _check(st, "spec_verify")
+    return out
+
+
+# --------------------------------------------------------------------------
+# GEMM diagnostic
+# --------------------------------------------------------------------------
+def gemm_bf16(A: torch.Tensor, B: torch.Tensor, C: Optional[torch.Tensor] = None, stream=None):
+    """C = A · B^T on the library's tcgen05 GEMM core (bf16 in/out, fp32 accumulate)."""
+    _need(A, "A", torch.bfloat16)
+    _need(B, "B", torch.bfloat16)
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise MtpError("A and B must share K")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _check(load().mtp_gemm_bf16(M, N, K, _ptr(A), _ptr(B), _ptr(C), _stream(stream)), "mtp_gemm_bf16")
+    return C
+
+
+# --------------------------------------------------------------------------
+# Chain
+# --------------------------------------------------------------------------
+def make_dims(cfg) -> Dims:
+    return Dims(cfg.B, cfg.T, cfg.d, cfg.n_heads, cfg.head_dim, cfg.ffn, cfg.V, cfg.D,
+                cfg.eps, cfg.rope_base, MTP_BF16 if cfg.dtype == "bf16" else MTP_F32)
+
+
+class ChainWeights:
+    """Holds the ctypes views of a weight dict (see synth.make_weights)."""
+
+    def __init__(self, weights: dict, D: int):
+        self._keep = []
+        self.struct = Weights()
+        self.struct.embed = weights["embed"].data_ptr()
+        self.struct.head = weights["head"].data_ptr()
+        self.struct.out_norm = weights["out_norm"].data_ptr()
+        for k in _WEIGHT_LISTS:
+            lst = weights[k]
+            if len(lst) != D:
+                raise MtpError(f"weights[{k!r}] must have D={D} entries")
+            arr = (ctypes.c_void_p * D)(*[t.data_ptr() for t in lst])
+            self._keep.append(arr)
+            setattr(self.struct, k, ctypes.cast(arr, _PP))
+
+
+def _check_chain_inputs(cfg, tokens, seg, pos, h0, weights):
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    for name, t in (("tokens", tokens), ("seg", seg), ("pos", pos)):
+        _need(t, name, torch.int32)
+        if tuple(t.shape) != (cfg.B, cfg.T):
+            raise MtpError(f"{name} must be [B, T]")
+    _need(h0, "h0", dt)
+    for k, v in weights.items():
+        for t in (v if isinstance(v, (list, tuple)) else [v]):
+            _need(t, k, dt)
+    return dt
+
+
+def chain_workspace_bytes(cfg) -> int:
+    dims = make_dims(cfg)
+    return int(load().mtp_chain_workspace_bytes(ctypes.byref(dims)))
+
+
+class Chain:
+    """Reusable call state (dims, weight views, workspace) for one shape."""
+
+    def __init__(self, cfg, weights: dict, device="cuda"):
+        self.cfg = cfg
+        self.dims = make_dims(cfg)
+        self.w = ChainWeights(weights, cfg.D)
+        self.weights = weights
+        nbytes = chain_workspace_bytes(cfg)
+        if nbytes == 0:
+            raise MtpError("invalid chain dimensions")
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def forward(self, tokens, seg, pos, h0, h_out=None, stream=None):
+        cfg = self.cfg
+        dt = _check_chain_inputs(cfg, tokens, seg, pos, h0, self.weights)
+        if h_out is None:
+            h_out = torch.empty((cfg.D, cfg.B, cfg.T, cfg.d), dtype=dt, device=h0.device)
+        st = load().mtp_chain_forward(ctypes.byref(self.dims), ctypes.byref(self.w.struct),
+                                      _ptr(tokens), _ptr(seg), _ptr(pos), _ptr(h0), _ptr(h_out),
+                                      _ptr(self.ws), self.ws.numel(), _stream(stream))
+        _check(st, "mtp_chain_forward")
+        return h_out
+
+    def loss(self, tokens, seg, pos, h0, lam=None, den="fixed", with_main=True,
+             row_loss=False, h_out=None, out=None, stream=None):
+        cfg = self.cfg
+        _check_chain_inputs(cfg, tokens, seg, pos, h0, self.weights)
+        dev = h0.device
+        if out is None:
+            out = {"sums_counts": torch.empty(2 * (cfg.D + 1), dtype=torch.float64, device=dev),
+                   "losses": torch.empty(cfg.D + 2, dtype=torch.float32, device=dev)}
+            if row_loss:
+                out["row_loss"] = torch.empty((cfg.D + 1, cfg.B, cfg.T), dtype=torch.float32, device=dev)
+        st = load().mtp_chain_loss(ctypes.byref(self.dims), ctypes.byref(self.w.struct),
+                                   _ptr(tokens), _ptr(seg), _ptr(pos), _ptr(h0),
+                                   float(cfg.lam if lam is None else lam), DEN[den], int(with_main),
+                                   _ptr(out["sums_counts"]), _ptr(out["losses"]),
+                                   _ptr(out.get("row_loss")), _ptr(h_out),
+                                   _ptr(self.ws), self.ws.numel(), _stream(stream))
+        _check(st, "mtp_chain_loss")
+        if h_out is not None:
+            out["h"] = h_out
+        return out

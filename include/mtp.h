@@ -1,0 +1,202 @@
+/*
+ * mtp.h -- C ABI of libmtp: the data-parallel hot path of DeepSeek-V3-style
+ * sequential multi-token prediction on NVIDIA GB300 (sm_103a).
+ *
+ * Sources ("the pages"):
+ *   [M7.6] "M7.6 - DeepSeek MTP: Sequential Modules, Teacher Forcing, and
+ *          Speculative Runtime" (transformer-system.numinens.com)
+ *   [M7.4] "M7.4 - Multi-Token Prediction Foundations" (same site)
+ *   [SD]   speculative-decoding page, ailearn.mscapital.top ("投机解码")
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is a DEVICE pointer (cudaMalloc / torch CUDA
+ *     memory) unless the argument says "host".  Tensors are dense,
+ *     row-major, 16-byte aligned.  The caller owns all memory; the library
+ *     allocates nothing and keeps no state besides one device error word per
+ *     translation unit (read with mtp_check_errors) and the tensor-map
+ *     encoder entry point resolved on first use.
+ *   - Calls are asynchronous on `stream`.  Argument errors are detected on the
+ *     host, return a status and launch nothing.  Data-dependent errors (token
+ *     id out of range, a kernel wait that ran out of time) set bits of the
+ *     device error word (MTP_DEVERR_*) and never trap; spec_verify reports
+ *     per-request statuses instead.
+ *   - bf16 means IEEE bfloat16 storage with fp32 accumulation.  f32 means
+ *     fp32 storage and arithmetic.
+ */
+#ifndef MTP_H
+#define MTP_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MTP_ABI_VERSION 1
+
+typedef enum mtp_status {
+  MTP_OK = 0,
+  MTP_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad enum        */
+  MTP_ERR_SHAPE = 2,        /* inconsistent dimensions                      */
+  MTP_ERR_ALIGNMENT = 3,    /* pointer not 16-byte aligned                  */
+  MTP_ERR_WORKSPACE = 4,    /* workspace smaller than the query returned     */
+  MTP_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed             */
+  MTP_ERR_DEVICE = 6,       /* a kernel set the device error word           */
+  MTP_ERR_UNSUPPORTED = 7   /* a shape/dtype combination this build lacks   */
+} mtp_status;
+
+typedef enum mtp_dtype { MTP_F32 = 0, MTP_BF16 = 1 } mtp_dtype;
+
+/* Denominator policy of each loss term ([M7.6] §0x05).
+ * FIXED: every term (main and each depth) divided by B*T, the paper's fixed
+ *        denominator for a batch of B packed rows of T positions.
+ * MASKED_MEAN: each term divided by its own count of supervised rows; an
+ *        empty term is 0 and stays in the D-depth mean ([M7.6] §0x06A). */
+typedef enum mtp_den { MTP_DEN_FIXED = 0, MTP_DEN_MASKED_MEAN = 1 } mtp_den;
+
+/* Per-request status written by spec_verify. */
+enum {
+  MTP_VERIFY_OK = 0,
+  MTP_VERIFY_INVALID_DRAFT = 1,   /* draft id outside [0,V) or q_j[y_j] <= 0  */
+  MTP_VERIFY_ZERO_RESIDUAL = 2,   /* rejection (or bonus row) with no mass     */
+  MTP_VERIFY_INVALID_PROBS = 3,   /* NaN/Inf/negative entry in a row it read   */
+  MTP_VERIFY_INVALID_BUDGET = 4   /* remaining < 1                             */
+};
+
+/* Bits of the device error word. */
+enum {
+  MTP_DEVERR_TOKEN_RANGE = 1u,  /* a token id outside [0, V) was read (clamped) */
+  MTP_DEVERR_TIMEOUT = 2u,      /* a bounded pipeline wait gave up             */
+  MTP_DEVERR_SEGMENTS = 4u      /* a segment id re-appears after another one   */
+};
+
+/* Problem sizes of one chain call.
+ * B packed rows of T positions; model width d = n_heads * head_dim; SwiGLU
+ * width ffn; shared vocabulary V; D sequential MTP depths.  eps is the RMSNorm
+ * epsilon (the pages leave it open; 1e-6 recommended).  rope_base > 0 applies
+ * rotate-half rotary embedding with that base to q and k at the given
+ * positions; 0 disables it.  dtype is an mtp_dtype.
+ * bf16 requires d % 64 == 0, head_dim in {64, 128}, ffn % 8 == 0. */
+typedef struct mtp_dims {
+  int B, T, d, n_heads, head_dim, ffn, V, D;
+  float eps;
+  float rope_base;
+  int dtype;
+} mtp_dims;
+
+/* Weights of the chain ([M7.6] §0x03, §0x04B).  Shared by the main head and
+ * every depth (passed once): embed [V,d], head [V,d], out_norm [d].
+ * Per depth k = 0..D-1, each field below is a HOST array of D device
+ * pointers: hnorm, enorm, attn_norm, ffn_norm [d]; eh_proj [d, 2d] whose
+ * first d columns multiply the normalised hidden state and last d columns
+ * the normalised embedding ("he" order, [M7.6] §0x03, §0x07B); wq, wk, wv,
+ * wo [d, d]; w_gate, w_up [ffn, d]; w_down [d, ffn].  Every linear map is
+ * y = x W^T (row-major [out, in]).  Element type = dims.dtype. */
+typedef struct mtp_weights {
+  const void* embed;
+  const void* head;
+  const void* out_norm;
+  const void* const* hnorm;
+  const void* const* enorm;
+  const void* const* eh_proj;
+  const void* const* attn_norm;
+  const void* const* wq;
+  const void* const* wk;
+  const void* const* wv;
+  const void* const* wo;
+  const void* const* ffn_norm;
+  const void* const* w_gate;
+  const void* const* w_up;
+  const void* const* w_down;
+} mtp_weights;
+
+/* Bytes of device workspace mtp_chain_forward / mtp_chain_loss need for
+ * these sizes (0 if the sizes are invalid). */
+size_t mtp_chain_workspace_bytes(const mtp_dims* dims);
+
+/* Teacher-forced MTP chain, depths 1..D ([M7.6] §0x02-§0x04C, §0x06A).
+ * For depth k and position t of packed row b:
+ *   h̄ = RMSNorm_{h,k}(h^{k-1}_t), ē = RMSNorm_{e,k}(E[x_{t+k}]),
+ *   u = M_k [h̄; ē], a = u + Attn_k(RMSNorm_{a,k}(u)), h^k_t = a + FFN_k(RMSNorm_{f,k}(a))
+ * where attention is causal within the segment of t and FFN is SwiGLU.
+ * Row t has a state at depth k iff t, ..., t+k are active and in one
+ * segment ([M7.6] §0x04C); rows without a state are computed on clamped
+ * inputs but their values are undefined.
+ *   tokens [B,T] int32 in [0,V); seg [B,T] int32 segment ids, -1 = padding,
+ *   each id one contiguous run; pos [B,T] int32 RoPE positions (typically
+ *   the index within the segment); h0 [B,T,d] main-model hidden states.
+ *   h_out [D,B,T,d] receives h^1..h^D (pre-final-norm states).
+ *   ws: workspace of at least mtp_chain_workspace_bytes(dims) bytes. */
+mtp_status mtp_chain_forward(const mtp_dims* dims, const mtp_weights* w,
+                             const int32_t* tokens, const int32_t* seg, const int32_t* pos,
+                             const void* h0, void* h_out,
+                             void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Chain forward plus the shared head and masked cross-entropy
+ * ([M7.6] §0x03, §0x05; [M7.4] §0x06F), without materialising logits:
+ *   ℓ_t = log Σ_v exp(z_v) - z_label, z = W_U RMSNorm_out(h_t).
+ * Term 0 (main) uses h0 with label x_{t+1}, supervised where t+1 is active
+ * and in the segment of t; term k uses h^k with label x_{t+k+1}, supervised
+ * where t..t+k+1 are active and in one segment.  Then
+ *   L = L_main + (lambda / D) Σ_k L^(k), each term reduced by `den`.
+ *   sums_counts [2*(D+1)] double: (Σℓ, count) for main, then depths 1..D.
+ *   losses [D+2] float: L, L_main, L^(1)..L^(D).
+ *   row_loss [(D+1),B,T] float, nullable: ℓ per term and row, NaN where the
+ *   row is not supervised.  h_out nullable, as in mtp_chain_forward.
+ *   with_main = 0 skips the main term (L_main = 0, its sum/count = 0). */
+mtp_status mtp_chain_loss(const mtp_dims* dims, const mtp_weights* w,
+                          const int32_t* tokens, const int32_t* seg, const int32_t* pos,
+                          const void* h0, float lambda, int den, int with_main,
+                          double* sums_counts, float* losses, float* row_loss, void* h_out,
+                          void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Exact speculative verification of R requests with gamma drafts each
+ * ([M7.6] §0x09 one-proposal selector, generalised to gamma by the
+ * left-to-right rule of [SD]).  For j = 0..gamma-1: accept y_j iff
+ * u_j < min(1, p_j[y_j] / q_j[y_j]) (fp64); the first rejection emits a
+ * correction drawn from (p_j - q_j)+ / Σ(p_j - q_j)+ and ends the round; an
+ * accepted y_j that equals eos, or that fills `remaining`, ends the round
+ * with no further token; if all gamma are accepted a bonus is drawn from
+ * p_gamma / Σ p_gamma.  A draw from weights w with uniform u' is the smallest
+ * index whose running sum exceeds u' Σ w.
+ *   p [R, gamma+1, V] f32 target rows; q [R, gamma, V] f32 draft rows;
+ *   draft [R, gamma] int32.  Uniforms: Philox4x32-10 with key (seed lo, hi)
+ *   and counter (j, r, offset lo, offset hi); word 0 -> accept uniform of
+ *   position j, word 1 -> correction/bonus uniform (j = gamma for the bonus);
+ *   u = (word >> 8) * 2^-24.
+ *   eos [R] nullable (-1 = none); remaining [R] nullable (default gamma+1).
+ *   Outputs [R] int32: accepted = number of drafts accepted, next_token =
+ *   correction or bonus (-1 if the round ended without one), n_emit =
+ *   accepted + (next_token >= 0), status = MTP_VERIFY_*.
+ * Reads only p_j[y_j], q_j[y_j] up to the decision and the one row pair (or
+ * bonus row) it samples from; those rows are checked for NaN/negatives. */
+mtp_status spec_verify(int R, int gamma, int V, const float* p, const float* q,
+                       const int32_t* draft, uint64_t seed, uint64_t offset,
+                       const int32_t* eos, const int32_t* remaining,
+                       int32_t* accepted, int32_t* next_token, int32_t* n_emit,
+                       int32_t* status, cudaStream_t stream);
+
+/* Diagnostic GEMM on the same tcgen05 core the chain uses:
+ * C[M,N] (bf16) = A[M,K] (bf16) · B[N,K]^T (bf16), fp32 accumulation.
+ * K % 8 == 0; A, B, C 16-byte aligned. */
+mtp_status mtp_gemm_bf16(int M, int N, int K, const void* A, const void* B, void* C,
+                         cudaStream_t stream);
+
+/* Synchronises `stream`, ORs the device error words of every kernel file
+ * into *flags (host, nullable) and clears them.  Returns MTP_ERR_DEVICE if
+ * any bit was set, MTP_ERR_CUDA if the synchronisation failed. */
+mtp_status mtp_check_errors(cudaStream_t stream, unsigned int* flags);
+
+/* Static string for a status code. */
+const char* mtp_status_string(int status);
+
+/* MTP_ABI_VERSION of the loaded library. */
+int mtp_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MTP_H */

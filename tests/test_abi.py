@@ -1,0 +1,52 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/mtp.h declares (no compute calls: runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mtp.h"), encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([a-z_][a-z0-9_]*)\s*\(",
+                       src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from deepseek_sequential_mtp_gb300 import build, lib as binding
+    build.build()
+    return binding.load()
+
+
+def test_header_declares_the_hot_path():
+    names = declared_functions()
+    for required in ("mtp_chain_forward", "mtp_chain_loss", "spec_verify",
+                     "mtp_chain_workspace_bytes", "mtp_check_errors", "mtp_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_host_only_calls(lib):
+    assert lib.mtp_abi_version() == 1
+    assert lib.mtp_status_string(0) == b"ok"
+    assert lib.mtp_status_string(7) == b"unsupported shape or dtype"
+
+
+def test_argument_errors_return_without_launching(lib):
+    # null pointers and bad sizes are rejected on the host
+    assert lib.spec_verify(4, 2, 10, None, None, None, 0, 0, None, None,
+                           None, None, None, None, None) == 1
+    assert lib.spec_verify(4, 40, 10, None, None, None, 0, 0, None, None,
+                           None, None, None, None, None) == 7
+    assert lib.spec_verify(0, 2, 10, None, None, None, 0, 0, None, None,
+                           None, None, None, None, None) == 0

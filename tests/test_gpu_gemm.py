@@ -1,0 +1,35 @@
+"""The tcgen05 GEMM core (C ABI diagnostic mtp_gemm_bf16) against a plain
+PyTorch fp32 reference of the same product, shapes spanning several tiles
+with ragged M, N and K tails."""
+import pytest
+import torch
+
+from deepseek_sequential_mtp_gb300 import lib
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 256), (300, 1000, 200),
+                                   (1024, 3072, 1024), (777, 1536, 2816), (8192, 1024, 2048)])
+def test_gemm_matches_fp32_reference(M, N, K):
+    g = torch.Generator(device="cuda").manual_seed(M * 7 + N)
+    A = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
+    B = torch.randn(N, K, device="cuda", generator=g).to(torch.bfloat16)
+    C = lib.gemm_bf16(A, B)
+    lib.check_errors()
+    ref = A.float() @ B.float().T
+    err = (C.float() - ref).abs()
+    # one bf16 rounding of the fp32 result (2^-8 relative) plus accumulation order
+    tol = ref.abs() * 2 ** -8 + 1e-3 * K ** 0.5
+    assert bool((err <= tol).all()), f"max err {err.max().item()}"
+
+
+def test_gemm_repeated_calls_stable():
+    A = torch.randn(512, 512, device="cuda").to(torch.bfloat16)
+    B = torch.randn(768, 512, device="cuda").to(torch.bfloat16)
+    C0 = lib.gemm_bf16(A, B)
+    for _ in range(20):
+        C1 = lib.gemm_bf16(A, B)
+    torch.cuda.synchronize()
+    assert torch.equal(C0, C1)
+    assert lib.check_errors() == 0

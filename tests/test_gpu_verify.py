@@ -1,0 +1,124 @@
+"""spec_verify on the GPU against the CPU oracle, through the C ABI.
+
+Bar: accepted length, emitted token, count and status bit-exact given the
+same Philox uniforms.  Accept decisions use the same fp64 division on both
+sides and are exact; a correction/bonus index is compared unless the oracle's
+running sum lies within 1e-7 (relative to the row's mass) of the draw point:
+the kernel forms each residual in fp32 (one rounding, at most 2^-24 of the
+element) and sums those with error-free compensated steps, so its running
+sums agree with the exact fp64 sums to 2^-24 = 6e-8 of their value."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from deepseek_sequential_mtp_gb300 import lib, synth
+from oracle import verify as ov
+
+pytestmark = pytest.mark.gpu
+
+MARGIN = 1e-7
+
+
+def run_both(case, seed, offset, eos=None, remaining=None):
+    dev = "cuda"
+    g = lib.spec_verify(case["p"].to(dev), case["q"].to(dev), case["draft"].to(dev), seed, offset,
+                        eos=None if eos is None else eos.to(dev),
+                        remaining=None if remaining is None else remaining.to(dev))
+    lib.check_errors()
+    r = ov.spec_verify(case["p"].numpy(), case["q"].numpy(), case["draft"].numpy(), seed, offset,
+                       eos=None if eos is None else eos.numpy(),
+                       remaining=None if remaining is None else remaining.numpy())
+    return {k: v.cpu().numpy() for k, v in g.items()}, r
+
+
+def assert_parity(g, r, max_excluded=0.05):
+    keep = r["margin"] > MARGIN
+    assert keep.mean() >= 1 - max_excluded, f"too many knife-edge draws: {(~keep).sum()}"
+    np.testing.assert_array_equal(g["accepted"][keep], r["accepted"][keep])
+    np.testing.assert_array_equal(g["next_token"][keep], r["token"][keep])
+    np.testing.assert_array_equal(g["n_emit"][keep], r["n_emit"][keep])
+    np.testing.assert_array_equal(g["status"][keep], r["status"][keep])
+
+
+@pytest.mark.parametrize("V", [64, 3000, 3001, 5000])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_small_parity(V, seed):
+    case = synth.make_small_verify_case(seed, R=48, gamma=3, V=V)
+    for offset in (0, 1, 2**33 + 5):
+        g, r = run_both(case, 1000 + seed, offset)
+        assert_parity(g, r)
+
+
+def test_config4_full_size_parity():
+    """64 requests, γ=4, V=129280 (the verify workload), several uniform streams."""
+    case = synth.make_verify_inputs(synth.VERIFY_C4, seed=1)
+    for offset in range(4):
+        g, r = run_both(case, 7, offset)
+        assert_parity(g, r, max_excluded=0.06)
+        assert np.all(r["status"] == 0)
+
+
+def test_eos_budget_and_gamma_zero():
+    case = synth.make_small_verify_case(4, R=40, gamma=4, V=256)
+    rng = np.random.default_rng(0)
+    eos = torch.from_numpy(np.where(rng.random(40) < 0.5, case["draft"][:, 1].numpy(), -1).astype(np.int32))
+    remaining = torch.from_numpy(rng.integers(0, 6, 40).astype(np.int32))
+    g, r = run_both(case, 3, 9, eos=eos, remaining=remaining)
+    assert_parity(g, r)
+    assert (r["status"] == ov.STATUS_INVALID_BUDGET).any()
+    c0 = {"p": case["p"][:, :1].contiguous(), "q": case["q"][:, :0].contiguous(),
+          "draft": case["draft"][:, :0].contiguous()}
+    g, r = run_both(c0, 3, 9)  # γ = 0: a pure draw from p_0
+    assert_parity(g, r)
+    assert np.all(g["n_emit"] == 1)
+
+
+def test_error_statuses():
+    case = synth.make_small_verify_case(5, R=6, gamma=2, V=128, overlap="none")
+    p, q, y = case["p"].clone(), case["q"].clone(), case["draft"].clone()
+    y[0, 0] = 128                      # out of range draft
+    q[1, 0, y[1, 0]] = 0.0             # q[y] = 0
+    p[2, 0, y[2, 0]] = float("nan")    # NaN on the decision scalar
+    p[3] *= 0.0                        # every rejection has no residual; bonus row empty
+    p[4, 0, 5] = -1.0                  # negative entry: reached only if row 0 is scanned
+    g, r = run_both({"p": p, "q": q, "draft": y}, 1, 0)
+    np.testing.assert_array_equal(g["status"], r["status"])
+    np.testing.assert_array_equal(g["n_emit"], r["n_emit"])
+    assert g["status"][0] == ov.STATUS_INVALID_DRAFT and g["status"][1] == ov.STATUS_INVALID_DRAFT
+    assert g["status"][2] == ov.STATUS_INVALID_PROBS
+    assert g["status"][3] in (ov.STATUS_ZERO_RESIDUAL, ov.STATUS_INVALID_DRAFT)
+
+
+@pytest.mark.parametrize("V", [3, 4])
+def test_expected_emitted_monte_carlo(V):
+    """E[N_emit] = (1 - α^{γ+1}) / (1 - α) at α = 0.7, γ = 3 and 4."""
+    alpha = 0.7
+    p_row = np.array([0.7, 0.3, 0.0, 0.0][:V], dtype=np.float32)
+    q_row = np.array([0.7, 0.0, 0.3, 0.0][:V], dtype=np.float32)
+    for gamma in (3, 4):
+        R = 50000
+        rng = np.random.default_rng(gamma)
+        p = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(p_row, (R, gamma + 1, V))))
+        q = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(q_row, (R, gamma, V))))
+        y = torch.from_numpy(rng.choice(V, size=(R, gamma), p=q_row / q_row.sum()).astype(np.int32))
+        out = lib.spec_verify(p.cuda(), q.cuda(), y.cuda(), seed=77, offset=gamma)
+        n = out["n_emit"].cpu().numpy().astype(np.float64)
+        assert np.all(out["status"].cpu().numpy() == 0)
+        want = (1 - alpha ** (gamma + 1)) / (1 - alpha)
+        se = n.std() / math.sqrt(R)
+        assert abs(n.mean() - want) < 4 * se, (n.mean(), want, se)
+
+
+def test_worked_example_correction_is_index_zero():
+    p = torch.tensor([[0.6, 0.3, 0.1], [0.6, 0.3, 0.1]]).expand(4000, 2, 3).contiguous()
+    q = torch.tensor([[0.4, 0.4, 0.2]]).expand(4000, 1, 3).contiguous()
+    y = torch.tensor([1, 2] * 2000, dtype=torch.int32)[:, None].contiguous()
+    out = lib.spec_verify(p.cuda(), q.cuda(), y.cuda(), seed=5, offset=0)
+    acc = out["accepted"].cpu().numpy()
+    tok = out["next_token"].cpu().numpy()
+    assert np.all(tok[acc == 0] == 0)
+    # acceptance rates p[y]/q[y] = 0.75 (y=1) and 0.5 (y=2)
+    yy = y[:, 0].numpy()
+    assert abs(acc[yy == 1].mean() - 0.75) < 0.04 and abs(acc[yy == 2].mean() - 0.5) < 0.04
