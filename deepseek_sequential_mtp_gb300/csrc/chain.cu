@@ -1,12 +1,661 @@
-#include "common.cuh"
+// The teacher-forced sequential MTP chain and its masked cross-entropy loss.
+//
+// "M7.6 - DeepSeek MTP: Sequential Modules, Teacher Forcing, and Speculative
+// Runtime": module equations (§0x03, §0x03C), depth alignment (§0x04), the
+// row compiler's state/label support (§0x04C), the per-depth objective and
+// L = L_main + λ/D Σ_k L^(k) (§0x05); "M7.4 - Multi-Token Prediction
+// Foundations": label ownership on packed batches (§0x01A, §0x03A) and the
+// max / sum-exp / target-logit form of the vocabulary cross-entropy (§0x06F).
+//
+// Dense layout: every depth keeps the [B, T, d] row = base-position identity.
+// Row t of depth k reads h^{k-1}[t] and E[x_{t+k}].  With contiguous segments
+// the row compiler's "t..t+k active and in one segment" is t+k < seg_end(t),
+// and its label condition is t+k+1 < seg_end(t); a segment-causal key range
+// [seg_start(t), t] only ever reaches rows that are themselves valid, so the
+// dense rows carry exactly the compact rows' values.  Rows without state are
+// computed on clamped inputs and never read by valid rows.
+//
+// Per depth (bf16): prologue (gather, dual RMSNorm, concat) -> eh_proj GEMM ->
+// RMSNorm_a -> QKV GEMM + RoPE epilogue -> flash attention -> O GEMM +
+// residual -> RMSNorm_f -> gate/up GEMM + SwiGLU epilogue -> down GEMM +
+// residual = h^k -> RMSNorm_out -> head GEMM with online max/sum-exp
+// epilogue (logits never stored) -> per-row CE and per-term sums.
+// GEMMs run on the tcgen05 core (gemm_tc.cu); the f32 specialisation (small
+// shapes) runs the same steps on SIMT kernels in fp32.
+#include <cmath>
+
+#include "gemm_tc.cuh"
+
 MTP_DEFINE_ERROR_WORD(mtp_take_errors_chain)
-extern "C" size_t mtp_chain_workspace_bytes(const mtp_dims*) { return 0; }
-extern "C" mtp_status mtp_chain_forward(const mtp_dims*, const mtp_weights*, const int32_t*, const int32_t*,
-                                        const int32_t*, const void*, void*, void*, size_t, cudaStream_t) {
-  return MTP_ERR_UNSUPPORTED;
+
+namespace mtp {
+mtp_status attn_launch(int dtype, const void* qkv, void* out, const int32_t* seg_start, int B, int T, int H,
+                       int hd, cudaStream_t stream);
 }
-extern "C" mtp_status mtp_chain_loss(const mtp_dims*, const mtp_weights*, const int32_t*, const int32_t*,
-                                     const int32_t*, const void*, float, int, int, double*, float*, float*,
-                                     void*, void*, size_t, cudaStream_t) {
-  return MTP_ERR_UNSUPPORTED;
+
+namespace {
+
+using mtp::from_f32;
+using mtp::load_f32;
+
+// ---------------------------------------------------------------------------
+// Segments: seg_start / seg_end (exclusive) of every position, token checks.
+// One CTA per packed row; a block-wide max-scan of run starts and a reverse
+// min-scan of run ends.  Pads get seg_start = seg_end = t.
+// ---------------------------------------------------------------------------
+constexpr int kScanThreads = 1024;
+
+__device__ int block_scan_max(int v, int* sh) {  // inclusive max-scan over threadIdx order
+  sh[threadIdx.x] = v;
+  __syncthreads();
+  for (int o = 1; o < blockDim.x; o <<= 1) {
+    const int n = threadIdx.x >= o ? sh[threadIdx.x - o] : INT_MIN;
+    __syncthreads();
+    v = max(v, n);
+    sh[threadIdx.x] = v;
+    __syncthreads();
+  }
+  return v;
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+segments_kernel(const int32_t* __restrict__ seg, const int32_t* __restrict__ tokens, int T, int V,
+                int32_t* __restrict__ seg_start, int32_t* __restrict__ seg_end) {
+  __shared__ int sh[kScanThreads];
+  const int b = blockIdx.x;
+  const int32_t* s = seg + static_cast<size_t>(b) * T;
+  const int32_t* x = tokens + static_cast<size_t>(b) * T;
+  int32_t* out_start = seg_start + static_cast<size_t>(b) * T;
+  int32_t* out_end = seg_end + static_cast<size_t>(b) * T;
+  const int per = (T + kScanThreads - 1) / kScanThreads;
+  auto run_begins = [&](int t) { return t == 0 || s[t] != s[t - 1]; };
+  auto run_ends = [&](int t) { return t == T - 1 || s[t] != s[t + 1]; };
+
+  // forward pass over chunk [t0, t1): carry = last run start / largest id to the left
+  const int t0 = min(T, threadIdx.x * per), t1 = min(T, t0 + per);
+  int last_start = INT_MIN, max_id = INT_MIN;
+  for (int t = t0; t < t1; ++t) {
+    if (run_begins(t)) last_start = t;
+    if (s[t] != -1) max_id = max(max_id, s[t]);
+  }
+  block_scan_max(last_start, sh);
+  int cur_start = threadIdx.x ? sh[threadIdx.x - 1] : INT_MIN;
+  __syncthreads();
+  block_scan_max(max_id, sh);
+  int prev_max = threadIdx.x ? sh[threadIdx.x - 1] : INT_MIN;
+  __syncthreads();
+  bool bad_seg = false, bad_tok = false;
+  for (int t = t0; t < t1; ++t) {
+    const bool nr = run_begins(t);
+    if (nr) cur_start = t;
+    if (s[t] != -1) {
+      if (nr && prev_max != INT_MIN && s[t] <= prev_max) bad_seg = true;  // an id re-appears
+      prev_max = max(prev_max, s[t]);
+    }
+    out_start[t] = s[t] == -1 ? t : cur_start;
+    if (x[t] < 0 || x[t] >= V) bad_tok = true;
+  }
+
+  // backward pass: thread i owns chunk (kScanThreads-1-i), so thread order runs
+  // right to left; carry = nearest run end to the right, scanned as max of -(end)
+  const int rc = kScanThreads - 1 - threadIdx.x;
+  const int r0 = min(T, rc * per), r1 = min(T, r0 + per);
+  int first_end = INT_MIN;
+  for (int t = r0; t < r1; ++t)
+    if (run_ends(t)) { first_end = -(t + 1); break; }
+  block_scan_max(first_end, sh);
+  int cur_end = threadIdx.x ? sh[threadIdx.x - 1] : INT_MIN;
+  __syncthreads();
+  for (int t = r1 - 1; t >= r0; --t) {
+    if (run_ends(t)) cur_end = -(t + 1);
+    out_end[t] = s[t] == -1 ? t : -cur_end;
+  }
+  if (bad_seg) atomicOr(&g_mtp_error_word, MTP_DEVERR_SEGMENTS);
+  if (bad_tok) atomicOr(&g_mtp_error_word, MTP_DEVERR_TOKEN_RANGE);
+}
+
+__device__ __forceinline__ int clamp_token(int v, int V) { return min(max(v, 0), V - 1); }
+
+// ---------------------------------------------------------------------------
+// Prologue: c = [RMSNorm_h(h^{k-1}); RMSNorm_e(E[x_{t+k}])] (one warp per row)
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void prologue_kernel(const T* __restrict__ h_prev, const int32_t* __restrict__ tokens,
+                                const T* __restrict__ embed, const T* __restrict__ g_h, const T* __restrict__ g_e,
+                                T* __restrict__ c, int M, int Tlen, int d, int V, int k, float eps) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= M) return;
+  const int m = warp;
+  const int t = m % Tlen;
+  const int src_t = min(t + k, Tlen - 1);
+  const int tok = clamp_token(tokens[m - t + src_t], V);
+  const T* h = h_prev + static_cast<size_t>(m) * d;
+  const T* e = embed + static_cast<size_t>(tok) * d;
+  float sh = 0.f, se = 0.f;
+  for (int i = lane; i < d; i += 32) {
+    const float a = load_f32(h + i), b = load_f32(e + i);
+    sh += a * a;
+    se += b * b;
+  }
+  sh = mtp::warp_sum(sh);
+  se = mtp::warp_sum(se);
+  const float rh = 1.0f / sqrtf(sh / d + eps);
+  const float re = 1.0f / sqrtf(se / d + eps);
+  T* out = c + static_cast<size_t>(m) * 2 * d;
+  for (int i = lane; i < d; i += 32) {
+    out[i] = from_f32<T>(load_f32(g_h + i) * (load_f32(h + i) * rh));
+    out[d + i] = from_f32<T>(load_f32(g_e + i) * (load_f32(e + i) * re));
+  }
+}
+
+// y = RMSNorm_g(x) row-wise (one warp per row)
+template <typename T>
+__global__ void rmsnorm_kernel(const T* __restrict__ x, const T* __restrict__ g, T* __restrict__ y, int M, int d,
+                               float eps) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= M) return;
+  const T* xr = x + static_cast<size_t>(warp) * d;
+  float ss = 0.f;
+  for (int i = lane; i < d; i += 32) {
+    const float a = load_f32(xr + i);
+    ss += a * a;
+  }
+  ss = mtp::warp_sum(ss);
+  const float r = 1.0f / sqrtf(ss / d + eps);
+  T* yr = y + static_cast<size_t>(warp) * d;
+  for (int i = lane; i < d; i += 32) yr[i] = from_f32<T>(load_f32(g + i) * (load_f32(xr + i) * r));
+}
+
+// (cos, sin) of position p times base^(-2j/hd), computed in double and rounded once
+__global__ void rope_table_kernel(float2* __restrict__ tab, int T, int half, int hd, double base) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= T * half) return;
+  const int p = i / half, j = i % half;
+  const double ang = static_cast<double>(p) * pow(base, -2.0 * j / hd);
+  tab[i] = make_float2(static_cast<float>(cos(ang)), static_cast<float>(sin(ang)));
+}
+
+// labels of term k (0 = main): x_{t+k+1} where t..t+k+1 lie in t's segment, else -1
+__global__ void labels_kernel(const int32_t* __restrict__ tokens, const int32_t* __restrict__ seg,
+                              const int32_t* __restrict__ seg_end, int32_t* __restrict__ labels, int M, int Tlen,
+                              int k, int V) {
+  const int m = blockIdx.x * blockDim.x + threadIdx.x;
+  if (m >= M) return;
+  const int t = m % Tlen;
+  const bool ok = seg[m] != -1 && t + k + 1 < seg_end[m];
+  labels[m] = ok ? clamp_token(tokens[m + k + 1], V) : -1;
+}
+
+// ---------------------------------------------------------------------------
+// f32 SIMT kernels (small shapes)
+// ---------------------------------------------------------------------------
+// C[M,N] = A[M,K] B[N,K]^T (+ R), 64x64 tiles, 16x16 threads, 4x4 per thread
+__global__ void gemm_f32_kernel(const float* __restrict__ A, int lda, const float* __restrict__ B, int ldb,
+                                float* __restrict__ C, int ldc, const float* __restrict__ R, int ldr, int M, int N,
+                                int K) {
+  __shared__ float As[16][65], Bs[16][65];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    for (int i = threadIdx.x; i < 64 * 16; i += 256) {
+      const int r = i / 16, kk = i % 16;
+      As[kk][r] = (m0 + r < M && k0 + kk < K) ? A[static_cast<size_t>(m0 + r) * lda + k0 + kk] : 0.f;
+      Bs[kk][r] = (n0 + r < N && k0 + kk < K) ? B[static_cast<size_t>(n0 + r) * ldb + k0 + kk] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] += As[kk][ty * 4 + i] * Bs[kk][tx * 4 + j];
+    __syncthreads();
+  }
+  for (int i = 0; i < 4; ++i)
+    for (int j = 0; j < 4; ++j) {
+      const int m = m0 + ty * 4 + i, n = n0 + tx * 4 + j;
+      if (m < M && n < N)
+        C[static_cast<size_t>(m) * ldc + n] = acc[i][j] + (R ? R[static_cast<size_t>(m) * ldr + n] : 0.f);
+    }
+}
+
+__global__ void rope_f32_kernel(float* __restrict__ qkv, const int32_t* __restrict__ pos,
+                                const float2* __restrict__ tab, int M, int d, int hd, int Tlen) {
+  const int half = hd / 2;
+  const int per_row = 2 * d / 2;  // pairs over q and k
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= M * per_row) return;
+  const int m = i / per_row, pr = i % per_row;
+  const int head = pr / half, j = pr % half;  // head index over q then k (2*H heads)
+  int p = pos[m];
+  if (p < 0 || p >= Tlen) {
+    atomicOr(&g_mtp_error_word, MTP_DEVERR_TOKEN_RANGE);
+    p = min(max(p, 0), Tlen - 1);
+  }
+  const float2 cs = tab[static_cast<size_t>(p) * half + j];
+  float* base = qkv + static_cast<size_t>(m) * 3 * d + head * hd;
+  const float a = base[j], b = base[j + half];
+  base[j] = a * cs.x - b * cs.y;
+  base[j + half] = b * cs.x + a * cs.y;
+}
+
+__global__ void swiglu_f32_kernel(const float* __restrict__ G, const float* __restrict__ U, float* __restrict__ out,
+                                  size_t n) {
+  const size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+  if (i >= n) return;
+  const float g = G[i];
+  out[i] = g / (1.0f + expf(-g)) * U[i];
+}
+
+// head logits of one row against a 256-wide vocabulary tile, reduced to the
+// tile's (max, sum-exp) and the label logit; same partial format as the
+// tcgen05 CE epilogue
+__global__ void head_ce_f32_kernel(const float* __restrict__ x, const float* __restrict__ W, int d, int V,
+                                   const int32_t* __restrict__ labels, float2* __restrict__ part, float* __restrict__ zt,
+                                   int nvt) {
+  __shared__ float red[256];
+  const int m = blockIdx.y, tile = blockIdx.x;
+  const int v = tile * 256 + threadIdx.x;
+  float z = -INFINITY;
+  if (v < V) {
+    float acc = 0.f;
+    const float* xr = x + static_cast<size_t>(m) * d;
+    const float* wr = W + static_cast<size_t>(v) * d;
+    for (int i = 0; i < d; ++i) acc += xr[i] * wr[i];
+    z = acc;
+    if (labels[m] == v) zt[m] = z;
+  }
+  red[threadIdx.x] = z;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if (threadIdx.x < o) red[threadIdx.x] = fmaxf(red[threadIdx.x], red[threadIdx.x + o]);
+    __syncthreads();
+  }
+  const float mx = red[0];
+  __syncthreads();
+  red[threadIdx.x] = v < V ? expf(z - mx) : 0.f;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) part[static_cast<size_t>(m) * nvt + tile] = make_float2(mx, red[0]);
+}
+
+// ---------------------------------------------------------------------------
+// CE reduction and loss assembly
+// ---------------------------------------------------------------------------
+// ℓ_t = max + log Σ_tiles s_j exp(m_j - max) - z_label for supervised rows
+__global__ void ce_reduce_kernel(int M, int nvt, const float2* __restrict__ part, const float* __restrict__ zt,
+                                 const int32_t* __restrict__ labels, float* __restrict__ row_loss,
+                                 double* __restrict__ sum_count) {
+  __shared__ double s_sum[8];
+  __shared__ int s_cnt[8];
+  const int m = blockIdx.x * blockDim.x + threadIdx.x;
+  double loss = 0.0;
+  int cnt = 0;
+  if (m < M) {
+    float out = NAN;
+    if (labels[m] >= 0) {
+      const float2* p = part + static_cast<size_t>(m) * nvt;
+      float mx = -INFINITY;
+      for (int j = 0; j < nvt; ++j) mx = fmaxf(mx, p[j].x);
+      float s = 0.f;
+      for (int j = 0; j < nvt; ++j) s += p[j].y * expf(p[j].x - mx);
+      out = (mx + logf(s)) - zt[m];
+      loss = out;
+      cnt = 1;
+    }
+    if (row_loss) row_loss[m] = out;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  loss = mtp::warp_sum(loss);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if (lane == 0) {
+    s_sum[warp] = loss;
+    s_cnt[warp] = cnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double a = 0.0;
+    int c = 0;
+    for (int w = 0; w < blockDim.x / 32; ++w) {
+      a += s_sum[w];
+      c += s_cnt[w];
+    }
+    if (c) {
+      atomicAdd(sum_count, a);
+      atomicAdd(sum_count + 1, static_cast<double>(c));
+    }
+  }
+}
+
+__global__ void zero_f64_kernel(double* p, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) p[i] = 0.0;
+}
+
+// losses = [L, L_main, L^(1..D)] from (sum, count) pairs
+__global__ void loss_assemble_kernel(const double* __restrict__ sc, float* __restrict__ losses, int D, double n_pos,
+                                     float lambda, int den, int with_main) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  auto term = [&](int i) -> double {
+    if (den == MTP_DEN_FIXED) return sc[2 * i] / n_pos;
+    return sc[2 * i + 1] > 0 ? sc[2 * i] / sc[2 * i + 1] : 0.0;
+  };
+  const double main = with_main ? term(0) : 0.0;
+  double mtp = 0.0;
+  for (int k = 1; k <= D; ++k) {
+    const double lk = term(k);
+    losses[1 + k] = static_cast<float>(lk);
+    mtp += lk;
+  }
+  losses[1] = static_cast<float>(main);
+  losses[0] = static_cast<float>(main + static_cast<double>(lambda) / D * mtp);
+}
+
+// ---------------------------------------------------------------------------
+// Host orchestration
+// ---------------------------------------------------------------------------
+inline size_t align_up(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+struct Layout {
+  size_t seg_start, seg_end, labels, c, u, x, qkv, o, a, g, g2, h0buf, h1buf, rope, ce_part, zt, total;
+  int nvt;
+};
+
+bool valid_dims(const mtp_dims& D) {
+  if (D.B <= 0 || D.T <= 0 || D.d <= 0 || D.n_heads <= 0 || D.head_dim <= 0 || D.ffn <= 0 || D.V <= 0 || D.D <= 0)
+    return false;
+  if (D.n_heads * D.head_dim != D.d || D.head_dim % 2) return false;
+  if (D.dtype != MTP_F32 && D.dtype != MTP_BF16) return false;
+  if (!(D.eps >= 0.f) || !(D.rope_base >= 0.f)) return false;
+  return true;
+}
+
+mtp_status supported(const mtp_dims& D) {
+  if (D.dtype == MTP_BF16) {
+    if (D.d % 128 || (D.head_dim != 64 && D.head_dim != 128) || D.ffn % 8) return MTP_ERR_UNSUPPORTED;
+  } else {
+    if (D.head_dim > 128 || static_cast<size_t>(D.T) * 16 > 200 * 1024) return MTP_ERR_UNSUPPORTED;
+  }
+  if (static_cast<long long>(D.B) * D.T > (1ll << 30)) return MTP_ERR_UNSUPPORTED;
+  return MTP_OK;
+}
+
+Layout make_layout(const mtp_dims& D) {
+  Layout L{};
+  const size_t M = static_cast<size_t>(D.B) * D.T;
+  const size_t es = D.dtype == MTP_BF16 ? 2 : 4;
+  L.nvt = (D.V + mtp::gemm_ce_tile_n() - 1) / mtp::gemm_ce_tile_n();
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes);
+    return o;
+  };
+  L.seg_start = take(M * 4);
+  L.seg_end = take(M * 4);
+  L.labels = take(M * 4);
+  L.c = take(M * 2 * D.d * es);
+  L.u = take(M * D.d * es);
+  L.x = take(M * D.d * es);
+  L.qkv = take(M * 3 * D.d * es);
+  L.o = take(M * D.d * es);
+  L.a = take(M * D.d * es);
+  L.g = take(M * D.ffn * es);
+  L.g2 = D.dtype == MTP_F32 ? take(M * D.ffn * es) : off;
+  L.h0buf = take(M * D.d * es);
+  L.h1buf = take(M * D.d * es);
+  L.rope = take(static_cast<size_t>(D.T) * (D.head_dim / 2) * sizeof(float2));
+  L.ce_part = take(M * L.nvt * sizeof(float2));
+  L.zt = take(M * 4);
+  L.total = off;
+  return L;
+}
+
+struct Ctx {
+  const mtp_dims& D;
+  const mtp_weights& W;
+  const int32_t* tokens;
+  const int32_t* seg;
+  const int32_t* pos;
+  uint8_t* ws;
+  Layout L;
+  cudaStream_t st;
+  int M;
+  template <typename T>
+  T* buf(size_t off) const {
+    return reinterpret_cast<T*>(ws + off);
+  }
+};
+
+inline int warp_blocks(int rows) { return (rows + 7) / 8; }  // 8 warps (256 threads) per block
+
+template <typename T>
+mtp_status gemm(const Ctx& C, const T* A, int lda, const T* const* Bs, int nseg, int seg_rows, int K, int N,
+                T* out, int ldo, int epi, const T* resid = nullptr, int ldr = 0, const T* B2 = nullptr);
+
+// bf16: the tcgen05 core
+template <>
+mtp_status gemm<__nv_bfloat16>(const Ctx& C, const __nv_bfloat16* A, int lda, const __nv_bfloat16* const* Bs,
+                               int nseg, int seg_rows, int K, int N, __nv_bfloat16* out, int ldo, int epi,
+                               const __nv_bfloat16* resid, int ldr, const __nv_bfloat16* B2) {
+  mtp::GemmDesc g;
+  g.M = C.M;
+  g.N = N;
+  g.K = K;
+  g.A = A;
+  g.lda = lda;
+  for (int i = 0; i < nseg; ++i) g.B[i] = Bs[i];
+  if (epi == mtp::EPI_SWIGLU) g.B[1] = B2;
+  g.ldb = K;
+  g.nseg = nseg;
+  g.seg_rows = seg_rows;
+  g.epi = epi;
+  g.out = out;
+  g.ldo = ldo;
+  g.resid = resid;
+  g.ldr = ldr;
+  if (epi == mtp::EPI_ROPE) {
+    g.pos = C.pos;
+    g.rope = C.buf<float2>(C.L.rope);
+    g.rope_len = C.D.T;
+    g.rope_cols = 2 * C.D.d;
+    g.head_dim = C.D.head_dim;
+  }
+  return mtp::gemm_bf16_launch(g, C.st);
+}
+
+// f32: SIMT tiles; RoPE and SwiGLU as separate elementwise kernels
+template <>
+mtp_status gemm<float>(const Ctx& C, const float* A, int lda, const float* const* Bs, int nseg, int seg_rows, int K,
+                       int N, float* out, int ldo, int epi, const float* resid, int ldr, const float* B2) {
+  auto run = [&](const float* B, float* o, int n, int ldo_, const float* R, int ldr_) {
+    const dim3 grid((n + 63) / 64, (C.M + 63) / 64);
+    gemm_f32_kernel<<<grid, 256, 0, C.st>>>(A, lda, B, K, o, ldo_, R, ldr_, C.M, n, K);
+  };
+  if (epi == mtp::EPI_SWIGLU) {
+    float* U = C.buf<float>(C.L.g2);
+    run(Bs[0], out, N, ldo, nullptr, 0);
+    run(B2, U, N, N, nullptr, 0);
+    const size_t n = static_cast<size_t>(C.M) * N;
+    swiglu_f32_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, C.st>>>(out, U, out, n);
+  } else {
+    for (int s = 0; s < nseg; ++s) run(Bs[s], out + static_cast<size_t>(s) * seg_rows, seg_rows, ldo, resid, ldr);
+    if (epi == mtp::EPI_ROPE && C.D.rope_base > 0.f) {
+      const int n = C.M * C.D.d;
+      rope_f32_kernel<<<(n + 255) / 256, 256, 0, C.st>>>(out, C.pos, C.buf<float2>(C.L.rope), C.M, C.D.d,
+                                                          C.D.head_dim, C.D.T);
+    }
+  }
+  MTP_LAUNCH_CHECK();
+  return MTP_OK;
+}
+
+#define TRY(expr)                          \
+  do {                                     \
+    mtp_status s_ = (expr);                \
+    if (s_ != MTP_OK) return s_;           \
+  } while (0)
+
+// head + CE for term `k` (0 = main) on hidden state h
+template <typename T>
+mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double* sum_count) {
+  const mtp_dims& D = C.D;
+  T* x = C.buf<T>(C.L.x);
+  int32_t* labels = C.buf<int32_t>(C.L.labels);
+  float2* part = C.buf<float2>(C.L.ce_part);
+  float* zt = C.buf<float>(C.L.zt);
+  rmsnorm_kernel<T><<<warp_blocks(C.M), 256, 0, C.st>>>(h, static_cast<const T*>(C.W.out_norm), x, C.M, D.d, D.eps);
+  labels_kernel<<<(C.M + 255) / 256, 256, 0, C.st>>>(C.tokens, C.seg, C.buf<int32_t>(C.L.seg_end), labels, C.M, D.T,
+                                                     k, D.V);
+  MTP_LAUNCH_CHECK();
+  if constexpr (sizeof(T) == 2) {
+    mtp::GemmDesc g;
+    g.M = C.M;
+    g.N = D.V;
+    g.K = D.d;
+    g.A = x;
+    g.lda = D.d;
+    g.B[0] = static_cast<const __nv_bfloat16*>(C.W.head);
+    g.ldb = D.d;
+    g.nseg = 1;
+    g.seg_rows = D.V;
+    g.epi = mtp::EPI_CE;
+    g.labels = labels;
+    g.ce_part = part;
+    g.z_tgt = zt;
+    TRY(mtp::gemm_bf16_launch(g, C.st));
+  } else {
+    head_ce_f32_kernel<<<dim3(C.L.nvt, C.M), 256, 0, C.st>>>(x, static_cast<const float*>(C.W.head), D.d, D.V, labels,
+                                                             part, zt, C.L.nvt);
+  }
+  ce_reduce_kernel<<<(C.M + 255) / 256, 256, 0, C.st>>>(C.M, C.L.nvt, part, zt, labels, row_loss_term, sum_count);
+  MTP_LAUNCH_CHECK();
+  return MTP_OK;
+}
+
+template <typename T>
+mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float lambda, int den, int with_main,
+                     double* sums_counts, float* losses, float* row_loss) {
+  const mtp_dims& D = C.D;
+  const int M = C.M, d = D.d;
+  const size_t Md = static_cast<size_t>(M) * d;
+  segments_kernel<<<D.B, kScanThreads, 0, C.st>>>(C.seg, C.tokens, D.T, D.V, C.buf<int32_t>(C.L.seg_start),
+                                                  C.buf<int32_t>(C.L.seg_end));
+  const int half = D.head_dim / 2;
+  if (D.rope_base > 0.f) {
+    rope_table_kernel<<<(D.T * half + 255) / 256, 256, 0, C.st>>>(C.buf<float2>(C.L.rope), D.T, half, D.head_dim,
+                                                                  static_cast<double>(D.rope_base));
+  } else {
+    cudaMemsetAsync(C.buf<float2>(C.L.rope), 0, static_cast<size_t>(D.T) * half * sizeof(float2), C.st);
+  }
+  MTP_LAUNCH_CHECK();
+  if (with_loss) {
+    zero_f64_kernel<<<1, 64, 0, C.st>>>(sums_counts, 2 * (D.D + 1));
+    if (with_main) TRY(head_ce<T>(C, h0, 0, row_loss, sums_counts));
+    else if (row_loss)
+      cudaMemsetAsync(row_loss, 0xff, static_cast<size_t>(M) * sizeof(float), C.st);  // NaN
+  }
+  T* c = C.buf<T>(C.L.c);
+  T* u = C.buf<T>(C.L.u);
+  T* x = C.buf<T>(C.L.x);
+  T* qkv = C.buf<T>(C.L.qkv);
+  T* o = C.buf<T>(C.L.o);
+  T* a = C.buf<T>(C.L.a);
+  T* g = C.buf<T>(C.L.g);
+  const T* h_prev = h0;
+  for (int k = 1; k <= D.D; ++k) {
+    const int i = k - 1;
+    T* h_k = h_out ? h_out + static_cast<size_t>(i) * Md : C.buf<T>((k & 1) ? C.L.h1buf : C.L.h0buf);
+    auto wt = [&](const void* const* arr) { return static_cast<const T*>(arr[i]); };
+    prologue_kernel<T><<<warp_blocks(M), 256, 0, C.st>>>(h_prev, C.tokens, static_cast<const T*>(C.W.embed),
+                                                         wt(C.W.hnorm), wt(C.W.enorm), c, M, D.T, d, D.V, k, D.eps);
+    MTP_LAUNCH_CHECK();
+    const T* proj[1] = {wt(C.W.eh_proj)};
+    TRY(gemm<T>(C, c, 2 * d, proj, 1, d, 2 * d, d, u, d, mtp::EPI_STORE));
+    rmsnorm_kernel<T><<<warp_blocks(M), 256, 0, C.st>>>(u, wt(C.W.attn_norm), x, M, d, D.eps);
+    const T* wqkv[3] = {wt(C.W.wq), wt(C.W.wk), wt(C.W.wv)};
+    TRY(gemm<T>(C, x, d, wqkv, 3, d, d, 3 * d, qkv, 3 * d, D.rope_base > 0.f ? mtp::EPI_ROPE : mtp::EPI_STORE));
+    TRY(mtp::attn_launch(D.dtype, qkv, o, C.buf<int32_t>(C.L.seg_start), D.B, D.T, D.n_heads, D.head_dim, C.st));
+    const T* wo[1] = {wt(C.W.wo)};
+    TRY(gemm<T>(C, o, d, wo, 1, d, d, d, a, d, mtp::EPI_RESID, u, d));
+    rmsnorm_kernel<T><<<warp_blocks(M), 256, 0, C.st>>>(a, wt(C.W.ffn_norm), x, M, d, D.eps);
+    const T* wg[1] = {wt(C.W.w_gate)};
+    TRY(gemm<T>(C, x, d, wg, 1, D.ffn, d, D.ffn, g, D.ffn, mtp::EPI_SWIGLU, nullptr, 0, wt(C.W.w_up)));
+    const T* wd[1] = {wt(C.W.w_down)};
+    TRY(gemm<T>(C, g, D.ffn, wd, 1, d, D.ffn, d, h_k, d, mtp::EPI_RESID, a, d));
+    if (with_loss)
+      TRY(head_ce<T>(C, h_k, k, row_loss ? row_loss + static_cast<size_t>(k) * M : nullptr, sums_counts + 2 * k));
+    h_prev = h_k;
+  }
+  if (with_loss) {
+    loss_assemble_kernel<<<1, 32, 0, C.st>>>(sums_counts, losses, D.D, static_cast<double>(M), lambda, den,
+                                             with_main);
+    MTP_LAUNCH_CHECK();
+  }
+  return MTP_OK;
+}
+
+mtp_status check_common(const mtp_dims* dims, const mtp_weights* w, const int32_t* tokens, const int32_t* seg,
+                        const int32_t* pos, const void* h0, void* ws, size_t ws_bytes) {
+  if (!dims || !w || !tokens || !seg || !pos || !h0) return MTP_ERR_INVALID_ARG;
+  if (!valid_dims(*dims)) return MTP_ERR_SHAPE;
+  TRY(supported(*dims));
+  if (!w->embed || !w->head || !w->out_norm) return MTP_ERR_INVALID_ARG;
+  const void* const* lists[] = {w->hnorm, w->enorm, w->eh_proj, w->attn_norm, w->wq, w->wk, w->wv,
+                                w->wo, w->ffn_norm, w->w_gate, w->w_up, w->w_down};
+  for (auto l : lists) {
+    if (!l) return MTP_ERR_INVALID_ARG;
+    for (int k = 0; k < dims->D; ++k) {
+      if (!l[k]) return MTP_ERR_INVALID_ARG;
+      if (!mtp::aligned16(l[k])) return MTP_ERR_ALIGNMENT;
+    }
+  }
+  for (const void* p : {static_cast<const void*>(tokens), static_cast<const void*>(seg),
+                        static_cast<const void*>(pos), h0, w->embed, w->head, w->out_norm})
+    if (!mtp::aligned16(p)) return MTP_ERR_ALIGNMENT;
+  if (!ws || !mtp::aligned16(ws)) return ws ? MTP_ERR_ALIGNMENT : MTP_ERR_WORKSPACE;
+  if (ws_bytes < make_layout(*dims).total) return MTP_ERR_WORKSPACE;
+  return MTP_OK;
+}
+
+}  // namespace
+
+extern "C" size_t mtp_chain_workspace_bytes(const mtp_dims* dims) {
+  if (!dims || !valid_dims(*dims) || supported(*dims) != MTP_OK) return 0;
+  return make_layout(*dims).total;
+}
+
+extern "C" mtp_status mtp_chain_forward(const mtp_dims* dims, const mtp_weights* w, const int32_t* tokens,
+                                        const int32_t* seg, const int32_t* pos, const void* h0, void* h_out, void* ws,
+                                        size_t ws_bytes, cudaStream_t stream) {
+  TRY(check_common(dims, w, tokens, seg, pos, h0, ws, ws_bytes));
+  if (!h_out) return MTP_ERR_INVALID_ARG;
+  if (!mtp::aligned16(h_out)) return MTP_ERR_ALIGNMENT;
+  Ctx C{*dims, *w, tokens, seg, pos, static_cast<uint8_t*>(ws), make_layout(*dims), stream, dims->B * dims->T};
+  if (dims->dtype == MTP_BF16)
+    return run_chain<__nv_bfloat16>(C, static_cast<const __nv_bfloat16*>(h0), static_cast<__nv_bfloat16*>(h_out),
+                                    false, 0.f, 0, 0, nullptr, nullptr, nullptr);
+  return run_chain<float>(C, static_cast<const float*>(h0), static_cast<float*>(h_out), false, 0.f, 0, 0, nullptr,
+                          nullptr, nullptr);
+}
+
+extern "C" mtp_status mtp_chain_loss(const mtp_dims* dims, const mtp_weights* w, const int32_t* tokens,
+                                     const int32_t* seg, const int32_t* pos, const void* h0, float lambda, int den,
+                                     int with_main, double* sums_counts, float* losses, float* row_loss, void* h_out,
+                                     void* ws, size_t ws_bytes, cudaStream_t stream) {
+  TRY(check_common(dims, w, tokens, seg, pos, h0, ws, ws_bytes));
+  if (!sums_counts || !losses) return MTP_ERR_INVALID_ARG;
+  if (den != MTP_DEN_FIXED && den != MTP_DEN_MASKED_MEAN) return MTP_ERR_INVALID_ARG;
+  if (h_out && !mtp::aligned16(h_out)) return MTP_ERR_ALIGNMENT;
+  Ctx C{*dims, *w, tokens, seg, pos, static_cast<uint8_t*>(ws), make_layout(*dims), stream, dims->B * dims->T};
+  if (dims->dtype == MTP_BF16)
+    return run_chain<__nv_bfloat16>(C, static_cast<const __nv_bfloat16*>(h0), static_cast<__nv_bfloat16*>(h_out),
+                                    true, lambda, den, with_main, sums_counts, losses, row_loss);
+  return run_chain<float>(C, static_cast<const float*>(h0), static_cast<float*>(h_out), true, lambda, den, with_main,
+                          sums_counts, losses, row_loss);
 }

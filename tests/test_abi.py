@@ -50,3 +50,43 @@ def test_argument_errors_return_without_launching(lib):
                            None, None, None, None, None) == 7
     assert lib.spec_verify(0, 2, 10, None, None, None, 0, 0, None, None,
                            None, None, None, None, None) == 0
+
+
+def _dims(binding, **kw):
+    from deepseek_sequential_mtp_gb300 import synth
+    cfg = synth.SMALL_BF16.with_(**kw)
+    return binding.make_dims(cfg)
+
+
+def test_chain_host_validation(lib):
+    import ctypes
+    from deepseek_sequential_mtp_gb300 import lib as binding
+    good = _dims(binding)
+    assert lib.mtp_chain_workspace_bytes(ctypes.byref(good)) > 0
+    for bad in (dict(B=0), dict(n_heads=3), dict(D=0), dict(V=0)):
+        d = _dims(binding, **bad)
+        assert lib.mtp_chain_workspace_bytes(ctypes.byref(d)) == 0
+    unsup = _dims(binding, d=192, n_heads=3, head_dim=64)  # bf16 needs d % 128 == 0
+    assert lib.mtp_chain_workspace_bytes(ctypes.byref(unsup)) == 0
+    # host-side errors return before any device work (fake, aligned pointers)
+    fake = ctypes.c_void_p(1 << 20)
+    arr = (ctypes.c_void_p * good.D)(*([1 << 20] * good.D))
+    w = binding.Weights()
+    w.embed = w.head = w.out_norm = 1 << 20
+    for k in binding._WEIGHT_LISTS:
+        setattr(w, k, ctypes.cast(arr, binding._PP))
+    sc = fake
+    st = lib.mtp_chain_loss(ctypes.byref(good), ctypes.byref(w), fake, fake, fake, fake, 0.3, 0, 1,
+                            sc, sc, None, None, fake, 16, None)
+    assert st == 4  # workspace too small
+    st = lib.mtp_chain_loss(ctypes.byref(good), ctypes.byref(w), fake, fake, fake, fake, 0.3, 7, 1,
+                            sc, sc, None, None, fake, 1 << 40, None)
+    assert st == 1  # bad denominator policy
+    bad = _dims(binding, B=0)
+    st = lib.mtp_chain_forward(ctypes.byref(bad), ctypes.byref(w), fake, fake, fake, fake, fake,
+                               fake, 1 << 40, None)
+    assert st == 2
+    mis = ctypes.c_void_p((1 << 20) + 4)
+    st = lib.mtp_chain_forward(ctypes.byref(good), ctypes.byref(w), mis, fake, fake, fake, fake,
+                               fake, 1 << 40, None)
+    assert st == 3

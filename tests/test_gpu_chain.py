@@ -1,0 +1,199 @@
+"""MTP chain on the GPU (mtp_chain_loss through the C ABI) against the CPU
+oracle.
+
+Bars: supervised-row counts exact; f32 configs: losses within 1e-5 relative,
+hidden states within 1e-4; bf16 configs: per-term losses within 1e-3
+relative, hidden states within 2e-2 absolute plus 2e-2 relative (one bf16 ulp
+at |h| in [4, 8) is 0.031, so a pure absolute 2e-2 bar would fail on a single
+legitimate rounding flip of a large entry).  At the full workload sizes the
+oracle runs on whole-segment prefixes ("windows") of chosen packed rows: by
+causality and the segment rule every row that has state inside the window
+depends on window inputs only, so its values are exact comparison points."""
+import numpy as np
+import pytest
+import torch
+
+from deepseek_sequential_mtp_gb300 import lib, synth
+from oracle import chain as oc
+from oracle.rows import compile_all_depths, label_owned
+
+pytestmark = pytest.mark.gpu
+
+
+def to_dev(inp):
+    out = {k: v.cuda() for k, v in inp.items() if k != "weights"}
+    out["weights"] = {k: ([t.cuda() for t in v] if isinstance(v, list) else v.cuda())
+                      for k, v in inp["weights"].items()}
+    return out
+
+
+def run_gpu(cfg, dev_inp, den="fixed", with_main=True, lam=None):
+    chain = lib.Chain(cfg, dev_inp["weights"])
+    dt = synth.torch_dtype(cfg.dtype)
+    h_out = torch.full((cfg.D, cfg.B, cfg.T, cfg.d), float("nan"), dtype=dt, device="cuda")
+    out = chain.loss(dev_inp["tokens"], dev_inp["seg"], dev_inp["pos"], dev_inp["h0"], lam=lam, den=den,
+                     with_main=with_main, row_loss=True, h_out=h_out)
+    lib.check_errors()
+    return {k: v.float().cpu().numpy() if v.dtype != torch.float64 else v.cpu().numpy() for k, v in out.items()}
+
+
+def run_oracle(cfg, inp, W=None, window=None, **kw):
+    W = W if W is not None else oc.weights_to_numpy(inp["weights"])
+    tok, seg, pos = (inp[k].numpy() for k in ("tokens", "seg", "pos"))
+    h0 = inp["h0"].float().numpy()
+    if window is not None:
+        b, s0, s1 = window
+        tok, seg, pos, h0 = tok[b:b + 1, s0:s1], seg[b:b + 1, s0:s1], pos[b:b + 1, s0:s1], h0[b:b + 1, s0:s1]
+    dims = oc.Dims(n_heads=cfg.n_heads, head_dim=cfg.head_dim, D=cfg.D, eps=cfg.eps, rope_base=cfg.rope_base)
+    return oc.chain_forward_loss(tok, seg, pos, h0, W, dims,
+                                 precision="bf16" if cfg.dtype == "bf16" else "f64", **kw)
+
+
+def tolerances(cfg):
+    return (1e-4, 0.0, 1e-5) if cfg.dtype == "f32" else (2e-2, 2e-2, 1e-3)
+
+
+def compare_rows(cfg, g, r, window=None):
+    atol, rtol, ltol = tolerances(cfg)
+    b, s0, s1 = window if window else (slice(None), 0, cfg.T)
+    gh = g["h"][:, b, s0:s1] if window else g["h"]
+    gl = g["row_loss"][:, b, s0:s1] if window else g["row_loss"]
+    rh, rl = (r["h"][:, 0], r["row_loss"][:, 0]) if window else (r["h"], r["row_loss"])
+    mh = np.isfinite(rh)
+    assert mh.any()
+    assert np.all(np.isfinite(gh[mh]))
+    err = np.abs(gh[mh] - rh[mh])
+    assert np.all(err <= atol + rtol * np.abs(rh[mh])), f"h max err {err.max()}"
+    ml = np.isfinite(rl)
+    assert np.array_equal(np.isfinite(gl[ml]), np.ones(ml.sum(), bool))
+    lerr = np.abs(gl[ml] - rl[ml]) / np.abs(rl[ml])
+    assert lerr.max() <= max(ltol * 5, 2e-3 if cfg.dtype == "bf16" else 1e-5), f"row loss rel err {lerr.max()}"
+    return err.max(), lerr.max()
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "small_f32_D3", "small_bf16_D2", "small_bf16_hd128"])
+@pytest.mark.parametrize("den", ["fixed", "masked_mean"])
+def test_full_parity_small(name, den):
+    cfg = synth.CHAIN_CONFIGS[name]
+    inp = synth.make_chain_inputs(cfg, seed=11)
+    g = run_gpu(cfg, to_dev(inp), den=den)
+    r = run_oracle(cfg, inp, lam=cfg.lam, den=den)
+    # supervised-row counts are exact
+    counts = g["sums_counts"][1::2]
+    assert np.array_equal(counts, r["counts"].astype(np.float64))
+    # rows without a label are NaN on both sides; rows with a label match
+    assert np.array_equal(np.isfinite(g["row_loss"]), np.isfinite(r["row_loss"]))
+    compare_rows(cfg, g, r)
+    _, _, ltol = tolerances(cfg)
+    want = [r["loss_total"], r["loss_main"], *r["loss_mtp"]]
+    np.testing.assert_allclose(g["losses"], want, rtol=ltol, atol=1e-7)
+    np.testing.assert_allclose(g["sums_counts"][0::2], r["sums"], rtol=ltol)
+
+
+def test_tiny_config_counts_and_no_main():
+    cfg = synth.TINY_F32
+    inp = synth.make_chain_inputs(cfg, seed=3)
+    g = run_gpu(cfg, to_dev(inp))
+    assert list(g["sums_counts"][1::2]) == [24.0, 21.0]
+    g0 = run_gpu(cfg, to_dev(inp), with_main=False, lam=0.0)
+    assert g0["losses"][0] == 0.0 and g0["sums_counts"][0] == 0.0
+    assert np.all(np.isnan(g0["row_loss"][0]))
+
+
+def test_exhausted_depths_contribute_zero():
+    cfg = synth.SMALL_F32.with_(name="short", T=4, D=3, layout="split", split_at=2)
+    inp = synth.make_chain_inputs(cfg, seed=5)
+    g = run_gpu(cfg, to_dev(inp), den="masked_mean")
+    r = run_oracle(cfg, inp, lam=cfg.lam, den="masked_mean")
+    assert list(g["sums_counts"][1::2]) == list(r["counts"].astype(float))
+    assert g["losses"][3] == 0.0 and g["losses"][4] == 0.0
+    np.testing.assert_allclose(g["losses"][:2], [r["loss_total"], r["loss_main"]], rtol=1e-5)
+
+
+def test_packing_invariance_on_gpu():
+    """A packed row equals its documents run in separate rows (segment rule
+    applies to the attention graph)."""
+    cfg = synth.SMALL_BF16.with_(name="pack", B=1, T=256, layout="split", split_at=100, pad_rows=0)
+    inp = synth.make_chain_inputs(cfg, seed=9)
+    packed = run_gpu(cfg, to_dev(inp))
+    cfg2 = cfg.with_(B=2)
+    sep = {k: torch.zeros((2,) + v.shape[1:], dtype=v.dtype) for k, v in inp.items() if k != "weights"}
+    sep["seg"][:] = -1
+    for row, (a, b) in enumerate(((0, 100), (100, 256))):
+        n = b - a
+        for k in ("tokens", "pos", "h0"):
+            sep[k][row, :n] = inp[k][0, a:b]
+        sep["seg"][row, :n] = 0
+    sep["weights"] = inp["weights"]
+    alone = run_gpu(cfg2, to_dev(sep))
+    for k in range(cfg.D):
+        for row, (a, b) in enumerate(((0, 100), (100, 256))):
+            n = b - a
+            ph, ah = packed["h"][k, 0, a:b], alone["h"][k, row, :n]
+            valid = np.arange(n) + k + 1 < n
+            # attention key blocks are cut differently, so rounding may differ slightly
+            np.testing.assert_allclose(ph[valid], ah[valid], atol=2e-2, rtol=2e-2)
+
+
+def window_starts(seg_row, n_windows, max_len):
+    """(start, end) of the first n_windows segments (whole-segment prefixes)."""
+    starts = [0] + [t for t in range(1, len(seg_row)) if seg_row[t] != seg_row[t - 1]]
+    out = []
+    for s in starts:
+        if seg_row[s] == -1:
+            continue
+        e = s
+        while e < len(seg_row) and seg_row[e] == seg_row[s]:
+            e += 1
+        out.append((s, min(e, s + max_len)))
+        if len(out) == n_windows:
+            break
+    return out
+
+
+def test_mid_config_sampled_windows():
+    """B=8, T=1024, d=1024, D=3, V=32000 (the mid-size workload), full size on
+    the GPU; oracle on whole-segment prefixes of two packed rows."""
+    cfg = synth.MID_BF16
+    inp = synth.make_chain_inputs(cfg, seed=1)
+    g = run_gpu(cfg, to_dev(inp))
+    W = oc.weights_to_numpy(inp["weights"])
+    seg = inp["seg"].numpy()
+    checked = 0
+    for b in (0, 5):
+        for (s0, s1) in window_starts(seg[b], 2, 192):
+            r = run_oracle(cfg, inp, W=W, window=(b, s0, s1), lam=cfg.lam)
+            compare_rows(cfg, g, r, window=(b, s0, s1))
+            checked += 1
+    assert checked >= 3
+    # counts over the whole batch equal the row compiler's, exactly
+    tok = inp["tokens"].numpy()
+    n_state = np.zeros(cfg.D, int)
+    n_loss = np.zeros(cfg.D, int)
+    n_main = 0
+    for b in range(cfg.B):
+        act = [s != -1 for s in seg[b]]
+        n_main += sum(label_owned(act, list(seg[b]), t, 1) for t in range(cfg.T))
+        for k, rows in enumerate(compile_all_depths(list(tok[b]), list(seg[b]), act, cfg.D)):
+            n_loss[k] += sum(r_.loss_valid for r_ in rows)
+    assert list(g["sums_counts"][1::2]) == [float(n_main)] + [float(c) for c in n_loss]
+    # the reported terms are the reported row losses reduced by the policy
+    rl = g["row_loss"]
+    sums = np.nansum(rl.reshape(cfg.D + 1, -1).astype(np.float64), axis=1)
+    np.testing.assert_allclose(g["sums_counts"][0::2], sums, rtol=1e-5)
+    terms = sums / (cfg.B * cfg.T)
+    np.testing.assert_allclose(g["losses"][1:], terms, rtol=1e-5)
+    np.testing.assert_allclose(g["losses"][0], terms[0] + cfg.lam / cfg.D * terms[1:].sum(), rtol=1e-5)
+
+
+def test_dsv3_width_sampled_windows():
+    """B=1, T=4096, d=7168, 56x128 heads, ffn 18432, V=129280, D=1, one
+    packed boundary at 2048; oracle on 64-row prefixes of both segments."""
+    cfg = synth.DSV3_BF16
+    inp = synth.make_chain_inputs(cfg, seed=2)
+    g = run_gpu(cfg, to_dev(inp))
+    W = oc.weights_to_numpy(inp["weights"])
+    for (s0, s1) in ((0, 64), (2048, 2112)):
+        r = run_oracle(cfg, inp, W=W, window=(0, s0, s1), lam=cfg.lam)
+        compare_rows(cfg, g, r, window=(0, s0, s1))
+    assert list(g["sums_counts"][1::2]) == [4094.0, 4092.0]
