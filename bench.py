@@ -1,0 +1,466 @@
+#!/usr/bin/env python3
+"""Benchmark of the sequential-MTP hot path on GB300.
+
+One step = the whole hot path over one batch of synthetic input:
+  * mtp_chain_loss on the mid-size MTP-chain workload (B=8 packed rows of
+    T=1024, d=1024, 16x64 heads, SwiGLU ffn 2816, V=32000, D=3 sequential
+    depths, Zipf(1.1) tokens, geometric documents of mean length 256): the
+    main term plus the masked CE of every depth and the assembled loss;
+  * spec_verify on the verification workload (64 requests, gamma=4 drafts,
+    V=129280, target/draft rows built with mean overlap ~0.70).
+
+value = MTP-chain tokens per step (sum over depths k of B*(T-k) rows) / the
+step's device time (CUDA events on the launching stream, max over ranks,
+times the number of ranks).  spec_verify rows/s (R*(gamma+1) rows per call)
+is reported beside it.  L2 is flushed (256 MiB write) between timed steps,
+outside the events.  `roofline` covers the dominant kernel (the shared-head
+GEMM with the fused online-softmax CE epilogue); `cpu_baseline` times the
+CPU oracle on a bounded sample of the same workload.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) each rank runs its own batch (weak scaling); the one
+exchange is the data-parallel all-reduce of the per-term (sum, count) pairs
+before the loss is assembled.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MTP-chain tokens/s (all depths) + spec_verify rows/s, % of roofline"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+HEAD_PROFILE = os.path.join(ROOT, "profiles", "head_ce_gemm_mid_bf16.md")
+GEMM_SOURCES = [os.path.join(ROOT, "deepseek_sequential_mtp_gb300", "csrc", f)
+                for f in ("gemm_tc.cu", "gemm_tc.cuh")]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            pk = json.load(fh)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def gemm_source_hash():
+    h = hashlib.sha256()
+    for p in GEMM_SOURCES:
+        with open(p, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """Per-launch DRAM traffic of the head GEMM from the committed ncu summary,
+    or None when it is absent or was taken on other kernel sources."""
+    try:
+        text = open(HEAD_PROFILE).read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, _, v = line[2:].partition(":")
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_sha256") != gemm_source_hash():
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------------------------
+# nvidia-smi clock sampling during the timed region
+# --------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle baseline (the reference arm and the cpu_baseline leg)
+# --------------------------------------------------------------------------
+def first_segment_window(seg_row, max_len):
+    s = 0
+    while s < len(seg_row) and seg_row[s] == -1:
+        s += 1
+    e = s
+    while e < len(seg_row) and seg_row[e] == seg_row[s] and e - s < max_len:
+        e += 1
+    return s, e
+
+
+def oracle_sample(cfg, batch, h0, W, b, max_len):
+    """Runs the oracle's chain + loss on one whole-segment prefix of packed row
+    b; returns (tokens processed, seconds)."""
+    import numpy as np
+    from oracle import chain as oc
+    s0, s1 = first_segment_window(batch["seg"][b], max_len)
+    dims = oc.Dims(n_heads=cfg.n_heads, head_dim=cfg.head_dim, D=cfg.D, eps=cfg.eps, rope_base=cfg.rope_base)
+    t = time.perf_counter()
+    out = oc.chain_forward_loss(batch["tokens"][b:b + 1, s0:s1], batch["seg"][b:b + 1, s0:s1],
+                                batch["pos"][b:b + 1, s0:s1], h0[b:b + 1, s0:s1], W, dims,
+                                precision="bf16", lam=cfg.lam)
+    dt = time.perf_counter() - t
+    tokens = int(np.isfinite(out["h"][:, 0, :, 0]).sum())  # state rows over all depths
+    return tokens, dt
+
+
+def cpu_oracle_inputs(cfg, seed):
+    from deepseek_sequential_mtp_gb300 import synth
+    from oracle import chain as oc
+    batch = synth.make_batch(cfg, seed)
+    h0 = synth.make_h0(cfg, seed).float().numpy()
+    W = oc.weights_to_numpy(synth.make_weights(cfg, seed + 1))
+    return batch, h0, W
+
+
+def cpu_baseline(cfg, seed, seconds, max_len=256):
+    batch, h0, W = cpu_oracle_inputs(cfg, seed)
+    tok_total, t_total, n = 0, 0.0, 0
+    while t_total < seconds or n == 0:
+        tok, dt = oracle_sample(cfg, batch, h0, W, n % cfg.B, max_len)
+        tok_total += tok
+        t_total += dt
+        n += 1
+    return {"value": tok_total / t_total, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} whole-segment prefixes (<= {max_len} rows) of the mid workload's packed rows, "
+                      f"all {cfg.D} depths + main and depth heads, fp64 numpy with bf16 storage rounding; "
+                      f"{t_total:.1f} s"}
+
+
+# --------------------------------------------------------------------------
+# Reference arm: the CPU oracle, timed on the host cores
+# --------------------------------------------------------------------------
+def run_reference(args):
+    from deepseek_sequential_mtp_gb300 import synth
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    cfg = synth.MID_BF16
+    batch, h0, W = cpu_oracle_inputs(cfg, 1)
+    per_step_rows = 32  # bounded sample per step so K + W steps end within minutes
+    for i in range(args.warmup):
+        oracle_sample(cfg, batch, h0, W, i % cfg.B, per_step_rows)
+    tok_total, t_total = 0, 0.0
+    for i in range(args.steps):
+        tok, dt = oracle_sample(cfg, batch, h0, W, i % cfg.B, per_step_rows)
+        tok_total += tok
+        t_total += dt
+    value = tok_total / t_total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"per step one whole-segment prefix (<= {per_step_rows} rows) of a packed "
+                                       f"row of the mid workload, all depths + heads, fp64 numpy"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config():
+    return {"workload": "mtp_chain mid_bf16_D3 (B=8, T=1024, d=1024, 16x64 heads, SwiGLU ffn=2816, V=32000, "
+                        "D=3, Zipf(1.1) tokens, geometric docs mean 256, lambda=0.3, main+3 depth CE) + "
+                        "spec_verify (R=64, gamma=4, V=129280, alpha~0.70)",
+            "global_batch": 8, "seq_len": 1024, "parallelism": "dp (independent packed rows per rank)",
+            "l2": "flushed between timed steps (256 MiB write outside the step events)"}
+
+
+# --------------------------------------------------------------------------
+# Our arm
+# --------------------------------------------------------------------------
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from deepseek_sequential_mtp_gb300 import build as mtp_build
+    from deepseek_sequential_mtp_gb300 import lib, synth
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    mtp_build.build()
+    dev = torch.device("cuda", local_rank if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    cfg = synth.MID_BF16
+    vcfg = synth.VERIFY_C4
+    seed = 1 + 1000 * rank
+
+    # inputs resident in HBM
+    batch = synth.make_batch(cfg, seed)
+    x = {k: torch.from_numpy(v).to(dev) for k, v in batch.items()}
+    x["h0"] = synth.make_h0(cfg, seed, device=dev)
+    weights = synth.make_weights(cfg, seed + 1, device=dev)
+    vin = synth.make_verify_inputs(vcfg, seed, device=dev)
+    chain = lib.Chain(cfg, weights, device=dev)
+    out = {"sums_counts": torch.empty(2 * (cfg.D + 1), dtype=torch.float64, device=dev),
+           "losses": torch.empty(cfg.D + 2, dtype=torch.float32, device=dev)}
+    K, W = args.steps, args.warmup
+    vouts = torch.empty((K + W, 4, vcfg.R), dtype=torch.int32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    global_losses = torch.empty(cfg.D + 2, dtype=torch.float32, device=dev)
+
+    def step(i):
+        chain.loss(x["tokens"], x["seg"], x["pos"], x["h0"], den="fixed", with_main=True, out=out)
+        if world > 1:
+            torch.distributed.all_reduce(out["sums_counts"])
+            lib.loss_assemble(out["sums_counts"], cfg.D, world * cfg.B * cfg.T, cfg.lam, "fixed", True,
+                              losses=global_losses)
+        vo = vouts[i]
+        lib.spec_verify(vin["p"], vin["q"], vin["draft"], seed=7 + rank, offset=i,
+                        out={"accepted": vo[0], "next_token": vo[1], "n_emit": vo[2], "status": vo[3]})
+
+    for i in range(W):
+        flush.zero_()
+        step(i)
+    torch.cuda.synchronize()
+    lib.check_errors()
+
+    timers = {name: lib.KernelTimer(name, launches * K)
+              for name, launches in (("head_ce_gemm", cfg.D + 1), ("gate_up_gemm", cfg.D), ("down_gemm", cfg.D),
+                                     ("qkv_gemm", cfg.D), ("o_gemm", cfg.D), ("proj_gemm", cfg.D),
+                                     ("attention", cfg.D), ("spec_verify", 1))}
+    torch.cuda.synchronize()
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for t in timers.values():
+        t.arm()
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    clocks = ClockSampler(visible[local_rank] if len(visible) > local_rank and visible[local_rank] else str(local_rank))
+    clocks.start()
+    launches0 = lib.kernel_launches()
+    t_wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        ev0[i].record()
+        step(W + i)
+        ev1[i].record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    launches = lib.kernel_launches() - launches0
+    clk = clocks.stop()
+    lib.KernelTimer.disarm_all()
+    lib.check_errors()
+
+    step_ms = sum(a.elapsed_time(b) for a, b in zip(ev0, ev1)) / K
+    step_ms_t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(step_ms_t, op=torch.distributed.ReduceOp.MAX)
+    step_ms_max = float(step_ms_t.item())
+    tokens_per_step = sum(cfg.B * (cfg.T - k) for k in range(1, cfg.D + 1))
+    value = world * tokens_per_step / (step_ms_max / 1e3)
+
+    # per-kernel durations measured inside the timed region
+    kern = {name: t.durations_ms() for name, t in timers.items()}
+    counts = out["sums_counts"][1::2].cpu().numpy()  # supervised rows per term (same every step)
+    peaks, peak_src = load_peaks()
+    head_ms = kern["head_ce_gemm"]
+    # algorithmic FLOPs of the head GEMM: 2 d V per supervised row, for main + each depth
+    head_flops_step = 2.0 * cfg.d * cfg.V * float(counts.sum())
+    head_ms_step = sum(head_ms) / K
+    head_launch_flops = head_flops_step / (cfg.D + 1)
+    head_launch_ms = head_ms_step / (cfg.D + 1)
+    achieved = head_launch_flops / (head_launch_ms / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    traffic = recorded_traffic()
+    roofline = {"bound": "tensor", "kernel": "gemm_tc_kernel<256, EPI_CE> (shared head + online CE)",
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": traffic,
+                "peak_source": f"bf16_tflops_sustained, {peak_src} (MEASURED_PEAKS.json)"
+                if peak_src == "measured" else "fallback 1.7 PFLOP/s sustained",
+                "algorithmic_flops_per_launch": head_launch_flops, "avg_launch_ms": head_launch_ms}
+
+    # per-kernel table: algorithmic FLOPs per step and achieved TFLOP/s
+    M = cfg.B * cfg.T
+    d, f = cfg.d, cfg.ffn
+    state_rows = float(tokens_per_step)  # rows with state over depths (upper bound used for the metric)
+    per_row = {"gate_up_gemm": 4 * d * f, "down_gemm": 2 * d * f, "qkv_gemm": 6 * d * d, "o_gemm": 2 * d * d,
+               "proj_gemm": 4 * d * d}
+    breakdown = {}
+    for name, ms in kern.items():
+        tot = sum(ms) / K
+        entry = {"ms_per_step": tot, "launches_per_step": len(ms) / K}
+        if name in per_row:
+            fl = per_row[name] * state_rows
+            entry["tflops"] = fl / (tot / 1e3) / 1e12 if tot > 0 else None
+            entry["frac_of_peak"] = entry["tflops"] / peak if entry["tflops"] else None
+        if name == "head_ce_gemm":
+            entry["tflops"] = achieved
+            entry["frac_of_peak"] = achieved / peak
+        breakdown[name] = entry
+
+    # spec_verify: rows/s and algorithmic HBM bytes (decision scalars + the one sampled row pair or row)
+    vo = vouts[W:].cpu().numpy()
+    acc, st = vo[:, 0], vo[:, 3]
+    n_tok = vo[:, 1]
+    rej = (acc < vcfg.gamma) & (n_tok >= 0)
+    bonus = (acc == vcfg.gamma) & (n_tok >= 0)
+    examined = np.minimum(acc + 1, vcfg.gamma)
+    vbytes = (8.0 * examined + 8.0 * vcfg.V * rej + 4.0 * vcfg.V * bonus).sum(axis=1)  # per call
+    v_ms = kern["spec_verify"]
+    v_ms_mean = sum(v_ms) / len(v_ms)
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    v_gbs = float(vbytes.mean()) / (v_ms_mean / 1e3) / 1e9
+    verify = {"rows_per_s": world * vcfg.R * (vcfg.gamma + 1) / (v_ms_mean / 1e3),
+              "requests_per_s": world * vcfg.R / (v_ms_mean / 1e3), "us_per_call": 1e3 * v_ms_mean,
+              "algorithmic_bytes_per_call": float(vbytes.mean()), "achieved_gbs": v_gbs, "peak_gbs": hbm_peak,
+              "frac": v_gbs / hbm_peak, "mean_accepted": float(acc.mean()), "status_nonzero": int((st != 0).sum())}
+
+    # end to end through the public API: pinned host inputs -> device, result -> host, every step
+    e2e = measure_e2e(cfg, vcfg, chain, batch, x, vin, args.e2e_steps, dev, rank, world, tokens_per_step)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, 1, args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+                "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic (seeded; random-init weights of the workload's shapes)",
+                "config": workload_config(), "roofline": roofline, "spec_verify": verify,
+                "spec_verify_rows_per_s": verify["rows_per_s"], "kernels": breakdown,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+                "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+                "clock_samples": clk["samples"], "wall_s_timed_region": t_wall,
+                "loss": float(out["losses"][0].item())}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def measure_e2e(cfg, vcfg, chain, batch, x, vin, steps, dev, rank, world, tokens_per_step):
+    import torch
+
+    from deepseek_sequential_mtp_gb300 import lib
+
+    host = {k: torch.from_numpy(v).pin_memory() for k, v in batch.items()}
+    host["h0"] = x["h0"].cpu().pin_memory()
+    hv = {k: v.cpu().pin_memory() for k, v in vin.items()}
+    dx = {k: torch.empty_like(v) for k, v in x.items()}
+    dv = {k: torch.empty_like(v) for k, v in vin.items()}
+    res_l = torch.empty(cfg.D + 2, dtype=torch.float32).pin_memory()
+    res_v = torch.empty((4, vcfg.R), dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + list(hv.values()))
+    d2h = res_l.numel() * 4 + res_v.numel() * 4
+    times = []
+    for i in range(steps + 2):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for k in dx:
+            dx[k].copy_(host[k], non_blocking=True)
+        for k in dv:
+            dv[k].copy_(hv[k], non_blocking=True)
+        o = chain.loss(dx["tokens"], dx["seg"], dx["pos"], dx["h0"], den="fixed", with_main=True)
+        v = lib.spec_verify(dv["p"], dv["q"], dv["draft"], seed=7 + rank, offset=10 ** 6 + i)
+        res_l.copy_(o["losses"], non_blocking=True)
+        for j, kk in enumerate(("accepted", "next_token", "n_emit", "status")):
+            res_v[j].copy_(v[kk], non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= 2:
+            times.append(time.perf_counter() - t0)
+    per = statistics.median(times)
+    return {"value": world * tokens_per_step / per, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": 1e3 * per,
+            "note": "chain inputs (tokens, seg, pos, h0) and verify inputs (p, q, drafts) copied from pinned "
+                    "host memory each step; losses and verify outputs read back"}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,6 +1,58 @@
 // Library-wide entry points: status strings, ABI version and the device
 // error-word check that ORs the words of every kernel file.
+#include <atomic>
+
 #include "common.cuh"
+
+namespace mtp {
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+struct Hook {
+  cudaEvent_t* ev = nullptr;
+  int n = 0;
+  int* recorded = nullptr;
+  int open = -1;  // index of the pair whose start has been recorded
+};
+Hook g_hooks[MTP_KC_COUNT];
+}  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+void prof_begin(int kernel_class, cudaStream_t stream) {
+  if (kernel_class < 0 || kernel_class >= MTP_KC_COUNT) return;
+  Hook& h = g_hooks[kernel_class];
+  if (!h.ev || *h.recorded >= h.n) return;
+  h.open = *h.recorded;
+  cudaEventRecord(h.ev[2 * h.open], stream);
+}
+
+void prof_end(int kernel_class, cudaStream_t stream) {
+  if (kernel_class < 0 || kernel_class >= MTP_KC_COUNT) return;
+  Hook& h = g_hooks[kernel_class];
+  if (!h.ev || h.open < 0) return;
+  cudaEventRecord(h.ev[2 * h.open + 1], stream);
+  *h.recorded = h.open + 1;
+  h.open = -1;
+}
+}  // namespace mtp
+
+extern "C" mtp_status mtp_profile_kernel(int kernel_class, cudaEvent_t* events, int n_pairs, int* recorded) {
+  if (kernel_class < 0 || kernel_class >= MTP_KC_COUNT) return MTP_ERR_INVALID_ARG;
+  mtp::Hook& h = mtp::g_hooks[kernel_class];
+  if (!events) {
+    h = mtp::Hook{};
+    return MTP_OK;
+  }
+  if (n_pairs < 0 || !recorded) return MTP_ERR_INVALID_ARG;
+  h.ev = events;
+  h.n = n_pairs;
+  h.recorded = recorded;
+  h.open = -1;
+  *recorded = 0;
+  return MTP_OK;
+}
+
+extern "C" unsigned long long mtp_kernel_launches(void) { return mtp::g_launches.load(); }
 
 unsigned int mtp_take_errors_chain();
 unsigned int mtp_take_errors_gemm();

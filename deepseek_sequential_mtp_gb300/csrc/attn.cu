@@ -281,6 +281,7 @@ mtp_status attn_launch(int dtype, const void* qkv, void* out, const int32_t* seg
       constexpr int smem = (kBQ + 4 * kBK) * 64 * 2;
       flash_attn_bf16_kernel<64><<<grid, kThreads, smem, stream>>>(
           static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out), seg_start, T, H, scale_log2);
+      mtp::note_launch();
     } else if (hd == 128) {
       constexpr int smem = (kBQ + 4 * kBK) * 128 * 2;
       static bool attr = false;
@@ -292,6 +293,7 @@ mtp_status attn_launch(int dtype, const void* qkv, void* out, const int32_t* seg
       }
       flash_attn_bf16_kernel<128><<<grid, kThreads, smem, stream>>>(
           static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out), seg_start, T, H, scale_log2);
+      mtp::note_launch();
     } else {
       return MTP_ERR_UNSUPPORTED;
     }
@@ -310,6 +312,7 @@ mtp_status attn_launch(int dtype, const void* qkv, void* out, const int32_t* seg
     attn_f32_kernel<<<(items + warps - 1) / warps, warps * 32, smem, stream>>>(
         static_cast<const float*>(qkv), static_cast<float*>(out), seg_start, B * T, T, H, hd,
         1.0f / sqrtf(static_cast<float>(hd)));
+    mtp::note_launch();
   }
   MTP_LAUNCH_CHECK();
   return MTP_OK;

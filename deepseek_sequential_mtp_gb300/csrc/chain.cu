@@ -476,6 +476,7 @@ mtp_status gemm<float>(const Ctx& C, const float* A, int lda, const float* const
   auto run = [&](const float* B, float* o, int n, int ldo_, const float* R, int ldr_) {
     const dim3 grid((n + 63) / 64, (C.M + 63) / 64);
     gemm_f32_kernel<<<grid, 256, 0, C.st>>>(A, lda, B, K, o, ldo_, R, ldr_, C.M, n, K);
+    mtp::note_launch();
   };
   if (epi == mtp::EPI_SWIGLU) {
     float* U = C.buf<float>(C.L.g2);
@@ -483,12 +484,14 @@ mtp_status gemm<float>(const Ctx& C, const float* A, int lda, const float* const
     run(B2, U, N, N, nullptr, 0);
     const size_t n = static_cast<size_t>(C.M) * N;
     swiglu_f32_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, C.st>>>(out, U, out, n);
+    mtp::note_launch();
   } else {
     for (int s = 0; s < nseg; ++s) run(Bs[s], out + static_cast<size_t>(s) * seg_rows, seg_rows, ldo, resid, ldr);
     if (epi == mtp::EPI_ROPE && C.D.rope_base > 0.f) {
       const int n = C.M * C.D.d;
       rope_f32_kernel<<<(n + 255) / 256, 256, 0, C.st>>>(out, C.pos, C.buf<float2>(C.L.rope), C.M, C.D.d,
                                                           C.D.head_dim, C.D.T);
+      mtp::note_launch();
     }
   }
   MTP_LAUNCH_CHECK();
@@ -510,8 +513,10 @@ mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double
   float2* part = C.buf<float2>(C.L.ce_part);
   float* zt = C.buf<float>(C.L.zt);
   rmsnorm_kernel<T><<<warp_blocks(C.M), 256, 0, C.st>>>(h, static_cast<const T*>(C.W.out_norm), x, C.M, D.d, D.eps);
+  mtp::note_launch();
   labels_kernel<<<(C.M + 255) / 256, 256, 0, C.st>>>(C.tokens, C.seg, C.buf<int32_t>(C.L.seg_end), labels, C.M, D.T,
                                                      k, D.V);
+  mtp::note_launch();
   MTP_LAUNCH_CHECK();
   if constexpr (sizeof(T) == 2) {
     mtp::GemmDesc g;
@@ -528,12 +533,16 @@ mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double
     g.labels = labels;
     g.ce_part = part;
     g.z_tgt = zt;
+    mtp::prof_begin(MTP_KC_HEAD_CE_GEMM, C.st);
     TRY(mtp::gemm_bf16_launch(g, C.st));
+    mtp::prof_end(MTP_KC_HEAD_CE_GEMM, C.st);
   } else {
     head_ce_f32_kernel<<<dim3(C.L.nvt, C.M), 256, 0, C.st>>>(x, static_cast<const float*>(C.W.head), D.d, D.V, labels,
                                                              part, zt, C.L.nvt);
+    mtp::note_launch();
   }
   ce_reduce_kernel<<<(C.M + 255) / 256, 256, 0, C.st>>>(C.M, C.L.nvt, part, zt, labels, row_loss_term, sum_count);
+  mtp::note_launch();
   MTP_LAUNCH_CHECK();
   return MTP_OK;
 }
@@ -546,16 +555,19 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
   const size_t Md = static_cast<size_t>(M) * d;
   segments_kernel<<<D.B, kScanThreads, 0, C.st>>>(C.seg, C.tokens, D.T, D.V, C.buf<int32_t>(C.L.seg_start),
                                                   C.buf<int32_t>(C.L.seg_end));
+  mtp::note_launch();
   const int half = D.head_dim / 2;
   if (D.rope_base > 0.f) {
     rope_table_kernel<<<(D.T * half + 255) / 256, 256, 0, C.st>>>(C.buf<float2>(C.L.rope), D.T, half, D.head_dim,
                                                                   static_cast<double>(D.rope_base));
+    mtp::note_launch();
   } else {
     cudaMemsetAsync(C.buf<float2>(C.L.rope), 0, static_cast<size_t>(D.T) * half * sizeof(float2), C.st);
   }
   MTP_LAUNCH_CHECK();
   if (with_loss) {
     zero_f64_kernel<<<1, 64, 0, C.st>>>(sums_counts, 2 * (D.D + 1));
+    mtp::note_launch();
     if (with_main) TRY(head_ce<T>(C, h0, 0, row_loss, sums_counts));
     else if (row_loss)
       cudaMemsetAsync(row_loss, 0xff, static_cast<size_t>(M) * sizeof(float), C.st);  // NaN
@@ -574,20 +586,35 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
     auto wt = [&](const void* const* arr) { return static_cast<const T*>(arr[i]); };
     prologue_kernel<T><<<warp_blocks(M), 256, 0, C.st>>>(h_prev, C.tokens, static_cast<const T*>(C.W.embed),
                                                          wt(C.W.hnorm), wt(C.W.enorm), c, M, D.T, d, D.V, k, D.eps);
+    mtp::note_launch();
     MTP_LAUNCH_CHECK();
     const T* proj[1] = {wt(C.W.eh_proj)};
+    mtp::prof_begin(MTP_KC_PROJ_GEMM, C.st);
     TRY(gemm<T>(C, c, 2 * d, proj, 1, d, 2 * d, d, u, d, mtp::EPI_STORE));
+    mtp::prof_end(MTP_KC_PROJ_GEMM, C.st);
     rmsnorm_kernel<T><<<warp_blocks(M), 256, 0, C.st>>>(u, wt(C.W.attn_norm), x, M, d, D.eps);
+    mtp::note_launch();
     const T* wqkv[3] = {wt(C.W.wq), wt(C.W.wk), wt(C.W.wv)};
+    mtp::prof_begin(MTP_KC_QKV_GEMM, C.st);
     TRY(gemm<T>(C, x, d, wqkv, 3, d, d, 3 * d, qkv, 3 * d, D.rope_base > 0.f ? mtp::EPI_ROPE : mtp::EPI_STORE));
+    mtp::prof_end(MTP_KC_QKV_GEMM, C.st);
+    mtp::prof_begin(MTP_KC_ATTENTION, C.st);
     TRY(mtp::attn_launch(D.dtype, qkv, o, C.buf<int32_t>(C.L.seg_start), D.B, D.T, D.n_heads, D.head_dim, C.st));
+    mtp::prof_end(MTP_KC_ATTENTION, C.st);
     const T* wo[1] = {wt(C.W.wo)};
+    mtp::prof_begin(MTP_KC_O_GEMM, C.st);
     TRY(gemm<T>(C, o, d, wo, 1, d, d, d, a, d, mtp::EPI_RESID, u, d));
+    mtp::prof_end(MTP_KC_O_GEMM, C.st);
     rmsnorm_kernel<T><<<warp_blocks(M), 256, 0, C.st>>>(a, wt(C.W.ffn_norm), x, M, d, D.eps);
+    mtp::note_launch();
     const T* wg[1] = {wt(C.W.w_gate)};
+    mtp::prof_begin(MTP_KC_GATE_UP_GEMM, C.st);
     TRY(gemm<T>(C, x, d, wg, 1, D.ffn, d, D.ffn, g, D.ffn, mtp::EPI_SWIGLU, nullptr, 0, wt(C.W.w_up)));
+    mtp::prof_end(MTP_KC_GATE_UP_GEMM, C.st);
     const T* wd[1] = {wt(C.W.w_down)};
+    mtp::prof_begin(MTP_KC_DOWN_GEMM, C.st);
     TRY(gemm<T>(C, g, D.ffn, wd, 1, d, D.ffn, d, h_k, d, mtp::EPI_RESID, a, d));
+    mtp::prof_end(MTP_KC_DOWN_GEMM, C.st);
     if (with_loss)
       TRY(head_ce<T>(C, h_k, k, row_loss ? row_loss + static_cast<size_t>(k) * M : nullptr, sums_counts + 2 * k));
     h_prev = h_k;
@@ -595,6 +622,7 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
   if (with_loss) {
     loss_assemble_kernel<<<1, 32, 0, C.st>>>(sums_counts, losses, D.D, static_cast<double>(M), lambda, den,
                                              with_main);
+    mtp::note_launch();
     MTP_LAUNCH_CHECK();
   }
   return MTP_OK;
@@ -658,4 +686,14 @@ extern "C" mtp_status mtp_chain_loss(const mtp_dims* dims, const mtp_weights* w,
                                     true, lambda, den, with_main, sums_counts, losses, row_loss);
   return run_chain<float>(C, static_cast<const float*>(h0), static_cast<float*>(h_out), true, lambda, den, with_main,
                           sums_counts, losses, row_loss);
+}
+
+extern "C" mtp_status mtp_loss_assemble(int D, const double* sums_counts, double n_positions, float lambda, int den,
+                                        int with_main, float* losses, cudaStream_t stream) {
+  if (D <= 0 || !sums_counts || !losses || !(n_positions > 0)) return MTP_ERR_INVALID_ARG;
+  if (den != MTP_DEN_FIXED && den != MTP_DEN_MASKED_MEAN) return MTP_ERR_INVALID_ARG;
+  loss_assemble_kernel<<<1, 32, 0, stream>>>(sums_counts, losses, D, n_positions, lambda, den, with_main);
+  mtp::note_launch();
+  MTP_LAUNCH_CHECK();
+  return MTP_OK;
 }

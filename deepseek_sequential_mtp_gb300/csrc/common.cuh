@@ -36,6 +36,11 @@
 
 namespace mtp {
 
+// Host-side launch accounting and the optional event hook (api.cu).
+void note_launch();
+void prof_begin(int kernel_class, cudaStream_t stream);
+void prof_end(int kernel_class, cudaStream_t stream);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

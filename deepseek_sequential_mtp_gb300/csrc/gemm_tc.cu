@@ -557,6 +557,7 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
   const int ntiles = a.tiles_m * a.tiles_n;
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
   gemm_tc_kernel<BN, EPI><<<grid, kThreads, C::kSmemBytes, stream>>>(ta, tb[0], tb[1], tb[2], a);
+  mtp::note_launch();
   MTP_LAUNCH_CHECK();
   return MTP_OK;
 }

@@ -315,6 +315,7 @@ extern "C" mtp_status spec_verify(int R, int gamma, int V, const float* p, const
   if (gamma > 0 && !q) return MTP_ERR_INVALID_ARG;
   const uint2 key = make_uint2((uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32));
   const uint32_t olo = (uint32_t)(offset & 0xFFFFFFFFu), ohi = (uint32_t)(offset >> 32);
+  mtp::prof_begin(MTP_KC_SPEC_VERIFY, stream);
   const bool vec = (V % 4 == 0) && mtp::aligned16(p) && (gamma == 0 || mtp::aligned16(q));
   if (vec)
     spec_verify_kernel<true><<<R, kThreads, 0, stream>>>(gamma, V, p, q, draft, key, olo, ohi, eos,
@@ -322,6 +323,8 @@ extern "C" mtp_status spec_verify(int R, int gamma, int V, const float* p, const
   else
     spec_verify_kernel<false><<<R, kThreads, 0, stream>>>(gamma, V, p, q, draft, key, olo, ohi, eos,
                                                            remaining, accepted, next_token, n_emit, status);
+  mtp::note_launch();
+  mtp::prof_end(MTP_KC_SPEC_VERIFY, stream);
   MTP_LAUNCH_CHECK();
   return MTP_OK;
 }

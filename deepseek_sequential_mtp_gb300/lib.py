@@ -73,6 +73,12 @@ def load() -> ctypes.CDLL:
     lib.mtp_chain_loss.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Weights),
                                    vp, vp, vp, vp, ctypes.c_float, i32, i32,
                                    vp, vp, vp, vp, vp, sz, vp]
+    lib.mtp_loss_assemble.restype = i32
+    lib.mtp_loss_assemble.argtypes = [i32, vp, ctypes.c_double, ctypes.c_float, i32, i32, vp, vp]
+    lib.mtp_profile_kernel.restype = i32
+    lib.mtp_profile_kernel.argtypes = [i32, vp, i32, ctypes.POINTER(ctypes.c_int)]
+    lib.mtp_kernel_launches.restype = ctypes.c_ulonglong
+    lib.mtp_kernel_launches.argtypes = []
     _lib = lib
     return lib
 
@@ -244,3 +250,52 @@ class Chain:
         if h_out is not None:
             out["h"] = h_out
         return out
+
+
+# --------------------------------------------------------------------------
+# Loss assembly (data-parallel callers) and measurement hooks
+# --------------------------------------------------------------------------
+def loss_assemble(sums_counts: torch.Tensor, D: int, n_positions: float, lam: float, den="fixed",
+                  with_main=True, losses: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """L, L_main, L^(1..D) from (already all-reduced) per-term sums and counts."""
+    _need(sums_counts, "sums_counts", torch.float64)
+    if losses is None:
+        losses = torch.empty(D + 2, dtype=torch.float32, device=sums_counts.device)
+    _check(load().mtp_loss_assemble(D, _ptr(sums_counts), float(n_positions), float(lam), DEN[den],
+                                    int(with_main), _ptr(losses), _stream(stream)), "mtp_loss_assemble")
+    return losses
+
+
+KERNEL_CLASSES = {"head_ce_gemm": 0, "gate_up_gemm": 1, "down_gemm": 2, "qkv_gemm": 3, "o_gemm": 4,
+                  "proj_gemm": 5, "attention": 6, "spec_verify": 7}
+
+
+class KernelTimer:
+    """Arms the library's event hook for one kernel class: CUDA events are
+    recorded on the launching stream around each launch of that class."""
+
+    def __init__(self, kernel_class: str, max_launches: int):
+        self.cls = KERNEL_CLASSES[kernel_class]
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * max_launches)]
+        for e in self.events:  # CUDA creates the events on first record
+            e.record()
+        self._handles = (ctypes.c_void_p * (2 * max_launches))(*[e.cuda_event for e in self.events])
+        self.recorded = ctypes.c_int(0)
+        self.max = max_launches
+
+    def arm(self):
+        _check(load().mtp_profile_kernel(self.cls, self._handles, self.max, ctypes.byref(self.recorded)),
+               "mtp_profile_kernel")
+
+    @staticmethod
+    def disarm_all():
+        for c in KERNEL_CLASSES.values():
+            load().mtp_profile_kernel(c, None, 0, None)
+
+    def durations_ms(self):
+        n = self.recorded.value
+        return [self.events[2 * i].elapsed_time(self.events[2 * i + 1]) for i in range(n)]
+
+
+def kernel_launches() -> int:
+    return int(load().mtp_kernel_launches())

@@ -78,7 +78,8 @@ enum {
  * epsilon (the pages leave it open; 1e-6 recommended).  rope_base > 0 applies
  * rotate-half rotary embedding with that base to q and k at the given
  * positions; 0 disables it.  dtype is an mtp_dtype.
- * bf16 requires d % 64 == 0, head_dim in {64, 128}, ffn % 8 == 0. */
+ * bf16 requires d % 128 == 0, head_dim in {64, 128}, ffn % 8 == 0; f32
+ * requires head_dim <= 128 and T <= 12800. */
 typedef struct mtp_dims {
   int B, T, d, n_heads, head_dim, ffn, V, D;
   float eps;
@@ -124,9 +125,11 @@ size_t mtp_chain_workspace_bytes(const mtp_dims* dims);
  * Row t has a state at depth k iff t, ..., t+k are active and in one
  * segment ([M7.6] §0x04C); rows without a state are computed on clamped
  * inputs but their values are undefined.
- *   tokens [B,T] int32 in [0,V); seg [B,T] int32 segment ids, -1 = padding,
- *   each id one contiguous run; pos [B,T] int32 RoPE positions (typically
- *   the index within the segment); h0 [B,T,d] main-model hidden states.
+ *   tokens [B,T] int32 in [0,V) (others set MTP_DEVERR_TOKEN_RANGE and are
+ *   clamped); seg [B,T] int32 segment ids, -1 = padding; within a packed row
+ *   the ids of successive segments strictly increase (a repeated id sets
+ *   MTP_DEVERR_SEGMENTS); pos [B,T] int32 RoPE positions in [0,T), typically
+ *   the index within the segment; h0 [B,T,d] main-model hidden states.
  *   h_out [D,B,T,d] receives h^1..h^D (pre-final-norm states).
  *   ws: workspace of at least mtp_chain_workspace_bytes(dims) bytes. */
 mtp_status mtp_chain_forward(const mtp_dims* dims, const mtp_weights* w,
@@ -151,6 +154,15 @@ mtp_status mtp_chain_loss(const mtp_dims* dims, const mtp_weights* w,
                           const void* h0, float lambda, int den, int with_main,
                           double* sums_counts, float* losses, float* row_loss, void* h_out,
                           void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Loss assembly from per-term (sum, count) pairs ([M7.6] §0x05, §0x06A):
+ * L = L_main + (lambda / D) Σ_k L^(k) with each term reduced by `den`
+ * (FIXED divides by n_positions).  A data-parallel caller all-reduces the
+ * sums_counts of mtp_chain_loss across ranks first -- numerators and
+ * denominators are reduced before dividing -- and passes the global
+ * n_positions.  sums_counts [2*(D+1)] double, losses [D+2] float (device). */
+mtp_status mtp_loss_assemble(int D, const double* sums_counts, double n_positions, float lambda,
+                             int den, int with_main, float* losses, cudaStream_t stream);
 
 /* Exact speculative verification of R requests with gamma drafts each
  * ([M7.6] §0x09 one-proposal selector, generalised to gamma by the
@@ -183,6 +195,32 @@ mtp_status spec_verify(int R, int gamma, int V, const float* p, const float* q,
  * K % 8 == 0; A, B, C 16-byte aligned. */
 mtp_status mtp_gemm_bf16(int M, int N, int K, const void* A, const void* B, void* C,
                          cudaStream_t stream);
+
+/* Kernel classes for mtp_profile_kernel. */
+enum {
+  MTP_KC_HEAD_CE_GEMM = 0,  /* shared head GEMM with the online max/sum-exp epilogue */
+  MTP_KC_GATE_UP_GEMM = 1,  /* gate/up GEMM with the SwiGLU epilogue                 */
+  MTP_KC_DOWN_GEMM = 2,     /* down-projection GEMM with the residual epilogue      */
+  MTP_KC_QKV_GEMM = 3,      /* QKV GEMM with the RoPE epilogue                      */
+  MTP_KC_O_GEMM = 4,        /* attention output GEMM with the residual epilogue     */
+  MTP_KC_PROJ_GEMM = 5,     /* eh_proj fusion GEMM                                  */
+  MTP_KC_ATTENTION = 6,     /* segment-causal attention                             */
+  MTP_KC_SPEC_VERIFY = 7,   /* spec_verify                                          */
+  MTP_KC_COUNT = 8
+};
+
+/* Measurement hook (not thread-safe; for benchmarks).  Each kernel class
+ * has its own slot.  While a slot is armed, every launch of that class issued
+ * by this library records events[2*i] on its stream just before and
+ * events[2*i+1] just after the launch, i = 0, 1, ... up to n_pairs;
+ * *recorded (host) counts the pairs used.  Events are created by the caller
+ * (timing enabled).  A null `events` disarms the slot.  Returns
+ * MTP_ERR_INVALID_ARG on a bad class. */
+mtp_status mtp_profile_kernel(int kernel_class, cudaEvent_t* events, int n_pairs, int* recorded);
+
+/* Number of kernel launches this library has issued since it was loaded
+ * (host-side counter). */
+unsigned long long mtp_kernel_launches(void);
 
 /* Synchronises `stream`, ORs the device error words of every kernel file
  * into *flags (host, nullable) and clears them.  Returns MTP_ERR_DEVICE if
