@@ -155,6 +155,27 @@ mtp_status mtp_chain_loss(const mtp_dims* dims, const mtp_weights* w,
                           double* sums_counts, float* losses, float* row_loss, void* h_out,
                           void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Allocation-free variant of mtp_chain_loss.  The pages have no counterpart:
+ * this is an integration entry point.  It is for callers that cannot call
+ * cudaMalloc or own device memory for a workspace -- plugin hosts whose
+ * allocator belongs to someone else, runtimes that forbid allocation on their
+ * hot path, code that must not touch the allocator in the middle of a
+ * stream.  Same arguments and results as mtp_chain_loss, without ws/ws_bytes:
+ * the workspace is a static device array of MTP_NOALLOC_SCRATCH_BYTES inside
+ * the library, held on every GPU that loads the library until the process
+ * exits.  Returns MTP_ERR_WORKSPACE, launching nothing, when
+ * mtp_chain_workspace_bytes(dims) exceeds that size (small shapes only).  The
+ * first call on a device looks up the array's device address with that device
+ * current; make that first call before any stream capture.  Calls share the
+ * one array: calls that overlap on the GPU race, so serialise them (one
+ * stream, or events).  It allocates nothing itself. */
+#define MTP_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+mtp_status mtp_chain_loss_noalloc(const mtp_dims* dims, const mtp_weights* w,
+                                  const int32_t* tokens, const int32_t* seg, const int32_t* pos,
+                                  const void* h0, float lambda, int den, int with_main,
+                                  double* sums_counts, float* losses, float* row_loss, void* h_out,
+                                  cudaStream_t stream);
+
 /* Loss assembly from per-term (sum, count) pairs ([M7.6] §0x05, §0x06A):
  * L = L_main + (lambda / D) Σ_k L^(k) with each term reduced by `den`
  * (FIXED divides by n_positions).  A data-parallel caller all-reduces the
