@@ -13,7 +13,11 @@
 //              i overlaps the MMAs of tile i+1.
 //   warps 2-5  epilogue: tcgen05.ld 32 lanes x 32 columns per load (warp w
 //              reads TMEM lanes 32*(w%4)..+31 = tile rows), applies the fused
-//              operation and stores bf16 rows (or CE partials).
+//              operation and writes each 32-row x 64-column bf16 box into a
+//              128-byte-swizzled shared-memory buffer (two per warp) that one
+//              lane ships with a TMA store; residual boxes arrive by TMA load
+//              into the same buffer.  The CE epilogue stores only per-row
+//              partials.
 // Every mbarrier wait is bounded: after ~1.5 s it sets MTP_DEVERR_TIMEOUT,
 // raises a CTA abort flag and every role drains out; the producer then waits
 // (bounded) for its in-flight copies and warp 1 for its MMAs before freeing
@@ -35,14 +39,17 @@ constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle atom row
 constexpr int kThreads = 192;
 constexpr int kGroupM = 16;
 
-template <int BN>
+template <int BN, int EPI>
 struct Cfg {
   static constexpr int kStages = BN == 256 ? 4 : 6;
   static constexpr int kABytes = BM * BK * 2;
   static constexpr int kBBytes = BN * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
+  // per epilogue warp: two 32 x 64 bf16 boxes (4 KB each); none for the CE epilogue
+  static constexpr int kBoxBytes = 32 * 64 * 2;
+  static constexpr int kStagingBytes = EPI == EPI_CE ? 0 : 4 * 2 * kBoxBytes;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024 + 256;
 };
 
 // ---------------------------------------------------------------------------
@@ -122,6 +129,20 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// at most one committed store group may still be reading shared memory
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// generic-proxy shared-memory writes become visible to the TMA (async proxy)
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // 32 consecutive fp32 columns of this thread's TMEM lane; the wait is part of
 // the same asm statement so no use of the registers can precede it.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
@@ -186,36 +207,50 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   tn = r / gsz;
 }
 
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&v)[32], int valid) {
-  if (valid >= 32) {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
+// A 32-row x 64-column bf16 box in shared memory with the 128-byte swizzle
+// (what TMA reads/writes with CU_TENSOR_MAP_SWIZZLE_128B): row r occupies
+// bytes [128 r, 128 r + 128) and its 16-byte chunk c sits at chunk c ^ (r & 7).
+// Thread `lane` owns row `lane`; `half` selects columns [32 half, 32 half + 32).
+__device__ __forceinline__ void box_write32(uint8_t* box, int lane, int half, const float (&v)[32]) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      __nv_bfloat162 h[4];
+  for (int q = 0; q < 4; ++q) {
+    __nv_bfloat162 h[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
-      d4[q] = *reinterpret_cast<uint4*>(h);
-    }
-  } else {
-    for (int i = 0; i < valid; ++i) dst[i] = __float2bfloat16_rn(v[i]);
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
+    const int c = half * 4 + q;
+    *reinterpret_cast<uint4*>(box + lane * 128 + ((c ^ (lane & 7)) << 4)) = *reinterpret_cast<uint4*>(h);
   }
 }
-__device__ __forceinline__ void load_row32(const __nv_bfloat16* src, float (&v)[32], int valid) {
-  if (valid >= 32) {
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+__device__ __forceinline__ void box_add32(const uint8_t* box, int lane, int half, float (&v)[32]) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 u = s4[q];
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+  for (int q = 0; q < 4; ++q) {
+    const int c = half * 4 + q;
+    uint4 u = *reinterpret_cast<const uint4*>(box + lane * 128 + ((c ^ (lane & 7)) << 4));
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h[i]);
-        v[8 * q + 2 * i] = f.x;
-        v[8 * q + 2 * i + 1] = f.y;
-      }
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      v[8 * q + 2 * i] += f.x;
+      v[8 * q + 2 * i + 1] += f.y;
     }
-  } else {
-    for (int i = 0; i < 32; ++i) v[i] = i < valid ? __bfloat162float(src[i]) : 0.0f;
+  }
+}
+// 32 (cos, sin) pairs of one RoPE table row, 16-byte loads
+__device__ __forceinline__ void load_cs32(const float2* tab, float2 (&cs)[32]) {
+  const float4* t4 = reinterpret_cast<const float4*>(tab);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float4 f = __ldg(t4 + i);
+    cs[2 * i] = make_float2(f.x, f.y);
+    cs[2 * i + 1] = make_float2(f.z, f.w);
+  }
+}
+__device__ __forceinline__ void rotate32(float (&x1)[32], float (&x2)[32], const float2 (&cs)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float a = x1[i], b = x2[i];
+    x1[i] = a * cs[i].x - b * cs[i].y;
+    x2[i] = b * cs[i].x + a * cs[i].y;
   }
 }
 
@@ -223,22 +258,25 @@ template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
+               const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmRes,
                const Args P) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, EPI>;
   constexpr int S = C::kStages;
   constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
+  uint8_t* staging = smem + S * C::kStageBytes;  // 1024-aligned: stage sizes are multiples of 1 KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + C::kStagingBytes);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
   const uint32_t final_bar = bar0 + 8u * (2 * S + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  auto res_bar = [&](int e, int b) { return bar0 + 8u * (2 * S + 5 + 2 * e + b); };  // residual box loads
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -252,6 +290,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       mbar_init(tempty_bar(a), 128);
     }
     mbar_init(final_bar, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(res_bar(i >> 1, i & 1), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -339,45 +378,87 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   } else if (warp >= 2) {
     // ------------------------------ epilogue ------------------------------
-    const int quarter = warp & 3;
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter.. = tile rows
+    const int ew = warp - 2;       // epilogue warp index: owns two staging boxes
+    uint8_t* boxes = staging + ew * 2 * C::kBoxBytes;
+    int nb = 0;                        // next staging box
+    uint32_t res_phase = 0;            // bit b: parity of box b's residual barrier
+    bool res_pending[2] = {false, false};
     int local = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++local) {
+    bool both_pending = false;         // the last store group read both boxes
+    // claim staging box nb: the store issued from it two boxes ago has read it
+    auto claim = [&]() -> uint8_t* {
+      if (lane == 0) {
+        if (both_pending) bulk_wait_read0();
+        else bulk_wait_read1();
+      }
+      both_pending = false;
+      __syncwarp();
+      return boxes + nb * C::kBoxBytes;
+    };
+    auto ship = [&](uint8_t* box, int col0, int row0w) {
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0 && col0 < P.N && row0w < P.M) {
+        tma_store_2d(&tmOut, col0, row0w, smem_u32(box));
+        bulk_commit();
+      }
+      nb ^= 1;
+    };
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++local) {
       int tm, tn;
       tile_coords(t, P.tiles_m, P.tiles_n, tm, tn);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
       tc_fence_after();
-      const int row = tm * BM + quarter * 32 + lane;
+      const int row0w = tm * BM + quarter * 32;
+      const int row = row0w + lane;
       const bool row_ok = row < P.M;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
 
       if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld32(taddr + c * 32, v);
-          const int col0 = tn * BN + c * 32;
-          if (row_ok && col0 < P.N) {
-            const int valid = min(32, P.N - col0);
-            if constexpr (EPI == EPI_RESID) {
-              float r[32];
-              load_row32(P.resid + static_cast<size_t>(row) * P.ldr + col0, r, valid);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] += r[i];
+        for (int c = 0; c < BN / 64 && ok; ++c) {
+          const int col0 = tn * BN + c * 64;
+          uint8_t* box = claim();
+          const int b = nb;
+          if constexpr (EPI == EPI_RESID) {
+            if (lane == 0 && col0 < P.N && row0w < P.M) {
+              mbar_expect_tx(res_bar(ew, b), C::kBoxBytes);
+              tma_load_2d(smem_u32(box), &tmRes, col0, row0w, res_bar(ew, b));
+              res_pending[b] = true;
             }
-            store_row32(P.out + static_cast<size_t>(row) * P.ldo + col0, v, valid);
           }
+          float v[32];
+          tmem_ld32(taddr + c * 64, v);
+          if constexpr (EPI == EPI_RESID) {
+            if (col0 < P.N && row0w < P.M) {
+              if (!mbar_wait(res_bar(ew, b), (res_phase >> b) & 1u, abort_flag)) { ok = false; break; }
+              res_phase ^= 1u << b;
+              if (lane == 0) res_pending[b] = false;
+            }
+            box_add32(box, lane, 0, v);
+          }
+          box_write32(box, lane, 0, v);
+          tmem_ld32(taddr + c * 64 + 32, v);
+          if constexpr (EPI == EPI_RESID) box_add32(box, lane, 1, v);
+          box_write32(box, lane, 1, v);
+          ship(box, col0, row0w);
         }
       } else if constexpr (EPI == EPI_ROPE) {
         const int tile_col0 = tn * BN;
         if (tile_col0 >= P.rope_cols) {
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
+          for (int c = 0; c < BN / 64; ++c) {
+            uint8_t* box = claim();
             float v[32];
-            tmem_ld32(taddr + c * 32, v);
-            const int col0 = tile_col0 + c * 32;
-            if (row_ok && col0 < P.N) store_row32(P.out + static_cast<size_t>(row) * P.ldo + col0, v, min(32, P.N - col0));
+            tmem_ld32(taddr + c * 64, v);
+            box_write32(box, lane, 0, v);
+            tmem_ld32(taddr + c * 64 + 32, v);
+            box_write32(box, lane, 1, v);
+            ship(box, tile_col0 + c * 64, row0w);
           }
         } else {
           const int hd = P.head_dim, half = hd >> 1;
@@ -387,40 +468,63 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             p = min(max(p, 0), P.rope_len - 1);
           }
           const float2* tab = P.rope + static_cast<size_t>(p) * half;
+          float2 cs[32];
+          if (hd == 64) {
+            load_cs32(tab, cs);  // one table row serves every head of the tile
 #pragma unroll 1
-          for (int h0 = 0; h0 < BN; h0 += hd) {
-#pragma unroll 1
-            for (int j = 0; j < half; j += 32) {
+            for (int h0 = 0; h0 < BN; h0 += 64) {
+              uint8_t* box = claim();
               float x1[32], x2[32];
-              tmem_ld32(taddr + h0 + j, x1);
-              tmem_ld32(taddr + h0 + half + j, x2);
-              if (row_ok) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                  const float2 cs = tab[j + i];
-                  const float a = x1[i], b = x2[i];
-                  x1[i] = a * cs.x - b * cs.y;
-                  x2[i] = b * cs.x + a * cs.y;
-                }
-                const int col = tile_col0 + h0 + j;
-                store_row32(P.out + static_cast<size_t>(row) * P.ldo + col, x1, 32);
-                store_row32(P.out + static_cast<size_t>(row) * P.ldo + col + half, x2, 32);
+              tmem_ld32(taddr + h0, x1);
+              tmem_ld32(taddr + h0 + 32, x2);
+              rotate32(x1, x2, cs);
+              box_write32(box, lane, 0, x1);
+              box_write32(box, lane, 1, x2);
+              ship(box, tile_col0 + h0, row0w);
+            }
+          } else {  // hd == 128: columns [h0, h0+64) and [h0+64, h0+128) go to the two boxes
+#pragma unroll 1
+            for (int h0 = 0; h0 < BN; h0 += 128) {
+              if (lane == 0) bulk_wait_read0();
+              __syncwarp();
+              uint8_t* box_lo = boxes;
+              uint8_t* box_hi = boxes + C::kBoxBytes;
+#pragma unroll 1
+              for (int j = 0; j < 64; j += 32) {
+                float x1[32], x2[32];
+                load_cs32(tab + j, cs);
+                tmem_ld32(taddr + h0 + j, x1);
+                tmem_ld32(taddr + h0 + 64 + j, x2);
+                rotate32(x1, x2, cs);
+                box_write32(box_lo, lane, j >> 5, x1);
+                box_write32(box_hi, lane, j >> 5, x2);
               }
+              fence_async_smem();
+              __syncwarp();
+              if (lane == 0 && row0w < P.M) {
+                tma_store_2d(&tmOut, tile_col0 + h0, row0w, smem_u32(box_lo));
+                tma_store_2d(&tmOut, tile_col0 + h0 + 64, row0w, smem_u32(box_hi));
+                bulk_commit();
+              }
+              both_pending = true;
             }
           }
         }
       } else if constexpr (EPI == EPI_SWIGLU) {
 #pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
-          float g[32], u[32];
-          tmem_ld32(taddr + c * 32, g);
-          tmem_ld32(taddr + BN / 2 + c * 32, u);
-          const int col0 = tn * (BN / 2) + c * 32;
-          if (row_ok && col0 < P.N) {
+        for (int c = 0; c < BN / 128; ++c) {
+          const int col0 = tn * (BN / 2) + c * 64;
+          uint8_t* box = claim();
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            float g[32], u[32];
+            tmem_ld32(taddr + c * 64 + h * 32, g);
+            tmem_ld32(taddr + BN / 2 + c * 64 + h * 32, u);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) g[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
-            store_row32(P.out + static_cast<size_t>(row) * P.ldo + col0, g, min(32, P.N - col0));
+            for (int i = 0; i < 32; ++i) g[i] = __fdividef(g[i], 1.0f + __expf(-g[i])) * u[i];
+            box_write32(box, lane, h, g);
           }
+          ship(box, col0, row0w);
         }
       } else if constexpr (EPI == EPI_CE) {
         const int lab = row_ok ? P.labels[row] : -1;
@@ -438,11 +542,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (i < valid) cmax = fmaxf(cmax, v[i]);
           const float m_new = fmaxf(m_run, cmax);
           if (m_new != -INFINITY) {
-            float s = 0.0f;
+            float sum = 0.0f;
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (i < valid) s += __expf(v[i] - m_new);
-            s_run = s_run * __expf(m_run - m_new) + s;
+              if (i < valid) sum += __expf(v[i] - m_new);
+            s_run = s_run * __expf(m_run - m_new) + sum;
             m_run = m_new;
           }
           const int off = lab - col0;
@@ -460,6 +564,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
+    }
+    if constexpr (EPI != EPI_CE) {
+      if (lane == 0) {
+        bulk_wait_all();  // every TMA store of this warp has completed
+        for (int b = 0; b < 2; ++b)  // an aborted residual load lands before the CTA exits
+          if (res_pending[b]) mbar_wait_drain(res_bar(ew, b), (res_phase >> b) & 1u, 20ull * 1000 * 1000);
+      }
+      __syncwarp();
     }
   }
 
@@ -517,7 +629,7 @@ int num_sms() {
 
 template <int BN, int EPI>
 mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, EPI>;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -534,6 +646,10 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
     const void* ptr = g.B[i < nmaps ? i : 0];
     if (!make_map(&tb[i], ptr, brows, g.K, g.ldb, box_b)) return MTP_ERR_INVALID_ARG;
   }
+  // output / residual boxes: 32 rows x 64 columns, 128-byte swizzle
+  CUtensorMap tout = ta, tres = ta;
+  if (EPI != EPI_CE && !make_map(&tout, g.out, g.M, g.N, g.ldo, 32)) return MTP_ERR_INVALID_ARG;
+  if (EPI == EPI_RESID && !make_map(&tres, g.resid, g.M, g.N, g.ldr, 32)) return MTP_ERR_INVALID_ARG;
   Args a{};
   a.M = g.M;
   a.N = g.N;
@@ -556,7 +672,7 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
   a.z_tgt = g.z_tgt;
   const int ntiles = a.tiles_m * a.tiles_n;
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
-  gemm_tc_kernel<BN, EPI><<<grid, kThreads, C::kSmemBytes, stream>>>(ta, tb[0], tb[1], tb[2], a);
+  gemm_tc_kernel<BN, EPI><<<grid, kThreads, C::kSmemBytes, stream>>>(ta, tb[0], tb[1], tb[2], tout, tres, a);
   mtp::note_launch();
   MTP_LAUNCH_CHECK();
   return MTP_OK;
