@@ -148,6 +148,70 @@ __global__ void prologue_kernel(const T* __restrict__ h_prev, const int32_t* __r
   }
 }
 
+// 8 bf16 <-> 8 floats
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __bfloat1622float2(h[i]);
+    f[2 * i] = v.x;
+    f[2 * i + 1] = v.y;
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint4 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return u;
+}
+__device__ __forceinline__ float sumsq8(const uint4& u) {
+  float f[8];
+  unpack8(u, f);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) s += f[i] * f[i];
+  return s;
+}
+// out = bf16(g * x * r) for one 8-element chunk
+__device__ __forceinline__ uint4 norm8(const uint4& x, const uint4& g, float r) {
+  float fx[8], fg[8];
+  unpack8(x, fx);
+  unpack8(g, fg);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) fx[i] = fg[i] * (fx[i] * r);
+  return pack8(fx);
+}
+
+// bf16 prologue with 16-byte accesses (d % 8 == 0); same arithmetic order as above
+__global__ void prologue_bf16_kernel(const uint4* __restrict__ h_prev, const int32_t* __restrict__ tokens,
+                                     const uint4* __restrict__ embed, const uint4* __restrict__ g_h,
+                                     const uint4* __restrict__ g_e, uint4* __restrict__ c, int M, int Tlen, int d8,
+                                     int V, int k, float eps) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= M) return;
+  const int m = warp;
+  const int t = m % Tlen;
+  const int tok = clamp_token(tokens[m - t + min(t + k, Tlen - 1)], V);
+  const uint4* h = h_prev + static_cast<size_t>(m) * d8;
+  const uint4* e = embed + static_cast<size_t>(tok) * d8;
+  float sh = 0.f, se = 0.f;
+  for (int i = lane; i < d8; i += 32) {
+    sh += sumsq8(h[i]);
+    se += sumsq8(e[i]);
+  }
+  sh = mtp::warp_sum(sh);
+  se = mtp::warp_sum(se);
+  const float d = 8.0f * d8;
+  const float rh = 1.0f / sqrtf(sh / d + eps);
+  const float re = 1.0f / sqrtf(se / d + eps);
+  uint4* out = c + static_cast<size_t>(m) * 2 * d8;
+  for (int i = lane; i < d8; i += 32) {
+    out[i] = norm8(h[i], g_h[i], rh);
+    out[d8 + i] = norm8(e[i], g_e[i], re);
+  }
+}
+
 // y = RMSNorm_g(x) row-wise (one warp per row)
 template <typename T>
 __global__ void rmsnorm_kernel(const T* __restrict__ x, const T* __restrict__ g, T* __restrict__ y, int M, int d,
@@ -166,13 +230,43 @@ __global__ void rmsnorm_kernel(const T* __restrict__ x, const T* __restrict__ g,
   for (int i = lane; i < d; i += 32) yr[i] = from_f32<T>(load_f32(g + i) * (load_f32(xr + i) * r));
 }
 
-// (cos, sin) of position p times base^(-2j/hd), computed in double and rounded once
+// bf16 RMSNorm with 16-byte accesses; when `labels` is given it also writes
+// the label of term k for the row (x_{t+k+1} if t..t+k+1 share t's segment,
+// else -1), which the head GEMM's CE epilogue consumes.
+__global__ void rmsnorm_bf16_kernel(const uint4* __restrict__ x, const uint4* __restrict__ g, uint4* __restrict__ y,
+                                    int M, int d8, float eps, const int32_t* __restrict__ tokens,
+                                    const int32_t* __restrict__ seg, const int32_t* __restrict__ seg_end,
+                                    int32_t* __restrict__ labels, int Tlen, int k, int V) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= M) return;
+  const uint4* xr = x + static_cast<size_t>(warp) * d8;
+  float ss = 0.f;
+  for (int i = lane; i < d8; i += 32) ss += sumsq8(xr[i]);
+  ss = mtp::warp_sum(ss);
+  const float r = 1.0f / sqrtf(ss / (8.0f * d8) + eps);
+  uint4* yr = y + static_cast<size_t>(warp) * d8;
+  for (int i = lane; i < d8; i += 32) yr[i] = norm8(xr[i], g[i], r);
+  if (labels && lane == 0) {
+    const int m = warp, t = m % Tlen;
+    const bool ok = seg[m] != -1 && t + k + 1 < seg_end[m];
+    labels[m] = ok ? clamp_token(tokens[m + k + 1], V) : -1;
+  }
+}
+
+// (cos, sin) of the angle p * base^(-2j/hd).  The angle is formed and
+// reduced modulo 2*pi in double (a handful of FP64 instructions), then the
+// fp32 sine and cosine of the reduced angle are taken.
 __global__ void rope_table_kernel(float2* __restrict__ tab, int T, int half, int hd, double base) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= T * half) return;
   const int p = i / half, j = i % half;
-  const double ang = static_cast<double>(p) * pow(base, -2.0 * j / hd);
-  tab[i] = make_float2(static_cast<float>(cos(ang)), static_cast<float>(sin(ang)));
+  const double inv_freq = exp2(-2.0 * j / hd * log2(base));
+  const double ang = static_cast<double>(p) * inv_freq;
+  const double two_pi = 6.283185307179586;
+  const double red = ang - rint(ang / two_pi) * two_pi;
+  float s, c;
+  sincosf(static_cast<float>(red), &s, &c);
+  tab[i] = make_float2(c, s);
 }
 
 // labels of term k (0 = main): x_{t+k+1} where t..t+k+1 lie in t's segment, else -1
@@ -286,45 +380,44 @@ __global__ void head_ce_f32_kernel(const float* __restrict__ x, const float* __r
 // ---------------------------------------------------------------------------
 // CE reduction and loss assembly
 // ---------------------------------------------------------------------------
-// ℓ_t = max + log Σ_tiles s_j exp(m_j - max) - z_label for supervised rows
+// ℓ_t = max + log Σ_tiles s_j exp(m_j - max) - z_label for supervised rows;
+// one warp per row, one (sum, count) atomic pair per block of 8 rows
 __global__ void ce_reduce_kernel(int M, int nvt, const float2* __restrict__ part, const float* __restrict__ zt,
                                  const int32_t* __restrict__ labels, float* __restrict__ row_loss,
                                  double* __restrict__ sum_count) {
-  __shared__ double s_sum[8];
-  __shared__ int s_cnt[8];
-  const int m = blockIdx.x * blockDim.x + threadIdx.x;
-  double loss = 0.0;
-  int cnt = 0;
-  if (m < M) {
-    float out = NAN;
-    if (labels[m] >= 0) {
-      const float2* p = part + static_cast<size_t>(m) * nvt;
-      float mx = -INFINITY;
-      for (int j = 0; j < nvt; ++j) mx = fmaxf(mx, p[j].x);
-      float s = 0.f;
-      for (int j = 0; j < nvt; ++j) s += p[j].y * expf(p[j].x - mx);
-      out = (mx + logf(s)) - zt[m];
-      loss = out;
-      cnt = 1;
-    }
-    if (row_loss) row_loss[m] = out;
-  }
+  __shared__ float s_loss[8];
+  __shared__ int s_sup[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  loss = mtp::warp_sum(loss);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  const int m = blockIdx.x * 8 + warp;
+  float loss = NAN;
+  const bool supervised = m < M && labels[m] >= 0;
+  if (supervised) {
+    const float2* p = part + static_cast<size_t>(m) * nvt;
+    float mx = -INFINITY;
+    for (int j = lane; j < nvt; j += 32) mx = fmaxf(mx, p[j].x);
+    mx = mtp::warp_max(mx);
+    float sum = 0.f;
+    for (int j = lane; j < nvt; j += 32) {
+      const float2 v = p[j];
+      sum += v.y * expf(v.x - mx);
+    }
+    sum = mtp::warp_sum(sum);
+    loss = (mx + logf(sum)) - zt[m];
+  }
   if (lane == 0) {
-    s_sum[warp] = loss;
-    s_cnt[warp] = cnt;
+    if (m < M && row_loss) row_loss[m] = loss;
+    s_loss[warp] = loss;
+    s_sup[warp] = supervised;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     double a = 0.0;
     int c = 0;
-    for (int w = 0; w < blockDim.x / 32; ++w) {
-      a += s_sum[w];
-      c += s_cnt[w];
-    }
+    for (int w = 0; w < 8; ++w)
+      if (s_sup[w]) {
+        a += s_loss[w];
+        ++c;
+      }
     if (c) {
       atomicAdd(sum_count, a);
       atomicAdd(sum_count + 1, static_cast<double>(c));
@@ -504,6 +597,27 @@ mtp_status gemm<float>(const Ctx& C, const float* A, int lda, const float* const
     if (s_ != MTP_OK) return s_;           \
   } while (0)
 
+// RMSNorm launch; with `labels` it also writes term k's labels (bf16 fuses
+// them into the norm kernel, f32 uses a separate kernel).
+template <typename T>
+void launch_rmsnorm(const Ctx& C, const T* x, const T* g, T* y, int32_t* labels = nullptr, int k = 0) {
+  const mtp_dims& D = C.D;
+  if constexpr (sizeof(T) == 2) {
+    rmsnorm_bf16_kernel<<<warp_blocks(C.M), 256, 0, C.st>>>(
+        reinterpret_cast<const uint4*>(x), reinterpret_cast<const uint4*>(g), reinterpret_cast<uint4*>(y), C.M,
+        D.d / 8, D.eps, C.tokens, C.seg, C.buf<int32_t>(C.L.seg_end), labels, D.T, k, D.V);
+    mtp::note_launch();
+  } else {
+    rmsnorm_kernel<T><<<warp_blocks(C.M), 256, 0, C.st>>>(x, g, y, C.M, D.d, D.eps);
+    mtp::note_launch();
+    if (labels) {
+      labels_kernel<<<(C.M + 255) / 256, 256, 0, C.st>>>(C.tokens, C.seg, C.buf<int32_t>(C.L.seg_end), labels, C.M,
+                                                         D.T, k, D.V);
+      mtp::note_launch();
+    }
+  }
+}
+
 // head + CE for term `k` (0 = main) on hidden state h
 template <typename T>
 mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double* sum_count) {
@@ -512,11 +626,7 @@ mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double
   int32_t* labels = C.buf<int32_t>(C.L.labels);
   float2* part = C.buf<float2>(C.L.ce_part);
   float* zt = C.buf<float>(C.L.zt);
-  rmsnorm_kernel<T><<<warp_blocks(C.M), 256, 0, C.st>>>(h, static_cast<const T*>(C.W.out_norm), x, C.M, D.d, D.eps);
-  mtp::note_launch();
-  labels_kernel<<<(C.M + 255) / 256, 256, 0, C.st>>>(C.tokens, C.seg, C.buf<int32_t>(C.L.seg_end), labels, C.M, D.T,
-                                                     k, D.V);
-  mtp::note_launch();
+  launch_rmsnorm<T>(C, h, static_cast<const T*>(C.W.out_norm), x, labels, k);
   MTP_LAUNCH_CHECK();
   if constexpr (sizeof(T) == 2) {
     mtp::GemmDesc g;
@@ -541,7 +651,7 @@ mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double
                                                              part, zt, C.L.nvt);
     mtp::note_launch();
   }
-  ce_reduce_kernel<<<(C.M + 255) / 256, 256, 0, C.st>>>(C.M, C.L.nvt, part, zt, labels, row_loss_term, sum_count);
+  ce_reduce_kernel<<<(C.M + 7) / 8, 256, 0, C.st>>>(C.M, C.L.nvt, part, zt, labels, row_loss_term, sum_count);
   mtp::note_launch();
   MTP_LAUNCH_CHECK();
   return MTP_OK;
@@ -584,16 +694,22 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
     const int i = k - 1;
     T* h_k = h_out ? h_out + static_cast<size_t>(i) * Md : C.buf<T>((k & 1) ? C.L.h1buf : C.L.h0buf);
     auto wt = [&](const void* const* arr) { return static_cast<const T*>(arr[i]); };
-    prologue_kernel<T><<<warp_blocks(M), 256, 0, C.st>>>(h_prev, C.tokens, static_cast<const T*>(C.W.embed),
-                                                         wt(C.W.hnorm), wt(C.W.enorm), c, M, D.T, d, D.V, k, D.eps);
+    if constexpr (sizeof(T) == 2) {
+      prologue_bf16_kernel<<<warp_blocks(M), 256, 0, C.st>>>(
+          reinterpret_cast<const uint4*>(h_prev), C.tokens, static_cast<const uint4*>(C.W.embed),
+          static_cast<const uint4*>(C.W.hnorm[i]), static_cast<const uint4*>(C.W.enorm[i]),
+          reinterpret_cast<uint4*>(c), M, D.T, d / 8, D.V, k, D.eps);
+    } else {
+      prologue_kernel<T><<<warp_blocks(M), 256, 0, C.st>>>(h_prev, C.tokens, static_cast<const T*>(C.W.embed),
+                                                           wt(C.W.hnorm), wt(C.W.enorm), c, M, D.T, d, D.V, k, D.eps);
+    }
     mtp::note_launch();
     MTP_LAUNCH_CHECK();
     const T* proj[1] = {wt(C.W.eh_proj)};
     mtp::prof_begin(MTP_KC_PROJ_GEMM, C.st);
     TRY(gemm<T>(C, c, 2 * d, proj, 1, d, 2 * d, d, u, d, mtp::EPI_STORE));
     mtp::prof_end(MTP_KC_PROJ_GEMM, C.st);
-    rmsnorm_kernel<T><<<warp_blocks(M), 256, 0, C.st>>>(u, wt(C.W.attn_norm), x, M, d, D.eps);
-    mtp::note_launch();
+    launch_rmsnorm<T>(C, u, wt(C.W.attn_norm), x);
     const T* wqkv[3] = {wt(C.W.wq), wt(C.W.wk), wt(C.W.wv)};
     mtp::prof_begin(MTP_KC_QKV_GEMM, C.st);
     TRY(gemm<T>(C, x, d, wqkv, 3, d, d, 3 * d, qkv, 3 * d, D.rope_base > 0.f ? mtp::EPI_ROPE : mtp::EPI_STORE));
@@ -605,8 +721,7 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
     mtp::prof_begin(MTP_KC_O_GEMM, C.st);
     TRY(gemm<T>(C, o, d, wo, 1, d, d, d, a, d, mtp::EPI_RESID, u, d));
     mtp::prof_end(MTP_KC_O_GEMM, C.st);
-    rmsnorm_kernel<T><<<warp_blocks(M), 256, 0, C.st>>>(a, wt(C.W.ffn_norm), x, M, d, D.eps);
-    mtp::note_launch();
+    launch_rmsnorm<T>(C, a, wt(C.W.ffn_norm), x);
     const T* wg[1] = {wt(C.W.w_gate)};
     mtp::prof_begin(MTP_KC_GATE_UP_GEMM, C.st);
     TRY(gemm<T>(C, x, d, wg, 1, D.ffn, d, D.ffn, g, D.ffn, mtp::EPI_SWIGLU, nullptr, 0, wt(C.W.w_up)));
