@@ -57,6 +57,7 @@ extern "C" unsigned long long mtp_kernel_launches(void) { return mtp::g_launches
 unsigned int mtp_take_errors_chain();
 unsigned int mtp_take_errors_gemm();
 unsigned int mtp_take_errors_attn();
+unsigned int mtp_take_errors_verify();
 
 extern "C" const char* mtp_status_string(int s) {
   switch (s) {
@@ -76,7 +77,8 @@ extern "C" int mtp_abi_version(void) { return MTP_ABI_VERSION; }
 
 extern "C" mtp_status mtp_check_errors(cudaStream_t stream, unsigned int* flags) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MTP_ERR_CUDA;
-  unsigned int v = mtp_take_errors_chain() | mtp_take_errors_gemm() | mtp_take_errors_attn();
+  unsigned int v = mtp_take_errors_chain() | mtp_take_errors_gemm() | mtp_take_errors_attn() |
+                     mtp_take_errors_verify();
   if (flags) *flags = v;
   return v ? MTP_ERR_DEVICE : MTP_OK;
 }

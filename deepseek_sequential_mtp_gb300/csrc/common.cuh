@@ -43,14 +43,12 @@ void prof_end(int kernel_class, cudaStream_t stream);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
+// Bounded waits count SM clock cycles (clock64 is monotonic per SM; the
+// global nanosecond timer can step when it is resynchronised with the host).
+// A legitimate wait lasts microseconds; the limit is ~1.5 s at 2 GHz.
+constexpr long long kWaitLimitCycles = 3000000000ll;
 
-// A pipeline wait gives up after this long; a legitimate wait lasts microseconds.
-constexpr uint64_t kWaitLimitNs = 1500ull * 1000ull * 1000ull;
+__device__ __forceinline__ long long cycles_now() { return clock64(); }
 
 __device__ __forceinline__ float bf16_to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
 __device__ __forceinline__ __nv_bfloat16 f32_to_bf16(float v) { return __float2bfloat16_rn(v); }

@@ -80,12 +80,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait for the phase of `parity` to complete; false on abort or timeout.
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const long long t0 = cycles_now();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (cycles_now() - t0 > kWaitLimitCycles) {
         *abort_flag = 1;
         atomicOr(&g_mtp_error_word, MTP_DEVERR_TIMEOUT);
         return false;
@@ -93,11 +93,11 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
     }
   }
 }
-// Teardown wait that ignores the abort flag (bounded by `limit_ns`).
-__device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  const uint64_t t0 = globaltimer_ns();
+// Teardown wait that ignores the abort flag (bounded by `limit_cycles`).
+__device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, long long limit_cycles) {
+  const long long t0 = cycles_now();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > limit_ns) return false;
+    if (cycles_now() - t0 > limit_cycles) return false;
   }
   return true;
 }
@@ -348,7 +348,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     if (*abort_flag) {  // let every copy this thread started land before the CTA exits
       for (int s = 0; s < S; ++s)
-        if (issued[s]) mbar_wait_drain(full_bar(s), armed[s], 20ull * 1000 * 1000);
+        if (issued[s]) mbar_wait_drain(full_bar(s), armed[s], 40000000ll);
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------ MMA issuer ------------------------------
@@ -569,7 +569,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (lane == 0) {
         bulk_wait_all();  // every TMA store of this warp has completed
         for (int b = 0; b < 2; ++b)  // an aborted residual load lands before the CTA exits
-          if (res_pending[b]) mbar_wait_drain(res_bar(ew, b), (res_phase >> b) & 1u, 20ull * 1000 * 1000);
+          if (res_pending[b]) mbar_wait_drain(res_bar(ew, b), (res_phase >> b) & 1u, 40000000ll);
       }
       __syncwarp();
     }
@@ -579,7 +579,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (warp == 1) {
     if (lane == 0) {  // every MMA this CTA issued has completed before TMEM is freed
       umma_commit(final_bar);
-      mbar_wait_drain(final_bar, 0, 20ull * 1000 * 1000);
+      mbar_wait_drain(final_bar, 0, 40000000ll);
     }
     __syncwarp();
     tc_fence_after();

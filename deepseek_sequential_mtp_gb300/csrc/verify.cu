@@ -6,25 +6,47 @@
 // truncation) generalised to gamma drafts by the left-to-right rule of the
 // speculative-decoding page.  Uniforms: Philox4x32-10 (Salmon et al., SC'11).
 //
-// Layout on the GPU: one CTA of 512 threads per request.
-//   phase A  warp 0: lane j evaluates draft position j (two scalar loads, one
-//            Philox block, one fp64 division); a ballot picks the first
-//            position that ends the round.
-//   phase B  all 16 warps: stream the one row pair (or the bonus row) the
-//            round samples from in 1024-element chunks with coalesced
-//            16-byte loads, forming residuals in fp32 and compensated
-//            (hi, lo) fp32 chunk sums.
-//   phase C  warp 0: fp64 prefix over chunk sums picks the chunk holding
-//            u' * mass, then rescans that one chunk (L2-resident) in index
-//            order to find the smallest index whose running sum exceeds it.
+// Layout on the GPU: a cluster of 2 CTAs per request, one CTA per SM (544
+// threads: 16 consumer warps and one producer warp, 160 KB ring), so the 64
+// requests of a decode batch occupy 128 SMs in one wave.
+//   phase A  warp 0 of every CTA: lane j evaluates draft position j (two
+//            scalar loads, one Philox block, one fp64 division); a ballot
+//            picks the first position that ends the round.  Both CTAs reach
+//            the same decision.
+//   phase B  CTA `rank` owns half of the chunks of the one row pair (or bonus
+//            row) the round samples from.  Its producer warp streams them
+//            with one-dimensional bulk copies into a ring of shared-memory
+//            stages (mbarrier-tracked); consumer warps form residuals in fp32
+//            and compensated (hi, lo) fp32 chunk sums.
+//   phase C  CTA 0 gathers the chunk sums through distributed shared memory,
+//            takes their fp64 prefix to find the chunk holding u' * mass, then
+//            rescans that one chunk in index order (staged in shared memory)
+//            to find the smallest index whose running sum exceeds it.
 // The kernel is HBM-bound: it reads 2*V*4 bytes for a rejection, V*4 for a
 // bonus, plus 8*gamma bytes of scalars.
+// Design note: with 4-CTA clusters and two CTAs per SM, about one launch in
+// 10^4-10^5 saw a ring barrier complete a phase that no copy had been issued
+// for (consumers ran ahead and the parity waits then deadlocked until the
+// bounded wait gave up); the same ring without clusters, and this 2-CTA
+// cluster with one CTA per SM, ran millions of launches without it.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
+
+namespace cg = cooperative_groups;
+
+MTP_DEFINE_ERROR_WORD(mtp_take_errors_verify)
 
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
+constexpr int kThreads = 544;  // 16 consumer warps + 1 producer warp
+constexpr int kCluster = 2;
+constexpr int kConsumerWarps = 16;
+constexpr int kStageChunks = 2;  // chunks per ring stage
+constexpr int kRing = 10;         // ring stages (2 x 4 KB x 2 rows each)
+constexpr int kStageBytes = 2 * kStageChunks * 1024 * 4;
+constexpr int kRingBytes = kRing * kStageBytes;
+
 constexpr int kChunk = 1024;       // elements per chunk
 constexpr int kMaxChunks = 512;    // V <= 524288
 constexpr int kMaxGamma = 31;
@@ -69,23 +91,96 @@ __device__ __forceinline__ void acc_add(float& hi, float& lo, float x) {
   hi = s;
   lo += e;
 }
+// Warp-wide sum of (hi, lo) pairs with TwoSum at every level; every lane
+// ends with the same pair.
+__device__ __forceinline__ void warp_two_sum(float& hi, float& lo) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ohi = __shfl_xor_sync(0xffffffffu, hi, o);
+    const float olo = __shfl_xor_sync(0xffffffffu, lo, o);
+    float sum, err;
+    two_sum(hi, ohi, sum, err);
+    hi = sum;
+    lo = (lo + olo) + err;
+  }
+}
 __device__ __forceinline__ double chunk_value(float2 v) { return (double)v.x + (double)v.y; }
 
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cnt(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// bounded wait; false after the library's wait limit (the caller reports it)
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = mtp::cycles_now();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if (it > 64) __nanosleep(32);
+    if ((it & 31u) == 0 && mtp::cycles_now() - t0 > mtp::kWaitLimitCycles) return false;
+  }
+}
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+// one-dimensional bulk copy global -> shared (16-byte aligned, size % 16 == 0)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 template <bool kVec4>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* __restrict__ q,
                    const int32_t* __restrict__ draft, uint2 key, uint32_t off_lo, uint32_t off_hi,
                    const int32_t* __restrict__ eos, const int32_t* __restrict__ remaining,
                    int32_t* __restrict__ accepted, int32_t* __restrict__ next_token,
                    int32_t* __restrict__ n_emit, int32_t* __restrict__ status) {
-  __shared__ float2 s_chunk[kMaxChunks];  // (hi, lo) pairs
+  extern __shared__ __align__(128) uint8_t ring[];   // kRing stages of p and q chunks
+  __shared__ float2 s_chunk[kMaxChunks / kCluster];  // (hi, lo) of this CTA's chunks c_begin + l
+  __shared__ float2 s_all[kMaxChunks];                 // CTA 0: every chunk of the request
   __shared__ float s_w[kChunk];
-  __shared__ int s_cstar;
-  __shared__ double s_before, s_target;
-  __shared__ int s_jstar, s_event, s_bad;
-  __shared__ double s_u;
+  __shared__ __align__(8) uint64_t s_bars[2 * kRing];
+  __shared__ int s_jstar, s_event, s_bad, s_cstar, s_timeout;
+  __shared__ double s_u, s_before, s_target;
+  const uint32_t s_full_bar = smem_u32(s_bars), s_empty_bar = s_full_bar + 8u * kRing;
+  auto ring_p = [&](int slot) { return smem_u32(ring + slot * kStageBytes); };
+  auto ring_q = [&](int slot) { return smem_u32(ring + slot * kStageBytes + kStageChunks * kChunk * 4); };
 
-  const int r = blockIdx.x;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int r = blockIdx.x / kCluster;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int budget = remaining ? remaining[r] : gamma + 1;
   const int eos_id = eos ? eos[r] : -1;
@@ -120,19 +215,25 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
       s_jstar = jstar;
       s_event = (jstar == gamma) ? EV_CONTINUE : evstar;
       s_bad = 0;
+      s_timeout = 0;
+      for (int i = 0; i < kRing; ++i) {
+        mbar_init(s_full_bar + 8u * i, 1);
+        mbar_init(s_empty_bar + 8u * i, kStageChunks);
+      }
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       const uint4 w = philox4x32_10(make_uint4((uint32_t)jstar, (uint32_t)r, off_lo, off_hi), key);
       s_u = uniform24(w.y);
-      if (budget < 1) {
-        s_event = -1;
-      }
+      if (budget < 1) s_event = -1;
     }
   }
-  __syncthreads();
+  cluster.sync();  // publishes the barrier initialisation at cluster scope before any bulk copy
   const int jstar = s_jstar;
   const int event = s_event;
 
+  // every CTA of the cluster takes the same branch here
   if (event != EV_CONTINUE && event != EV_REJECT) {
-    if (threadIdx.x == 0) {
+    if (rank == 0 && threadIdx.x == 0) {
       int st = MTP_VERIFY_OK, acc = jstar;
       if (event == -1) { st = MTP_VERIFY_INVALID_BUDGET; acc = 0; }
       else if (event == EV_STOP) acc = jstar + 1;
@@ -147,81 +248,146 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
   }
 
   // ---------------- phase B: chunk sums of the sampled weights ----------------
-  // Residual elements are formed in fp32 (one rounding each, at most 2^-24 of
-  // the element).  A chunk's sum is accumulated as an unevaluated pair
-  // (hi, lo) of fp32 values with error-free TwoSum steps, per lane and then
-  // across the warp, so the sum of the fp32 elements is kept to ~2^-45
-  // relative without FP64 instructions (GB300 issues FP64 warp instructions
-  // at a small fraction of the FP32 rate).
+  // CTA `rank` owns the contiguous chunks [c_begin, c_end).  Residual elements
+  // are formed in fp32 (one rounding each, at most 2^-24 of the element); a
+  // chunk's sum is accumulated as an unevaluated pair (hi, lo) of fp32 values
+  // with error-free TwoSum steps, per lane and then across the warp, keeping
+  // the sum of the fp32 elements to ~2^-45 relative without FP64
+  // instructions (GB300 issues FP64 warp instructions at a small fraction of
+  // the FP32 rate).  With 16-byte-aligned rows a producer warp streams the
+  // rows with bulk copies into a ring of shared-memory stages (two chunks of
+  // p and of q per stage) and the eight consumer warps reduce them.
   const bool residual = (event == EV_REJECT);
   const float* prow = p + ((size_t)r * (gamma + 1) + jstar) * V;
   const float* qrow = residual ? q + ((size_t)r * gamma + jstar) * V : prow;
   const int n_chunks = (V + kChunk - 1) / kChunk;
+  const int npc = (n_chunks + kCluster - 1) / kCluster;
+  const int c_begin = min(n_chunks, rank * npc);
+  const int n_local = min(n_chunks, c_begin + npc) - c_begin;
   bool bad = false;
-  for (int c = warp; c < n_chunks; c += kWarps) {
-    const int base = c * kChunk;
-    float hi = 0.0f, lo = 0.0f;
-    if constexpr (kVec4) {
-      float4 pv[8], qv[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = base + 4 * (lane + 32 * i);
-        pv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        qv[i] = pv[i];
-        if (e < V) {
-          pv[i] = __ldcs(reinterpret_cast<const float4*>(prow + e));
-          if (residual) qv[i] = __ldcs(reinterpret_cast<const float4*>(qrow + e));
+  if constexpr (kVec4) {
+    const int n_stages = (n_local + kStageChunks - 1) / kStageChunks;
+    if (warp == kConsumerWarps) {
+      // producer warp: every lane waits, lane 0 issues the copies
+      int issued_last = -1;
+      for (int st = 0; st < n_stages; ++st) {
+        const int slot = st % kRing, use = st / kRing;
+        if (use > 0 && !mbar_wait(s_empty_bar + 8u * slot, (use - 1) & 1)) {
+          if (lane == 0) {
+            atomicOr(&g_mtp_error_word, MTP_DEVERR_TIMEOUT);
+            s_timeout = 1;
+          }
+          break;
         }
+        if (lane == 0) {
+          const int chunk0 = c_begin + st * kStageChunks;
+          const int nch = min(kStageChunks, n_local - st * kStageChunks);
+          const uint32_t bytes = 4u * static_cast<uint32_t>(min(nch * kChunk, V - chunk0 * kChunk));
+          const uint32_t full = s_full_bar + 8u * slot;
+          mbar_expect_tx(full, residual ? 2u * bytes : bytes);
+          const uint32_t me = static_cast<uint32_t>(rank);
+          bulk_load(cluster_addr(ring_p(slot), me), prow + (size_t)chunk0 * kChunk, bytes, cluster_addr(full, me));
+          if (residual) bulk_load(cluster_addr(ring_q(slot), me), qrow + (size_t)chunk0 * kChunk, bytes, cluster_addr(full, me));
+        }
+        issued_last = st;
+        __syncwarp();
       }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        bad |= !(prob_ok(pv[i].x) && prob_ok(pv[i].y) && prob_ok(pv[i].z) && prob_ok(pv[i].w));
-        if (residual)
-          bad |= !(prob_ok(qv[i].x) && prob_ok(qv[i].y) && prob_ok(qv[i].z) && prob_ok(qv[i].w));
-        acc_add(hi, lo, weight_of(pv[i].x, qv[i].x, residual));
-        acc_add(hi, lo, weight_of(pv[i].y, qv[i].y, residual));
-        acc_add(hi, lo, weight_of(pv[i].z, qv[i].z, residual));
-        acc_add(hi, lo, weight_of(pv[i].w, qv[i].w, residual));
+      if (s_timeout && lane == 0) {
+        for (int st = max(0, issued_last - kRing + 1); st <= issued_last; ++st)
+          for (int w = 0; w < 1000000 && !mbar_try_wait(s_full_bar + 8u * (st % kRing), (st / kRing) & 1); ++w) {
+          }
       }
+      __syncwarp();
     } else {
-#pragma unroll 4
-      for (int i = 0; i < kChunk / 32; ++i) {
-        const int e = base + lane + 32 * i;
-        float pv = 0.f, qv = 0.f;
-        if (e < V) {
-          pv = prow[e];
-          if (residual) qv = qrow[e];
+      for (int li = warp; li < n_local && !s_timeout; li += kConsumerWarps) {
+        const int st = li / kStageChunks, i = li % kStageChunks;
+        const int slot = st % kRing, use = st / kRing;
+        if (!mbar_wait(s_full_bar + 8u * slot, use & 1)) {
+          if (lane == 0) {
+            atomicOr(&g_mtp_error_word, MTP_DEVERR_TIMEOUT);
+            s_timeout = 1;
+          }
+          break;
         }
-        bad |= !prob_ok(pv) || (residual && !prob_ok(qv));
-        acc_add(hi, lo, weight_of(pv, qv, residual));
+        const float* sp = reinterpret_cast<const float*>(ring + slot * kStageBytes) + i * kChunk;
+        const float* sq = sp + kStageChunks * kChunk;
+        const int base = (c_begin + li) * kChunk;
+        float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int off = 4 * (lane + 32 * k);
+          if (base + off < V) {
+            const float4 pv = *reinterpret_cast<const float4*>(sp + off);
+            const float4 qv = residual ? *reinterpret_cast<const float4*>(sq + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+            bad |= !(prob_ok(pv.x) && prob_ok(pv.y) && prob_ok(pv.z) && prob_ok(pv.w));
+            if (residual) bad |= !(prob_ok(qv.x) && prob_ok(qv.y) && prob_ok(qv.z) && prob_ok(qv.w));
+            acc_add(hi, lo, weight_of(pv.x, qv.x, residual));
+            acc_add(hi, lo, weight_of(pv.y, qv.y, residual));
+            acc_add(hi, lo, weight_of(pv.z, qv.z, residual));
+            acc_add(hi, lo, weight_of(pv.w, qv.w, residual));
+          }
+        }
+        warp_two_sum(hi, lo);
+        __syncwarp();
+        if (lane == 0) {
+          s_chunk[li] = make_float2(hi, lo);
+          const int nch = min(kStageChunks, n_local - st * kStageChunks);
+          mbar_arrive_cnt(s_empty_bar + 8u * slot, nch == kStageChunks ? 1u : static_cast<uint32_t>(kStageChunks));
+        }
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ohi = __shfl_xor_sync(0xffffffffu, hi, o);
-      const float olo = __shfl_xor_sync(0xffffffffu, lo, o);
-      float sum, err;
-      two_sum(hi, ohi, sum, err);
-      hi = sum;
-      lo = (lo + olo) + err;
+  } else {
+    if (warp < kConsumerWarps) {
+      for (int li = warp; li < n_local; li += kConsumerWarps) {
+        const int base = (c_begin + li) * kChunk;
+        float hi = 0.0f, lo = 0.0f;
+#pragma unroll 4
+        for (int i = 0; i < kChunk / 32; ++i) {
+          const int e = base + lane + 32 * i;
+          float pv = 0.f, qv = 0.f;
+          if (e < V) {
+            pv = prow[e];
+            if (residual) qv = qrow[e];
+          }
+          bad |= !prob_ok(pv) || (residual && !prob_ok(qv));
+          acc_add(hi, lo, weight_of(pv, qv, residual));
+        }
+        warp_two_sum(hi, lo);
+        if (lane == 0) s_chunk[li] = make_float2(hi, lo);
+      }
     }
-    if (lane == 0) s_chunk[c] = make_float2(hi, lo);
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&s_bad, 1);
-  __syncthreads();
+
+  // CTA 0 gathers every CTA's chunk sums and error flags through distributed
+  // shared memory; the second cluster barrier keeps the peers' shared memory
+  // alive until the gather is done.
+  cluster.sync();
+  if (rank == 0) {
+    for (int c = threadIdx.x; c < n_chunks; c += kThreads)
+      s_all[c] = cluster.map_shared_rank(s_chunk, c / npc)[c % npc];
+    if (threadIdx.x > 0 && threadIdx.x < kCluster) {
+      if (*cluster.map_shared_rank(&s_bad, (int)threadIdx.x)) atomicOr(&s_bad, 1);
+      if (*cluster.map_shared_rank(&s_timeout, (int)threadIdx.x)) atomicOr(&s_timeout, 1);
+    }
+  }
+  cluster.sync();
+  if (rank != 0) return;
 
   // ---------------- phase C: locate u' * mass ----------------
   if (warp == 0) {
     int st = MTP_VERIFY_OK;
     int cstar = -1;
     double before = 0.0, target = 0.0;
-    if (s_bad) {
+    if (s_timeout) {
+      st = MTP_VERIFY_DEVICE_TIMEOUT;
+    } else if (s_bad) {
       st = MTP_VERIFY_INVALID_PROBS;
     } else {
       // lane l owns chunks [l*per, (l+1)*per)
       const int per = (n_chunks + 31) / 32;
       double own = 0.0;
-      for (int c = lane * per; c < min(n_chunks, (lane + 1) * per); ++c) own += chunk_value(s_chunk[c]);
+      for (int c = lane * per; c < min(n_chunks, (lane + 1) * per); ++c) own += chunk_value(s_all[c]);
       const double incl = mtp::warp_inclusive_scan(own);
       const double mass = __shfl_sync(0xffffffffu, incl, 31);
       if (!(mass > 0.0)) {
@@ -237,7 +403,7 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
           int last_pos = -1;
           double before_last = run;
           for (int c = lane * per; c < min(n_chunks, (lane + 1) * per); ++c) {
-            const double cv = chunk_value(s_chunk[c]);
+            const double cv = chunk_value(s_all[c]);
             if (cv > 0.0) { last_pos = c; before_last = run; }
             if (over && run + cv > target) { cstar = c; before = run; break; }
             run += cv;
@@ -262,7 +428,7 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
     }
     return;
   }
-  // stage the chosen chunk's weights in shared memory (one element per thread)
+  // stage the chosen chunk's weights in shared memory
   for (int i = threadIdx.x; i < kChunk; i += kThreads) {
     const int e = s_cstar * kChunk + i;
     s_w[i] = e < V ? weight_of(prow[e], residual ? qrow[e] : 0.0f, residual) : 0.0f;
@@ -317,11 +483,20 @@ extern "C" mtp_status spec_verify(int R, int gamma, int V, const float* p, const
   const uint32_t olo = (uint32_t)(offset & 0xFFFFFFFFu), ohi = (uint32_t)(offset >> 32);
   mtp::prof_begin(MTP_KC_SPEC_VERIFY, stream);
   const bool vec = (V % 4 == 0) && mtp::aligned16(p) && (gamma == 0 || mtp::aligned16(q));
+  if (vec) {
+    static bool attr = false;
+    if (!attr) {
+      if (cudaFuncSetAttribute(spec_verify_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes) !=
+          cudaSuccess)
+        return MTP_ERR_CUDA;
+      attr = true;
+    }
+  }
   if (vec)
-    spec_verify_kernel<true><<<R, kThreads, 0, stream>>>(gamma, V, p, q, draft, key, olo, ohi, eos,
+    spec_verify_kernel<true><<<R * kCluster, kThreads, kRingBytes, stream>>>(gamma, V, p, q, draft, key, olo, ohi, eos,
                                                           remaining, accepted, next_token, n_emit, status);
   else
-    spec_verify_kernel<false><<<R, kThreads, 0, stream>>>(gamma, V, p, q, draft, key, olo, ohi, eos,
+    spec_verify_kernel<false><<<R * kCluster, kThreads, 0, stream>>>(gamma, V, p, q, draft, key, olo, ohi, eos,
                                                            remaining, accepted, next_token, n_emit, status);
   mtp::note_launch();
   mtp::prof_end(MTP_KC_SPEC_VERIFY, stream);

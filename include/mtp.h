@@ -62,7 +62,9 @@ enum {
   MTP_VERIFY_INVALID_DRAFT = 1,   /* draft id outside [0,V) or q_j[y_j] <= 0  */
   MTP_VERIFY_ZERO_RESIDUAL = 2,   /* rejection (or bonus row) with no mass     */
   MTP_VERIFY_INVALID_PROBS = 3,   /* NaN/Inf/negative entry in a row it read   */
-  MTP_VERIFY_INVALID_BUDGET = 4   /* remaining < 1                             */
+  MTP_VERIFY_INVALID_BUDGET = 4,  /* remaining < 1                             */
+  MTP_VERIFY_DEVICE_TIMEOUT = 5   /* a bounded wait gave up (also sets the
+                                     device error word's MTP_DEVERR_TIMEOUT)  */
 };
 
 /* Bits of the device error word. */
