@@ -168,8 +168,7 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
                    int32_t* __restrict__ accepted, int32_t* __restrict__ next_token,
                    int32_t* __restrict__ n_emit, int32_t* __restrict__ status) {
   extern __shared__ __align__(128) uint8_t ring[];   // kRing stages of p and q chunks
-  __shared__ float2 s_chunk[kMaxChunks / kCluster];  // (hi, lo) of this CTA's chunks c_begin + l
-  __shared__ float2 s_all[kMaxChunks];                 // CTA 0: every chunk of the request
+  __shared__ float2 s_all[kMaxChunks];  // CTA 0: (hi, lo) sum of every chunk of the request
   __shared__ float s_w[kChunk];
   __shared__ __align__(8) uint64_t s_bars[2 * kRing];
   __shared__ int s_jstar, s_event, s_bad, s_cstar, s_timeout;
@@ -265,6 +264,7 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
   const int c_begin = min(n_chunks, rank * npc);
   const int n_local = min(n_chunks, c_begin + npc) - c_begin;
   bool bad = false;
+  float2* all0 = cluster.map_shared_rank(s_all, 0);  // rank 0's chunk table
   if constexpr (kVec4) {
     const int n_stages = (n_local + kStageChunks - 1) / kStageChunks;
     if (warp == kConsumerWarps) {
@@ -330,7 +330,7 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
         warp_two_sum(hi, lo);
         __syncwarp();
         if (lane == 0) {
-          s_chunk[li] = make_float2(hi, lo);
+          all0[c_begin + li] = make_float2(hi, lo);
           const int nch = min(kStageChunks, n_local - st * kStageChunks);
           mbar_arrive_cnt(s_empty_bar + 8u * slot, nch == kStageChunks ? 1u : static_cast<uint32_t>(kStageChunks));
         }
@@ -353,26 +353,23 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
           acc_add(hi, lo, weight_of(pv, qv, residual));
         }
         warp_two_sum(hi, lo);
-        if (lane == 0) s_chunk[li] = make_float2(hi, lo);
+        if (lane == 0) all0[c_begin + li] = make_float2(hi, lo);
       }
     }
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&s_bad, 1);
 
-  // CTA 0 gathers every CTA's chunk sums and error flags through distributed
-  // shared memory; the second cluster barrier keeps the peers' shared memory
-  // alive until the gather is done.
-  cluster.sync();
-  if (rank == 0) {
-    for (int c = threadIdx.x; c < n_chunks; c += kThreads)
-      s_all[c] = cluster.map_shared_rank(s_chunk, c / npc)[c % npc];
-    if (threadIdx.x > 0 && threadIdx.x < kCluster) {
-      if (*cluster.map_shared_rank(&s_bad, (int)threadIdx.x)) atomicOr(&s_bad, 1);
-      if (*cluster.map_shared_rank(&s_timeout, (int)threadIdx.x)) atomicOr(&s_timeout, 1);
-    }
+  // Every CTA has pushed its chunk sums into CTA 0's table; it now ORs its
+  // error flags into CTA 0's and arrives on the cluster barrier (release).
+  // CTA 0 waits (acquire) and continues alone; the others are done.
+  __syncthreads();
+  if (rank != 0 && threadIdx.x == 0) {
+    if (s_bad) atomicOr(cluster.map_shared_rank(&s_bad, 0), 1);
+    if (s_timeout) atomicOr(cluster.map_shared_rank(&s_timeout, 0), 1);
   }
-  cluster.sync();
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   if (rank != 0) return;
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 
   // ---------------- phase C: locate u' * mass ----------------
   if (warp == 0) {
@@ -435,9 +432,12 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
   }
   __syncthreads();
   if (warp != 0) return;
-  // lane l holds elements [32l, 32l+32) of the chunk, summed in index order
-  double lane_sum = 0.0;
-  for (int i = 0; i < 32; ++i) lane_sum += (double)s_w[32 * lane + i];
+  // lane l holds elements [32l, 32l+32) of the chunk: compensated fp32 lane
+  // sums, an fp64 scan over lanes, then a compensated scan of the chosen
+  // lane's 32 elements spread across the warp.
+  float lhi = 0.0f, llo = 0.0f;
+  for (int i = 0; i < 32; ++i) acc_add(lhi, llo, s_w[32 * lane + i]);
+  const double lane_sum = (double)lhi + (double)llo;
   const double target = s_target;
   const double lincl = mtp::warp_inclusive_scan(lane_sum) + s_before;
   const unsigned lover = __ballot_sync(0xffffffffu, lincl > target);
@@ -449,21 +449,32 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
     return;
   }
   const int lsrc = lover ? __ffs(lover) - 1 : 31 - __clz(lpos);
-  if (lane == lsrc) {
-    double run = lincl - lane_sum;
-    int pick = -1, last_pos = -1;
-    const int base = s_cstar * kChunk + 32 * lane;
-    for (int i = 0; i < 32; ++i) {
-      const float wv = s_w[32 * lane + i];
-      if (wv > 0.0f) last_pos = base + i;
-      run += (double)wv;
-      if (lover && run > target) { pick = base + i; break; }
+  // distance from the start of lane lsrc's elements to the target
+  const double delta = __shfl_sync(0xffffffffu, target - (lincl - lane_sum), lsrc);
+  const float wv = s_w[32 * lsrc + lane];
+  float phi = wv, plo = 0.0f;  // inclusive compensated scan of the 32 elements
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float nhi = __shfl_up_sync(0xffffffffu, phi, o);
+    const float nlo = __shfl_up_sync(0xffffffffu, plo, o);
+    if (lane >= o) {
+      float sum, err;
+      two_sum(phi, nhi, sum, err);
+      phi = sum;
+      plo = (plo + nlo) + err;
     }
-    if (pick < 0) pick = last_pos;
+  }
+  const unsigned eover = __ballot_sync(0xffffffffu, lover && ((double)phi + (double)plo) > delta);
+  const unsigned epos = __ballot_sync(0xffffffffu, wv > 0.0f);
+  if (lane == 0) {
+    const int base = s_cstar * kChunk + 32 * lsrc;
+    int pick = -1;
+    if (eover) pick = base + __ffs(eover) - 1;
+    else if (epos) pick = base + 31 - __clz(epos);
     accepted[r] = jstar;
     next_token[r] = pick;
-    n_emit[r] = jstar + 1;
-    status[r] = MTP_VERIFY_OK;
+    n_emit[r] = pick >= 0 ? jstar + 1 : jstar;
+    status[r] = pick >= 0 ? MTP_VERIFY_OK : MTP_VERIFY_ZERO_RESIDUAL;
   }
 }
 
