@@ -255,7 +255,7 @@ def run_ours(args):
     import torch
 
     from deepseek_sequential_mtp_gb300 import build as mtp_build
-    from deepseek_sequential_mtp_gb300 import lib, synth
+    from deepseek_sequential_mtp_gb300 import dp, lib, synth
 
     rank, local_rank, world = dist_env()
     if world > 1:
@@ -286,9 +286,9 @@ def run_ours(args):
     def step(i):
         chain.loss(x["tokens"], x["seg"], x["pos"], x["h0"], den="fixed", with_main=True, out=out)
         if world > 1:
-            torch.distributed.all_reduce(out["sums_counts"])
-            lib.loss_assemble(out["sums_counts"], cfg.D, world * cfg.B * cfg.T, cfg.lam, "fixed", True,
-                              losses=global_losses)
+            dp.allreduce_sums_counts(out["sums_counts"])
+            lib.loss_assemble(out["sums_counts"], cfg.D, dp.global_positions(cfg.B, cfg.T), cfg.lam, "fixed",
+                              True, losses=global_losses)
         vo = vouts[i]
         lib.spec_verify(vin["p"], vin["q"], vin["draft"], seed=7 + rank, offset=i,
                         out={"accepted": vo[0], "next_token": vo[1], "n_emit": vo[2], "status": vo[3]})
