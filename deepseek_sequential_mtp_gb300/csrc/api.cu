@@ -58,6 +58,7 @@ unsigned int mtp_take_errors_chain();
 unsigned int mtp_take_errors_gemm();
 unsigned int mtp_take_errors_attn();
 unsigned int mtp_take_errors_verify();
+unsigned int mtp_take_errors_draft();
 
 extern "C" const char* mtp_status_string(int s) {
   switch (s) {
@@ -78,7 +79,7 @@ extern "C" int mtp_abi_version(void) { return MTP_ABI_VERSION; }
 extern "C" mtp_status mtp_check_errors(cudaStream_t stream, unsigned int* flags) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MTP_ERR_CUDA;
   unsigned int v = mtp_take_errors_chain() | mtp_take_errors_gemm() | mtp_take_errors_attn() |
-                     mtp_take_errors_verify();
+                     mtp_take_errors_verify() | mtp_take_errors_draft();
   if (flags) *flags = v;
   return v ? MTP_ERR_DEVICE : MTP_OK;
 }

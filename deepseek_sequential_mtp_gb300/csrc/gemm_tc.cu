@@ -41,14 +41,14 @@ constexpr int kGroupM = 16;
 
 template <int BN, int EPI>
 struct Cfg {
-  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 10);
   static constexpr int kABytes = BM * BK * 2;
   static constexpr int kBBytes = BN * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
   // per epilogue warp: two 32 x 64 bf16 boxes (4 KB each); none for the CE epilogue
   static constexpr int kBoxBytes = 32 * 64 * 2;
-  static constexpr int kStagingBytes = EPI == EPI_CE ? 0 : 4 * 2 * kBoxBytes;
+  static constexpr int kStagingBytes = (EPI == EPI_CE || EPI >= EPI_T_STORE) ? 0 : 4 * 2 * kBoxBytes;
   static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024 + 256;
 };
 
@@ -195,6 +195,8 @@ struct Args {
   const int32_t* labels;
   float2* ce_part;
   float* z_tgt;
+  float* out_f32;
+  int splits;
 };
 
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
@@ -304,8 +306,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int ntiles = P.tiles_m * P.tiles_n;
+  // work units: (tile, K split); split s covers k-blocks [kb_lo(s), kb_lo(s+1))
+  const int ntiles = P.tiles_m * P.tiles_n * P.splits;
   const int nk = P.nk;
+  auto kb_lo = [&](int sp) { return static_cast<int>((static_cast<long long>(nk) * sp) / P.splits); };
 
   if (warp == 0 && lane == 0) {
     // ------------------------------ producer ------------------------------
@@ -316,7 +320,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
     for (int s = 0; s < S; ++s) { issued[s] = false; armed[s] = 0; }
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+    for (int u = blockIdx.x; ok && u < ntiles; u += gridDim.x) {
+      const int t = u / P.splits, sp = u % P.splits;
       int tm, tn;
       tile_coords(t, P.tiles_m, P.tiles_n, tm, tn);
       const CUtensorMap* bmap = &tmB0;
@@ -329,7 +334,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         by = n0 - seg * P.seg_rows;
         bmap = seg == 0 ? &tmB0 : (seg == 1 ? &tmB1 : &tmB2);
       }
-      for (int kb = 0; kb < nk; ++kb) {
+      for (int kb = kb_lo(sp); kb < kb_lo(sp + 1); ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
         const uint32_t sa = base + stage * C::kStageBytes;
         const uint32_t sb = sa + C::kABytes;
@@ -356,13 +361,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint32_t phase = 0;
     int local = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++local) {
+    for (int u = blockIdx.x; ok && u < ntiles; u += gridDim.x, ++local) {
+      const int sp = u % P.splits;
+      const int kb0 = kb_lo(sp);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
-      for (int kb = 0; kb < nk; ++kb) {
+      for (int kb = kb0; kb < kb_lo(sp + 1); ++kb) {
         if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sa = base + stage * C::kStageBytes;
@@ -370,7 +377,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const uint64_t bdesc = sdesc_sw128(sa + C::kABytes);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (kb | kk) != 0);
+          umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (kb != kb0 || kk != 0) ? 1u : 0u);
         umma_commit(empty_bar(stage));
         if (++stage == S) { stage = 0; phase ^= 1u; }
       }
@@ -406,7 +413,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       nb ^= 1;
     };
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++local) {
+    for (int u = blockIdx.x; ok && u < ntiles; u += gridDim.x, ++local) {
+      const int t = u / P.splits;
       int tm, tn;
       tile_coords(t, P.tiles_m, P.tiles_n, tm, tn);
       const int acc = local & 1;
@@ -525,6 +533,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             box_write32(box, lane, h, g);
           }
           ship(box, col0, row0w);
+        }
+      } else if constexpr (EPI == EPI_T_STORE || EPI == EPI_T_ATOMIC) {
+        // row = feature; TMEM columns = tokens; for a fixed token the warp's
+        // 32 lanes write 32 consecutive features (128 bytes)
+        float v[32];
+        tmem_ld32(taddr, v);
+        if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j < P.N) {
+              float* dst = P.out_f32 + static_cast<size_t>(j) * P.ldo + row;
+              if constexpr (EPI == EPI_T_ATOMIC) atomicAdd(dst, v[j]);
+              else *dst = v[j];
+            }
+          }
         }
       } else if constexpr (EPI == EPI_CE) {
         const int lab = row_ok ? P.labels[row] : -1;
@@ -648,7 +671,7 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
   }
   // output / residual boxes: 32 rows x 64 columns, 128-byte swizzle
   CUtensorMap tout = ta, tres = ta;
-  if (EPI != EPI_CE && !make_map(&tout, g.out, g.M, g.N, g.ldo, 32)) return MTP_ERR_INVALID_ARG;
+  if (EPI != EPI_CE && EPI < EPI_T_STORE && !make_map(&tout, g.out, g.M, g.N, g.ldo, 32)) return MTP_ERR_INVALID_ARG;
   if (EPI == EPI_RESID && !make_map(&tres, g.resid, g.M, g.N, g.ldr, 32)) return MTP_ERR_INVALID_ARG;
   Args a{};
   a.M = g.M;
@@ -670,7 +693,9 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
   a.labels = g.labels;
   a.ce_part = g.ce_part;
   a.z_tgt = g.z_tgt;
-  const int ntiles = a.tiles_m * a.tiles_n;
+  a.out_f32 = g.out_f32;
+  a.splits = g.splits > 0 ? g.splits : 1;
+  const int ntiles = a.tiles_m * a.tiles_n * a.splits;
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
   gemm_tc_kernel<BN, EPI><<<grid, kThreads, C::kSmemBytes, stream>>>(ta, tb[0], tb[1], tb[2], tout, tres, a);
   mtp::note_launch();
@@ -689,7 +714,7 @@ mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream) {
   if (!aligned16(g.A)) return MTP_ERR_ALIGNMENT;
   for (int i = 0; i < 3; ++i)
     if (g.B[i] && !aligned16(g.B[i])) return MTP_ERR_ALIGNMENT;
-  if (g.epi != EPI_CE && (!g.out || g.ldo % 8 || !aligned16(g.out))) return MTP_ERR_ALIGNMENT;
+  if (g.epi != EPI_CE && g.epi < EPI_T_STORE && (!g.out || g.ldo % 8 || !aligned16(g.out))) return MTP_ERR_ALIGNMENT;
   if (!encoder()) return MTP_ERR_CUDA;
   switch (g.epi) {
     case EPI_STORE:
@@ -714,6 +739,13 @@ mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream) {
     case EPI_CE:
       if (!g.labels || !g.ce_part || !g.z_tgt) return MTP_ERR_INVALID_ARG;
       return launch<256, EPI_CE>(g, stream);
+    case EPI_T_STORE:
+    case EPI_T_ATOMIC: {
+      if (g.N > 32 || !g.out_f32 || g.nseg != 1) return MTP_ERR_UNSUPPORTED;
+      const int nk = (g.K + BK - 1) / BK;
+      if (g.splits < 1 || g.splits > nk || (g.epi == EPI_T_STORE && g.splits != 1)) return MTP_ERR_INVALID_ARG;
+      return g.epi == EPI_T_STORE ? launch<32, EPI_T_STORE>(g, stream) : launch<32, EPI_T_ATOMIC>(g, stream);
+    }
     default:
       return MTP_ERR_INVALID_ARG;
   }

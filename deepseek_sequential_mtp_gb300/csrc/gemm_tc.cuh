@@ -10,7 +10,12 @@ enum GemmEpilogue : int {
   EPI_RESID = 1,   // out = resid + acc
   EPI_ROPE = 2,    // out = RoPE(acc) on columns < rope_cols, acc elsewhere
   EPI_SWIGLU = 3,  // out[:, j] = silu(gate_j) * up_j; B = (gate, up) stacked per tile
-  EPI_CE = 4       // no output: per (row, vocab tile) online max / sum-exp and the label logit
+  EPI_CE = 4,      // no output: per (row, vocab tile) online max / sum-exp and the label logit
+  // swap-AB (decode-shaped) variants: A = weights [features, K] on the
+  // 128-row side, B = activations [tokens <= 32, K]; the accumulator tile is
+  // [128 features, 32 tokens] and is written transposed, out[token, feature]
+  EPI_T_STORE = 5,  // out_f32[token * ldo + feature] = acc (no split-K)
+  EPI_T_ATOMIC = 6  // out_f32[token * ldo + feature] += acc (split-K partials; out zeroed first)
 };
 
 // C-side description of one GEMM  acc[M, N] = A[M, K] · B[N, K]^T  (bf16 in,
@@ -38,6 +43,9 @@ struct GemmDesc {
   const int32_t* labels = nullptr;
   float2* ce_part = nullptr;
   float* z_tgt = nullptr;
+  // swap-AB variants: fp32 output and the number of K splits
+  float* out_f32 = nullptr;
+  int splits = 1;
 };
 
 // Tile width along N the launcher will use for this descriptor (CE partial

@@ -77,6 +77,11 @@ def load() -> ctypes.CDLL:
     lib.mtp_loss_assemble.argtypes = [i32, vp, ctypes.c_double, ctypes.c_float, i32, i32, vp, vp]
     lib.mtp_profile_kernel.restype = i32
     lib.mtp_profile_kernel.argtypes = [i32, vp, i32, ctypes.POINTER(ctypes.c_int)]
+    lib.mtp_draft_workspace_bytes.restype = sz
+    lib.mtp_draft_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
+    lib.mtp_draft_step.restype = i32
+    lib.mtp_draft_step.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Weights), vp, vp, vp, vp, vp, vp,
+                                   u64, u64, vp, vp, vp, vp, sz, vp]
     lib.mtp_kernel_launches.restype = ctypes.c_ulonglong
     lib.mtp_kernel_launches.argtypes = []
     _lib = lib
@@ -299,3 +304,44 @@ class KernelTimer:
 
 def kernel_launches() -> int:
     return int(load().mtp_kernel_launches())
+
+
+# --------------------------------------------------------------------------
+# Draft step (decode-shaped MTP proposal)
+# --------------------------------------------------------------------------
+class DraftStep:
+    """Reusable call state of mtp_draft_step for one shape (see synth.DraftConfig)."""
+
+    def __init__(self, cfg, weights: dict, device="cuda"):
+        self.cfg = cfg
+        self.dims = Dims(cfg.R, cfg.ctx, cfg.d, cfg.n_heads, cfg.head_dim, cfg.ffn, cfg.V, 1, cfg.eps,
+                         cfg.rope_base, MTP_BF16)
+        self.weights = weights
+        self.w = ChainWeights(weights, 1)
+        nbytes = int(load().mtp_draft_workspace_bytes(ctypes.byref(self.dims)))
+        if nbytes == 0:
+            raise MtpError("invalid draft-step dimensions")
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def __call__(self, parent_hidden, frontier, pos, kv_k, kv_v, ctx_len, seed, offset,
+                 out=None, h_out=None, stream=None):
+        cfg = self.cfg
+        _need(parent_hidden, "parent_hidden", torch.bfloat16)
+        for name, t in (("kv_k", kv_k), ("kv_v", kv_v)):
+            _need(t, name, torch.bfloat16)
+            if tuple(t.shape) != (cfg.R, cfg.ctx, cfg.d):
+                raise MtpError(f"{name} must be [R, ctx, d]")
+        for name, t in (("frontier", frontier), ("pos", pos), ("ctx_len", ctx_len)):
+            _need(t, name, torch.int32)
+        dev = parent_hidden.device
+        if out is None:
+            out = {"q": torch.empty((cfg.R, cfg.V), dtype=torch.float32, device=dev),
+                   "y": torch.empty(cfg.R, dtype=torch.int32, device=dev)}
+        st = load().mtp_draft_step(ctypes.byref(self.dims), ctypes.byref(self.w.struct), _ptr(parent_hidden),
+                                   _ptr(frontier), _ptr(pos), _ptr(kv_k), _ptr(kv_v), _ptr(ctx_len),
+                                   int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(out["q"]),
+                                   _ptr(out["y"]), _ptr(h_out), _ptr(self.ws), self.ws.numel(), _stream(stream))
+        _check(st, "mtp_draft_step")
+        if h_out is not None:
+            out["h"] = h_out
+        return out

@@ -213,6 +213,34 @@ mtp_status spec_verify(int R, int gamma, int V, const float* p, const float* q,
                        int32_t* accepted, int32_t* next_token, int32_t* n_emit,
                        int32_t* status, cudaStream_t stream);
 
+/* Bytes of device workspace mtp_draft_step needs (0 if the sizes are invalid). */
+size_t mtp_draft_workspace_bytes(const mtp_dims* dims);
+
+/* Decode-shaped MTP draft step: one proposal per request ([M7.6] §0x09: a
+ * carried-frontier round proposes y from the saved parent hidden state and
+ * E(f) and keeps q for verification; §0x09A: the MTP block attends over its
+ * own K/V cache).  For request r:
+ *   c = [RMSNorm_h(parent_hidden_r); RMSNorm_e(E[frontier_r])], u = M c,
+ *   a = u + Attn(RMSNorm_a u) over cached rows [0, ctx_len_r) and the new row
+ *   (RoPE at pos_r for its q and k; cached keys are used as stored),
+ *   h = a + SwiGLU(RMSNorm_f a), q_r = softmax(W_U RMSNorm_out(h)),
+ *   y_r = smallest v with Σ_{i<=v} q_r[i] > u Σ q_r, u = (word 2 >> 8) * 2^-24
+ *   of Philox4x32-10 with key (seed lo, hi) and counter (0, r, offset lo, hi).
+ * dims: B = R requests (<= 32), T = cache capacity, D = 1, dtype MTP_BF16,
+ * d % 64 == 0, head_dim in {64, 128}, ffn % 8 == 0; weights as for the chain
+ * (depth arrays of length 1).
+ *   parent_hidden [R, d]; frontier [R] int32; pos [R] int32 in [0, T];
+ *   kv_k, kv_v [R, T, d] bf16 cached keys/values; ctx_len [R] int32 in [0, T].
+ *   q_out [R, V] float receives q; y_out [R] int32 the draws; h_out [R, d]
+ *   nullable receives the pre-final-norm state of the new row.
+ * Streams the block's weights, the head and the cache once: it is
+ * HBM-bandwidth bound. */
+mtp_status mtp_draft_step(const mtp_dims* dims, const mtp_weights* w, const void* parent_hidden,
+                          const int32_t* frontier, const int32_t* pos, const void* kv_k,
+                          const void* kv_v, const int32_t* ctx_len, uint64_t seed, uint64_t offset,
+                          float* q_out, int32_t* y_out, void* h_out, void* ws, size_t ws_bytes,
+                          cudaStream_t stream);
+
 /* Diagnostic GEMM on the same tcgen05 core the chain uses:
  * C[M,N] (bf16) = A[M,K] (bf16) · B[N,K]^T (bf16), fp32 accumulation.
  * K % 8 == 0; A, B, C 16-byte aligned. */

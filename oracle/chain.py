@@ -106,32 +106,47 @@ def segment_causal_attention(q, k, v, segments, bases, n_heads, head_dim):
     return out
 
 
-def transformer_block(u, W, k, positions, segments, bases, dims: Dims, rnd):
-    """Pre-norm block of depth k (M7.6 §0x03C):
-    a = u + Attention(Norm_a(u)); h = a + FFN(Norm_f(a))."""
+def block_qkv(u, W, k, positions, dims: Dims, rnd):
+    """Attention inputs of the block: x = Norm_a(u); q, k after RoPE, v."""
     x = rnd(rmsnorm(u, W["attn_norm"][k], dims.eps))
-    q = x @ _f64(W["wq"][k]).T
-    kk = x @ _f64(W["wk"][k]).T
-    v = x @ _f64(W["wv"][k]).T
-    q = rnd(rope(q, positions, dims.n_heads, dims.head_dim, dims.rope_base))
-    kk = rnd(rope(kk, positions, dims.n_heads, dims.head_dim, dims.rope_base))
-    v = rnd(v)
-    o = rnd(segment_causal_attention(q, kk, v, segments, bases, dims.n_heads, dims.head_dim))
-    a = rnd(u + o @ _f64(W["wo"][k]).T)
+    q = rnd(rope(x @ _f64(W["wq"][k]).T, positions, dims.n_heads, dims.head_dim, dims.rope_base))
+    kk = rnd(rope(x @ _f64(W["wk"][k]).T, positions, dims.n_heads, dims.head_dim, dims.rope_base))
+    v = rnd(x @ _f64(W["wv"][k]).T)
+    return q, kk, v
+
+
+def block_tail(u, o, W, k, dims: Dims, rnd):
+    """a = u + o W_o^T; h = a + SwiGLU(Norm_f(a)) (M7.6 §0x03C)."""
+    a = rnd(u + _f64(o) @ _f64(W["wo"][k]).T)
     y = rnd(rmsnorm(a, W["ffn_norm"][k], dims.eps))
     g = rnd(silu(y @ _f64(W["w_gate"][k]).T) * (y @ _f64(W["w_up"][k]).T))
     return rnd(a + g @ _f64(W["w_down"][k]).T)
 
 
-def mtp_module(prev_hidden, shifted_tokens, W, k, positions, segments, bases, dims, rnd):
-    """One MTP module (M7.6 §0x03): normalise both paths, concatenate in
-    hidden-then-embedding order, project 2d -> d, run the block."""
+def transformer_block(u, W, k, positions, segments, bases, dims: Dims, rnd, return_kv=False):
+    """Pre-norm block of depth k (M7.6 §0x03C):
+    a = u + Attention(Norm_a(u)); h = a + FFN(Norm_f(a)).  With
+    ``return_kv`` the rotated keys and the values are returned as well."""
+    q, kk, v = block_qkv(u, W, k, positions, dims, rnd)
+    o = rnd(segment_causal_attention(q, kk, v, segments, bases, dims.n_heads, dims.head_dim))
+    h = block_tail(u, o, W, k, dims, rnd)
+    return (h, kk, v) if return_kv else h
+
+
+def fusion(prev_hidden, shifted_tokens, W, k, dims, rnd):
+    """u = M_k [RMSNorm_h(h^{k-1}); RMSNorm_e(E(x))] (M7.6 §0x03)."""
     e = _f64(W["embed"][np.asarray(shifted_tokens)])
     h_bar = rmsnorm(prev_hidden, W["hnorm"][k], dims.eps)
     e_bar = rmsnorm(e, W["enorm"][k], dims.eps)
     c = rnd(np.concatenate([h_bar, e_bar], axis=1))
-    u = rnd(c @ _f64(W["eh_proj"][k]).T)
-    return transformer_block(u, W, k, positions, segments, bases, dims, rnd)
+    return rnd(c @ _f64(W["eh_proj"][k]).T)
+
+
+def mtp_module(prev_hidden, shifted_tokens, W, k, positions, segments, bases, dims, rnd, return_kv=False):
+    """One MTP module (M7.6 §0x03): normalise both paths, concatenate in
+    hidden-then-embedding order, project 2d -> d, run the block."""
+    u = fusion(prev_hidden, shifted_tokens, W, k, dims, rnd)
+    return transformer_block(u, W, k, positions, segments, bases, dims, rnd, return_kv=return_kv)
 
 
 def row_cross_entropy(h, labels, W, dims, rnd, vocab_chunk=16384):
