@@ -7,7 +7,7 @@
 // speculative-decoding page.  Uniforms: Philox4x32-10 (Salmon et al., SC'11).
 //
 // Layout on the GPU: a cluster of 2 CTAs per request, one CTA per SM (544
-// threads: 16 consumer warps and one producer warp, 160 KB ring), so the 64
+// threads: 16 consumer warps and one producer warp, 128 KB ring), so the 64
 // requests of a decode batch occupy 128 SMs in one wave.
 //   phase A  warp 0 of every CTA: lane j evaluates draft position j (two
 //            scalar loads, one Philox block, one fp64 division); a ballot
@@ -24,11 +24,13 @@
 //            to find the smallest index whose running sum exceeds it.
 // The kernel is HBM-bound: it reads 2*V*4 bytes for a rejection, V*4 for a
 // bonus, plus 8*gamma bytes of scalars.
-// Design note: with 4-CTA clusters and two CTAs per SM, about one launch in
-// 10^4-10^5 saw a ring barrier complete a phase that no copy had been issued
-// for (consumers ran ahead and the parity waits then deadlocked until the
-// bounded wait gave up); the same ring without clusters, and this 2-CTA
-// cluster with one CTA per SM, ran millions of launches without it.
+// Ring invariant: a parity wait cannot tell phase u+1 from phase u-1, so no
+// waiter may reach a barrier more than one phase ahead of its last completed
+// phase.  Consumer warp w takes chunks w, w+16, ..., i.e. stages w/2 + 8m;
+// with a ring of 8 stages it always lands on slot w/2 and sees that slot's
+// phases one after another (it waited on use u-1 itself before waiting on
+// use u).  The producer issues use u of a slot only after both consumers of
+// use u-1 released it, and waits for every copy it issued before it leaves.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -43,13 +45,15 @@ constexpr int kThreads = 544;  // 16 consumer warps + 1 producer warp
 constexpr int kCluster = 2;
 constexpr int kConsumerWarps = 16;
 constexpr int kStageChunks = 2;  // chunks per ring stage
-constexpr int kRing = 10;         // ring stages (2 x 4 KB x 2 rows each)
+constexpr int kRing = 8;          // ring stages (2 x 4 KB x 2 rows each)
 constexpr int kStageBytes = 2 * kStageChunks * 1024 * 4;
 constexpr int kRingBytes = kRing * kStageBytes;
 
 constexpr int kChunk = 1024;       // elements per chunk
 constexpr int kMaxChunks = 512;    // V <= 524288
 constexpr int kMaxGamma = 31;
+// each consumer warp must revisit the same ring slot (see the ring invariant)
+static_assert(kRing % (kConsumerWarps / kStageChunks) == 0, "ring length must be a multiple of the warp stage stride");
 
 enum Event { EV_CONTINUE = 0, EV_STOP = 1, EV_REJECT = 2, EV_INVALID_DRAFT = 3, EV_INVALID_PROBS = 4 };
 
@@ -117,16 +121,6 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 }
 __device__ __forceinline__ void mbar_arrive_cnt(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
 }
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -292,9 +286,13 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
         issued_last = st;
         __syncwarp();
       }
-      if (s_timeout && lane == 0) {
+      // no copy may still be landing in this CTA's shared memory when it leaves:
+      // wait (bounded) for the last use of every slot that was issued
+      if (lane == 0) {
         for (int st = max(0, issued_last - kRing + 1); st <= issued_last; ++st)
-          for (int w = 0; w < 1000000 && !mbar_try_wait(s_full_bar + 8u * (st % kRing), (st / kRing) & 1); ++w) {
+          if (!mbar_wait(s_full_bar + 8u * (st % kRing), (st / kRing) & 1)) {
+            atomicOr(&g_mtp_error_word, MTP_DEVERR_TIMEOUT);
+            s_timeout = 1;
           }
       }
       __syncwarp();

@@ -71,7 +71,13 @@ enum {
 enum {
   MTP_DEVERR_TOKEN_RANGE = 1u,  /* a token id outside [0, V) was read (clamped) */
   MTP_DEVERR_TIMEOUT = 2u,      /* a bounded pipeline wait gave up             */
-  MTP_DEVERR_SEGMENTS = 4u      /* a segment id re-appears after another one   */
+  MTP_DEVERR_SEGMENTS = 4u,     /* a segment id re-appears after another one   */
+  /* set beside the condition bits above: which kernel family raised them */
+  MTP_DEVERR_FROM_CHAIN = 1u << 8,   /* prologue, norms, segment scan, CE reduce */
+  MTP_DEVERR_FROM_GEMM = 1u << 9,    /* tcgen05 GEMM core                        */
+  MTP_DEVERR_FROM_ATTN = 1u << 10,   /* chain attention                           */
+  MTP_DEVERR_FROM_VERIFY = 1u << 11, /* spec_verify                               */
+  MTP_DEVERR_FROM_DRAFT = 1u << 12   /* draft-step kernels                        */
 };
 
 /* Problem sizes of one chain call.

@@ -122,3 +122,26 @@ def test_worked_example_correction_is_index_zero():
     # acceptance rates p[y]/q[y] = 0.75 (y=1) and 0.5 (y=2)
     yy = y[:, 0].numpy()
     assert abs(acc[yy == 1].mean() - 0.75) < 0.04 and abs(acc[yy == 2].mean() - 0.5) < 0.04
+
+
+def test_ring_with_cold_cache_is_deterministic():
+    """The shared-memory ring under out-of-order copy completion: with L2
+    flushed before every call (slow, reordered bulk copies) the outputs must
+    equal those of back-to-back calls and no bounded wait may run out."""
+    dev = "cuda"
+    case = synth.make_verify_inputs(synth.VERIFY_C4, seed=3, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    n = 600
+    res = {}
+    for mode in ("flushed", "warm"):
+        out = torch.empty((n, 4, synth.VERIFY_C4.R), dtype=torch.int32, device=dev)
+        for i in range(n):
+            if mode == "flushed":
+                flush.zero_()
+            o = out[i]
+            lib.spec_verify(case["p"], case["q"], case["draft"], seed=11, offset=i,
+                            out={"accepted": o[0], "next_token": o[1], "n_emit": o[2], "status": o[3]})
+        assert lib.check_errors() == 0
+        res[mode] = out.cpu()
+    assert torch.equal(res["flushed"], res["warm"])
+    assert int((res["warm"][:, 3] != 0).sum()) == 0
