@@ -55,6 +55,7 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--draft-steps", type=int, default=30)
     return ap.parse_args()
 
 
@@ -395,6 +396,9 @@ def run_ours(args):
               "algorithmic_bytes_per_call": float(vbytes.mean()), "achieved_gbs": v_gbs, "peak_gbs": hbm_peak,
               "frac": v_gbs / hbm_peak, "mean_accepted": float(acc.mean()), "status_nonzero": int((st != 0).sum())}
 
+    # decode-shaped draft step (its own workload, measured beside the step)
+    draft = measure_draft(args, dev, rank, peaks)
+
     # end to end through the public API: pinned host inputs -> device, result -> host, every step
     e2e = measure_e2e(cfg, vcfg, chain, batch, x, vin, args.e2e_steps, dev, rank, world, tokens_per_step)
 
@@ -407,7 +411,7 @@ def run_ours(args):
                 "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic (seeded; random-init weights of the workload's shapes)",
                 "config": workload_config(), "roofline": roofline, "spec_verify": verify,
-                "spec_verify_rows_per_s": verify["rows_per_s"], "kernels": breakdown,
+                "spec_verify_rows_per_s": verify["rows_per_s"], "kernels": breakdown, "draft_step": draft,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
                 "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
                 "clock_samples": clk["samples"], "wall_s_timed_region": t_wall,
@@ -415,6 +419,67 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def measure_draft(args, dev, rank, peaks):
+    """mtp_draft_step on the self-speculative decode workload (32 requests,
+    module cache 8192 x d=7168, 56x128 heads, ffn 18432, V=129280) followed by
+    gamma=1 verification of its draws; L2 flushed before every timed call.
+    Algorithmic bytes: block weights + head + the 32 caches (K and V) + q."""
+    import torch
+
+    from deepseek_sequential_mtp_gb300 import lib, synth
+
+    if args.draft_steps <= 0:
+        return None
+    cfg = synth.DRAFT_C5
+    inp = synth.make_draft_inputs(cfg, 11 + rank, device=dev)
+    step = lib.DraftStep(cfg, inp["weights"], device=dev)
+    vcfg = synth.VerifyConfig(name="verify_R32_g1", R=cfg.R, gamma=1, V=cfg.V)
+    vin = synth.make_verify_inputs(vcfg, 13 + rank, device=dev)
+    out = {"q": torch.empty((cfg.R, cfg.V), dtype=torch.float32, device=dev),
+           "y": torch.empty(cfg.R, dtype=torch.int32, device=dev)}
+    vout = {k: torch.empty(cfg.R, dtype=torch.int32, device=dev)
+            for k in ("accepted", "next_token", "n_emit", "status")}
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def call(i):
+        step(inp["parent_hidden"], inp["frontier"], inp["pos"], inp["kv_k"], inp["kv_v"], inp["ctx_len"],
+             seed=3, offset=i, out=out)
+
+    for i in range(3):
+        call(i)
+        lib.spec_verify(vin["p"], out["q"].view(cfg.R, 1, cfg.V), out["y"].view(cfg.R, 1), seed=4, offset=i,
+                        out=vout)
+    torch.cuda.synchronize()
+    lib.check_errors()
+    n = args.draft_steps
+    e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+          torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        flush.zero_()
+        e[i][0].record()
+        call(100 + i)
+        e[i][1].record()
+        lib.spec_verify(vin["p"], out["q"].view(cfg.R, 1, cfg.V), out["y"].view(cfg.R, 1), seed=4, offset=100 + i,
+                        out=vout)
+        e[i][2].record()
+    torch.cuda.synchronize()
+    lib.check_errors()
+    d_ms = sorted(a.elapsed_time(b) for a, b, _ in e)[n // 2]
+    v_ms = sorted(b.elapsed_time(c) for _, b, c in e)[n // 2]
+    d, f, V, R = cfg.d, cfg.ffn, cfg.V, cfg.R
+    weight_bytes = 2.0 * (2 * d * d + 4 * d * d + 3 * d * f)
+    head_bytes = 2.0 * V * d
+    cache_bytes = 2.0 * 2 * R * cfg.ctx * d
+    q_bytes = 4.0 * R * V
+    total = weight_bytes + head_bytes + cache_bytes + q_bytes
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gbs = total / (d_ms / 1e3) / 1e9
+    return {"workload": "draft step R=32, cache 8192 x d=7168 (56x128), ffn 18432, V=129280 + gamma=1 verify",
+            "ms_median": d_ms, "verify_ms_median": v_ms, "algorithmic_bytes": total,
+            "achieved_gbs": gbs, "peak_gbs": hbm_peak, "frac": gbs / hbm_peak,
+            "bound": "hbm", "steps": n, "l2": "flushed before every timed call"}
 
 
 def measure_e2e(cfg, vcfg, chain, batch, x, vin, steps, dev, rank, world, tokens_per_step):
