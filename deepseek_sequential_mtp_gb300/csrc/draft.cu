@@ -15,22 +15,21 @@
 // N = 32) with split-K so that the weight stream covers every SM; partial
 // tiles accumulate into an fp32 buffer with atomics and small "finish"
 // kernels round to bf16 with the fused RoPE / residual / SwiGLU / RMSNorm.
-// Attention is flash-decoding: (request, 8 heads, 512-key chunk) CTAs write
-// partial (max, sum, output) records that a combine kernel merges with the
-// new row's key.  The head writes logits into q_out, which a per-request
+// Attention is split-K decoding: persistent CTAs stream the cache with TMA
+// and write partial (max, sum, output) records per (request, head, key
+// split) that a combine kernel merges with the new row's key.  The head writes logits into q_out, which a per-request
 // kernel turns into probabilities in place and samples from.
 #include <algorithm>
 #include <cmath>
 
 #include "gemm_tc.cuh"
+#include "mbarrier.cuh"
 
 MTP_DEFINE_ERROR_WORD(mtp_take_errors_draft)
 
 namespace {
 
 constexpr int kMaxR = 32;
-constexpr int kHeadsPerCta = 8;
-constexpr int kKeysPerChunk = 512;
 
 __device__ __forceinline__ float bf(const __nv_bfloat16& v) { return __bfloat162float(v); }
 
@@ -175,92 +174,245 @@ __global__ void finish_swiglu_kernel(const float* __restrict__ acc, __nv_bfloat1
 }
 
 // ---------------------------------------------------------------------------
-// flash-decoding: CTA = (request, 8 heads, 512-key chunk of the cache); warp = head
-// part record: [max, sum, o(hd)] (fp32) per (r, head, chunk)
+// Decode attention over the module's K/V cache, streamed by TMA.
+// Persistent CTAs (one per SM) walk work units u -> (head h, key split sp,
+// request r), heads fastest so that concurrently running units read
+// neighbouring 256-byte pieces of the same cache rows.  A producer warp
+// streams [64 keys x head_dim] tiles of K and V into a shared-memory ring;
+// each of the 8 consumer warps takes 8 keys of every tile (so every consumer
+// waits on every ring phase in order) and keeps its own online-softmax state
+// (m, l, o); at the end of a unit the warps' states are merged into one
+// record part[r, h, sp] = (max, sum, o[head_dim]).
 // ---------------------------------------------------------------------------
+constexpr int kAttnTileKeys = 64;
+constexpr int kAttnWarps = 8;
+constexpr int kAttnKeysPerWarp = kAttnTileKeys / kAttnWarps;
+constexpr int kAttnThreads = (kAttnWarps + 1) * 32;
+constexpr int kAttnRingBytes = 192 * 1024;
+constexpr int kAttnSplitKeys = 1024;  // target keys per work unit
+static_assert(kAttnKeysPerWarp == 8, "the transposed reduction below is written for 8 keys per warp");
+
 template <int HD>
-__global__ void __launch_bounds__(256)
-decode_attn_partial_kernel(const __nv_bfloat16* __restrict__ qkv, const __nv_bfloat16* __restrict__ kc,
-                           const __nv_bfloat16* __restrict__ vc, const int32_t* __restrict__ ctx_len,
-                           float* __restrict__ part, int H, int T, int n_chunks, float scale) {
-  __shared__ float sq[kHeadsPerCta][HD];
-  __shared__ float sp[kHeadsPerCta][kKeysPerChunk];
-  const int r = blockIdx.x, chunk = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y * kHeadsPerCta + warp;
-  const int d = H * HD;
-  const int len = min(max(ctx_len[r], 0), T);
-  const int s0 = chunk * kKeysPerChunk, s1 = min(s0 + kKeysPerChunk, len);
-  float* rec = part + ((static_cast<size_t>(r) * H + h) * n_chunks + chunk) * (HD + 2);
-  if (h >= H) return;
-  for (int i = lane; i < HD; i += 32) sq[warp][i] = bf(qkv[static_cast<size_t>(r) * 3 * d + h * HD + i]) * scale;
-  __syncwarp();
-  if (s1 <= s0) {  // empty chunk
-    if (lane == 0) {
-      rec[0] = -INFINITY;
-      rec[1] = 0.f;
-    }
-    for (int i = lane; i < HD; i += 32) rec[2 + i] = 0.f;
-    return;
+struct AttnCfg {
+  static constexpr int kTileBytes = kAttnTileKeys * HD * 2;
+  static constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
+  static constexpr int kStages = kAttnRingBytes / kStageBytes;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+};
+
+// v[j] holds this lane's partial dot product for key j of the warp's 8 keys
+// (lanes own head_dim slices).  Reduce-scatter over the warp: 4 + 2 + 1
+// exchanges halve the keys held, two more finish the sums.  Lane l ends with
+// the full dot product of key 4*bit4(l) + 2*bit3(l) + bit2(l).
+__device__ __forceinline__ float reduce8_transposed(const float (&v)[8], int lane) {
+  const bool b16 = lane & 16, b8 = lane & 8, b4 = lane & 4;
+  float a[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = b16 ? v[i] : v[i + 4];
+    const float keep = b16 ? v[i + 4] : v[i];
+    a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
   }
-  // scores: lane per key
-  float mx = -INFINITY;
-  for (int s = s0 + lane; s < s1; s += 32) {
-    const uint4* k4 = reinterpret_cast<const uint4*>(kc + (static_cast<size_t>(r) * T + s) * d + h * HD);
-    float acc = 0.f;
+  float c[2];
 #pragma unroll
-    for (int c = 0; c < HD / 8; ++c) {
-      const uint4 u = __ldcs(k4 + c);
-      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float2 f = __bfloat1622float2(b[t]);
-        acc += f.x * sq[warp][c * 8 + 2 * t] + f.y * sq[warp][c * 8 + 2 * t + 1];
+  for (int i = 0; i < 2; ++i) {
+    const float send = b8 ? a[i] : a[i + 2];
+    const float keep = b8 ? a[i + 2] : a[i];
+    c[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  const float send = b4 ? c[0] : c[1];
+  float e = (b4 ? c[1] : c[0]) + __shfl_xor_sync(0xffffffffu, send, 4);
+  e += __shfl_xor_sync(0xffffffffu, e, 2);
+  e += __shfl_xor_sync(0xffffffffu, e, 1);
+  return e;
+}
+__device__ __forceinline__ int key_of_lane(int lane) { return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1); }
+__device__ __forceinline__ int lane_of_key(int j) { return ((j >> 2) & 1) * 16 + ((j >> 1) & 1) * 8 + (j & 1) * 4; }
+
+template <int KD>
+__device__ __forceinline__ void load_bf16x(const void* p, float (&f)[KD]) {
+  if constexpr (KD == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    f[0] = f0.x; f[1] = f0.y; f[2] = f1.x; f[3] = f1.y;
+  } else {
+    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+    f[0] = f0.x; f[1] = f0.y;
+  }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+decode_attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const __nv_bfloat16* __restrict__ qkv, const int32_t* __restrict__ ctx_len,
+                   float* __restrict__ part, int H, int T, int n_split, int split_keys, int n_units, float scale) {
+  using C = AttnCfg<HD>;
+  constexpr int S = C::kStages;
+  constexpr int kDim = HD / 32;
+  extern __shared__ uint8_t attn_smem_raw[];
+  __shared__ __align__(8) uint64_t bars[2 * S];
+  __shared__ float s_m[2][kAttnWarps], s_l[2][kAttnWarps];
+  __shared__ float s_o[2][kAttnWarps][HD];
+  __shared__ int s_abort;
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(attn_smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t ring_s = mtp::smem_u32(ring);
+  const uint32_t full0 = mtp::smem_u32(bars), empty0 = full0 + 8u * S;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = H * HD;
+  volatile int* abort_flag = &s_abort;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mtp::mbar_init(full0 + 8u * i, 1);
+      mtp::mbar_init(empty0 + 8u * i, kAttnWarps);
+    }
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+
+  auto unit = [&](int u, int& r, int& h, int& sp, int& lo, int& hi) {
+    h = u % H;
+    const int rest = u / H;
+    sp = rest % n_split;
+    r = rest / n_split;
+    const int len = min(max(ctx_len[r], 0), T);
+    lo = sp * split_keys;
+    hi = min(lo + split_keys, len);
+  };
+
+  if (warp == kAttnWarps) {
+    // ------------------------------ producer ------------------------------
+    uint32_t g = 0;  // tiles issued
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+      int r, h, sp, lo, hi;
+      unit(u, r, h, sp, lo, hi);
+      for (int s = lo; s < hi; s += kAttnTileKeys) {
+        const uint32_t slot = g % S, use = g / S;
+        // warp-uniform outcome: every lane waits, all must have seen the phase
+        if (use > 0 && !__all_sync(0xffffffffu, mtp::mbar_wait_bounded(empty0 + 8u * slot, (use - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t full = full0 + 8u * slot;
+          const uint32_t dst = ring_s + slot * C::kStageBytes;
+          mtp::mbar_expect_tx(full, C::kStageBytes);
+          mtp::tma_tile_2d(dst, &tmK, h * HD, r * T + s, full);
+          mtp::tma_tile_2d(dst + C::kTileBytes, &tmV, h * HD, r * T + s, full);
+        }
+        __syncwarp();
+        ++g;
       }
     }
-    sp[warp][s - s0] = acc;
-    mx = fmaxf(mx, acc);
+    if (lane == 0) {
+      if (!ok) {
+        atomicOr(&g_mtp_error_word, MTP_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // no copy may still be landing in shared memory when the CTA leaves
+      for (uint32_t t = g > static_cast<uint32_t>(S) ? g - S : 0; t < g; ++t)
+        if (!mtp::mbar_wait_bounded(full0 + 8u * (t % S), (t / S) & 1)) {
+          atomicOr(&g_mtp_error_word, MTP_DEVERR_TIMEOUT);
+          break;
+        }
+    }
+    return;
   }
-  mx = mtp::warp_max(mx);
-  float sum = 0.f;
-  for (int s = s0 + lane; s < s1; s += 32) {
-    const float e = __expf(sp[warp][s - s0] - mx);
-    sp[warp][s - s0] = e;
-    sum += e;
-  }
-  sum = mtp::warp_sum(sum);
-  __syncwarp();
-  // P V: lane owns HD/32 consecutive dims
-  constexpr int kDim = HD / 32;
-  float o[kDim];
+
+  // ------------------------------ consumers ------------------------------
+  uint32_t g = 0;
+  int k = 0;
+  const int jkey = key_of_lane(lane);
+  for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++k) {
+    int r, h, sp, lo, hi;
+    unit(u, r, h, sp, lo, hi);
+    float qv[kDim];
+    load_bf16x<kDim>(qkv + static_cast<size_t>(r) * 3 * d + h * HD + lane * kDim, qv);
 #pragma unroll
-  for (int t = 0; t < kDim; ++t) o[t] = 0.f;
-  const __nv_bfloat16* vbase = vc + static_cast<size_t>(r) * T * d + h * HD + lane * kDim;
-#pragma unroll 4
-  for (int s = s0; s < s1; ++s) {
-    const float p = sp[warp][s - s0];
-    const __nv_bfloat16* vr = vbase + static_cast<size_t>(s) * d;
-    if constexpr (kDim == 4) {
-      const uint2 u = __ldcs(reinterpret_cast<const uint2*>(vr));
-      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
-      const float2 f0 = __bfloat1622float2(b[0]), f1 = __bfloat1622float2(b[1]);
-      o[0] += p * f0.x;
-      o[1] += p * f0.y;
-      o[2] += p * f1.x;
-      o[3] += p * f1.y;
-    } else {
-      const __nv_bfloat162 u = __ldcs(reinterpret_cast<const __nv_bfloat162*>(vr));
-      const float2 f = __bfloat1622float2(u);
-      o[0] += p * f.x;
-      o[1] += p * f.y;
+    for (int t = 0; t < kDim; ++t) qv[t] *= scale;
+    float m = -INFINITY, l = 0.f, o[kDim];
+#pragma unroll
+    for (int t = 0; t < kDim; ++t) o[t] = 0.f;
+    for (int s = lo; s < hi; s += kAttnTileKeys, ++g) {
+      const uint32_t slot = g % S, use = g / S;
+      // the skip decision is warp-uniform (lane 0's view of the flag)
+      bool skip = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
+      if (!skip && !__all_sync(0xffffffffu, mtp::mbar_wait_bounded(full0 + 8u * slot, use & 1))) {
+        if (lane == 0) {
+          atomicOr(&g_mtp_error_word, MTP_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        skip = true;
+      }
+      if (skip) continue;
+      const uint8_t* tk = ring + slot * C::kStageBytes + warp * kAttnKeysPerWarp * HD * 2 + lane * kDim * 2;
+      const uint8_t* tv = tk + C::kTileBytes;
+      float part_dot[kAttnKeysPerWarp];
+#pragma unroll
+      for (int j = 0; j < kAttnKeysPerWarp; ++j) {
+        float kv[kDim];
+        load_bf16x<kDim>(tk + j * HD * 2, kv);
+        float acc = 0.f;
+#pragma unroll
+        for (int t = 0; t < kDim; ++t) acc = fmaf(qv[t], kv[t], acc);
+        part_dot[j] = acc;
+      }
+      const float dot = reduce8_transposed(part_dot, lane);
+      const bool valid = s + warp * kAttnKeysPerWarp + jkey < hi;
+      const float score = valid ? dot : -INFINITY;
+      const float m_new = fmaxf(m, mtp::warp_max(score));
+      if (m_new != -INFINITY) {  // warp-uniform
+        const float alpha = __expf(m - m_new);
+        const float p = valid ? __expf(score - m_new) : 0.f;
+        l = l * alpha + mtp::warp_sum((lane & 3) == 0 ? p : 0.f);
+#pragma unroll
+        for (int t = 0; t < kDim; ++t) o[t] *= alpha;
+#pragma unroll
+        for (int j = 0; j < kAttnKeysPerWarp; ++j) {
+          const float pj = __shfl_sync(0xffffffffu, p, lane_of_key(j));
+          float vv[kDim];
+          load_bf16x<kDim>(tv + j * HD * 2, vv);
+#pragma unroll
+          for (int t = 0; t < kDim; ++t) o[t] = fmaf(pj, vv[t], o[t]);
+        }
+        m = m_new;
+      }
+      __syncwarp();
+      if (lane == 0) mtp::mbar_arrive_cnt(empty0 + 8u * slot, 1);
+    }
+    // merge the 8 warps' states of this unit (double-buffered: one barrier per unit)
+    const int b = k & 1;
+    if (lane == 0) {
+      s_m[b][warp] = m;
+      s_l[b][warp] = l;
+    }
+#pragma unroll
+    for (int t = 0; t < kDim; ++t) s_o[b][warp][lane * kDim + t] = o[t];
+    asm volatile("bar.sync 1, %0;" ::"n"(kAttnWarps * 32) : "memory");
+    if (threadIdx.x < HD) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, s_m[b][w]);
+      float L = 0.f, O = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) {
+          const float e = __expf(s_m[b][w] - M);
+          L += e * s_l[b][w];
+          O += e * s_o[b][w][threadIdx.x];
+        }
+      }
+      float* rec = part + ((static_cast<size_t>(r) * H + h) * n_split + sp) * (HD + 2);
+      if (threadIdx.x == 0) {
+        rec[0] = M;
+        rec[1] = L;
+      }
+      rec[2 + threadIdx.x] = O;
     }
   }
-  if (lane == 0) {
-    rec[0] = mx;
-    rec[1] = sum;
-  }
-#pragma unroll
-  for (int t = 0; t < kDim; ++t) rec[2 + lane * kDim + t] = o[t];
 }
 
 // merge the chunk records with the new row's own key/value; one warp per (r, head)
@@ -445,7 +597,7 @@ struct DraftLayout {
 DraftLayout draft_layout(const mtp_dims& D) {
   DraftLayout L{};
   const size_t R = D.B, d = D.d;
-  L.n_chunks = (D.T + kKeysPerChunk - 1) / kKeysPerChunk;
+  L.n_chunks = std::max(1, (D.T + kAttnSplitKeys - 1) / kAttnSplitKeys);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -575,18 +727,41 @@ extern "C" mtp_status mtp_draft_step(const mtp_dims* dims, const mtp_weights* w,
   // attention over the module's own cache plus the new row
   const float scale = 1.0f / sqrtf(static_cast<float>(hd));
   float* part = reinterpret_cast<float*>(base + L.part);
-  const dim3 agrid(R, (H + kHeadsPerCta - 1) / kHeadsPerCta, L.n_chunks);
   const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(kv_k);
   const __nv_bfloat16* vc = static_cast<const __nv_bfloat16*>(kv_v);
+  const int n_split = L.n_chunks;
+  const int split_keys = ((D.T + n_split - 1) / n_split + kAttnTileKeys - 1) / kAttnTileKeys * kAttnTileKeys;
+  const int n_units = R * H * n_split;
+  const int agrid = std::min(n_units, sm_count());
+  CUtensorMap tmk, tmv;
+  const uint64_t cache_rows = static_cast<uint64_t>(R) * D.T;
+  if (cache_rows > 0x7FFFFFFFull) return MTP_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
+  if (!mtp::tensor_map_bf16_2d(&tmk, kc, cache_rows, d, d, hd, kAttnTileKeys) ||
+      !mtp::tensor_map_bf16_2d(&tmv, vc, cache_rows, d, d, hd, kAttnTileKeys))
+    return MTP_ERR_CUDA;
   mtp::prof_begin(MTP_KC_ATTENTION, st);
   if (hd == 128) {
-    decode_attn_partial_kernel<128><<<agrid, 256, 0, st>>>(qkv, kc, vc, ctx_len, part, H, D.T, L.n_chunks, scale);
+    static bool attr = false;
+    if (!attr) {
+      MTP_CUDA_TRY(cudaFuncSetAttribute(decode_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        AttnCfg<128>::kSmemBytes));
+      attr = true;
+    }
+    decode_attn_kernel<128><<<agrid, kAttnThreads, AttnCfg<128>::kSmemBytes, st>>>(
+        tmk, tmv, qkv, ctx_len, part, H, D.T, n_split, split_keys, n_units, scale);
     mtp::note_launch();
-    decode_attn_combine_kernel<128><<<(R * H + 7) / 8, 256, 0, st>>>(qkv, part, o, R, H, L.n_chunks, scale);
+    decode_attn_combine_kernel<128><<<(R * H + 7) / 8, 256, 0, st>>>(qkv, part, o, R, H, n_split, scale);
   } else {
-    decode_attn_partial_kernel<64><<<agrid, 256, 0, st>>>(qkv, kc, vc, ctx_len, part, H, D.T, L.n_chunks, scale);
+    static bool attr = false;
+    if (!attr) {
+      MTP_CUDA_TRY(cudaFuncSetAttribute(decode_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        AttnCfg<64>::kSmemBytes));
+      attr = true;
+    }
+    decode_attn_kernel<64><<<agrid, kAttnThreads, AttnCfg<64>::kSmemBytes, st>>>(
+        tmk, tmv, qkv, ctx_len, part, H, D.T, n_split, split_keys, n_units, scale);
     mtp::note_launch();
-    decode_attn_combine_kernel<64><<<(R * H + 7) / 8, 256, 0, st>>>(qkv, part, o, R, H, L.n_chunks, scale);
+    decode_attn_combine_kernel<64><<<(R * H + 7) / 8, 256, 0, st>>>(qkv, part, o, R, H, n_split, scale);
   }
   mtp::note_launch();
   mtp::prof_end(MTP_KC_ATTENTION, st);

@@ -1,6 +1,8 @@
 // Internal interface of the tcgen05 GEMM core (gemm_tc.cu) used by the chain.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace mtp {
@@ -53,5 +55,11 @@ struct GemmDesc {
 int gemm_ce_tile_n();
 
 mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream);
+
+// Tensor map of a row-major bf16 matrix [rows, cols] (row stride ld
+// elements, a multiple of 8) for tiled loads of box_cols x box_rows without
+// swizzle; false if the encoder is unavailable or rejects the description.
+bool tensor_map_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
+                        uint32_t box_cols, uint32_t box_rows);
 
 }  // namespace mtp

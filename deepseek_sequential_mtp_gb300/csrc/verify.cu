@@ -34,6 +34,7 @@
 #include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "mbarrier.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -110,49 +111,13 @@ __device__ __forceinline__ void warp_two_sum(float& hi, float& lo) {
 }
 __device__ __forceinline__ double chunk_value(float2 v) { return (double)v.x + (double)v.y; }
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_cnt(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// bounded wait; false after the library's wait limit (the caller reports it)
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_test_wait(bar, parity)) return true;
-  const long long t0 = mtp::cycles_now();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if (it > 64) __nanosleep(32);
-    if ((it & 31u) == 0 && mtp::cycles_now() - t0 > mtp::kWaitLimitCycles) return false;
-  }
-}
-__device__ __forceinline__ uint32_t cluster_addr(uint32_t a, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-  return r;
-}
-// one-dimensional bulk copy global -> shared (16-byte aligned, size % 16 == 0)
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
+using mtp::bulk_load;
+using mtp::cluster_addr;
+using mtp::mbar_arrive_cnt;
+using mtp::mbar_expect_tx;
+using mtp::mbar_init;
+using mtp::smem_u32;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) { return mtp::mbar_wait_bounded(bar, parity); }
 
 template <bool kVec4>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
@@ -266,7 +231,8 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
       int issued_last = -1;
       for (int st = 0; st < n_stages; ++st) {
         const int slot = st % kRing, use = st / kRing;
-        if (use > 0 && !mbar_wait(s_empty_bar + 8u * slot, (use - 1) & 1)) {
+        // warp-uniform outcome: every lane waits, all must have seen the phase
+        if (use > 0 && !__all_sync(0xffffffffu, mbar_wait(s_empty_bar + 8u * slot, (use - 1) & 1))) {
           if (lane == 0) {
             atomicOr(&g_mtp_error_word, MTP_DEVERR_TIMEOUT);
             s_timeout = 1;
@@ -297,10 +263,13 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
       }
       __syncwarp();
     } else {
-      for (int li = warp; li < n_local && !s_timeout; li += kConsumerWarps) {
+      volatile int* timeout_flag = &s_timeout;
+      for (int li = warp; li < n_local; li += kConsumerWarps) {
         const int st = li / kStageChunks, i = li % kStageChunks;
         const int slot = st % kRing, use = st / kRing;
-        if (!mbar_wait(s_full_bar + 8u * slot, use & 1)) {
+        // warp-uniform decisions: lane 0's view of the flag, all lanes' waits
+        if (__shfl_sync(0xffffffffu, *timeout_flag, 0)) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full_bar + 8u * slot, use & 1))) {
           if (lane == 0) {
             atomicOr(&g_mtp_error_word, MTP_DEVERR_TIMEOUT);
             s_timeout = 1;

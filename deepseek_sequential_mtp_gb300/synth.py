@@ -160,6 +160,9 @@ DRAFT_C5 = DraftConfig(name="draft_R32_ctx8192_d7168", R=32, ctx=8192, d=7168,
                        n_heads=56, head_dim=128, ffn=18432, V=129280)
 DRAFT_SMALL = DraftConfig(name="draft_small", R=5, ctx=300, d=256, n_heads=4,
                           head_dim=64, ffn=576, V=1000, w_std=0.05, gain_std=0.1)
+# 128-wide heads, two key splits of 576 keys, ragged last tiles
+DRAFT_SMALL_HD128 = DraftConfig(name="draft_small_hd128", R=4, ctx=1100, d=256, n_heads=2,
+                                head_dim=128, ffn=512, V=777, w_std=0.05, gain_std=0.1)
 
 
 # --------------------------------------------------------------------------

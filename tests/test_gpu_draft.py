@@ -76,6 +76,17 @@ def test_small_full_parity(seed):
                 assert gy[i] == r["y"][i]
 
 
+def test_hd128_split_keys_parity():
+    """head_dim 128 with the cache split into two 576-key units: empty, one
+    ragged tile, a split boundary crossed by one key, and a full cache."""
+    cfg = synth.DRAFT_SMALL_HD128
+    inp = synth.make_draft_inputs(cfg, 7)
+    inp["ctx_len"] = torch.tensor([0, 63, 577, 1100], dtype=torch.int32)
+    inp["pos"] = inp["ctx_len"].clone()
+    g, r, req = run(cfg, inp, seed=9, offset=1)
+    check(g, r, req)
+
+
 def test_full_size_sampled_requests():
     """32 requests, module cache 8192 x d=7168 (56 x 128 heads), ffn 18432,
     V=129280; oracle on two requests, draw consistency on all 32."""
