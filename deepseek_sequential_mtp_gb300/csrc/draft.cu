@@ -19,11 +19,15 @@
 // and write partial (max, sum, output) records per (request, head, key
 // split) that a combine kernel merges with the new row's key.  The head writes logits into q_out, which a per-request
 // kernel turns into probabilities in place and samples from.
+#include <cooperative_groups.h>
+
 #include <algorithm>
 #include <cmath>
 
 #include "gemm_tc.cuh"
 #include "mbarrier.cuh"
+
+namespace cg = cooperative_groups;
 
 MTP_DEFINE_ERROR_WORD(mtp_take_errors_draft)
 
@@ -67,24 +71,36 @@ __device__ float block_sum(float v, float* sh) {
   for (int i = 0; i < (blockDim.x >> 5); ++i) t += sh[i];
   return t;
 }
-__device__ float block_max(float v, float* sh) {
-  v = mtp::warp_max(v);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) sh[w] = v;
-  __syncthreads();
-  float t = -INFINITY;
-  for (int i = 0; i < (blockDim.x >> 5); ++i) t = fmaxf(t, sh[i]);
-  return t;
-}
 
 // ---------------------------------------------------------------------------
-// c = [RMSNorm_h(parent_hidden); RMSNorm_e(E[frontier])], one CTA per request
+// Row kernels: one 1024-thread CTA per request row, vector accesses (d is a
+// multiple of 64), so a row takes one or two memory round trips per pass.
 // ---------------------------------------------------------------------------
-__global__ void draft_prologue_kernel(const __nv_bfloat16* __restrict__ hp, const int32_t* __restrict__ frontier,
-                                      const __nv_bfloat16* __restrict__ embed, const __nv_bfloat16* __restrict__ gh,
-                                      const __nv_bfloat16* __restrict__ ge, __nv_bfloat16* __restrict__ c, int d, int V,
-                                      float eps) {
+constexpr int kRowThreads = 1024;
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float2 v = __bfloat1622float2(b[t]);
+    f[2 * t] = v.x;
+    f[2 * t + 1] = v.y;
+  }
+}
+__device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8]) {
+  uint4 u;
+  __nv_bfloat162* b = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) b[t] = __floats2bfloat162_rn(f[2 * t], f[2 * t + 1]);
+  return u;
+}
+
+// c = [RMSNorm_h(parent_hidden); RMSNorm_e(E[frontier])]
+__global__ void __launch_bounds__(kRowThreads)
+draft_prologue_kernel(const __nv_bfloat16* __restrict__ hp, const int32_t* __restrict__ frontier,
+                      const __nv_bfloat16* __restrict__ embed, const __nv_bfloat16* __restrict__ gh,
+                      const __nv_bfloat16* __restrict__ ge, __nv_bfloat16* __restrict__ c, int d, int V,
+                      float eps) {
   __shared__ float sh[32];
   const int r = blockIdx.x;
   int tok = frontier[r];
@@ -92,76 +108,122 @@ __global__ void draft_prologue_kernel(const __nv_bfloat16* __restrict__ hp, cons
     if (threadIdx.x == 0) atomicOr(&g_mtp_error_word, MTP_DEVERR_TOKEN_RANGE);
     tok = min(max(tok, 0), V - 1);
   }
-  const __nv_bfloat16* h = hp + static_cast<size_t>(r) * d;
-  const __nv_bfloat16* e = embed + static_cast<size_t>(tok) * d;
+  const uint4* h8 = reinterpret_cast<const uint4*>(hp + static_cast<size_t>(r) * d);
+  const uint4* e8 = reinterpret_cast<const uint4*>(embed + static_cast<size_t>(tok) * d);
+  const int n8 = d / 8;
   float a = 0.f, b = 0.f;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    const float x = bf(h[i]), y = bf(e[i]);
-    a += x * x;
-    b += y * y;
+  for (int i = threadIdx.x; i < n8; i += kRowThreads) {
+    float x[8], y[8];
+    bf16x8_to_f32(h8[i], x);
+    bf16x8_to_f32(e8[i], y);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      a += x[t] * x[t];
+      b += y[t] * y[t];
+    }
   }
   a = block_sum(a, sh);
   b = block_sum(b, sh);
   const float rh = 1.0f / sqrtf(a / d + eps), re = 1.0f / sqrtf(b / d + eps);
-  __nv_bfloat16* out = c + static_cast<size_t>(r) * 2 * d;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    out[i] = __float2bfloat16_rn(bf(gh[i]) * (bf(h[i]) * rh));
-    out[d + i] = __float2bfloat16_rn(bf(ge[i]) * (bf(e[i]) * re));
+  uint4* out = reinterpret_cast<uint4*>(c + static_cast<size_t>(r) * 2 * d);
+  for (int i = threadIdx.x; i < n8; i += kRowThreads) {
+    float x[8], y[8], g1[8], g2[8];
+    bf16x8_to_f32(h8[i], x);
+    bf16x8_to_f32(e8[i], y);
+    bf16x8_to_f32(reinterpret_cast<const uint4*>(gh)[i], g1);
+    bf16x8_to_f32(reinterpret_cast<const uint4*>(ge)[i], g2);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      x[t] = g1[t] * (x[t] * rh);
+      y[t] = g2[t] * (y[t] * re);
+    }
+    out[i] = f32_to_bf16x8(x);
+    out[n8 + i] = f32_to_bf16x8(y);
   }
 }
 
-// y = bf16(acc [+ resid]); optionally norm_out = bf16(RMSNorm_g(y)) (one CTA per row)
-__global__ void finish_row_kernel(const float* __restrict__ acc, const __nv_bfloat16* __restrict__ resid,
-                                  __nv_bfloat16* __restrict__ y, const __nv_bfloat16* __restrict__ g,
-                                  __nv_bfloat16* __restrict__ norm_out, int d, float eps) {
+// y = bf16(acc [+ resid]); optionally norm_out = bf16(RMSNorm_g(y))
+__global__ void __launch_bounds__(kRowThreads)
+finish_row_kernel(const float* __restrict__ acc, const __nv_bfloat16* __restrict__ resid,
+                  __nv_bfloat16* __restrict__ y, const __nv_bfloat16* __restrict__ g,
+                  __nv_bfloat16* __restrict__ norm_out, int d, float eps) {
   __shared__ float sh[32];
   const int r = blockIdx.x;
-  const float* a = acc + static_cast<size_t>(r) * d;
-  __nv_bfloat16* yr = y + static_cast<size_t>(r) * d;
+  const int n8 = d / 8;
+  const float4* a4 = reinterpret_cast<const float4*>(acc + static_cast<size_t>(r) * d);
+  uint4* y8 = reinterpret_cast<uint4*>(y + static_cast<size_t>(r) * d);
   float ss = 0.f;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    float v = a[i];
-    if (resid) v += bf(resid[static_cast<size_t>(r) * d + i]);
-    const __nv_bfloat16 vb = __float2bfloat16_rn(v);
-    yr[i] = vb;
-    const float vf = bf(vb);
-    ss += vf * vf;
+  for (int i = threadIdx.x; i < n8; i += kRowThreads) {
+    const float4 lo = a4[2 * i], hi = a4[2 * i + 1];
+    float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    if (resid) {
+      float rv[8];
+      bf16x8_to_f32(reinterpret_cast<const uint4*>(resid + static_cast<size_t>(r) * d)[i], rv);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) v[t] += rv[t];
+    }
+    const uint4 vb = f32_to_bf16x8(v);
+    y8[i] = vb;
+    float vf[8];
+    bf16x8_to_f32(vb, vf);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) ss += vf[t] * vf[t];
   }
   if (!norm_out) return;
   ss = block_sum(ss, sh);
   const float rn = 1.0f / sqrtf(ss / d + eps);
-  for (int i = threadIdx.x; i < d; i += blockDim.x)
-    norm_out[static_cast<size_t>(r) * d + i] = __float2bfloat16_rn(bf(g[i]) * (bf(yr[i]) * rn));
+  uint4* o8 = reinterpret_cast<uint4*>(norm_out + static_cast<size_t>(r) * d);
+  for (int i = threadIdx.x; i < n8; i += kRowThreads) {
+    float vf[8], gf[8];
+    bf16x8_to_f32(y8[i], vf);
+    bf16x8_to_f32(reinterpret_cast<const uint4*>(g)[i], gf);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) vf[t] = gf[t] * (vf[t] * rn);
+    o8[i] = f32_to_bf16x8(vf);
+  }
 }
 
-// qkv = bf16(RoPE(q), RoPE(k), v) at the request's position; the angle is
-// formed and reduced modulo 2*pi in double, sine/cosine taken in fp32
-__global__ void finish_qkv_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ qkv,
-                                  const int32_t* __restrict__ pos, int d, int hd, float base, int pos_max) {
+// qkv = bf16(RoPE(q), RoPE(k), v) at the request's position.  CTA (x, r)
+// covers pairs / v columns [x*1024, x*1024 + 1024) of row r; the row's
+// (cos, sin) per frequency index is computed once per CTA: angle formed and
+// reduced modulo 2*pi in double, sine/cosine taken in fp32.
+constexpr int kQkvCols = 1024;
+__global__ void __launch_bounds__(256)
+finish_qkv_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ qkv, const int32_t* __restrict__ pos,
+                  int d, int hd, float base, int pos_max) {
+  __shared__ float2 cs[64];  // hd / 2 <= 64
   const int r = blockIdx.y;
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // pair index over q and k, or a v column
   const int half = hd / 2;
-  const float* a = acc + static_cast<size_t>(r) * 3 * d;
-  __nv_bfloat16* o = qkv + static_cast<size_t>(r) * 3 * d;
-  if (i < d) {  // d pairs: q and k heads, (j, j + half) within each head
-    const int head = i / half, j = i % half;  // head index over 2*H (q heads then k heads)
-    const int col = head * hd + j;
-    const float x1 = a[col], x2 = a[col + half];
+  if (threadIdx.x < half) {
     float c = 1.f, s = 0.f;
     if (base > 0.f) {
       int p = pos[r];
       if (p < 0 || p > pos_max) {
-        if (j == 0) atomicOr(&g_mtp_error_word, MTP_DEVERR_TOKEN_RANGE);
+        if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(&g_mtp_error_word, MTP_DEVERR_TOKEN_RANGE);
         p = min(max(p, 0), pos_max);
       }
+      const int j = threadIdx.x;
       const double ang = static_cast<double>(p) * exp2(-2.0 * j / hd * log2(static_cast<double>(base)));
       const double two_pi = 6.283185307179586;
       sincosf(static_cast<float>(ang - rint(ang / two_pi) * two_pi), &s, &c);
     }
-    o[col] = __float2bfloat16_rn(x1 * c - x2 * s);
-    o[col + half] = __float2bfloat16_rn(x2 * c + x1 * s);
+    cs[threadIdx.x] = make_float2(c, s);
   }
-  if (i < d) o[2 * d + i] = __float2bfloat16_rn(a[2 * d + i]);  // v
+  __syncthreads();
+  const float* a = acc + static_cast<size_t>(r) * 3 * d;
+  __nv_bfloat16* o = qkv + static_cast<size_t>(r) * 3 * d;
+  const int i0 = blockIdx.x * kQkvCols;
+  const int i1 = min(i0 + kQkvCols, d);
+  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+    // pair i: head i / half over the 2H q and k heads, (j, j + half) within it
+    const int head = i / half, j = i % half;
+    const int col = head * hd + j;
+    const float x1 = a[col], x2 = a[col + half];
+    const float2 t = cs[j];
+    o[col] = __float2bfloat16_rn(x1 * t.x - x2 * t.y);
+    o[col + half] = __float2bfloat16_rn(x2 * t.x + x1 * t.y);
+    o[2 * d + i] = __float2bfloat16_rn(a[2 * d + i]);  // v
+  }
 }
 
 // g = bf16(silu(gate) * up) from acc [R, 2*ffn] (gate then up)
@@ -415,97 +477,172 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   }
 }
 
-// merge the chunk records with the new row's own key/value; one warp per (r, head)
+// merge the split records with the new row's own key/value; one warp per
+// (request, head): lanes read the records' (max, sum) in parallel, then the
+// weighted outputs, lanes owning head_dim slices
 template <int HD>
 __global__ void decode_attn_combine_kernel(const __nv_bfloat16* __restrict__ qkv, const float* __restrict__ part,
-                                           __nv_bfloat16* __restrict__ out, int R, int H, int n_chunks, float scale) {
+                                           __nv_bfloat16* __restrict__ out, int R, int H, int n_split, float scale) {
   const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (item >= R * H) return;
   const int r = item / H, h = item % H;
   const int d = H * HD;
   constexpr int kDim = HD / 32;
+  constexpr int kRec = HD + 2;
   const __nv_bfloat16* row = qkv + static_cast<size_t>(r) * 3 * d;
-  // the new key
+  float qv[kDim], kv[kDim], vv[kDim];
+  load_bf16x<kDim>(row + h * HD + lane * kDim, qv);
+  load_bf16x<kDim>(row + d + h * HD + lane * kDim, kv);
+  load_bf16x<kDim>(row + 2 * d + h * HD + lane * kDim, vv);
   float qk = 0.f;
-  for (int i = lane; i < HD; i += 32) qk += bf(row[h * HD + i]) * bf(row[d + h * HD + i]);
+#pragma unroll
+  for (int t = 0; t < kDim; ++t) qk = fmaf(qv[t], kv[t], qk);
   qk = mtp::warp_sum(qk) * scale;
-  const float* rec0 = part + (static_cast<size_t>(r) * H + h) * n_chunks * (HD + 2);
+  const float* rec0 = part + (static_cast<size_t>(r) * H + h) * n_split * kRec;
   float m = qk;
-  for (int c = 0; c < n_chunks; ++c) m = fmaxf(m, rec0[c * (HD + 2)]);
-  float l = __expf(qk - m);
-  float o[kDim];
+  for (int c = lane; c < n_split; c += 32) m = fmaxf(m, rec0[static_cast<size_t>(c) * kRec]);
+  m = mtp::warp_max(m);
+  const float wn = __expf(qk - m);
+  float l = 0.f, o[kDim];
 #pragma unroll
-  for (int t = 0; t < kDim; ++t) o[t] = l * bf(row[2 * d + h * HD + lane * kDim + t]);
-  for (int c = 0; c < n_chunks; ++c) {
-    const float* rec = rec0 + c * (HD + 2);
-    if (rec[1] <= 0.f) continue;
-    const float w = __expf(rec[0] - m);
-    l += w * rec[1];
+  for (int t = 0; t < kDim; ++t) o[t] = wn * vv[t];
+  for (int cb = 0; cb < n_split; cb += 32) {
+    const int c = cb + lane;
+    float wc = 0.f;
+    if (c < n_split) {
+      const float mc = rec0[static_cast<size_t>(c) * kRec], lc = rec0[static_cast<size_t>(c) * kRec + 1];
+      if (lc > 0.f) {
+        wc = __expf(mc - m);
+        l += wc * lc;
+      }
+    }
+    const int nc = min(32, n_split - cb);
+#pragma unroll 8
+    for (int k = 0; k < nc; ++k) {
+      const float wk = __shfl_sync(0xffffffffu, wc, k);
+      if (wk != 0.f) {  // warp-uniform
+        float pv[kDim];
+        const float* src = rec0 + static_cast<size_t>(cb + k) * kRec + 2 + lane * kDim;
 #pragma unroll
-    for (int t = 0; t < kDim; ++t) o[t] += w * rec[2 + lane * kDim + t];
+        for (int t = 0; t < kDim; ++t) pv[t] = src[t];
+#pragma unroll
+        for (int t = 0; t < kDim; ++t) o[t] = fmaf(wk, pv[t], o[t]);
+      }
+    }
   }
+  l = mtp::warp_sum(l) + wn;
   const float inv = 1.0f / l;
+  __nv_bfloat16* dst = out + static_cast<size_t>(r) * d + h * HD + lane * kDim;
 #pragma unroll
-  for (int t = 0; t < kDim; ++t)
-    out[static_cast<size_t>(r) * d + h * HD + lane * kDim + t] = __float2bfloat16_rn(o[t] * inv);
+  for (int t = 0; t < kDim; ++t) dst[t] = __float2bfloat16_rn(o[t] * inv);
 }
 
 // ---------------------------------------------------------------------------
-// q = softmax(z) in place and y ~ q by inverse CDF; one CTA (1024 threads) per request
+// q = softmax(z) in place and y ~ q by inverse CDF.  A cluster of 8 CTAs
+// per request: CTA `rank` owns chunks [rank*cpc, rank*cpc + cpc) of 1024
+// vocabulary entries.  Pass A: online (max, sum exp) per CTA, combined in
+// CTA 0 through distributed shared memory.  Pass B: q written in place and
+// compensated (hi, lo) chunk sums pushed into CTA 0.  CTA 0 takes the fp64
+// prefix over chunks to find the chunk holding u * mass; the CTA owning that
+// chunk rescans it in index order for the smallest index whose running sum
+// exceeds the target.
 // ---------------------------------------------------------------------------
-constexpr int kSampleThreads = 1024;
+constexpr int kSampleCluster = 8;
+constexpr int kSampleThreads = 512;
 constexpr int kSampleChunk = 1024;
 constexpr int kMaxSampleChunks = 512;
 
-__global__ void __launch_bounds__(kSampleThreads)
+// (m, s) <- the pair describing the union of two sets, s = sum exp(x - m)
+__device__ __forceinline__ void merge_max_sum(float& m, float& s, float m2, float s2) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) return;
+  s = s * __expf(m - M) + s2 * __expf(m2 - M);
+  m = M;
+}
+
+__global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kSampleThreads)
 softmax_sample_kernel(float* __restrict__ q, int V, uint2 key, uint32_t off_lo, uint32_t off_hi,
                       int32_t* __restrict__ y_out) {
-  __shared__ float sh[32];
-  __shared__ float2 s_chunk[kMaxSampleChunks];
+  __shared__ float2 s_red[kSampleThreads / 32];
+  __shared__ float2 s_ms[kSampleCluster];         // CTA 0: (max, sum) of every CTA
+  __shared__ float2 s_chunk[kMaxSampleChunks];    // CTA 0: compensated chunk sums
   __shared__ float s_w[kSampleChunk];
   __shared__ int s_cstar;
   __shared__ double s_before, s_target;
-  const int r = blockIdx.x;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int r = blockIdx.x / kSampleCluster;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* z = q + static_cast<size_t>(r) * V;
-  float mx = -INFINITY;
-  for (int v = threadIdx.x; v < V; v += kSampleThreads) mx = fmaxf(mx, z[v]);
-  mx = block_max(mx, sh);
-  float sum = 0.f;
-  for (int v = threadIdx.x; v < V; v += kSampleThreads) sum += __expf(z[v] - mx);
-  sum = block_sum(sum, sh);
-  const float inv = 1.0f / sum;
-  __syncthreads();
-  // write q and compensated per-chunk sums (chunk c = [c*1024, c*1024+1024), warp-strided)
   const int n_chunks = (V + kSampleChunk - 1) / kSampleChunk;
-  for (int c = warp; c < n_chunks; c += kSampleThreads / 32) {
+  const int cpc = (n_chunks + kSampleCluster - 1) / kSampleCluster;
+  const int c0 = min(n_chunks, rank * cpc), c1 = min(n_chunks, c0 + cpc);
+  const int v0 = c0 * kSampleChunk, v1 = min(V, c1 * kSampleChunk);
+
+  // pass A: online max / sum-exp
+  float m = -INFINITY, sm = 0.f;
+  for (int v = v0 + threadIdx.x; v < v1; v += kSampleThreads) {
+    const float x = z[v];
+    if (x > m) {
+      sm = sm * __expf(m - x) + 1.f;
+      m = x;
+    } else {
+      sm += __expf(x - m);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    merge_max_sum(m, sm, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, sm, o));
+  if (lane == 0) s_red[warp] = make_float2(m, sm);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kSampleThreads / 32; ++w) merge_max_sum(m, sm, s_red[w].x, s_red[w].y);
+    *cluster.map_shared_rank(&s_ms[rank], 0) = make_float2(m, sm);
+  }
+  cluster.sync();
+  float M = -INFINITY, S = 0.f;
+  {
+    const float2* all = cluster.map_shared_rank(s_ms, 0);
+#pragma unroll
+    for (int k = 0; k < kSampleCluster; ++k) {
+      const float2 t = all[k];
+      merge_max_sum(M, S, t.x, t.y);
+    }
+  }
+  const float inv = 1.0f / S;
+
+  // pass B: q in place and compensated chunk sums (warp per chunk)
+  float2* chunk0 = cluster.map_shared_rank(s_chunk, 0);
+  for (int c = c0 + warp; c < c1; c += kSampleThreads / 32) {
     float hi = 0.f, lo = 0.f;
     for (int i = lane; i < kSampleChunk; i += 32) {
       const int v = c * kSampleChunk + i;
       if (v < V) {
-        const float pv = __expf(z[v] - mx) * inv;
+        const float pv = __expf(z[v] - M) * inv;
         z[v] = pv;
-        float s, e;
-        two_sum(hi, pv, s, e);
-        hi = s;
+        float t, e;
+        two_sum(hi, pv, t, e);
+        hi = t;
         lo += e;
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ohi = __shfl_xor_sync(0xffffffffu, hi, o), olo = __shfl_xor_sync(0xffffffffu, lo, o);
-      float s, e;
-      two_sum(hi, ohi, s, e);
-      hi = s;
+      float t, e;
+      two_sum(hi, ohi, t, e);
+      hi = t;
       lo = (lo + olo) + e;
     }
-    if (lane == 0) s_chunk[c] = make_float2(hi, lo);
+    if (lane == 0) chunk0[c] = make_float2(hi, lo);
   }
-  __syncthreads();
-  const uint4 w = philox4x32_10(make_uint4(0u, static_cast<uint32_t>(r), off_lo, off_hi), key);
-  const double u = static_cast<double>(w.z >> 8) * (1.0 / 16777216.0);
-  if (warp == 0) {
+  cluster.sync();
+
+  // CTA 0: the chunk holding u * mass
+  if (rank == 0 && warp == 0) {
+    const uint4 w = philox4x32_10(make_uint4(0u, static_cast<uint32_t>(r), off_lo, off_hi), key);
+    const double u = static_cast<double>(w.z >> 8) * (1.0 / 16777216.0);
     const int per = (n_chunks + 31) / 32;
     double own = 0.0;
     for (int c = lane * per; c < min(n_chunks, (lane + 1) * per); ++c)
@@ -536,14 +673,17 @@ softmax_sample_kernel(float* __restrict__ q, int V, uint2 key, uint32_t off_lo, 
       s_cstar = cstar;
       s_before = before;
       s_target = target;
+      if (cstar < 0) y_out[r] = -1;
     }
   }
-  __syncthreads();
-  const int cstar = s_cstar;
-  if (cstar < 0) {
-    if (threadIdx.x == 0) y_out[r] = -1;
-    return;
-  }
+  cluster.sync();
+  const int cstar = *cluster.map_shared_rank(&s_cstar, 0);
+  const double before = *cluster.map_shared_rank(&s_before, 0);
+  const double target = *cluster.map_shared_rank(&s_target, 0);
+  // CTA 0's shared memory is read above; nobody touches it after this barrier
+  cluster.sync();
+  if (cstar < 0 || cstar / cpc != rank) return;
+  // the owning CTA rescans the chosen chunk (its own writes of pass B)
   for (int i = threadIdx.x; i < kSampleChunk; i += kSampleThreads) {
     const int v = cstar * kSampleChunk + i;
     s_w[i] = v < V ? z[v] : 0.f;
@@ -558,8 +698,7 @@ softmax_sample_kernel(float* __restrict__ q, int V, uint2 key, uint32_t off_lo, 
     llo += e;
   }
   const double lane_sum = static_cast<double>(lhi) + static_cast<double>(llo);
-  const double lincl = mtp::warp_inclusive_scan(lane_sum) + s_before;
-  const double target = s_target;
+  const double lincl = mtp::warp_inclusive_scan(lane_sum) + before;
   const unsigned lover = __ballot_sync(0xffffffffu, lincl > target);
   const unsigned lpos = __ballot_sync(0xffffffffu, lane_sum > 0.0);
   const int lsrc = lover ? __ffs(lover) - 1 : (lpos ? 31 - __clz(lpos) : 0);
@@ -691,7 +830,8 @@ extern "C" mtp_status mtp_draft_step(const mtp_dims* dims, const mtp_weights* w,
                                 w->wo, w->ffn_norm, w->w_gate, w->w_up, w->w_down};
   for (auto l : lists)
     if (!l || !l[0] || !mtp::aligned16(l[0])) return l && l[0] ? MTP_ERR_ALIGNMENT : MTP_ERR_INVALID_ARG;
-  const void* ptrs[] = {parent_hidden, kv_k, kv_v, static_cast<const void*>(q_out), ws, w->embed, w->head};
+  const void* ptrs[] = {parent_hidden, kv_k, kv_v, static_cast<const void*>(q_out), ws, w->embed, w->head,
+                        w->out_norm};
   for (const void* p : ptrs)
     if (!mtp::aligned16(p)) return MTP_ERR_ALIGNMENT;
   if (h_out && !mtp::aligned16(h_out)) return MTP_ERR_ALIGNMENT;
@@ -707,10 +847,10 @@ extern "C" mtp_status mtp_draft_step(const mtp_dims* dims, const mtp_weights* w,
   __nv_bfloat16 *c = bfp(L.c), *u = bfp(L.u), *x = bfp(L.x), *qkv = bfp(L.qkv), *o = bfp(L.o), *a = bfp(L.a),
                 *g = bfp(L.g);
   __nv_bfloat16* h = h_out ? static_cast<__nv_bfloat16*>(h_out) : bfp(L.h);
-  const int fin_threads = 256;
+  const int fin_threads = kRowThreads;
 
   // c, u = M c, x = RMSNorm_a(u)
-  draft_prologue_kernel<<<R, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(parent_hidden), frontier, E,
+  draft_prologue_kernel<<<R, kRowThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(parent_hidden), frontier, E,
                                            W0(w->hnorm), W0(w->enorm), c, d, V, D.eps);
   mtp::note_launch();
   MTP_CUDA_TRY(cudaMemsetAsync(acc, 0, static_cast<size_t>(R) * d * 4, st));
@@ -722,7 +862,7 @@ extern "C" mtp_status mtp_draft_step(const mtp_dims* dims, const mtp_weights* w,
   TRY(skinny_gemm(W0(w->wq), d, d, x, R, acc, 3 * d, st));
   TRY(skinny_gemm(W0(w->wk), d, d, x, R, acc + d, 3 * d, st));
   TRY(skinny_gemm(W0(w->wv), d, d, x, R, acc + 2 * d, 3 * d, st));
-  finish_qkv_kernel<<<dim3((d + 255) / 256, R), 256, 0, st>>>(acc, qkv, pos, d, hd, D.rope_base, D.T);
+  finish_qkv_kernel<<<dim3((d + kQkvCols - 1) / kQkvCols, R), 256, 0, st>>>(acc, qkv, pos, d, hd, D.rope_base, D.T);
   mtp::note_launch();
   // attention over the module's own cache plus the new row
   const float scale = 1.0f / sqrtf(static_cast<float>(hd));
@@ -787,7 +927,7 @@ extern "C" mtp_status mtp_draft_step(const mtp_dims* dims, const mtp_weights* w,
   TRY(skinny_gemm(static_cast<const __nv_bfloat16*>(w->head), V, d, x, R, q_out, V, st, true));
   mtp::prof_end(MTP_KC_HEAD_CE_GEMM, st);
   const uint2 key = make_uint2(static_cast<uint32_t>(seed & 0xFFFFFFFFu), static_cast<uint32_t>(seed >> 32));
-  softmax_sample_kernel<<<R, kSampleThreads, 0, st>>>(q_out, V, key, static_cast<uint32_t>(offset & 0xFFFFFFFFu),
+  softmax_sample_kernel<<<R * kSampleCluster, kSampleThreads, 0, st>>>(q_out, V, key, static_cast<uint32_t>(offset & 0xFFFFFFFFu),
                                                       static_cast<uint32_t>(offset >> 32), y_out);
   mtp::note_launch();
   MTP_LAUNCH_CHECK();
