@@ -239,12 +239,19 @@ __global__ void finish_swiglu_kernel(const float* __restrict__ acc, __nv_bfloat1
 // Decode attention over the module's K/V cache, streamed by TMA.
 // Persistent CTAs (one per SM) walk work units u -> (head h, key split sp,
 // request r), heads fastest so that concurrently running units read
-// neighbouring 256-byte pieces of the same cache rows.  A producer warp
-// streams [64 keys x head_dim] tiles of K and V into a shared-memory ring;
-// each of the 8 consumer warps takes 8 keys of every tile (so every consumer
-// waits on every ring phase in order) and keeps its own online-softmax state
-// (m, l, o); at the end of a unit the warps' states are merged into one
-// record part[r, h, sp] = (max, sum, o[head_dim]).
+// neighbouring pieces of the same cache rows.  A producer warp streams
+// [64 keys x head_dim] tiles of K and V into a shared-memory ring as
+// [64 x 64] boxes with the 128-byte swizzle; each of the 8 consumer warps
+// takes 8 keys of every tile (so every consumer waits on every ring phase in
+// order) and keeps its own online-softmax state.  Both products run on
+// mma.sync.m16n8k16 with the single query as the one real row of the 16-row
+// operand: scores S[1 x 8] = q K^T (K rows loaded by ldmatrix as the
+// column-major B operand) and O[1 x hd] += P V (V by ldmatrix.trans); the
+// score accumulator's lanes 0-3 already hold P in the A-operand layout.  P
+// enters the P V product as two bf16 rows, p_hi = bf16(p) and
+// p_lo = bf16(p - p_hi), whose output rows are added once per unit, so the
+// weights are exact to ~2^-17 relative.  At the end of a unit the warps' (m, l, o) states merge
+// into one record part[r, h, sp] = (max, sum, o[head_dim]).
 // ---------------------------------------------------------------------------
 constexpr int kAttnTileKeys = 64;
 constexpr int kAttnWarps = 8;
@@ -252,44 +259,17 @@ constexpr int kAttnKeysPerWarp = kAttnTileKeys / kAttnWarps;
 constexpr int kAttnThreads = (kAttnWarps + 1) * 32;
 constexpr int kAttnRingBytes = 192 * 1024;
 constexpr int kAttnSplitKeys = 1024;  // target keys per work unit
-static_assert(kAttnKeysPerWarp == 8, "the transposed reduction below is written for 8 keys per warp");
+constexpr int kAttnBoxBytes = kAttnTileKeys * 64 * 2;  // [64 keys x 64 dims] bf16, 128-byte swizzled
+static_assert(kAttnKeysPerWarp == 8, "one n8 MMA tile of keys per warp");
 
 template <int HD>
 struct AttnCfg {
-  static constexpr int kTileBytes = kAttnTileKeys * HD * 2;
-  static constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
+  static constexpr int kBoxes = HD / 64;                   // boxes per K (or V) tile
+  static constexpr int kTileBytes = kBoxes * kAttnBoxBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;       // K tile then V tile
   static constexpr int kStages = kAttnRingBytes / kStageBytes;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
 };
-
-// v[j] holds this lane's partial dot product for key j of the warp's 8 keys
-// (lanes own head_dim slices).  Reduce-scatter over the warp: 4 + 2 + 1
-// exchanges halve the keys held, two more finish the sums.  Lane l ends with
-// the full dot product of key 4*bit4(l) + 2*bit3(l) + bit2(l).
-__device__ __forceinline__ float reduce8_transposed(const float (&v)[8], int lane) {
-  const bool b16 = lane & 16, b8 = lane & 8, b4 = lane & 4;
-  float a[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float send = b16 ? v[i] : v[i + 4];
-    const float keep = b16 ? v[i + 4] : v[i];
-    a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-  }
-  float c[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float send = b8 ? a[i] : a[i + 2];
-    const float keep = b8 ? a[i + 2] : a[i];
-    c[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-  }
-  const float send = b4 ? c[0] : c[1];
-  float e = (b4 ? c[1] : c[0]) + __shfl_xor_sync(0xffffffffu, send, 4);
-  e += __shfl_xor_sync(0xffffffffu, e, 2);
-  e += __shfl_xor_sync(0xffffffffu, e, 1);
-  return e;
-}
-__device__ __forceinline__ int key_of_lane(int lane) { return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1); }
-__device__ __forceinline__ int lane_of_key(int j) { return ((j >> 2) & 1) * 16 + ((j >> 1) & 1) * 8 + (j & 1) * 4; }
 
 template <int KD>
 __device__ __forceinline__ void load_bf16x(const void* p, float (&f)[KD]) {
@@ -304,6 +284,32 @@ __device__ __forceinline__ void load_bf16x(const void* p, float (&f)[KD]) {
   }
 }
 
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// c += A(16x16, row) * B(16x8, col), bf16 in, fp32 accumulate; A rows 8..15 are zero here
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+// shared address of 16-byte row piece (row, col..col+7) of a [64 x 64] box with the 128-byte swizzle
+__device__ __forceinline__ uint32_t swz(uint32_t box, int row, int col) {
+  return box + row * 128 + ((((col >> 3) ^ row) & 7) << 4);
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 decode_attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -311,7 +317,8 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                    float* __restrict__ part, int H, int T, int n_split, int split_keys, int n_units, float scale) {
   using C = AttnCfg<HD>;
   constexpr int S = C::kStages;
-  constexpr int kDim = HD / 32;
+  constexpr int kKSteps = HD / 16;  // score MMAs per 8 keys
+  constexpr int kNTiles = HD / 8;   // P V MMAs per 8 keys
   extern __shared__ uint8_t attn_smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * S];
   __shared__ float s_m[2][kAttnWarps], s_l[2][kAttnWarps];
@@ -362,8 +369,11 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
           const uint32_t full = full0 + 8u * slot;
           const uint32_t dst = ring_s + slot * C::kStageBytes;
           mtp::mbar_expect_tx(full, C::kStageBytes);
-          mtp::tma_tile_2d(dst, &tmK, h * HD, r * T + s, full);
-          mtp::tma_tile_2d(dst + C::kTileBytes, &tmV, h * HD, r * T + s, full);
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx) {
+            mtp::tma_tile_2d(dst + bx * kAttnBoxBytes, &tmK, h * HD + bx * 64, r * T + s, full);
+            mtp::tma_tile_2d(dst + C::kTileBytes + bx * kAttnBoxBytes, &tmV, h * HD + bx * 64, r * T + s, full);
+          }
         }
         __syncwarp();
         ++g;
@@ -385,19 +395,31 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   }
 
   // ------------------------------ consumers ------------------------------
+  // lanes 0-3 carry the real row of every fragment: key pair 2t, 2t+1 of the
+  // warp's 8 keys, head_dim pairs 8j + 2t, 8j + 2t + 1 of the output
+  const int t4 = lane & 3;
+  const bool row0 = lane < 4;
+  const int key_row = warp * kAttnKeysPerWarp + (lane & 7);  // ldmatrix row address of this lane
+  const int col_sel = 8 * (lane >> 3);                       // ... and its column offset in a 32-column group
   uint32_t g = 0;
   int k = 0;
-  const int jkey = key_of_lane(lane);
   for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++k) {
     int r, h, sp, lo, hi;
     unit(u, r, h, sp, lo, hi);
-    float qv[kDim];
-    load_bf16x<kDim>(qkv + static_cast<size_t>(r) * 3 * d + h * HD + lane * kDim, qv);
+    // q as the A operand: row 0 real (lanes 0-3), pairs 16kk + 2t (a0) and 16kk + 8 + 2t (a2)
+    uint32_t qa[kKSteps][2];
+    {
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qkv + static_cast<size_t>(r) * 3 * d + h * HD);
 #pragma unroll
-    for (int t = 0; t < kDim; ++t) qv[t] *= scale;
-    float m = -INFINITY, l = 0.f, o[kDim];
+      for (int kk = 0; kk < kKSteps; ++kk) {
+        qa[kk][0] = row0 ? qrow[8 * kk + t4] : 0u;
+        qa[kk][1] = row0 ? qrow[8 * kk + 4 + t4] : 0u;
+      }
+    }
+    float m = -INFINITY, l = 0.f;
+    float o[kNTiles][4];
 #pragma unroll
-    for (int t = 0; t < kDim; ++t) o[t] = 0.f;
+    for (int j = 0; j < kNTiles; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
     for (int s = lo; s < hi; s += kAttnTileKeys, ++g) {
       const uint32_t slot = g % S, use = g / S;
       // the skip decision is warp-uniform (lane 0's view of the flag)
@@ -410,40 +432,63 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         skip = true;
       }
       if (skip) continue;
-      const uint8_t* tk = ring + slot * C::kStageBytes + warp * kAttnKeysPerWarp * HD * 2 + lane * kDim * 2;
-      const uint8_t* tv = tk + C::kTileBytes;
-      float part_dot[kAttnKeysPerWarp];
+      const uint32_t kbase = ring_s + slot * C::kStageBytes, vbase = kbase + C::kTileBytes;
+      // scores: two independent accumulation chains over the head_dim steps
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-      for (int j = 0; j < kAttnKeysPerWarp; ++j) {
-        float kv[kDim];
-        load_bf16x<kDim>(tk + j * HD * 2, kv);
-        float acc = 0.f;
-#pragma unroll
-        for (int t = 0; t < kDim; ++t) acc = fmaf(qv[t], kv[t], acc);
-        part_dot[j] = acc;
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t b[4];
+        const int col = 32 * c + col_sel;
+        ldsm_x4(swz(kbase + (col >> 6) * kAttnBoxBytes, key_row, col & 63), b);
+        mma_16816(sc[0], qa[2 * c][0], qa[2 * c][1], b[0], b[1]);
+        mma_16816(sc[1], qa[2 * c + 1][0], qa[2 * c + 1][1], b[2], b[3]);
       }
-      const float dot = reduce8_transposed(part_dot, lane);
-      const bool valid = s + warp * kAttnKeysPerWarp + jkey < hi;
-      const float score = valid ? dot : -INFINITY;
-      const float m_new = fmaxf(m, mtp::warp_max(score));
-      if (m_new != -INFINITY) {  // warp-uniform
-        const float alpha = __expf(m - m_new);
-        const float p = valid ? __expf(score - m_new) : 0.f;
-        l = l * alpha + mtp::warp_sum((lane & 3) == 0 ? p : 0.f);
+      const int key0 = s + warp * kAttnKeysPerWarp + 2 * t4;
+      const float s0 = key0 < hi ? (sc[0][0] + sc[1][0]) * scale : -INFINITY;
+      const float s1 = key0 + 1 < hi ? (sc[0][1] + sc[1][1]) * scale : -INFINITY;
+      float mx = fmaxf(s0, s1);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m, __shfl_sync(0xffffffffu, mx, 0));  // warp-uniform
+      if (m_new != -INFINITY) {
+        if (m_new > m) {
+          const float alpha = __expf(m - m_new);
+          l *= alpha;
 #pragma unroll
-        for (int t = 0; t < kDim; ++t) o[t] *= alpha;
-#pragma unroll
-        for (int j = 0; j < kAttnKeysPerWarp; ++j) {
-          const float pj = __shfl_sync(0xffffffffu, p, lane_of_key(j));
-          float vv[kDim];
-          load_bf16x<kDim>(tv + j * HD * 2, vv);
-#pragma unroll
-          for (int t = 0; t < kDim; ++t) o[t] = fmaf(pj, vv[t], o[t]);
+          for (int j = 0; j < kNTiles; ++j) {
+            o[j][0] *= alpha;
+            o[j][1] *= alpha;
+          }
+          m = m_new;
         }
-        m = m_new;
+        // P = p_hi + p_lo (two bf16 parts, ~2^-17 relative): row 0 of the A
+        // operand carries p_hi (lanes 0-3), row 1 carries p_lo (lanes 4-7)
+        const float p0 = __expf(s0 - m), p1 = __expf(s1 - m);
+        const uint32_t ph = pack_bf16x2(p0, p1);
+        const float2 phf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ph));
+        const uint32_t pl = __shfl_sync(0xffffffffu, pack_bf16x2(p0 - phf.x, p1 - phf.y), lane & 3);
+        l += p0 + p1;
+        const uint32_t pa = row0 ? ph : (lane < 8 ? pl : 0u);
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t b[4];
+          const int col = 32 * c + col_sel;
+          ldsm_x4_t(swz(vbase + (col >> 6) * kAttnBoxBytes, key_row, col & 63), b);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) mma_16816(o[4 * c + i], pa, 0u, b[i], 0u);
+        }
       }
       __syncwarp();
       if (lane == 0) mtp::mbar_arrive_cnt(empty0 + 8u * slot, 1);
+    }
+    // this warp's sum over its keys lives in lanes 0-3; its output in rows 0
+    // (lanes 0-3, p_hi part) and 1 (lanes 4-7, p_lo part) of the accumulators
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+#pragma unroll
+    for (int j = 0; j < kNTiles; ++j) {
+      o[j][0] += __shfl_xor_sync(0xffffffffu, o[j][0], 4);
+      o[j][1] += __shfl_xor_sync(0xffffffffu, o[j][1], 4);
     }
     // merge the 8 warps' states of this unit (double-buffered: one barrier per unit)
     const int b = k & 1;
@@ -451,8 +496,13 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       s_m[b][warp] = m;
       s_l[b][warp] = l;
     }
+    if (row0) {
 #pragma unroll
-    for (int t = 0; t < kDim; ++t) s_o[b][warp][lane * kDim + t] = o[t];
+      for (int j = 0; j < kNTiles; ++j) {
+        s_o[b][warp][8 * j + 2 * t4] = o[j][0];
+        s_o[b][warp][8 * j + 2 * t4 + 1] = o[j][1];
+      }
+    }
     asm volatile("bar.sync 1, %0;" ::"n"(kAttnWarps * 32) : "memory");
     if (threadIdx.x < HD) {
       float M = -INFINITY;
@@ -876,8 +926,8 @@ extern "C" mtp_status mtp_draft_step(const mtp_dims* dims, const mtp_weights* w,
   CUtensorMap tmk, tmv;
   const uint64_t cache_rows = static_cast<uint64_t>(R) * D.T;
   if (cache_rows > 0x7FFFFFFFull) return MTP_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
-  if (!mtp::tensor_map_bf16_2d(&tmk, kc, cache_rows, d, d, hd, kAttnTileKeys) ||
-      !mtp::tensor_map_bf16_2d(&tmv, vc, cache_rows, d, d, hd, kAttnTileKeys))
+  if (!mtp::tensor_map_bf16_2d(&tmk, kc, cache_rows, d, d, 64, kAttnTileKeys, true) ||
+      !mtp::tensor_map_bf16_2d(&tmv, vc, cache_rows, d, d, 64, kAttnTileKeys, true))
     return MTP_ERR_CUDA;
   mtp::prof_begin(MTP_KC_ATTENTION, st);
   if (hd == 128) {

@@ -57,9 +57,10 @@ int gemm_ce_tile_n();
 mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream);
 
 // Tensor map of a row-major bf16 matrix [rows, cols] (row stride ld
-// elements, a multiple of 8) for tiled loads of box_cols x box_rows without
-// swizzle; false if the encoder is unavailable or rejects the description.
+// elements, a multiple of 8) for tiled loads of box_cols x box_rows, either
+// unswizzled or with the 128-byte swizzle (box_cols * 2 <= 128); false if
+// the encoder is unavailable or rejects the description.
 bool tensor_map_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
-                        uint32_t box_cols, uint32_t box_rows);
+                        uint32_t box_cols, uint32_t box_rows, bool swizzle128);
 
 }  // namespace mtp
