@@ -27,6 +27,7 @@ before the loss is assembled.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -58,6 +59,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--draft-steps", type=int, default=30)
+    ap.add_argument("--draft-requests", type=int, default=32,
+                    help="requests of the draft-step section (32 = the measured workload; fewer for profiling)")
     return ap.parse_args()
 
 
@@ -452,6 +455,8 @@ def measure_draft(args, dev, rank, peaks):
     if args.draft_steps <= 0:
         return None
     cfg = synth.DRAFT_C5
+    if args.draft_requests != cfg.R:
+        cfg = dataclasses.replace(cfg, name=f"{cfg.name}_R{args.draft_requests}", R=args.draft_requests)
     inp = synth.make_draft_inputs(cfg, 11 + rank, device=dev)
     step = lib.DraftStep(cfg, inp["weights"], device=dev)
     vcfg = synth.VerifyConfig(name="verify_R32_g1", R=cfg.R, gamma=1, V=cfg.V)
@@ -495,7 +500,7 @@ def measure_draft(args, dev, rank, peaks):
     total = weight_bytes + head_bytes + cache_bytes + q_bytes
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     gbs = total / (d_ms / 1e3) / 1e9
-    return {"workload": "draft step R=32, cache 8192 x d=7168 (56x128), ffn 18432, V=129280 + gamma=1 verify",
+    return {"workload": f"draft step R={cfg.R}, cache 8192 x d=7168 (56x128), ffn 18432, V=129280 + gamma=1 verify",
             "ms_median": d_ms, "verify_ms_median": v_ms, "algorithmic_bytes": total,
             "achieved_gbs": gbs, "peak_gbs": hbm_peak, "frac": gbs / hbm_peak,
             "bound": "hbm", "steps": n, "l2": "flushed before every timed call (256 MiB written then read)"}
