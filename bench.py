@@ -59,6 +59,7 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--draft-steps", type=int, default=30)
+    ap.add_argument("--c3-steps", type=int, default=4, help="timed calls of the DeepSeek-V3-width section (0 = off)")
     ap.add_argument("--draft-requests", type=int, default=32,
                     help="requests of the draft-step section (32 = the measured workload; fewer for profiling)")
     return ap.parse_args()
@@ -325,7 +326,7 @@ def run_ours(args):
     timers = {name: lib.KernelTimer(name, launches * K)
               for name, launches in (("head_ce_gemm", cfg.D + 1), ("gate_up_gemm", cfg.D), ("down_gemm", cfg.D),
                                      ("qkv_gemm", cfg.D), ("o_gemm", cfg.D), ("proj_gemm", cfg.D),
-                                     ("attention", cfg.D), ("spec_verify", 1))}
+                                     ("attention", cfg.D), ("spec_verify", 1), ("prologue", cfg.D))}
     torch.cuda.synchronize()
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -399,6 +400,10 @@ def run_ours(args):
         if name == "head_ce_gemm":
             entry["tflops"] = achieved
             entry["frac_of_peak"] = achieved / peak
+        if name == "prologue":  # gather E[x_{t+k}], read h^{k-1}, write c = [h; e] normalised: 8 d bytes per row
+            hbm = float(load_peaks()[0].get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+            entry["gbs"] = 8.0 * cfg.d * state_rows / (tot / 1e3) / 1e9 if tot > 0 else None
+            entry["frac_of_hbm"] = entry["gbs"] / hbm if entry["gbs"] else None
         breakdown[name] = entry
 
     # spec_verify: rows/s and algorithmic HBM bytes (decision scalars + the one sampled row pair or row)
@@ -420,6 +425,8 @@ def run_ours(args):
 
     # decode-shaped draft step (its own workload, measured beside the step)
     draft = measure_draft(args, dev, rank, peaks)
+    # DeepSeek-V3-width single depth (its own workload, measured beside the step)
+    dsv3 = measure_dsv3(args, dev, rank, peaks)
 
     # end to end through the public API: pinned host inputs -> device, result -> host, every step
     e2e = measure_e2e(cfg, vcfg, chain, batch, x, vin, args.e2e_steps, dev, rank, world, tokens_per_step)
@@ -433,7 +440,7 @@ def run_ours(args):
                 "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic (seeded; random-init weights of the workload's shapes)",
                 "config": workload_config(), "roofline": roofline, "spec_verify": verify,
-                "spec_verify_rows_per_s": verify["rows_per_s"], "kernels": breakdown, "draft_step": draft,
+                "spec_verify_rows_per_s": verify["rows_per_s"], "kernels": breakdown, "draft_step": draft, "dsv3_width": dsv3,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
                 "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
                 "clock_samples": clk["samples"], "wall_s_timed_region": t_wall,
@@ -504,6 +511,72 @@ def measure_draft(args, dev, rank, peaks):
             "ms_median": d_ms, "verify_ms_median": v_ms, "algorithmic_bytes": total,
             "achieved_gbs": gbs, "peak_gbs": hbm_peak, "frac": gbs / hbm_peak,
             "bound": "hbm", "steps": n, "l2": "flushed before every timed call (256 MiB written then read)"}
+
+
+def measure_dsv3(args, dev, rank, peaks):
+    """mtp_chain_loss on the DeepSeek-V3-width workload (B=1, T=4096, d=7168,
+    56x128 heads, ffn 18432, V=129280, D=1, main + depth head): tokens/s and
+    each GEMM class's TFLOP/s against the measured sustained bf16 peak.
+    Algorithmic FLOPs count rows with state (T-1 at depth 1) and, for the
+    heads, the supervised rows.  L2 flushed before every timed call."""
+    import torch
+
+    from deepseek_sequential_mtp_gb300 import lib, synth
+
+    if args.c3_steps <= 0:
+        return None
+    cfg = synth.DSV3_BF16
+    seed = 21 + rank
+    batch = synth.make_batch(cfg, seed)
+    x = {k: torch.from_numpy(v).to(dev) for k, v in batch.items()}
+    h0 = synth.make_h0(cfg, seed, device=dev)
+    chain = lib.Chain(cfg, synth.make_weights(cfg, seed + 1, device=dev), device=dev)
+    out = {"sums_counts": torch.empty(2 * (cfg.D + 1), dtype=torch.float64, device=dev),
+           "losses": torch.empty(cfg.D + 2, dtype=torch.float32, device=dev)}
+    flush = L2Flush(dev)
+
+    def call():
+        chain.loss(x["tokens"], x["seg"], x["pos"], h0, den="fixed", with_main=True, out=out)
+
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    lib.check_errors()
+    n = args.c3_steps
+    classes = ("head_ce_gemm", "gate_up_gemm", "down_gemm", "qkv_gemm", "o_gemm", "proj_gemm", "attention",
+               "prologue")
+    timers = {c: lib.KernelTimer(c, n * (cfg.D + 1)) for c in classes}
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for t in timers.values():
+        t.arm()
+    for i in range(n):
+        flush()
+        ev[i][0].record()
+        call()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    lib.KernelTimer.disarm_all()
+    lib.check_errors()
+    ms = sorted(a.elapsed_time(b) for a, b in ev)[n // 2]
+    counts = out["sums_counts"][1::2].cpu().numpy()
+    rows = float(sum(cfg.B * (cfg.T - k) for k in range(1, cfg.D + 1)))
+    d, f, V = cfg.d, cfg.ffn, cfg.V
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    flops = {"head_ce_gemm": 2.0 * d * V * float(counts.sum()), "gate_up_gemm": 4.0 * d * f * rows,
+             "down_gemm": 2.0 * d * f * rows, "qkv_gemm": 6.0 * d * d * rows, "o_gemm": 2.0 * d * d * rows,
+             "proj_gemm": 4.0 * d * d * rows}
+    kernels = {}
+    for c, t in timers.items():
+        tot = sum(t.durations_ms()) / n
+        e = {"ms_per_call": tot}
+        if c in flops and tot > 0:
+            e["tflops"] = flops[c] / (tot / 1e3) / 1e12
+            e["frac_of_peak"] = e["tflops"] / peak
+        kernels[c] = e
+    return {"workload": "mtp_chain dsv3_width_D1 (B=1, T=4096, d=7168, 56x128 heads, ffn 18432, V=129280, "
+                        "one packed boundary at 2048, main + depth-1 heads)",
+            "tokens_per_s": rows / (ms / 1e3), "ms_per_call": ms, "steps": n, "kernels": kernels,
+            "peak_tflops": peak, "l2": "flushed before every timed call (256 MiB written then read)"}
 
 
 def measure_e2e(cfg, vcfg, chain, batch, x, vin, steps, dev, rank, world, tokens_per_step):

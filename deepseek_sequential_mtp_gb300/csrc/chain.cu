@@ -694,6 +694,7 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
     const int i = k - 1;
     T* h_k = h_out ? h_out + static_cast<size_t>(i) * Md : C.buf<T>((k & 1) ? C.L.h1buf : C.L.h0buf);
     auto wt = [&](const void* const* arr) { return static_cast<const T*>(arr[i]); };
+    mtp::prof_begin(MTP_KC_PROLOGUE, C.st);
     if constexpr (sizeof(T) == 2) {
       prologue_bf16_kernel<<<warp_blocks(M), 256, 0, C.st>>>(
           reinterpret_cast<const uint4*>(h_prev), C.tokens, static_cast<const uint4*>(C.W.embed),
@@ -703,6 +704,7 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
       prologue_kernel<T><<<warp_blocks(M), 256, 0, C.st>>>(h_prev, C.tokens, static_cast<const T*>(C.W.embed),
                                                            wt(C.W.hnorm), wt(C.W.enorm), c, M, D.T, d, D.V, k, D.eps);
     }
+    mtp::prof_end(MTP_KC_PROLOGUE, C.st);
     mtp::note_launch();
     MTP_LAUNCH_CHECK();
     const T* proj[1] = {wt(C.W.eh_proj)};

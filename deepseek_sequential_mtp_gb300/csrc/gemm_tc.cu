@@ -15,9 +15,10 @@
 //              reads TMEM lanes 32*(w%4)..+31 = tile rows), applies the fused
 //              operation and writes each 32-row x 64-column bf16 box into a
 //              128-byte-swizzled shared-memory buffer (two per warp) that one
-//              lane ships with a TMA store; residual boxes arrive by TMA load
-//              into the same buffer.  The CE epilogue stores only per-row
-//              partials.
+//              lane ships with a TMA store.  The residual is read into
+//              registers from global memory: the tile's first two 64-column
+//              pieces while its MMAs still run, later pieces two ahead.  The
+//              CE epilogue stores only per-row partials.
 // Every mbarrier wait is bounded: after ~1.5 s it sets MTP_DEVERR_TIMEOUT,
 // raises a CTA abort flag and every role drains out; the producer then waits
 // (bounded) for its in-flight copies and warp 1 for its MMAs before freeing
@@ -237,6 +238,39 @@ __device__ __forceinline__ void box_add32(const uint8_t* box, int lane, int half
     }
   }
 }
+// 64 residual columns [col0, col0 + 64) of one row as 8 x (8 bf16); zero outside [0, M) x [0, N)
+__device__ __forceinline__ void load_res64(uint4 (&r)[8], const __nv_bfloat16* resid, int ldr, int M, int N, int row,
+                                           int col0) {
+  const __nv_bfloat16* src = resid + static_cast<size_t>(row) * ldr + col0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int col = col0 + 8 * k;
+    r[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (row < M && col + 8 <= N) {
+      r[k] = __ldg(reinterpret_cast<const uint4*>(src + 8 * k));
+    } else if (row < M && col < N) {  // ragged right edge: element by element
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (col + i < N)
+          w[i >> 1] |= static_cast<uint32_t>(__bfloat16_as_ushort(src[8 * k + i])) << (16 * (i & 1));
+      r[k] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+// v[i] += residual column 32*half + i (pieces 4*half .. 4*half + 3)
+__device__ __forceinline__ void add_res32(float (&v)[32], const uint4 (&r)[8], int half) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r[4 * half + q]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      v[8 * q + 2 * i] += f.x;
+      v[8 * q + 2 * i + 1] += f.y;
+    }
+  }
+}
 // 32 (cos, sin) pairs of one RoPE table row, 16-byte loads
 __device__ __forceinline__ void load_cs32(const float2* tab, float2 (&cs)[32]) {
   const float4* t4 = reinterpret_cast<const float4*>(tab);
@@ -260,7 +294,7 @@ template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
-               const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmRes,
+               const __grid_constant__ CUtensorMap tmOut,
                const Args P) {
   using C = Cfg<BN, EPI>;
   constexpr int S = C::kStages;
@@ -277,7 +311,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
   const uint32_t final_bar = bar0 + 8u * (2 * S + 4);
-  auto res_bar = [&](int e, int b) { return bar0 + 8u * (2 * S + 5 + 2 * e + b); };  // residual box loads
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -292,7 +325,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       mbar_init(tempty_bar(a), 128);
     }
     mbar_init(final_bar, 1);
-    for (int i = 0; i < 8; ++i) mbar_init(res_bar(i >> 1, i & 1), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -389,8 +421,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int ew = warp - 2;       // epilogue warp index: owns two staging boxes
     uint8_t* boxes = staging + ew * 2 * C::kBoxBytes;
     int nb = 0;                        // next staging box
-    uint32_t res_phase = 0;            // bit b: parity of box b's residual barrier
-    bool res_pending[2] = {false, false};
     int local = 0;
     bool both_pending = false;         // the last store group read both boxes
     // claim staging box nb: the store issued from it two boxes ago has read it
@@ -419,6 +449,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tile_coords(t, P.tiles_m, P.tiles_n, tm, tn);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
+      // residual: the first two 64-column pieces of this lane's row are fetched while the
+      // tile's MMAs run; piece c + 2 is fetched while piece c is written
+      uint4 rq[2][8];
+      if constexpr (EPI == EPI_RESID) {
+        const int rrow = tm * BM + quarter * 32 + lane;
+        load_res64(rq[0], P.resid, P.ldr, P.M, P.N, rrow, tn * BN);
+        load_res64(rq[1], P.resid, P.ldr, P.M, P.N, rrow, tn * BN + 64);
+      }
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
       tc_fence_after();
       const int row0w = tm * BM + quarter * 32;
@@ -426,33 +464,31 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const bool row_ok = row < P.M;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
 
-      if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
+      if constexpr (EPI == EPI_STORE) {
 #pragma unroll 1
-        for (int c = 0; c < BN / 64 && ok; ++c) {
+        for (int c = 0; c < BN / 64; ++c) {
           const int col0 = tn * BN + c * 64;
           uint8_t* box = claim();
-          const int b = nb;
-          if constexpr (EPI == EPI_RESID) {
-            if (lane == 0 && col0 < P.N && row0w < P.M) {
-              mbar_expect_tx(res_bar(ew, b), C::kBoxBytes);
-              tma_load_2d(smem_u32(box), &tmRes, col0, row0w, res_bar(ew, b));
-              res_pending[b] = true;
-            }
-          }
           float v[32];
           tmem_ld32(taddr + c * 64, v);
-          if constexpr (EPI == EPI_RESID) {
-            if (col0 < P.N && row0w < P.M) {
-              if (!mbar_wait(res_bar(ew, b), (res_phase >> b) & 1u, abort_flag)) { ok = false; break; }
-              res_phase ^= 1u << b;
-              if (lane == 0) res_pending[b] = false;
-            }
-            box_add32(box, lane, 0, v);
-          }
           box_write32(box, lane, 0, v);
           tmem_ld32(taddr + c * 64 + 32, v);
-          if constexpr (EPI == EPI_RESID) box_add32(box, lane, 1, v);
           box_write32(box, lane, 1, v);
+          ship(box, col0, row0w);
+        }
+      } else if constexpr (EPI == EPI_RESID) {
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c) {
+          const int col0 = tn * BN + c * 64;
+          uint8_t* box = claim();
+          float v[32];
+          tmem_ld32(taddr + c * 64, v);
+          add_res32(v, rq[c & 1], 0);
+          box_write32(box, lane, 0, v);
+          tmem_ld32(taddr + c * 64 + 32, v);
+          add_res32(v, rq[c & 1], 1);
+          box_write32(box, lane, 1, v);
+          if (c + 2 < BN / 64) load_res64(rq[c & 1], P.resid, P.ldr, P.M, P.N, row, col0 + 128);
           ship(box, col0, row0w);
         }
       } else if constexpr (EPI == EPI_ROPE) {
@@ -591,8 +627,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if constexpr (EPI != EPI_CE) {
       if (lane == 0) {
         bulk_wait_all();  // every TMA store of this warp has completed
-        for (int b = 0; b < 2; ++b)  // an aborted residual load lands before the CTA exits
-          if (res_pending[b]) mbar_wait_drain(res_bar(ew, b), (res_phase >> b) & 1u, 40000000ll);
       }
       __syncwarp();
     }
@@ -670,9 +704,8 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
     if (!make_map(&tb[i], ptr, brows, g.K, g.ldb, box_b)) return MTP_ERR_INVALID_ARG;
   }
   // output / residual boxes: 32 rows x 64 columns, 128-byte swizzle
-  CUtensorMap tout = ta, tres = ta;
+  CUtensorMap tout = ta;
   if (EPI != EPI_CE && EPI < EPI_T_STORE && !make_map(&tout, g.out, g.M, g.N, g.ldo, 32)) return MTP_ERR_INVALID_ARG;
-  if (EPI == EPI_RESID && !make_map(&tres, g.resid, g.M, g.N, g.ldr, 32)) return MTP_ERR_INVALID_ARG;
   Args a{};
   a.M = g.M;
   a.N = g.N;
@@ -697,7 +730,7 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
   a.splits = g.splits > 0 ? g.splits : 1;
   const int ntiles = a.tiles_m * a.tiles_n * a.splits;
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
-  gemm_tc_kernel<BN, EPI><<<grid, kThreads, C::kSmemBytes, stream>>>(ta, tb[0], tb[1], tb[2], tout, tres, a);
+  gemm_tc_kernel<BN, EPI><<<grid, kThreads, C::kSmemBytes, stream>>>(ta, tb[0], tb[1], tb[2], tout, a);
   mtp::note_launch();
   MTP_LAUNCH_CHECK();
   return MTP_OK;

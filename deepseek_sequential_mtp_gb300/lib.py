@@ -272,7 +272,7 @@ def loss_assemble(sums_counts: torch.Tensor, D: int, n_positions: float, lam: fl
 
 
 KERNEL_CLASSES = {"head_ce_gemm": 0, "gate_up_gemm": 1, "down_gemm": 2, "qkv_gemm": 3, "o_gemm": 4,
-                  "proj_gemm": 5, "attention": 6, "spec_verify": 7}
+                  "proj_gemm": 5, "attention": 6, "spec_verify": 7, "prologue": 8}
 
 
 class KernelTimer:

@@ -263,7 +263,8 @@ enum {
   MTP_KC_PROJ_GEMM = 5,     /* eh_proj fusion GEMM                                  */
   MTP_KC_ATTENTION = 6,     /* segment-causal attention                             */
   MTP_KC_SPEC_VERIFY = 7,   /* spec_verify                                          */
-  MTP_KC_COUNT = 8
+  MTP_KC_PROLOGUE = 8,      /* embedding gather + dual RMSNorm + concat of a depth  */
+  MTP_KC_COUNT = 9
 };
 
 /* Measurement hook (not thread-safe; for benchmarks).  Each kernel class
