@@ -53,3 +53,69 @@ def test_draft_distribution_and_draw():
     # the draft stream is independent of the verifier's words 0 and 1
     ua, ur = ov.verify_uniforms(11, 4, 0, 0)
     assert od.draft_uniform(11, 4, 0) not in (float(ua), float(ur))
+
+
+def _np(t):
+    return t.float().numpy() if t.dtype.is_floating_point else t.numpy()
+
+
+def test_round_of_one_is_the_draft_step():
+    cfg = synth.DRAFT_SMALL
+    inp = synth.make_draft_inputs(cfg, 2)
+    W = oc.weights_to_numpy(inp["weights"])
+    dims = oc.Dims(n_heads=cfg.n_heads, head_dim=cfg.head_dim, D=1)
+    args = [_np(inp[k]) for k in ("parent_hidden", "frontier", "pos", "kv_k", "kv_v", "ctx_len")]
+    one = od.draft_step(*args, W, dims, 5, 9, requests=[1, 4])
+    rnd = od.draft_round(*args, W, dims, 1, 5, 9, requests=[1, 4])
+    for k in ("h", "q", "y", "margin"):
+        np.testing.assert_array_equal(rnd[k][:, 0], one[k])
+
+
+def test_round_steps_are_draft_steps_over_the_extended_cache():
+    """Step s of a round = one draft step from step s-1's state and draw, at
+    position pos + s, over the cache extended by the rows staged by steps
+    0..s-1 (keys rotated at their own positions)."""
+    cfg = synth.DRAFT_SMALL
+    inp = synth.make_draft_inputs(cfg, 4)
+    W = oc.weights_to_numpy(inp["weights"])
+    dims = oc.Dims(n_heads=cfg.n_heads, head_dim=cfg.head_dim, D=1)
+    ph, fr, pos, kk, vv, L = (_np(inp[k]) for k in ("parent_hidden", "frontier", "pos", "kv_k", "kv_v", "ctx_len"))
+    L = np.array([0, 7, 120, 299, 300])[:cfg.R].astype(np.int32)
+    pos = L.copy()
+    gamma = 3
+    rnd = od.draft_round(ph, fr, pos, kk, vv, L, W, dims, gamma, 3, 1, precision="f64")
+    for r in range(cfg.R):
+        parent, f = ph[r], int(fr[r])
+        k_ext, v_ext = kk[r][:L[r]].astype(np.float64), vv[r][:L[r]].astype(np.float64)
+        for s in range(gamma):
+            one = od.draft_step(parent[None], [f], [pos[r] + s], k_ext[None], v_ext[None], [L[r] + s], W, dims, 3, 1,
+                                precision="f64")
+            np.testing.assert_allclose(rnd["h"][r, s], one["h"][0], rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(rnd["q"][r, s], one["q"][0], rtol=1e-10, atol=1e-15)
+            # the staged row of step s: the new row's rotated key and value
+            u = oc.fusion(parent[None].astype(np.float64), [f], W, 0, dims, lambda a: a)
+            _, k_new, v_new = oc.block_qkv(u, W, 0, [pos[r] + s], dims, lambda a: a)
+            k_ext = np.concatenate([k_ext, k_new], axis=0)
+            v_ext = np.concatenate([v_ext, v_new], axis=0)
+            parent, f = rnd["h"][r, s], int(rnd["y"][r, s])
+        # each step draws with its own counter
+        for s in range(gamma):
+            assert rnd["y"][r, s] == ov.inverse_cdf(rnd["q"][r, s], od.draft_uniform(3, 1, r, s))[0]
+
+
+def test_forced_frontier_tokens():
+    cfg = synth.DRAFT_SMALL
+    inp = synth.make_draft_inputs(cfg, 6)
+    W = oc.weights_to_numpy(inp["weights"])
+    dims = oc.Dims(n_heads=cfg.n_heads, head_dim=cfg.head_dim, D=1)
+    args = [_np(inp[k]) for k in ("parent_hidden", "frontier", "pos", "kv_k", "kv_v", "ctx_len")]
+    free = od.draft_round(*args, W, dims, 3, 8, 2, requests=[2])
+    forced = od.draft_round(*args, W, dims, 3, 8, 2, requests=[2], forced_y=np.tile(free["y"][0], (cfg.R, 1)))
+    for k in ("h", "q", "y"):
+        np.testing.assert_array_equal(forced[k], free[k])
+    other = (free["y"][0] + 1) % cfg.V
+    moved = od.draft_round(*args, W, dims, 3, 8, 2, requests=[2], forced_y=np.tile(other, (cfg.R, 1)))
+    np.testing.assert_array_equal(moved["q"][0, 0], free["q"][0, 0])  # step 0 does not see the forcing
+    assert not np.allclose(moved["q"][0, 1], free["q"][0, 1])
+    # the draft streams of different steps differ
+    assert len({od.draft_uniform(8, 2, 2, s) for s in range(3)}) == 3
