@@ -73,7 +73,7 @@ def _module_row(parent, frontier, position, k_prev, v_prev, W, dims: Dims, rnd):
 
 
 def draft_round(parent_hidden, frontier, pos, kv_k, kv_v, ctx_len, W, dims: Dims, gamma, seed, offset,
-                precision="bf16", requests=None, forced_y=None):
+                precision="bf16", requests=None, forced_y=None, forced_h=None):
     """gamma recurrent draft steps per request by reuse of one module (M7.6
     §0x09: the retained depth proposes the next token from its own output
     state).  Step s (0-based) runs on parent h_{s-1} and frontier y_{s-1}
@@ -82,7 +82,9 @@ def draft_round(parent_hidden, frontier, pos, kv_k, kv_v, ctx_len, W, dims: Dims
     0..s-1 (their post-RoPE keys and values) and the row itself.  The draw y_s
     is the inverse CDF of q_s at draft_uniform(seed, offset, r, s).  With
     ``forced_y`` [R, gamma] the next step's frontier is forced_y[r][s] instead
-    of the own draw (the draw and its margin are still reported).
+    of the own draw (the draw and its margin are still reported); with
+    ``forced_h`` [R, gamma, d] the next step's parent state is forced_h[r][s]
+    instead of the own state (so each step can be compared on its own).
 
     Returns h [R', gamma, d], q [R', gamma, V], y and margin [R', gamma]."""
     rnd = round_bf16 if precision == "bf16" else (lambda a: a)
@@ -103,7 +105,7 @@ def draft_round(parent_hidden, frontier, pos, kv_k, kv_v, ctx_len, W, dims: Dims
             ms.append(m)
             k_prev = np.concatenate([k_prev, k[None]], axis=0)
             v_prev = np.concatenate([v_prev, v[None]], axis=0)
-            parent = h
+            parent = forced_h[r][step] if forced_h is not None else h
             f = int(forced_y[r][step]) if forced_y is not None else y
         out["h"].append(hs)
         out["q"].append(qs)

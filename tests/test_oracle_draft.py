@@ -119,3 +119,10 @@ def test_forced_frontier_tokens():
     assert not np.allclose(moved["q"][0, 1], free["q"][0, 1])
     # the draft streams of different steps differ
     assert len({od.draft_uniform(8, 2, 2, s) for s in range(3)}) == 3
+    # forcing the own states changes nothing; forcing other states moves later steps only
+    same = od.draft_round(*args, W, dims, 3, 8, 2, requests=[2], forced_h=np.tile(free["h"][0], (cfg.R, 1, 1)))
+    np.testing.assert_array_equal(same["q"], free["q"])
+    bumped = od.draft_round(*args, W, dims, 3, 8, 2, requests=[2],
+                            forced_h=np.tile(free["h"][0] * 1.5, (cfg.R, 1, 1)))
+    np.testing.assert_array_equal(bumped["q"][0, 0], free["q"][0, 0])
+    assert not np.allclose(bumped["q"][0, 1], free["q"][0, 1])
