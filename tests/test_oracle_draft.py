@@ -122,7 +122,8 @@ def test_forced_frontier_tokens():
     # forcing the own states changes nothing; forcing other states moves later steps only
     same = od.draft_round(*args, W, dims, 3, 8, 2, requests=[2], forced_h=np.tile(free["h"][0], (cfg.R, 1, 1)))
     np.testing.assert_array_equal(same["q"], free["q"])
+    noise = np.random.default_rng(0).standard_normal(free["h"][0].shape)  # RMSNorm ignores a pure rescale
     bumped = od.draft_round(*args, W, dims, 3, 8, 2, requests=[2],
-                            forced_h=np.tile(free["h"][0] * 1.5, (cfg.R, 1, 1)))
+                            forced_h=np.tile(free["h"][0] + noise, (cfg.R, 1, 1)))
     np.testing.assert_array_equal(bumped["q"][0, 0], free["q"][0, 0])
     assert not np.allclose(bumped["q"][0, 1], free["q"][0, 1])
