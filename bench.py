@@ -60,6 +60,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--draft-steps", type=int, default=30)
     ap.add_argument("--c3-steps", type=int, default=4, help="timed calls of the DeepSeek-V3-width section (0 = off)")
+    ap.add_argument("--draft-gamma", type=int, default=4, help="steps of the recurrent draft round (<= 1: off)")
     ap.add_argument("--draft-requests", type=int, default=32,
                     help="requests of the draft-step section (32 = the measured workload; fewer for profiling)")
     return ap.parse_args()
@@ -507,10 +508,50 @@ def measure_draft(args, dev, rank, peaks):
     total = weight_bytes + head_bytes + cache_bytes + q_bytes
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     gbs = total / (d_ms / 1e3) / 1e9
-    return {"workload": f"draft step R={cfg.R}, cache 8192 x d=7168 (56x128), ffn 18432, V=129280 + gamma=1 verify",
-            "ms_median": d_ms, "verify_ms_median": v_ms, "algorithmic_bytes": total,
-            "achieved_gbs": gbs, "peak_gbs": hbm_peak, "frac": gbs / hbm_peak,
-            "bound": "hbm", "steps": n, "l2": "flushed before every timed call (256 MiB written then read)"}
+    res = {"workload": f"draft step R={cfg.R}, cache 8192 x d=7168 (56x128), ffn 18432, V=129280 + gamma=1 verify",
+           "ms_median": d_ms, "verify_ms_median": v_ms, "algorithmic_bytes": total,
+           "achieved_gbs": gbs, "peak_gbs": hbm_peak, "frac": gbs / hbm_peak,
+           "bound": "hbm", "steps": n, "l2": "flushed before every timed call (256 MiB written then read)"}
+    del out, vout, step, vin
+
+    # recurrent round of gamma draft steps, then gamma-position verification of its draws
+    g = args.draft_gamma
+    if g > 1:
+        rnd = lib.DraftRound(cfg, inp["weights"], g, device=dev)
+        rin = synth.make_verify_inputs(synth.VerifyConfig(name=f"verify_R{cfg.R}_g{g}", R=cfg.R, gamma=g, V=cfg.V),
+                                       15 + rank, device=dev)
+        rout = {"q": torch.empty((cfg.R, g, cfg.V), dtype=torch.float32, device=dev),
+                "y": torch.empty((cfg.R, g), dtype=torch.int32, device=dev)}
+        vout = {k: torch.empty(cfg.R, dtype=torch.int32, device=dev)
+                for k in ("accepted", "next_token", "n_emit", "status")}
+
+        def round_call(i):
+            rnd(inp["parent_hidden"], inp["frontier"], inp["pos"], inp["kv_k"], inp["kv_v"], inp["ctx_len"],
+                seed=5, offset=i, out=rout)
+
+        round_call(0)
+        torch.cuda.synchronize()
+        nr = max(3, n // g)
+        er = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(nr)]
+        for i in range(nr):
+            flush()
+            er[i][0].record()
+            round_call(200 + i)
+            er[i][1].record()
+            lib.spec_verify(rin["p"], rout["q"], rout["y"], seed=6, offset=200 + i, out=vout)
+            er[i][2].record()
+        torch.cuda.synchronize()
+        lib.check_errors()
+        r_ms = sorted(a.elapsed_time(b) for a, b, _ in er)[nr // 2]
+        rv_ms = sorted(b.elapsed_time(c) for _, b, c in er)[nr // 2]
+        r_bytes = g * (weight_bytes + head_bytes + cache_bytes + q_bytes)
+        res["round"] = {"gamma": g, "ms_median": r_ms, "verify_ms_median": rv_ms,
+                        "drafted_tokens_per_s": cfg.R * g / (r_ms / 1e3), "algorithmic_bytes": r_bytes,
+                        "achieved_gbs": r_bytes / (r_ms / 1e3) / 1e9,
+                        "frac": r_bytes / (r_ms / 1e3) / 1e9 / hbm_peak, "calls": nr,
+                        "note": "gamma recurrent steps of one module; the cache is streamed once per step"}
+    return res
 
 
 def measure_dsv3(args, dev, rank, peaks):

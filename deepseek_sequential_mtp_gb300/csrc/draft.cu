@@ -97,18 +97,18 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8]) {
 
 // c = [RMSNorm_h(parent_hidden); RMSNorm_e(E[frontier])]
 __global__ void __launch_bounds__(kRowThreads)
-draft_prologue_kernel(const __nv_bfloat16* __restrict__ hp, const int32_t* __restrict__ frontier,
+draft_prologue_kernel(const __nv_bfloat16* __restrict__ hp, int ld_h, const int32_t* __restrict__ frontier, int f_stride,
                       const __nv_bfloat16* __restrict__ embed, const __nv_bfloat16* __restrict__ gh,
                       const __nv_bfloat16* __restrict__ ge, __nv_bfloat16* __restrict__ c, int d, int V,
                       float eps) {
   __shared__ float sh[32];
   const int r = blockIdx.x;
-  int tok = frontier[r];
+  int tok = frontier[static_cast<size_t>(r) * f_stride];
   if (tok < 0 || tok >= V) {
     if (threadIdx.x == 0) atomicOr(&g_mtp_error_word, MTP_DEVERR_TOKEN_RANGE);
     tok = min(max(tok, 0), V - 1);
   }
-  const uint4* h8 = reinterpret_cast<const uint4*>(hp + static_cast<size_t>(r) * d);
+  const uint4* h8 = reinterpret_cast<const uint4*>(hp + static_cast<size_t>(r) * ld_h);
   const uint4* e8 = reinterpret_cast<const uint4*>(embed + static_cast<size_t>(tok) * d);
   const int n8 = d / 8;
   float a = 0.f, b = 0.f;
@@ -145,13 +145,13 @@ draft_prologue_kernel(const __nv_bfloat16* __restrict__ hp, const int32_t* __res
 // y = bf16(acc [+ resid]); optionally norm_out = bf16(RMSNorm_g(y))
 __global__ void __launch_bounds__(kRowThreads)
 finish_row_kernel(const float* __restrict__ acc, const __nv_bfloat16* __restrict__ resid,
-                  __nv_bfloat16* __restrict__ y, const __nv_bfloat16* __restrict__ g,
+                  __nv_bfloat16* __restrict__ y, int ld_y, const __nv_bfloat16* __restrict__ g,
                   __nv_bfloat16* __restrict__ norm_out, int d, float eps) {
   __shared__ float sh[32];
   const int r = blockIdx.x;
   const int n8 = d / 8;
   const float4* a4 = reinterpret_cast<const float4*>(acc + static_cast<size_t>(r) * d);
-  uint4* y8 = reinterpret_cast<uint4*>(y + static_cast<size_t>(r) * d);
+  uint4* y8 = reinterpret_cast<uint4*>(y + static_cast<size_t>(r) * ld_y);
   float ss = 0.f;
   for (int i = threadIdx.x; i < n8; i += kRowThreads) {
     const float4 lo = a4[2 * i], hi = a4[2 * i + 1];
@@ -183,14 +183,17 @@ finish_row_kernel(const float* __restrict__ acc, const __nv_bfloat16* __restrict
   }
 }
 
-// qkv = bf16(RoPE(q), RoPE(k), v) at the request's position.  CTA (x, r)
+// qkv = bf16(RoPE(q), RoPE(k), v) at the request's position pos[r] + step;
+// the new row's rotated key and its value also go to slot `step` of the
+// staging rows [R, n_slots, d] that later draft steps attend to.  CTA (x, r)
 // covers pairs / v columns [x*1024, x*1024 + 1024) of row r; the row's
 // (cos, sin) per frequency index is computed once per CTA: angle formed and
 // reduced modulo 2*pi in double, sine/cosine taken in fp32.
 constexpr int kQkvCols = 1024;
 __global__ void __launch_bounds__(256)
 finish_qkv_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ qkv, const int32_t* __restrict__ pos,
-                  int d, int hd, float base, int pos_max) {
+                  int step, int d, int hd, float base, int pos_max, __nv_bfloat16* __restrict__ stage_k,
+                  __nv_bfloat16* __restrict__ stage_v, int n_slots) {
   __shared__ float2 cs[64];  // hd / 2 <= 64
   const int r = blockIdx.y;
   const int half = hd / 2;
@@ -202,6 +205,7 @@ finish_qkv_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ qkv
         if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(&g_mtp_error_word, MTP_DEVERR_TOKEN_RANGE);
         p = min(max(p, 0), pos_max);
       }
+      p += step;
       const int j = threadIdx.x;
       const double ang = static_cast<double>(p) * exp2(-2.0 * j / hd * log2(static_cast<double>(base)));
       const double two_pi = 6.283185307179586;
@@ -212,6 +216,8 @@ finish_qkv_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ qkv
   __syncthreads();
   const float* a = acc + static_cast<size_t>(r) * 3 * d;
   __nv_bfloat16* o = qkv + static_cast<size_t>(r) * 3 * d;
+  __nv_bfloat16* sk = stage_k + (static_cast<size_t>(r) * n_slots + step) * d;
+  __nv_bfloat16* sv = stage_v + (static_cast<size_t>(r) * n_slots + step) * d;
   const int i0 = blockIdx.x * kQkvCols;
   const int i1 = min(i0 + kQkvCols, d);
   for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
@@ -220,9 +226,17 @@ finish_qkv_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ qkv
     const int col = head * hd + j;
     const float x1 = a[col], x2 = a[col + half];
     const float2 t = cs[j];
-    o[col] = __float2bfloat16_rn(x1 * t.x - x2 * t.y);
-    o[col + half] = __float2bfloat16_rn(x2 * t.x + x1 * t.y);
-    o[2 * d + i] = __float2bfloat16_rn(a[2 * d + i]);  // v
+    const __nv_bfloat16 y1 = __float2bfloat16_rn(x1 * t.x - x2 * t.y);
+    const __nv_bfloat16 y2 = __float2bfloat16_rn(x2 * t.x + x1 * t.y);
+    o[col] = y1;
+    o[col + half] = y2;
+    if (col >= d) {  // a key head: stage the rotated key
+      sk[col - d] = y1;
+      sk[col - d + half] = y2;
+    }
+    const __nv_bfloat16 vv = __float2bfloat16_rn(a[2 * d + i]);
+    o[2 * d + i] = vv;
+    sv[i] = vv;
   }
 }
 
@@ -527,12 +541,16 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   }
 }
 
-// merge the split records with the new row's own key/value; one warp per
-// (request, head): lanes read the records' (max, sum) in parallel, then the
-// weighted outputs, lanes owning head_dim slices
+// merge the split records with the staged rows 0..n_staged-1 (the rows of
+// earlier draft steps and, last, the new row itself); one warp per (request,
+// head): lane j scores staged row j, lanes read the records' (max, sum) in
+// parallel, then the weighted outputs, lanes owning head_dim slices
 template <int HD>
-__global__ void decode_attn_combine_kernel(const __nv_bfloat16* __restrict__ qkv, const float* __restrict__ part,
-                                           __nv_bfloat16* __restrict__ out, int R, int H, int n_split, float scale) {
+__global__ void decode_attn_combine_kernel(const __nv_bfloat16* __restrict__ qkv,
+                                           const __nv_bfloat16* __restrict__ stage_k,
+                                           const __nv_bfloat16* __restrict__ stage_v, int n_slots, int n_staged,
+                                           const float* __restrict__ part, __nv_bfloat16* __restrict__ out, int R,
+                                           int H, int n_split, float scale) {
   const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (item >= R * H) return;
@@ -540,23 +558,35 @@ __global__ void decode_attn_combine_kernel(const __nv_bfloat16* __restrict__ qkv
   const int d = H * HD;
   constexpr int kDim = HD / 32;
   constexpr int kRec = HD + 2;
-  const __nv_bfloat16* row = qkv + static_cast<size_t>(r) * 3 * d;
-  float qv[kDim], kv[kDim], vv[kDim];
-  load_bf16x<kDim>(row + h * HD + lane * kDim, qv);
-  load_bf16x<kDim>(row + d + h * HD + lane * kDim, kv);
-  load_bf16x<kDim>(row + 2 * d + h * HD + lane * kDim, vv);
-  float qk = 0.f;
+  float qv[kDim];
+  load_bf16x<kDim>(qkv + static_cast<size_t>(r) * 3 * d + h * HD + lane * kDim, qv);
+  const __nv_bfloat16* sk = stage_k + static_cast<size_t>(r) * n_slots * d + h * HD + lane * kDim;
+  const __nv_bfloat16* sv = stage_v + static_cast<size_t>(r) * n_slots * d + h * HD + lane * kDim;
+  float s_own = -INFINITY;  // lane j: score of staged row j
+  for (int j = 0; j < n_staged; ++j) {
+    float kv[kDim];
+    load_bf16x<kDim>(sk + static_cast<size_t>(j) * d, kv);
+    float qk = 0.f;
 #pragma unroll
-  for (int t = 0; t < kDim; ++t) qk = fmaf(qv[t], kv[t], qk);
-  qk = mtp::warp_sum(qk) * scale;
+    for (int t = 0; t < kDim; ++t) qk = fmaf(qv[t], kv[t], qk);
+    qk = mtp::warp_sum(qk) * scale;
+    if (lane == j) s_own = qk;
+  }
   const float* rec0 = part + (static_cast<size_t>(r) * H + h) * n_split * kRec;
-  float m = qk;
+  float m = s_own;
   for (int c = lane; c < n_split; c += 32) m = fmaxf(m, rec0[static_cast<size_t>(c) * kRec]);
   m = mtp::warp_max(m);
-  const float wn = __expf(qk - m);
-  float l = 0.f, o[kDim];
+  const float w_own = lane < n_staged ? __expf(s_own - m) : 0.f;
+  float l = w_own, o[kDim];
 #pragma unroll
-  for (int t = 0; t < kDim; ++t) o[t] = wn * vv[t];
+  for (int t = 0; t < kDim; ++t) o[t] = 0.f;
+  for (int j = 0; j < n_staged; ++j) {
+    const float wj = __shfl_sync(0xffffffffu, w_own, j);
+    float vv[kDim];
+    load_bf16x<kDim>(sv + static_cast<size_t>(j) * d, vv);
+#pragma unroll
+    for (int t = 0; t < kDim; ++t) o[t] = fmaf(wj, vv[t], o[t]);
+  }
   for (int cb = 0; cb < n_split; cb += 32) {
     const int c = cb + lane;
     float wc = 0.f;
@@ -581,7 +611,7 @@ __global__ void decode_attn_combine_kernel(const __nv_bfloat16* __restrict__ qkv
       }
     }
   }
-  l = mtp::warp_sum(l) + wn;
+  l = mtp::warp_sum(l);
   const float inv = 1.0f / l;
   __nv_bfloat16* dst = out + static_cast<size_t>(r) * d + h * HD + lane * kDim;
 #pragma unroll
@@ -612,8 +642,8 @@ __device__ __forceinline__ void merge_max_sum(float& m, float& s, float m2, floa
 }
 
 __global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kSampleThreads)
-softmax_sample_kernel(float* __restrict__ q, int V, uint2 key, uint32_t off_lo, uint32_t off_hi,
-                      int32_t* __restrict__ y_out) {
+softmax_sample_kernel(float* __restrict__ q, int V, size_t ldq, uint2 key, uint32_t step, uint32_t off_lo,
+                      uint32_t off_hi, int32_t* __restrict__ y_out, int y_stride) {
   __shared__ float2 s_red[kSampleThreads / 32];
   __shared__ float2 s_ms[kSampleCluster];         // CTA 0: (max, sum) of every CTA
   __shared__ float2 s_chunk[kMaxSampleChunks];    // CTA 0: compensated chunk sums
@@ -624,7 +654,8 @@ softmax_sample_kernel(float* __restrict__ q, int V, uint2 key, uint32_t off_lo, 
   const int rank = static_cast<int>(cluster.block_rank());
   const int r = blockIdx.x / kSampleCluster;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* z = q + static_cast<size_t>(r) * V;
+  float* z = q + static_cast<size_t>(r) * ldq;
+  int32_t* y_dst = y_out + static_cast<size_t>(r) * y_stride;
   const int n_chunks = (V + kSampleChunk - 1) / kSampleChunk;
   const int cpc = (n_chunks + kSampleCluster - 1) / kSampleCluster;
   const int c0 = min(n_chunks, rank * cpc), c1 = min(n_chunks, c0 + cpc);
@@ -691,7 +722,7 @@ softmax_sample_kernel(float* __restrict__ q, int V, uint2 key, uint32_t off_lo, 
 
   // CTA 0: the chunk holding u * mass
   if (rank == 0 && warp == 0) {
-    const uint4 w = philox4x32_10(make_uint4(0u, static_cast<uint32_t>(r), off_lo, off_hi), key);
+    const uint4 w = philox4x32_10(make_uint4(step, static_cast<uint32_t>(r), off_lo, off_hi), key);
     const double u = static_cast<double>(w.z >> 8) * (1.0 / 16777216.0);
     const int per = (n_chunks + 31) / 32;
     double own = 0.0;
@@ -723,7 +754,7 @@ softmax_sample_kernel(float* __restrict__ q, int V, uint2 key, uint32_t off_lo, 
       s_cstar = cstar;
       s_before = before;
       s_target = target;
-      if (cstar < 0) y_out[r] = -1;
+      if (cstar < 0) *y_dst = -1;
     }
   }
   cluster.sync();
@@ -769,7 +800,7 @@ softmax_sample_kernel(float* __restrict__ q, int V, uint2 key, uint32_t off_lo, 
   const unsigned epos = __ballot_sync(0xffffffffu, wv > 0.0f);
   if (lane == 0) {
     const int base = cstar * kSampleChunk + 32 * lsrc;
-    y_out[r] = eover ? base + __ffs(eover) - 1 : (epos ? base + 31 - __clz(epos) : -1);
+    *y_dst = eover ? base + __ffs(eover) - 1 : (epos ? base + 31 - __clz(epos) : -1);
   }
 }
 
@@ -778,12 +809,16 @@ softmax_sample_kernel(float* __restrict__ q, int V, uint2 key, uint32_t off_lo, 
 // ---------------------------------------------------------------------------
 inline size_t align_up(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
+constexpr int kMaxRoundGamma = 31;  // draft steps per round (spec_verify takes gamma <= 31)
+
 struct DraftLayout {
-  size_t c, acc, u, x, qkv, o, a, g, h, part, total;
+  size_t c, acc, u, x, qkv, o, a, g, h, part, stage_k, stage_v, total;
   int n_chunks;
 };
 
-DraftLayout draft_layout(const mtp_dims& D) {
+// h holds two [R, d] rows (the state of the step and of the previous one);
+// stage_k / stage_v hold the rotated key and the value of every step's row
+DraftLayout draft_layout(const mtp_dims& D, int gamma) {
   DraftLayout L{};
   const size_t R = D.B, d = D.d;
   L.n_chunks = std::max(1, (D.T + kAttnSplitKeys - 1) / kAttnSplitKeys);
@@ -802,8 +837,10 @@ DraftLayout draft_layout(const mtp_dims& D) {
   L.o = take(R * d * 2);
   L.a = take(R * d * 2);
   L.g = take(R * static_cast<size_t>(D.ffn) * 2);
-  L.h = take(R * d * 2);
+  L.h = take(2 * R * d * 2);
   L.part = take(R * static_cast<size_t>(D.n_heads) * L.n_chunks * (D.head_dim + 2) * 4);
+  L.stage_k = take(R * static_cast<size_t>(gamma) * d * 2);
+  L.stage_v = take(R * static_cast<size_t>(gamma) * d * 2);
   L.total = off;
   return L;
 }
@@ -861,60 +898,42 @@ mtp_status skinny_gemm(const __nv_bfloat16* W, int features, int K, const __nv_b
 
 }  // namespace
 
-extern "C" size_t mtp_draft_workspace_bytes(const mtp_dims* dims) {
-  if (!dims || !draft_dims_ok(*dims)) return 0;
-  return draft_layout(*dims).total;
-}
+namespace {
 
-extern "C" mtp_status mtp_draft_step(const mtp_dims* dims, const mtp_weights* w, const void* parent_hidden,
-                                     const int32_t* frontier, const int32_t* pos, const void* kv_k, const void* kv_v,
-                                     const int32_t* ctx_len, uint64_t seed, uint64_t offset, float* q_out,
-                                     int32_t* y_out, void* h_out, void* ws, size_t ws_bytes, cudaStream_t st) {
-  if (!dims || !w) return MTP_ERR_INVALID_ARG;
-  const mtp_dims& D = *dims;
-  if (!draft_dims_ok(D)) return D.dtype != MTP_BF16 || D.D != 1 || D.B > kMaxR ? MTP_ERR_UNSUPPORTED : MTP_ERR_SHAPE;
-  if (!parent_hidden || !frontier || !pos || !kv_k || !kv_v || !ctx_len || !q_out || !y_out || !ws)
-    return MTP_ERR_INVALID_ARG;
-  if (!w->embed || !w->head || !w->out_norm) return MTP_ERR_INVALID_ARG;
-  const void* const* lists[] = {w->hnorm, w->enorm, w->eh_proj, w->attn_norm, w->wq, w->wk, w->wv,
-                                w->wo, w->ffn_norm, w->w_gate, w->w_up, w->w_down};
-  for (auto l : lists)
-    if (!l || !l[0] || !mtp::aligned16(l[0])) return l && l[0] ? MTP_ERR_ALIGNMENT : MTP_ERR_INVALID_ARG;
-  const void* ptrs[] = {parent_hidden, kv_k, kv_v, static_cast<const void*>(q_out), ws, w->embed, w->head,
-                        w->out_norm};
-  for (const void* p : ptrs)
-    if (!mtp::aligned16(p)) return MTP_ERR_ALIGNMENT;
-  if (h_out && !mtp::aligned16(h_out)) return MTP_ERR_ALIGNMENT;
-  const DraftLayout L = draft_layout(D);
-  if (ws_bytes < L.total) return MTP_ERR_WORKSPACE;
-
+// One draft step s of a round: reads the parent state (row stride ld_parent)
+// and the frontier token (stride f_stride), writes the step's state h_s (row
+// stride ld_h), logits/q into q_s (row stride ldq), the draw into y_s (stride
+// y_stride) and the step's key/value into staging slot s.
+mtp_status draft_one_step(const mtp_dims& D, const mtp_weights* w, const DraftLayout& L, uint8_t* base,
+                          const __nv_bfloat16* parent, int ld_parent, const int32_t* frontier, int f_stride,
+                          const int32_t* pos, const void* kv_k, const void* kv_v, const int32_t* ctx_len, int step,
+                          int gamma, uint2 key, uint64_t offset, float* q_s, size_t ldq, int32_t* y_s, int y_stride,
+                          __nv_bfloat16* h_s, int ld_h, cudaStream_t st) {
   const int R = D.B, d = D.d, ffn = D.ffn, V = D.V, H = D.n_heads, hd = D.head_dim;
-  uint8_t* base = static_cast<uint8_t*>(ws);
   auto bfp = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(base + off); };
   float* acc = reinterpret_cast<float*>(base + L.acc);
   auto W0 = [&](const void* const* l) { return static_cast<const __nv_bfloat16*>(l[0]); };
   const __nv_bfloat16* E = static_cast<const __nv_bfloat16*>(w->embed);
   __nv_bfloat16 *c = bfp(L.c), *u = bfp(L.u), *x = bfp(L.x), *qkv = bfp(L.qkv), *o = bfp(L.o), *a = bfp(L.a),
-                *g = bfp(L.g);
-  __nv_bfloat16* h = h_out ? static_cast<__nv_bfloat16*>(h_out) : bfp(L.h);
-  const int fin_threads = kRowThreads;
+                *g = bfp(L.g), *sk = bfp(L.stage_k), *sv = bfp(L.stage_v);
 
   // c, u = M c, x = RMSNorm_a(u)
-  draft_prologue_kernel<<<R, kRowThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(parent_hidden), frontier, E,
-                                           W0(w->hnorm), W0(w->enorm), c, d, V, D.eps);
+  draft_prologue_kernel<<<R, kRowThreads, 0, st>>>(parent, ld_parent, frontier, f_stride, E, W0(w->hnorm),
+                                                   W0(w->enorm), c, d, V, D.eps);
   mtp::note_launch();
   MTP_CUDA_TRY(cudaMemsetAsync(acc, 0, static_cast<size_t>(R) * d * 4, st));
   TRY(skinny_gemm(W0(w->eh_proj), d, 2 * d, c, R, acc, d, st));
-  finish_row_kernel<<<R, fin_threads, 0, st>>>(acc, nullptr, u, W0(w->attn_norm), x, d, D.eps);
+  finish_row_kernel<<<R, kRowThreads, 0, st>>>(acc, nullptr, u, d, W0(w->attn_norm), x, d, D.eps);
   mtp::note_launch();
-  // q, k, v with RoPE on q, k
+  // q, k, v with RoPE on q, k at pos + step; the row's k, v staged in slot `step`
   MTP_CUDA_TRY(cudaMemsetAsync(acc, 0, static_cast<size_t>(R) * 3 * d * 4, st));
   TRY(skinny_gemm(W0(w->wq), d, d, x, R, acc, 3 * d, st));
   TRY(skinny_gemm(W0(w->wk), d, d, x, R, acc + d, 3 * d, st));
   TRY(skinny_gemm(W0(w->wv), d, d, x, R, acc + 2 * d, 3 * d, st));
-  finish_qkv_kernel<<<dim3((d + kQkvCols - 1) / kQkvCols, R), 256, 0, st>>>(acc, qkv, pos, d, hd, D.rope_base, D.T);
+  finish_qkv_kernel<<<dim3((d + kQkvCols - 1) / kQkvCols, R), 256, 0, st>>>(acc, qkv, pos, step, d, hd, D.rope_base,
+                                                                            D.T, sk, sv, gamma);
   mtp::note_launch();
-  // attention over the module's own cache plus the new row
+  // attention over the module's own cache, the rows staged by earlier steps and the new row
   const float scale = 1.0f / sqrtf(static_cast<float>(hd));
   float* part = reinterpret_cast<float*>(base + L.part);
   const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(kv_k);
@@ -940,7 +959,8 @@ extern "C" mtp_status mtp_draft_step(const mtp_dims* dims, const mtp_weights* w,
     decode_attn_kernel<128><<<agrid, kAttnThreads, AttnCfg<128>::kSmemBytes, st>>>(
         tmk, tmv, qkv, ctx_len, part, H, D.T, n_split, split_keys, n_units, scale);
     mtp::note_launch();
-    decode_attn_combine_kernel<128><<<(R * H + 7) / 8, 256, 0, st>>>(qkv, part, o, R, H, n_split, scale);
+    decode_attn_combine_kernel<128><<<(R * H + 7) / 8, 256, 0, st>>>(qkv, sk, sv, gamma, step + 1, part, o, R, H,
+                                                                     n_split, scale);
   } else {
     static bool attr = false;
     if (!attr) {
@@ -951,14 +971,15 @@ extern "C" mtp_status mtp_draft_step(const mtp_dims* dims, const mtp_weights* w,
     decode_attn_kernel<64><<<agrid, kAttnThreads, AttnCfg<64>::kSmemBytes, st>>>(
         tmk, tmv, qkv, ctx_len, part, H, D.T, n_split, split_keys, n_units, scale);
     mtp::note_launch();
-    decode_attn_combine_kernel<64><<<(R * H + 7) / 8, 256, 0, st>>>(qkv, part, o, R, H, n_split, scale);
+    decode_attn_combine_kernel<64><<<(R * H + 7) / 8, 256, 0, st>>>(qkv, sk, sv, gamma, step + 1, part, o, R, H,
+                                                                    n_split, scale);
   }
   mtp::note_launch();
   mtp::prof_end(MTP_KC_ATTENTION, st);
   // a = u + o Wo^T, x = RMSNorm_f(a)
   MTP_CUDA_TRY(cudaMemsetAsync(acc, 0, static_cast<size_t>(R) * d * 4, st));
   TRY(skinny_gemm(W0(w->wo), d, d, o, R, acc, d, st));
-  finish_row_kernel<<<R, fin_threads, 0, st>>>(acc, u, a, W0(w->ffn_norm), x, d, D.eps);
+  finish_row_kernel<<<R, kRowThreads, 0, st>>>(acc, u, a, d, W0(w->ffn_norm), x, d, D.eps);
   mtp::note_launch();
   // g = silu(x Wg^T) * (x Wu^T)
   MTP_CUDA_TRY(cudaMemsetAsync(acc, 0, static_cast<size_t>(R) * 2 * ffn * 4, st));
@@ -969,17 +990,87 @@ extern "C" mtp_status mtp_draft_step(const mtp_dims* dims, const mtp_weights* w,
   // h = a + g Wd^T, x = RMSNorm_out(h)
   MTP_CUDA_TRY(cudaMemsetAsync(acc, 0, static_cast<size_t>(R) * d * 4, st));
   TRY(skinny_gemm(W0(w->w_down), d, ffn, g, R, acc, d, st));
-  finish_row_kernel<<<R, fin_threads, 0, st>>>(acc, a, h, static_cast<const __nv_bfloat16*>(w->out_norm), x, d,
-                                               D.eps);
+  finish_row_kernel<<<R, kRowThreads, 0, st>>>(acc, a, h_s, ld_h, static_cast<const __nv_bfloat16*>(w->out_norm),
+                                               x, d, D.eps);
   mtp::note_launch();
-  // logits into q_out, then softmax and the draw
+  // logits into q, then softmax and the draw
   mtp::prof_begin(MTP_KC_HEAD_CE_GEMM, st);
-  TRY(skinny_gemm(static_cast<const __nv_bfloat16*>(w->head), V, d, x, R, q_out, V, st, true));
+  if (ldq > 0x7FFFFFFFull) return MTP_ERR_UNSUPPORTED;
+  TRY(skinny_gemm(static_cast<const __nv_bfloat16*>(w->head), V, d, x, R, q_s, static_cast<int>(ldq), st, true));
   mtp::prof_end(MTP_KC_HEAD_CE_GEMM, st);
-  const uint2 key = make_uint2(static_cast<uint32_t>(seed & 0xFFFFFFFFu), static_cast<uint32_t>(seed >> 32));
-  softmax_sample_kernel<<<R * kSampleCluster, kSampleThreads, 0, st>>>(q_out, V, key, static_cast<uint32_t>(offset & 0xFFFFFFFFu),
-                                                      static_cast<uint32_t>(offset >> 32), y_out);
+  softmax_sample_kernel<<<R * kSampleCluster, kSampleThreads, 0, st>>>(
+      q_s, V, ldq, key, static_cast<uint32_t>(step), static_cast<uint32_t>(offset & 0xFFFFFFFFu),
+      static_cast<uint32_t>(offset >> 32), y_s, y_stride);
   mtp::note_launch();
   MTP_LAUNCH_CHECK();
   return MTP_OK;
+}
+
+}  // namespace
+
+extern "C" size_t mtp_draft_round_workspace_bytes(const mtp_dims* dims, int gamma) {
+  if (!dims || !draft_dims_ok(*dims) || gamma < 1 || gamma > kMaxRoundGamma) return 0;
+  return draft_layout(*dims, gamma).total;
+}
+
+extern "C" size_t mtp_draft_workspace_bytes(const mtp_dims* dims) { return mtp_draft_round_workspace_bytes(dims, 1); }
+
+extern "C" mtp_status mtp_draft_round(const mtp_dims* dims, const mtp_weights* w, const void* parent_hidden,
+                                      const int32_t* frontier, const int32_t* pos, const void* kv_k,
+                                      const void* kv_v, const int32_t* ctx_len, int gamma, uint64_t seed,
+                                      uint64_t offset, float* q_out, int32_t* y_out, void* h_out, void* ws,
+                                      size_t ws_bytes, cudaStream_t st) {
+  if (!dims || !w) return MTP_ERR_INVALID_ARG;
+  const mtp_dims& D = *dims;
+  if (!draft_dims_ok(D)) return D.dtype != MTP_BF16 || D.D != 1 || D.B > kMaxR ? MTP_ERR_UNSUPPORTED : MTP_ERR_SHAPE;
+  if (gamma < 1) return MTP_ERR_INVALID_ARG;
+  if (gamma > kMaxRoundGamma) return MTP_ERR_UNSUPPORTED;
+  if (!parent_hidden || !frontier || !pos || !kv_k || !kv_v || !ctx_len || !q_out || !y_out || !ws)
+    return MTP_ERR_INVALID_ARG;
+  if (!w->embed || !w->head || !w->out_norm) return MTP_ERR_INVALID_ARG;
+  const void* const* lists[] = {w->hnorm, w->enorm, w->eh_proj, w->attn_norm, w->wq, w->wk, w->wv,
+                                w->wo, w->ffn_norm, w->w_gate, w->w_up, w->w_down};
+  for (auto l : lists)
+    if (!l || !l[0] || !mtp::aligned16(l[0])) return l && l[0] ? MTP_ERR_ALIGNMENT : MTP_ERR_INVALID_ARG;
+  const void* ptrs[] = {parent_hidden, kv_k, kv_v, static_cast<const void*>(q_out), ws, w->embed, w->head,
+                        w->out_norm};
+  for (const void* p : ptrs)
+    if (!mtp::aligned16(p)) return MTP_ERR_ALIGNMENT;
+  if (h_out && !mtp::aligned16(h_out)) return MTP_ERR_ALIGNMENT;
+  const DraftLayout L = draft_layout(D, gamma);
+  if (ws_bytes < L.total) return MTP_ERR_WORKSPACE;
+
+  const int R = D.B, d = D.d;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  __nv_bfloat16* hbuf = reinterpret_cast<__nv_bfloat16*>(base + L.h);
+  const uint2 key = make_uint2(static_cast<uint32_t>(seed & 0xFFFFFFFFu), static_cast<uint32_t>(seed >> 32));
+  const size_t ldq = static_cast<size_t>(gamma) * D.V;
+  for (int s = 0; s < gamma; ++s) {
+    // the step's state: into h_out [R, gamma, d] if given, else a workspace ping-pong row
+    __nv_bfloat16* h_s = h_out ? static_cast<__nv_bfloat16*>(h_out) + static_cast<size_t>(s) * d
+                               : hbuf + static_cast<size_t>(s & 1) * R * d;
+    const int ld_h = h_out ? gamma * d : d;
+    const __nv_bfloat16* parent = static_cast<const __nv_bfloat16*>(parent_hidden);
+    int ld_parent = d;
+    const int32_t* f = frontier;
+    int f_stride = 1;
+    if (s > 0) {  // recurrent reuse: the previous step's state and draw
+      parent = h_out ? static_cast<const __nv_bfloat16*>(h_out) + static_cast<size_t>(s - 1) * d
+                     : hbuf + static_cast<size_t>((s - 1) & 1) * R * d;
+      ld_parent = ld_h;
+      f = y_out + (s - 1);
+      f_stride = gamma;
+    }
+    TRY(draft_one_step(D, w, L, base, parent, ld_parent, f, f_stride, pos, kv_k, kv_v, ctx_len, s, gamma, key,
+                       offset, q_out + static_cast<size_t>(s) * D.V, ldq, y_out + s, gamma, h_s, ld_h, st));
+  }
+  return MTP_OK;
+}
+
+extern "C" mtp_status mtp_draft_step(const mtp_dims* dims, const mtp_weights* w, const void* parent_hidden,
+                                     const int32_t* frontier, const int32_t* pos, const void* kv_k, const void* kv_v,
+                                     const int32_t* ctx_len, uint64_t seed, uint64_t offset, float* q_out,
+                                     int32_t* y_out, void* h_out, void* ws, size_t ws_bytes, cudaStream_t st) {
+  return mtp_draft_round(dims, w, parent_hidden, frontier, pos, kv_k, kv_v, ctx_len, 1, seed, offset, q_out, y_out,
+                         h_out, ws, ws_bytes, st);
 }

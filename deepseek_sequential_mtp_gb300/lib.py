@@ -79,6 +79,11 @@ def load() -> ctypes.CDLL:
     lib.mtp_profile_kernel.argtypes = [i32, vp, i32, ctypes.POINTER(ctypes.c_int)]
     lib.mtp_draft_workspace_bytes.restype = sz
     lib.mtp_draft_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
+    lib.mtp_draft_round_workspace_bytes.restype = sz
+    lib.mtp_draft_round_workspace_bytes.argtypes = [ctypes.POINTER(Dims), i32]
+    lib.mtp_draft_round.restype = i32
+    lib.mtp_draft_round.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Weights), vp, vp, vp, vp, vp, vp, i32,
+                                    ctypes.c_uint64, ctypes.c_uint64, vp, vp, vp, vp, sz, vp]
     lib.mtp_draft_step.restype = i32
     lib.mtp_draft_step.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Weights), vp, vp, vp, vp, vp, vp,
                                    u64, u64, vp, vp, vp, vp, sz, vp]
@@ -342,6 +347,50 @@ class DraftStep:
                                    int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(out["q"]),
                                    _ptr(out["y"]), _ptr(h_out), _ptr(self.ws), self.ws.numel(), _stream(stream))
         _check(st, "mtp_draft_step")
+        if h_out is not None:
+            out["h"] = h_out
+        return out
+
+
+class DraftRound:
+    """Reusable call state of mtp_draft_round: gamma recurrent draft steps of
+    one module for one shape (see synth.DraftConfig)."""
+
+    def __init__(self, cfg, weights: dict, gamma: int, device="cuda"):
+        self.cfg = cfg
+        self.gamma = int(gamma)
+        self.dims = Dims(cfg.R, cfg.ctx, cfg.d, cfg.n_heads, cfg.head_dim, cfg.ffn, cfg.V, 1, cfg.eps,
+                         cfg.rope_base, MTP_BF16)
+        self.weights = weights
+        self.w = ChainWeights(weights, 1)
+        nbytes = int(load().mtp_draft_round_workspace_bytes(ctypes.byref(self.dims), self.gamma))
+        if nbytes == 0:
+            raise MtpError("invalid draft-round dimensions or gamma")
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def __call__(self, parent_hidden, frontier, pos, kv_k, kv_v, ctx_len, seed, offset,
+                 out=None, h_out=None, stream=None):
+        cfg, g = self.cfg, self.gamma
+        _need(parent_hidden, "parent_hidden", torch.bfloat16)
+        for name, t in (("kv_k", kv_k), ("kv_v", kv_v)):
+            _need(t, name, torch.bfloat16)
+            if tuple(t.shape) != (cfg.R, cfg.ctx, cfg.d):
+                raise MtpError(f"{name} must be [R, ctx, d]")
+        for name, t in (("frontier", frontier), ("pos", pos), ("ctx_len", ctx_len)):
+            _need(t, name, torch.int32)
+        if h_out is not None:
+            _need(h_out, "h_out", torch.bfloat16)
+            if tuple(h_out.shape) != (cfg.R, g, cfg.d):
+                raise MtpError("h_out must be [R, gamma, d]")
+        dev = parent_hidden.device
+        if out is None:
+            out = {"q": torch.empty((cfg.R, g, cfg.V), dtype=torch.float32, device=dev),
+                   "y": torch.empty((cfg.R, g), dtype=torch.int32, device=dev)}
+        st = load().mtp_draft_round(ctypes.byref(self.dims), ctypes.byref(self.w.struct), _ptr(parent_hidden),
+                                    _ptr(frontier), _ptr(pos), _ptr(kv_k), _ptr(kv_v), _ptr(ctx_len), g,
+                                    int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(out["q"]),
+                                    _ptr(out["y"]), _ptr(h_out), _ptr(self.ws), self.ws.numel(), _stream(stream))
+        _check(st, "mtp_draft_round")
         if h_out is not None:
             out["h"] = h_out
         return out

@@ -247,6 +247,30 @@ mtp_status mtp_draft_step(const mtp_dims* dims, const mtp_weights* w, const void
                           float* q_out, int32_t* y_out, void* h_out, void* ws, size_t ws_bytes,
                           cudaStream_t stream);
 
+/* Bytes of device workspace mtp_draft_round needs for `gamma` steps (0 if the
+ * sizes are invalid or gamma is outside [1, 31]). */
+size_t mtp_draft_round_workspace_bytes(const mtp_dims* dims, int gamma);
+
+/* gamma recurrent draft steps by reuse of one MTP module ([M7.6] §0x09: the
+ * retained depth proposes the next token from its own output state).  Step s
+ * (0-based) is mtp_draft_step's computation with
+ *   parent = h of step s-1 (step 0: parent_hidden), frontier = y of step s-1
+ *   (step 0: frontier), position pos_r + s, keys = the cached rows
+ *   [0, ctx_len_r), the rows of steps 0..s-1 (their rotated keys and values,
+ *   staged in the workspace) and the row itself,
+ * and its draw uses word 2 of Philox4x32-10 at counter (s, r, offset lo, hi).
+ * The staged rows are not written back to the cache.
+ *   q_out [R, gamma, V] float: q of every step (the draft distributions that
+ *   spec_verify takes); y_out [R, gamma] int32: the draws (spec_verify's
+ *   draft tokens); h_out [R, gamma, d] bf16 nullable: every step's state.
+ * gamma in [1, 31]; other arguments as for mtp_draft_step, whose call equals
+ * this one with gamma = 1.  The block's weights, the head and the cache are
+ * streamed once per step. */
+mtp_status mtp_draft_round(const mtp_dims* dims, const mtp_weights* w, const void* parent_hidden,
+                           const int32_t* frontier, const int32_t* pos, const void* kv_k, const void* kv_v,
+                           const int32_t* ctx_len, int gamma, uint64_t seed, uint64_t offset, float* q_out,
+                           int32_t* y_out, void* h_out, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Diagnostic GEMM on the same tcgen05 core the chain uses:
  * C[M,N] (bf16) = A[M,K] (bf16) · B[N,K]^T (bf16), fp32 accumulation.
  * K % 8 == 0; A, B, C 16-byte aligned. */

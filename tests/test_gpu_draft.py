@@ -99,3 +99,85 @@ def test_full_size_sampled_requests():
         y_own, m_own = ov.inverse_cdf(g["q"][rid].astype(np.float64), od.draft_uniform(5, 2, rid))
         if m_own > 1e-6:
             assert g["y"][rid] == y_own
+
+
+def _round_case(cfg, seed, ctx, gamma, dseed, offset):
+    inp = synth.make_draft_inputs(cfg, seed)
+    inp["ctx_len"] = torch.tensor(ctx, dtype=torch.int32)
+    inp["pos"] = inp["ctx_len"].clone()
+    dev = {k: v.cuda() for k, v in inp.items() if k != "weights"}
+    wdev = {k: ([t.cuda() for t in v] if isinstance(v, list) else v.cuda()) for k, v in inp["weights"].items()}
+    rnd = lib.DraftRound(cfg, wdev, gamma)
+    h = torch.empty((cfg.R, gamma, cfg.d), dtype=torch.bfloat16, device="cuda")
+    g = rnd(dev["parent_hidden"], dev["frontier"], dev["pos"], dev["kv_k"], dev["kv_v"], dev["ctx_len"],
+            dseed, offset, h_out=h)
+    lib.check_errors()
+    g = {k: _np(v) for k, v in g.items()}
+    W = oc.weights_to_numpy(inp["weights"])
+    dims = oc.Dims(n_heads=cfg.n_heads, head_dim=cfg.head_dim, D=1, eps=cfg.eps, rope_base=cfg.rope_base)
+    # each step is compared on its own: the oracle continues from the GPU's state and draw of the
+    # previous step (a wrong parent or frontier on the GPU would show as a mismatch of the next step)
+    r = od.draft_round(*[_np(inp[k]) for k in ("parent_hidden", "frontier", "pos", "kv_k", "kv_v", "ctx_len")],
+                       W, dims, gamma, dseed, offset, forced_y=g["y"], forced_h=g["h"])
+    return g, r
+
+
+def _check_round(cfg, g, r, dseed, offset):
+    """Per-step bars as for one draft step, except the per-entry q bar of
+    steps >= 1: 5e-3 max(q).  The oracle continues from the GPU's state and
+    draw, but its staged rows of earlier steps are its own (equal to the GPU's
+    up to bf16 rounding flips), and with a small cache each staged row carries
+    a large share of the attention weight (one flip moved q by ~0.2%)."""
+    gamma = g["y"].shape[1]
+    for s in range(gamma):
+        err = np.abs(g["h"][:, s] - r["h"][:, s])
+        assert np.all(err <= 2e-2 + 2e-2 * np.abs(r["h"][:, s])), (s, err.max())
+        gq = g["q"][:, s]
+        assert np.all(np.isfinite(gq)) and np.allclose(gq.sum(1), 1.0, atol=1e-4)
+        assert (0.5 * np.abs(gq - r["q"][:, s]).sum(1)).max() < 5e-3, s
+        bar = 2e-3 if s == 0 else 5e-3
+        assert np.all(np.abs(gq - r["q"][:, s]).max(1) <= bar * r["q"][:, s].max(1)), s
+        for rid in range(cfg.R):
+            y_own, m_own = ov.inverse_cdf(gq[rid].astype(np.float64), od.draft_uniform(dseed, offset, rid, s))
+            if m_own > 1e-6:
+                assert g["y"][rid, s] == y_own, (rid, s)
+            if r["margin"][rid, s] > 5e-3:
+                assert g["y"][rid, s] == r["y"][rid, s], (rid, s)
+
+
+@pytest.mark.parametrize("gamma", [2, 4])
+def test_round_parity_hd64(gamma):
+    """Recurrent drafting, head_dim 64: empty, one-key and ragged caches."""
+    cfg = synth.DRAFT_SMALL
+    g, r = _round_case(cfg, 3, [0, 1, 100, 299, 300][:cfg.R], gamma, dseed=31, offset=7)
+    _check_round(cfg, g, r, 31, 7)
+
+
+def test_round_parity_hd128():
+    cfg = synth.DRAFT_SMALL_HD128
+    g, r = _round_case(cfg, 8, [0, 63, 577, 1100], 3, dseed=2, offset=2**33 + 1)
+    _check_round(cfg, g, r, 2, 2**33 + 1)
+
+
+def test_round_of_one_is_the_step_and_feeds_verify():
+    """mtp_draft_round with gamma = 1 equals mtp_draft_step bit for bit; a
+    gamma = 3 round's q and draws drive spec_verify as its draft distributions
+    and tokens, matching the verify oracle on the same inputs."""
+    cfg = synth.DRAFT_SMALL
+    inp = synth.make_draft_inputs(cfg, 5)
+    dev = {k: v.cuda() for k, v in inp.items() if k != "weights"}
+    wdev = {k: ([t.cuda() for t in v] if isinstance(v, list) else v.cuda()) for k, v in inp["weights"].items()}
+    args = (dev["parent_hidden"], dev["frontier"], dev["pos"], dev["kv_k"], dev["kv_v"], dev["ctx_len"])
+    one = lib.DraftRound(cfg, wdev, 1)(*args, 4, 9)
+    step = lib.DraftStep(cfg, wdev)(*args, 4, 9)
+    assert torch.equal(one["q"][:, 0], step["q"]) and torch.equal(one["y"][:, 0], step["y"])
+    gamma = 3
+    rnd = lib.DraftRound(cfg, wdev, gamma)(*args, 4, 9)
+    vcase = synth.make_small_verify_case(2, R=cfg.R, gamma=gamma, V=cfg.V)
+    p = vcase["p"].cuda()
+    vout = lib.spec_verify(p, rnd["q"], rnd["y"], seed=17, offset=3)
+    lib.check_errors()
+    ref = ov.spec_verify(vcase["p"].numpy(), rnd["q"].cpu().numpy(), rnd["y"].cpu().numpy(), 17, 3)
+    keep = ref["margin"] > 1e-7
+    for kg, kr in (("accepted", "accepted"), ("next_token", "token"), ("n_emit", "n_emit"), ("status", "status")):
+        np.testing.assert_array_equal(vout[kg].cpu().numpy()[keep], ref[kr][keep])
