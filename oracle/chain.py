@@ -229,20 +229,52 @@ def chain_forward_loss(tokens, seg, pos, h0, W, dims: Dims, precision="f64",
     return out
 
 
-def assemble_loss(sums, counts, n_positions, D, lam, den, with_main=True):
-    """L = L_main + (λ/D) Σ_k L^(k) (M7.6 §0x05) with per-term denominators
-    chosen by ``den``; an empty masked-mean term is 0 and stays in the mean."""
+REDUCTIONS = ("fixed", "masked_mean", "sum", "global", "weighted_pair")
+
+
+def assemble_loss(sums, counts, n_positions, D, lam, den, with_main=True, depth_weights=None):
+    """L = L_main + Σ_k w_k L^(k) with per-depth weights w_k (default λ/D,
+    M7.6 §0x05: L_main + (λ/D) Σ_k L^(k)) and the depth reduction ``den``
+    (the four reductions of "M7.4 - Multi-Token Prediction Foundations"
+    §0x02C, plus the fixed denominator):
+      fixed          L^(k) = S_k / n_positions (the paper's 1/T for a batch)
+      masked_mean    L^(k) = S_k / N_k          (head mean; empty term -> 0)
+      sum            L^(k) = S_k
+      global         L^(k) = S_k / Σ_j N_j      (so Σ_k w_k L^(k) = Σ w S / Σ N)
+      weighted_pair  L^(k) = S_k / Σ_j w_j N_j  (so Σ_k w_k L^(k) = Σ w S / Σ w N)
+    with S_k, N_k the loss sum and supervised-row count of depth k.  The main
+    term is S_0 / n_positions (fixed), S_0 (sum) or S_0 / N_0 (the others);
+    an empty denominator gives 0."""
+    if den not in REDUCTIONS:
+        raise ValueError(den)
+    w = [lam / D] * D if depth_weights is None else [float(x) for x in depth_weights]
+    n_all = sum(counts[1:D + 1])
+    wn_all = sum(w[k - 1] * counts[k] for k in range(1, D + 1))
+
+    def div(a, b):
+        return a / b if b > 0 else 0.0
+
     def term(i):
         if den == "fixed":
             return sums[i] / n_positions
-        if den == "masked_mean":
-            return sums[i] / counts[i] if counts[i] > 0 else 0.0
-        raise ValueError(den)
+        if den == "sum":
+            return sums[i]
+        if den == "masked_mean" or i == 0:
+            return div(sums[i], counts[i])
+        if den == "global":
+            return div(sums[i], n_all)
+        return div(sums[i], wn_all)
 
     L_main = term(0) if with_main else 0.0
     L_k = [term(i) for i in range(1, D + 1)]
     return {"loss_main": L_main, "loss_mtp": L_k,
-            "loss_total": L_main + lam / D * sum(L_k)}
+            "loss_total": L_main + sum(w[k] * L_k[k] for k in range(D))}
+
+
+def deepseek_v3_lambda(tokens_seen: float) -> float:
+    """MTP weight of the DeepSeek-V3 schedule quoted by M7.6 §0x05: 0.3 for the
+    first 10T training tokens, 0.1 for the rest."""
+    return 0.3 if tokens_seen < 10e12 else 0.1
 
 
 def weights_to_numpy(weights) -> dict:
