@@ -431,23 +431,47 @@ __global__ void zero_f64_kernel(double* p, int n) {
 }
 
 // losses = [L, L_main, L^(1..D)] from (sum, count) pairs
+// Per-depth weights of the loss assembly (uniform lambda/D unless given).
+constexpr int kMaxDepthWeights = 32;
+struct DepthWeights {
+  float w[kMaxDepthWeights];
+  float lambda;
+  int uniform;
+};
+
+// L^(k) and the total under reduction `den` (the enum's definitions in
+// include/mtp.h): sums_counts holds (S_k, N_k), k = 0 main, 1..D depths.
 __global__ void loss_assemble_kernel(const double* __restrict__ sc, float* __restrict__ losses, int D, double n_pos,
-                                     float lambda, int den, int with_main) {
+                                     DepthWeights W, int den, int with_main) {
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  auto weight = [&](int k) -> double {
+    return W.uniform ? static_cast<double>(W.lambda) / D : static_cast<double>(W.w[k - 1]);
+  };
+  double n_all = 0.0, wn_all = 0.0;
+  for (int k = 1; k <= D; ++k) {
+    n_all += sc[2 * k + 1];
+    wn_all += weight(k) * sc[2 * k + 1];
+  }
+  auto div = [](double a, double b) { return b > 0.0 ? a / b : 0.0; };
   auto term = [&](int i) -> double {
     if (den == MTP_DEN_FIXED) return sc[2 * i] / n_pos;
-    return sc[2 * i + 1] > 0 ? sc[2 * i] / sc[2 * i + 1] : 0.0;
+    if (den == MTP_DEN_SUM) return sc[2 * i];
+    if (den == MTP_DEN_MASKED_MEAN || i == 0) return div(sc[2 * i], sc[2 * i + 1]);
+    if (den == MTP_DEN_GLOBAL) return div(sc[2 * i], n_all);
+    return div(sc[2 * i], wn_all);
   };
   const double main = with_main ? term(0) : 0.0;
   double mtp = 0.0;
   for (int k = 1; k <= D; ++k) {
     const double lk = term(k);
     losses[1 + k] = static_cast<float>(lk);
-    mtp += lk;
+    mtp += weight(k) * lk;
   }
   losses[1] = static_cast<float>(main);
-  losses[0] = static_cast<float>(main + static_cast<double>(lambda) / D * mtp);
+  losses[0] = static_cast<float>(main + mtp);
 }
+
+inline bool valid_den(int den) { return den >= MTP_DEN_FIXED && den <= MTP_DEN_WEIGHTED_PAIR; }
 
 // ---------------------------------------------------------------------------
 // Host orchestration
@@ -737,8 +761,10 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
     h_prev = h_k;
   }
   if (with_loss) {
-    loss_assemble_kernel<<<1, 32, 0, C.st>>>(sums_counts, losses, D.D, static_cast<double>(M), lambda, den,
-                                             with_main);
+    DepthWeights W{};
+    W.lambda = lambda;
+    W.uniform = 1;
+    loss_assemble_kernel<<<1, 32, 0, C.st>>>(sums_counts, losses, D.D, static_cast<double>(M), W, den, with_main);
     mtp::note_launch();
     MTP_LAUNCH_CHECK();
   }
@@ -795,7 +821,7 @@ extern "C" mtp_status mtp_chain_loss(const mtp_dims* dims, const mtp_weights* w,
                                      void* ws, size_t ws_bytes, cudaStream_t stream) {
   TRY(check_common(dims, w, tokens, seg, pos, h0, ws, ws_bytes));
   if (!sums_counts || !losses) return MTP_ERR_INVALID_ARG;
-  if (den != MTP_DEN_FIXED && den != MTP_DEN_MASKED_MEAN) return MTP_ERR_INVALID_ARG;
+  if (!valid_den(den)) return MTP_ERR_INVALID_ARG;
   if (h_out && !mtp::aligned16(h_out)) return MTP_ERR_ALIGNMENT;
   Ctx C{*dims, *w, tokens, seg, pos, static_cast<uint8_t*>(ws), make_layout(*dims), stream, dims->B * dims->T};
   if (dims->dtype == MTP_BF16)
@@ -805,12 +831,24 @@ extern "C" mtp_status mtp_chain_loss(const mtp_dims* dims, const mtp_weights* w,
                           sums_counts, losses, row_loss);
 }
 
-extern "C" mtp_status mtp_loss_assemble(int D, const double* sums_counts, double n_positions, float lambda, int den,
-                                        int with_main, float* losses, cudaStream_t stream) {
+extern "C" mtp_status mtp_loss_assemble_weighted(int D, const double* sums_counts, double n_positions,
+                                                 const float* depth_weights, float lambda, int den, int with_main,
+                                                 float* losses, cudaStream_t stream) {
   if (D <= 0 || !sums_counts || !losses || !(n_positions > 0)) return MTP_ERR_INVALID_ARG;
-  if (den != MTP_DEN_FIXED && den != MTP_DEN_MASKED_MEAN) return MTP_ERR_INVALID_ARG;
-  loss_assemble_kernel<<<1, 32, 0, stream>>>(sums_counts, losses, D, n_positions, lambda, den, with_main);
+  if (!valid_den(den)) return MTP_ERR_INVALID_ARG;
+  if (depth_weights && D > kMaxDepthWeights) return MTP_ERR_UNSUPPORTED;
+  DepthWeights W{};
+  W.lambda = lambda;
+  W.uniform = depth_weights ? 0 : 1;
+  if (depth_weights)
+    for (int k = 0; k < D; ++k) W.w[k] = depth_weights[k];
+  loss_assemble_kernel<<<1, 32, 0, stream>>>(sums_counts, losses, D, n_positions, W, den, with_main);
   mtp::note_launch();
   MTP_LAUNCH_CHECK();
   return MTP_OK;
+}
+
+extern "C" mtp_status mtp_loss_assemble(int D, const double* sums_counts, double n_positions, float lambda, int den,
+                                        int with_main, float* losses, cudaStream_t stream) {
+  return mtp_loss_assemble_weighted(D, sums_counts, n_positions, nullptr, lambda, den, with_main, losses, stream);
 }

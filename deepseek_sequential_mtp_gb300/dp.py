@@ -25,3 +25,9 @@ def global_positions(B: int, T: int, group=None) -> int:
     """B*T summed over ranks: the fixed-denominator policy's global B*T."""
     world = dist.get_world_size(group) if dist.is_available() and dist.is_initialized() else 1
     return world * B * T
+
+
+def deepseek_v3_lambda(tokens_seen: float) -> float:
+    """MTP loss weight of the DeepSeek-V3 schedule ("M7.6 - DeepSeek MTP"
+    §0x05): 0.3 for the first 10T training tokens, 0.1 afterwards."""
+    return 0.3 if tokens_seen < 10e12 else 0.1

@@ -17,7 +17,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmtp.so")
 
 MTP_F32, MTP_BF16 = 0, 1
-DEN = {"fixed": 0, "masked_mean": 1}
+DEN = {"fixed": 0, "masked_mean": 1, "sum": 2, "global": 3, "weighted_pair": 4}
 VERIFY_STATUS = {0: "ok", 1: "invalid_draft", 2: "zero_residual", 3: "invalid_probs",
                  4: "invalid_budget"}
 
@@ -73,6 +73,9 @@ def load() -> ctypes.CDLL:
     lib.mtp_chain_loss.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Weights),
                                    vp, vp, vp, vp, ctypes.c_float, i32, i32,
                                    vp, vp, vp, vp, vp, sz, vp]
+    lib.mtp_loss_assemble_weighted.restype = i32
+    lib.mtp_loss_assemble_weighted.argtypes = [i32, vp, ctypes.c_double, ctypes.POINTER(ctypes.c_float),
+                                               ctypes.c_float, i32, i32, vp, vp]
     lib.mtp_loss_assemble.restype = i32
     lib.mtp_loss_assemble.argtypes = [i32, vp, ctypes.c_double, ctypes.c_float, i32, i32, vp, vp]
     lib.mtp_profile_kernel.restype = i32
@@ -266,13 +269,22 @@ class Chain:
 # Loss assembly (data-parallel callers) and measurement hooks
 # --------------------------------------------------------------------------
 def loss_assemble(sums_counts: torch.Tensor, D: int, n_positions: float, lam: float, den="fixed",
-                  with_main=True, losses: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """L, L_main, L^(1..D) from (already all-reduced) per-term sums and counts."""
+                  with_main=True, losses: Optional[torch.Tensor] = None, stream=None,
+                  depth_weights=None) -> torch.Tensor:
+    """L, L_main, L^(1..D) from (already all-reduced) per-term sums and counts
+    under reduction ``den`` (include/mtp.h: mtp_den) with per-depth weights
+    (a sequence of D floats; None = lam / D each)."""
     _need(sums_counts, "sums_counts", torch.float64)
     if losses is None:
         losses = torch.empty(D + 2, dtype=torch.float32, device=sums_counts.device)
-    _check(load().mtp_loss_assemble(D, _ptr(sums_counts), float(n_positions), float(lam), DEN[den],
-                                    int(with_main), _ptr(losses), _stream(stream)), "mtp_loss_assemble")
+    w = None
+    if depth_weights is not None:
+        if len(depth_weights) != D:
+            raise MtpError("depth_weights must hold D values")
+        w = (ctypes.c_float * D)(*[float(x) for x in depth_weights])
+    _check(load().mtp_loss_assemble_weighted(D, _ptr(sums_counts), float(n_positions), w, float(lam), DEN[den],
+                                             int(with_main), _ptr(losses), _stream(stream)),
+           "mtp_loss_assemble_weighted")
     return losses
 
 

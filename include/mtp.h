@@ -54,7 +54,24 @@ typedef enum mtp_dtype { MTP_F32 = 0, MTP_BF16 = 1 } mtp_dtype;
  *        denominator for a batch of B packed rows of T positions.
  * MASKED_MEAN: each term divided by its own count of supervised rows; an
  *        empty term is 0 and stays in the D-depth mean ([M7.6] §0x06A). */
-typedef enum mtp_den { MTP_DEN_FIXED = 0, MTP_DEN_MASKED_MEAN = 1 } mtp_den;
+/* How the per-depth loss sums S_k (k = 0 main, 1..D depths) and counts N_k
+ * become the reported terms L^(k) ("M7.4 - Multi-Token Prediction
+ * Foundations" §0x02C names the last four):
+ *   FIXED          L^(k) = S_k / n_positions (the paper's 1/T, batch form)
+ *   MASKED_MEAN    L^(k) = S_k / N_k          (head mean)
+ *   SUM            L^(k) = S_k
+ *   GLOBAL         L^(k) = S_k / sum_j N_j    (depths only)
+ *   WEIGHTED_PAIR  L^(k) = S_k / sum_j w_j N_j (depths only)
+ * and total = L_main + sum_k w_k L^(k), w_k the per-depth weights (lambda/D
+ * unless given).  L_main is S_0 / n_positions (FIXED), S_0 (SUM), else
+ * S_0 / N_0.  A zero denominator gives 0. */
+typedef enum mtp_den {
+  MTP_DEN_FIXED = 0,
+  MTP_DEN_MASKED_MEAN = 1,
+  MTP_DEN_SUM = 2,
+  MTP_DEN_GLOBAL = 3,
+  MTP_DEN_WEIGHTED_PAIR = 4
+} mtp_den;
 
 /* Per-request status written by spec_verify. */
 enum {
@@ -192,6 +209,12 @@ mtp_status mtp_chain_loss_noalloc(const mtp_dims* dims, const mtp_weights* w,
  * n_positions.  sums_counts [2*(D+1)] double, losses [D+2] float (device). */
 mtp_status mtp_loss_assemble(int D, const double* sums_counts, double n_positions, float lambda,
                              int den, int with_main, float* losses, cudaStream_t stream);
+
+/* mtp_loss_assemble with per-depth weights: depth_weights is a HOST array of
+ * D floats copied at the call (NULL = lambda/D each; D <= 32 when given). */
+mtp_status mtp_loss_assemble_weighted(int D, const double* sums_counts, double n_positions,
+                                      const float* depth_weights, float lambda, int den, int with_main,
+                                      float* losses, cudaStream_t stream);
 
 /* Exact speculative verification of R requests with gamma drafts each
  * ([M7.6] §0x09 one-proposal selector, generalised to gamma by the

@@ -79,3 +79,10 @@ def test_two_rank_reduction_matches_single_process():
                 for l in (l0, l1)]
     ref = oc.assemble_loss(single[0::2], single[1::2], CFG.B * CFG.T, CFG.D, CFG.lam, "masked_mean")["loss_total"]
     assert not np.isclose(np.mean(per_rank), ref, rtol=1e-9)
+
+
+def test_lambda_schedule_matches_the_oracle():
+    from deepseek_sequential_mtp_gb300 import dp
+    from oracle import chain as oc
+    for t in (0, 1e12, 9.99e12, 10e12, 12e12, 14.8e12):
+        assert dp.deepseek_v3_lambda(t) == oc.deepseek_v3_lambda(t)
