@@ -7,7 +7,8 @@
 // speculative-decoding page.  Uniforms: Philox4x32-10 (Salmon et al., SC'11).
 //
 // Layout on the GPU: a cluster of 2 CTAs per request, one CTA per SM (544
-// threads: 16 consumer warps and one producer warp, 128 KB ring), so the 64
+// threads: 16 consumer warps and one producer warp, 128 KB ring of four
+// 32 KB stages), so the 64
 // requests of a decode batch occupy 128 SMs in one wave.
 //   phase A  warp 0 of every CTA: lane j evaluates draft position j (two
 //            scalar loads, one Philox block, one fp64 division); a ballot
@@ -26,11 +27,12 @@
 // bonus, plus 8*gamma bytes of scalars.
 // Ring invariant: a parity wait cannot tell phase u+1 from phase u-1, so no
 // waiter may reach a barrier more than one phase ahead of its last completed
-// phase.  Consumer warp w takes chunks w, w+16, ..., i.e. stages w/2 + 8m;
-// with a ring of 8 stages it always lands on slot w/2 and sees that slot's
-// phases one after another (it waited on use u-1 itself before waiting on
-// use u).  The producer issues use u of a slot only after both consumers of
-// use u-1 released it, and waits for every copy it issued before it leaves.
+// phase.  With S chunks per stage, consumer warp w takes chunks w, w+16, ...,
+// i.e. stages w/S + (16/S) m; a ring of a multiple of 16/S stages keeps it on
+// the same slot(s), so it sees each slot's phases one after another (it
+// waited on use u-1 itself before waiting on use u).  The producer issues use
+// u of a slot only after every consumer of use u-1 released it, and waits for
+// every copy it issued before it leaves.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -45,8 +47,8 @@ namespace {
 constexpr int kThreads = 544;  // 16 consumer warps + 1 producer warp
 constexpr int kCluster = 2;
 constexpr int kConsumerWarps = 16;
-constexpr int kStageChunks = 2;  // chunks per ring stage
-constexpr int kRing = 8;          // ring stages (2 x 4 KB x 2 rows each)
+constexpr int kStageChunks = 4;  // chunks per ring stage: 16 KB bulk copies per row (a copy has a fixed cost)
+constexpr int kRing = 4;          // ring stages (4 x 4 KB x 2 rows each)
 constexpr int kStageBytes = 2 * kStageChunks * 1024 * 4;
 constexpr int kRingBytes = kRing * kStageBytes;
 
@@ -298,8 +300,10 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
         __syncwarp();
         if (lane == 0) {
           all0[c_begin + li] = make_float2(hi, lo);
+          // a stage expects kStageChunks arrivals; in a partial last stage the
+          // consumer of its first chunk also supplies those of the missing chunks
           const int nch = min(kStageChunks, n_local - st * kStageChunks);
-          mbar_arrive_cnt(s_empty_bar + 8u * slot, nch == kStageChunks ? 1u : static_cast<uint32_t>(kStageChunks));
+          mbar_arrive_cnt(s_empty_bar + 8u * slot, i == 0 ? 1u + static_cast<uint32_t>(kStageChunks - nch) : 1u);
         }
       }
     }
