@@ -22,6 +22,7 @@
 // epilogue (logits never stored) -> per-row CE and per-term sums.
 // GEMMs run on the tcgen05 core (gemm_tc.cu); the f32 specialisation (small
 // shapes) runs the same steps on SIMT kernels in fp32.
+#include <algorithm>
 #include <cmath>
 
 #include "gemm_tc.cuh"
@@ -384,7 +385,7 @@ __global__ void head_ce_f32_kernel(const float* __restrict__ x, const float* __r
 // one warp per row, one (sum, count) atomic pair per block of 8 rows
 __global__ void ce_reduce_kernel(int M, int nvt, const float2* __restrict__ part, const float* __restrict__ zt,
                                  const int32_t* __restrict__ labels, float* __restrict__ row_loss,
-                                 double* __restrict__ sum_count) {
+                                 double* __restrict__ sum_count, float* __restrict__ lse_out) {
   __shared__ float s_loss[8];
   __shared__ int s_sup[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -402,7 +403,9 @@ __global__ void ce_reduce_kernel(int M, int nvt, const float2* __restrict__ part
       sum += v.y * expf(v.x - mx);
     }
     sum = mtp::warp_sum(sum);
-    loss = (mx + logf(sum)) - zt[m];
+    const float lse = mx + logf(sum);
+    loss = lse - zt[m];
+    if (lse_out && lane == 0) lse_out[m] = lse;
   }
   if (lane == 0) {
     if (m < M && row_loss) row_loss[m] = loss;
@@ -543,6 +546,7 @@ struct Ctx {
   Layout L;
   cudaStream_t st;
   int M;
+  float* lse_save = nullptr;  // training: per-term log-sum-exp of every supervised row, [(D+1), M]
   template <typename T>
   T* buf(size_t off) const {
     return reinterpret_cast<T*>(ws + off);
@@ -675,7 +679,9 @@ mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double
                                                              part, zt, C.L.nvt);
     mtp::note_launch();
   }
-  ce_reduce_kernel<<<(C.M + 7) / 8, 256, 0, C.st>>>(C.M, C.L.nvt, part, zt, labels, row_loss_term, sum_count);
+  ce_reduce_kernel<<<(C.M + 7) / 8, 256, 0, C.st>>>(
+      C.M, C.L.nvt, part, zt, labels, row_loss_term, sum_count,
+      C.lse_save ? C.lse_save + static_cast<size_t>(k) * C.M : nullptr);
   mtp::note_launch();
   MTP_LAUNCH_CHECK();
   return MTP_OK;
@@ -851,4 +857,278 @@ extern "C" mtp_status mtp_loss_assemble_weighted(int D, const double* sums_count
 extern "C" mtp_status mtp_loss_assemble(int D, const double* sums_counts, double n_positions, float lambda, int den,
                                         int with_main, float* losses, cudaStream_t stream) {
   return mtp_loss_assemble_weighted(D, sums_counts, n_positions, nullptr, lambda, den, with_main, losses, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Training step: the forward with its states saved, then gradients.
+// "M7.6 - DeepSeek MTP" §0x05: the shared head (and embedding) receive the
+// main term's and every depth's gradient; depth k's states receive the
+// gradients of terms k..D through the recurrence.
+// ---------------------------------------------------------------------------
+namespace {
+
+// dL/dl of one supervised row of each term (the loss assembly's definitions)
+__global__ void term_scale_kernel(const double* __restrict__ sc, float* __restrict__ scale, int D, double n_pos,
+                                  DepthWeights W, int den, int with_main) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  auto weight = [&](int k) -> double {
+    return W.uniform ? static_cast<double>(W.lambda) / D : static_cast<double>(W.w[k - 1]);
+  };
+  double n_all = 0.0, wn_all = 0.0;
+  for (int k = 1; k <= D; ++k) {
+    n_all += sc[2 * k + 1];
+    wn_all += weight(k) * sc[2 * k + 1];
+  }
+  auto inv = [](double b) { return b > 0.0 ? 1.0 / b : 0.0; };
+  auto term_inv = [&](int t) -> double {
+    if (den == MTP_DEN_FIXED) return 1.0 / n_pos;
+    if (den == MTP_DEN_SUM) return 1.0;
+    if (den == MTP_DEN_MASKED_MEAN || t == 0) return inv(sc[2 * t + 1]);
+    if (den == MTP_DEN_GLOBAL) return inv(n_all);
+    return inv(wn_all);
+  };
+  scale[0] = with_main ? static_cast<float>(term_inv(0)) : 0.f;
+  for (int k = 1; k <= D; ++k) scale[k] = static_cast<float>(weight(k) * term_inv(k));
+}
+
+// out[c][r] = in[r][c] for a bf16 [R, C] matrix; 32 x 32 tiles through shared memory
+__global__ void transpose_bf16_kernel(const __nv_bfloat16* __restrict__ in, int R, int Cn, int ldi,
+                                      __nv_bfloat16* __restrict__ out, int ldo) {
+  __shared__ __nv_bfloat16 tile[32][34];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  const int tx = threadIdx.x, ty = threadIdx.y;  // block (32, 8)
+  for (int j = ty; j < 32; j += 8) {
+    const int r = r0 + j, c = c0 + tx;
+    if (r < R && c < Cn) tile[j][tx] = in[static_cast<size_t>(r) * ldi + c];
+  }
+  __syncthreads();
+  for (int j = ty; j < 32; j += 8) {
+    const int c = c0 + j, r = r0 + tx;
+    if (c < Cn && r < R) out[static_cast<size_t>(c) * ldo + r] = tile[tx][j];
+  }
+}
+
+void transpose_bf16(const __nv_bfloat16* in, int R, int Cn, int ldi, __nv_bfloat16* out, int ldo, cudaStream_t st) {
+  transpose_bf16_kernel<<<dim3((Cn + 31) / 32, (R + 31) / 32), dim3(32, 8), 0, st>>>(in, R, Cn, ldi, out, ldo);
+  mtp::note_launch();
+}
+
+// RMSNorm backward for y = g * h * r, r = (mean(h^2) + eps)^(-1/2), given
+// dy: dh += r (g dy - xh * mean(g dy xh)) with xh = h r; dg += sum over rows
+// of dy xh.  A block of 8 warps takes 64 rows (8 per warp); the gain
+// gradient is summed in shared memory and added to dg once per block.
+constexpr int kNormBwdRows = 64;
+__global__ void __launch_bounds__(256)
+rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, const __nv_bfloat16* __restrict__ g,
+                   const float* __restrict__ dy, float* __restrict__ dh, float* __restrict__ dg, int M, int d,
+                   float eps) {
+  extern __shared__ float s_dg[];
+  for (int i = threadIdx.x; i < d; i += blockDim.x) s_dg[i] = 0.f;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int j = 0; j < kNormBwdRows / 8; ++j) {
+    const int m = blockIdx.x * kNormBwdRows + warp * (kNormBwdRows / 8) + j;
+    if (m >= M) break;
+    const __nv_bfloat16* hr = h + static_cast<size_t>(m) * d;
+    const float* dyr = dy + static_cast<size_t>(m) * d;
+    float ss = 0.f, dot = 0.f;
+    for (int i = lane; i < d; i += 32) {
+      const float hv = __bfloat162float(hr[i]);
+      ss += hv * hv;
+      dot += __bfloat162float(g[i]) * dyr[i] * hv;
+    }
+    ss = mtp::warp_sum(ss);
+    dot = mtp::warp_sum(dot);
+    const float r = 1.0f / sqrtf(ss / d + eps);
+    const float mean_gdx = dot * r / d;  // mean over the row of g dy xh
+    float* dhr = dh + static_cast<size_t>(m) * d;
+    for (int i = lane; i < d; i += 32) {
+      const float xh = __bfloat162float(hr[i]) * r;
+      const float dyv = dyr[i];
+      dhr[i] += r * (__bfloat162float(g[i]) * dyv - xh * mean_gdx);
+      atomicAdd(&s_dg[i], dyv * xh);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < d; i += blockDim.x) atomicAdd(&dg[i], s_dg[i]);
+}
+
+// a += b (fp32, n elements)
+__global__ void add_f32_kernel(float* __restrict__ a, const float* __restrict__ b, size_t n) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    a[i] += b[i];
+}
+
+inline int round_up8(int v) { return (v + 7) / 8 * 8; }
+
+struct TrainLayout {
+  size_t hs, lse, scale, wut, xt, dz, dzt, dx, dstate, total;
+  int vc, vp, mp;
+};
+
+// after the forward's own workspace: the saved states h^1..h^D, the per-term
+// log-sum-exp, the per-term row scales, W_U^T, and the head-backward buffers
+TrainLayout make_train_layout(const mtp_dims& D) {
+  TrainLayout T{};
+  const size_t M = static_cast<size_t>(D.B) * D.T, d = D.d;
+  T.vp = round_up8(D.V);
+  T.mp = round_up8(static_cast<int>(M));
+  T.vc = std::min(8192, T.vp);
+  size_t off = make_layout(D).total;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes);
+    return o;
+  };
+  T.hs = take(static_cast<size_t>(D.D) * M * d * 2);
+  T.lse = take(static_cast<size_t>(D.D + 1) * M * 4);
+  T.scale = take(static_cast<size_t>(D.D + 1) * 4);
+  T.wut = take(d * T.vp * 2);
+  T.xt = take(d * T.mp * 2);
+  T.dz = take(M * T.vc * 2);
+  T.dzt = take(static_cast<size_t>(T.vc) * T.mp * 2);
+  T.dx = take(M * d * 4);
+  T.dstate = take(static_cast<size_t>(D.D + 1) * M * d * 4);
+  T.total = off;
+  return T;
+}
+
+mtp::GemmDesc gdesc(int M, int N, int K, const __nv_bfloat16* A, int lda, const __nv_bfloat16* B, int ldb) {
+  mtp::GemmDesc g;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.A = A;
+  g.lda = lda;
+  g.B[0] = B;
+  g.ldb = ldb;
+  g.nseg = 1;
+  g.seg_rows = N;
+  return g;
+}
+
+// gradients through the shared head and the final norm of term t (state h_t):
+// per vocabulary chunk the logits are recomputed twice -- as [tokens, chunk]
+// for dz and as [chunk, tokens] for dz^T -- and never stored whole; then
+// dX += dz W_U[chunk] and d_head[chunk] += dz^T X; finally the final RMSNorm's
+// backward adds d h_t into dstate[t] and accumulates d_out_norm.
+mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_bfloat16* h_t, float* d_head,
+                         float* d_out_norm) {
+  using bf = __nv_bfloat16;
+  const mtp_dims& D = C.D;
+  const int M = C.M, d = D.d, V = D.V;
+  bf* x = C.buf<bf>(C.L.x);
+  int32_t* labels = C.buf<int32_t>(C.L.labels);
+  const bf* WU = static_cast<const bf*>(C.W.head);
+  const bf* out_norm = static_cast<const bf*>(C.W.out_norm);
+  bf* xt = C.buf<bf>(T.xt);
+  bf* dz = C.buf<bf>(T.dz);
+  bf* dzt = C.buf<bf>(T.dzt);
+  bf* wut = C.buf<bf>(T.wut);
+  float* dx = C.buf<float>(T.dx);
+  const float* lse = C.buf<float>(T.lse) + static_cast<size_t>(t) * M;
+  const float* scale = C.buf<float>(T.scale) + t;
+  launch_rmsnorm<bf>(C, h_t, out_norm, x, labels, t);
+  transpose_bf16(x, M, d, d, xt, T.mp, C.st);
+  MTP_CUDA_TRY(cudaMemsetAsync(dx, 0, static_cast<size_t>(M) * d * 4, C.st));
+  for (int v0 = 0; v0 < V; v0 += T.vc) {
+    const int vc = std::min(T.vc, V - v0);
+    mtp::GemmDesc g = gdesc(M, vc, d, x, d, WU + static_cast<size_t>(v0) * d, d);
+    g.epi = mtp::EPI_CE_GRAD;
+    g.out = dz;
+    g.ldo = T.vc;
+    g.labels = labels;
+    g.lse = lse;
+    g.ce_scale = scale;
+    g.ce_offset = v0;
+    TRY(mtp::gemm_bf16_launch(g, C.st));
+    g = gdesc(vc, M, d, WU + static_cast<size_t>(v0) * d, d, x, d);
+    g.epi = mtp::EPI_CE_GRAD_T;
+    g.out = dzt;
+    g.ldo = T.mp;
+    g.labels = labels;
+    g.lse = lse;
+    g.ce_scale = scale;
+    g.ce_offset = v0;
+    TRY(mtp::gemm_bf16_launch(g, C.st));
+    g = gdesc(M, d, vc, dz, T.vc, wut + v0, T.vp);
+    g.epi = mtp::EPI_F32_ACC;
+    g.out_f32 = dx;
+    g.ldo = d;
+    TRY(mtp::gemm_bf16_launch(g, C.st));
+    g = gdesc(vc, d, M, dzt, T.mp, xt, T.mp);
+    g.epi = mtp::EPI_F32_ACC;
+    g.out_f32 = d_head + static_cast<size_t>(v0) * d;
+    g.ldo = d;
+    TRY(mtp::gemm_bf16_launch(g, C.st));
+  }
+  float* dstate_t = C.buf<float>(T.dstate) + static_cast<size_t>(t) * M * d;
+  rmsnorm_bwd_kernel<<<(M + kNormBwdRows - 1) / kNormBwdRows, 256, d * sizeof(float), C.st>>>(
+      h_t, out_norm, dx, dstate_t, d_out_norm, M, d, D.eps);
+  mtp::note_launch();
+  MTP_LAUNCH_CHECK();
+  return MTP_OK;
+}
+
+}  // namespace
+
+extern "C" size_t mtp_chain_grad_workspace_bytes(const mtp_dims* dims) {
+  if (!dims || !valid_dims(*dims) || supported(*dims) != MTP_OK || dims->dtype != MTP_BF16) return 0;
+  return make_train_layout(*dims).total;
+}
+
+extern "C" mtp_status mtp_chain_loss_grad(const mtp_dims* dims, const mtp_weights* w, const int32_t* tokens,
+                                          const int32_t* seg, const int32_t* pos, const void* h0, float lambda,
+                                          int den, int with_main, const float* depth_weights, double* sums_counts,
+                                          float* losses, const mtp_grads* grads, void* ws, size_t ws_bytes,
+                                          cudaStream_t stream) {
+  using bf = __nv_bfloat16;
+  if (!dims) return MTP_ERR_INVALID_ARG;
+  if (dims->dtype != MTP_BF16) return MTP_ERR_UNSUPPORTED;
+  TRY(check_common(dims, w, tokens, seg, pos, h0, ws, ws_bytes));
+  if (!sums_counts || !losses || !grads || !grads->head || !grads->out_norm) return MTP_ERR_INVALID_ARG;
+  if (!valid_den(den)) return MTP_ERR_INVALID_ARG;
+  if (depth_weights && dims->D > kMaxDepthWeights) return MTP_ERR_UNSUPPORTED;
+  const mtp_dims& D = *dims;
+  // this build computes the shared head's and the final norm's gradients for
+  // every term, and the gradient of h^0 when only the main term is weighted
+  bool depth_weighted = depth_weights ? false : lambda != 0.f;
+  if (depth_weights)
+    for (int k = 0; k < D.D; ++k) depth_weighted |= depth_weights[k] != 0.f;
+  if (grads->embed || (grads->h0 && depth_weighted)) return MTP_ERR_UNSUPPORTED;
+  for (const void* p : {static_cast<const void*>(grads->head), static_cast<const void*>(grads->out_norm),
+                        static_cast<const void*>(grads->h0)})
+    if (p && !mtp::aligned16(p)) return MTP_ERR_ALIGNMENT;
+  const TrainLayout T = make_train_layout(D);
+  if (ws_bytes < T.total) return MTP_ERR_WORKSPACE;
+  Ctx C{D, *w, tokens, seg, pos, static_cast<uint8_t*>(ws), make_layout(D), stream, D.B * D.T};
+  C.lse_save = C.buf<float>(T.lse);
+  bf* hs = C.buf<bf>(T.hs);
+  const int M = C.M, d = D.d;
+  const size_t Md = static_cast<size_t>(M) * d;
+  TRY(run_chain<bf>(C, static_cast<const bf*>(h0), hs, true, lambda, den, with_main, sums_counts, losses, nullptr));
+  DepthWeights W{};
+  W.lambda = lambda;
+  W.uniform = depth_weights ? 0 : 1;
+  if (depth_weights) {
+    for (int k = 0; k < D.D; ++k) W.w[k] = depth_weights[k];
+    loss_assemble_kernel<<<1, 32, 0, stream>>>(sums_counts, losses, D.D, static_cast<double>(M), W, den, with_main);
+    mtp::note_launch();
+  }
+  term_scale_kernel<<<1, 32, 0, stream>>>(sums_counts, C.buf<float>(T.scale), D.D, static_cast<double>(M), W, den,
+                                          with_main);
+  mtp::note_launch();
+  transpose_bf16(static_cast<const bf*>(w->head), D.V, d, d, C.buf<bf>(T.wut), T.vp, stream);
+  MTP_CUDA_TRY(cudaMemsetAsync(C.buf<float>(T.dstate), 0, static_cast<size_t>(D.D + 1) * Md * 4, stream));
+  for (int t = with_main ? 0 : 1; t <= D.D; ++t) {
+    const bf* h_t = t == 0 ? static_cast<const bf*>(h0) : hs + static_cast<size_t>(t - 1) * Md;
+    TRY(head_backward(C, T, t, h_t, grads->head, grads->out_norm));
+  }
+  if (grads->h0) {
+    add_f32_kernel<<<2 * 152, 256, 0, stream>>>(grads->h0, C.buf<float>(T.dstate), Md);
+    mtp::note_launch();
+  }
+  MTP_LAUNCH_CHECK();
+  return MTP_OK;
 }

@@ -49,7 +49,7 @@ struct Cfg {
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
   // per epilogue warp: two 32 x 64 bf16 boxes (4 KB each); none for the CE epilogue
   static constexpr int kBoxBytes = 32 * 64 * 2;
-  static constexpr int kStagingBytes = (EPI == EPI_CE || EPI >= EPI_T_STORE) ? 0 : 4 * 2 * kBoxBytes;
+  static constexpr int kStagingBytes = epi_uses_staging(EPI) ? 4 * 2 * kBoxBytes : 0;
   static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024 + 256;
 };
 
@@ -198,6 +198,9 @@ struct Args {
   float* z_tgt;
   float* out_f32;
   int splits;
+  const float* lse;
+  const float* ce_scale;
+  int ce_offset;
 };
 
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
@@ -585,6 +588,74 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
           }
         }
+      } else if constexpr (EPI == EPI_CE_GRAD) {
+        const int lab = row_ok ? P.labels[row] : -1;
+        const float lse = lab >= 0 ? P.lse[row] : 0.f;
+        const float sc = lab >= 0 ? *P.ce_scale : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          const int col0 = tn * BN + c * 64;
+          uint8_t* box = claim();
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float v[32];
+            tmem_ld32(taddr + c * 64 + half * 32, v);
+            const int off = lab - (P.ce_offset + col0 + half * 32);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = lab >= 0 ? (__expf(v[i] - lse) - (i == off ? 1.f : 0.f)) * sc : 0.f;
+            box_write32(box, lane, half, v);
+          }
+          ship(box, col0, row0w);
+        }
+      } else if constexpr (EPI == EPI_CE_GRAD_T) {
+        // rows = vocabulary entries, columns = tokens: lane i fetches token
+        // (col + i)'s label and lse, shuffles hand them to every row's lane
+        const float sc = *P.ce_scale;
+        const int vocab = P.ce_offset + row;
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          const int col0 = tn * BN + c * 64;
+          uint8_t* box = claim();
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int tok = col0 + half * 32 + lane;
+            const int my_lab = tok < P.N ? P.labels[tok] : -1;
+            const float my_lse = my_lab >= 0 ? P.lse[tok] : 0.f;
+            float v[32];
+            tmem_ld32(taddr + c * 64 + half * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int lab = __shfl_sync(0xffffffffu, my_lab, i);
+              const float lse = __shfl_sync(0xffffffffu, my_lse, i);
+              v[i] = lab >= 0 ? (__expf(v[i] - lse) - (vocab == lab ? 1.f : 0.f)) * sc : 0.f;
+            }
+            box_write32(box, lane, half, v);
+          }
+          ship(box, col0, row0w);
+        }
+      } else if constexpr (EPI == EPI_F32_ACC) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(taddr + c * 32, v);
+          const int col0 = tn * BN + c * 32;
+          if (row_ok && col0 < P.N) {
+            float* dst = P.out_f32 + static_cast<size_t>(row) * P.ldo + col0;
+            if (col0 + 32 <= P.N) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                float4 o = *reinterpret_cast<float4*>(dst + 4 * q);
+                o.x += v[4 * q];
+                o.y += v[4 * q + 1];
+                o.z += v[4 * q + 2];
+                o.w += v[4 * q + 3];
+                *reinterpret_cast<float4*>(dst + 4 * q) = o;
+              }
+            } else {
+              for (int i = 0; i < 32 && col0 + i < P.N; ++i) dst[i] += v[i];
+            }
+          }
+        }
       } else if constexpr (EPI == EPI_CE) {
         const int lab = row_ok ? P.labels[row] : -1;
         float m_run = -INFINITY, s_run = 0.0f, zt = 0.0f;
@@ -705,7 +776,7 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
   }
   // output / residual boxes: 32 rows x 64 columns, 128-byte swizzle
   CUtensorMap tout = ta;
-  if (EPI != EPI_CE && EPI < EPI_T_STORE && !make_map(&tout, g.out, g.M, g.N, g.ldo, 32)) return MTP_ERR_INVALID_ARG;
+  if (epi_uses_staging(EPI) && !make_map(&tout, g.out, g.M, g.N, g.ldo, 32)) return MTP_ERR_INVALID_ARG;
   Args a{};
   a.M = g.M;
   a.N = g.N;
@@ -728,6 +799,9 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
   a.z_tgt = g.z_tgt;
   a.out_f32 = g.out_f32;
   a.splits = g.splits > 0 ? g.splits : 1;
+  a.lse = g.lse;
+  a.ce_scale = g.ce_scale;
+  a.ce_offset = g.ce_offset;
   const int ntiles = a.tiles_m * a.tiles_n * a.splits;
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
   gemm_tc_kernel<BN, EPI><<<grid, kThreads, C::kSmemBytes, stream>>>(ta, tb[0], tb[1], tb[2], tout, a);
@@ -755,11 +829,13 @@ bool tensor_map_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t
 mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return MTP_ERR_SHAPE;
   if (!g.A || !g.B[0]) return MTP_ERR_INVALID_ARG;
-  if (g.K % 8 || g.lda % 8 || g.ldb % 8) return MTP_ERR_ALIGNMENT;
+  // TMA needs 16-byte row strides; a K extent that is not a multiple of the
+  // k-block is zero-filled by the copies
+  if (g.lda % 8 || g.ldb % 8) return MTP_ERR_ALIGNMENT;
   if (!aligned16(g.A)) return MTP_ERR_ALIGNMENT;
   for (int i = 0; i < 3; ++i)
     if (g.B[i] && !aligned16(g.B[i])) return MTP_ERR_ALIGNMENT;
-  if (g.epi != EPI_CE && g.epi < EPI_T_STORE && (!g.out || g.ldo % 8 || !aligned16(g.out))) return MTP_ERR_ALIGNMENT;
+  if (epi_uses_staging(g.epi) && (!g.out || g.ldo % 8 || !aligned16(g.out))) return MTP_ERR_ALIGNMENT;
   if (!encoder()) return MTP_ERR_CUDA;
   switch (g.epi) {
     case EPI_STORE:
@@ -784,6 +860,13 @@ mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream) {
     case EPI_CE:
       if (!g.labels || !g.ce_part || !g.z_tgt) return MTP_ERR_INVALID_ARG;
       return launch<256, EPI_CE>(g, stream);
+    case EPI_CE_GRAD:
+    case EPI_CE_GRAD_T:
+      if (!g.labels || !g.lse || !g.ce_scale) return MTP_ERR_INVALID_ARG;
+      return g.epi == EPI_CE_GRAD ? launch<256, EPI_CE_GRAD>(g, stream) : launch<256, EPI_CE_GRAD_T>(g, stream);
+    case EPI_F32_ACC:
+      if (!g.out_f32 || g.ldo % 4 || !aligned16(g.out_f32) || g.splits > 1) return MTP_ERR_INVALID_ARG;
+      return launch<256, EPI_F32_ACC>(g, stream);
     case EPI_T_STORE:
     case EPI_T_ATOMIC: {
       if (g.N > 32 || !g.out_f32 || g.nseg != 1) return MTP_ERR_UNSUPPORTED;

@@ -43,6 +43,11 @@ class Weights(ctypes.Structure):
                 ("out_norm", ctypes.c_void_p)] + [(k, _PP) for k in _WEIGHT_LISTS]
 
 
+class Grads(ctypes.Structure):
+    _fields_ = [("embed", ctypes.c_void_p), ("head", ctypes.c_void_p), ("out_norm", ctypes.c_void_p),
+                ("h0", ctypes.c_void_p)] + [(k, _PP) for k in _WEIGHT_LISTS]
+
+
 _lib = None
 
 
@@ -90,6 +95,12 @@ def load() -> ctypes.CDLL:
     lib.mtp_draft_step.restype = i32
     lib.mtp_draft_step.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Weights), vp, vp, vp, vp, vp, vp,
                                    u64, u64, vp, vp, vp, vp, sz, vp]
+    lib.mtp_chain_grad_workspace_bytes.restype = sz
+    lib.mtp_chain_grad_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
+    lib.mtp_chain_loss_grad.restype = i32
+    lib.mtp_chain_loss_grad.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Weights), vp, vp, vp, vp,
+                                        ctypes.c_float, i32, i32, ctypes.POINTER(ctypes.c_float), vp, vp,
+                                        ctypes.POINTER(Grads), vp, sz, vp]
     lib.mtp_kernel_launches.restype = ctypes.c_ulonglong
     lib.mtp_kernel_launches.argtypes = []
     _lib = lib
@@ -231,6 +242,47 @@ class Chain:
         if nbytes == 0:
             raise MtpError("invalid chain dimensions")
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def loss_grad(self, tokens, seg, pos, h0, grads: dict, lam=None, den="fixed", with_main=True,
+                  depth_weights=None, out=None, stream=None):
+        """Training step (include/mtp.h: mtp_chain_loss_grad): losses as
+        ``loss`` and the gradients added into ``grads`` (fp32 tensors keyed as
+        the weights, plus "h0"; per-depth entries are lists; missing keys are
+        not computed)."""
+        cfg = self.cfg
+        _check_chain_inputs(cfg, tokens, seg, pos, h0, self.weights)
+        if not hasattr(self, "gws"):
+            nbytes = int(load().mtp_chain_grad_workspace_bytes(ctypes.byref(self.dims)))
+            if nbytes == 0:
+                raise MtpError("the training step does not support these dimensions")
+            self.gws = torch.empty(nbytes, dtype=torch.uint8, device=h0.device)
+        dev = h0.device
+        if out is None:
+            out = {"sums_counts": torch.empty(2 * (cfg.D + 1), dtype=torch.float64, device=dev),
+                   "losses": torch.empty(cfg.D + 2, dtype=torch.float32, device=dev)}
+        g = Grads()
+        keep = []
+        for k in ("embed", "head", "out_norm", "h0"):
+            t = grads.get(k)
+            if t is not None:
+                _need(t, f"grads[{k!r}]", torch.float32)
+                setattr(g, k, t.data_ptr())
+        for k in _WEIGHT_LISTS:
+            lst = grads.get(k)
+            if lst is not None:
+                arr = (ctypes.c_void_p * cfg.D)(*[t.data_ptr() for t in lst])
+                keep.append(arr)
+                setattr(g, k, ctypes.cast(arr, _PP))
+        w = None
+        if depth_weights is not None:
+            w = (ctypes.c_float * cfg.D)(*[float(x) for x in depth_weights])
+        st = load().mtp_chain_loss_grad(ctypes.byref(self.dims), ctypes.byref(self.w.struct),
+                                        _ptr(tokens), _ptr(seg), _ptr(pos), _ptr(h0),
+                                        float(cfg.lam if lam is None else lam), DEN[den], int(with_main), w,
+                                        _ptr(out["sums_counts"]), _ptr(out["losses"]), ctypes.byref(g),
+                                        _ptr(self.gws), self.gws.numel(), _stream(stream))
+        _check(st, "mtp_chain_loss_grad")
+        return out
 
     def forward(self, tokens, seg, pos, h0, h_out=None, stream=None):
         cfg = self.cfg

@@ -242,6 +242,48 @@ mtp_status spec_verify(int R, int gamma, int V, const float* p, const float* q,
                        int32_t* accepted, int32_t* next_token, int32_t* n_emit,
                        int32_t* status, cudaStream_t stream);
 
+/* Gradient buffers of the training step (fp32, device, same shapes as the
+ * corresponding weights; the step ADDS into them, so the caller zeroes them
+ * or accumulates across calls).  Per-depth members are host arrays of D
+ * device pointers.  NULL members are not computed. */
+typedef struct mtp_grads {
+  float* embed;     /* [V, d] */
+  float* head;      /* [V, d] */
+  float* out_norm;  /* [d] */
+  float* h0;        /* [B, T, d]: gradient with respect to the main model's hidden states */
+  float* const* hnorm;
+  float* const* enorm;
+  float* const* eh_proj;
+  float* const* attn_norm;
+  float* const* wq;
+  float* const* wk;
+  float* const* wv;
+  float* const* wo;
+  float* const* ffn_norm;
+  float* const* w_gate;
+  float* const* w_up;
+  float* const* w_down;
+} mtp_grads;
+
+/* Bytes of device workspace mtp_chain_loss_grad needs (0 if unsupported). */
+size_t mtp_chain_grad_workspace_bytes(const mtp_dims* dims);
+
+/* Training step of the chain: mtp_chain_loss's forward (same arguments and
+ * outputs, with optional per-depth weights as in mtp_loss_assemble_weighted)
+ * followed by the gradients of the assembled loss, added into `grads`
+ * ([M7.6] §0x05: the shared head receives the main term's and every depth's
+ * gradient).  The head backward recomputes the logits per vocabulary chunk
+ * (as [tokens, chunk] for dz = (softmax - onehot) dL/dl and as [chunk,
+ * tokens] for dz^T) and never stores them whole.  bf16 only.
+ * This build fills grads->head and grads->out_norm for every term and
+ * grads->h0 when no depth term is weighted (lambda = 0 or all depth weights
+ * 0); requesting grads->embed, or grads->h0 with weighted depth terms,
+ * returns MTP_ERR_UNSUPPORTED. */
+mtp_status mtp_chain_loss_grad(const mtp_dims* dims, const mtp_weights* w, const int32_t* tokens,
+                               const int32_t* seg, const int32_t* pos, const void* h0, float lambda, int den,
+                               int with_main, const float* depth_weights, double* sums_counts, float* losses,
+                               const mtp_grads* grads, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Bytes of device workspace mtp_draft_step needs (0 if the sizes are invalid). */
 size_t mtp_draft_workspace_bytes(const mtp_dims* dims);
 
