@@ -536,6 +536,11 @@ Layout make_layout(const mtp_dims& D) {
   return L;
 }
 
+// per-depth activations a training step keeps (offsets inside one depth's slot)
+struct SaveOff {
+  size_t c, u, x, qkv, o, a, y, bytes;
+};
+
 struct Ctx {
   const mtp_dims& D;
   const mtp_weights& W;
@@ -547,6 +552,8 @@ struct Ctx {
   cudaStream_t st;
   int M;
   float* lse_save = nullptr;  // training: per-term log-sum-exp of every supervised row, [(D+1), M]
+  uint8_t* save = nullptr;     // training: depth i's activations at save + i * so.bytes
+  SaveOff so{};
   template <typename T>
   T* buf(size_t off) const {
     return reinterpret_cast<T*>(ws + off);
@@ -719,9 +726,20 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
   T* o = C.buf<T>(C.L.o);
   T* a = C.buf<T>(C.L.a);
   T* g = C.buf<T>(C.L.g);
+  T* y = x;  // the FFN norm's output (its own saved buffer in a training step)
   const T* h_prev = h0;
   for (int k = 1; k <= D.D; ++k) {
     const int i = k - 1;
+    if (C.save) {
+      uint8_t* sv = C.save + static_cast<size_t>(i) * C.so.bytes;
+      c = reinterpret_cast<T*>(sv + C.so.c);
+      u = reinterpret_cast<T*>(sv + C.so.u);
+      x = reinterpret_cast<T*>(sv + C.so.x);
+      qkv = reinterpret_cast<T*>(sv + C.so.qkv);
+      o = reinterpret_cast<T*>(sv + C.so.o);
+      a = reinterpret_cast<T*>(sv + C.so.a);
+      y = reinterpret_cast<T*>(sv + C.so.y);
+    }
     T* h_k = h_out ? h_out + static_cast<size_t>(i) * Md : C.buf<T>((k & 1) ? C.L.h1buf : C.L.h0buf);
     auto wt = [&](const void* const* arr) { return static_cast<const T*>(arr[i]); };
     mtp::prof_begin(MTP_KC_PROLOGUE, C.st);
@@ -753,10 +771,10 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
     mtp::prof_begin(MTP_KC_O_GEMM, C.st);
     TRY(gemm<T>(C, o, d, wo, 1, d, d, d, a, d, mtp::EPI_RESID, u, d));
     mtp::prof_end(MTP_KC_O_GEMM, C.st);
-    launch_rmsnorm<T>(C, a, wt(C.W.ffn_norm), x);
+    launch_rmsnorm<T>(C, a, wt(C.W.ffn_norm), y);
     const T* wg[1] = {wt(C.W.w_gate)};
     mtp::prof_begin(MTP_KC_GATE_UP_GEMM, C.st);
-    TRY(gemm<T>(C, x, d, wg, 1, D.ffn, d, D.ffn, g, D.ffn, mtp::EPI_SWIGLU, nullptr, 0, wt(C.W.w_up)));
+    TRY(gemm<T>(C, y, d, wg, 1, D.ffn, d, D.ffn, g, D.ffn, mtp::EPI_SWIGLU, nullptr, 0, wt(C.W.w_up)));
     mtp::prof_end(MTP_KC_GATE_UP_GEMM, C.st);
     const T* wd[1] = {wt(C.W.w_down)};
     mtp::prof_begin(MTP_KC_DOWN_GEMM, C.st);
@@ -915,13 +933,15 @@ void transpose_bf16(const __nv_bfloat16* in, int R, int Cn, int ldi, __nv_bfloat
 
 // RMSNorm backward for y = g * h * r, r = (mean(h^2) + eps)^(-1/2), given
 // dy: dh += r (g dy - xh * mean(g dy xh)) with xh = h r; dg += sum over rows
-// of dy xh.  A block of 8 warps takes 64 rows (8 per warp); the gain
-// gradient is summed in shared memory and added to dg once per block.
+// of dy xh.  Row m reads h row h_rows[m] (or m) and adds its dh into row
+// dh_rows[m] with atomics (or row m plainly); dh may be null.  A block of 8
+// warps takes 64 rows (8 per warp); the gain gradient is summed in shared
+// memory and added to dg once per block.
 constexpr int kNormBwdRows = 64;
 __global__ void __launch_bounds__(256)
-rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, const __nv_bfloat16* __restrict__ g,
-                   const float* __restrict__ dy, float* __restrict__ dh, float* __restrict__ dg, int M, int d,
-                   float eps) {
+rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, int ld_h, const int32_t* __restrict__ h_rows,
+                   const __nv_bfloat16* __restrict__ g, const float* __restrict__ dy, int ld_dy, float* __restrict__ dh,
+                   int ld_dh, const int32_t* __restrict__ dh_rows, float* __restrict__ dg, int M, int d, float eps) {
   extern __shared__ float s_dg[];
   for (int i = threadIdx.x; i < d; i += blockDim.x) s_dg[i] = 0.f;
   __syncthreads();
@@ -929,8 +949,8 @@ rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, const __nv_bfloat16* __r
   for (int j = 0; j < kNormBwdRows / 8; ++j) {
     const int m = blockIdx.x * kNormBwdRows + warp * (kNormBwdRows / 8) + j;
     if (m >= M) break;
-    const __nv_bfloat16* hr = h + static_cast<size_t>(m) * d;
-    const float* dyr = dy + static_cast<size_t>(m) * d;
+    const __nv_bfloat16* hr = h + static_cast<size_t>(h_rows ? h_rows[m] : m) * ld_h;
+    const float* dyr = dy + static_cast<size_t>(m) * ld_dy;
     float ss = 0.f, dot = 0.f;
     for (int i = lane; i < d; i += 32) {
       const float hv = __bfloat162float(hr[i]);
@@ -941,16 +961,29 @@ rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, const __nv_bfloat16* __r
     dot = mtp::warp_sum(dot);
     const float r = 1.0f / sqrtf(ss / d + eps);
     const float mean_gdx = dot * r / d;  // mean over the row of g dy xh
-    float* dhr = dh + static_cast<size_t>(m) * d;
+    float* dhr = dh ? dh + static_cast<size_t>(dh_rows ? dh_rows[m] : m) * ld_dh : nullptr;
     for (int i = lane; i < d; i += 32) {
       const float xh = __bfloat162float(hr[i]) * r;
       const float dyv = dyr[i];
-      dhr[i] += r * (__bfloat162float(g[i]) * dyv - xh * mean_gdx);
+      if (dhr) {
+        const float v = r * (__bfloat162float(g[i]) * dyv - xh * mean_gdx);
+        if (dh_rows) atomicAdd(dhr + i, v);
+        else dhr[i] += v;
+      }
       atomicAdd(&s_dg[i], dyv * xh);
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < d; i += blockDim.x) atomicAdd(&dg[i], s_dg[i]);
+  if (dg)
+    for (int i = threadIdx.x; i < d; i += blockDim.x) atomicAdd(&dg[i], s_dg[i]);
+}
+
+void rmsnorm_bwd(const __nv_bfloat16* h, int ld_h, const int32_t* h_rows, const __nv_bfloat16* g, const float* dy,
+                 int ld_dy, float* dh, int ld_dh, const int32_t* dh_rows, float* dg, int M, int d, float eps,
+                 cudaStream_t st) {
+  rmsnorm_bwd_kernel<<<(M + kNormBwdRows - 1) / kNormBwdRows, 256, d * sizeof(float), st>>>(
+      h, ld_h, h_rows, g, dy, ld_dy, dh, ld_dh, dh_rows, dg, M, d, eps);
+  mtp::note_launch();
 }
 
 // a += b (fp32, n elements)
@@ -963,9 +996,11 @@ __global__ void add_f32_kernel(float* __restrict__ a, const float* __restrict__ 
 inline int round_up8(int v) { return (v + 7) / 8 * 8; }
 
 struct TrainLayout {
-  size_t hs, lse, scale, wut, xt, dz, dzt, dx, dstate, total;
+  size_t hs, lse, scale, wut, xt, dz, dzt, dx, dstate, save, total;
   int vc, vp, mp;
 };
+
+SaveOff make_save_off(const mtp_dims& D);
 
 // after the forward's own workspace: the saved states h^1..h^D, the per-term
 // log-sum-exp, the per-term row scales, W_U^T, and the head-backward buffers
@@ -990,6 +1025,7 @@ TrainLayout make_train_layout(const mtp_dims& D) {
   T.dzt = take(static_cast<size_t>(T.vc) * T.mp * 2);
   T.dx = take(M * d * 4);
   T.dstate = take(static_cast<size_t>(D.D + 1) * M * d * 4);
+  T.save = take(static_cast<size_t>(D.D) * make_save_off(D).bytes);
   T.total = off;
   return T;
 }
@@ -1030,7 +1066,7 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
   const float* lse = C.buf<float>(T.lse) + static_cast<size_t>(t) * M;
   const float* scale = C.buf<float>(T.scale) + t;
   launch_rmsnorm<bf>(C, h_t, out_norm, x, labels, t);
-  transpose_bf16(x, M, d, d, xt, T.mp, C.st);
+  if (d_head) transpose_bf16(x, M, d, d, xt, T.mp, C.st);
   MTP_CUDA_TRY(cudaMemsetAsync(dx, 0, static_cast<size_t>(M) * d * 4, C.st));
   for (int v0 = 0; v0 < V; v0 += T.vc) {
     const int vc = std::min(T.vc, V - v0);
@@ -1043,6 +1079,12 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
     g.ce_scale = scale;
     g.ce_offset = v0;
     TRY(mtp::gemm_bf16_launch(g, C.st));
+    g = gdesc(M, d, vc, dz, T.vc, wut + v0, T.vp);
+    g.epi = mtp::EPI_F32_ACC;
+    g.out_f32 = dx;
+    g.ldo = d;
+    TRY(mtp::gemm_bf16_launch(g, C.st));
+    if (!d_head) continue;
     g = gdesc(vc, M, d, WU + static_cast<size_t>(v0) * d, d, x, d);
     g.epi = mtp::EPI_CE_GRAD_T;
     g.out = dzt;
@@ -1052,11 +1094,6 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
     g.ce_scale = scale;
     g.ce_offset = v0;
     TRY(mtp::gemm_bf16_launch(g, C.st));
-    g = gdesc(M, d, vc, dz, T.vc, wut + v0, T.vp);
-    g.epi = mtp::EPI_F32_ACC;
-    g.out_f32 = dx;
-    g.ldo = d;
-    TRY(mtp::gemm_bf16_launch(g, C.st));
     g = gdesc(vc, d, M, dzt, T.mp, xt, T.mp);
     g.epi = mtp::EPI_F32_ACC;
     g.out_f32 = d_head + static_cast<size_t>(v0) * d;
@@ -1064,9 +1101,411 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
     TRY(mtp::gemm_bf16_launch(g, C.st));
   }
   float* dstate_t = C.buf<float>(T.dstate) + static_cast<size_t>(t) * M * d;
-  rmsnorm_bwd_kernel<<<(M + kNormBwdRows - 1) / kNormBwdRows, 256, d * sizeof(float), C.st>>>(
-      h_t, out_norm, dx, dstate_t, d_out_norm, M, d, D.eps);
+  rmsnorm_bwd(h_t, d, nullptr, out_norm, dx, d, dstate_t, d, nullptr, d_out_norm, M, d, D.eps, C.st);
+  MTP_LAUNCH_CHECK();
+  return MTP_OK;
+}
+
+// ---- block backward -------------------------------------------------------
+
+// y[i] = bf16(x[i]) for an fp32 [R, C] matrix (row strides ldx, ldy)
+__global__ void f32_to_bf16_kernel(const float* __restrict__ x, int ldx, __nv_bfloat16* __restrict__ y, int ldy, int R,
+                                   int Cn) {
+  const size_t n = static_cast<size_t>(R) * Cn;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t r = i / Cn, c = i % Cn;
+    y[r * ldy + c] = __float2bfloat16_rn(x[r * ldx + c]);
+  }
+}
+void f32_to_bf16(const float* x, int ldx, __nv_bfloat16* y, int ldy, int R, int Cn, cudaStream_t st) {
+  f32_to_bf16_kernel<<<4 * 152, 256, 0, st>>>(x, ldx, y, ldy, R, Cn);
   mtp::note_launch();
+}
+
+// SwiGLU backward from the recomputed pre-activations pq = [p | q] ([M, 2 ffn]
+// bf16) and dg ([M, ffn] fp32): g = silu(p) q, dp = dg q silu'(p), dq = dg silu(p)
+__global__ void swiglu_bwd_kernel(const __nv_bfloat16* __restrict__ pq, const float* __restrict__ dg,
+                                  __nv_bfloat16* __restrict__ g, __nv_bfloat16* __restrict__ dpq, int M, int ffn) {
+  const size_t n = static_cast<size_t>(M) * ffn;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t m = i / ffn, j = i % ffn;
+    const float p = __bfloat162float(pq[m * 2 * ffn + j]), q = __bfloat162float(pq[m * 2 * ffn + ffn + j]);
+    const float sg = 1.0f / (1.0f + expf(-p));
+    const float silu = p * sg;
+    const float dgv = dg[i];
+    g[i] = __float2bfloat16_rn(silu * q);
+    dpq[m * 2 * ffn + j] = __float2bfloat16_rn(dgv * q * (sg * (1.0f + p * (1.0f - sg))));
+    dpq[m * 2 * ffn + ffn + j] = __float2bfloat16_rn(dgv * silu);
+  }
+}
+
+// RoPE backward: the forward rotated (x1, x2) -> (x1 c - x2 s, x2 c + x1 s) at
+// the row's position; the gradient rotates back: (d1 c + d2 s, d2 c - d1 s).
+// dqkv [M, 3d] fp32 -> out [M, 3d] bf16 (v copied)
+__global__ void rope_bwd_kernel(const float* __restrict__ dqkv, const float2* __restrict__ rope,
+                                const int32_t* __restrict__ pos, __nv_bfloat16* __restrict__ out, int M, int d, int hd,
+                                int Tlen, int use_rope) {
+  const int half = hd / 2;
+  const size_t n = static_cast<size_t>(M) * d;  // d pairs (q and k heads) + d v columns per row
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t m = i / d;
+    const int pi = static_cast<int>(i % d);
+    const float* src = dqkv + m * 3 * d;
+    __nv_bfloat16* dst = out + m * 3 * d;
+    const int head = pi / half, j = pi % half;
+    const int col = head * hd + j;
+    const float d1 = src[col], d2 = src[col + half];
+    float c = 1.f, sn = 0.f;
+    if (use_rope) {
+      const int p = min(max(pos[m], 0), Tlen - 1);
+      const float2 cs = rope[static_cast<size_t>(p) * half + j];
+      c = cs.x;
+      sn = cs.y;
+    }
+    dst[col] = __float2bfloat16_rn(d1 * c + d2 * sn);
+    dst[col + half] = __float2bfloat16_rn(d2 * c - d1 * sn);
+    dst[2 * d + pi] = __float2bfloat16_rn(src[2 * d + pi]);
+  }
+}
+
+// token gathered by row m at depth k (the forward prologue's clamped rule)
+__global__ void shifted_tokens_kernel(const int32_t* __restrict__ tokens, int32_t* __restrict__ out, int M, int Tlen,
+                                      int k, int V) {
+  const int m = blockIdx.x * blockDim.x + threadIdx.x;
+  if (m >= M) return;
+  const int t = m % Tlen;
+  out[m] = clamp_token(tokens[m - t + min(t + k, Tlen - 1)], V);
+}
+
+// Segment-causal attention backward (SIMT; one warp per (row, head), lanes
+// own head_dim slices).  Pass 1 (per query row m): log-sum-exp of the scores
+// over keys [seg_start(m), m], D_m = do_m . o_m, and
+// dq_m = scale sum_s P_ms (do_m . v_s - D_m) k_s.
+template <int HD>
+__global__ void attn_bwd_dq_kernel(const __nv_bfloat16* __restrict__ qkv, const __nv_bfloat16* __restrict__ o,
+                                   const __nv_bfloat16* __restrict__ dO, const int32_t* __restrict__ seg_start,
+                                   float* __restrict__ dqkv, float* __restrict__ lse_out, float* __restrict__ dsum_out,
+                                   int M, int Tlen, int H, float scale) {
+  constexpr int KD = HD / 32;
+  const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (item >= M * H) return;
+  const int m = item / H, h = item % H;
+  const int d = H * HD, t = m % Tlen, row0 = m - t;
+  float q[KD], dov[KD], ov[KD];
+#pragma unroll
+  for (int i = 0; i < KD; ++i) {
+    q[i] = __bfloat162float(qkv[static_cast<size_t>(m) * 3 * d + h * HD + lane * KD + i]);
+    dov[i] = __bfloat162float(dO[static_cast<size_t>(m) * d + h * HD + lane * KD + i]);
+    ov[i] = __bfloat162float(o[static_cast<size_t>(m) * d + h * HD + lane * KD + i]);
+  }
+  float dsum = 0.f;
+#pragma unroll
+  for (int i = 0; i < KD; ++i) dsum += dov[i] * ov[i];
+  dsum = mtp::warp_sum(dsum);
+  const int lo = row0 + seg_start[m];
+  float mx = -INFINITY, l = 0.f;
+  for (int s = lo; s <= m; ++s) {
+    const __nv_bfloat16* kr = qkv + static_cast<size_t>(s) * 3 * d + d + h * HD + lane * KD;
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < KD; ++i) acc += q[i] * __bfloat162float(kr[i]);
+    const float sc = mtp::warp_sum(acc) * scale;
+    const float mn = fmaxf(mx, sc);
+    l = l * expf(mx - mn) + expf(sc - mn);
+    mx = mn;
+  }
+  const float lse = mx + logf(l);
+  float dq[KD] = {};
+  for (int s = lo; s <= m; ++s) {
+    const __nv_bfloat16* kr = qkv + static_cast<size_t>(s) * 3 * d + d + h * HD + lane * KD;
+    const __nv_bfloat16* vr = kr + d;
+    float acc = 0.f, dp = 0.f;
+    float kv[KD];
+#pragma unroll
+    for (int i = 0; i < KD; ++i) {
+      kv[i] = __bfloat162float(kr[i]);
+      acc += q[i] * kv[i];
+      dp += dov[i] * __bfloat162float(vr[i]);
+    }
+    const float sc = mtp::warp_sum(acc) * scale;
+    dp = mtp::warp_sum(dp);
+    const float ds = expf(sc - lse) * (dp - dsum);
+#pragma unroll
+    for (int i = 0; i < KD; ++i) dq[i] += ds * kv[i];
+  }
+#pragma unroll
+  for (int i = 0; i < KD; ++i) dqkv[static_cast<size_t>(m) * 3 * d + h * HD + lane * KD + i] = dq[i] * scale;
+  if (lane == 0) {
+    lse_out[static_cast<size_t>(m) * H + h] = lse;
+    dsum_out[static_cast<size_t>(m) * H + h] = dsum;
+  }
+}
+
+// Pass 2 (per key row s): the queries that see s are [s, max(seg_end(s), s+1));
+// dv_s = sum_t P_ts do_t, dk_s = scale sum_t P_ts (do_t . v_s - D_t) q_t.
+template <int HD>
+__global__ void attn_bwd_dkdv_kernel(const __nv_bfloat16* __restrict__ qkv, const __nv_bfloat16* __restrict__ dO,
+                                     const int32_t* __restrict__ seg_end, const float* __restrict__ lse,
+                                     const float* __restrict__ dsum, float* __restrict__ dqkv, int M, int Tlen, int H,
+                                     float scale) {
+  constexpr int KD = HD / 32;
+  const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (item >= M * H) return;
+  const int s = item / H, h = item % H;
+  const int d = H * HD, t = s % Tlen, row0 = s - t;
+  float kv[KD], vv[KD];
+#pragma unroll
+  for (int i = 0; i < KD; ++i) {
+    kv[i] = __bfloat162float(qkv[static_cast<size_t>(s) * 3 * d + d + h * HD + lane * KD + i]);
+    vv[i] = __bfloat162float(qkv[static_cast<size_t>(s) * 3 * d + 2 * d + h * HD + lane * KD + i]);
+  }
+  const int hi = row0 + max(seg_end[s], t + 1);
+  float dk[KD] = {}, dv[KD] = {};
+  for (int m = s; m < hi; ++m) {
+    const __nv_bfloat16* qr = qkv + static_cast<size_t>(m) * 3 * d + h * HD + lane * KD;
+    const __nv_bfloat16* dor = dO + static_cast<size_t>(m) * d + h * HD + lane * KD;
+    float qv[KD], dov[KD];
+    float acc = 0.f, dp = 0.f;
+#pragma unroll
+    for (int i = 0; i < KD; ++i) {
+      qv[i] = __bfloat162float(qr[i]);
+      dov[i] = __bfloat162float(dor[i]);
+      acc += qv[i] * kv[i];
+      dp += dov[i] * vv[i];
+    }
+    const float sc = mtp::warp_sum(acc) * scale;
+    dp = mtp::warp_sum(dp);
+    const float p = expf(sc - lse[static_cast<size_t>(m) * H + h]);
+    const float ds = p * (dp - dsum[static_cast<size_t>(m) * H + h]);
+#pragma unroll
+    for (int i = 0; i < KD; ++i) {
+      dv[i] += p * dov[i];
+      dk[i] += ds * qv[i];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < KD; ++i) {
+    dqkv[static_cast<size_t>(s) * 3 * d + d + h * HD + lane * KD + i] = dk[i] * scale;
+    dqkv[static_cast<size_t>(s) * 3 * d + 2 * d + h * HD + lane * KD + i] = dv[i];
+  }
+}
+
+// scratch of the block backward (reused depth after depth)
+struct BwdLayout {
+  size_t dhb, dhT, pq, gb, gT, dgf, dpq, dpqT, yT, dyf, daf, dab, daT, oT, dof, dob, dqkvf, dqkvb, dqkvT, xT, dxf,
+      duf, dub, duT, cT, dcf, alse, adsum, tok, wdT, wgT, wuT, woT, wqkvT, mT, total;
+};
+
+BwdLayout make_bwd_layout(const mtp_dims& D, size_t start, int mp) {
+  BwdLayout B{};
+  const size_t M = static_cast<size_t>(D.B) * D.T, d = D.d, f = D.ffn, Mp = mp;
+  size_t off = start;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes);
+    return o;
+  };
+  B.dhb = take(M * d * 2);
+  B.dhT = take(d * Mp * 2);
+  B.pq = take(M * 2 * f * 2);
+  B.gb = take(M * f * 2);
+  B.gT = take(f * Mp * 2);
+  B.dgf = take(M * f * 4);
+  B.dpq = take(M * 2 * f * 2);
+  B.dpqT = take(2 * f * Mp * 2);
+  B.yT = take(d * Mp * 2);
+  B.dyf = take(M * d * 4);
+  B.daf = take(M * d * 4);
+  B.dab = take(M * d * 2);
+  B.daT = take(d * Mp * 2);
+  B.oT = take(d * Mp * 2);
+  B.dof = take(M * d * 4);
+  B.dob = take(M * d * 2);
+  B.dqkvf = take(M * 3 * d * 4);
+  B.dqkvb = take(M * 3 * d * 2);
+  B.dqkvT = take(3 * d * Mp * 2);
+  B.xT = take(d * Mp * 2);
+  B.dxf = take(M * d * 4);
+  B.duf = take(M * d * 4);
+  B.dub = take(M * d * 2);
+  B.duT = take(d * Mp * 2);
+  B.cT = take(2 * d * Mp * 2);
+  B.dcf = take(M * 2 * d * 4);
+  B.alse = take(M * D.n_heads * 4);
+  B.adsum = take(M * D.n_heads * 4);
+  B.tok = take(M * 4);
+  B.wdT = take(f * d * 2);
+  B.wgT = take(d * f * 2);
+  B.wuT = take(d * f * 2);
+  B.woT = take(d * d * 2);
+  B.wqkvT = take(d * 3 * d * 2);
+  B.mT = take(2 * d * d * 2);
+  B.total = off;
+  return B;
+}
+
+SaveOff make_save_off(const mtp_dims& D) {
+  SaveOff S{};
+  const size_t M = static_cast<size_t>(D.B) * D.T, d = D.d;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes);
+    return o;
+  };
+  S.c = take(M * 2 * d * 2);
+  S.u = take(M * d * 2);
+  S.x = take(M * d * 2);
+  S.qkv = take(M * 3 * d * 2);
+  S.o = take(M * d * 2);
+  S.a = take(M * d * 2);
+  S.y = take(M * d * 2);
+  S.bytes = off;
+  return S;
+}
+
+// C += A B^T into fp32 (one writer per element)
+mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, const __nv_bfloat16* B, int ldb, float* out,
+                    int ldo, cudaStream_t st) {
+  mtp::GemmDesc g = gdesc(M, N, K, A, lda, B, ldb);
+  g.epi = mtp::EPI_F32_ACC;
+  g.out_f32 = out;
+  g.ldo = ldo;
+  return mtp::gemm_bf16_launch(g, st);
+}
+
+// gradients of depth k's module given dstate[k] = dL/dh_k (complete): weight
+// gradients into `grads` (those given), dL/dh_{k-1} added into dstate[k-1],
+// the embedding rows' gradient scattered into grads->embed.
+mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B, int k, const __nv_bfloat16* h_prev,
+                          const mtp_grads* G) {
+  using bf = __nv_bfloat16;
+  const mtp_dims& D = C.D;
+  const int M = C.M, d = D.d, f = D.ffn, H = D.n_heads, hd = D.head_dim, Mp = T.mp, i = k - 1;
+  const size_t Md = static_cast<size_t>(M) * d;
+  cudaStream_t st = C.st;
+  auto wt = [&](const void* const* arr) { return static_cast<const bf*>(arr[i]); };
+  auto gp = [&](float* const* arr) -> float* { return arr ? arr[i] : nullptr; };
+  auto bb = [&](size_t off) { return C.buf<bf>(off); };
+  auto fb = [&](size_t off) { return C.buf<float>(off); };
+  uint8_t* sv = C.save + static_cast<size_t>(i) * C.so.bytes;
+  const bf *c = reinterpret_cast<const bf*>(sv + C.so.c), *u = reinterpret_cast<const bf*>(sv + C.so.u),
+           *x = reinterpret_cast<const bf*>(sv + C.so.x), *qkv = reinterpret_cast<const bf*>(sv + C.so.qkv),
+           *o = reinterpret_cast<const bf*>(sv + C.so.o), *a = reinterpret_cast<const bf*>(sv + C.so.a),
+           *y = reinterpret_cast<const bf*>(sv + C.so.y);
+  const float* dh = fb(T.dstate) + static_cast<size_t>(k) * Md;
+  float* dh_prev = fb(T.dstate) + static_cast<size_t>(k - 1) * Md;
+  // weights of the depth, transposed for the input-gradient GEMMs
+  transpose_bf16(wt(C.W.w_down), d, f, f, bb(B.wdT), d, st);
+  transpose_bf16(wt(C.W.w_gate), f, d, d, bb(B.wgT), f, st);
+  transpose_bf16(wt(C.W.w_up), f, d, d, bb(B.wuT), f, st);
+  transpose_bf16(wt(C.W.wo), d, d, d, bb(B.woT), d, st);
+  transpose_bf16(wt(C.W.wq), d, d, d, bb(B.wqkvT), 3 * d, st);
+  transpose_bf16(wt(C.W.wk), d, d, d, bb(B.wqkvT) + d, 3 * d, st);
+  transpose_bf16(wt(C.W.wv), d, d, d, bb(B.wqkvT) + 2 * d, 3 * d, st);
+  transpose_bf16(wt(C.W.eh_proj), d, 2 * d, 2 * d, bb(B.mT), d, st);
+
+  // h = a + g W_d^T: dW_d += dh^T g; dg = dh W_d; da = dh (+ the FFN path below)
+  f32_to_bf16(dh, d, bb(B.dhb), d, M, d, st);
+  transpose_bf16(bb(B.dhb), M, d, d, bb(B.dhT), Mp, st);
+  {  // recompute the gate and up pre-activations p = y Wg^T, q = y Wu^T into pq = [p | q]
+    mtp::GemmDesc g = gdesc(M, f, d, y, d, wt(C.W.w_gate), d);
+    g.epi = mtp::EPI_STORE;
+    g.out = bb(B.pq);
+    g.ldo = 2 * f;
+    TRY(mtp::gemm_bf16_launch(g, st));
+    g = gdesc(M, f, d, y, d, wt(C.W.w_up), d);
+    g.epi = mtp::EPI_STORE;
+    g.out = bb(B.pq) + f;
+    g.ldo = 2 * f;
+    TRY(mtp::gemm_bf16_launch(g, st));
+  }
+  MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dgf), 0, static_cast<size_t>(M) * f * 4, st));
+  TRY(gemm_acc(M, f, d, bb(B.dhb), d, bb(B.wdT), d, fb(B.dgf), f, st));
+  swiglu_bwd_kernel<<<4 * 152, 256, 0, st>>>(bb(B.pq), fb(B.dgf), bb(B.gb), bb(B.dpq), M, f);
+  mtp::note_launch();
+  if (float* gwd = gp(G->w_down)) {
+    transpose_bf16(bb(B.gb), M, f, f, bb(B.gT), Mp, st);
+    TRY(gemm_acc(d, f, M, bb(B.dhT), Mp, bb(B.gT), Mp, gwd, f, st));
+  }
+  // g = silu(y Wg^T) (y Wu^T): dWg += dp^T y; dWu += dq^T y; dy = dp Wg + dq Wu
+  transpose_bf16(bb(B.dpq), M, 2 * f, 2 * f, bb(B.dpqT), Mp, st);
+  transpose_bf16(y, M, d, d, bb(B.yT), Mp, st);
+  if (float* gg = gp(G->w_gate)) TRY(gemm_acc(f, d, M, bb(B.dpqT), Mp, bb(B.yT), Mp, gg, d, st));
+  if (float* gu = gp(G->w_up))
+    TRY(gemm_acc(f, d, M, bb(B.dpqT) + static_cast<size_t>(f) * Mp, Mp, bb(B.yT), Mp, gu, d, st));
+  MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dyf), 0, Md * 4, st));
+  TRY(gemm_acc(M, d, f, bb(B.dpq), 2 * f, bb(B.wgT), f, fb(B.dyf), d, st));
+  TRY(gemm_acc(M, d, f, bb(B.dpq) + f, 2 * f, bb(B.wuT), f, fb(B.dyf), d, st));
+  // y = RMSNorm_f(a): da = dh + RMSNorm backward
+  MTP_CUDA_TRY(cudaMemcpyAsync(fb(B.daf), dh, Md * 4, cudaMemcpyDeviceToDevice, st));
+  rmsnorm_bwd(a, d, nullptr, wt(C.W.ffn_norm), fb(B.dyf), d, fb(B.daf), d, nullptr, gp(G->ffn_norm), M, d, D.eps, st);
+  // a = u + o Wo^T: dWo += da^T o; do = da Wo; du = da (+ the attention path)
+  f32_to_bf16(fb(B.daf), d, bb(B.dab), d, M, d, st);
+  if (float* gwo = gp(G->wo)) {
+    transpose_bf16(bb(B.dab), M, d, d, bb(B.daT), Mp, st);
+    transpose_bf16(o, M, d, d, bb(B.oT), Mp, st);
+    TRY(gemm_acc(d, d, M, bb(B.daT), Mp, bb(B.oT), Mp, gwo, d, st));
+  }
+  MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dof), 0, Md * 4, st));
+  TRY(gemm_acc(M, d, d, bb(B.dab), d, bb(B.woT), d, fb(B.dof), d, st));
+  f32_to_bf16(fb(B.dof), d, bb(B.dob), d, M, d, st);
+  // segment-causal attention backward, then RoPE backward
+  const float scale = 1.0f / sqrtf(static_cast<float>(hd));
+  const int items = M * H;
+  const int32_t* ss = C.buf<int32_t>(C.L.seg_start);
+  const int32_t* se = C.buf<int32_t>(C.L.seg_end);
+  if (hd == 128) {
+    attn_bwd_dq_kernel<128><<<(items + 7) / 8, 256, 0, st>>>(qkv, o, bb(B.dob), ss, fb(B.dqkvf), fb(B.alse),
+                                                             fb(B.adsum), M, D.T, H, scale);
+    attn_bwd_dkdv_kernel<128><<<(items + 7) / 8, 256, 0, st>>>(qkv, bb(B.dob), se, fb(B.alse), fb(B.adsum),
+                                                               fb(B.dqkvf), M, D.T, H, scale);
+  } else {
+    attn_bwd_dq_kernel<64><<<(items + 7) / 8, 256, 0, st>>>(qkv, o, bb(B.dob), ss, fb(B.dqkvf), fb(B.alse),
+                                                            fb(B.adsum), M, D.T, H, scale);
+    attn_bwd_dkdv_kernel<64><<<(items + 7) / 8, 256, 0, st>>>(qkv, bb(B.dob), se, fb(B.alse), fb(B.adsum),
+                                                              fb(B.dqkvf), M, D.T, H, scale);
+  }
+  mtp::note_launch();
+  mtp::note_launch();
+  rope_bwd_kernel<<<4 * 152, 256, 0, st>>>(fb(B.dqkvf), C.buf<float2>(C.L.rope), C.pos, bb(B.dqkvb), M, d, hd, D.T,
+                                           D.rope_base > 0.f ? 1 : 0);
+  mtp::note_launch();
+  // q, k, v = x W{q,k,v}^T: dW += d{q,k,v}^T x; dx = [dq dk dv] [Wq; Wk; Wv]
+  transpose_bf16(bb(B.dqkvb), M, 3 * d, 3 * d, bb(B.dqkvT), Mp, st);
+  transpose_bf16(x, M, d, d, bb(B.xT), Mp, st);
+  float* gq[3] = {gp(G->wq), gp(G->wk), gp(G->wv)};
+  for (int j = 0; j < 3; ++j)
+    if (gq[j])
+      TRY(gemm_acc(d, d, M, bb(B.dqkvT) + static_cast<size_t>(j) * d * Mp, Mp, bb(B.xT), Mp, gq[j], d, st));
+  MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dxf), 0, Md * 4, st));
+  TRY(gemm_acc(M, d, 3 * d, bb(B.dqkvb), 3 * d, bb(B.wqkvT), 3 * d, fb(B.dxf), d, st));
+  // x = RMSNorm_a(u): du = da + RMSNorm backward
+  MTP_CUDA_TRY(cudaMemcpyAsync(fb(B.duf), fb(B.daf), Md * 4, cudaMemcpyDeviceToDevice, st));
+  rmsnorm_bwd(u, d, nullptr, wt(C.W.attn_norm), fb(B.dxf), d, fb(B.duf), d, nullptr, gp(G->attn_norm), M, d, D.eps,
+              st);
+  // u = c M^T: dM += du^T c; dc = du M
+  f32_to_bf16(fb(B.duf), d, bb(B.dub), d, M, d, st);
+  if (float* gm = gp(G->eh_proj)) {
+    transpose_bf16(bb(B.dub), M, d, d, bb(B.duT), Mp, st);
+    transpose_bf16(c, M, 2 * d, 2 * d, bb(B.cT), Mp, st);
+    TRY(gemm_acc(d, 2 * d, M, bb(B.duT), Mp, bb(B.cT), Mp, gm, 2 * d, st));
+  }
+  MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dcf), 0, static_cast<size_t>(M) * 2 * d * 4, st));
+  TRY(gemm_acc(M, 2 * d, d, bb(B.dub), d, bb(B.mT), d, fb(B.dcf), 2 * d, st));
+  // c = [RMSNorm_h(h_{k-1}); RMSNorm_e(E[x_{t+k}])]: dh_{k-1} += ..., dE[x_{t+k}] += ...
+  rmsnorm_bwd(h_prev, d, nullptr, wt(C.W.hnorm), fb(B.dcf), 2 * d, dh_prev, d, nullptr, gp(G->hnorm), M, d, D.eps,
+              st);
+  int32_t* tok = C.buf<int32_t>(B.tok);
+  shifted_tokens_kernel<<<(M + 255) / 256, 256, 0, st>>>(C.tokens, tok, M, D.T, k, D.V);
+  mtp::note_launch();
+  rmsnorm_bwd(static_cast<const bf*>(C.W.embed), d, tok, wt(C.W.enorm), fb(B.dcf) + d, 2 * d, G->embed, d, tok,
+              gp(G->enorm), M, d, D.eps, st);
   MTP_LAUNCH_CHECK();
   return MTP_OK;
 }
@@ -1075,7 +1514,8 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
 
 extern "C" size_t mtp_chain_grad_workspace_bytes(const mtp_dims* dims) {
   if (!dims || !valid_dims(*dims) || supported(*dims) != MTP_OK || dims->dtype != MTP_BF16) return 0;
-  return make_train_layout(*dims).total;
+  const TrainLayout T = make_train_layout(*dims);
+  return make_bwd_layout(*dims, T.total, T.mp).total;
 }
 
 extern "C" mtp_status mtp_chain_loss_grad(const mtp_dims* dims, const mtp_weights* w, const int32_t* tokens,
@@ -1087,23 +1527,26 @@ extern "C" mtp_status mtp_chain_loss_grad(const mtp_dims* dims, const mtp_weight
   if (!dims) return MTP_ERR_INVALID_ARG;
   if (dims->dtype != MTP_BF16) return MTP_ERR_UNSUPPORTED;
   TRY(check_common(dims, w, tokens, seg, pos, h0, ws, ws_bytes));
-  if (!sums_counts || !losses || !grads || !grads->head || !grads->out_norm) return MTP_ERR_INVALID_ARG;
+  if (!sums_counts || !losses || !grads) return MTP_ERR_INVALID_ARG;
   if (!valid_den(den)) return MTP_ERR_INVALID_ARG;
   if (depth_weights && dims->D > kMaxDepthWeights) return MTP_ERR_UNSUPPORTED;
   const mtp_dims& D = *dims;
-  // this build computes the shared head's and the final norm's gradients for
-  // every term, and the gradient of h^0 when only the main term is weighted
-  bool depth_weighted = depth_weights ? false : lambda != 0.f;
-  if (depth_weights)
-    for (int k = 0; k < D.D; ++k) depth_weighted |= depth_weights[k] != 0.f;
-  if (grads->embed || (grads->h0 && depth_weighted)) return MTP_ERR_UNSUPPORTED;
   for (const void* p : {static_cast<const void*>(grads->head), static_cast<const void*>(grads->out_norm),
-                        static_cast<const void*>(grads->h0)})
+                        static_cast<const void*>(grads->h0), static_cast<const void*>(grads->embed)})
     if (p && !mtp::aligned16(p)) return MTP_ERR_ALIGNMENT;
+  float* const* lists[] = {grads->hnorm, grads->enorm, grads->eh_proj, grads->attn_norm, grads->wq, grads->wk,
+                           grads->wv, grads->wo, grads->ffn_norm, grads->w_gate, grads->w_up, grads->w_down};
+  for (float* const* l : lists)
+    if (l)
+      for (int k = 0; k < D.D; ++k)
+        if (!l[k] || !mtp::aligned16(l[k])) return l[k] ? MTP_ERR_ALIGNMENT : MTP_ERR_INVALID_ARG;
   const TrainLayout T = make_train_layout(D);
-  if (ws_bytes < T.total) return MTP_ERR_WORKSPACE;
+  const BwdLayout BL = make_bwd_layout(D, T.total, T.mp);
+  if (ws_bytes < BL.total) return MTP_ERR_WORKSPACE;
   Ctx C{D, *w, tokens, seg, pos, static_cast<uint8_t*>(ws), make_layout(D), stream, D.B * D.T};
   C.lse_save = C.buf<float>(T.lse);
+  C.save = C.buf<uint8_t>(T.save);
+  C.so = make_save_off(D);
   bf* hs = C.buf<bf>(T.hs);
   const int M = C.M, d = D.d;
   const size_t Md = static_cast<size_t>(M) * d;
@@ -1124,6 +1567,11 @@ extern "C" mtp_status mtp_chain_loss_grad(const mtp_dims* dims, const mtp_weight
   for (int t = with_main ? 0 : 1; t <= D.D; ++t) {
     const bf* h_t = t == 0 ? static_cast<const bf*>(h0) : hs + static_cast<size_t>(t - 1) * Md;
     TRY(head_backward(C, T, t, h_t, grads->head, grads->out_norm));
+  }
+  // depths D..1: each depth's state gradient is complete once the deeper depth has run
+  for (int k = D.D; k >= 1; --k) {
+    const bf* h_prev = k == 1 ? static_cast<const bf*>(h0) : hs + static_cast<size_t>(k - 2) * Md;
+    TRY(block_backward(C, T, BL, k, h_prev, grads));
   }
   if (grads->h0) {
     add_f32_kernel<<<2 * 152, 256, 0, stream>>>(grads->h0, C.buf<float>(T.dstate), Md);

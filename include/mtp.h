@@ -274,11 +274,14 @@ size_t mtp_chain_grad_workspace_bytes(const mtp_dims* dims);
  * ([M7.6] §0x05: the shared head receives the main term's and every depth's
  * gradient).  The head backward recomputes the logits per vocabulary chunk
  * (as [tokens, chunk] for dz = (softmax - onehot) dL/dl and as [chunk,
- * tokens] for dz^T) and never stores them whole.  bf16 only.
- * This build fills grads->head and grads->out_norm for every term and
- * grads->h0 when no depth term is weighted (lambda = 0 or all depth weights
- * 0); requesting grads->embed, or grads->h0 with weighted depth terms,
- * returns MTP_ERR_UNSUPPORTED. */
+ * tokens] for dz^T) and never stores them whole.  The module backward then
+ * runs depth D down to 1 on activations the forward saved: GEMMs for the
+ * weight gradients (on transposed activations) and the input gradients (on
+ * transposed weights), SwiGLU from recomputed gate/up pre-activations,
+ * segment-causal attention (scores recomputed), RoPE, the norms, and the
+ * prologue's two RMSNorms -- the state's into depth k-1, the embedding rows'
+ * scattered into grads->embed.  Gradients flow through the bf16 rounding
+ * points unchanged.  bf16 only. */
 mtp_status mtp_chain_loss_grad(const mtp_dims* dims, const mtp_weights* w, const int32_t* tokens,
                                const int32_t* seg, const int32_t* pos, const void* h0, float lambda, int den,
                                int with_main, const float* depth_weights, double* sums_counts, float* losses,

@@ -64,12 +64,71 @@ def test_hd128_depth_weights_and_accumulation():
     assert _rel(g["out_norm"], r["grads"]["out_norm"]) < 2e-2
 
 
-def test_unsupported_requests_are_refused():
-    cfg = synth.SMALL_BF16
-    inp = synth.make_chain_inputs(cfg, seed=1)
+PER_DEPTH = ("hnorm", "enorm", "eh_proj", "attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up",
+             "w_down")
+
+
+def _run_all(cfg, seed, lam, den, with_main=True, depth_weights=None):
+    inp = synth.make_chain_inputs(cfg, seed=seed)
     w = {k: ([t.cuda() for t in v] if isinstance(v, list) else v.cuda()) for k, v in inp["weights"].items()}
     chain = lib.Chain(cfg, w)
-    grads = {"head": torch.zeros((cfg.V, cfg.d), device="cuda"), "out_norm": torch.zeros(cfg.d, device="cuda"),
-             "h0": torch.zeros((cfg.B, cfg.T, cfg.d), device="cuda")}
-    with pytest.raises(lib.MtpError):
-        chain.loss_grad(inp["tokens"].cuda(), inp["seg"].cuda(), inp["pos"].cuda(), inp["h0"].cuda(), grads, lam=0.3)
+    z = lambda t: torch.zeros(tuple(t.shape), dtype=torch.float32, device="cuda")  # noqa: E731
+    grads = {k: z(w[k]) for k in ("embed", "head", "out_norm")}
+    grads["h0"] = torch.zeros((cfg.B, cfg.T, cfg.d), dtype=torch.float32, device="cuda")
+    for k in PER_DEPTH:
+        grads[k] = [z(t) for t in w[k]]
+    out = chain.loss_grad(inp["tokens"].cuda(), inp["seg"].cuda(), inp["pos"].cuda(), inp["h0"].cuda(), grads,
+                          lam=lam, den=den, with_main=with_main, depth_weights=depth_weights)
+    lib.check_errors()
+    W = oc.weights_to_numpy(inp["weights"])
+    dims = oc.Dims(n_heads=cfg.n_heads, head_dim=cfg.head_dim, D=cfg.D, eps=cfg.eps, rope_base=cfg.rope_base)
+    r = og.chain_loss_grads(inp["tokens"].numpy(), inp["seg"].numpy(), inp["pos"].numpy(),
+                            inp["h0"].float().numpy(), W, dims, lam=lam, den=den, with_main=with_main,
+                            depth_weights=depth_weights)
+    return out, grads, r
+
+
+def _check_all(cfg, grads, r, bar=2e-2):
+    errs = {}
+    for k in ("embed", "head", "out_norm"):
+        errs[k] = _rel(grads[k].cpu().numpy(), r["grads"][k])
+    errs["h0"] = _rel(grads["h0"].cpu().numpy(), r["dh0"])
+    for k in PER_DEPTH:
+        for i in range(cfg.D):
+            errs[f"{k}[{i}]"] = _rel(grads[k][i].cpu().numpy(), r["grads"][k][i])
+    bad = {k: v for k, v in errs.items() if not v < bar}
+    assert not bad, bad
+    return errs
+
+
+@pytest.mark.parametrize("den", ["fixed", "masked_mean", "global"])
+def test_full_chain_gradients(den):
+    """Every gradient of the two-depth chain: shared embedding/head/final norm,
+    h^0, and each depth's fusion, block and norm weights."""
+    cfg = synth.SMALL_BF16
+    out, grads, r = _run_all(cfg, 8, 0.3, den)
+    assert np.isclose(out["losses"][0].item(), r["loss_total"], rtol=2e-3)
+    _check_all(cfg, grads, r)
+
+
+def test_full_chain_gradients_hd128_weights():
+    cfg = synth.SMALL_BF16_HD128
+    out, grads, r = _run_all(cfg, 9, 0.3, "weighted_pair", with_main=False, depth_weights=[0.6, 0.4])
+    _check_all(cfg, grads, r)
+
+
+def test_gradients_accumulate():
+    """Two calls add their gradients into the same buffers."""
+    cfg = synth.SMALL_BF16
+    inp = synth.make_chain_inputs(cfg, seed=4)
+    w = {k: ([t.cuda() for t in v] if isinstance(v, list) else v.cuda()) for k, v in inp["weights"].items()}
+    chain = lib.Chain(cfg, w)
+    g1 = {"head": torch.zeros((cfg.V, cfg.d), device="cuda"), "wq": [torch.zeros_like(t, dtype=torch.float32)
+                                                                      for t in w["wq"]]}
+    args = (inp["tokens"].cuda(), inp["seg"].cuda(), inp["pos"].cuda(), inp["h0"].cuda())
+    chain.loss_grad(*args, g1)
+    once = {"head": g1["head"].clone(), "wq": [t.clone() for t in g1["wq"]]}
+    chain.loss_grad(*args, g1)
+    lib.check_errors()
+    torch.testing.assert_close(g1["head"], 2 * once["head"], rtol=1e-5, atol=1e-7)
+    torch.testing.assert_close(g1["wq"][1], 2 * once["wq"][1], rtol=1e-5, atol=1e-7)
