@@ -59,6 +59,7 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--draft-steps", type=int, default=30)
+    ap.add_argument("--train-steps", type=int, default=5, help="timed training steps (0 = off)")
     ap.add_argument("--c3-steps", type=int, default=4, help="timed calls of the DeepSeek-V3-width section (0 = off)")
     ap.add_argument("--draft-gamma", type=int, default=4, help="steps of the recurrent draft round (<= 1: off)")
     ap.add_argument("--draft-requests", type=int, default=32,
@@ -419,7 +420,24 @@ def run_ours(args):
     v_ms_mean = sum(v_ms) / len(v_ms)
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     v_gbs = float(vbytes.mean()) / (v_ms_mean / 1e3) / 1e9
+    # floor for one pass over this many bytes: a read-only reduction over a buffer of the same size,
+    # timed alike (L2 flushed first)
+    nb = int(vbytes.mean()) // 16 * 16
+    src_buf = torch.ones(nb // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+    read_ms = []
+    for _ in range(12):
+        flush()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record()
+        torch.sum(src_buf, dim=0, out=sink)
+        c1.record()
+        torch.cuda.synchronize()
+        read_ms.append(c0.elapsed_time(c1))
+    read_us = 1e3 * sorted(read_ms[2:])[len(read_ms[2:]) // 2]
+    del src_buf
     verify = {"rows_per_s": world * vcfg.R * (vcfg.gamma + 1) / (v_ms_mean / 1e3),
+              "same_size_read_us": read_us,
               "requests_per_s": world * vcfg.R / (v_ms_mean / 1e3), "us_per_call": 1e3 * v_ms_mean,
               "algorithmic_bytes_per_call": float(vbytes.mean()), "achieved_gbs": v_gbs, "peak_gbs": hbm_peak,
               "frac": v_gbs / hbm_peak, "mean_accepted": float(acc.mean()), "status_nonzero": int((st != 0).sum())}
@@ -428,6 +446,8 @@ def run_ours(args):
     draft = measure_draft(args, dev, rank, peaks)
     # DeepSeek-V3-width single depth (its own workload, measured beside the step)
     dsv3 = measure_dsv3(args, dev, rank, peaks)
+    # training step (forward + backward) on the mid workload
+    train = measure_train(args, dev, rank, peaks, chain, x, weights, cfg)
 
     # end to end through the public API: pinned host inputs -> device, result -> host, every step
     e2e = measure_e2e(cfg, vcfg, chain, batch, x, vin, args.e2e_steps, dev, rank, world, tokens_per_step)
@@ -441,7 +461,7 @@ def run_ours(args):
                 "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic (seeded; random-init weights of the workload's shapes)",
                 "config": workload_config(), "roofline": roofline, "spec_verify": verify,
-                "spec_verify_rows_per_s": verify["rows_per_s"], "kernels": breakdown, "draft_step": draft, "dsv3_width": dsv3,
+                "spec_verify_rows_per_s": verify["rows_per_s"], "kernels": breakdown, "draft_step": draft, "dsv3_width": dsv3, "train_step": train,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
                 "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
                 "clock_samples": clk["samples"], "wall_s_timed_region": t_wall,
@@ -618,6 +638,58 @@ def measure_dsv3(args, dev, rank, peaks):
                         "one packed boundary at 2048, main + depth-1 heads)",
             "tokens_per_s": rows / (ms / 1e3), "ms_per_call": ms, "steps": n, "kernels": kernels,
             "peak_tflops": peak, "l2": "flushed before every timed call (256 MiB written then read)"}
+
+
+def measure_train(args, dev, rank, peaks, chain, x, weights, cfg):
+    """mtp_chain_loss_grad on the step's workload: the forward and the
+    gradients of h^0 and of every weight (fp32, added into zeroed buffers).
+    Algorithmic FLOPs = 3 x the forward's (rows with state for the block and
+    projection GEMMs, supervised rows for the heads); the head logits are
+    recomputed twice and the gate/up pre-activations once, which is extra work
+    not counted.  L2 flushed before every timed step."""
+    import torch
+
+    from deepseek_sequential_mtp_gb300 import lib
+
+    if args.train_steps <= 0:
+        return None
+    z = lambda t: torch.zeros(tuple(t.shape), dtype=torch.float32, device=dev)  # noqa: E731
+    grads = {k: z(weights[k]) for k in ("embed", "head", "out_norm")}
+    grads["h0"] = torch.zeros((cfg.B, cfg.T, cfg.d), dtype=torch.float32, device=dev)
+    for k in ("hnorm", "enorm", "eh_proj", "attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up",
+              "w_down"):
+        grads[k] = [z(t) for t in weights[k]]
+    out = {"sums_counts": torch.empty(2 * (cfg.D + 1), dtype=torch.float64, device=dev),
+           "losses": torch.empty(cfg.D + 2, dtype=torch.float32, device=dev)}
+    flush = L2Flush(dev)
+
+    def call():
+        chain.loss_grad(x["tokens"], x["seg"], x["pos"], x["h0"], grads, den="fixed", with_main=True, out=out)
+
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    lib.check_errors()
+    n = args.train_steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        flush()
+        ev[i][0].record()
+        call()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    lib.check_errors()
+    ms = sorted(a.elapsed_time(b) for a, b in ev)[n // 2]
+    counts = out["sums_counts"][1::2].cpu().numpy()
+    rows = float(sum(cfg.B * (cfg.T - k) for k in range(1, cfg.D + 1)))
+    d, f, V = cfg.d, cfg.ffn, cfg.V
+    fwd = (4 * d * d + 6 * d * d + 2 * d * d + 4 * d * f + 2 * d * f) * rows + 2.0 * d * V * float(counts.sum())
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    tflops = 3.0 * fwd / (ms / 1e3) / 1e12
+    return {"workload": "mtp_chain_loss_grad on the step's mid workload (all gradients)", "ms_median": ms,
+            "tokens_per_s": rows / (ms / 1e3), "algorithmic_tflop": 3.0 * fwd / 1e12, "achieved_tflops": tflops,
+            "frac_of_peak": tflops / peak, "steps": n,
+            "l2": "flushed before every timed step (256 MiB written then read)"}
 
 
 def measure_e2e(cfg, vcfg, chain, batch, x, vin, steps, dev, rank, world, tokens_per_step):

@@ -19,7 +19,10 @@ MTP_DEFINE_ERROR_WORD(mtp_take_errors_attn)
 namespace mtp {
 
 mtp_status attn_launch(int dtype, const void* qkv, void* out, const int32_t* seg_start, int B, int T,
-                       int H, int hd, cudaStream_t stream);
+                       int H, int hd, cudaStream_t stream, float* lse2_out = nullptr);
+mtp_status attn_bwd_launch(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16* dO,
+                           const float* lse2, const int32_t* seg_start, const int32_t* seg_end, float* dqkv,
+                           float* dsum, int B, int T, int H, int hd, cudaStream_t stream);
 
 namespace {
 
@@ -85,7 +88,8 @@ __device__ __forceinline__ void load_tile(uint32_t tile, const __nv_bfloat16* qk
 template <int HD>
 __global__ void __launch_bounds__(kThreads)
 flash_attn_bf16_kernel(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16* __restrict__ out,
-                       const int32_t* __restrict__ seg_start, int T, int H, float scale_log2) {
+                       const int32_t* __restrict__ seg_start, int T, int H, float scale_log2,
+                       float* __restrict__ lse2_out) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sQ = smem_u32(smem);
   const uint32_t sK0 = sQ + kBQ * HD * 2;
@@ -219,6 +223,10 @@ flash_attn_bf16_kernel(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16* __r
   l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
   const float inv_a = l_a > 0.f ? 1.f / l_a : 0.f;
   const float inv_b = l_b > 0.f ? 1.f / l_b : 0.f;
+  if (lse2_out && tq == 0) {  // log2-domain log-sum-exp of the scaled scores, for the backward
+    if (row_a < T) lse2_out[(static_cast<size_t>(b) * T + row_a) * H + h] = m_a + log2f(l_a);
+    if (row_b < T) lse2_out[(static_cast<size_t>(b) * T + row_b) * H + h] = m_b + log2f(l_b);
+  }
 #pragma unroll
   for (int dt = 0; dt < HD / 8; ++dt) {
     const int col = h * HD + dt * 8 + 2 * tq;
@@ -228,6 +236,245 @@ flash_attn_bf16_kernel(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16* __r
     if (row_b < T)
       *reinterpret_cast<__nv_bfloat162*>(out + (static_cast<size_t>(b) * T + row_b) * d + col) =
           __floats2bfloat162_rn(o[dt][2] * inv_b, o[dt][3] * inv_b);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Backward, flash-attention-2 form: one CTA per (64-key block, head, packed
+// row).  K and V of the block stay in shared memory; every 64-query block
+// that can see one of its keys streams through (Q and dO double-buffered
+// with cp.async).  Warp w owns keys 16w..16w+15:
+//   S^T = K_w Q^T, dP^T = V_w dO^T            (m16n8k16, K/V rows as A)
+//   P = exp2(S scale_log2 - lse2[q]) on visible (key, query) pairs
+//   dS^T = P (dP - D[q]),  D[q] = do_q . o_q
+//   dV_w += P^T dO,  dK_w += dS^T Q           (accumulated in registers)
+// dS^T goes to shared memory and each warp forms 16 rows of dQ = dS K,
+// added to the fp32 dq rows with atomics (every key block contributes).
+// P and dS are rounded to bf16 for the products.
+// ---------------------------------------------------------------------------
+template <int HD>
+__global__ void attn_dsum_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
+                                 float* __restrict__ dsum, int items, int H) {
+  constexpr int KD = HD / 32;
+  const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (item >= items) return;
+  const int m = item / H, h = item % H;
+  const size_t base = static_cast<size_t>(m) * H * HD + h * HD + lane * KD;
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < KD; ++i) acc += __bfloat162float(o[base + i]) * __bfloat162float(dO[base + i]);
+  acc = warp_sum(acc);
+  if (lane == 0) dsum[item] = acc;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+flash_attn_bwd_kernel(const __nv_bfloat16* __restrict__ qkv, const __nv_bfloat16* __restrict__ dO,
+                      const float* __restrict__ lse2, const float* __restrict__ dsum,
+                      const int32_t* __restrict__ seg_start, const int32_t* __restrict__ seg_end,
+                      float* __restrict__ dqkv, int T, int H, float scale_log2, float scale) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int kTile = kBK * HD * 2;
+  const uint32_t sK = smem_u32(smem);
+  const uint32_t sV = sK + kTile;
+  const uint32_t sQ0 = sV + kTile;
+  const uint32_t sdO0 = sQ0 + 2 * kTile;
+  const uint32_t sdS = sdO0 + 2 * kTile;  // [64 keys][64 queries] bf16, rows XOR-swizzled
+  uint8_t* sdS_ptr = smem + (sdS - sK);
+  float* s_lse = reinterpret_cast<float*>(sdS_ptr + kBK * kBQ * 2);  // [2][64]
+  float* s_D = s_lse + 2 * kBQ;
+  int* s_qss = reinterpret_cast<int*>(s_D + 2 * kBQ);
+  int* s_red = s_qss + 2 * kBQ;
+  const int kb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int d = H * HD, ld3 = 3 * d;
+  const int k0 = kb * kBK;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, tq = lane & 3;
+  const int32_t* ss = seg_start + static_cast<size_t>(b) * T;
+  const int32_t* se = seg_end + static_cast<size_t>(b) * T;
+
+  // the last query that sees one of the block's keys
+  int qhi = -1;
+  for (int i = threadIdx.x; i < kBK; i += kThreads) {
+    const int s = k0 + i;
+    if (s < T) qhi = max(qhi, max(se[s], s + 1) - 1);
+  }
+  qhi = __reduce_max_sync(0xffffffffu, qhi);
+  if (lane == 0) s_red[warp] = qhi;
+  __syncthreads();
+  qhi = max(max(s_red[0], s_red[1]), max(s_red[2], s_red[3]));
+  const int qb_first = kb, qb_last = qhi / kBQ;
+
+  auto load_params = [&](int buf, int qb) {
+    for (int i = threadIdx.x; i < kBQ; i += kThreads) {
+      const int q = qb * kBQ + i;
+      const bool ok = q < T;
+      const size_t item = (static_cast<size_t>(b) * T + (ok ? q : 0)) * H + h;
+      s_lse[buf * kBQ + i] = ok ? lse2[item] : INFINITY;
+      s_D[buf * kBQ + i] = ok ? dsum[item] : 0.f;
+      s_qss[buf * kBQ + i] = ok ? ss[q] : 0x7fffffff;
+    }
+  };
+  load_tile<HD>(sK, qkv, b, T, ld3, k0, d + h * HD);
+  load_tile<HD>(sV, qkv, b, T, ld3, k0, 2 * d + h * HD);
+  load_tile<HD>(sQ0, qkv, b, T, ld3, qb_first * kBQ, h * HD);
+  load_tile<HD>(sdO0, dO, b, T, d, qb_first * kBQ, h * HD);
+  cp_async_commit();
+  load_params(0, qb_first);
+
+  float dk[HD / 8][4], dv[HD / 8][4];
+#pragma unroll
+  for (int i = 0; i < HD / 8; ++i) {
+    dk[i][0] = dk[i][1] = dk[i][2] = dk[i][3] = 0.f;
+    dv[i][0] = dv[i][1] = dv[i][2] = dv[i][3] = 0.f;
+  }
+  const int key_a = k0 + warp * 16 + g, key_b = key_a + 8;
+
+  for (int qb = qb_first; qb <= qb_last; ++qb) {
+    const int buf = (qb - qb_first) & 1;
+    cp_async_wait_all();
+    __syncthreads();
+    if (qb < qb_last) {
+      const int nb = buf ^ 1;
+      load_tile<HD>(sQ0 + nb * kTile, qkv, b, T, ld3, (qb + 1) * kBQ, h * HD);
+      load_tile<HD>(sdO0 + nb * kTile, dO, b, T, d, (qb + 1) * kBQ, h * HD);
+      cp_async_commit();
+      load_params(nb, qb + 1);
+    }
+    const uint32_t sQ = sQ0 + buf * kTile, sdO = sdO0 + buf * kTile;
+    const float* lse_b = s_lse + buf * kBQ;
+    const float* D_b = s_D + buf * kBQ;
+    const int* qss_b = s_qss + buf * kBQ;
+
+    // S^T = K_w Q^T and dP^T = V_w dO^T: 16 keys x 64 queries per warp
+    float st[8][4], dp[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      st[nt][0] = st[nt][1] = st[nt][2] = st[nt][3] = 0.f;
+      dp[nt][0] = dp[nt][1] = dp[nt][2] = dp[nt][3] = 0.f;
+    }
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      uint32_t ka[4], va[4];
+      ldsm_x4(sK + swz<HD>(warp * 16 + (lane & 15), kk * 16 + (lane >> 4) * 8), ka[0], ka[1], ka[2], ka[3]);
+      ldsm_x4(sV + swz<HD>(warp * 16 + (lane & 15), kk * 16 + (lane >> 4) * 8), va[0], va[1], va[2], va[3]);
+#pragma unroll
+      for (int nt = 0; nt < 8; nt += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(sQ + swz<HD>(nt * 8 + (lane & 7) + ((lane >> 4) << 3), kk * 16 + ((lane >> 3) & 1) * 8), b0, b1,
+                b2, b3);
+        mma_bf16(st[nt], ka, b0, b1);
+        mma_bf16(st[nt + 1], ka, b2, b3);
+        ldsm_x4(sdO + swz<HD>(nt * 8 + (lane & 7) + ((lane >> 4) << 3), kk * 16 + ((lane >> 3) & 1) * 8), b0, b1,
+                b2, b3);
+        mma_bf16(dp[nt], va, b0, b1);
+        mma_bf16(dp[nt + 1], va, b2, b3);
+      }
+    }
+    // P^T (into st) and dS^T (into dp) on visible pairs: seg_start(q) <= key <= q
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int ql = nt * 8 + 2 * tq + e, q = qb * kBQ + ql;
+        const float lse = lse_b[ql], Dq = D_b[ql];
+        const int qss = qss_b[ql];
+        const bool va_ok = key_a < T && key_a >= qss && key_a <= q;
+        const bool vb_ok = key_b < T && key_b >= qss && key_b <= q;
+        const float pa = va_ok ? exp2f(st[nt][e] * scale_log2 - lse) : 0.f;
+        const float pb = vb_ok ? exp2f(st[nt][2 + e] * scale_log2 - lse) : 0.f;
+        st[nt][e] = pa;
+        st[nt][2 + e] = pb;
+        dp[nt][e] = pa * (dp[nt][e] - Dq);
+        dp[nt][2 + e] = pb * (dp[nt][2 + e] - Dq);
+      }
+    }
+    // dV_w += P^T dO and dK_w += dS^T Q (k-steps of 16 queries)
+#pragma unroll
+    for (int kt = 0; kt < 4; ++kt) {
+      uint32_t pa[4], da[4];
+      pa[0] = pack_bf16(st[2 * kt][0], st[2 * kt][1]);
+      pa[1] = pack_bf16(st[2 * kt][2], st[2 * kt][3]);
+      pa[2] = pack_bf16(st[2 * kt + 1][0], st[2 * kt + 1][1]);
+      pa[3] = pack_bf16(st[2 * kt + 1][2], st[2 * kt + 1][3]);
+      da[0] = pack_bf16(dp[2 * kt][0], dp[2 * kt][1]);
+      da[1] = pack_bf16(dp[2 * kt][2], dp[2 * kt][3]);
+      da[2] = pack_bf16(dp[2 * kt + 1][0], dp[2 * kt + 1][1]);
+      da[3] = pack_bf16(dp[2 * kt + 1][2], dp[2 * kt + 1][3]);
+#pragma unroll
+      for (int dt = 0; dt < HD / 8; dt += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(sdO + swz<HD>(kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, dt * 8 + (lane >> 4) * 8), b0, b1, b2,
+                  b3);
+        mma_bf16(dv[dt], pa, b0, b1);
+        mma_bf16(dv[dt + 1], pa, b2, b3);
+        ldsm_x4_t(sQ + swz<HD>(kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, dt * 8 + (lane >> 4) * 8), b0, b1, b2,
+                  b3);
+        mma_bf16(dk[dt], da, b0, b1);
+        mma_bf16(dk[dt + 1], da, b2, b3);
+      }
+    }
+    // dS^T to shared memory (row = key, column = query)
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = nt * 8 + 2 * tq;
+      *reinterpret_cast<uint32_t*>(sdS_ptr + swz<64>(warp * 16 + g, col)) = pack_bf16(dp[nt][0], dp[nt][1]);
+      *reinterpret_cast<uint32_t*>(sdS_ptr + swz<64>(warp * 16 + g + 8, col)) = pack_bf16(dp[nt][2], dp[nt][3]);
+    }
+    __syncthreads();
+    // dQ rows 16w..16w+15 of the query block: dS (A, read transposed) times K (B, read transposed)
+    float dq[HD / 8][4];
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i) dq[i][0] = dq[i][1] = dq[i][2] = dq[i][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < kBK / 16; ++kk) {
+      uint32_t a[4];
+      ldsm_x4_t(sdS + swz<64>(kk * 16 + (lane & 7) + ((lane >> 4) << 3), warp * 16 + ((lane >> 3) & 1) * 8), a[0],
+                a[1], a[2], a[3]);
+#pragma unroll
+      for (int dt = 0; dt < HD / 8; dt += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(sK + swz<HD>(kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, dt * 8 + (lane >> 4) * 8), b0, b1, b2,
+                  b3);
+        mma_bf16(dq[dt], a, b0, b1);
+        mma_bf16(dq[dt + 1], a, b2, b3);
+      }
+    }
+    const int qa_row = qb * kBQ + warp * 16 + g, qb_row = qa_row + 8;
+#pragma unroll
+    for (int dt = 0; dt < HD / 8; ++dt) {
+      const int col = h * HD + dt * 8 + 2 * tq;
+      if (qa_row < T) {
+        float* dst = dqkv + (static_cast<size_t>(b) * T + qa_row) * ld3 + col;
+        atomicAdd(dst, dq[dt][0] * scale);
+        atomicAdd(dst + 1, dq[dt][1] * scale);
+      }
+      if (qb_row < T) {
+        float* dst = dqkv + (static_cast<size_t>(b) * T + qb_row) * ld3 + col;
+        atomicAdd(dst, dq[dt][2] * scale);
+        atomicAdd(dst + 1, dq[dt][3] * scale);
+      }
+    }
+  }
+  // dK (scaled) and dV of the warp's 16 keys
+#pragma unroll
+  for (int dt = 0; dt < HD / 8; ++dt) {
+    const int col = h * HD + dt * 8 + 2 * tq;
+    if (key_a < T) {
+      float* r = dqkv + (static_cast<size_t>(b) * T + key_a) * ld3;
+      r[d + col] = dk[dt][0] * scale;
+      r[d + col + 1] = dk[dt][1] * scale;
+      r[2 * d + col] = dv[dt][0];
+      r[2 * d + col + 1] = dv[dt][1];
+    }
+    if (key_b < T) {
+      float* r = dqkv + (static_cast<size_t>(b) * T + key_b) * ld3;
+      r[d + col] = dk[dt][2] * scale;
+      r[d + col + 1] = dk[dt][3] * scale;
+      r[2 * d + col] = dv[dt][2];
+      r[2 * d + col + 1] = dv[dt][3];
+    }
   }
 }
 
@@ -272,7 +519,7 @@ __global__ void attn_f32_kernel(const float* __restrict__ qkv, float* __restrict
 }  // namespace
 
 mtp_status attn_launch(int dtype, const void* qkv, void* out, const int32_t* seg_start, int B, int T, int H,
-                       int hd, cudaStream_t stream) {
+                       int hd, cudaStream_t stream, float* lse2_out) {
   if (B <= 0 || T <= 0) return MTP_OK;
   if (dtype == MTP_BF16) {
     const dim3 grid((T + kBQ - 1) / kBQ, H, B);
@@ -280,7 +527,8 @@ mtp_status attn_launch(int dtype, const void* qkv, void* out, const int32_t* seg
     if (hd == 64) {
       constexpr int smem = (kBQ + 4 * kBK) * 64 * 2;
       flash_attn_bf16_kernel<64><<<grid, kThreads, smem, stream>>>(
-          static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out), seg_start, T, H, scale_log2);
+          static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out), seg_start, T, H, scale_log2,
+          lse2_out);
       mtp::note_launch();
     } else if (hd == 128) {
       constexpr int smem = (kBQ + 4 * kBK) * 128 * 2;
@@ -292,7 +540,8 @@ mtp_status attn_launch(int dtype, const void* qkv, void* out, const int32_t* seg
         attr = true;
       }
       flash_attn_bf16_kernel<128><<<grid, kThreads, smem, stream>>>(
-          static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out), seg_start, T, H, scale_log2);
+          static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out), seg_start, T, H, scale_log2,
+          lse2_out);
       mtp::note_launch();
     } else {
       return MTP_ERR_UNSUPPORTED;
@@ -314,6 +563,50 @@ mtp_status attn_launch(int dtype, const void* qkv, void* out, const int32_t* seg
         1.0f / sqrtf(static_cast<float>(hd)));
     mtp::note_launch();
   }
+  MTP_LAUNCH_CHECK();
+  return MTP_OK;
+}
+
+mtp_status attn_bwd_launch(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16* dO,
+                           const float* lse2, const int32_t* seg_start, const int32_t* seg_end, float* dqkv,
+                           float* dsum, int B, int T, int H, int hd, cudaStream_t stream) {
+  if (B <= 0 || T <= 0) return MTP_OK;
+  const int items = B * T * H;
+  const dim3 grid((T + kBK - 1) / kBK, H, B);
+  const float scale = 1.0f / sqrtf(static_cast<float>(hd));
+  const float scale_log2 = 1.4426950408889634f * scale;
+  // dq is accumulated with atomics by every key block: start from zero
+  if (cudaMemsetAsync(dqkv, 0, static_cast<size_t>(B) * T * 3 * H * hd * sizeof(float), stream) != cudaSuccess)
+    return MTP_ERR_CUDA;
+  if (hd == 64) {
+    attn_dsum_kernel<64><<<(items + 7) / 8, 256, 0, stream>>>(o, dO, dsum, items, H);
+    constexpr int smem = (6 * kBK * 64 + kBK * kBQ) * 2 + 2 * kBQ * 12 + 64;
+    static bool attr = false;
+    if (!attr) {
+      if (cudaFuncSetAttribute(flash_attn_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+          cudaSuccess)
+        return MTP_ERR_CUDA;
+      attr = true;
+    }
+    flash_attn_bwd_kernel<64><<<grid, kThreads, smem, stream>>>(qkv, dO, lse2, dsum, seg_start, seg_end, dqkv, T, H,
+                                                                scale_log2, scale);
+  } else if (hd == 128) {
+    attn_dsum_kernel<128><<<(items + 7) / 8, 256, 0, stream>>>(o, dO, dsum, items, H);
+    constexpr int smem = (6 * kBK * 128 + kBK * kBQ) * 2 + 2 * kBQ * 12 + 64;
+    static bool attr = false;
+    if (!attr) {
+      if (cudaFuncSetAttribute(flash_attn_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+          cudaSuccess)
+        return MTP_ERR_CUDA;
+      attr = true;
+    }
+    flash_attn_bwd_kernel<128><<<grid, kThreads, smem, stream>>>(qkv, dO, lse2, dsum, seg_start, seg_end, dqkv, T,
+                                                                 H, scale_log2, scale);
+  } else {
+    return MTP_ERR_UNSUPPORTED;
+  }
+  mtp::note_launch();
+  mtp::note_launch();
   MTP_LAUNCH_CHECK();
   return MTP_OK;
 }

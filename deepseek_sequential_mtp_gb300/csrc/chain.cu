@@ -30,8 +30,11 @@
 MTP_DEFINE_ERROR_WORD(mtp_take_errors_chain)
 
 namespace mtp {
+mtp_status attn_bwd_launch(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16* dO,
+                           const float* lse2, const int32_t* seg_start, const int32_t* seg_end, float* dqkv,
+                           float* dsum, int B, int T, int H, int hd, cudaStream_t stream);
 mtp_status attn_launch(int dtype, const void* qkv, void* out, const int32_t* seg_start, int B, int T, int H,
-                       int hd, cudaStream_t stream);
+                       int hd, cudaStream_t stream, float* lse2_out = nullptr);
 }
 
 namespace {
@@ -538,7 +541,7 @@ Layout make_layout(const mtp_dims& D) {
 
 // per-depth activations a training step keeps (offsets inside one depth's slot)
 struct SaveOff {
-  size_t c, u, x, qkv, o, a, y, bytes;
+  size_t c, u, x, qkv, o, a, y, lse2, bytes;
 };
 
 struct Ctx {
@@ -765,7 +768,9 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
     TRY(gemm<T>(C, x, d, wqkv, 3, d, d, 3 * d, qkv, 3 * d, D.rope_base > 0.f ? mtp::EPI_ROPE : mtp::EPI_STORE));
     mtp::prof_end(MTP_KC_QKV_GEMM, C.st);
     mtp::prof_begin(MTP_KC_ATTENTION, C.st);
-    TRY(mtp::attn_launch(D.dtype, qkv, o, C.buf<int32_t>(C.L.seg_start), D.B, D.T, D.n_heads, D.head_dim, C.st));
+    float* lse2 = C.save ? reinterpret_cast<float*>(C.save + static_cast<size_t>(i) * C.so.bytes + C.so.lse2) : nullptr;
+    TRY(mtp::attn_launch(D.dtype, qkv, o, C.buf<int32_t>(C.L.seg_start), D.B, D.T, D.n_heads, D.head_dim, C.st,
+                         lse2));
     mtp::prof_end(MTP_KC_ATTENTION, C.st);
     const T* wo[1] = {wt(C.W.wo)};
     mtp::prof_begin(MTP_KC_O_GEMM, C.st);
@@ -1180,125 +1185,10 @@ __global__ void shifted_tokens_kernel(const int32_t* __restrict__ tokens, int32_
   out[m] = clamp_token(tokens[m - t + min(t + k, Tlen - 1)], V);
 }
 
-// Segment-causal attention backward (SIMT; one warp per (row, head), lanes
-// own head_dim slices).  Pass 1 (per query row m): log-sum-exp of the scores
-// over keys [seg_start(m), m], D_m = do_m . o_m, and
-// dq_m = scale sum_s P_ms (do_m . v_s - D_m) k_s.
-template <int HD>
-__global__ void attn_bwd_dq_kernel(const __nv_bfloat16* __restrict__ qkv, const __nv_bfloat16* __restrict__ o,
-                                   const __nv_bfloat16* __restrict__ dO, const int32_t* __restrict__ seg_start,
-                                   float* __restrict__ dqkv, float* __restrict__ lse_out, float* __restrict__ dsum_out,
-                                   int M, int Tlen, int H, float scale) {
-  constexpr int KD = HD / 32;
-  const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (item >= M * H) return;
-  const int m = item / H, h = item % H;
-  const int d = H * HD, t = m % Tlen, row0 = m - t;
-  float q[KD], dov[KD], ov[KD];
-#pragma unroll
-  for (int i = 0; i < KD; ++i) {
-    q[i] = __bfloat162float(qkv[static_cast<size_t>(m) * 3 * d + h * HD + lane * KD + i]);
-    dov[i] = __bfloat162float(dO[static_cast<size_t>(m) * d + h * HD + lane * KD + i]);
-    ov[i] = __bfloat162float(o[static_cast<size_t>(m) * d + h * HD + lane * KD + i]);
-  }
-  float dsum = 0.f;
-#pragma unroll
-  for (int i = 0; i < KD; ++i) dsum += dov[i] * ov[i];
-  dsum = mtp::warp_sum(dsum);
-  const int lo = row0 + seg_start[m];
-  float mx = -INFINITY, l = 0.f;
-  for (int s = lo; s <= m; ++s) {
-    const __nv_bfloat16* kr = qkv + static_cast<size_t>(s) * 3 * d + d + h * HD + lane * KD;
-    float acc = 0.f;
-#pragma unroll
-    for (int i = 0; i < KD; ++i) acc += q[i] * __bfloat162float(kr[i]);
-    const float sc = mtp::warp_sum(acc) * scale;
-    const float mn = fmaxf(mx, sc);
-    l = l * expf(mx - mn) + expf(sc - mn);
-    mx = mn;
-  }
-  const float lse = mx + logf(l);
-  float dq[KD] = {};
-  for (int s = lo; s <= m; ++s) {
-    const __nv_bfloat16* kr = qkv + static_cast<size_t>(s) * 3 * d + d + h * HD + lane * KD;
-    const __nv_bfloat16* vr = kr + d;
-    float acc = 0.f, dp = 0.f;
-    float kv[KD];
-#pragma unroll
-    for (int i = 0; i < KD; ++i) {
-      kv[i] = __bfloat162float(kr[i]);
-      acc += q[i] * kv[i];
-      dp += dov[i] * __bfloat162float(vr[i]);
-    }
-    const float sc = mtp::warp_sum(acc) * scale;
-    dp = mtp::warp_sum(dp);
-    const float ds = expf(sc - lse) * (dp - dsum);
-#pragma unroll
-    for (int i = 0; i < KD; ++i) dq[i] += ds * kv[i];
-  }
-#pragma unroll
-  for (int i = 0; i < KD; ++i) dqkv[static_cast<size_t>(m) * 3 * d + h * HD + lane * KD + i] = dq[i] * scale;
-  if (lane == 0) {
-    lse_out[static_cast<size_t>(m) * H + h] = lse;
-    dsum_out[static_cast<size_t>(m) * H + h] = dsum;
-  }
-}
-
-// Pass 2 (per key row s): the queries that see s are [s, max(seg_end(s), s+1));
-// dv_s = sum_t P_ts do_t, dk_s = scale sum_t P_ts (do_t . v_s - D_t) q_t.
-template <int HD>
-__global__ void attn_bwd_dkdv_kernel(const __nv_bfloat16* __restrict__ qkv, const __nv_bfloat16* __restrict__ dO,
-                                     const int32_t* __restrict__ seg_end, const float* __restrict__ lse,
-                                     const float* __restrict__ dsum, float* __restrict__ dqkv, int M, int Tlen, int H,
-                                     float scale) {
-  constexpr int KD = HD / 32;
-  const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (item >= M * H) return;
-  const int s = item / H, h = item % H;
-  const int d = H * HD, t = s % Tlen, row0 = s - t;
-  float kv[KD], vv[KD];
-#pragma unroll
-  for (int i = 0; i < KD; ++i) {
-    kv[i] = __bfloat162float(qkv[static_cast<size_t>(s) * 3 * d + d + h * HD + lane * KD + i]);
-    vv[i] = __bfloat162float(qkv[static_cast<size_t>(s) * 3 * d + 2 * d + h * HD + lane * KD + i]);
-  }
-  const int hi = row0 + max(seg_end[s], t + 1);
-  float dk[KD] = {}, dv[KD] = {};
-  for (int m = s; m < hi; ++m) {
-    const __nv_bfloat16* qr = qkv + static_cast<size_t>(m) * 3 * d + h * HD + lane * KD;
-    const __nv_bfloat16* dor = dO + static_cast<size_t>(m) * d + h * HD + lane * KD;
-    float qv[KD], dov[KD];
-    float acc = 0.f, dp = 0.f;
-#pragma unroll
-    for (int i = 0; i < KD; ++i) {
-      qv[i] = __bfloat162float(qr[i]);
-      dov[i] = __bfloat162float(dor[i]);
-      acc += qv[i] * kv[i];
-      dp += dov[i] * vv[i];
-    }
-    const float sc = mtp::warp_sum(acc) * scale;
-    dp = mtp::warp_sum(dp);
-    const float p = expf(sc - lse[static_cast<size_t>(m) * H + h]);
-    const float ds = p * (dp - dsum[static_cast<size_t>(m) * H + h]);
-#pragma unroll
-    for (int i = 0; i < KD; ++i) {
-      dv[i] += p * dov[i];
-      dk[i] += ds * qv[i];
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < KD; ++i) {
-    dqkv[static_cast<size_t>(s) * 3 * d + d + h * HD + lane * KD + i] = dk[i] * scale;
-    dqkv[static_cast<size_t>(s) * 3 * d + 2 * d + h * HD + lane * KD + i] = dv[i];
-  }
-}
-
 // scratch of the block backward (reused depth after depth)
 struct BwdLayout {
   size_t dhb, dhT, pq, gb, gT, dgf, dpq, dpqT, yT, dyf, daf, dab, daT, oT, dof, dob, dqkvf, dqkvb, dqkvT, xT, dxf,
-      duf, dub, duT, cT, dcf, alse, adsum, tok, wdT, wgT, wuT, woT, wqkvT, mT, total;
+      duf, dub, duT, cT, dcf, adsum, tok, wdT, wgT, wuT, woT, wqkvT, mT, total;
 };
 
 BwdLayout make_bwd_layout(const mtp_dims& D, size_t start, int mp) {
@@ -1336,7 +1226,6 @@ BwdLayout make_bwd_layout(const mtp_dims& D, size_t start, int mp) {
   B.duT = take(d * Mp * 2);
   B.cT = take(2 * d * Mp * 2);
   B.dcf = take(M * 2 * d * 4);
-  B.alse = take(M * D.n_heads * 4);
   B.adsum = take(M * D.n_heads * 4);
   B.tok = take(M * 4);
   B.wdT = take(f * d * 2);
@@ -1365,6 +1254,7 @@ SaveOff make_save_off(const mtp_dims& D) {
   S.o = take(M * d * 2);
   S.a = take(M * d * 2);
   S.y = take(M * d * 2);
+  S.lse2 = take(M * D.n_heads * 4);
   S.bytes = off;
   return S;
 }
@@ -1455,24 +1345,10 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
   MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dof), 0, Md * 4, st));
   TRY(gemm_acc(M, d, d, bb(B.dab), d, bb(B.woT), d, fb(B.dof), d, st));
   f32_to_bf16(fb(B.dof), d, bb(B.dob), d, M, d, st);
-  // segment-causal attention backward, then RoPE backward
-  const float scale = 1.0f / sqrtf(static_cast<float>(hd));
-  const int items = M * H;
-  const int32_t* ss = C.buf<int32_t>(C.L.seg_start);
-  const int32_t* se = C.buf<int32_t>(C.L.seg_end);
-  if (hd == 128) {
-    attn_bwd_dq_kernel<128><<<(items + 7) / 8, 256, 0, st>>>(qkv, o, bb(B.dob), ss, fb(B.dqkvf), fb(B.alse),
-                                                             fb(B.adsum), M, D.T, H, scale);
-    attn_bwd_dkdv_kernel<128><<<(items + 7) / 8, 256, 0, st>>>(qkv, bb(B.dob), se, fb(B.alse), fb(B.adsum),
-                                                               fb(B.dqkvf), M, D.T, H, scale);
-  } else {
-    attn_bwd_dq_kernel<64><<<(items + 7) / 8, 256, 0, st>>>(qkv, o, bb(B.dob), ss, fb(B.dqkvf), fb(B.alse),
-                                                            fb(B.adsum), M, D.T, H, scale);
-    attn_bwd_dkdv_kernel<64><<<(items + 7) / 8, 256, 0, st>>>(qkv, bb(B.dob), se, fb(B.alse), fb(B.adsum),
-                                                              fb(B.dqkvf), M, D.T, H, scale);
-  }
-  mtp::note_launch();
-  mtp::note_launch();
+  // segment-causal attention backward (tensor cores), then RoPE backward
+  TRY(mtp::attn_bwd_launch(qkv, o, bb(B.dob), reinterpret_cast<const float*>(sv + C.so.lse2),
+                           C.buf<int32_t>(C.L.seg_start), C.buf<int32_t>(C.L.seg_end), fb(B.dqkvf), fb(B.adsum), D.B,
+                           D.T, H, hd, st));
   rope_bwd_kernel<<<4 * 152, 256, 0, st>>>(fb(B.dqkvf), C.buf<float2>(C.L.rope), C.pos, bb(B.dqkvb), M, d, hd, D.T,
                                            D.rope_base > 0.f ? 1 : 0);
   mtp::note_launch();
