@@ -914,46 +914,80 @@ __global__ void term_scale_kernel(const double* __restrict__ sc, float* __restri
   for (int k = 1; k <= D; ++k) scale[k] = static_cast<float>(weight(k) * term_inv(k));
 }
 
-// out[c][r] = in[r][c] for a bf16 [R, C] matrix; 32 x 32 tiles through shared memory
-__global__ void transpose_bf16_kernel(const __nv_bfloat16* __restrict__ in, int R, int Cn, int ldi,
-                                      __nv_bfloat16* __restrict__ out, int ldo) {
-  __shared__ __nv_bfloat16 tile[32][34];
-  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
-  const int tx = threadIdx.x, ty = threadIdx.y;  // block (32, 8)
-  for (int j = ty; j < 32; j += 8) {
-    const int r = r0 + j, c = c0 + tx;
-    if (r < R && c < Cn) tile[j][tx] = in[static_cast<size_t>(r) * ldi + c];
-  }
-  __syncthreads();
-  for (int j = ty; j < 32; j += 8) {
-    const int c = c0 + j, r = r0 + tx;
-    if (c < Cn && r < R) out[static_cast<size_t>(c) * ldo + r] = tile[tx][j];
+// out[c][r] = in[r][c] for a bf16 [R, C] matrix.  64 x 64 tiles through
+// shared memory (rows padded by 4 bytes so that reading 8 rows of one column
+// hits distinct banks); with 16-byte-aligned rows (C, ldi, ldo multiples of 8)
+// rows are read and written 8 elements at a time, else element by element.
+constexpr int kTp = 64;
+__global__ void __launch_bounds__(256)
+transpose_bf16_kernel(const __nv_bfloat16* __restrict__ in, int R, int Cn, int ldi, __nv_bfloat16* __restrict__ out,
+                      int ldo, int vec) {
+  __shared__ __nv_bfloat16 tile[kTp][kTp + 2];
+  const int c0 = blockIdx.x * kTp, r0 = blockIdx.y * kTp;
+  const int t = threadIdx.x;
+  if (vec) {
+    // 64 rows x 8 pieces of 8 elements: 2 pieces per thread
+    for (int p = t; p < kTp * 8; p += 256) {
+      const int r = p >> 3, c = (p & 7) * 8;
+      uint4 u = make_uint4(0u, 0u, 0u, 0u);
+      if (r0 + r < R && c0 + c < Cn) u = *reinterpret_cast<const uint4*>(in + static_cast<size_t>(r0 + r) * ldi + c0 + c);
+      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) tile[r][c + i] = e[i];
+    }
+    __syncthreads();
+    for (int p = t; p < kTp * 8; p += 256) {
+      const int c = p >> 3, r = (p & 7) * 8;  // output row c (input column), 8 input rows
+      if (c0 + c >= Cn || r0 + r >= R) continue;
+      uint4 u;
+      __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(&u);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) e[i] = tile[r + i][c];
+      if (r0 + r + 8 <= R) {
+        *reinterpret_cast<uint4*>(out + static_cast<size_t>(c0 + c) * ldo + r0 + r) = u;
+      } else {
+        for (int i = 0; i < 8 && r0 + r + i < R; ++i) out[static_cast<size_t>(c0 + c) * ldo + r0 + r + i] = e[i];
+      }
+    }
+  } else {
+    for (int p = t; p < kTp * kTp; p += 256) {
+      const int r = p / kTp, c = p % kTp;
+      if (r0 + r < R && c0 + c < Cn) tile[r][c] = in[static_cast<size_t>(r0 + r) * ldi + c0 + c];
+    }
+    __syncthreads();
+    for (int p = t; p < kTp * kTp; p += 256) {
+      const int c = p / kTp, r = p % kTp;
+      if (c0 + c < Cn && r0 + r < R) out[static_cast<size_t>(c0 + c) * ldo + r0 + r] = tile[r][c];
+    }
   }
 }
 
 void transpose_bf16(const __nv_bfloat16* in, int R, int Cn, int ldi, __nv_bfloat16* out, int ldo, cudaStream_t st) {
-  transpose_bf16_kernel<<<dim3((Cn + 31) / 32, (R + 31) / 32), dim3(32, 8), 0, st>>>(in, R, Cn, ldi, out, ldo);
+  const int vec = (Cn % 8 == 0 && ldi % 8 == 0 && ldo % 8 == 0 && mtp::aligned16(in) && mtp::aligned16(out)) ? 1 : 0;
+  transpose_bf16_kernel<<<dim3((Cn + kTp - 1) / kTp, (R + kTp - 1) / kTp), 256, 0, st>>>(in, R, Cn, ldi, out, ldo,
+                                                                                      vec);
   mtp::note_launch();
 }
 
 // RMSNorm backward for y = g * h * r, r = (mean(h^2) + eps)^(-1/2), given
 // dy: dh += r (g dy - xh * mean(g dy xh)) with xh = h r; dg += sum over rows
 // of dy xh.  Row m reads h row h_rows[m] (or m) and adds its dh into row
-// dh_rows[m] with atomics (or row m plainly); dh may be null.  A block of 8
-// warps takes 64 rows (8 per warp); the gain gradient is summed in shared
-// memory and added to dg once per block.
-constexpr int kNormBwdRows = 64;
+// dh_rows[m] with atomics (or row m plainly); dh may be null.  A block
+// takes 16 rows: its warps first form each row's r and mean(g dy xh), then
+// threads sweep columns across the rows (coalesced), summing the gain
+// gradient in a register and adding it to dg once per block.
+constexpr int kNormBwdRows = 16;
 __global__ void __launch_bounds__(256)
 rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, int ld_h, const int32_t* __restrict__ h_rows,
                    const __nv_bfloat16* __restrict__ g, const float* __restrict__ dy, int ld_dy, float* __restrict__ dh,
                    int ld_dh, const int32_t* __restrict__ dh_rows, float* __restrict__ dg, int M, int d, float eps) {
-  extern __shared__ float s_dg[];
-  for (int i = threadIdx.x; i < d; i += blockDim.x) s_dg[i] = 0.f;
-  __syncthreads();
+  __shared__ float s_r[kNormBwdRows], s_mean[kNormBwdRows];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int j = 0; j < kNormBwdRows / 8; ++j) {
-    const int m = blockIdx.x * kNormBwdRows + warp * (kNormBwdRows / 8) + j;
-    if (m >= M) break;
+  const int m0 = blockIdx.x * kNormBwdRows;
+  const int rows = min(kNormBwdRows, M - m0);
+  // row statistics: r = (mean(h^2) + eps)^(-1/2) and mean(g dy xh) (2 rows per warp)
+  for (int j = warp; j < rows; j += 8) {
+    const int m = m0 + j;
     const __nv_bfloat16* hr = h + static_cast<size_t>(h_rows ? h_rows[m] : m) * ld_h;
     const float* dyr = dy + static_cast<size_t>(m) * ld_dy;
     float ss = 0.f, dot = 0.f;
@@ -964,29 +998,39 @@ rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, int ld_h, const int32_t*
     }
     ss = mtp::warp_sum(ss);
     dot = mtp::warp_sum(dot);
-    const float r = 1.0f / sqrtf(ss / d + eps);
-    const float mean_gdx = dot * r / d;  // mean over the row of g dy xh
-    float* dhr = dh ? dh + static_cast<size_t>(dh_rows ? dh_rows[m] : m) * ld_dh : nullptr;
-    for (int i = lane; i < d; i += 32) {
-      const float xh = __bfloat162float(hr[i]) * r;
-      const float dyv = dyr[i];
-      if (dhr) {
-        const float v = r * (__bfloat162float(g[i]) * dyv - xh * mean_gdx);
-        if (dh_rows) atomicAdd(dhr + i, v);
-        else dhr[i] += v;
-      }
-      atomicAdd(&s_dg[i], dyv * xh);
+    if (lane == 0) {
+      const float r = 1.0f / sqrtf(ss / d + eps);
+      s_r[j] = r;
+      s_mean[j] = dot * r / d;
     }
   }
   __syncthreads();
-  if (dg)
-    for (int i = threadIdx.x; i < d; i += blockDim.x) atomicAdd(&dg[i], s_dg[i]);
+  // columns across the block's rows: coalesced row reads, the gain gradient summed in a register
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    const float gi = __bfloat162float(g[i]);
+    float dg_acc = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < rows; ++j) {
+      const int m = m0 + j;
+      const float r = s_r[j];
+      const float xh = __bfloat162float(h[static_cast<size_t>(h_rows ? h_rows[m] : m) * ld_h + i]) * r;
+      const float dyv = dy[static_cast<size_t>(m) * ld_dy + i];
+      dg_acc += dyv * xh;
+      if (dh) {
+        const float v = r * (gi * dyv - xh * s_mean[j]);
+        float* dst = dh + static_cast<size_t>(dh_rows ? dh_rows[m] : m) * ld_dh + i;
+        if (dh_rows) atomicAdd(dst, v);
+        else *dst += v;
+      }
+    }
+    if (dg) atomicAdd(&dg[i], dg_acc);
+  }
 }
 
 void rmsnorm_bwd(const __nv_bfloat16* h, int ld_h, const int32_t* h_rows, const __nv_bfloat16* g, const float* dy,
                  int ld_dy, float* dh, int ld_dh, const int32_t* dh_rows, float* dg, int M, int d, float eps,
                  cudaStream_t st) {
-  rmsnorm_bwd_kernel<<<(M + kNormBwdRows - 1) / kNormBwdRows, 256, d * sizeof(float), st>>>(
+  rmsnorm_bwd_kernel<<<(M + kNormBwdRows - 1) / kNormBwdRows, 256, 0, st>>>(
       h, ld_h, h_rows, g, dy, ld_dy, dh, ld_dh, dh_rows, dg, M, d, eps);
   mtp::note_launch();
 }
@@ -1050,10 +1094,11 @@ mtp::GemmDesc gdesc(int M, int N, int K, const __nv_bfloat16* A, int lda, const 
 }
 
 // gradients through the shared head and the final norm of term t (state h_t):
-// per vocabulary chunk the logits are recomputed twice -- as [tokens, chunk]
-// for dz and as [chunk, tokens] for dz^T -- and never stored whole; then
-// dX += dz W_U[chunk] and d_head[chunk] += dz^T X; finally the final RMSNorm's
-// backward adds d h_t into dstate[t] and accumulates d_out_norm.
+// per vocabulary chunk the logits are recomputed by one GEMM whose epilogue
+// writes dz = (softmax - onehot) dL/dl (the logits are never stored whole);
+// then dX += dz W_U[chunk] and, from dz^T (a transpose), d_head[chunk] +=
+// dz^T X; finally the final RMSNorm's backward adds d h_t into dstate[t] and
+// accumulates d_out_norm.
 mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_bfloat16* h_t, float* d_head,
                          float* d_out_norm) {
   using bf = __nv_bfloat16;
@@ -1090,15 +1135,7 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
     g.ldo = d;
     TRY(mtp::gemm_bf16_launch(g, C.st));
     if (!d_head) continue;
-    g = gdesc(vc, M, d, WU + static_cast<size_t>(v0) * d, d, x, d);
-    g.epi = mtp::EPI_CE_GRAD_T;
-    g.out = dzt;
-    g.ldo = T.mp;
-    g.labels = labels;
-    g.lse = lse;
-    g.ce_scale = scale;
-    g.ce_offset = v0;
-    TRY(mtp::gemm_bf16_launch(g, C.st));
+    transpose_bf16(dz, M, vc, T.vc, dzt, T.mp, C.st);  // dz^T for the head's weight gradient
     g = gdesc(vc, d, M, dzt, T.mp, xt, T.mp);
     g.epi = mtp::EPI_F32_ACC;
     g.out_f32 = d_head + static_cast<size_t>(v0) * d;
@@ -1259,13 +1296,26 @@ SaveOff make_save_off(const mtp_dims& D) {
   return S;
 }
 
-// C += A B^T into fp32 (one writer per element)
+// C += A B^T into fp32.  When the output has fewer 128 x 256 tiles than two
+// per SM, K is split (partial tiles added with vector atomics).
 mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, const __nv_bfloat16* B, int ldb, float* out,
                     int ldo, cudaStream_t st) {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
   mtp::GemmDesc g = gdesc(M, N, K, A, lda, B, ldb);
   g.epi = mtp::EPI_F32_ACC;
   g.out_f32 = out;
   g.ldo = ldo;
+  const int tiles = ((M + 127) / 128) * ((N + 255) / 256);
+  const int nk = (K + 63) / 64;
+  int splits = 1;
+  if (tiles < 2 * sms) splits = std::max(1, std::min((2 * sms + tiles - 1) / tiles, nk / 8));
+  g.splits = splits;
   return mtp::gemm_bf16_launch(g, st);
 }
 

@@ -460,6 +460,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         load_res64(rq[0], P.resid, P.ldr, P.M, P.N, rrow, tn * BN);
         load_res64(rq[1], P.resid, P.ldr, P.M, P.N, rrow, tn * BN + 64);
       }
+      // CE backward: the row's label, log-sum-exp and scale, fetched while the MMAs run
+      // (log2 domain; a row without a label gets lse = +inf, so its exp is 0 and its scale 0)
+      int ce_lab = -1;
+      float ce_lse2 = INFINITY, ce_sc = 0.f;
+      if constexpr (EPI == EPI_CE_GRAD) {
+        const int prow = tm * BM + quarter * 32 + lane;
+        if (prow < P.M) {
+          ce_lab = P.labels[prow];
+          if (ce_lab >= 0) {
+            ce_lse2 = P.lse[prow] * 1.4426950408889634f;
+            ce_sc = *P.ce_scale;
+          }
+        }
+      }
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
       tc_fence_after();
       const int row0w = tm * BM + quarter * 32;
@@ -589,9 +603,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
         }
       } else if constexpr (EPI == EPI_CE_GRAD) {
-        const int lab = row_ok ? P.labels[row] : -1;
-        const float lse = lab >= 0 ? P.lse[row] : 0.f;
-        const float sc = lab >= 0 ? *P.ce_scale : 0.f;
+        const float lse2 = ce_lse2, sc = ce_sc;
 #pragma unroll 1
         for (int c = 0; c < BN / 64; ++c) {
           const int col0 = tn * BN + c * 64;
@@ -600,9 +612,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           for (int half = 0; half < 2; ++half) {
             float v[32];
             tmem_ld32(taddr + c * 64 + half * 32, v);
-            const int off = lab - (P.ce_offset + col0 + half * 32);
+            const int off = ce_lab - (P.ce_offset + col0 + half * 32);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = lab >= 0 ? (__expf(v[i] - lse) - (i == off ? 1.f : 0.f)) * sc : 0.f;
+            for (int i = 0; i < 32; ++i)
+              v[i] = fmaf(exp2f(fmaf(v[i], 1.4426950408889634f, -lse2)), sc, i == off ? -sc : 0.f);
             box_write32(box, lane, half, v);
           }
           ship(box, col0, row0w);
@@ -641,7 +654,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const int col0 = tn * BN + c * 32;
           if (row_ok && col0 < P.N) {
             float* dst = P.out_f32 + static_cast<size_t>(row) * P.ldo + col0;
-            if (col0 + 32 <= P.N) {
+            if (P.splits > 1) {  // split-K partial tile: vector atomics
+              if (col0 + 32 <= P.N) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                  atomicAdd(reinterpret_cast<float4*>(dst + 4 * q),
+                            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+              } else {
+                for (int i = 0; i < 32 && col0 + i < P.N; ++i) atomicAdd(dst + i, v[i]);
+              }
+            } else if (col0 + 32 <= P.N) {
 #pragma unroll
               for (int q = 0; q < 8; ++q) {
                 float4 o = *reinterpret_cast<float4*>(dst + 4 * q);
@@ -864,9 +886,12 @@ mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream) {
     case EPI_CE_GRAD_T:
       if (!g.labels || !g.lse || !g.ce_scale) return MTP_ERR_INVALID_ARG;
       return g.epi == EPI_CE_GRAD ? launch<256, EPI_CE_GRAD>(g, stream) : launch<256, EPI_CE_GRAD_T>(g, stream);
-    case EPI_F32_ACC:
-      if (!g.out_f32 || g.ldo % 4 || !aligned16(g.out_f32) || g.splits > 1) return MTP_ERR_INVALID_ARG;
+    case EPI_F32_ACC: {
+      if (!g.out_f32 || g.ldo % 4 || !aligned16(g.out_f32)) return MTP_ERR_INVALID_ARG;
+      const int nk = (g.K + BK - 1) / BK;
+      if (g.splits < 1 || g.splits > nk) return MTP_ERR_INVALID_ARG;
       return launch<256, EPI_F32_ACC>(g, stream);
+    }
     case EPI_T_STORE:
     case EPI_T_ATOMIC: {
       if (g.N > 32 || !g.out_f32 || g.nseg != 1) return MTP_ERR_UNSUPPORTED;

@@ -24,7 +24,7 @@ enum GemmEpilogue : int {
   EPI_CE_GRAD = 7,
   // the same with rows = vocabulary entries ce_offset + row and columns = tokens
   EPI_CE_GRAD_T = 8,
-  EPI_F32_ACC = 9  // out_f32[row * ldo + col] += acc (one writer per element: no split-K)
+  EPI_F32_ACC = 9  // out_f32[row * ldo + col] += acc (read-modify-write; with split-K, vector atomics)
 };
 
 // Epilogues that write bf16 boxes through the shared-memory staging buffers.
