@@ -1058,7 +1058,7 @@ TrainLayout make_train_layout(const mtp_dims& D) {
   const size_t M = static_cast<size_t>(D.B) * D.T, d = D.d;
   T.vp = round_up8(D.V);
   T.mp = round_up8(static_cast<int>(M));
-  T.vc = std::min(8192, T.vp);
+  T.vc = std::min(32768, T.vp);  // vocabulary chunk of the head backward
   size_t off = make_layout(D).total;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -1078,6 +1078,9 @@ TrainLayout make_train_layout(const mtp_dims& D) {
   T.total = off;
   return T;
 }
+
+mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, const __nv_bfloat16* B, int ldb, float* out,
+                    int ldo, cudaStream_t st);
 
 mtp::GemmDesc gdesc(int M, int N, int K, const __nv_bfloat16* A, int lda, const __nv_bfloat16* B, int ldb) {
   mtp::GemmDesc g;
@@ -1129,18 +1132,10 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
     g.ce_scale = scale;
     g.ce_offset = v0;
     TRY(mtp::gemm_bf16_launch(g, C.st));
-    g = gdesc(M, d, vc, dz, T.vc, wut + v0, T.vp);
-    g.epi = mtp::EPI_F32_ACC;
-    g.out_f32 = dx;
-    g.ldo = d;
-    TRY(mtp::gemm_bf16_launch(g, C.st));
+    TRY(gemm_acc(M, d, vc, dz, T.vc, wut + v0, T.vp, dx, d, C.st));
     if (!d_head) continue;
     transpose_bf16(dz, M, vc, T.vc, dzt, T.mp, C.st);  // dz^T for the head's weight gradient
-    g = gdesc(vc, d, M, dzt, T.mp, xt, T.mp);
-    g.epi = mtp::EPI_F32_ACC;
-    g.out_f32 = d_head + static_cast<size_t>(v0) * d;
-    g.ldo = d;
-    TRY(mtp::gemm_bf16_launch(g, C.st));
+    TRY(gemm_acc(vc, d, M, dzt, T.mp, xt, T.mp, d_head + static_cast<size_t>(v0) * d, d, C.st));
   }
   float* dstate_t = C.buf<float>(T.dstate) + static_cast<size_t>(t) * M * d;
   rmsnorm_bwd(h_t, d, nullptr, out_norm, dx, d, dstate_t, d, nullptr, d_out_norm, M, d, D.eps, C.st);
@@ -1150,18 +1145,18 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
 
 // ---- block backward -------------------------------------------------------
 
-// y[i] = bf16(x[i]) for an fp32 [R, C] matrix (row strides ldx, ldy)
+// y = bf16(x) for an fp32 [R, C] matrix (row strides ldx, ldy); block rows
+// stride over matrix rows, threads over columns (no per-element division)
 __global__ void f32_to_bf16_kernel(const float* __restrict__ x, int ldx, __nv_bfloat16* __restrict__ y, int ldy, int R,
                                    int Cn) {
-  const size_t n = static_cast<size_t>(R) * Cn;
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const size_t r = i / Cn, c = i % Cn;
-    y[r * ldy + c] = __float2bfloat16_rn(x[r * ldx + c]);
+  for (int r = blockIdx.x; r < R; r += gridDim.x) {
+    const float* xr = x + static_cast<size_t>(r) * ldx;
+    __nv_bfloat16* yr = y + static_cast<size_t>(r) * ldy;
+    for (int c = threadIdx.x; c < Cn; c += blockDim.x) yr[c] = __float2bfloat16_rn(xr[c]);
   }
 }
 void f32_to_bf16(const float* x, int ldx, __nv_bfloat16* y, int ldy, int R, int Cn, cudaStream_t st) {
-  f32_to_bf16_kernel<<<4 * 152, 256, 0, st>>>(x, ldx, y, ldy, R, Cn);
+  f32_to_bf16_kernel<<<std::min(R, 16 * 152), 256, 0, st>>>(x, ldx, y, ldy, R, Cn);
   mtp::note_launch();
 }
 
@@ -1169,17 +1164,20 @@ void f32_to_bf16(const float* x, int ldx, __nv_bfloat16* y, int ldy, int R, int 
 // bf16) and dg ([M, ffn] fp32): g = silu(p) q, dp = dg q silu'(p), dq = dg silu(p)
 __global__ void swiglu_bwd_kernel(const __nv_bfloat16* __restrict__ pq, const float* __restrict__ dg,
                                   __nv_bfloat16* __restrict__ g, __nv_bfloat16* __restrict__ dpq, int M, int ffn) {
-  const size_t n = static_cast<size_t>(M) * ffn;
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const size_t m = i / ffn, j = i % ffn;
-    const float p = __bfloat162float(pq[m * 2 * ffn + j]), q = __bfloat162float(pq[m * 2 * ffn + ffn + j]);
-    const float sg = 1.0f / (1.0f + expf(-p));
-    const float silu = p * sg;
-    const float dgv = dg[i];
-    g[i] = __float2bfloat16_rn(silu * q);
-    dpq[m * 2 * ffn + j] = __float2bfloat16_rn(dgv * q * (sg * (1.0f + p * (1.0f - sg))));
-    dpq[m * 2 * ffn + ffn + j] = __float2bfloat16_rn(dgv * silu);
+  for (int m = blockIdx.x; m < M; m += gridDim.x) {
+    const __nv_bfloat16* pr = pq + static_cast<size_t>(m) * 2 * ffn;
+    const float* dgr = dg + static_cast<size_t>(m) * ffn;
+    __nv_bfloat16* gr = g + static_cast<size_t>(m) * ffn;
+    __nv_bfloat16* dr = dpq + static_cast<size_t>(m) * 2 * ffn;
+    for (int j = threadIdx.x; j < ffn; j += blockDim.x) {
+      const float p = __bfloat162float(pr[j]), q = __bfloat162float(pr[ffn + j]);
+      const float sg = 1.0f / (1.0f + __expf(-p));
+      const float silu = p * sg;
+      const float dgv = dgr[j];
+      gr[j] = __float2bfloat16_rn(silu * q);
+      dr[j] = __float2bfloat16_rn(dgv * q * (sg * (1.0f + p * (1.0f - sg))));
+      dr[ffn + j] = __float2bfloat16_rn(dgv * silu);
+    }
   }
 }
 
@@ -1190,26 +1188,24 @@ __global__ void rope_bwd_kernel(const float* __restrict__ dqkv, const float2* __
                                 const int32_t* __restrict__ pos, __nv_bfloat16* __restrict__ out, int M, int d, int hd,
                                 int Tlen, int use_rope) {
   const int half = hd / 2;
-  const size_t n = static_cast<size_t>(M) * d;  // d pairs (q and k heads) + d v columns per row
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const size_t m = i / d;
-    const int pi = static_cast<int>(i % d);
-    const float* src = dqkv + m * 3 * d;
-    __nv_bfloat16* dst = out + m * 3 * d;
-    const int head = pi / half, j = pi % half;
-    const int col = head * hd + j;
-    const float d1 = src[col], d2 = src[col + half];
-    float c = 1.f, sn = 0.f;
-    if (use_rope) {
-      const int p = min(max(pos[m], 0), Tlen - 1);
-      const float2 cs = rope[static_cast<size_t>(p) * half + j];
-      c = cs.x;
-      sn = cs.y;
+  for (int m = blockIdx.x; m < M; m += gridDim.x) {
+    const float* src = dqkv + static_cast<size_t>(m) * 3 * d;
+    __nv_bfloat16* dst = out + static_cast<size_t>(m) * 3 * d;
+    const float2* cs_row = rope + static_cast<size_t>(min(max(pos[m], 0), Tlen - 1)) * half;
+    for (int pi = threadIdx.x; pi < d; pi += blockDim.x) {  // d pairs of the q and k heads, then v column pi
+      const int head = pi / half, j = pi - head * half;
+      const int col = head * hd + j;
+      const float d1 = src[col], d2 = src[col + half];
+      float c = 1.f, sn = 0.f;
+      if (use_rope) {
+        const float2 cs = cs_row[j];
+        c = cs.x;
+        sn = cs.y;
+      }
+      dst[col] = __float2bfloat16_rn(d1 * c + d2 * sn);
+      dst[col + half] = __float2bfloat16_rn(d2 * c - d1 * sn);
+      dst[2 * d + pi] = __float2bfloat16_rn(src[2 * d + pi]);
     }
-    dst[col] = __float2bfloat16_rn(d1 * c + d2 * sn);
-    dst[col + half] = __float2bfloat16_rn(d2 * c - d1 * sn);
-    dst[2 * d + pi] = __float2bfloat16_rn(src[2 * d + pi]);
   }
 }
 
@@ -1225,7 +1221,7 @@ __global__ void shifted_tokens_kernel(const int32_t* __restrict__ tokens, int32_
 // scratch of the block backward (reused depth after depth)
 struct BwdLayout {
   size_t dhb, dhT, pq, gb, gT, dgf, dpq, dpqT, yT, dyf, daf, dab, daT, oT, dof, dob, dqkvf, dqkvb, dqkvT, xT, dxf,
-      duf, dub, duT, cT, dcf, adsum, tok, wdT, wgT, wuT, woT, wqkvT, mT, total;
+      duf, dub, duT, cT, dcf, adsum, tok, wdT, wgT, woT, wqkvT, mT, total;
 };
 
 BwdLayout make_bwd_layout(const mtp_dims& D, size_t start, int mp) {
@@ -1266,8 +1262,7 @@ BwdLayout make_bwd_layout(const mtp_dims& D, size_t start, int mp) {
   B.adsum = take(M * D.n_heads * 4);
   B.tok = take(M * 4);
   B.wdT = take(f * d * 2);
-  B.wgT = take(d * f * 2);
-  B.wuT = take(d * f * 2);
+  B.wgT = take(d * 2 * f * 2);
   B.woT = take(d * d * 2);
   B.wqkvT = take(d * 3 * d * 2);
   B.mT = take(2 * d * d * 2);
@@ -1296,8 +1291,10 @@ SaveOff make_save_off(const mtp_dims& D) {
   return S;
 }
 
-// C += A B^T into fp32.  When the output has fewer 128 x 256 tiles than two
-// per SM, K is split (partial tiles added with vector atomics).
+// C += A B^T into fp32.  K is split (partial tiles added with vector atomics)
+// when that fills the SMs' waves better: the smallest split whose work units
+// fill at least 90% of their last wave, else the best one (at most 16, and
+// at least 8 k-blocks per split).
 mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, const __nv_bfloat16* B, int ldb, float* out,
                     int ldo, cudaStream_t st) {
   static int sms = 0;
@@ -1313,8 +1310,18 @@ mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, const 
   g.ldo = ldo;
   const int tiles = ((M + 127) / 128) * ((N + 255) / 256);
   const int nk = (K + 63) / 64;
+  const int max_split = std::max(1, std::min(16, nk / 8));
   int splits = 1;
-  if (tiles < 2 * sms) splits = std::max(1, std::min((2 * sms + tiles - 1) / tiles, nk / 8));
+  double best = 0.0;
+  for (int sp = 1; sp <= max_split; ++sp) {
+    const long long units = static_cast<long long>(tiles) * sp;
+    const double eff = static_cast<double>(units) / (static_cast<double>(sms) * ((units + sms - 1) / sms));
+    if (eff > best + 1e-9) {
+      best = eff;
+      splits = sp;
+    }
+    if (eff >= 0.9) break;
+  }
   g.splits = splits;
   return mtp::gemm_bf16_launch(g, st);
 }
@@ -1342,8 +1349,8 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
   float* dh_prev = fb(T.dstate) + static_cast<size_t>(k - 1) * Md;
   // weights of the depth, transposed for the input-gradient GEMMs
   transpose_bf16(wt(C.W.w_down), d, f, f, bb(B.wdT), d, st);
-  transpose_bf16(wt(C.W.w_gate), f, d, d, bb(B.wgT), f, st);
-  transpose_bf16(wt(C.W.w_up), f, d, d, bb(B.wuT), f, st);
+  transpose_bf16(wt(C.W.w_gate), f, d, d, bb(B.wgT), 2 * f, st);      // [Wg^T | Wu^T]: [d, 2 ffn]
+  transpose_bf16(wt(C.W.w_up), f, d, d, bb(B.wgT) + f, 2 * f, st);
   transpose_bf16(wt(C.W.wo), d, d, d, bb(B.woT), d, st);
   transpose_bf16(wt(C.W.wq), d, d, d, bb(B.wqkvT), 3 * d, st);
   transpose_bf16(wt(C.W.wk), d, d, d, bb(B.wqkvT) + d, 3 * d, st);
@@ -1367,7 +1374,7 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
   }
   MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dgf), 0, static_cast<size_t>(M) * f * 4, st));
   TRY(gemm_acc(M, f, d, bb(B.dhb), d, bb(B.wdT), d, fb(B.dgf), f, st));
-  swiglu_bwd_kernel<<<4 * 152, 256, 0, st>>>(bb(B.pq), fb(B.dgf), bb(B.gb), bb(B.dpq), M, f);
+  swiglu_bwd_kernel<<<std::min(M, 16 * 152), 256, 0, st>>>(bb(B.pq), fb(B.dgf), bb(B.gb), bb(B.dpq), M, f);
   mtp::note_launch();
   if (float* gwd = gp(G->w_down)) {
     transpose_bf16(bb(B.gb), M, f, f, bb(B.gT), Mp, st);
@@ -1380,8 +1387,7 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
   if (float* gu = gp(G->w_up))
     TRY(gemm_acc(f, d, M, bb(B.dpqT) + static_cast<size_t>(f) * Mp, Mp, bb(B.yT), Mp, gu, d, st));
   MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dyf), 0, Md * 4, st));
-  TRY(gemm_acc(M, d, f, bb(B.dpq), 2 * f, bb(B.wgT), f, fb(B.dyf), d, st));
-  TRY(gemm_acc(M, d, f, bb(B.dpq) + f, 2 * f, bb(B.wuT), f, fb(B.dyf), d, st));
+  TRY(gemm_acc(M, d, 2 * f, bb(B.dpq), 2 * f, bb(B.wgT), 2 * f, fb(B.dyf), d, st));
   // y = RMSNorm_f(a): da = dh + RMSNorm backward
   MTP_CUDA_TRY(cudaMemcpyAsync(fb(B.daf), dh, Md * 4, cudaMemcpyDeviceToDevice, st));
   rmsnorm_bwd(a, d, nullptr, wt(C.W.ffn_norm), fb(B.dyf), d, fb(B.daf), d, nullptr, gp(G->ffn_norm), M, d, D.eps, st);
@@ -1399,7 +1405,7 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
   TRY(mtp::attn_bwd_launch(qkv, o, bb(B.dob), reinterpret_cast<const float*>(sv + C.so.lse2),
                            C.buf<int32_t>(C.L.seg_start), C.buf<int32_t>(C.L.seg_end), fb(B.dqkvf), fb(B.adsum), D.B,
                            D.T, H, hd, st));
-  rope_bwd_kernel<<<4 * 152, 256, 0, st>>>(fb(B.dqkvf), C.buf<float2>(C.L.rope), C.pos, bb(B.dqkvb), M, d, hd, D.T,
+  rope_bwd_kernel<<<std::min(M, 16 * 152), 256, 0, st>>>(fb(B.dqkvf), C.buf<float2>(C.L.rope), C.pos, bb(B.dqkvb), M, d, hd, D.T,
                                            D.rope_base > 0.f ? 1 : 0);
   mtp::note_launch();
   // q, k, v = x W{q,k,v}^T: dW += d{q,k,v}^T x; dx = [dq dk dv] [Wq; Wk; Wv]
