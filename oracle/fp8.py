@@ -14,12 +14,25 @@ taken exactly (an e4m3 value has 4 significant bits and the scale 24, so the
 float64 product is exact).  The FP8 draft step is the draft-step oracle run on
 these exact weights.
 
+The activations of such a GEMM enter the tensor cores as e4m3 too (the
+runtime's compute representation; reading): each 128-wide k-tile of a token's
+bf16 activation row is scaled by the power of two 2^E with the smallest E such
+that max|x| <= 448 * 2^E, and represented as 2^E (hi + lo) with
+hi = RNE_e4m3(x / 2^E) and lo = RNE_e4m3(x / 2^E - hi) (round to nearest,
+ties to even, saturating).  Because a bf16 value has 8 significant bits and an
+e4m3 value 4, the two terms reproduce every element of magnitude >= 2^(E-2)
+exactly; smaller ones are off by at most 2^(E-10) (the e4m3 subnormal step is
+2^-9).  ``split_activations`` states this; ``gemm_split`` is the GEMM on the
+represented activations.
+
 Pins (tests/test_oracle_fp8.py): the decoder against torch's float8_e4m3fn
 conversion on all 256 codes and at the format's landmarks (448, 2^-6, 2^-9,
 ±0, NaN); dequantisation with unit scales is the decoder; a scale grid that is
 one except for a single block multiplies exactly that block's elements
 (ragged edges included); the GEMM against x @ (decoded q * Kronecker-expanded
-scale grid)^T built from library routines.
+scale grid)^T built from library routines; the rounding function against
+torch's float8 conversion on random and tie values; the split's exponent
+minimality, exactness region and error bound.
 """
 from __future__ import annotations
 
@@ -75,3 +88,67 @@ def draft_weights(W: dict, fp8: dict) -> dict:
         q, s = fp8[name]
         out[name] = [dequantize(np.asarray(q), np.asarray(s))]
     return out
+
+
+# ---------------------------------------------------------------------------
+# activations as two e4m3 terms per 128-wide k-tile
+# ---------------------------------------------------------------------------
+_POS = np.array(sorted(v for v in _TABLE[:0x7F] if v >= 0.0))  # the 127 finite non-negative values, codes 0..126
+
+
+def e4m3_round(v) -> np.ndarray:
+    """Nearest E4M3 value to each float (ties to the even code, i.e. the
+    value whose mantissa's last bit is 0), saturating at +-448."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.minimum(np.abs(v), 448.0)
+    hi = np.searchsorted(_POS, a, side="left")          # first value >= a
+    hi = np.minimum(hi, len(_POS) - 1)
+    lo = np.maximum(hi - 1, 0)
+    dlo, dhi = a - _POS[lo], _POS[hi] - a
+    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    return np.copysign(_POS[pick], v)
+
+
+def split_exponent(amax: float) -> int:
+    """Smallest integer E with amax <= 448 * 2^E (0 for amax = 0)."""
+    if amax == 0.0:
+        return 0
+    E = int(np.floor(np.log2(amax / 448.0)))
+    while amax > 448.0 * 2.0 ** E:
+        E += 1
+    while amax <= 448.0 * 2.0 ** (E - 1):
+        E -= 1
+    return E
+
+
+def split_activations(x):
+    """x [R, K] (bf16 values) -> (E [R, ceil(K/128)] int, hi, lo [R, K] float64
+    e4m3 values) with x ~= 2^E (hi + lo) per 128-wide k-tile."""
+    x = np.asarray(x, dtype=np.float64)
+    R, K = x.shape
+    nkb = -(-K // BLOCK)
+    E = np.zeros((R, nkb), dtype=np.int64)
+    hi = np.zeros_like(x)
+    lo = np.zeros_like(x)
+    for r in range(R):
+        for kb in range(nkb):
+            sl = slice(kb * BLOCK, min(K, (kb + 1) * BLOCK))
+            e = split_exponent(float(np.abs(x[r, sl]).max()))
+            v = x[r, sl] / 2.0 ** e
+            h = e4m3_round(v)
+            E[r, kb] = e
+            hi[r, sl] = h
+            lo[r, sl] = e4m3_round(v - h)
+    return E, hi, lo
+
+
+def represented_activations(x) -> np.ndarray:
+    """2^E (hi + lo): the activations the FP8 GEMM multiplies."""
+    E, hi, lo = split_activations(x)
+    scale = np.repeat(2.0 ** E.astype(np.float64), BLOCK, axis=1)[:, :np.asarray(x).shape[1]]
+    return scale * (hi + lo)
+
+
+def gemm_split(x, q, scale) -> np.ndarray:
+    """x [R, K] @ W^T with x in its two-term e4m3 form and W dequantised."""
+    return represented_activations(x) @ dequantize(q, scale).T

@@ -1,7 +1,8 @@
 """Pins of the FP8 block-scaled weight oracle (oracle/fp8.py) against things
 other than itself: torch's float8_e4m3fn conversion, the E4M3 format's
-landmark values, the block structure of the scale grid, and a library-built
-expansion of the dequantised GEMM."""
+landmark values, the block structure of the scale grid, a library-built
+expansion of the dequantised GEMM, and the two-term activation split's
+exponent, exactness region and error bound."""
 import numpy as np
 import pytest
 import torch
@@ -102,3 +103,54 @@ def test_dequantised_product_is_exact():
     s = np.array([[np.float32(0.0123456789)]], dtype=np.float64)
     W = of.dequantize(q, s)
     assert np.array_equal(W / s[0, 0], of.decode(q))
+
+
+def test_rounding_matches_torch():
+    """RNE to E4M3 against torch's float8_e4m3fn conversion on values spread
+    over the whole range, and on every tie between neighbouring values."""
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal(200000) * np.exp(rng.uniform(-14, 6.1, 200000))
+    v = np.clip(v, -448.0, 448.0).astype(np.float32)
+    vals = np.array(sorted(set(of.decode(np.arange(0, 127, dtype=np.uint8)).tolist())))
+    ties = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)
+    for t in (v, ties, -ties):
+        ref = torch.from_numpy(t).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+        assert np.array_equal(of.e4m3_round(t.astype(np.float64)), ref)
+
+
+def test_split_exponent_is_minimal():
+    rng = np.random.default_rng(4)
+    for amax in np.concatenate([rng.uniform(1e-6, 1e4, 500), [448.0, 224.0, 448.0 * 2 ** -7, 1.0, 2.0 ** -30]]):
+        E = of.split_exponent(float(amax))
+        assert amax <= 448.0 * 2.0 ** E and amax > 448.0 * 2.0 ** (E - 1)
+    assert of.split_exponent(0.0) == 0
+
+
+def _bf16(a):
+    return torch.from_numpy(np.asarray(a, dtype=np.float32)).to(torch.bfloat16).double().numpy()
+
+
+def test_split_is_exact_within_its_range_and_bounded_below():
+    """x~ = x for every element of magnitude >= 2^(E-2); below that the
+    error is at most 2^(E-10); hi and lo are e4m3 values."""
+    rng = np.random.default_rng(5)
+    x = _bf16(rng.standard_normal((6, 300)) * np.exp(rng.uniform(-12, 4, (6, 300))))
+    E, hi, lo = of.split_activations(x)
+    xt = of.represented_activations(x)
+    s = np.repeat(2.0 ** E, 128, axis=1)[:, :300]
+    big = np.abs(x) >= s / 4
+    assert big.sum() > 100 and (~big).sum() > 100
+    assert np.array_equal(xt[big], x[big])
+    assert np.all(np.abs(xt - x) <= s * 2.0 ** -10)
+    assert np.array_equal(of.e4m3_round(hi), hi) and np.array_equal(of.e4m3_round(lo), lo)
+
+
+def test_split_of_e4m3_representable_values_has_no_low_term():
+    """An activation tile that is exactly 2^E times e4m3 values splits into
+    hi = those values and lo = 0."""
+    rng = np.random.default_rng(6)
+    codes = _codes(rng, (2, 128))
+    codes[:, 0] = 0x7E  # make 448 the tile maximum so E = 0 after scaling by 2^3
+    v = of.decode(codes) * 8.0
+    E, hi, lo = of.split_activations(v)
+    assert np.all(E == 3) and np.array_equal(hi * 8.0, v) and not lo.any()
