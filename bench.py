@@ -62,6 +62,8 @@ def parse_args():
     ap.add_argument("--train-steps", type=int, default=5, help="timed training steps (0 = off)")
     ap.add_argument("--c3-steps", type=int, default=4, help="timed calls of the DeepSeek-V3-width section (0 = off)")
     ap.add_argument("--draft-gamma", type=int, default=4, help="steps of the recurrent draft round (<= 1: off)")
+    ap.add_argument("--no-draft-fp8", dest="draft_fp8", action="store_false",
+                    help="skip the draft step with FP8 block-scaled module weights")
     ap.add_argument("--draft-requests", type=int, default=32,
                     help="requests of the draft-step section (32 = the measured workload; fewer for profiling)")
     return ap.parse_args()
@@ -533,6 +535,43 @@ def measure_draft(args, dev, rank, peaks):
            "achieved_gbs": gbs, "peak_gbs": hbm_peak, "frac": gbs / hbm_peak,
            "bound": "hbm", "steps": n, "l2": "flushed before every timed call (256 MiB written then read)"}
     del out, vout, step, vin
+
+    # the same step with the module's linear maps in FP8 block-scaled form
+    # (e4m3 codes + one fp32 scale per 128 x 128 block; head and cache bf16)
+    if args.draft_fp8:
+        f8 = synth.make_fp8_block(inp["weights"])
+        step8 = lib.DraftStep(cfg, inp["weights"], device=dev, fp8=f8)
+        out8 = {"q": torch.empty((cfg.R, cfg.V), dtype=torch.float32, device=dev),
+                "y": torch.empty(cfg.R, dtype=torch.int32, device=dev)}
+
+        def call8(i):
+            step8(inp["parent_hidden"], inp["frontier"], inp["pos"], inp["kv_k"], inp["kv_v"], inp["ctx_len"],
+                  seed=3, offset=i, out=out8)
+
+        for i in range(3):
+            call8(i)
+        torch.cuda.synchronize()
+        lib.check_errors()
+        e8 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            flush()
+            e8[i][0].record()
+            call8(300 + i)
+            e8[i][1].record()
+        torch.cuda.synchronize()
+        lib.check_errors()
+        f_ms = sorted(a.elapsed_time(b) for a, b in e8)[n // 2]
+        n_w = 2 * d * d + 4 * d * d + 3 * d * f
+        blocks = sum(((r + 127) // 128) * ((k + 127) // 128)
+                     for r, k in ((d, 2 * d), (d, d), (d, d), (d, d), (d, d), (f, d), (f, d), (d, f)))
+        f_bytes = 1.0 * n_w + 4.0 * blocks + head_bytes + cache_bytes + q_bytes
+        res["fp8"] = {"ms_median": f_ms, "algorithmic_bytes": f_bytes,
+                      "achieved_gbs": f_bytes / (f_ms / 1e3) / 1e9,
+                      "frac": f_bytes / (f_ms / 1e3) / 1e9 / hbm_peak,
+                      "speedup_vs_bf16_weights": d_ms / f_ms, "steps": n,
+                      "note": "module linear maps as e4m3 + fp32 128x128 block scales (1 B per weight); "
+                              "head, norms and cache bf16"}
+        del step8, out8, f8
 
     # recurrent round of gamma draft steps, then gamma-position verification of its draws
     g = args.draft_gamma

@@ -19,11 +19,16 @@
 // and write partial (max, sum, output) records per (request, head, key
 // split) that a combine kernel merges with the new row's key.  The head writes logits into q_out, which a per-request
 // kernel turns into probabilities in place and samples from.
+// With the module's linear maps in FP8 block-scaled form (mtp_draft_round_fp8)
+// the same products run on the FP8 weight GEMM of fp8.cu, which streams half
+// the bytes; the head stays bf16.
 #include <cooperative_groups.h>
 
 #include <algorithm>
 #include <cmath>
+#include <initializer_list>
 
+#include "fp8.cuh"
 #include "gemm_tc.cuh"
 #include "mbarrier.cuh"
 
@@ -812,7 +817,7 @@ inline size_t align_up(size_t v) { return (v + 255) & ~static_cast<size_t>(255);
 constexpr int kMaxRoundGamma = 31;  // draft steps per round (spec_verify takes gamma <= 31)
 
 struct DraftLayout {
-  size_t c, acc, u, x, qkv, o, a, g, h, part, stage_k, stage_v, total;
+  size_t c, acc, u, x, qkv, o, a, g, h, part, stage_k, stage_v, f8ws, f8ws_bytes, total;
   int n_chunks;
 };
 
@@ -841,6 +846,9 @@ DraftLayout draft_layout(const mtp_dims& D, int gamma) {
   L.part = take(R * static_cast<size_t>(D.n_heads) * L.n_chunks * (D.head_dim + 2) * 4);
   L.stage_k = take(R * static_cast<size_t>(gamma) * d * 2);
   L.stage_v = take(R * static_cast<size_t>(gamma) * d * 2);
+  // the FP8 linear maps' split activations (largest reduction length: 2d or ffn)
+  L.f8ws_bytes = mtp::fp8w_workspace_bytes(std::max(2 * D.d, D.ffn));
+  L.f8ws = take(L.f8ws_bytes);
   L.total = off;
   return L;
 }
@@ -904,7 +912,8 @@ namespace {
 // and the frontier token (stride f_stride), writes the step's state h_s (row
 // stride ld_h), logits/q into q_s (row stride ldq), the draw into y_s (stride
 // y_stride) and the step's key/value into staging slot s.
-mtp_status draft_one_step(const mtp_dims& D, const mtp_weights* w, const DraftLayout& L, uint8_t* base,
+mtp_status draft_one_step(const mtp_dims& D, const mtp_weights* w, const mtp_block_fp8* f8, const DraftLayout& L,
+                          uint8_t* base,
                           const __nv_bfloat16* parent, int ld_parent, const int32_t* frontier, int f_stride,
                           const int32_t* pos, const void* kv_k, const void* kv_v, const int32_t* ctx_len, int step,
                           int gamma, uint2 key, uint64_t offset, float* q_s, size_t ldq, int32_t* y_s, int y_stride,
@@ -916,20 +925,46 @@ mtp_status draft_one_step(const mtp_dims& D, const mtp_weights* w, const DraftLa
   const __nv_bfloat16* E = static_cast<const __nv_bfloat16*>(w->embed);
   __nv_bfloat16 *c = bfp(L.c), *u = bfp(L.u), *x = bfp(L.x), *qkv = bfp(L.qkv), *o = bfp(L.o), *a = bfp(L.a),
                 *g = bfp(L.g), *sk = bfp(L.stage_k), *sv = bfp(L.stage_v);
+  // acc[:, col + (0..n)] += xin · W^T for one to three linear maps of the
+  // block that share their input: bf16 weights on the swap-AB tcgen05 core,
+  // FP8 block-scaled ones in one grouped launch of the FP8 weight GEMM
+  struct Map {
+    const void* const* bf;
+    const mtp_fp8_matrix* q8;
+    int n, col;
+  };
+  auto linear = [&](std::initializer_list<Map> maps, int K, const __nv_bfloat16* xin, int ldo) -> mtp_status {
+    if (f8) {
+      mtp::Fp8Seg segs[3];
+      int i = 0;
+      for (const Map& m : maps) {
+        segs[i].q = static_cast<const uint8_t*>(m.q8->q);
+        segs[i].scale = m.q8->scale;
+        segs[i].n = m.n;
+        segs[i].out = acc + m.col;
+        ++i;
+      }
+      return mtp::fp8w_gemm_launch(segs, i, K, xin, R, ldo, base + L.f8ws, L.f8ws_bytes, st);
+    }
+    for (const Map& m : maps) TRY(skinny_gemm(W0(m.bf), m.n, K, xin, R, acc + m.col, ldo, st));
+    return MTP_OK;
+  };
+  auto q8 = [&](const mtp_fp8_matrix mtp_block_fp8::*field) { return f8 ? &(f8->*field) : nullptr; };
 
   // c, u = M c, x = RMSNorm_a(u)
   draft_prologue_kernel<<<R, kRowThreads, 0, st>>>(parent, ld_parent, frontier, f_stride, E, W0(w->hnorm),
                                                    W0(w->enorm), c, d, V, D.eps);
   mtp::note_launch();
   MTP_CUDA_TRY(cudaMemsetAsync(acc, 0, static_cast<size_t>(R) * d * 4, st));
-  TRY(skinny_gemm(W0(w->eh_proj), d, 2 * d, c, R, acc, d, st));
+  TRY(linear({{w->eh_proj, q8(&mtp_block_fp8::eh_proj), d, 0}}, 2 * d, c, d));
   finish_row_kernel<<<R, kRowThreads, 0, st>>>(acc, nullptr, u, d, W0(w->attn_norm), x, d, D.eps);
   mtp::note_launch();
   // q, k, v with RoPE on q, k at pos + step; the row's k, v staged in slot `step`
   MTP_CUDA_TRY(cudaMemsetAsync(acc, 0, static_cast<size_t>(R) * 3 * d * 4, st));
-  TRY(skinny_gemm(W0(w->wq), d, d, x, R, acc, 3 * d, st));
-  TRY(skinny_gemm(W0(w->wk), d, d, x, R, acc + d, 3 * d, st));
-  TRY(skinny_gemm(W0(w->wv), d, d, x, R, acc + 2 * d, 3 * d, st));
+  TRY(linear({{w->wq, q8(&mtp_block_fp8::wq), d, 0},
+              {w->wk, q8(&mtp_block_fp8::wk), d, d},
+              {w->wv, q8(&mtp_block_fp8::wv), d, 2 * d}},
+             d, x, 3 * d));
   finish_qkv_kernel<<<dim3((d + kQkvCols - 1) / kQkvCols, R), 256, 0, st>>>(acc, qkv, pos, step, d, hd, D.rope_base,
                                                                             D.T, sk, sv, gamma);
   mtp::note_launch();
@@ -978,18 +1013,18 @@ mtp_status draft_one_step(const mtp_dims& D, const mtp_weights* w, const DraftLa
   mtp::prof_end(MTP_KC_ATTENTION, st);
   // a = u + o Wo^T, x = RMSNorm_f(a)
   MTP_CUDA_TRY(cudaMemsetAsync(acc, 0, static_cast<size_t>(R) * d * 4, st));
-  TRY(skinny_gemm(W0(w->wo), d, d, o, R, acc, d, st));
+  TRY(linear({{w->wo, q8(&mtp_block_fp8::wo), d, 0}}, d, o, d));
   finish_row_kernel<<<R, kRowThreads, 0, st>>>(acc, u, a, d, W0(w->ffn_norm), x, d, D.eps);
   mtp::note_launch();
   // g = silu(x Wg^T) * (x Wu^T)
   MTP_CUDA_TRY(cudaMemsetAsync(acc, 0, static_cast<size_t>(R) * 2 * ffn * 4, st));
-  TRY(skinny_gemm(W0(w->w_gate), ffn, d, x, R, acc, 2 * ffn, st));
-  TRY(skinny_gemm(W0(w->w_up), ffn, d, x, R, acc + ffn, 2 * ffn, st));
+  TRY(linear({{w->w_gate, q8(&mtp_block_fp8::w_gate), ffn, 0}, {w->w_up, q8(&mtp_block_fp8::w_up), ffn, ffn}}, d, x,
+             2 * ffn));
   finish_swiglu_kernel<<<dim3((ffn + 255) / 256, R), 256, 0, st>>>(acc, g, ffn);
   mtp::note_launch();
   // h = a + g Wd^T, x = RMSNorm_out(h)
   MTP_CUDA_TRY(cudaMemsetAsync(acc, 0, static_cast<size_t>(R) * d * 4, st));
-  TRY(skinny_gemm(W0(w->w_down), d, ffn, g, R, acc, d, st));
+  TRY(linear({{w->w_down, q8(&mtp_block_fp8::w_down), d, 0}}, ffn, g, d));
   finish_row_kernel<<<R, kRowThreads, 0, st>>>(acc, a, h_s, ld_h, static_cast<const __nv_bfloat16*>(w->out_norm),
                                                x, d, D.eps);
   mtp::note_launch();
@@ -1015,11 +1050,12 @@ extern "C" size_t mtp_draft_round_workspace_bytes(const mtp_dims* dims, int gamm
 
 extern "C" size_t mtp_draft_workspace_bytes(const mtp_dims* dims) { return mtp_draft_round_workspace_bytes(dims, 1); }
 
-extern "C" mtp_status mtp_draft_round(const mtp_dims* dims, const mtp_weights* w, const void* parent_hidden,
-                                      const int32_t* frontier, const int32_t* pos, const void* kv_k,
-                                      const void* kv_v, const int32_t* ctx_len, int gamma, uint64_t seed,
-                                      uint64_t offset, float* q_out, int32_t* y_out, void* h_out, void* ws,
-                                      size_t ws_bytes, cudaStream_t st) {
+namespace {
+
+mtp_status draft_round_impl(const mtp_dims* dims, const mtp_weights* w, const mtp_block_fp8* f8,
+                            const void* parent_hidden, const int32_t* frontier, const int32_t* pos, const void* kv_k,
+                            const void* kv_v, const int32_t* ctx_len, int gamma, uint64_t seed, uint64_t offset,
+                            float* q_out, int32_t* y_out, void* h_out, void* ws, size_t ws_bytes, cudaStream_t st) {
   if (!dims || !w) return MTP_ERR_INVALID_ARG;
   const mtp_dims& D = *dims;
   if (!draft_dims_ok(D)) return D.dtype != MTP_BF16 || D.D != 1 || D.B > kMaxR ? MTP_ERR_UNSUPPORTED : MTP_ERR_SHAPE;
@@ -1028,10 +1064,22 @@ extern "C" mtp_status mtp_draft_round(const mtp_dims* dims, const mtp_weights* w
   if (!parent_hidden || !frontier || !pos || !kv_k || !kv_v || !ctx_len || !q_out || !y_out || !ws)
     return MTP_ERR_INVALID_ARG;
   if (!w->embed || !w->head || !w->out_norm) return MTP_ERR_INVALID_ARG;
-  const void* const* lists[] = {w->hnorm, w->enorm, w->eh_proj, w->attn_norm, w->wq, w->wk, w->wv,
-                                w->wo, w->ffn_norm, w->w_gate, w->w_up, w->w_down};
-  for (auto l : lists)
+  const void* const* norms[] = {w->hnorm, w->enorm, w->attn_norm, w->ffn_norm};
+  for (auto l : norms)
     if (!l || !l[0] || !mtp::aligned16(l[0])) return l && l[0] ? MTP_ERR_ALIGNMENT : MTP_ERR_INVALID_ARG;
+  if (f8) {
+    if (D.ffn % 16) return MTP_ERR_UNSUPPORTED;  // 16-byte rows of the e4m3 down projection
+    const mtp_fp8_matrix* mats[] = {&f8->eh_proj, &f8->wq, &f8->wk, &f8->wv, &f8->wo,
+                                    &f8->w_gate, &f8->w_up, &f8->w_down};
+    for (auto m : mats) {
+      if (!m->q || !m->scale) return MTP_ERR_INVALID_ARG;
+      if (!mtp::aligned16(m->q) || (reinterpret_cast<uintptr_t>(m->scale) & 3u)) return MTP_ERR_ALIGNMENT;
+    }
+  } else {
+    const void* const* lists[] = {w->eh_proj, w->wq, w->wk, w->wv, w->wo, w->w_gate, w->w_up, w->w_down};
+    for (auto l : lists)
+      if (!l || !l[0] || !mtp::aligned16(l[0])) return l && l[0] ? MTP_ERR_ALIGNMENT : MTP_ERR_INVALID_ARG;
+  }
   const void* ptrs[] = {parent_hidden, kv_k, kv_v, static_cast<const void*>(q_out), ws, w->embed, w->head,
                         w->out_norm};
   for (const void* p : ptrs)
@@ -1061,10 +1109,31 @@ extern "C" mtp_status mtp_draft_round(const mtp_dims* dims, const mtp_weights* w
       f = y_out + (s - 1);
       f_stride = gamma;
     }
-    TRY(draft_one_step(D, w, L, base, parent, ld_parent, f, f_stride, pos, kv_k, kv_v, ctx_len, s, gamma, key,
+    TRY(draft_one_step(D, w, f8, L, base, parent, ld_parent, f, f_stride, pos, kv_k, kv_v, ctx_len, s, gamma, key,
                        offset, q_out + static_cast<size_t>(s) * D.V, ldq, y_out + s, gamma, h_s, ld_h, st));
   }
   return MTP_OK;
+}
+
+}  // namespace
+
+extern "C" mtp_status mtp_draft_round(const mtp_dims* dims, const mtp_weights* w, const void* parent_hidden,
+                                      const int32_t* frontier, const int32_t* pos, const void* kv_k,
+                                      const void* kv_v, const int32_t* ctx_len, int gamma, uint64_t seed,
+                                      uint64_t offset, float* q_out, int32_t* y_out, void* h_out, void* ws,
+                                      size_t ws_bytes, cudaStream_t st) {
+  return draft_round_impl(dims, w, nullptr, parent_hidden, frontier, pos, kv_k, kv_v, ctx_len, gamma, seed, offset,
+                          q_out, y_out, h_out, ws, ws_bytes, st);
+}
+
+extern "C" mtp_status mtp_draft_round_fp8(const mtp_dims* dims, const mtp_weights* w, const mtp_block_fp8* f8,
+                                          const void* parent_hidden, const int32_t* frontier, const int32_t* pos,
+                                          const void* kv_k, const void* kv_v, const int32_t* ctx_len, int gamma,
+                                          uint64_t seed, uint64_t offset, float* q_out, int32_t* y_out, void* h_out,
+                                          void* ws, size_t ws_bytes, cudaStream_t st) {
+  if (!f8) return MTP_ERR_INVALID_ARG;
+  return draft_round_impl(dims, w, f8, parent_hidden, frontier, pos, kv_k, kv_v, ctx_len, gamma, seed, offset, q_out,
+                          y_out, h_out, ws, ws_bytes, st);
 }
 
 extern "C" mtp_status mtp_draft_step(const mtp_dims* dims, const mtp_weights* w, const void* parent_hidden,

@@ -80,4 +80,10 @@ mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream);
 bool tensor_map_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
                         uint32_t box_cols, uint32_t box_rows, bool swizzle128);
 
+// Tensor map of a row-major byte matrix [rows, cols] (row stride ld bytes, a
+// multiple of 16) for tiled loads of box_cols x box_rows with the 128-byte
+// swizzle (box_cols <= 128).
+bool tensor_map_u8_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_cols,
+                      uint32_t box_rows);
+
 }  // namespace mtp

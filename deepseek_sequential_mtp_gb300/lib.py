@@ -48,6 +48,17 @@ class Grads(ctypes.Structure):
                 ("h0", ctypes.c_void_p)] + [(k, _PP) for k in _WEIGHT_LISTS]
 
 
+FP8_LINEAR_MAPS = ("eh_proj", "wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+
+
+class Fp8Matrix(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
+
+
+class BlockFp8(ctypes.Structure):
+    _fields_ = [(k, Fp8Matrix) for k in FP8_LINEAR_MAPS]
+
+
 _lib = None
 
 
@@ -95,6 +106,14 @@ def load() -> ctypes.CDLL:
     lib.mtp_draft_step.restype = i32
     lib.mtp_draft_step.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Weights), vp, vp, vp, vp, vp, vp,
                                    u64, u64, vp, vp, vp, vp, sz, vp]
+    lib.mtp_draft_round_fp8.restype = i32
+    lib.mtp_draft_round_fp8.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Weights), ctypes.POINTER(BlockFp8),
+                                        vp, vp, vp, vp, vp, vp, i32, ctypes.c_uint64, ctypes.c_uint64, vp, vp, vp,
+                                        vp, sz, vp]
+    lib.mtp_gemm_fp8w_workspace_bytes.restype = sz
+    lib.mtp_gemm_fp8w_workspace_bytes.argtypes = [i32]
+    lib.mtp_gemm_fp8w.restype = i32
+    lib.mtp_gemm_fp8w.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
     lib.mtp_chain_grad_workspace_bytes.restype = sz
     lib.mtp_chain_grad_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
     lib.mtp_chain_loss_grad.restype = i32
@@ -210,6 +229,43 @@ class ChainWeights:
             arr = (ctypes.c_void_p * D)(*[t.data_ptr() for t in lst])
             self._keep.append(arr)
             setattr(self.struct, k, ctypes.cast(arr, _PP))
+
+
+class Fp8Block:
+    """ctypes view of the FP8 linear maps of one module: fp8[name] = (q, scale)
+    with q uint8 [n, K] e4m3 codes and scale float32 [ceil(n/128), ceil(K/128)]."""
+
+    def __init__(self, fp8: dict):
+        self.fp8 = fp8
+        self.struct = BlockFp8()
+        for name in FP8_LINEAR_MAPS:
+            q, sc = fp8[name]
+            _need(q, name + ".q", torch.uint8)
+            _need(sc, name + ".scale", torch.float32)
+            nb, kb = -(-q.shape[0] // 128), -(-q.shape[1] // 128)
+            if tuple(sc.shape) != (nb, kb):
+                raise MtpError(f"{name}.scale must be [{nb}, {kb}]")
+            m = getattr(self.struct, name)
+            m.q = q.data_ptr()
+            m.scale = sc.data_ptr()
+
+
+def gemm_fp8w(x: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, out: torch.Tensor, stream=None, ws=None):
+    """out[R, N] += x~[R, K] @ W^T, W = e4m3(q) * block scales, x~ the two-term
+    e4m3 form of x (mtp_gemm_fp8w)."""
+    _need(x, "x", torch.bfloat16)
+    _need(q, "q", torch.uint8)
+    _need(scale, "scale", torch.float32)
+    _need(out, "out", torch.float32)
+    R, K = x.shape
+    N = q.shape[0]
+    if q.shape[1] != K or tuple(out.shape) != (R, N):
+        raise MtpError("gemm_fp8w: x [R, K], q [N, K], out [R, N]")
+    if ws is None:
+        ws = torch.empty(max(16, int(load().mtp_gemm_fp8w_workspace_bytes(K))), dtype=torch.uint8, device=x.device)
+    _check(load().mtp_gemm_fp8w(R, N, K, _ptr(x), _ptr(q), _ptr(scale), _ptr(out), _ptr(ws), ws.numel(),
+                                _stream(stream)), "mtp_gemm_fp8w")
+    return out
 
 
 def _check_chain_inputs(cfg, tokens, seg, pos, h0, weights):
@@ -381,12 +437,13 @@ def kernel_launches() -> int:
 class DraftStep:
     """Reusable call state of mtp_draft_step for one shape (see synth.DraftConfig)."""
 
-    def __init__(self, cfg, weights: dict, device="cuda"):
+    def __init__(self, cfg, weights: dict, device="cuda", fp8: Optional[dict] = None):
         self.cfg = cfg
         self.dims = Dims(cfg.R, cfg.ctx, cfg.d, cfg.n_heads, cfg.head_dim, cfg.ffn, cfg.V, 1, cfg.eps,
                          cfg.rope_base, MTP_BF16)
         self.weights = weights
         self.w = ChainWeights(weights, 1)
+        self.f8 = Fp8Block(fp8) if fp8 is not None else None
         nbytes = int(load().mtp_draft_workspace_bytes(ctypes.byref(self.dims)))
         if nbytes == 0:
             raise MtpError("invalid draft-step dimensions")
@@ -406,11 +463,21 @@ class DraftStep:
         if out is None:
             out = {"q": torch.empty((cfg.R, cfg.V), dtype=torch.float32, device=dev),
                    "y": torch.empty(cfg.R, dtype=torch.int32, device=dev)}
-        st = load().mtp_draft_step(ctypes.byref(self.dims), ctypes.byref(self.w.struct), _ptr(parent_hidden),
-                                   _ptr(frontier), _ptr(pos), _ptr(kv_k), _ptr(kv_v), _ptr(ctx_len),
-                                   int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(out["q"]),
-                                   _ptr(out["y"]), _ptr(h_out), _ptr(self.ws), self.ws.numel(), _stream(stream))
-        _check(st, "mtp_draft_step")
+        if self.f8 is not None:  # one step of the FP8 round
+            st = load().mtp_draft_round_fp8(ctypes.byref(self.dims), ctypes.byref(self.w.struct),
+                                            ctypes.byref(self.f8.struct), _ptr(parent_hidden), _ptr(frontier),
+                                            _ptr(pos), _ptr(kv_k), _ptr(kv_v), _ptr(ctx_len), 1,
+                                            int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(out["q"]),
+                                            _ptr(out["y"]), _ptr(h_out), _ptr(self.ws), self.ws.numel(),
+                                            _stream(stream))
+            _check(st, "mtp_draft_round_fp8")
+        else:
+            st = load().mtp_draft_step(ctypes.byref(self.dims), ctypes.byref(self.w.struct), _ptr(parent_hidden),
+                                       _ptr(frontier), _ptr(pos), _ptr(kv_k), _ptr(kv_v), _ptr(ctx_len),
+                                       int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(out["q"]),
+                                       _ptr(out["y"]), _ptr(h_out), _ptr(self.ws), self.ws.numel(),
+                                       _stream(stream))
+            _check(st, "mtp_draft_step")
         if h_out is not None:
             out["h"] = h_out
         return out
@@ -420,13 +487,14 @@ class DraftRound:
     """Reusable call state of mtp_draft_round: gamma recurrent draft steps of
     one module for one shape (see synth.DraftConfig)."""
 
-    def __init__(self, cfg, weights: dict, gamma: int, device="cuda"):
+    def __init__(self, cfg, weights: dict, gamma: int, device="cuda", fp8: Optional[dict] = None):
         self.cfg = cfg
         self.gamma = int(gamma)
         self.dims = Dims(cfg.R, cfg.ctx, cfg.d, cfg.n_heads, cfg.head_dim, cfg.ffn, cfg.V, 1, cfg.eps,
                          cfg.rope_base, MTP_BF16)
         self.weights = weights
         self.w = ChainWeights(weights, 1)
+        self.f8 = Fp8Block(fp8) if fp8 is not None else None
         nbytes = int(load().mtp_draft_round_workspace_bytes(ctypes.byref(self.dims), self.gamma))
         if nbytes == 0:
             raise MtpError("invalid draft-round dimensions or gamma")
@@ -450,11 +518,21 @@ class DraftRound:
         if out is None:
             out = {"q": torch.empty((cfg.R, g, cfg.V), dtype=torch.float32, device=dev),
                    "y": torch.empty((cfg.R, g), dtype=torch.int32, device=dev)}
-        st = load().mtp_draft_round(ctypes.byref(self.dims), ctypes.byref(self.w.struct), _ptr(parent_hidden),
-                                    _ptr(frontier), _ptr(pos), _ptr(kv_k), _ptr(kv_v), _ptr(ctx_len), g,
-                                    int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(out["q"]),
-                                    _ptr(out["y"]), _ptr(h_out), _ptr(self.ws), self.ws.numel(), _stream(stream))
-        _check(st, "mtp_draft_round")
+        if self.f8 is not None:
+            st = load().mtp_draft_round_fp8(ctypes.byref(self.dims), ctypes.byref(self.w.struct),
+                                            ctypes.byref(self.f8.struct), _ptr(parent_hidden), _ptr(frontier),
+                                            _ptr(pos), _ptr(kv_k), _ptr(kv_v), _ptr(ctx_len), g,
+                                            int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(out["q"]),
+                                            _ptr(out["y"]), _ptr(h_out), _ptr(self.ws), self.ws.numel(),
+                                            _stream(stream))
+            _check(st, "mtp_draft_round_fp8")
+        else:
+            st = load().mtp_draft_round(ctypes.byref(self.dims), ctypes.byref(self.w.struct), _ptr(parent_hidden),
+                                        _ptr(frontier), _ptr(pos), _ptr(kv_k), _ptr(kv_v), _ptr(ctx_len), g,
+                                        int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(out["q"]),
+                                        _ptr(out["y"]), _ptr(h_out), _ptr(self.ws), self.ws.numel(),
+                                        _stream(stream))
+            _check(st, "mtp_draft_round")
         if h_out is not None:
             out["h"] = h_out
         return out

@@ -353,6 +353,32 @@ def make_small_verify_case(seed: int, R: int, gamma: int, V: int, device="cpu",
 # --------------------------------------------------------------------------
 # Draft-step inputs (decode-shaped)
 # --------------------------------------------------------------------------
+FP8_LINEAR_MAPS = ("eh_proj", "wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+
+
+def quantize_fp8_blocks(w: torch.Tensor):
+    """Synthetic FP8 checkpoint form of one [n, K] weight matrix, the format
+    DeepSeek-V3 releases: per 128 x 128 block a float32 scale = max|w| / 448
+    and the E4M3 codes of w / scale (torch's float8_e4m3fn conversion).
+    Returns (q uint8 [n, K], scale float32 [ceil(n/128), ceil(K/128)]) on w's
+    device.  Input generation only: the hot path reads q and scale as given."""
+    w32 = w.float()
+    n, k = w32.shape
+    nb, kb = -(-n // 128), -(-k // 128)
+    pad = torch.zeros((nb * 128, kb * 128), dtype=torch.float32, device=w.device)
+    pad[:n, :k] = w32.abs()
+    amax = pad.view(nb, 128, kb, 128).amax(dim=(1, 3))
+    scale = torch.clamp(amax, min=1e-30) / 448.0
+    expanded = scale.repeat_interleave(128, 0)[:n].repeat_interleave(128, 1)[:, :k]
+    q = torch.clamp(w32 / expanded, -448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    return q.contiguous(), scale.contiguous()
+
+
+def make_fp8_block(weights: dict) -> dict:
+    """FP8 forms of the depth-1 module's eight linear maps of a weight dict."""
+    return {name: quantize_fp8_blocks(weights[name][0]) for name in FP8_LINEAR_MAPS}
+
+
 def make_draft_inputs(cfg: DraftConfig, seed: int, device="cpu") -> dict:
     """parent_hidden [R, d], frontier tokens [R], position [R], the module's own
     K/V cache [R, ctx, d] (bf16, N(0,1)) with ctx_len [R], and depth-1 weights."""

@@ -94,7 +94,8 @@ enum {
   MTP_DEVERR_FROM_GEMM = 1u << 9,    /* tcgen05 GEMM core                        */
   MTP_DEVERR_FROM_ATTN = 1u << 10,   /* chain attention                           */
   MTP_DEVERR_FROM_VERIFY = 1u << 11, /* spec_verify                               */
-  MTP_DEVERR_FROM_DRAFT = 1u << 12   /* draft-step kernels                        */
+  MTP_DEVERR_FROM_DRAFT = 1u << 12,  /* draft-step kernels                        */
+  MTP_DEVERR_FROM_FP8 = 1u << 13     /* FP8 block-scaled weight GEMM              */
 };
 
 /* Problem sizes of one chain call.
@@ -338,6 +339,55 @@ mtp_status mtp_draft_round(const mtp_dims* dims, const mtp_weights* w, const voi
                            const int32_t* frontier, const int32_t* pos, const void* kv_k, const void* kv_v,
                            const int32_t* ctx_len, int gamma, uint64_t seed, uint64_t offset, float* q_out,
                            int32_t* y_out, void* h_out, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* One FP8 block-scaled weight matrix W [n, K] ([M7.6] §0x03C: released
+ * weights are FP8 with block scales; the runtime chooses the compute
+ * representation).  q: e4m3 codes (OCP FP8 E4M3: sign, 4 exponent bits with
+ * bias 7, 3 mantissa bits, subnormals, no infinities, 0x7F/0xFF = NaN),
+ * row-major with row stride K bytes, 16-byte aligned; scale: fp32
+ * [ceil(n/128), ceil(K/128)] row-major, one factor per 128 x 128 block.
+ * The represented weight is W[m][k] = e4m3(q[m][k]) * scale[m/128][k/128],
+ * used exactly.  The activations meet it on the tensor cores as e4m3 in two
+ * terms: per token and 128-wide k-tile, x~ = 2^E (hi + lo) with 2^E the
+ * smallest power of two such that max|x| <= 448 * 2^E, hi = RNE_e4m3(x/2^E),
+ * lo = RNE_e4m3(x/2^E - hi); x~ = x for every element of magnitude >=
+ * 2^(E-2) and |x~ - x| <= 2^(E-10) otherwise.  Products are summed in fp32,
+ * one fp32 partial per 128-wide k-block scaled by its block factors. */
+typedef struct mtp_fp8_matrix {
+  const void* q;
+  const float* scale;
+} mtp_fp8_matrix;
+
+/* The linear maps of one MTP module in FP8 (shapes as in mtp_weights:
+ * eh_proj [d, 2d], wq/wk/wv/wo [d, d], w_gate/w_up [ffn, d], w_down [d, ffn]). */
+typedef struct mtp_block_fp8 {
+  mtp_fp8_matrix eh_proj, wq, wk, wv, wo, w_gate, w_up, w_down;
+} mtp_block_fp8;
+
+/* mtp_draft_round with the module's linear maps in FP8 block-scaled form
+ * ([M7.6] §0x03C; it halves the decode step's weight bytes).
+ * w supplies the bf16 embedding, head and norm gains (its linear-map fields
+ * are not read and may be null: the output head and norms stay in bf16, as
+ * the pages keep them in higher precision); f8 the eight linear maps.
+ * Requires ffn % 16 == 0.  Everything else, including the outputs and the
+ * random stream, is as for mtp_draft_round. */
+mtp_status mtp_draft_round_fp8(const mtp_dims* dims, const mtp_weights* w, const mtp_block_fp8* f8,
+                               const void* parent_hidden, const int32_t* frontier, const int32_t* pos,
+                               const void* kv_k, const void* kv_v, const int32_t* ctx_len, int gamma,
+                               uint64_t seed, uint64_t offset, float* q_out, int32_t* y_out, void* h_out,
+                               void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Bytes of device workspace mtp_gemm_fp8w needs for reduction length K. */
+size_t mtp_gemm_fp8w_workspace_bytes(int K);
+
+/* Diagnostic FP8 weight GEMM (the kernel the FP8 draft step uses):
+ * out[R, N] (fp32, row stride N) += x~[R, K] · W^T with W the FP8
+ * block-scaled matrix (wq [N, K] e4m3, scale [ceil(N/128), ceil(K/128)]) and
+ * x~ the two-term e4m3 form of x (bf16) described at mtp_fp8_matrix.
+ * R in [1, 32], K % 16 == 0, x and wq 16-byte aligned; ws: at least
+ * mtp_gemm_fp8w_workspace_bytes(K) bytes of device memory, 16-byte aligned. */
+mtp_status mtp_gemm_fp8w(int R, int N, int K, const void* x, const void* wq, const float* scale, float* out,
+                         void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Diagnostic GEMM on the same tcgen05 core the chain uses:
  * C[M,N] (bf16) = A[M,K] (bf16) · B[N,K]^T (bf16), fp32 accumulation.

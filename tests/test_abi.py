@@ -90,3 +90,21 @@ def test_chain_host_validation(lib):
     st = lib.mtp_chain_forward(ctypes.byref(good), ctypes.byref(w), mis, fake, fake, fake, fake,
                                fake, 1 << 40, None)
     assert st == 3
+
+
+def test_fp8_host_validation(lib):
+    """FP8 entry points reject bad arguments on the host, before any launch."""
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.mtp_gemm_fp8w(4, 128, 128, None, fake, fake, fake, fake, 1 << 20, None) == 1
+    assert lib.mtp_gemm_fp8w(4, 128, 120, fake, fake, fake, fake, fake, 1 << 20, None) == 3   # K % 16 != 0
+    assert lib.mtp_gemm_fp8w(33, 128, 128, fake, fake, fake, fake, fake, 1 << 20, None) == 2  # > 32 tokens
+    assert lib.mtp_gemm_fp8w(4, 128, 128, fake, fake, fake, fake, fake, 16, None) == 4         # workspace
+    assert lib.mtp_gemm_fp8w_workspace_bytes(7168) >= 64 * 7168
+    from deepseek_sequential_mtp_gb300 import lib as binding, synth
+    cfg = synth.DRAFT_SMALL
+    dims = binding.Dims(cfg.R, cfg.ctx, cfg.d, cfg.n_heads, cfg.head_dim, cfg.ffn, cfg.V, 1, cfg.eps,
+                        cfg.rope_base, binding.MTP_BF16)
+    w = binding.Weights()
+    st = lib.mtp_draft_round_fp8(ctypes.byref(dims), ctypes.byref(w), None, fake, fake, fake, fake, fake, fake, 1,
+                                 0, 0, fake, fake, None, fake, 1 << 30, None)
+    assert st == 1

@@ -47,14 +47,14 @@ def run(cfg, inp, seed, offset, requests=None, W=None):
     return {k: _np(v) for k, v in g.items()}, r, requests
 
 
-def check(g, r, requests):
+def check(g, r, requests, qbar=2e-3):
     gh, gq, gy = g["h"][requests], g["q"][requests], g["y"][requests]
     err = np.abs(gh - r["h"])
     assert np.all(err <= 2e-2 + 2e-2 * np.abs(r["h"])), err.max()
     assert np.all(np.isfinite(gq)) and np.allclose(gq.sum(1), 1.0, atol=1e-4)
     tv = 0.5 * np.abs(gq - r["q"]).sum(1)
     assert tv.max() < 5e-3, tv
-    assert np.all(np.abs(gq - r["q"]).max(1) <= 2e-3 * r["q"].max(1))
+    assert np.all(np.abs(gq - r["q"]).max(1) <= qbar * r["q"].max(1))
     return gy
 
 
@@ -122,7 +122,7 @@ def _round_case(cfg, seed, ctx, gamma, dseed, offset):
     return g, r
 
 
-def _check_round(cfg, g, r, dseed, offset):
+def _check_round(cfg, g, r, dseed, offset, bar0=2e-3):
     """Per-step bars as for one draft step, except the per-entry q bar of
     steps >= 1: 5e-3 max(q).  The oracle continues from the GPU's state and
     draw, but its staged rows of earlier steps are its own (equal to the GPU's
@@ -135,7 +135,7 @@ def _check_round(cfg, g, r, dseed, offset):
         gq = g["q"][:, s]
         assert np.all(np.isfinite(gq)) and np.allclose(gq.sum(1), 1.0, atol=1e-4)
         assert (0.5 * np.abs(gq - r["q"][:, s]).sum(1)).max() < 5e-3, s
-        bar = 2e-3 if s == 0 else 5e-3
+        bar = bar0 if s == 0 else 5e-3
         assert np.all(np.abs(gq - r["q"][:, s]).max(1) <= bar * r["q"][:, s].max(1)), s
         for rid in range(cfg.R):
             y_own, m_own = ov.inverse_cdf(gq[rid].astype(np.float64), od.draft_uniform(dseed, offset, rid, s))
