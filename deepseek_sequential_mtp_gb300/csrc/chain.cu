@@ -914,60 +914,6 @@ __global__ void term_scale_kernel(const double* __restrict__ sc, float* __restri
   for (int k = 1; k <= D; ++k) scale[k] = static_cast<float>(weight(k) * term_inv(k));
 }
 
-// out[c][r] = in[r][c] for a bf16 [R, C] matrix.  64 x 64 tiles through
-// shared memory (rows padded by 4 bytes so that reading 8 rows of one column
-// hits distinct banks); with 16-byte-aligned rows (C, ldi, ldo multiples of 8)
-// rows are read and written 8 elements at a time, else element by element.
-constexpr int kTp = 64;
-__global__ void __launch_bounds__(256)
-transpose_bf16_kernel(const __nv_bfloat16* __restrict__ in, int R, int Cn, int ldi, __nv_bfloat16* __restrict__ out,
-                      int ldo, int vec) {
-  __shared__ __nv_bfloat16 tile[kTp][kTp + 2];
-  const int c0 = blockIdx.x * kTp, r0 = blockIdx.y * kTp;
-  const int t = threadIdx.x;
-  if (vec) {
-    // 64 rows x 8 pieces of 8 elements: 2 pieces per thread
-    for (int p = t; p < kTp * 8; p += 256) {
-      const int r = p >> 3, c = (p & 7) * 8;
-      uint4 u = make_uint4(0u, 0u, 0u, 0u);
-      if (r0 + r < R && c0 + c < Cn) u = *reinterpret_cast<const uint4*>(in + static_cast<size_t>(r0 + r) * ldi + c0 + c);
-      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&u);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) tile[r][c + i] = e[i];
-    }
-    __syncthreads();
-    for (int p = t; p < kTp * 8; p += 256) {
-      const int c = p >> 3, r = (p & 7) * 8;  // output row c (input column), 8 input rows
-      if (c0 + c >= Cn || r0 + r >= R) continue;
-      uint4 u;
-      __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(&u);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) e[i] = tile[r + i][c];
-      if (r0 + r + 8 <= R) {
-        *reinterpret_cast<uint4*>(out + static_cast<size_t>(c0 + c) * ldo + r0 + r) = u;
-      } else {
-        for (int i = 0; i < 8 && r0 + r + i < R; ++i) out[static_cast<size_t>(c0 + c) * ldo + r0 + r + i] = e[i];
-      }
-    }
-  } else {
-    for (int p = t; p < kTp * kTp; p += 256) {
-      const int r = p / kTp, c = p % kTp;
-      if (r0 + r < R && c0 + c < Cn) tile[r][c] = in[static_cast<size_t>(r0 + r) * ldi + c0 + c];
-    }
-    __syncthreads();
-    for (int p = t; p < kTp * kTp; p += 256) {
-      const int c = p / kTp, r = p % kTp;
-      if (c0 + c < Cn && r0 + r < R) out[static_cast<size_t>(c0 + c) * ldo + r0 + r] = tile[r][c];
-    }
-  }
-}
-
-void transpose_bf16(const __nv_bfloat16* in, int R, int Cn, int ldi, __nv_bfloat16* out, int ldo, cudaStream_t st) {
-  const int vec = (Cn % 8 == 0 && ldi % 8 == 0 && ldo % 8 == 0 && mtp::aligned16(in) && mtp::aligned16(out)) ? 1 : 0;
-  transpose_bf16_kernel<<<dim3((Cn + kTp - 1) / kTp, (R + kTp - 1) / kTp), 256, 0, st>>>(in, R, Cn, ldi, out, ldo,
-                                                                                      vec);
-  mtp::note_launch();
-}
 
 // RMSNorm backward for y = g * h * r, r = (mean(h^2) + eps)^(-1/2), given
 // dy: dh += r (g dy - xh * mean(g dy xh)) with xh = h r; dg += sum over rows
@@ -1045,14 +991,14 @@ __global__ void add_f32_kernel(float* __restrict__ a, const float* __restrict__ 
 inline int round_up8(int v) { return (v + 7) / 8 * 8; }
 
 struct TrainLayout {
-  size_t hs, lse, scale, wut, xt, dz, dzt, dx, dstate, save, total;
+  size_t hs, lse, scale, dz, dx, dstate, save, total;
   int vc, vp, mp;
 };
 
 SaveOff make_save_off(const mtp_dims& D);
 
 // after the forward's own workspace: the saved states h^1..h^D, the per-term
-// log-sum-exp, the per-term row scales, W_U^T, and the head-backward buffers
+// log-sum-exp, the per-term row scales and the head-backward buffers
 TrainLayout make_train_layout(const mtp_dims& D) {
   TrainLayout T{};
   const size_t M = static_cast<size_t>(D.B) * D.T, d = D.d;
@@ -1068,10 +1014,7 @@ TrainLayout make_train_layout(const mtp_dims& D) {
   T.hs = take(static_cast<size_t>(D.D) * M * d * 2);
   T.lse = take(static_cast<size_t>(D.D + 1) * M * 4);
   T.scale = take(static_cast<size_t>(D.D + 1) * 4);
-  T.wut = take(d * T.vp * 2);
-  T.xt = take(d * T.mp * 2);
   T.dz = take(M * T.vc * 2);
-  T.dzt = take(static_cast<size_t>(T.vc) * T.mp * 2);
   T.dx = take(M * d * 4);
   T.dstate = take(static_cast<size_t>(D.D + 1) * M * d * 4);
   T.save = take(static_cast<size_t>(D.D) * make_save_off(D).bytes);
@@ -1079,8 +1022,8 @@ TrainLayout make_train_layout(const mtp_dims& D) {
   return T;
 }
 
-mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, const __nv_bfloat16* B, int ldb, float* out,
-                    int ldo, cudaStream_t st);
+mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, bool a_mn, const __nv_bfloat16* B, int ldb,
+                    bool b_mn, float* out, int ldo, cudaStream_t st);
 
 mtp::GemmDesc gdesc(int M, int N, int K, const __nv_bfloat16* A, int lda, const __nv_bfloat16* B, int ldb) {
   mtp::GemmDesc g;
@@ -1111,15 +1054,11 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
   int32_t* labels = C.buf<int32_t>(C.L.labels);
   const bf* WU = static_cast<const bf*>(C.W.head);
   const bf* out_norm = static_cast<const bf*>(C.W.out_norm);
-  bf* xt = C.buf<bf>(T.xt);
   bf* dz = C.buf<bf>(T.dz);
-  bf* dzt = C.buf<bf>(T.dzt);
-  bf* wut = C.buf<bf>(T.wut);
   float* dx = C.buf<float>(T.dx);
   const float* lse = C.buf<float>(T.lse) + static_cast<size_t>(t) * M;
   const float* scale = C.buf<float>(T.scale) + t;
   launch_rmsnorm<bf>(C, h_t, out_norm, x, labels, t);
-  if (d_head) transpose_bf16(x, M, d, d, xt, T.mp, C.st);
   MTP_CUDA_TRY(cudaMemsetAsync(dx, 0, static_cast<size_t>(M) * d * 4, C.st));
   for (int v0 = 0; v0 < V; v0 += T.vc) {
     const int vc = std::min(T.vc, V - v0);
@@ -1132,10 +1071,11 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
     g.ce_scale = scale;
     g.ce_offset = v0;
     TRY(mtp::gemm_bf16_launch(g, C.st));
-    TRY(gemm_acc(M, d, vc, dz, T.vc, wut + v0, T.vp, dx, d, C.st));
+    // dX += dz W_U[v0 : v0 + vc] (W_U rows read as the MN-major B operand)
+    TRY(gemm_acc(M, d, vc, dz, T.vc, false, WU + static_cast<size_t>(v0) * d, d, true, dx, d, C.st));
     if (!d_head) continue;
-    transpose_bf16(dz, M, vc, T.vc, dzt, T.mp, C.st);  // dz^T for the head's weight gradient
-    TRY(gemm_acc(vc, d, M, dzt, T.mp, xt, T.mp, d_head + static_cast<size_t>(v0) * d, d, C.st));
+    // dW_U[v0 : v0 + vc] += dz^T X (both operands read MN-major)
+    TRY(gemm_acc(vc, d, M, dz, T.vc, true, x, d, true, d_head + static_cast<size_t>(v0) * d, d, C.st));
   }
   float* dstate_t = C.buf<float>(T.dstate) + static_cast<size_t>(t) * M * d;
   rmsnorm_bwd(h_t, d, nullptr, out_norm, dx, d, dstate_t, d, nullptr, d_out_norm, M, d, D.eps, C.st);
@@ -1220,13 +1160,12 @@ __global__ void shifted_tokens_kernel(const int32_t* __restrict__ tokens, int32_
 
 // scratch of the block backward (reused depth after depth)
 struct BwdLayout {
-  size_t dhb, dhT, pq, gb, gT, dgf, dpq, dpqT, yT, dyf, daf, dab, daT, oT, dof, dob, dqkvf, dqkvb, dqkvT, xT, dxf,
-      duf, dub, duT, cT, dcf, adsum, tok, wdT, wgT, woT, wqkvT, mT, total;
+  size_t dhb, pq, gb, dgf, dpq, dyf, daf, dab, dof, dob, dqkvf, dqkvb, dxf, duf, dub, dcf, adsum, tok, total;
 };
 
 BwdLayout make_bwd_layout(const mtp_dims& D, size_t start, int mp) {
   BwdLayout B{};
-  const size_t M = static_cast<size_t>(D.B) * D.T, d = D.d, f = D.ffn, Mp = mp;
+  const size_t M = static_cast<size_t>(D.B) * D.T, d = D.d, f = D.ffn;
   size_t off = start;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -1234,38 +1173,23 @@ BwdLayout make_bwd_layout(const mtp_dims& D, size_t start, int mp) {
     return o;
   };
   B.dhb = take(M * d * 2);
-  B.dhT = take(d * Mp * 2);
   B.pq = take(M * 2 * f * 2);
   B.gb = take(M * f * 2);
-  B.gT = take(f * Mp * 2);
   B.dgf = take(M * f * 4);
   B.dpq = take(M * 2 * f * 2);
-  B.dpqT = take(2 * f * Mp * 2);
-  B.yT = take(d * Mp * 2);
   B.dyf = take(M * d * 4);
   B.daf = take(M * d * 4);
   B.dab = take(M * d * 2);
-  B.daT = take(d * Mp * 2);
-  B.oT = take(d * Mp * 2);
   B.dof = take(M * d * 4);
   B.dob = take(M * d * 2);
   B.dqkvf = take(M * 3 * d * 4);
   B.dqkvb = take(M * 3 * d * 2);
-  B.dqkvT = take(3 * d * Mp * 2);
-  B.xT = take(d * Mp * 2);
   B.dxf = take(M * d * 4);
   B.duf = take(M * d * 4);
   B.dub = take(M * d * 2);
-  B.duT = take(d * Mp * 2);
-  B.cT = take(2 * d * Mp * 2);
   B.dcf = take(M * 2 * d * 4);
   B.adsum = take(M * D.n_heads * 4);
   B.tok = take(M * 4);
-  B.wdT = take(f * d * 2);
-  B.wgT = take(d * 2 * f * 2);
-  B.woT = take(d * d * 2);
-  B.wqkvT = take(d * 3 * d * 2);
-  B.mT = take(2 * d * d * 2);
   B.total = off;
   return B;
 }
@@ -1291,12 +1215,14 @@ SaveOff make_save_off(const mtp_dims& D) {
   return S;
 }
 
-// C += A B^T into fp32.  K is split (partial tiles added with vector atomics)
+// C += A B^T into fp32; A is [M, K] (a_mn: stored [K, M]) and B is [N, K]
+// (b_mn: stored [K, N]), so transposes of row-major operands are read in
+// place.  K is split (partial tiles added with vector atomics)
 // when that fills the SMs' waves better: the smallest split whose work units
 // fill at least 90% of their last wave, else the best one (at most 16, and
 // at least 8 k-blocks per split).
-mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, const __nv_bfloat16* B, int ldb, float* out,
-                    int ldo, cudaStream_t st) {
+mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, bool a_mn, const __nv_bfloat16* B, int ldb,
+                    bool b_mn, float* out, int ldo, cudaStream_t st) {
   static int sms = 0;
   if (sms == 0) {
     int dev = 0;
@@ -1306,6 +1232,8 @@ mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, const 
   }
   mtp::GemmDesc g = gdesc(M, N, K, A, lda, B, ldb);
   g.epi = mtp::EPI_F32_ACC;
+  g.a_mn = a_mn;
+  g.b_mn = b_mn;
   g.out_f32 = out;
   g.ldo = ldo;
   const int tiles = ((M + 127) / 128) * ((N + 255) / 256);
@@ -1333,7 +1261,7 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
                           const mtp_grads* G) {
   using bf = __nv_bfloat16;
   const mtp_dims& D = C.D;
-  const int M = C.M, d = D.d, f = D.ffn, H = D.n_heads, hd = D.head_dim, Mp = T.mp, i = k - 1;
+  const int M = C.M, d = D.d, f = D.ffn, H = D.n_heads, hd = D.head_dim, i = k - 1;
   const size_t Md = static_cast<size_t>(M) * d;
   cudaStream_t st = C.st;
   auto wt = [&](const void* const* arr) { return static_cast<const bf*>(arr[i]); };
@@ -1347,19 +1275,12 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
            *y = reinterpret_cast<const bf*>(sv + C.so.y);
   const float* dh = fb(T.dstate) + static_cast<size_t>(k) * Md;
   float* dh_prev = fb(T.dstate) + static_cast<size_t>(k - 1) * Md;
-  // weights of the depth, transposed for the input-gradient GEMMs
-  transpose_bf16(wt(C.W.w_down), d, f, f, bb(B.wdT), d, st);
-  transpose_bf16(wt(C.W.w_gate), f, d, d, bb(B.wgT), 2 * f, st);      // [Wg^T | Wu^T]: [d, 2 ffn]
-  transpose_bf16(wt(C.W.w_up), f, d, d, bb(B.wgT) + f, 2 * f, st);
-  transpose_bf16(wt(C.W.wo), d, d, d, bb(B.woT), d, st);
-  transpose_bf16(wt(C.W.wq), d, d, d, bb(B.wqkvT), 3 * d, st);
-  transpose_bf16(wt(C.W.wk), d, d, d, bb(B.wqkvT) + d, 3 * d, st);
-  transpose_bf16(wt(C.W.wv), d, d, d, bb(B.wqkvT) + 2 * d, 3 * d, st);
-  transpose_bf16(wt(C.W.eh_proj), d, 2 * d, 2 * d, bb(B.mT), d, st);
+  // Input gradients dX = dY W read the row-major weights W [out, in] as the
+  // MN-major B operand; weight gradients dW = dY^T X read both activations
+  // as MN-major operands.  Nothing is transposed in memory.
 
   // h = a + g W_d^T: dW_d += dh^T g; dg = dh W_d; da = dh (+ the FFN path below)
   f32_to_bf16(dh, d, bb(B.dhb), d, M, d, st);
-  transpose_bf16(bb(B.dhb), M, d, d, bb(B.dhT), Mp, st);
   {  // recompute the gate and up pre-activations p = y Wg^T, q = y Wu^T into pq = [p | q]
     mtp::GemmDesc g = gdesc(M, f, d, y, d, wt(C.W.w_gate), d);
     g.epi = mtp::EPI_STORE;
@@ -1373,33 +1294,24 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
     TRY(mtp::gemm_bf16_launch(g, st));
   }
   MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dgf), 0, static_cast<size_t>(M) * f * 4, st));
-  TRY(gemm_acc(M, f, d, bb(B.dhb), d, bb(B.wdT), d, fb(B.dgf), f, st));
+  TRY(gemm_acc(M, f, d, bb(B.dhb), d, false, wt(C.W.w_down), f, true, fb(B.dgf), f, st));
   swiglu_bwd_kernel<<<std::min(M, 16 * 152), 256, 0, st>>>(bb(B.pq), fb(B.dgf), bb(B.gb), bb(B.dpq), M, f);
   mtp::note_launch();
-  if (float* gwd = gp(G->w_down)) {
-    transpose_bf16(bb(B.gb), M, f, f, bb(B.gT), Mp, st);
-    TRY(gemm_acc(d, f, M, bb(B.dhT), Mp, bb(B.gT), Mp, gwd, f, st));
-  }
+  if (float* gwd = gp(G->w_down)) TRY(gemm_acc(d, f, M, bb(B.dhb), d, true, bb(B.gb), f, true, gwd, f, st));
   // g = silu(y Wg^T) (y Wu^T): dWg += dp^T y; dWu += dq^T y; dy = dp Wg + dq Wu
-  transpose_bf16(bb(B.dpq), M, 2 * f, 2 * f, bb(B.dpqT), Mp, st);
-  transpose_bf16(y, M, d, d, bb(B.yT), Mp, st);
-  if (float* gg = gp(G->w_gate)) TRY(gemm_acc(f, d, M, bb(B.dpqT), Mp, bb(B.yT), Mp, gg, d, st));
-  if (float* gu = gp(G->w_up))
-    TRY(gemm_acc(f, d, M, bb(B.dpqT) + static_cast<size_t>(f) * Mp, Mp, bb(B.yT), Mp, gu, d, st));
+  if (float* gg = gp(G->w_gate)) TRY(gemm_acc(f, d, M, bb(B.dpq), 2 * f, true, y, d, true, gg, d, st));
+  if (float* gu = gp(G->w_up)) TRY(gemm_acc(f, d, M, bb(B.dpq) + f, 2 * f, true, y, d, true, gu, d, st));
   MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dyf), 0, Md * 4, st));
-  TRY(gemm_acc(M, d, 2 * f, bb(B.dpq), 2 * f, bb(B.wgT), 2 * f, fb(B.dyf), d, st));
+  TRY(gemm_acc(M, d, f, bb(B.dpq), 2 * f, false, wt(C.W.w_gate), d, true, fb(B.dyf), d, st));
+  TRY(gemm_acc(M, d, f, bb(B.dpq) + f, 2 * f, false, wt(C.W.w_up), d, true, fb(B.dyf), d, st));
   // y = RMSNorm_f(a): da = dh + RMSNorm backward
   MTP_CUDA_TRY(cudaMemcpyAsync(fb(B.daf), dh, Md * 4, cudaMemcpyDeviceToDevice, st));
   rmsnorm_bwd(a, d, nullptr, wt(C.W.ffn_norm), fb(B.dyf), d, fb(B.daf), d, nullptr, gp(G->ffn_norm), M, d, D.eps, st);
   // a = u + o Wo^T: dWo += da^T o; do = da Wo; du = da (+ the attention path)
   f32_to_bf16(fb(B.daf), d, bb(B.dab), d, M, d, st);
-  if (float* gwo = gp(G->wo)) {
-    transpose_bf16(bb(B.dab), M, d, d, bb(B.daT), Mp, st);
-    transpose_bf16(o, M, d, d, bb(B.oT), Mp, st);
-    TRY(gemm_acc(d, d, M, bb(B.daT), Mp, bb(B.oT), Mp, gwo, d, st));
-  }
+  if (float* gwo = gp(G->wo)) TRY(gemm_acc(d, d, M, bb(B.dab), d, true, o, d, true, gwo, d, st));
   MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dof), 0, Md * 4, st));
-  TRY(gemm_acc(M, d, d, bb(B.dab), d, bb(B.woT), d, fb(B.dof), d, st));
+  TRY(gemm_acc(M, d, d, bb(B.dab), d, false, wt(C.W.wo), d, true, fb(B.dof), d, st));
   f32_to_bf16(fb(B.dof), d, bb(B.dob), d, M, d, st);
   // segment-causal attention backward (tensor cores), then RoPE backward
   TRY(mtp::attn_bwd_launch(qkv, o, bb(B.dob), reinterpret_cast<const float*>(sv + C.so.lse2),
@@ -1409,27 +1321,22 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
                                            D.rope_base > 0.f ? 1 : 0);
   mtp::note_launch();
   // q, k, v = x W{q,k,v}^T: dW += d{q,k,v}^T x; dx = [dq dk dv] [Wq; Wk; Wv]
-  transpose_bf16(bb(B.dqkvb), M, 3 * d, 3 * d, bb(B.dqkvT), Mp, st);
-  transpose_bf16(x, M, d, d, bb(B.xT), Mp, st);
   float* gq[3] = {gp(G->wq), gp(G->wk), gp(G->wv)};
+  const bf* wqkv[3] = {wt(C.W.wq), wt(C.W.wk), wt(C.W.wv)};
   for (int j = 0; j < 3; ++j)
-    if (gq[j])
-      TRY(gemm_acc(d, d, M, bb(B.dqkvT) + static_cast<size_t>(j) * d * Mp, Mp, bb(B.xT), Mp, gq[j], d, st));
+    if (gq[j]) TRY(gemm_acc(d, d, M, bb(B.dqkvb) + static_cast<size_t>(j) * d, 3 * d, true, x, d, true, gq[j], d, st));
   MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dxf), 0, Md * 4, st));
-  TRY(gemm_acc(M, d, 3 * d, bb(B.dqkvb), 3 * d, bb(B.wqkvT), 3 * d, fb(B.dxf), d, st));
+  for (int j = 0; j < 3; ++j)
+    TRY(gemm_acc(M, d, d, bb(B.dqkvb) + static_cast<size_t>(j) * d, 3 * d, false, wqkv[j], d, true, fb(B.dxf), d, st));
   // x = RMSNorm_a(u): du = da + RMSNorm backward
   MTP_CUDA_TRY(cudaMemcpyAsync(fb(B.duf), fb(B.daf), Md * 4, cudaMemcpyDeviceToDevice, st));
   rmsnorm_bwd(u, d, nullptr, wt(C.W.attn_norm), fb(B.dxf), d, fb(B.duf), d, nullptr, gp(G->attn_norm), M, d, D.eps,
               st);
   // u = c M^T: dM += du^T c; dc = du M
   f32_to_bf16(fb(B.duf), d, bb(B.dub), d, M, d, st);
-  if (float* gm = gp(G->eh_proj)) {
-    transpose_bf16(bb(B.dub), M, d, d, bb(B.duT), Mp, st);
-    transpose_bf16(c, M, 2 * d, 2 * d, bb(B.cT), Mp, st);
-    TRY(gemm_acc(d, 2 * d, M, bb(B.duT), Mp, bb(B.cT), Mp, gm, 2 * d, st));
-  }
+  if (float* gm = gp(G->eh_proj)) TRY(gemm_acc(d, 2 * d, M, bb(B.dub), d, true, c, 2 * d, true, gm, 2 * d, st));
   MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dcf), 0, static_cast<size_t>(M) * 2 * d * 4, st));
-  TRY(gemm_acc(M, 2 * d, d, bb(B.dub), d, bb(B.mT), d, fb(B.dcf), 2 * d, st));
+  TRY(gemm_acc(M, 2 * d, d, bb(B.dub), d, false, wt(C.W.eh_proj), 2 * d, true, fb(B.dcf), 2 * d, st));
   // c = [RMSNorm_h(h_{k-1}); RMSNorm_e(E[x_{t+k}])]: dh_{k-1} += ..., dE[x_{t+k}] += ...
   rmsnorm_bwd(h_prev, d, nullptr, wt(C.W.hnorm), fb(B.dcf), 2 * d, dh_prev, d, nullptr, gp(G->hnorm), M, d, D.eps,
               st);
@@ -1494,7 +1401,6 @@ extern "C" mtp_status mtp_chain_loss_grad(const mtp_dims* dims, const mtp_weight
   term_scale_kernel<<<1, 32, 0, stream>>>(sums_counts, C.buf<float>(T.scale), D.D, static_cast<double>(M), W, den,
                                           with_main);
   mtp::note_launch();
-  transpose_bf16(static_cast<const bf*>(w->head), D.V, d, d, C.buf<bf>(T.wut), T.vp, stream);
   MTP_CUDA_TRY(cudaMemsetAsync(C.buf<float>(T.dstate), 0, static_cast<size_t>(D.D + 1) * Md * 4, stream));
   for (int t = with_main ? 0 : 1; t <= D.D; ++t) {
     const bf* h_t = t == 0 ? static_cast<const bf*>(h0) : hs + static_cast<size_t>(t - 1) * Md;

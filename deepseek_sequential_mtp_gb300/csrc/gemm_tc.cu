@@ -174,13 +174,28 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
          (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
          (static_cast<uint64_t>(2) << 61);
 }
+// Shared-memory matrix descriptor of an MN-major bf16 tile with the 128-byte
+// swizzle: each 64-element (128-byte) piece of the MN extent is a TMA box of
+// [64 MN x 64 k] with the k rows 128 bytes apart; leading byte offset = the
+// 8 KB between those MN pieces (bits 16-29), stride byte offset = 1024 B
+// between groups of 8 k rows (bits 32-45).  A K = 16 step advances the start
+// by 16 rows = 2048 B.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(8192 >> 4) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
-// (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits
-// 17-22, M >> 4 at bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+// (bits 7-9 = 1, 10-12 = 1), A / B MN-major when bit 15 / 16 is set (MNF bit
+// 0 / 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, int mnf = 0) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(mnf & 1) << 15) |
+         (static_cast<uint32_t>((mnf >> 1) & 1) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(m >> 4) << 24);
 }
+// MNF bits: 1 = A stored MN-major ([K rows][M], the M extent contiguous),
+// 2 = B stored MN-major ([K rows][N]); such operands arrive as [64 x 64] boxes.
+constexpr int kMnBox = 64 * 64 * 2;
 
 struct Args {
   int M, N, K;
@@ -293,7 +308,7 @@ __device__ __forceinline__ void rotate32(float (&x1)[32], float (&x2)[32], const
   }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, int MNF = 0>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
@@ -301,7 +316,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                const Args P) {
   using C = Cfg<BN, EPI>;
   constexpr int S = C::kStages;
-  constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
+  constexpr uint32_t kIdesc = idesc_bf16(BM, BN, MNF);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -374,8 +389,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const uint32_t sa = base + stage * C::kStageBytes;
         const uint32_t sb = sa + C::kABytes;
         mbar_expect_tx(full_bar(stage), C::kStageBytes);
-        tma_load_2d(sa, &tmA, kb * BK, tm * BM, full_bar(stage));
-        if constexpr (EPI == EPI_SWIGLU) {
+        if constexpr (MNF & 1) {
+#pragma unroll
+          for (int c = 0; c < BM / 64; ++c) tma_load_2d(sa + c * kMnBox, &tmA, tm * BM + 64 * c, kb * BK, full_bar(stage));
+        } else {
+          tma_load_2d(sa, &tmA, kb * BK, tm * BM, full_bar(stage));
+        }
+        if constexpr (MNF & 2) {
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + c * kMnBox, &tmB0, tn * BN + 64 * c, kb * BK, full_bar(stage));
+        } else if constexpr (EPI == EPI_SWIGLU) {
           tma_load_2d(sb, &tmB0, kb * BK, by, full_bar(stage));
           tma_load_2d(sb + (BN / 2) * BK * 2, &tmB1, kb * BK, by, full_bar(stage));
         } else {
@@ -408,11 +431,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sa = base + stage * C::kStageBytes;
-        const uint64_t adesc = sdesc_sw128(sa);
-        const uint64_t bdesc = sdesc_sw128(sa + C::kABytes);
+        // K-major: a K = 16 step is 32 bytes along the swizzled row; MN-major: 16 rows of 128 bytes
+        constexpr uint64_t kStepA = (MNF & 1) ? 2048 >> 4 : 2, kStepB = (MNF & 2) ? 2048 >> 4 : 2;
+        const uint64_t adesc = (MNF & 1) ? sdesc_mn_sw128(sa) : sdesc_sw128(sa);
+        const uint64_t bdesc = (MNF & 2) ? sdesc_mn_sw128(sa + C::kABytes) : sdesc_sw128(sa + C::kABytes);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+          umma_bf16(d_tmem, adesc + kStepA * kk, bdesc + kStepB * kk, kIdesc, (kb != kb0 || kk != 0) ? 1u : 0u);
         umma_commit(empty_bar(stage));
         if (++stage == S) { stage = 0; phase ^= 1u; }
       }
@@ -777,24 +802,27 @@ int num_sms() {
   return n;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, int MNF = 0>
 mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
   using C = Cfg<BN, EPI>;
   static bool attr_done = false;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, MNF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return MTP_ERR_CUDA;
     attr_done = true;
   }
   CUtensorMap ta, tb[3];
   const int box_b = EPI == EPI_SWIGLU ? BN / 2 : BN;
-  if (!make_map(&ta, g.A, g.M, g.K, g.lda, BM)) return MTP_ERR_INVALID_ARG;
+  // MN-major operands are [K rows][M or N] in memory, loaded as [64 x 64] boxes
+  if (!((MNF & 1) ? make_map(&ta, g.A, g.K, g.M, g.lda, 64) : make_map(&ta, g.A, g.M, g.K, g.lda, BM)))
+    return MTP_ERR_INVALID_ARG;
   const int nmaps = EPI == EPI_SWIGLU ? 2 : g.nseg;
   const int brows = EPI == EPI_SWIGLU ? g.N : g.seg_rows;
   for (int i = 0; i < 3; ++i) {
     const void* ptr = g.B[i < nmaps ? i : 0];
-    if (!make_map(&tb[i], ptr, brows, g.K, g.ldb, box_b)) return MTP_ERR_INVALID_ARG;
+    if (!((MNF & 2) ? make_map(&tb[i], ptr, g.K, g.N, g.ldb, 64) : make_map(&tb[i], ptr, brows, g.K, g.ldb, box_b)))
+      return MTP_ERR_INVALID_ARG;
   }
   // output / residual boxes: 32 rows x 64 columns, 128-byte swizzle
   CUtensorMap tout = ta;
@@ -826,7 +854,7 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
   a.ce_offset = g.ce_offset;
   const int ntiles = a.tiles_m * a.tiles_n * a.splits;
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
-  gemm_tc_kernel<BN, EPI><<<grid, kThreads, C::kSmemBytes, stream>>>(ta, tb[0], tb[1], tb[2], tout, a);
+  gemm_tc_kernel<BN, EPI, MNF><<<grid, kThreads, C::kSmemBytes, stream>>>(ta, tb[0], tb[1], tb[2], tout, a);
   mtp::note_launch();
   MTP_LAUNCH_CHECK();
   return MTP_OK;
@@ -866,6 +894,7 @@ mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream) {
   // TMA needs 16-byte row strides; a K extent that is not a multiple of the
   // k-block is zero-filled by the copies
   if (g.lda % 8 || g.ldb % 8) return MTP_ERR_ALIGNMENT;
+  if ((g.a_mn || g.b_mn) && g.epi != EPI_F32_ACC) return MTP_ERR_UNSUPPORTED;
   if (!aligned16(g.A)) return MTP_ERR_ALIGNMENT;
   for (int i = 0; i < 3; ++i)
     if (g.B[i] && !aligned16(g.B[i])) return MTP_ERR_ALIGNMENT;
@@ -901,8 +930,13 @@ mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream) {
     case EPI_F32_ACC: {
       if (!g.out_f32 || g.ldo % 4 || !aligned16(g.out_f32)) return MTP_ERR_INVALID_ARG;
       const int nk = (g.K + BK - 1) / BK;
-      if (g.splits < 1 || g.splits > nk) return MTP_ERR_INVALID_ARG;
-      return launch<256, EPI_F32_ACC>(g, stream);
+      if (g.splits < 1 || g.splits > nk || g.nseg != 1) return MTP_ERR_INVALID_ARG;
+      switch ((g.a_mn ? 1 : 0) | (g.b_mn ? 2 : 0)) {
+        case 0: return launch<256, EPI_F32_ACC, 0>(g, stream);
+        case 1: return launch<256, EPI_F32_ACC, 1>(g, stream);
+        case 2: return launch<256, EPI_F32_ACC, 2>(g, stream);
+        default: return launch<256, EPI_F32_ACC, 3>(g, stream);
+      }
     }
     case EPI_T_STORE:
     case EPI_T_ATOMIC: {
@@ -934,5 +968,27 @@ extern "C" mtp_status mtp_gemm_bf16(int M, int N, int K, const void* A, const vo
   g.epi = mtp::EPI_STORE;
   g.out = static_cast<__nv_bfloat16*>(C);
   g.ldo = N;
+  return mtp::gemm_bf16_launch(g, stream);
+}
+
+extern "C" mtp_status mtp_gemm_f32acc(int M, int N, int K, const void* A, int lda, int a_mn, const void* B, int ldb,
+                                      int b_mn, float* out, int ldo, int splits, cudaStream_t stream) {
+  if (!A || !B || !out) return MTP_ERR_INVALID_ARG;
+  mtp::GemmDesc g;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.A = static_cast<const __nv_bfloat16*>(A);
+  g.lda = lda;
+  g.a_mn = a_mn != 0;
+  g.B[0] = static_cast<const __nv_bfloat16*>(B);
+  g.ldb = ldb;
+  g.b_mn = b_mn != 0;
+  g.nseg = 1;
+  g.seg_rows = N;
+  g.epi = mtp::EPI_F32_ACC;
+  g.out_f32 = out;
+  g.ldo = ldo;
+  g.splits = splits;
   return mtp::gemm_bf16_launch(g, stream);
 }

@@ -110,6 +110,8 @@ def load() -> ctypes.CDLL:
     lib.mtp_draft_round_fp8.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Weights), ctypes.POINTER(BlockFp8),
                                         vp, vp, vp, vp, vp, vp, i32, ctypes.c_uint64, ctypes.c_uint64, vp, vp, vp,
                                         vp, sz, vp]
+    lib.mtp_gemm_f32acc.restype = i32
+    lib.mtp_gemm_f32acc.argtypes = [i32, i32, i32, vp, i32, i32, vp, i32, i32, vp, i32, i32, vp]
     lib.mtp_gemm_fp8w_workspace_bytes.restype = sz
     lib.mtp_gemm_fp8w_workspace_bytes.argtypes = [i32]
     lib.mtp_gemm_fp8w.restype = i32
@@ -248,6 +250,22 @@ class Fp8Block:
             m = getattr(self.struct, name)
             m.q = q.data_ptr()
             m.scale = sc.data_ptr()
+
+
+def gemm_f32acc(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor, a_mn=False, b_mn=False, splits=1, stream=None):
+    """out += A' B'^T (mtp_gemm_f32acc): A' = A ([M, K]) or, with a_mn, A^T of a
+    [K, M] tensor; B' = B ([N, K]) or, with b_mn, B^T of a [K, N] tensor."""
+    _need(A, "A", torch.bfloat16)
+    _need(B, "B", torch.bfloat16)
+    _need(out, "out", torch.float32)
+    M = A.shape[1] if a_mn else A.shape[0]
+    K = A.shape[0] if a_mn else A.shape[1]
+    N = B.shape[1] if b_mn else B.shape[0]
+    if (B.shape[0] if b_mn else B.shape[1]) != K or tuple(out.shape) != (M, N):
+        raise MtpError("gemm_f32acc: inconsistent shapes")
+    _check(load().mtp_gemm_f32acc(M, N, K, _ptr(A), A.shape[1], int(a_mn), _ptr(B), B.shape[1], int(b_mn), _ptr(out),
+                                  out.shape[1], int(splits), _stream(stream)), "mtp_gemm_f32acc")
+    return out
 
 
 def gemm_fp8w(x: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, out: torch.Tensor, stream=None, ws=None):

@@ -395,6 +395,16 @@ mtp_status mtp_gemm_fp8w(int R, int N, int K, const void* x, const void* wq, con
 mtp_status mtp_gemm_bf16(int M, int N, int K, const void* A, const void* B, void* C,
                          cudaStream_t stream);
 
+/* Diagnostic fp32-accumulating GEMM on the same core (the training step's
+ * gradient GEMMs): out[M,N] (fp32, row stride ldo) += A · B^T, bf16 operands.
+ * a_mn = 0: A is row-major [M, K] (row stride lda); a_mn = 1: A is stored as
+ * [K, M] (row stride lda), i.e. the product reads the transpose of a
+ * row-major [K, M] matrix.  b_mn likewise for B ([N, K] or [K, N]).  K is
+ * split into `splits` ranges (1..ceil(K/64)) whose partial tiles are added
+ * with fp32 atomics.  Leading dimensions % 8 == 0; pointers 16-byte aligned. */
+mtp_status mtp_gemm_f32acc(int M, int N, int K, const void* A, int lda, int a_mn, const void* B, int ldb, int b_mn,
+                           float* out, int ldo, int splits, cudaStream_t stream);
+
 /* Kernel classes for mtp_profile_kernel. */
 enum {
   MTP_KC_HEAD_CE_GEMM = 0,  /* shared head GEMM with the online max/sum-exp epilogue */

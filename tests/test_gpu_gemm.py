@@ -33,3 +33,24 @@ def test_gemm_repeated_calls_stable():
     torch.cuda.synchronize()
     assert torch.equal(C0, C1)
     assert lib.check_errors() == 0
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (True, False), (False, True), (True, True)])
+@pytest.mark.parametrize("M,N,K,splits", [(128, 256, 64, 1), (296, 1000, 200, 1), (1024, 512, 8192, 4),
+                                          (200, 776, 1000, 2)])
+def test_f32acc_operand_layouts(a_mn, b_mn, M, N, K, splits):
+    """out += A B^T into fp32 with either operand read K-major or MN-major
+    (the transpose of a row-major matrix, as the training step's weight and
+    input gradients use): against the fp32 product of the same bf16 values."""
+    g = torch.Generator(device="cuda").manual_seed(M + 3 * N + K)
+    A = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
+    B = torch.randn(N, K, device="cuda", generator=g).to(torch.bfloat16)
+    out0 = torch.randn(M, N, device="cuda", generator=g)
+    out = out0.clone()
+    lib.gemm_f32acc(A.t().contiguous() if a_mn else A, B.t().contiguous() if b_mn else B, out, a_mn=a_mn, b_mn=b_mn,
+                    splits=splits)
+    lib.check_errors()
+    ref = out0.double() + A.double() @ B.double().T
+    err = (out.double() - ref).abs()
+    tol = 1e-5 * (A.double().abs() @ B.double().abs().T) + 1e-5 * out0.double().abs() + 1e-6
+    assert bool((err <= tol).all()), f"max err {err.max().item()}"
