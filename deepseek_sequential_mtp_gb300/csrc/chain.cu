@@ -918,29 +918,40 @@ __global__ void term_scale_kernel(const double* __restrict__ sc, float* __restri
 // RMSNorm backward for y = g * h * r, r = (mean(h^2) + eps)^(-1/2), given
 // dy: dh += r (g dy - xh * mean(g dy xh)) with xh = h r; dg += sum over rows
 // of dy xh.  Row m reads h row h_rows[m] (or m) and adds its dh into row
-// dh_rows[m] with atomics (or row m plainly); dh may be null.  A block
-// takes 16 rows: its warps first form each row's r and mean(g dy xh), then
-// threads sweep columns across the rows (coalesced), summing the gain
-// gradient in a register and adding it to dg once per block.
-constexpr int kNormBwdRows = 16;
+// dh_rows[m] with atomics (or row m plainly); dh may be null.  A block takes
+// 32 rows: its warps first form each row's r and mean(g dy xh), then each
+// thread sweeps 4 adjacent columns down the rows (16-byte loads and stores),
+// summing the gain gradient in registers; the block writes that column sum to
+// its row of dg_part and a second kernel adds the blocks' rows into dg, so no
+// two blocks contend for the same dg entry.  Requires d % 4 == 0.
+constexpr int kNormBwdRows = 32;
 __global__ void __launch_bounds__(256)
 rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, int ld_h, const int32_t* __restrict__ h_rows,
                    const __nv_bfloat16* __restrict__ g, const float* __restrict__ dy, int ld_dy, float* __restrict__ dh,
-                   int ld_dh, const int32_t* __restrict__ dh_rows, float* __restrict__ dg, int M, int d, float eps) {
+                   int ld_dh, const int32_t* __restrict__ dh_rows, float* __restrict__ dg_part, int M, int d,
+                   float eps) {
   __shared__ float s_r[kNormBwdRows], s_mean[kNormBwdRows];
+  __shared__ int s_hrow[kNormBwdRows], s_dhrow[kNormBwdRows];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * kNormBwdRows;
   const int rows = min(kNormBwdRows, M - m0);
-  // row statistics: r = (mean(h^2) + eps)^(-1/2) and mean(g dy xh) (2 rows per warp)
+  // row statistics: r = (mean(h^2) + eps)^(-1/2) and mean(g dy xh) (4 rows per warp)
   for (int j = warp; j < rows; j += 8) {
     const int m = m0 + j;
-    const __nv_bfloat16* hr = h + static_cast<size_t>(h_rows ? h_rows[m] : m) * ld_h;
+    const int hrow = h_rows ? h_rows[m] : m;
+    const __nv_bfloat16* hr = h + static_cast<size_t>(hrow) * ld_h;
     const float* dyr = dy + static_cast<size_t>(m) * ld_dy;
     float ss = 0.f, dot = 0.f;
-    for (int i = lane; i < d; i += 32) {
-      const float hv = __bfloat162float(hr[i]);
-      ss += hv * hv;
-      dot += __bfloat162float(g[i]) * dyr[i] * hv;
+    for (int i = 4 * lane; i < d; i += 128) {
+      const uint2 hv = *reinterpret_cast<const uint2*>(hr + i);
+      const uint2 gv = *reinterpret_cast<const uint2*>(g + i);
+      const float4 dv = *reinterpret_cast<const float4*>(dyr + i);
+      const float2 h01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hv.x));
+      const float2 h23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hv.y));
+      const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv.x));
+      const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv.y));
+      ss += h01.x * h01.x + h01.y * h01.y + h23.x * h23.x + h23.y * h23.y;
+      dot += g01.x * dv.x * h01.x + g01.y * dv.y * h01.y + g23.x * dv.z * h23.x + g23.y * dv.w * h23.y;
     }
     ss = mtp::warp_sum(ss);
     dot = mtp::warp_sum(dot);
@@ -948,37 +959,68 @@ rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, int ld_h, const int32_t*
       const float r = 1.0f / sqrtf(ss / d + eps);
       s_r[j] = r;
       s_mean[j] = dot * r / d;
+      s_hrow[j] = hrow;
+      s_dhrow[j] = dh_rows ? dh_rows[m] : m;
     }
   }
   __syncthreads();
-  // columns across the block's rows: coalesced row reads, the gain gradient summed in a register
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    const float gi = __bfloat162float(g[i]);
-    float dg_acc = 0.f;
+  for (int i = 4 * threadIdx.x; i < d; i += 4 * blockDim.x) {
+    const uint2 gv = *reinterpret_cast<const uint2*>(g + i);
+    const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv.x));
+    const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv.y));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
     for (int j = 0; j < rows; ++j) {
-      const int m = m0 + j;
-      const float r = s_r[j];
-      const float xh = __bfloat162float(h[static_cast<size_t>(h_rows ? h_rows[m] : m) * ld_h + i]) * r;
-      const float dyv = dy[static_cast<size_t>(m) * ld_dy + i];
-      dg_acc += dyv * xh;
+      const float r = s_r[j], mean = s_mean[j];
+      const uint2 hv = *reinterpret_cast<const uint2*>(h + static_cast<size_t>(s_hrow[j]) * ld_h + i);
+      const float2 h01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hv.x));
+      const float2 h23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hv.y));
+      const float4 dv = *reinterpret_cast<const float4*>(dy + static_cast<size_t>(m0 + j) * ld_dy + i);
+      const float4 xh = make_float4(h01.x * r, h01.y * r, h23.x * r, h23.y * r);
+      acc.x += dv.x * xh.x;
+      acc.y += dv.y * xh.y;
+      acc.z += dv.z * xh.z;
+      acc.w += dv.w * xh.w;
       if (dh) {
-        const float v = r * (gi * dyv - xh * s_mean[j]);
-        float* dst = dh + static_cast<size_t>(dh_rows ? dh_rows[m] : m) * ld_dh + i;
-        if (dh_rows) atomicAdd(dst, v);
-        else *dst += v;
+        const float4 v = make_float4(r * (g01.x * dv.x - xh.x * mean), r * (g01.y * dv.y - xh.y * mean),
+                                     r * (g23.x * dv.z - xh.z * mean), r * (g23.y * dv.w - xh.w * mean));
+        float4* dst = reinterpret_cast<float4*>(dh + static_cast<size_t>(s_dhrow[j]) * ld_dh + i);
+        if (dh_rows) {
+          atomicAdd(dst, v);
+        } else {
+          float4 o = *dst;
+          o.x += v.x;
+          o.y += v.y;
+          o.z += v.z;
+          o.w += v.w;
+          *dst = o;
+        }
       }
     }
-    if (dg) atomicAdd(&dg[i], dg_acc);
+    if (dg_part) *reinterpret_cast<float4*>(dg_part + static_cast<size_t>(blockIdx.x) * d + i) = acc;
   }
 }
 
+// dg[i] += Σ_b part[b][i] over the row blocks of rmsnorm_bwd_kernel
+__global__ void colsum_add_kernel(const float* __restrict__ part, int nb, int d, float* __restrict__ dg) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= d) return;
+  float s = 0.f;
+  for (int b = 0; b < nb; ++b) s += part[static_cast<size_t>(b) * d + i];
+  dg[i] += s;
+}
+
 void rmsnorm_bwd(const __nv_bfloat16* h, int ld_h, const int32_t* h_rows, const __nv_bfloat16* g, const float* dy,
-                 int ld_dy, float* dh, int ld_dh, const int32_t* dh_rows, float* dg, int M, int d, float eps,
-                 cudaStream_t st) {
-  rmsnorm_bwd_kernel<<<(M + kNormBwdRows - 1) / kNormBwdRows, 256, 0, st>>>(
-      h, ld_h, h_rows, g, dy, ld_dy, dh, ld_dh, dh_rows, dg, M, d, eps);
+                 int ld_dy, float* dh, int ld_dh, const int32_t* dh_rows, float* dg, float* dg_part, int M, int d,
+                 float eps, cudaStream_t st) {
+  const int nb = (M + kNormBwdRows - 1) / kNormBwdRows;
+  rmsnorm_bwd_kernel<<<nb, 256, 0, st>>>(h, ld_h, h_rows, g, dy, ld_dy, dh, ld_dh, dh_rows, dg ? dg_part : nullptr,
+                                         M, d, eps);
   mtp::note_launch();
+  if (dg) {
+    colsum_add_kernel<<<(d + 255) / 256, 256, 0, st>>>(dg_part, nb, d, dg);
+    mtp::note_launch();
+  }
 }
 
 // a += b (fp32, n elements)
@@ -991,7 +1033,7 @@ __global__ void add_f32_kernel(float* __restrict__ a, const float* __restrict__ 
 inline int round_up8(int v) { return (v + 7) / 8 * 8; }
 
 struct TrainLayout {
-  size_t hs, lse, scale, dz, dx, dstate, save, total;
+  size_t hs, lse, scale, dz, dx, dgp, dstate, save, total;
   int vc, vp, mp;
 };
 
@@ -1016,6 +1058,7 @@ TrainLayout make_train_layout(const mtp_dims& D) {
   T.scale = take(static_cast<size_t>(D.D + 1) * 4);
   T.dz = take(M * T.vc * 2);
   T.dx = take(M * d * 4);
+  T.dgp = take(static_cast<size_t>((M + kNormBwdRows - 1) / kNormBwdRows) * d * 4);  // RMSNorm gain partials
   T.dstate = take(static_cast<size_t>(D.D + 1) * M * d * 4);
   T.save = take(static_cast<size_t>(D.D) * make_save_off(D).bytes);
   T.total = off;
@@ -1078,7 +1121,8 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
     TRY(gemm_acc(vc, d, M, dz, T.vc, true, x, d, true, d_head + static_cast<size_t>(v0) * d, d, C.st));
   }
   float* dstate_t = C.buf<float>(T.dstate) + static_cast<size_t>(t) * M * d;
-  rmsnorm_bwd(h_t, d, nullptr, out_norm, dx, d, dstate_t, d, nullptr, d_out_norm, M, d, D.eps, C.st);
+  rmsnorm_bwd(h_t, d, nullptr, out_norm, dx, d, dstate_t, d, nullptr, d_out_norm, C.buf<float>(T.dgp), M, d, D.eps,
+              C.st);
   MTP_LAUNCH_CHECK();
   return MTP_OK;
 }
@@ -1306,7 +1350,9 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
   TRY(gemm_acc(M, d, f, bb(B.dpq) + f, 2 * f, false, wt(C.W.w_up), d, true, fb(B.dyf), d, st));
   // y = RMSNorm_f(a): da = dh + RMSNorm backward
   MTP_CUDA_TRY(cudaMemcpyAsync(fb(B.daf), dh, Md * 4, cudaMemcpyDeviceToDevice, st));
-  rmsnorm_bwd(a, d, nullptr, wt(C.W.ffn_norm), fb(B.dyf), d, fb(B.daf), d, nullptr, gp(G->ffn_norm), M, d, D.eps, st);
+  float* dgp = fb(T.dgp);
+  rmsnorm_bwd(a, d, nullptr, wt(C.W.ffn_norm), fb(B.dyf), d, fb(B.daf), d, nullptr, gp(G->ffn_norm), dgp, M, d, D.eps,
+              st);
   // a = u + o Wo^T: dWo += da^T o; do = da Wo; du = da (+ the attention path)
   f32_to_bf16(fb(B.daf), d, bb(B.dab), d, M, d, st);
   if (float* gwo = gp(G->wo)) TRY(gemm_acc(d, d, M, bb(B.dab), d, true, o, d, true, gwo, d, st));
@@ -1330,7 +1376,7 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
     TRY(gemm_acc(M, d, d, bb(B.dqkvb) + static_cast<size_t>(j) * d, 3 * d, false, wqkv[j], d, true, fb(B.dxf), d, st));
   // x = RMSNorm_a(u): du = da + RMSNorm backward
   MTP_CUDA_TRY(cudaMemcpyAsync(fb(B.duf), fb(B.daf), Md * 4, cudaMemcpyDeviceToDevice, st));
-  rmsnorm_bwd(u, d, nullptr, wt(C.W.attn_norm), fb(B.dxf), d, fb(B.duf), d, nullptr, gp(G->attn_norm), M, d, D.eps,
+  rmsnorm_bwd(u, d, nullptr, wt(C.W.attn_norm), fb(B.dxf), d, fb(B.duf), d, nullptr, gp(G->attn_norm), dgp, M, d, D.eps,
               st);
   // u = c M^T: dM += du^T c; dc = du M
   f32_to_bf16(fb(B.duf), d, bb(B.dub), d, M, d, st);
@@ -1338,13 +1384,13 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
   MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dcf), 0, static_cast<size_t>(M) * 2 * d * 4, st));
   TRY(gemm_acc(M, 2 * d, d, bb(B.dub), d, false, wt(C.W.eh_proj), 2 * d, true, fb(B.dcf), 2 * d, st));
   // c = [RMSNorm_h(h_{k-1}); RMSNorm_e(E[x_{t+k}])]: dh_{k-1} += ..., dE[x_{t+k}] += ...
-  rmsnorm_bwd(h_prev, d, nullptr, wt(C.W.hnorm), fb(B.dcf), 2 * d, dh_prev, d, nullptr, gp(G->hnorm), M, d, D.eps,
+  rmsnorm_bwd(h_prev, d, nullptr, wt(C.W.hnorm), fb(B.dcf), 2 * d, dh_prev, d, nullptr, gp(G->hnorm), dgp, M, d, D.eps,
               st);
   int32_t* tok = C.buf<int32_t>(B.tok);
   shifted_tokens_kernel<<<(M + 255) / 256, 256, 0, st>>>(C.tokens, tok, M, D.T, k, D.V);
   mtp::note_launch();
   rmsnorm_bwd(static_cast<const bf*>(C.W.embed), d, tok, wt(C.W.enorm), fb(B.dcf) + d, 2 * d, G->embed, d, tok,
-              gp(G->enorm), M, d, D.eps, st);
+              gp(G->enorm), dgp, M, d, D.eps, st);
   MTP_LAUNCH_CHECK();
   return MTP_OK;
 }
