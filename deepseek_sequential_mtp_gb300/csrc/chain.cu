@@ -1001,13 +1001,25 @@ rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, int ld_h, const int32_t*
   }
 }
 
-// dg[i] += Σ_b part[b][i] over the row blocks of rmsnorm_bwd_kernel
-__global__ void colsum_add_kernel(const float* __restrict__ part, int nb, int d, float* __restrict__ dg) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= d) return;
-  float s = 0.f;
-  for (int b = 0; b < nb; ++b) s += part[static_cast<size_t>(b) * d + i];
-  dg[i] += s;
+// dg[i] += Σ_b part[b][i] over the row blocks of rmsnorm_bwd_kernel: a block
+// takes 32 columns, its 8 warps stride over the rows (coalesced 128-byte row
+// pieces) and combine their sums in shared memory
+__global__ void __launch_bounds__(256) colsum_add_kernel(const float* __restrict__ part, int nb, int d,
+                                                         float* __restrict__ dg) {
+  __shared__ float s_sum[8][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x * 32 + lane;
+  float acc = 0.f;
+  if (i < d)
+    for (int b = warp; b < nb; b += 8) acc += part[static_cast<size_t>(b) * d + i];
+  s_sum[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0 && i < d) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += s_sum[w][lane];
+    dg[i] += t;
+  }
 }
 
 void rmsnorm_bwd(const __nv_bfloat16* h, int ld_h, const int32_t* h_rows, const __nv_bfloat16* g, const float* dy,
@@ -1018,7 +1030,7 @@ void rmsnorm_bwd(const __nv_bfloat16* h, int ld_h, const int32_t* h_rows, const 
                                          M, d, eps);
   mtp::note_launch();
   if (dg) {
-    colsum_add_kernel<<<(d + 255) / 256, 256, 0, st>>>(dg_part, nb, d, dg);
+    colsum_add_kernel<<<(d + 31) / 32, 256, 0, st>>>(dg_part, nb, d, dg);
     mtp::note_launch();
   }
 }
@@ -1066,7 +1078,7 @@ TrainLayout make_train_layout(const mtp_dims& D) {
 }
 
 mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, bool a_mn, const __nv_bfloat16* B, int ldb,
-                    bool b_mn, float* out, int ldo, cudaStream_t st);
+                    bool b_mn, float* out, int ldo, cudaStream_t st, bool overwrite = false);
 
 mtp::GemmDesc gdesc(int M, int N, int K, const __nv_bfloat16* A, int lda, const __nv_bfloat16* B, int ldb) {
   mtp::GemmDesc g;
@@ -1102,7 +1114,6 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
   const float* lse = C.buf<float>(T.lse) + static_cast<size_t>(t) * M;
   const float* scale = C.buf<float>(T.scale) + t;
   launch_rmsnorm<bf>(C, h_t, out_norm, x, labels, t);
-  MTP_CUDA_TRY(cudaMemsetAsync(dx, 0, static_cast<size_t>(M) * d * 4, C.st));
   for (int v0 = 0; v0 < V; v0 += T.vc) {
     const int vc = std::min(T.vc, V - v0);
     mtp::GemmDesc g = gdesc(M, vc, d, x, d, WU + static_cast<size_t>(v0) * d, d);
@@ -1115,7 +1126,7 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
     g.ce_offset = v0;
     TRY(mtp::gemm_bf16_launch(g, C.st));
     // dX += dz W_U[v0 : v0 + vc] (W_U rows read as the MN-major B operand)
-    TRY(gemm_acc(M, d, vc, dz, T.vc, false, WU + static_cast<size_t>(v0) * d, d, true, dx, d, C.st));
+    TRY(gemm_acc(M, d, vc, dz, T.vc, false, WU + static_cast<size_t>(v0) * d, d, true, dx, d, C.st, v0 == 0));
     if (!d_head) continue;
     // dW_U[v0 : v0 + vc] += dz^T X (both operands read MN-major)
     TRY(gemm_acc(vc, d, M, dz, T.vc, true, x, d, true, d_head + static_cast<size_t>(v0) * d, d, C.st));
@@ -1204,7 +1215,7 @@ __global__ void shifted_tokens_kernel(const int32_t* __restrict__ tokens, int32_
 
 // scratch of the block backward (reused depth after depth)
 struct BwdLayout {
-  size_t dhb, pq, gb, dgf, dpq, dyf, daf, dab, dof, dob, dqkvf, dqkvb, dxf, duf, dub, dcf, adsum, tok, total;
+  size_t dhb, pq, gb, dgf, dpq, dyf, daf, dab, dob, dqkvf, dqkvb, dxf, duf, dub, dcf, adsum, tok, total;
 };
 
 BwdLayout make_bwd_layout(const mtp_dims& D, size_t start, int mp) {
@@ -1224,7 +1235,6 @@ BwdLayout make_bwd_layout(const mtp_dims& D, size_t start, int mp) {
   B.dyf = take(M * d * 4);
   B.daf = take(M * d * 4);
   B.dab = take(M * d * 2);
-  B.dof = take(M * d * 4);
   B.dob = take(M * d * 2);
   B.dqkvf = take(M * 3 * d * 4);
   B.dqkvb = take(M * 3 * d * 2);
@@ -1259,14 +1269,14 @@ SaveOff make_save_off(const mtp_dims& D) {
   return S;
 }
 
-// C += A B^T into fp32; A is [M, K] (a_mn: stored [K, M]) and B is [N, K]
+// C += A B^T (C = A B^T with `overwrite`) into fp32; A is [M, K] (a_mn: stored [K, M]) and B is [N, K]
 // (b_mn: stored [K, N]), so transposes of row-major operands are read in
 // place.  K is split (partial tiles added with vector atomics)
 // when that fills the SMs' waves better: the smallest split whose work units
 // fill at least 90% of their last wave, else the best one (at most 16, and
 // at least 8 k-blocks per split).
 mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, bool a_mn, const __nv_bfloat16* B, int ldb,
-                    bool b_mn, float* out, int ldo, cudaStream_t st) {
+                    bool b_mn, float* out, int ldo, cudaStream_t st, bool overwrite) {
   static int sms = 0;
   if (sms == 0) {
     int dev = 0;
@@ -1295,6 +1305,12 @@ mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, bool a
     if (eff >= 0.9) break;
   }
   g.splits = splits;
+  if (overwrite) {  // out = A B^T: one split stores directly, several add into a zeroed output
+    if (splits == 1)
+      g.f32_overwrite = true;
+    else
+      MTP_CUDA_TRY(cudaMemset2DAsync(out, static_cast<size_t>(ldo) * 4, 0, static_cast<size_t>(N) * 4, M, st));
+  }
   return mtp::gemm_bf16_launch(g, st);
 }
 
@@ -1337,16 +1353,14 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
     g.ldo = 2 * f;
     TRY(mtp::gemm_bf16_launch(g, st));
   }
-  MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dgf), 0, static_cast<size_t>(M) * f * 4, st));
-  TRY(gemm_acc(M, f, d, bb(B.dhb), d, false, wt(C.W.w_down), f, true, fb(B.dgf), f, st));
+  TRY(gemm_acc(M, f, d, bb(B.dhb), d, false, wt(C.W.w_down), f, true, fb(B.dgf), f, st, true));
   swiglu_bwd_kernel<<<std::min(M, 16 * 152), 256, 0, st>>>(bb(B.pq), fb(B.dgf), bb(B.gb), bb(B.dpq), M, f);
   mtp::note_launch();
   if (float* gwd = gp(G->w_down)) TRY(gemm_acc(d, f, M, bb(B.dhb), d, true, bb(B.gb), f, true, gwd, f, st));
   // g = silu(y Wg^T) (y Wu^T): dWg += dp^T y; dWu += dq^T y; dy = dp Wg + dq Wu
   if (float* gg = gp(G->w_gate)) TRY(gemm_acc(f, d, M, bb(B.dpq), 2 * f, true, y, d, true, gg, d, st));
   if (float* gu = gp(G->w_up)) TRY(gemm_acc(f, d, M, bb(B.dpq) + f, 2 * f, true, y, d, true, gu, d, st));
-  MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dyf), 0, Md * 4, st));
-  TRY(gemm_acc(M, d, f, bb(B.dpq), 2 * f, false, wt(C.W.w_gate), d, true, fb(B.dyf), d, st));
+  TRY(gemm_acc(M, d, f, bb(B.dpq), 2 * f, false, wt(C.W.w_gate), d, true, fb(B.dyf), d, st, true));
   TRY(gemm_acc(M, d, f, bb(B.dpq) + f, 2 * f, false, wt(C.W.w_up), d, true, fb(B.dyf), d, st));
   // y = RMSNorm_f(a): da = dh + RMSNorm backward
   MTP_CUDA_TRY(cudaMemcpyAsync(fb(B.daf), dh, Md * 4, cudaMemcpyDeviceToDevice, st));
@@ -1356,9 +1370,14 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
   // a = u + o Wo^T: dWo += da^T o; do = da Wo; du = da (+ the attention path)
   f32_to_bf16(fb(B.daf), d, bb(B.dab), d, M, d, st);
   if (float* gwo = gp(G->wo)) TRY(gemm_acc(d, d, M, bb(B.dab), d, true, o, d, true, gwo, d, st));
-  MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dof), 0, Md * 4, st));
-  TRY(gemm_acc(M, d, d, bb(B.dab), d, false, wt(C.W.wo), d, true, fb(B.dof), d, st));
-  f32_to_bf16(fb(B.dof), d, bb(B.dob), d, M, d, st);
+  {  // do = da Wo, written in bf16 straight from the accumulator (the attention backward's input)
+    mtp::GemmDesc g = gdesc(M, d, d, bb(B.dab), d, wt(C.W.wo), d);
+    g.b_mn = true;
+    g.epi = mtp::EPI_STORE;
+    g.out = bb(B.dob);
+    g.ldo = d;
+    TRY(mtp::gemm_bf16_launch(g, st));
+  }
   // segment-causal attention backward (tensor cores), then RoPE backward
   TRY(mtp::attn_bwd_launch(qkv, o, bb(B.dob), reinterpret_cast<const float*>(sv + C.so.lse2),
                            C.buf<int32_t>(C.L.seg_start), C.buf<int32_t>(C.L.seg_end), fb(B.dqkvf), fb(B.adsum), D.B,
@@ -1371,9 +1390,9 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
   const bf* wqkv[3] = {wt(C.W.wq), wt(C.W.wk), wt(C.W.wv)};
   for (int j = 0; j < 3; ++j)
     if (gq[j]) TRY(gemm_acc(d, d, M, bb(B.dqkvb) + static_cast<size_t>(j) * d, 3 * d, true, x, d, true, gq[j], d, st));
-  MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dxf), 0, Md * 4, st));
   for (int j = 0; j < 3; ++j)
-    TRY(gemm_acc(M, d, d, bb(B.dqkvb) + static_cast<size_t>(j) * d, 3 * d, false, wqkv[j], d, true, fb(B.dxf), d, st));
+    TRY(gemm_acc(M, d, d, bb(B.dqkvb) + static_cast<size_t>(j) * d, 3 * d, false, wqkv[j], d, true, fb(B.dxf), d, st,
+                 j == 0));
   // x = RMSNorm_a(u): du = da + RMSNorm backward
   MTP_CUDA_TRY(cudaMemcpyAsync(fb(B.duf), fb(B.daf), Md * 4, cudaMemcpyDeviceToDevice, st));
   rmsnorm_bwd(u, d, nullptr, wt(C.W.attn_norm), fb(B.dxf), d, fb(B.duf), d, nullptr, gp(G->attn_norm), dgp, M, d, D.eps,
@@ -1381,8 +1400,7 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
   // u = c M^T: dM += du^T c; dc = du M
   f32_to_bf16(fb(B.duf), d, bb(B.dub), d, M, d, st);
   if (float* gm = gp(G->eh_proj)) TRY(gemm_acc(d, 2 * d, M, bb(B.dub), d, true, c, 2 * d, true, gm, 2 * d, st));
-  MTP_CUDA_TRY(cudaMemsetAsync(fb(B.dcf), 0, static_cast<size_t>(M) * 2 * d * 4, st));
-  TRY(gemm_acc(M, 2 * d, d, bb(B.dub), d, false, wt(C.W.eh_proj), 2 * d, true, fb(B.dcf), 2 * d, st));
+  TRY(gemm_acc(M, 2 * d, d, bb(B.dub), d, false, wt(C.W.eh_proj), 2 * d, true, fb(B.dcf), 2 * d, st, true));
   // c = [RMSNorm_h(h_{k-1}); RMSNorm_e(E[x_{t+k}])]: dh_{k-1} += ..., dE[x_{t+k}] += ...
   rmsnorm_bwd(h_prev, d, nullptr, wt(C.W.hnorm), fb(B.dcf), 2 * d, dh_prev, d, nullptr, gp(G->hnorm), dgp, M, d, D.eps,
               st);

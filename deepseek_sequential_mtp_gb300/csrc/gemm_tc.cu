@@ -213,6 +213,7 @@ struct Args {
   float* z_tgt;
   float* out_f32;
   int splits;
+  int f32_overwrite;
   const float* lse;
   const float* ce_scale;
   int ce_offset;
@@ -688,6 +689,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               } else {
                 for (int i = 0; i < 32 && col0 + i < P.N; ++i) atomicAdd(dst + i, v[i]);
               }
+            } else if (P.f32_overwrite) {  // the first product into this output: no read
+              if (col0 + 32 <= P.N) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                  *reinterpret_cast<float4*>(dst + 4 * q) =
+                      make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+              } else {
+                for (int i = 0; i < 32 && col0 + i < P.N; ++i) dst[i] = v[i];
+              }
             } else if (col0 + 32 <= P.N) {
 #pragma unroll
               for (int q = 0; q < 8; ++q) {
@@ -849,6 +859,7 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
   a.z_tgt = g.z_tgt;
   a.out_f32 = g.out_f32;
   a.splits = g.splits > 0 ? g.splits : 1;
+  a.f32_overwrite = g.f32_overwrite ? 1 : 0;
   a.lse = g.lse;
   a.ce_scale = g.ce_scale;
   a.ce_offset = g.ce_offset;
@@ -894,7 +905,8 @@ mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream) {
   // TMA needs 16-byte row strides; a K extent that is not a multiple of the
   // k-block is zero-filled by the copies
   if (g.lda % 8 || g.ldb % 8) return MTP_ERR_ALIGNMENT;
-  if ((g.a_mn || g.b_mn) && g.epi != EPI_F32_ACC) return MTP_ERR_UNSUPPORTED;
+  if ((g.a_mn || g.b_mn) && g.epi != EPI_F32_ACC && g.epi != EPI_STORE) return MTP_ERR_UNSUPPORTED;
+  if (g.f32_overwrite && (g.epi != EPI_F32_ACC || g.splits > 1)) return MTP_ERR_INVALID_ARG;
   if (!aligned16(g.A)) return MTP_ERR_ALIGNMENT;
   for (int i = 0; i < 3; ++i)
     if (g.B[i] && !aligned16(g.B[i])) return MTP_ERR_ALIGNMENT;
@@ -907,6 +919,10 @@ mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream) {
       const int seg = g.seg_rows > 0 ? g.seg_rows : g.N;
       if (g.nseg > 1 && seg % 128) return MTP_ERR_UNSUPPORTED;
       const bool wide = (g.nseg == 1 || seg % 256 == 0);
+      if (g.epi == EPI_STORE && (g.a_mn || g.b_mn)) {  // bf16 output of a product with a transposed operand
+        if (g.nseg != 1 || g.a_mn) return MTP_ERR_UNSUPPORTED;
+        return launch<256, EPI_STORE, 2>(g, stream);
+      }
       if (g.epi == EPI_STORE) return wide ? launch<256, EPI_STORE>(g, stream) : launch<128, EPI_STORE>(g, stream);
       return wide ? launch<256, EPI_RESID>(g, stream) : launch<128, EPI_RESID>(g, stream);
     }

@@ -34,7 +34,7 @@ constexpr bool epi_uses_staging(int epi) {
 }
 
 // C-side description of one GEMM  acc[M, N] = A[M, K] · B[N, K]^T  (bf16 in,
-// fp32 accumulate).  a_mn / b_mn (EPI_F32_ACC only): the operand is stored
+// fp32 accumulate).  a_mn / b_mn (EPI_F32_ACC; b_mn also EPI_STORE): the operand is stored
 // MN-major, i.e. as [K rows][M] (resp. [K rows][N]) with row stride lda (ldb),
 // so A^T or B^T of a row-major matrix is read without a transposed copy.  B may be given as up to three row segments of
 // `seg_rows` rows each (q/k/v weights); for EPI_SWIGLU B[0] = gate [N, K]
@@ -49,6 +49,8 @@ struct GemmDesc {
   int seg_rows = 0;
   int epi = EPI_STORE;
   bool a_mn = false, b_mn = false;
+  // EPI_F32_ACC with one split: store instead of adding (the output's first product)
+  bool f32_overwrite = false;
   __nv_bfloat16* out = nullptr;
   int ldo = 0;
   const __nv_bfloat16* resid = nullptr;
