@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmtp.so")
 
-SOURCES = ["api.cu", "verify.cu", "chain.cu", "gemm_tc.cu", "attn.cu", "noalloc.cu", "draft.cu", "fp8.cu"]
+SOURCES = ["api.cu", "verify.cu", "chain.cu", "gemm_tc.cu", "attn.cu", "noalloc.cu", "draft.cu", "fp8.cu", "decode_gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", "-I", INCLUDE]

@@ -60,6 +60,7 @@ unsigned int mtp_take_errors_attn();
 unsigned int mtp_take_errors_verify();
 unsigned int mtp_take_errors_draft();
 unsigned int mtp_take_errors_fp8();
+unsigned int mtp_take_errors_dgemm();
 
 extern "C" const char* mtp_status_string(int s) {
   switch (s) {
@@ -79,12 +80,14 @@ extern "C" int mtp_abi_version(void) { return MTP_ABI_VERSION; }
 
 extern "C" mtp_status mtp_check_errors(cudaStream_t stream, unsigned int* flags) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MTP_ERR_CUDA;
-  const unsigned int parts[6] = {mtp_take_errors_chain(), mtp_take_errors_gemm(), mtp_take_errors_attn(),
-                                 mtp_take_errors_verify(), mtp_take_errors_draft(), mtp_take_errors_fp8()};
-  const unsigned int from[6] = {MTP_DEVERR_FROM_CHAIN, MTP_DEVERR_FROM_GEMM, MTP_DEVERR_FROM_ATTN,
-                                MTP_DEVERR_FROM_VERIFY, MTP_DEVERR_FROM_DRAFT, MTP_DEVERR_FROM_FP8};
+  const unsigned int parts[7] = {mtp_take_errors_chain(), mtp_take_errors_gemm(), mtp_take_errors_attn(),
+                                 mtp_take_errors_verify(), mtp_take_errors_draft(), mtp_take_errors_fp8(),
+                                 mtp_take_errors_dgemm()};
+  const unsigned int from[7] = {MTP_DEVERR_FROM_CHAIN, MTP_DEVERR_FROM_GEMM, MTP_DEVERR_FROM_ATTN,
+                                MTP_DEVERR_FROM_VERIFY, MTP_DEVERR_FROM_DRAFT, MTP_DEVERR_FROM_FP8,
+                                MTP_DEVERR_FROM_DGEMM};
   unsigned int v = 0;
-  for (int i = 0; i < 6; ++i)
+  for (int i = 0; i < 7; ++i)
     if (parts[i]) v |= parts[i] | from[i];
   if (flags) *flags = v;
   return v ? MTP_ERR_DEVICE : MTP_OK;

@@ -10,11 +10,13 @@
 //   q_r = softmax(W_U RMSNorm_out(h)), y_r = smallest v with Σ_{i<=v} q_i > u·Σq
 //   where u = word 2 of Philox4x32-10(key = seed, counter = (0, r, offset)).
 //
-// Every weight-streaming product is a skinny GEMM (R <= 32 tokens): the
-// tcgen05 core runs it swap-AB (weights on the 128-row side, tokens as
-// N = 32) with split-K so that the weight stream covers every SM; partial
-// tiles accumulate into an fp32 buffer with atomics and small "finish"
-// kernels round to bf16 with the fused RoPE / residual / SwiGLU / RMSNorm.
+// Every weight-streaming product is a skinny GEMM (R <= 32 tokens).  The
+// block's linear maps run on the decode GEMM (decode_gemm.cu: weights on the
+// N = 256 side of the tcgen05 MMA, equal weight streams per SM), the head on
+// the swap-AB mode of the tcgen05 core (weights on the 128-row side, logits
+// stored transposed); partial tiles accumulate into an fp32 buffer with
+// atomics and small "finish" kernels round to bf16 with the fused RoPE /
+// residual / SwiGLU / RMSNorm.
 // Attention is split-K decoding: persistent CTAs stream the cache with TMA
 // and write partial (max, sum, output) records per (request, head, key
 // split) that a combine kernel merges with the new row's key.  The head writes logits into q_out, which a per-request
@@ -28,6 +30,7 @@
 #include <cmath>
 #include <initializer_list>
 
+#include "decode_gemm.cuh"
 #include "fp8.cuh"
 #include "gemm_tc.cuh"
 #include "mbarrier.cuh"
@@ -926,8 +929,8 @@ mtp_status draft_one_step(const mtp_dims& D, const mtp_weights* w, const mtp_blo
   __nv_bfloat16 *c = bfp(L.c), *u = bfp(L.u), *x = bfp(L.x), *qkv = bfp(L.qkv), *o = bfp(L.o), *a = bfp(L.a),
                 *g = bfp(L.g), *sk = bfp(L.stage_k), *sv = bfp(L.stage_v);
   // acc[:, col + (0..n)] += xin · W^T for one to three linear maps of the
-  // block that share their input: bf16 weights on the swap-AB tcgen05 core,
-  // FP8 block-scaled ones in one grouped launch of the FP8 weight GEMM
+  // block that share their input, in one grouped launch: bf16 weights on the
+  // decode GEMM (decode_gemm.cu), FP8 block-scaled ones on the FP8 GEMM
   struct Map {
     const void* const* bf;
     const mtp_fp8_matrix* q8;
@@ -946,8 +949,15 @@ mtp_status draft_one_step(const mtp_dims& D, const mtp_weights* w, const mtp_blo
       }
       return mtp::fp8w_gemm_launch(segs, i, K, xin, R, ldo, base + L.f8ws, L.f8ws_bytes, st);
     }
-    for (const Map& m : maps) TRY(skinny_gemm(W0(m.bf), m.n, K, xin, R, acc + m.col, ldo, st));
-    return MTP_OK;
+    mtp::DecSeg segs[3];
+    int i = 0;
+    for (const Map& m : maps) {
+      segs[i].w = W0(m.bf);
+      segs[i].n = m.n;
+      segs[i].out = acc + m.col;
+      ++i;
+    }
+    return mtp::dgemm_bf16_launch(segs, i, K, xin, R, ldo, st);
   };
   auto q8 = [&](const mtp_fp8_matrix mtp_block_fp8::*field) { return f8 ? &(f8->*field) : nullptr; };
 

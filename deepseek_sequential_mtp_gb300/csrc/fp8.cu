@@ -48,6 +48,7 @@
 #include "fp8.cuh"
 #include "gemm_tc.cuh"
 #include "mbarrier.cuh"
+#include "tcgen05.cuh"
 
 MTP_DEFINE_ERROR_WORD(mtp_take_errors_fp8)
 
@@ -84,47 +85,6 @@ struct Args {
   int nseg, K, nkb, R, ldo, total;
 };
 
-__device__ __forceinline__ void mbar_arrive1(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Wait for the phase of `parity`; false on abort or after the wait limit.
-__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try(bar, parity)) return true;
-  const long long t0 = cycles_now();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try(bar, parity)) return true;
-    if ((it & 31u) == 0) {
-      if (*abort_flag) return false;
-      if (cycles_now() - t0 > kWaitLimitCycles) {
-        *abort_flag = 1;
-        atomicOr(&g_mtp_error_word, MTP_DEVERR_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-// Teardown wait that ignores the abort flag, bounded by `limit_cycles`.
-__device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, long long limit_cycles) {
-  const long long t0 = cycles_now();
-  while (!mbar_try(bar, parity))
-    if (cycles_now() - t0 > limit_cycles) return false;
-  return true;
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
 // D[tmem] (+)= A[smem] · B[smem]^T, kind::f8f6f4
 __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                         uint32_t accumulate) {
@@ -134,34 +94,9 @@ __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t adesc, uint64_
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// K-major tile of 128-byte rows with the 128-byte swizzle (as TMA writes it):
-// start >> 4, stride 1024 B between 8-row groups, descriptor version 1,
-// layout 2 = 128-byte swizzle; tile bases are 1024-byte aligned.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
-         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
-         (static_cast<uint64_t>(2) << 61);
-}
 // kind::f8f6f4 instruction descriptor: D fp32 (bits 4-5 = 1), A and B e4m3
 // (format 0 at bits 7-9 and 10-12), both K-major, N >> 3 at 17, M >> 4 at 24.
 constexpr uint32_t kIdesc = (1u << 4) | (static_cast<uint32_t>(kN >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
-
-// 32 consecutive fp32 TMEM columns of this thread's lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-      "tcgen05.wait::ld.sync.aligned;\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 __device__ __forceinline__ void decode(const Args& P, int i, int& sg, int& nt, int& kb) {
   sg = 0;
@@ -234,7 +169,7 @@ fp8w_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
       for (int l = 0; l < n_local; ++l) {
         const int s = l % kStages;
         const uint32_t ph = (l / kStages) & 1;
-        if (!wait_phase(empty(s), ph ^ 1u, abort_flag)) break;
+        if (!wait_phase(empty(s), ph ^ 1u, abort_flag, &g_mtp_error_word)) break;
         int sg, nt, kb;
         decode(P, lo + l, sg, nt, kb);
         const uint32_t sw = base + s * kStageBytes, sa = sw + kWBytes;
@@ -256,11 +191,11 @@ fp8w_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
     if (lane == 0) {
       for (int l = 0; l < n_local; ++l) {
         const int s = l % kStages, b = l & 1;
-        if (!wait_phase(full(s), (l / kStages) & 1, abort_flag)) break;
-        if (!wait_phase(dempty(b), ((l >> 1) & 1) ^ 1u, abort_flag)) break;
+        if (!wait_phase(full(s), (l / kStages) & 1, abort_flag, &g_mtp_error_word)) break;
+        if (!wait_phase(dempty(b), ((l >> 1) & 1) ^ 1u, abort_flag, &g_mtp_error_word)) break;
         tc_fence_after();
         const uint32_t sw = base + s * kStageBytes;
-        const uint64_t adesc = sdesc_sw128(sw + kWBytes), bdesc = sdesc_sw128(sw);
+        const uint64_t adesc = sdesc_k_sw128(sw + kWBytes), bdesc = sdesc_k_sw128(sw);
         const uint32_t d = tmem + 256 * b;
 #pragma unroll
         for (int kk = 0; kk < kKb / 32; ++kk) umma_f8(d, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, kk ? 1u : 0u);
@@ -299,7 +234,7 @@ fp8w_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
       }
       float sc2 = 0.f;
       if (l + 1 < n_local && nt2 * kN + col0 < P.seg[sg2].n) sc2 = pair_scale(sg2, nt2, kb2);
-      const bool ok = wait_phase(dfull(b), (l >> 1) & 1, abort_flag);
+      const bool ok = wait_phase(dfull(b), (l >> 1) & 1, abort_flag, &g_mtp_error_word);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       float v[32];

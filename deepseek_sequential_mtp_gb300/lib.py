@@ -110,6 +110,8 @@ def load() -> ctypes.CDLL:
     lib.mtp_draft_round_fp8.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Weights), ctypes.POINTER(BlockFp8),
                                         vp, vp, vp, vp, vp, vp, i32, ctypes.c_uint64, ctypes.c_uint64, vp, vp, vp,
                                         vp, sz, vp]
+    lib.mtp_gemm_decode_bf16.restype = i32
+    lib.mtp_gemm_decode_bf16.argtypes = [i32, i32, i32, vp, vp, vp, vp]
     lib.mtp_gemm_f32acc.restype = i32
     lib.mtp_gemm_f32acc.argtypes = [i32, i32, i32, vp, i32, i32, vp, i32, i32, vp, i32, i32, vp]
     lib.mtp_gemm_fp8w_workspace_bytes.restype = sz
@@ -250,6 +252,19 @@ class Fp8Block:
             m = getattr(self.struct, name)
             m.q = q.data_ptr()
             m.scale = sc.data_ptr()
+
+
+def gemm_decode_bf16(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor, stream=None):
+    """out[R, N] += x[R, K] @ w[N, K]^T for R <= 32 tokens (mtp_gemm_decode_bf16)."""
+    _need(x, "x", torch.bfloat16)
+    _need(w, "w", torch.bfloat16)
+    _need(out, "out", torch.float32)
+    R, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K or tuple(out.shape) != (R, N):
+        raise MtpError("gemm_decode_bf16: x [R, K], w [N, K], out [R, N]")
+    _check(load().mtp_gemm_decode_bf16(R, N, K, _ptr(x), _ptr(w), _ptr(out), _stream(stream)), "mtp_gemm_decode_bf16")
+    return out
 
 
 def gemm_f32acc(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor, a_mn=False, b_mn=False, splits=1, stream=None):

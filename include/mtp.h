@@ -95,7 +95,8 @@ enum {
   MTP_DEVERR_FROM_ATTN = 1u << 10,   /* chain attention                           */
   MTP_DEVERR_FROM_VERIFY = 1u << 11, /* spec_verify                               */
   MTP_DEVERR_FROM_DRAFT = 1u << 12,  /* draft-step kernels                        */
-  MTP_DEVERR_FROM_FP8 = 1u << 13     /* FP8 block-scaled weight GEMM              */
+  MTP_DEVERR_FROM_FP8 = 1u << 13,    /* FP8 block-scaled weight GEMM              */
+  MTP_DEVERR_FROM_DGEMM = 1u << 14   /* bf16 decode-shaped GEMM                   */
 };
 
 /* Problem sizes of one chain call.
@@ -394,6 +395,12 @@ mtp_status mtp_gemm_fp8w(int R, int N, int K, const void* x, const void* wq, con
  * K % 8 == 0; A, B, C 16-byte aligned. */
 mtp_status mtp_gemm_bf16(int M, int N, int K, const void* A, const void* B, void* C,
                          cudaStream_t stream);
+
+/* Diagnostic bf16 decode-shaped GEMM (the draft step's linear maps):
+ * out[R, N] (fp32, row stride N) += x[R, K] · W^T with x bf16 [R, K] (R in
+ * [1, 32]) and W bf16 [N, K]; K % 8 == 0, x and W 16-byte aligned. */
+mtp_status mtp_gemm_decode_bf16(int R, int N, int K, const void* x, const void* w, float* out,
+                                cudaStream_t stream);
 
 /* Diagnostic fp32-accumulating GEMM on the same core (the training step's
  * gradient GEMMs): out[M,N] (fp32, row stride ldo) += A · B^T, bf16 operands.

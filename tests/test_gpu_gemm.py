@@ -54,3 +54,22 @@ def test_f32acc_operand_layouts(a_mn, b_mn, M, N, K, splits):
     err = (out.double() - ref).abs()
     tol = 1e-5 * (A.double().abs() @ B.double().abs().T) + 1e-5 * out0.double().abs() + 1e-6
     assert bool((err <= tol).all()), f"max err {err.max().item()}"
+
+
+@pytest.mark.parametrize("R,N,K", [(1, 256, 64), (5, 200, 136), (32, 7168, 7168), (17, 1000, 2064),
+                                   (32, 18432, 7168), (3, 300, 18432)])
+def test_decode_gemm(R, N, K):
+    """The draft step's bf16 decode GEMM (weights on the N = 256 side, stream-K
+    ranges, atomics across CTAs): out += x W^T against the fp32 product of the
+    same bf16 values; ragged N and K, 1..32 tokens."""
+    g = torch.Generator(device="cuda").manual_seed(R + N + K)
+    x = torch.randn(R, K, device="cuda", generator=g).to(torch.bfloat16)
+    w = (0.05 * torch.randn(N, K, device="cuda", generator=g)).to(torch.bfloat16)
+    out0 = torch.randn(R, N, device="cuda", generator=g)
+    out = out0.clone()
+    lib.gemm_decode_bf16(x, w, out)
+    lib.check_errors()
+    ref = out0.double() + x.double() @ w.double().T
+    err = (out.double() - ref).abs()
+    tol = 1e-5 * (x.double().abs() @ w.double().abs().T) + 1e-5 * out0.double().abs() + 1e-6
+    assert bool((err <= tol).all()), f"max err {err.max().item()}"
