@@ -37,14 +37,19 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle atom row
-constexpr int kThreads = 192;
 constexpr int kGroupM = 16;
 
-template <int BN, int EPI>
+// PAIR: a cluster of two CTAs computes a 256 x BN tile with 2-SM MMAs; each
+// CTA stages its 128 rows of A and half (BN / 2 rows) of B.
+template <int BN, int EPI, bool PAIR = false>
 struct Cfg {
-  static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 10);
+  // epilogue warps: 4 (one per TMEM lane quadrant), 8 for the CE epilogue, whose
+  // exp-heavy work then splits each tile's columns between two warps per quadrant
+  static constexpr int kEpiWarps = EPI == EPI_CE ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kStages = PAIR ? 6 : (BN == 256 ? 4 : (BN == 128 ? 6 : 10));
   static constexpr int kABytes = BM * BK * 2;
-  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
   // per epilogue warp: two 32 x 64 bf16 boxes (4 KB each); none for the CE epilogue
@@ -126,6 +131,58 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+// 2-SM (CTA pair) forms.  The pair's TMEM is allocated collectively by one warp
+// of each CTA; the leader (even cluster rank) issues the MMAs, which read A
+// rows 0-127 and B rows 0..BN/2-1 from its own shared memory and the rest from
+// the peer's at the same offsets, and write each CTA's 128 accumulator rows
+// into that CTA's TMEM.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void tmem_alloc2(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive on the barrier at this offset in both CTAs of the pair when the leader's MMAs complete
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(static_cast<uint16_t>(3))
+               : "memory");
+}
+// tiled load into this CTA's shared memory that completes its bytes on the
+// leader's barrier (`bar` is a shared::cluster address)
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
@@ -214,6 +271,7 @@ struct Args {
   float* out_f32;
   int splits;
   int f32_overwrite;
+  int ce_nparts;  // CE partials per row: one per 128 vocabulary columns
   const float* lse;
   const float* ce_scale;
   int ce_offset;
@@ -309,15 +367,16 @@ __device__ __forceinline__ void rotate32(float (&x1)[32], float (&x2)[32], const
   }
 }
 
-template <int BN, int EPI, int MNF = 0>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, int EPI, int MNF = 0, bool PAIR = false>
+__global__ void __launch_bounds__(Cfg<BN, EPI, PAIR>::kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
                const __grid_constant__ CUtensorMap tmOut,
                const Args P) {
-  using C = Cfg<BN, EPI>;
+  using C = Cfg<BN, EPI, PAIR>;
   constexpr int S = C::kStages;
-  constexpr uint32_t kIdesc = idesc_bf16(BM, BN, MNF);
+  constexpr uint32_t kIdesc = idesc_bf16(PAIR ? 2 * BM : BM, BN, MNF);
+  static_assert(!PAIR || (MNF == 0 && BN == 256), "CTA pairs: K-major operands, 256-wide tiles");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -341,7 +400,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 128);
+      mbar_init(tempty_bar(a), (PAIR ? 2 : 1) * 32 * C::kEpiWarps);  // a pair: both CTAs' epilogue threads
     }
     mbar_init(final_bar, 1);
     *abort_flag = 0;
@@ -349,18 +408,32 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc2(smem_u32(tmem_slot), C::kTmemCols);
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // the peer's barriers are initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const uint32_t crank = PAIR ? cluster_ctarank() & 1u : 0u;  // 0: the leader of the pair
 
-  // work units: (tile, K split); split s covers k-blocks [kb_lo(s), kb_lo(s+1))
-  const int ntiles = P.tiles_m * P.tiles_n * P.splits;
+  // work units: (tile, K split); split s covers k-blocks [kb_lo(s), kb_lo(s+1)).  A pair
+  // takes units of two M-tiles: 2 tm2 (leader) and 2 tm2 + 1 (peer) with the same N-tile.
+  const int tiles_m_u = PAIR ? (P.tiles_m + 1) / 2 : P.tiles_m;
+  const int ntiles = tiles_m_u * P.tiles_n * P.splits;
+  const int u_first = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int u_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const int nk = P.nk;
   auto kb_lo = [&](int sp) { return static_cast<int>((static_cast<long long>(nk) * sp) / P.splits); };
+  auto unit_tile = [&](int t, int& tm, int& tn) {
+    tile_coords(t, tiles_m_u, P.tiles_n, tm, tn);
+    if constexpr (PAIR) tm = 2 * tm + static_cast<int>(crank);
+  };
 
   if (warp == 0 && lane == 0) {
     // ------------------------------ producer ------------------------------
@@ -371,16 +444,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
     for (int s = 0; s < S; ++s) { issued[s] = false; armed[s] = 0; }
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < ntiles; u += gridDim.x) {
+    const uint32_t full_leader0 = PAIR ? map_to_rank(full_bar(0), 0) : full_bar(0);
+    for (int u = u_first; ok && u < ntiles; u += u_step) {
       const int t = u / P.splits, sp = u % P.splits;
       int tm, tn;
-      tile_coords(t, P.tiles_m, P.tiles_n, tm, tn);
+      unit_tile(t, tm, tn);
       const CUtensorMap* bmap = &tmB0;
       int by;
       if constexpr (EPI == EPI_SWIGLU) {
         by = tn * (BN / 2);
+        if constexpr (PAIR) bmap = crank ? &tmB1 : &tmB0;  // the leader stages the gate rows, the peer the up rows
       } else {
-        const int n0 = tn * BN;
+        const int n0 = tn * BN + (PAIR ? static_cast<int>(crank) * (BN / 2) : 0);  // a pair splits B's rows
         const int seg = n0 / P.seg_rows;
         by = n0 - seg * P.seg_rows;
         bmap = seg == 0 ? &tmB0 : (seg == 1 ? &tmB1 : &tmB2);
@@ -389,6 +464,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
         const uint32_t sa = base + stage * C::kStageBytes;
         const uint32_t sb = sa + C::kABytes;
+        if constexpr (PAIR) {  // both CTAs' copies complete on the leader's barrier
+          const uint32_t fl = full_leader0 + 8u * stage;
+          if (crank == 0) mbar_expect_tx(full_bar(stage), 2 * C::kStageBytes);
+          tma_load_2d_pair(sa, &tmA, kb * BK, tm * BM, fl);
+          tma_load_2d_pair(sb, bmap, kb * BK, by, fl);
+          issued[stage] = true;
+          armed[stage] = phase;
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+          continue;
+        }
         mbar_expect_tx(full_bar(stage), C::kStageBytes);
         if constexpr (MNF & 1) {
 #pragma unroll
@@ -411,16 +496,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
     }
     if (*abort_flag) {  // let every copy this thread started land before the CTA exits
-      for (int s = 0; s < S; ++s)
-        if (issued[s]) mbar_wait_drain(full_bar(s), armed[s], 40000000ll);
+      if (PAIR && crank != 0) {
+        // the peer's copies complete on the leader's barrier: give them a bounded time to land
+        const long long t0 = cycles_now();
+        while (cycles_now() - t0 < 40000000ll) __nanosleep(1000);
+      } else {
+        for (int s = 0; s < S; ++s)
+          if (issued[s]) mbar_wait_drain(full_bar(s), armed[s], 40000000ll);
+      }
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1 && lane == 0 && crank == 0) {
     // ------------------------------ MMA issuer ------------------------------
     int stage = 0;
     uint32_t phase = 0;
     int local = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < ntiles; u += gridDim.x, ++local) {
+    for (int u = u_first; ok && u < ntiles; u += u_step, ++local) {
       const int sp = u % P.splits;
       const int kb0 = kb_lo(sp);
       const int acc = local & 1;
@@ -436,13 +527,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         constexpr uint64_t kStepA = (MNF & 1) ? 2048 >> 4 : 2, kStepB = (MNF & 2) ? 2048 >> 4 : 2;
         const uint64_t adesc = (MNF & 1) ? sdesc_mn_sw128(sa) : sdesc_sw128(sa);
         const uint64_t bdesc = (MNF & 2) ? sdesc_mn_sw128(sa + C::kABytes) : sdesc_sw128(sa + C::kABytes);
+        if constexpr (PAIR) {
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          umma_bf16(d_tmem, adesc + kStepA * kk, bdesc + kStepB * kk, kIdesc, (kb != kb0 || kk != 0) ? 1u : 0u);
-        umma_commit(empty_bar(stage));
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16_pair(d_tmem, adesc + kStepA * kk, bdesc + kStepB * kk, kIdesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+          umma_commit_pair(empty_bar(stage));  // frees the stage in both CTAs
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16(d_tmem, adesc + kStepA * kk, bdesc + kStepB * kk, kIdesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+          umma_commit(empty_bar(stage));
+        }
         if (++stage == S) { stage = 0; phase ^= 1u; }
       }
-      if (ok) umma_commit(tfull_bar(acc));
+      if (ok) {
+        if constexpr (PAIR) umma_commit_pair(tfull_bar(acc));
+        else umma_commit(tfull_bar(acc));
+      }
     }
   } else if (warp >= 2) {
     // ------------------------------ epilogue ------------------------------
@@ -472,10 +573,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       nb ^= 1;
     };
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < ntiles; u += gridDim.x, ++local) {
+    for (int u = u_first; ok && u < ntiles; u += u_step, ++local) {
       const int t = u / P.splits;
       int tm, tn;
-      tile_coords(t, P.tiles_m, P.tiles_n, tm, tn);
+      unit_tile(t, tm, tn);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       // residual: the first two 64-column pieces of this lane's row are fetched while the
@@ -714,26 +815,36 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
         }
       } else if constexpr (EPI == EPI_CE) {
+        // this warp's columns: [128 sub, 128 sub + 128) of the tile with 8 epilogue warps
+        constexpr int kNsub = C::kEpiWarps / 4, kChunks = BN / 32 / kNsub;
+        const int sub = (warp - 2) >> 2;
         const int lab = row_ok ? P.labels[row] : -1;
         float m_run = -INFINITY, s_run = 0.0f, zt = 0.0f;
         bool has_t = false;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = sub * kChunks; c < (sub + 1) * kChunks; ++c) {
           float v[32];
           tmem_ld32(taddr + c * 32, v);
           const int col0 = tn * BN + c * 32;
           const int valid = min(32, P.N - col0);
-          float cmax = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (i < valid) cmax = fmaxf(cmax, v[i]);
-          const float m_new = fmaxf(m_run, cmax);
-          if (m_new != -INFINITY) {
-            float sum = 0.0f;
+          if (valid < 32) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (i < valid) sum += __expf(v[i] - m_new);
-            s_run = s_run * __expf(m_run - m_new) + sum;
+              if (i >= valid) v[i] = -INFINITY;
+          }
+          // tree reductions (short dependency chains): chunk maximum, then Σ exp
+          float mx[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(fmaxf(v[i], v[i + 8]), fmaxf(v[i + 16], v[i + 24]));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) mx[i] = fmaxf(mx[i], mx[i + 4]);
+          const float cmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          const float m_new = fmaxf(m_run, cmax);
+          if (m_new != -INFINITY) {
+            float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < 32; ++i) e[i & 3] += __expf(v[i] - m_new);
+            s_run = s_run * __expf(m_run - m_new) + ((e[0] + e[1]) + (e[2] + e[3]));
             m_run = m_new;
           }
           const int off = lab - col0;
@@ -744,13 +855,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             has_t = true;
           }
         }
-        if (row_ok) {
-          P.ce_part[static_cast<size_t>(row) * P.tiles_n + tn] = make_float2(m_run, s_run);
+        const int pidx = tn * kNsub + sub;
+        if (row_ok && pidx * (BN / kNsub) < P.N) {
+          P.ce_part[static_cast<size_t>(row) * P.ce_nparts + pidx] = make_float2(m_run, s_run);
           if (has_t) P.z_tgt[row] = zt;
         }
       }
       tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
+      if constexpr (PAIR) {  // the leader's MMA warp waits for both CTAs' epilogues
+        if (crank == 0) mbar_arrive(tempty_bar(acc));
+        else mbar_arrive_remote(map_to_rank(tempty_bar(acc), 0));
+      } else {
+        mbar_arrive(tempty_bar(acc));
+      }
     }
     if constexpr (EPI != EPI_CE) {
       if (lane == 0) {
@@ -761,14 +878,30 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 
   __syncthreads();
-  if (warp == 1) {
-    if (lane == 0) {  // every MMA this CTA issued has completed before TMEM is freed
-      umma_commit(final_bar);
+  if constexpr (PAIR) {
+    // every MMA of the pair has completed (the leader's final commit reaches both CTAs)
+    // before either CTA frees its TMEM or leaves (the MMAs read both CTAs' shared memory)
+    if (warp == 1 && lane == 0) {
+      if (crank == 0) umma_commit_pair(final_bar);
       mbar_wait_drain(final_bar, 0, 40000000ll);
     }
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc2(tmem_base, C::kTmemCols);
+    }
+  } else {
+    if (warp == 1) {
+      if (lane == 0) {  // every MMA this CTA issued has completed before TMEM is freed
+        umma_commit(final_bar);
+        mbar_wait_drain(final_bar, 0, 40000000ll);
+      }
+      __syncwarp();
+      tc_fence_after();
+      tmem_dealloc(tmem_base, C::kTmemCols);
+    }
   }
 }
 
@@ -812,18 +945,18 @@ int num_sms() {
   return n;
 }
 
-template <int BN, int EPI, int MNF = 0>
+template <int BN, int EPI, int MNF = 0, bool PAIR = false>
 mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
-  using C = Cfg<BN, EPI>;
+  using C = Cfg<BN, EPI, PAIR>;
   static bool attr_done = false;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, MNF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, MNF, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return MTP_ERR_CUDA;
     attr_done = true;
   }
   CUtensorMap ta, tb[3];
-  const int box_b = EPI == EPI_SWIGLU ? BN / 2 : BN;
+  const int box_b = (EPI == EPI_SWIGLU || PAIR) ? BN / 2 : BN;  // a pair stages half of B per CTA
   // MN-major operands are [K rows][M or N] in memory, loaded as [64 x 64] boxes
   if (!((MNF & 1) ? make_map(&ta, g.A, g.K, g.M, g.lda, 64) : make_map(&ta, g.A, g.M, g.K, g.lda, BM)))
     return MTP_ERR_INVALID_ARG;
@@ -860,12 +993,31 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
   a.out_f32 = g.out_f32;
   a.splits = g.splits > 0 ? g.splits : 1;
   a.f32_overwrite = g.f32_overwrite ? 1 : 0;
+  a.ce_nparts = (g.N + BN / (C::kEpiWarps / 4) - 1) / (BN / (C::kEpiWarps / 4));
   a.lse = g.lse;
   a.ce_scale = g.ce_scale;
   a.ce_offset = g.ce_offset;
-  const int ntiles = a.tiles_m * a.tiles_n * a.splits;
-  const int grid = ntiles < num_sms() ? ntiles : num_sms();
-  gemm_tc_kernel<BN, EPI, MNF><<<grid, kThreads, C::kSmemBytes, stream>>>(ta, tb[0], tb[1], tb[2], tout, a);
+  if constexpr (PAIR) {  // clusters of two CTAs, one pair per two SMs
+    const int units = ((a.tiles_m + 1) / 2) * a.tiles_n * a.splits;
+    const int pairs = units < num_sms() / 2 ? units : num_sms() / 2;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    MTP_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EPI, MNF, PAIR>, ta, tb[0], tb[1], tb[2], tout, a));
+  } else {
+    const int ntiles = a.tiles_m * a.tiles_n * a.splits;
+    const int grid = ntiles < num_sms() ? ntiles : num_sms();
+    gemm_tc_kernel<BN, EPI, MNF><<<grid, C::kThreads, C::kSmemBytes, stream>>>(ta, tb[0], tb[1], tb[2], tout, a);
+  }
   mtp::note_launch();
   MTP_LAUNCH_CHECK();
   return MTP_OK;
@@ -873,7 +1025,7 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
 
 }  // namespace
 
-int gemm_ce_tile_n() { return 256; }
+int gemm_ce_tile_n() { return 128; }
 
 bool tensor_map_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
                         uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
@@ -923,32 +1075,39 @@ mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream) {
         if (g.nseg != 1 || g.a_mn) return MTP_ERR_UNSUPPORTED;
         return launch<256, EPI_STORE, 2>(g, stream);
       }
-      if (g.epi == EPI_STORE) return wide ? launch<256, EPI_STORE>(g, stream) : launch<128, EPI_STORE>(g, stream);
-      return wide ? launch<256, EPI_RESID>(g, stream) : launch<128, EPI_RESID>(g, stream);
+      const bool pair = wide && g.M > BM;
+      if (g.epi == EPI_STORE)
+        return pair ? launch<256, EPI_STORE, 0, true>(g, stream)
+                    : (wide ? launch<256, EPI_STORE>(g, stream) : launch<128, EPI_STORE>(g, stream));
+      return pair ? launch<256, EPI_RESID, 0, true>(g, stream)
+                  : (wide ? launch<256, EPI_RESID>(g, stream) : launch<128, EPI_RESID>(g, stream));
     }
     case EPI_ROPE: {
       const int seg = g.seg_rows > 0 ? g.seg_rows : g.N;
       if ((g.head_dim != 64 && g.head_dim != 128) || !g.pos || !g.rope || g.rope_len <= 0) return MTP_ERR_INVALID_ARG;
       if (seg % 128 || g.rope_cols % 128) return MTP_ERR_UNSUPPORTED;
-      return (seg % 256 == 0 && g.rope_cols % 256 == 0) ? launch<256, EPI_ROPE>(g, stream)
-                                                         : launch<128, EPI_ROPE>(g, stream);
+      if (seg % 256 == 0 && g.rope_cols % 256 == 0)
+        return g.M > BM ? launch<256, EPI_ROPE, 0, true>(g, stream) : launch<256, EPI_ROPE>(g, stream);
+      return launch<128, EPI_ROPE>(g, stream);
     }
     case EPI_SWIGLU:
       if (!g.B[1] || !aligned16(g.B[1])) return MTP_ERR_INVALID_ARG;
-      return launch<256, EPI_SWIGLU>(g, stream);
+      return g.M > BM ? launch<256, EPI_SWIGLU, 0, true>(g, stream) : launch<256, EPI_SWIGLU>(g, stream);
     case EPI_CE:
       if (!g.labels || !g.ce_part || !g.z_tgt) return MTP_ERR_INVALID_ARG;
-      return launch<256, EPI_CE>(g, stream);
+      return g.M > BM ? launch<256, EPI_CE, 0, true>(g, stream) : launch<256, EPI_CE>(g, stream);
     case EPI_CE_GRAD:
     case EPI_CE_GRAD_T:
       if (!g.labels || !g.lse || !g.ce_scale) return MTP_ERR_INVALID_ARG;
-      return g.epi == EPI_CE_GRAD ? launch<256, EPI_CE_GRAD>(g, stream) : launch<256, EPI_CE_GRAD_T>(g, stream);
+      if (g.epi == EPI_CE_GRAD)
+        return g.M > BM ? launch<256, EPI_CE_GRAD, 0, true>(g, stream) : launch<256, EPI_CE_GRAD>(g, stream);
+      return launch<256, EPI_CE_GRAD_T>(g, stream);
     case EPI_F32_ACC: {
       if (!g.out_f32 || g.ldo % 4 || !aligned16(g.out_f32)) return MTP_ERR_INVALID_ARG;
       const int nk = (g.K + BK - 1) / BK;
       if (g.splits < 1 || g.splits > nk || g.nseg != 1) return MTP_ERR_INVALID_ARG;
       switch ((g.a_mn ? 1 : 0) | (g.b_mn ? 2 : 0)) {
-        case 0: return launch<256, EPI_F32_ACC, 0>(g, stream);
+        case 0: return g.M > BM ? launch<256, EPI_F32_ACC, 0, true>(g, stream) : launch<256, EPI_F32_ACC, 0>(g, stream);
         case 1: return launch<256, EPI_F32_ACC, 1>(g, stream);
         case 2: return launch<256, EPI_F32_ACC, 2>(g, stream);
         default: return launch<256, EPI_F32_ACC, 3>(g, stream);
