@@ -43,7 +43,6 @@ namespace {
 
 constexpr int kMaxR = 32;
 
-__device__ __forceinline__ float bf(const __nv_bfloat16& v) { return __bfloat162float(v); }
 
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon et al., SC'11) -- the draw uses word 2

@@ -301,20 +301,6 @@ __device__ __forceinline__ void box_write32(uint8_t* box, int lane, int half, co
     *reinterpret_cast<uint4*>(box + lane * 128 + ((c ^ (lane & 7)) << 4)) = *reinterpret_cast<uint4*>(h);
   }
 }
-__device__ __forceinline__ void box_add32(const uint8_t* box, int lane, int half, float (&v)[32]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int c = half * 4 + q;
-    uint4 u = *reinterpret_cast<const uint4*>(box + lane * 128 + ((c ^ (lane & 7)) << 4));
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __bfloat1622float2(h[i]);
-      v[8 * q + 2 * i] += f.x;
-      v[8 * q + 2 * i + 1] += f.y;
-    }
-  }
-}
 // 64 residual columns [col0, col0 + 64) of one row as 8 x (8 bf16); zero outside [0, M) x [0, N)
 __device__ __forceinline__ void load_res64(uint4 (&r)[8], const __nv_bfloat16* resid, int ldr, int M, int N, int row,
                                            int col0) {
