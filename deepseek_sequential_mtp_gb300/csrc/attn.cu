@@ -113,6 +113,13 @@ flash_attn_bf16_kernel(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16* __r
   const int row_a = q0 + warp * 16 + g, row_b = row_a + 8;
   const int st_a = row_a < T ? ss[row_a] : row_a;
   const int st_b = row_b < T ? ss[row_b] : row_b;
+  // a k-block at or past every row's segment start and wholly below the warp's first row
+  // needs no mask (skipping invisible 16-key groups instead was measured slower: the
+  // branches break the unrolled MMA schedule)
+  int st_max = max(st_a, st_b);
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) st_max = max(st_max, __shfl_xor_sync(0xffffffffu, st_max, o));
+  const int wrow0 = q0 + warp * 16;
 
   uint32_t qa[HD / 16][4];
   float o[HD / 8][4];
@@ -140,6 +147,7 @@ flash_attn_bf16_kernel(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16* __r
     const uint32_t sV = sV0 + buf * kBK * HD * 2;
 
     // S = Q K^T : 16 rows x 64 keys per warp
+    const int kbase = kb * kBK;
     float s[8][4];
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
@@ -155,17 +163,29 @@ flash_attn_bf16_kernel(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16* __r
       }
     }
     // mask, scale, online softmax
-    const int kbase = kb * kBK;
     float mx_a = -INFINITY, mx_b = -INFINITY;
+    if (kbase >= st_max && kbase + kBK - 1 <= wrow0) {  // every key visible to every row of the warp
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int key = kbase + nt * 8 + 2 * tq + e;
-        s[nt][e] = (key >= st_a && key <= row_a) ? s[nt][e] * scale_log2 : -INFINITY;
-        s[nt][2 + e] = (key >= st_b && key <= row_b) ? s[nt][2 + e] * scale_log2 : -INFINITY;
-        mx_a = fmaxf(mx_a, s[nt][e]);
-        mx_b = fmaxf(mx_b, s[nt][2 + e]);
+        for (int e = 0; e < 2; ++e) {
+          s[nt][e] *= scale_log2;
+          s[nt][2 + e] *= scale_log2;
+          mx_a = fmaxf(mx_a, s[nt][e]);
+          mx_b = fmaxf(mx_b, s[nt][2 + e]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int key = kbase + nt * 8 + 2 * tq + e;
+          s[nt][e] = (key >= st_a && key <= row_a) ? s[nt][e] * scale_log2 : -INFINITY;
+          s[nt][2 + e] = (key >= st_b && key <= row_b) ? s[nt][2 + e] * scale_log2 : -INFINITY;
+          mx_a = fmaxf(mx_a, s[nt][e]);
+          mx_b = fmaxf(mx_b, s[nt][2 + e]);
+        }
       }
     }
     mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
