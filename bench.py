@@ -307,7 +307,8 @@ def run_ours(args):
     out = {"sums_counts": torch.empty(2 * (cfg.D + 1), dtype=torch.float64, device=dev),
            "losses": torch.empty(cfg.D + 2, dtype=torch.float32, device=dev)}
     K, W = args.steps, args.warmup
-    vouts = torch.empty((K + W, 4, vcfg.R), dtype=torch.int32, device=dev)
+    KB = min(K, 20)  # steps of the per-kernel breakdown pass
+    vouts = torch.empty((K + W + KB, 4, vcfg.R), dtype=torch.int32, device=dev)
     flush = L2Flush(dev)
     global_losses = torch.empty(cfg.D + 2, dtype=torch.float32, device=dev)
 
@@ -327,10 +328,12 @@ def run_ours(args):
     torch.cuda.synchronize()
     lib.check_errors()
 
-    timers = {name: lib.KernelTimer(name, launches * K)
-              for name, launches in (("head_ce_gemm", cfg.D + 1), ("gate_up_gemm", cfg.D), ("down_gemm", cfg.D),
-                                     ("qkv_gemm", cfg.D), ("o_gemm", cfg.D), ("proj_gemm", cfg.D),
-                                     ("attention", cfg.D), ("spec_verify", 1), ("prologue", cfg.D))}
+    # only the dominant kernel's event timer is armed in the timed loop: an event record between two
+    # kernels costs ~2 us of stream time and stops the next launch from overlapping its predecessor
+    launches_per_step = (("head_ce_gemm", cfg.D + 1), ("gate_up_gemm", cfg.D), ("down_gemm", cfg.D),
+                         ("qkv_gemm", cfg.D), ("o_gemm", cfg.D), ("proj_gemm", cfg.D), ("attention", cfg.D),
+                         ("spec_verify", 1), ("prologue", cfg.D))
+    timers = {"head_ce_gemm": lib.KernelTimer("head_ce_gemm", (cfg.D + 1) * K)}
     torch.cuda.synchronize()
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -367,11 +370,30 @@ def run_ours(args):
     tokens_per_step = sum(cfg.B * (cfg.T - k) for k in range(1, cfg.D + 1))
     value = world * tokens_per_step / (step_ms_max / 1e3)
 
-    # per-kernel durations measured inside the timed region
-    kern = {name: t.durations_ms() for name, t in timers.items()}
+    head_ms = timers["head_ce_gemm"].durations_ms()  # measured inside the timed region
+
+    # per-kernel breakdown: a separate pass of KB steps with every kernel class's timer armed
+    btimers = {name: lib.KernelTimer(name, n * KB) for name, n in launches_per_step}
+    torch.cuda.synchronize()
+    for t in btimers.values():
+        t.arm()
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b_ms = 0.0
+    for i in range(KB):
+        flush()
+        b0.record()
+        step(W + K + i)
+        b1.record()
+        b1.synchronize()
+        b_ms += b0.elapsed_time(b1)
+    lib.KernelTimer.disarm_all()
+    lib.check_errors()
+    kern = {name: t.durations_ms() for name, t in btimers.items()}
+    kern["head_ce_gemm"] = head_ms
+    kern_steps = {name: KB for name in kern}
+    kern_steps["head_ce_gemm"] = K
     counts = out["sums_counts"][1::2].cpu().numpy()  # supervised rows per term (same every step)
     peaks, peak_src = load_peaks()
-    head_ms = kern["head_ce_gemm"]
     # algorithmic FLOPs of the head GEMM: 2 d V per supervised row, for main + each depth
     head_flops_step = 2.0 * cfg.d * cfg.V * float(counts.sum())
     head_ms_step = sum(head_ms) / K
@@ -395,8 +417,8 @@ def run_ours(args):
                "proj_gemm": 4 * d * d}
     breakdown = {}
     for name, ms in kern.items():
-        tot = sum(ms) / K
-        entry = {"ms_per_step": tot, "launches_per_step": len(ms) / K}
+        tot = sum(ms) / kern_steps[name]
+        entry = {"ms_per_step": tot, "launches_per_step": len(ms) / kern_steps[name]}
         if name in per_row:
             fl = per_row[name] * state_rows
             entry["tflops"] = fl / (tot / 1e3) / 1e12 if tot > 0 else None
@@ -411,13 +433,15 @@ def run_ours(args):
         breakdown[name] = entry
 
     # spec_verify: rows/s and algorithmic HBM bytes (decision scalars + the one sampled row pair or row)
-    vo = vouts[W:].cpu().numpy()
+    vo = vouts[W:W + K].cpu().numpy()
     acc, st = vo[:, 0], vo[:, 3]
-    n_tok = vo[:, 1]
-    rej = (acc < vcfg.gamma) & (n_tok >= 0)
-    bonus = (acc == vcfg.gamma) & (n_tok >= 0)
-    examined = np.minimum(acc + 1, vcfg.gamma)
-    vbytes = (8.0 * examined + 8.0 * vcfg.V * rej + 4.0 * vcfg.V * bonus).sum(axis=1)  # per call
+    # the calls timed are those of the breakdown pass: their bytes
+    vb = vouts[W + K:].cpu().numpy()
+    b_acc, b_tok = vb[:, 0], vb[:, 1]
+    b_rej = (b_acc < vcfg.gamma) & (b_tok >= 0)
+    b_bonus = (b_acc == vcfg.gamma) & (b_tok >= 0)
+    examined = np.minimum(b_acc + 1, vcfg.gamma)
+    vbytes = (8.0 * examined + 8.0 * vcfg.V * b_rej + 4.0 * vcfg.V * b_bonus).sum(axis=1)  # per call
     v_ms = kern["spec_verify"]
     v_ms_mean = sum(v_ms) / len(v_ms)
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -463,7 +487,11 @@ def run_ours(args):
                 "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic (seeded; random-init weights of the workload's shapes)",
                 "config": workload_config(), "roofline": roofline, "spec_verify": verify,
-                "spec_verify_rows_per_s": verify["rows_per_s"], "kernels": breakdown, "draft_step": draft, "dsv3_width": dsv3, "train_step": train,
+                "spec_verify_rows_per_s": verify["rows_per_s"], "kernels": breakdown,
+                "kernels_pass": {"steps": KB, "ms_per_step_all_timers": b_ms / KB,
+                                 "note": "per-kernel times other than head_ce_gemm come from this separate pass "
+                                         "with an event pair around every launch"},
+                "draft_step": draft, "dsv3_width": dsv3, "train_step": train,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
                 "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
                 "clock_samples": clk["samples"], "wall_s_timed_region": t_wall,

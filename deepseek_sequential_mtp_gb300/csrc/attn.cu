@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(kThreads)
 flash_attn_bf16_kernel(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16* __restrict__ out,
                        const int32_t* __restrict__ seg_start, int T, int H, float scale_log2,
                        float* __restrict__ lse2_out) {
+  pdl_trigger();  // the output projection that follows may start its setup
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sQ = smem_u32(smem);
   const uint32_t sK0 = sQ + kBQ * HD * 2;

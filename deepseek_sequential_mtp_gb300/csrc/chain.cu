@@ -192,6 +192,7 @@ __global__ void prologue_bf16_kernel(const uint4* __restrict__ h_prev, const int
                                      const uint4* __restrict__ embed, const uint4* __restrict__ g_h,
                                      const uint4* __restrict__ g_e, uint4* __restrict__ c, int M, int Tlen, int d8,
                                      int V, int k, float eps) {
+  mtp::pdl_trigger();  // a GEMM that follows may start its setup
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= M) return;
   const int m = warp;
@@ -241,6 +242,7 @@ __global__ void rmsnorm_bf16_kernel(const uint4* __restrict__ x, const uint4* __
                                     int M, int d8, float eps, const int32_t* __restrict__ tokens,
                                     const int32_t* __restrict__ seg, const int32_t* __restrict__ seg_end,
                                     int32_t* __restrict__ labels, int Tlen, int k, int V) {
+  mtp::pdl_trigger();  // a GEMM that follows may start its setup
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= M) return;
   const uint4* xr = x + static_cast<size_t>(warp) * d8;
@@ -261,6 +263,7 @@ __global__ void rmsnorm_bf16_kernel(const uint4* __restrict__ x, const uint4* __
 // reduced modulo 2*pi in double (a handful of FP64 instructions), then the
 // fp32 sine and cosine of the reduced angle are taken.
 __global__ void rope_table_kernel(float2* __restrict__ tab, int T, int half, int hd, double base) {
+  mtp::pdl_trigger();  // a GEMM that follows may start its setup
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= T * half) return;
   const int p = i / half, j = i % half;
@@ -277,6 +280,7 @@ __global__ void rope_table_kernel(float2* __restrict__ tab, int T, int half, int
 __global__ void labels_kernel(const int32_t* __restrict__ tokens, const int32_t* __restrict__ seg,
                               const int32_t* __restrict__ seg_end, int32_t* __restrict__ labels, int M, int Tlen,
                               int k, int V) {
+  mtp::pdl_trigger();  // a GEMM that follows may start its setup
   const int m = blockIdx.x * blockDim.x + threadIdx.x;
   if (m >= M) return;
   const int t = m % Tlen;
@@ -389,6 +393,7 @@ __global__ void head_ce_f32_kernel(const float* __restrict__ x, const float* __r
 __global__ void ce_reduce_kernel(int M, int nvt, const float2* __restrict__ part, const float* __restrict__ zt,
                                  const int32_t* __restrict__ labels, float* __restrict__ row_loss,
                                  double* __restrict__ sum_count, float* __restrict__ lse_out) {
+  mtp::pdl_trigger();  // a GEMM that follows may start its setup
   __shared__ float s_loss[8];
   __shared__ int s_sup[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -590,6 +595,7 @@ mtp_status gemm<__nv_bfloat16>(const Ctx& C, const __nv_bfloat16* A, int lda, co
   g.ldo = ldo;
   g.resid = resid;
   g.ldr = ldr;
+  g.pdl = true;  // every forward-chain GEMM follows one of this library's kernels
   if (epi == mtp::EPI_ROPE) {
     g.pos = C.pos;
     g.rope = C.buf<float2>(C.L.rope);
@@ -681,6 +687,7 @@ mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double
     g.labels = labels;
     g.ce_part = part;
     g.z_tgt = zt;
+    g.pdl = true;  // follows the RMSNorm kernel
     mtp::prof_begin(MTP_KC_HEAD_CE_GEMM, C.st);
     TRY(mtp::gemm_bf16_launch(g, C.st));
     mtp::prof_end(MTP_KC_HEAD_CE_GEMM, C.st);
@@ -930,6 +937,7 @@ rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, int ld_h, const int32_t*
                    const __nv_bfloat16* __restrict__ g, const float* __restrict__ dy, int ld_dy, float* __restrict__ dh,
                    int ld_dh, const int32_t* __restrict__ dh_rows, float* __restrict__ dg_part, int M, int d,
                    float eps) {
+  mtp::pdl_trigger();  // a GEMM that follows may start its setup
   __shared__ float s_r[kNormBwdRows], s_mean[kNormBwdRows];
   __shared__ int s_hrow[kNormBwdRows], s_dhrow[kNormBwdRows];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1006,6 +1014,7 @@ rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, int ld_h, const int32_t*
 // pieces) and combine their sums in shared memory
 __global__ void __launch_bounds__(256) colsum_add_kernel(const float* __restrict__ part, int nb, int d,
                                                          float* __restrict__ dg) {
+  mtp::pdl_trigger();  // a GEMM that follows may start its setup
   __shared__ float s_sum[8][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x * 32 + lane;
@@ -1077,6 +1086,9 @@ TrainLayout make_train_layout(const mtp_dims& D) {
   return T;
 }
 
+// out (+)= A B^T in fp32 (declared here, defined with the block backward).  The
+// GEMM is launched for programmatic dependent launch, so the stream's previous
+// operation must be a kernel (not a memset or a copy).
 mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, bool a_mn, const __nv_bfloat16* B, int ldb,
                     bool b_mn, float* out, int ldo, cudaStream_t st, bool overwrite = false);
 
@@ -1124,6 +1136,7 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
     g.lse = lse;
     g.ce_scale = scale;
     g.ce_offset = v0;
+    g.pdl = true;  // follows the RMSNorm kernel or the previous chunk's GEMM
     TRY(mtp::gemm_bf16_launch(g, C.st));
     // dX += dz W_U[v0 : v0 + vc] (W_U rows read as the MN-major B operand)
     TRY(gemm_acc(M, d, vc, dz, T.vc, false, WU + static_cast<size_t>(v0) * d, d, true, dx, d, C.st, v0 == 0));
@@ -1144,6 +1157,7 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
 // stride over matrix rows, threads over columns (no per-element division)
 __global__ void f32_to_bf16_kernel(const float* __restrict__ x, int ldx, __nv_bfloat16* __restrict__ y, int ldy, int R,
                                    int Cn) {
+  mtp::pdl_trigger();  // a GEMM that follows may start its setup
   for (int r = blockIdx.x; r < R; r += gridDim.x) {
     const float* xr = x + static_cast<size_t>(r) * ldx;
     __nv_bfloat16* yr = y + static_cast<size_t>(r) * ldy;
@@ -1159,6 +1173,7 @@ void f32_to_bf16(const float* x, int ldx, __nv_bfloat16* y, int ldy, int R, int 
 // bf16) and dg ([M, ffn] fp32): g = silu(p) q, dp = dg q silu'(p), dq = dg silu(p)
 __global__ void swiglu_bwd_kernel(const __nv_bfloat16* __restrict__ pq, const float* __restrict__ dg,
                                   __nv_bfloat16* __restrict__ g, __nv_bfloat16* __restrict__ dpq, int M, int ffn) {
+  mtp::pdl_trigger();  // a GEMM that follows may start its setup
   for (int m = blockIdx.x; m < M; m += gridDim.x) {
     const __nv_bfloat16* pr = pq + static_cast<size_t>(m) * 2 * ffn;
     const float* dgr = dg + static_cast<size_t>(m) * ffn;
@@ -1182,6 +1197,7 @@ __global__ void swiglu_bwd_kernel(const __nv_bfloat16* __restrict__ pq, const fl
 __global__ void rope_bwd_kernel(const float* __restrict__ dqkv, const float2* __restrict__ rope,
                                 const int32_t* __restrict__ pos, __nv_bfloat16* __restrict__ out, int M, int d, int hd,
                                 int Tlen, int use_rope) {
+  mtp::pdl_trigger();  // a GEMM that follows may start its setup
   const int half = hd / 2;
   for (int m = blockIdx.x; m < M; m += gridDim.x) {
     const float* src = dqkv + static_cast<size_t>(m) * 3 * d;
@@ -1305,11 +1321,14 @@ mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, bool a
     if (eff >= 0.9) break;
   }
   g.splits = splits;
+  g.pdl = true;
   if (overwrite) {  // out = A B^T: one split stores directly, several add into a zeroed output
-    if (splits == 1)
+    if (splits == 1) {
       g.f32_overwrite = true;
-    else
+    } else {
       MTP_CUDA_TRY(cudaMemset2DAsync(out, static_cast<size_t>(ldo) * 4, 0, static_cast<size_t>(N) * 4, M, st));
+      g.pdl = false;  // a memset precedes the GEMM
+    }
   }
   return mtp::gemm_bf16_launch(g, st);
 }
@@ -1346,11 +1365,13 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
     g.epi = mtp::EPI_STORE;
     g.out = bb(B.pq);
     g.ldo = 2 * f;
+    g.pdl = true;  // follows the conversion kernel
     TRY(mtp::gemm_bf16_launch(g, st));
     g = gdesc(M, f, d, y, d, wt(C.W.w_up), d);
     g.epi = mtp::EPI_STORE;
     g.out = bb(B.pq) + f;
     g.ldo = 2 * f;
+    g.pdl = true;
     TRY(mtp::gemm_bf16_launch(g, st));
   }
   TRY(gemm_acc(M, f, d, bb(B.dhb), d, false, wt(C.W.w_down), f, true, fb(B.dgf), f, st, true));
@@ -1376,6 +1397,7 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
     g.epi = mtp::EPI_STORE;
     g.out = bb(B.dob);
     g.ldo = d;
+    g.pdl = true;  // follows a GEMM or the conversion kernel
     TRY(mtp::gemm_bf16_launch(g, st));
   }
   // segment-causal attention backward (tensor cores), then RoPE backward

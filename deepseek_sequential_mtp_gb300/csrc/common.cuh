@@ -50,6 +50,15 @@ constexpr long long kWaitLimitCycles = 3000000000ll;
 
 __device__ __forceinline__ long long cycles_now() { return clock64(); }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the previous kernel of the stream is still
+// running; it must call pdl_wait() before its first access to memory that
+// earlier kernels write (the wait returns once they have completed and their
+// writes are visible).  pdl_trigger() lets such a dependent start early; a
+// kernel that never calls it releases its dependent at completion.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ float bf16_to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
 __device__ __forceinline__ __nv_bfloat16 f32_to_bf16(float v) { return __float2bfloat16_rn(v); }
 

@@ -380,6 +380,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
+    // the tensor maps are launch parameters: fetch them while an earlier kernel may still run
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB0)) : "memory");
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
@@ -407,6 +410,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t crank = PAIR ? cluster_ctarank() & 1u : 0u;  // 0: the leader of the pair
+  // setup above overlaps the previous kernel (programmatic dependent launch); every
+  // access to global memory below follows its completion.  This kernel releases its
+  // own dependents only by completing: with an explicit early release the backward
+  // pass's results came out wrong on GB300 (cause not identified), and the release
+  // bought no measurable time.
+  pdl_wait();
 
   // work units: (tile, K split); split s covers k-blocks [kb_lo(s), kb_lo(s+1)).  A pair
   // takes units of two M-tiles: 2 tm2 (leader) and 2 tm2 + 1 (peer) with the same N-tile.
@@ -991,18 +1000,29 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = g.pdl ? 2 : 1;
     MTP_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EPI, MNF, PAIR>, ta, tb[0], tb[1], tb[2], tout, a));
   } else {
     const int ntiles = a.tiles_m * a.tiles_n * a.splits;
-    const int grid = ntiles < num_sms() ? ntiles : num_sms();
-    gemm_tc_kernel<BN, EPI, MNF><<<grid, C::kThreads, C::kSmemBytes, stream>>>(ta, tb[0], tb[1], tb[2], tout, a);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(ntiles < num_sms() ? ntiles : num_sms());
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g.pdl ? 1 : 0;
+    MTP_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EPI, MNF, PAIR>, ta, tb[0], tb[1], tb[2], tout, a));
   }
   mtp::note_launch();
   MTP_LAUNCH_CHECK();

@@ -51,6 +51,9 @@ struct GemmDesc {
   bool a_mn = false, b_mn = false;
   // EPI_F32_ACC with one split: store instead of adding (the output's first product)
   bool f32_overwrite = false;
+  // programmatic dependent launch: the kernel's setup may overlap the stream's previous
+  // kernel.  Only for launches whose stream predecessor is a kernel (not a memset or copy).
+  bool pdl = false;
   __nv_bfloat16* out = nullptr;
   int ldo = 0;
   const __nv_bfloat16* resid = nullptr;
