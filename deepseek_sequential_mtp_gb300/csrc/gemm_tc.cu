@@ -43,9 +43,10 @@ constexpr int kGroupM = 16;
 // CTA stages its 128 rows of A and half (BN / 2 rows) of B.
 template <int BN, int EPI, bool PAIR = false>
 struct Cfg {
-  // epilogue warps: 4 (one per TMEM lane quadrant), 8 for the CE epilogue, whose
-  // exp-heavy work then splits each tile's columns between two warps per quadrant
-  static constexpr int kEpiWarps = EPI == EPI_CE ? 8 : 4;
+  // epilogue warps: 4, one per TMEM lane quadrant.  (Eight, two per quadrant with
+  // half of the columns each, finish the CE epilogue sooner but slow the concurrent
+  // MMAs of the next tile more: the head GEMM measured 3% slower with them.)
+  static constexpr int kEpiWarps = 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kStages = PAIR ? 6 : (BN == 256 ? 4 : (BN == 128 ? 6 : 10));
   static constexpr int kABytes = BM * BK * 2;
@@ -271,7 +272,7 @@ struct Args {
   float* out_f32;
   int splits;
   int f32_overwrite;
-  int ce_nparts;  // CE partials per row: one per 128 vocabulary columns
+  int ce_nparts;  // CE partials per row: one per gemm_ce_tile_n() vocabulary columns
   const float* lse;
   const float* ce_scale;
   int ce_offset;
@@ -810,7 +811,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
         }
       } else if constexpr (EPI == EPI_CE) {
-        // this warp's columns: [128 sub, 128 sub + 128) of the tile with 8 epilogue warps
+        // this warp's columns: [BN/kNsub · sub, BN/kNsub · (sub + 1)) of the tile
         constexpr int kNsub = C::kEpiWarps / 4, kChunks = BN / 32 / kNsub;
         const int sub = (warp - 2) >> 2;
         const int lab = row_ok ? P.labels[row] : -1;
@@ -836,10 +837,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const float cmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
           const float m_new = fmaxf(m_run, cmax);
           if (m_new != -INFINITY) {
+            // exp(v - m) = 2^(v log2e - m log2e): one FFMA and one exp2 per element
             float e[4] = {0.f, 0.f, 0.f, 0.f};
+            const float ml2 = m_new * 1.4426950408889634f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) e[i & 3] += __expf(v[i] - m_new);
-            s_run = s_run * __expf(m_run - m_new) + ((e[0] + e[1]) + (e[2] + e[3]));
+            for (int i = 0; i < 32; ++i) e[i & 3] += exp2f(fmaf(v[i], 1.4426950408889634f, -ml2));
+            s_run = s_run * exp2f((m_run - m_new) * 1.4426950408889634f) + ((e[0] + e[1]) + (e[2] + e[3]));
             m_run = m_new;
           }
           const int off = lab - col0;
@@ -1031,7 +1034,7 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
 
 }  // namespace
 
-int gemm_ce_tile_n() { return 128; }
+int gemm_ce_tile_n() { return 256 / (Cfg<256, EPI_CE, true>::kEpiWarps / 4); }
 
 bool tensor_map_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
                         uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
