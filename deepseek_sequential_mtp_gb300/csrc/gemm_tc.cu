@@ -38,6 +38,7 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle atom row
 constexpr int kGroupM = 16;
+static_assert((kGroupM & (kGroupM - 1)) == 0, "tile_coords masks by kGroupM - 1");
 
 // PAIR: a cluster of two CTAs computes a 256 x BN tile with 2-SM MMAs; each
 // CTA stages its 128 rows of A and half (BN / 2 rows) of B.
@@ -284,8 +285,13 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   const int first_m = group * kGroupM;
   const int gsz = min(tiles_m - first_m, kGroupM);
   const int r = t - group * per_group;
-  tm = first_m + r % gsz;
-  tn = r / gsz;
+  if (gsz == kGroupM) {  // every group but a ragged last one: shifts, no division
+    tm = first_m + (r & (kGroupM - 1));
+    tn = r / kGroupM;
+  } else {
+    tm = first_m + r % gsz;
+    tn = r / gsz;
+  }
 }
 
 // A 32-row x 64-column bf16 box in shared memory with the 128-byte swizzle
@@ -425,7 +431,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int u_first = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int u_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const int nk = P.nk;
-  auto kb_lo = [&](int sp) { return static_cast<int>((static_cast<long long>(nk) * sp) / P.splits); };
+  const int splits = P.splits;  // nk * splits < 2^31: 32-bit index arithmetic throughout
+  auto kb_lo = [&](int sp) { return splits == 1 ? (sp == 0 ? 0 : nk) : (nk * sp) / splits; };
   auto unit_tile = [&](int t, int& tm, int& tn) {
     tile_coords(t, tiles_m_u, P.tiles_n, tm, tn);
     if constexpr (PAIR) tm = 2 * tm + static_cast<int>(crank);
@@ -442,7 +449,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     bool ok = true;
     const uint32_t full_leader0 = PAIR ? map_to_rank(full_bar(0), 0) : full_bar(0);
     for (int u = u_first; ok && u < ntiles; u += u_step) {
-      const int t = u / P.splits, sp = u % P.splits;
+      const int t = splits == 1 ? u : u / splits, sp = splits == 1 ? 0 : u % splits;
       int tm, tn;
       unit_tile(t, tm, tn);
       const CUtensorMap* bmap = &tmB0;
@@ -452,11 +459,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if constexpr (PAIR) bmap = crank ? &tmB1 : &tmB0;  // the leader stages the gate rows, the peer the up rows
       } else {
         const int n0 = tn * BN + (PAIR ? static_cast<int>(crank) * (BN / 2) : 0);  // a pair splits B's rows
-        const int seg = n0 / P.seg_rows;
+        const int seg = n0 < P.seg_rows ? 0 : (n0 < 2 * P.seg_rows ? 1 : 2);  // at most three segments
         by = n0 - seg * P.seg_rows;
         bmap = seg == 0 ? &tmB0 : (seg == 1 ? &tmB1 : &tmB2);
       }
-      for (int kb = kb_lo(sp); kb < kb_lo(sp + 1); ++kb) {
+      const int kb_end = kb_lo(sp + 1);
+      for (int kb = kb_lo(sp); kb < kb_end; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
         const uint32_t sa = base + stage * C::kStageBytes;
         const uint32_t sb = sa + C::kABytes;
@@ -508,14 +516,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     int local = 0;
     bool ok = true;
     for (int u = u_first; ok && u < ntiles; u += u_step, ++local) {
-      const int sp = u % P.splits;
-      const int kb0 = kb_lo(sp);
+      const int sp = splits == 1 ? 0 : u % splits;
+      const int kb0 = kb_lo(sp), kb_end = kb_lo(sp + 1);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
-      for (int kb = kb0; kb < kb_lo(sp + 1); ++kb) {
+      for (int kb = kb0; kb < kb_end; ++kb) {
         if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sa = base + stage * C::kStageBytes;
@@ -570,7 +578,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     };
     bool ok = true;
     for (int u = u_first; ok && u < ntiles; u += u_step, ++local) {
-      const int t = u / P.splits;
+      const int t = splits == 1 ? u : u / splits;
       int tm, tn;
       unit_tile(t, tm, tn);
       const int acc = local & 1;
@@ -1062,7 +1070,9 @@ bool tensor_map_u8_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t c
 
 mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return MTP_ERR_SHAPE;
-  if (!g.A || !g.B[0]) return MTP_ERR_INVALID_ARG;
+  if (!g.A || !g.B[0] || g.nseg < 1 || g.nseg > 3) return MTP_ERR_INVALID_ARG;
+  // B's segments must cover the N columns (the kernel picks a column's segment by comparison)
+  if (g.seg_rows > 0 && static_cast<long long>(g.seg_rows) * g.nseg < g.N) return MTP_ERR_SHAPE;
   // TMA needs 16-byte row strides; a K extent that is not a multiple of the
   // k-block is zero-filled by the copies
   if (g.lda % 8 || g.ldb % 8) return MTP_ERR_ALIGNMENT;
