@@ -309,6 +309,10 @@ __device__ __forceinline__ void box_write32(uint8_t* box, int lane, int half, co
   }
 }
 // 64 residual columns [col0, col0 + 64) of one row as 8 x (8 bf16); zero outside [0, M) x [0, N)
+// Fetch `bytes` (a multiple of 16, from a 16-byte aligned address) into L2 without waiting.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void load_res64(uint4 (&r)[8], const __nv_bfloat16* resid, int ldr, int M, int N, int row,
                                            int col0) {
   const __nv_bfloat16* src = resid + static_cast<size_t>(row) * ldr + col0;
@@ -588,6 +592,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint4 rq[2][8];
       if constexpr (EPI == EPI_RESID) {
         const int rrow = tm * BM + quarter * 32 + lane;
+        // the whole row piece of the tile goes to L2 now, so that pieces 2 and 3, read during
+        // the epilogue, do not queue DRAM misses behind the next tile's operand loads
+        if (rrow < P.M) {
+          const uint32_t bytes = static_cast<uint32_t>(2 * min(BN, P.N - tn * BN)) & ~15u;
+          if (bytes) prefetch_l2_bulk(P.resid + static_cast<size_t>(rrow) * P.ldr + tn * BN, bytes);
+        }
         load_res64(rq[0], P.resid, P.ldr, P.M, P.N, rrow, tn * BN);
         load_res64(rq[1], P.resid, P.ldr, P.M, P.N, rrow, tn * BN + 64);
       }
