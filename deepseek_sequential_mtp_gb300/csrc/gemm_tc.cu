@@ -373,7 +373,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   using C = Cfg<BN, EPI, PAIR>;
   constexpr int S = C::kStages;
   constexpr uint32_t kIdesc = idesc_bf16(PAIR ? 2 * BM : BM, BN, MNF);
-  static_assert(!PAIR || (MNF == 0 && BN == 256), "CTA pairs: K-major operands, 256-wide tiles");
+  static_assert(!PAIR || BN == 256, "CTA pairs: 256-wide tiles");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -475,8 +475,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if constexpr (PAIR) {  // both CTAs' copies complete on the leader's barrier
           const uint32_t fl = full_leader0 + 8u * stage;
           if (crank == 0) mbar_expect_tx(full_bar(stage), 2 * C::kStageBytes);
-          tma_load_2d_pair(sa, &tmA, kb * BK, tm * BM, fl);
-          tma_load_2d_pair(sb, bmap, kb * BK, by, fl);
+          if constexpr (MNF & 1) {  // this CTA's 128 rows of A as two [64 M x 64 k] boxes
+#pragma unroll
+            for (int c = 0; c < BM / 64; ++c) tma_load_2d_pair(sa + c * kMnBox, &tmA, tm * BM + 64 * c, kb * BK, fl);
+          } else {
+            tma_load_2d_pair(sa, &tmA, kb * BK, tm * BM, fl);
+          }
+          if constexpr (MNF & 2) {  // this CTA's half of B's 256 columns as two [64 N x 64 k] boxes
+#pragma unroll
+            for (int c = 0; c < BN / 128; ++c)
+              tma_load_2d_pair(sb + c * kMnBox, &tmB0, tn * BN + static_cast<int>(crank) * (BN / 2) + 64 * c, kb * BK, fl);
+          } else {
+            tma_load_2d_pair(sb, bmap, kb * BK, by, fl);
+          }
           issued[stage] = true;
           armed[stage] = phase;
           if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -1102,7 +1113,7 @@ mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream) {
       const bool wide = (g.nseg == 1 || seg % 256 == 0);
       if (g.epi == EPI_STORE && (g.a_mn || g.b_mn)) {  // bf16 output of a product with a transposed operand
         if (g.nseg != 1 || g.a_mn) return MTP_ERR_UNSUPPORTED;
-        return launch<256, EPI_STORE, 2>(g, stream);
+        return g.M > BM ? launch<256, EPI_STORE, 2, true>(g, stream) : launch<256, EPI_STORE, 2>(g, stream);
       }
       const bool pair = wide && g.M > BM;
       if (g.epi == EPI_STORE)
@@ -1137,9 +1148,9 @@ mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream) {
       if (g.splits < 1 || g.splits > nk || g.nseg != 1) return MTP_ERR_INVALID_ARG;
       switch ((g.a_mn ? 1 : 0) | (g.b_mn ? 2 : 0)) {
         case 0: return g.M > BM ? launch<256, EPI_F32_ACC, 0, true>(g, stream) : launch<256, EPI_F32_ACC, 0>(g, stream);
-        case 1: return launch<256, EPI_F32_ACC, 1>(g, stream);
-        case 2: return launch<256, EPI_F32_ACC, 2>(g, stream);
-        default: return launch<256, EPI_F32_ACC, 3>(g, stream);
+        case 1: return g.M > BM ? launch<256, EPI_F32_ACC, 1, true>(g, stream) : launch<256, EPI_F32_ACC, 1>(g, stream);
+        case 2: return g.M > BM ? launch<256, EPI_F32_ACC, 2, true>(g, stream) : launch<256, EPI_F32_ACC, 2>(g, stream);
+        default: return g.M > BM ? launch<256, EPI_F32_ACC, 3, true>(g, stream) : launch<256, EPI_F32_ACC, 3>(g, stream);
       }
     }
     case EPI_T_STORE:
