@@ -1044,11 +1044,23 @@ void rmsnorm_bwd(const __nv_bfloat16* h, int ld_h, const int32_t* h_rows, const 
   }
 }
 
-// a += b (fp32, n elements)
+// a += b (fp32, n elements): 16-byte steps when both bases are 16-byte aligned,
+// the n % 4 tail (or everything, unaligned) element by element
 __global__ void add_f32_kernel(float* __restrict__ a, const float* __restrict__ b, size_t n) {
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x)
-    a[i] += b[i];
+  const size_t tid = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  const bool vec = ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 15u) == 0;
+  const size_t n4 = vec ? n / 4 : 0;
+  for (size_t i = tid; i < n4; i += stride) {
+    float4 x = reinterpret_cast<float4*>(a)[i];
+    const float4 y = reinterpret_cast<const float4*>(b)[i];
+    x.x += y.x;
+    x.y += y.y;
+    x.z += y.z;
+    x.w += y.w;
+    reinterpret_cast<float4*>(a)[i] = x;
+  }
+  for (size_t i = 4 * n4 + tid; i < n; i += stride) a[i] += b[i];
 }
 
 inline int round_up8(int v) { return (v + 7) / 8 * 8; }
@@ -1154,23 +1166,51 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
 // ---- block backward -------------------------------------------------------
 
 // y = bf16(x) for an fp32 [R, C] matrix (row strides ldx, ldy); block rows
-// stride over matrix rows, threads over columns (no per-element division)
+// stride over matrix rows, threads over columns (no per-element division).
+// VEC: 8 columns per thread step (two 16-byte loads, one 16-byte store), for
+// C, ldx and ldy multiples of 8 and 16-byte aligned bases.
+template <bool VEC>
 __global__ void f32_to_bf16_kernel(const float* __restrict__ x, int ldx, __nv_bfloat16* __restrict__ y, int ldy, int R,
                                    int Cn) {
   mtp::pdl_trigger();  // a GEMM that follows may start its setup
   for (int r = blockIdx.x; r < R; r += gridDim.x) {
     const float* xr = x + static_cast<size_t>(r) * ldx;
     __nv_bfloat16* yr = y + static_cast<size_t>(r) * ldy;
-    for (int c = threadIdx.x; c < Cn; c += blockDim.x) yr[c] = __float2bfloat16_rn(xr[c]);
+    if constexpr (VEC) {
+      for (int c = 8 * threadIdx.x; c < Cn; c += 8 * blockDim.x) {
+        const float4 a = *reinterpret_cast<const float4*>(xr + c);
+        const float4 b = *reinterpret_cast<const float4*>(xr + c + 4);
+        uint4 o;
+        o.x = mtp::pack2_bf16(a.x, a.y);
+        o.y = mtp::pack2_bf16(a.z, a.w);
+        o.z = mtp::pack2_bf16(b.x, b.y);
+        o.w = mtp::pack2_bf16(b.z, b.w);
+        *reinterpret_cast<uint4*>(yr + c) = o;
+      }
+    } else {
+      for (int c = threadIdx.x; c < Cn; c += blockDim.x) yr[c] = __float2bfloat16_rn(xr[c]);
+    }
   }
 }
 void f32_to_bf16(const float* x, int ldx, __nv_bfloat16* y, int ldy, int R, int Cn, cudaStream_t st) {
-  f32_to_bf16_kernel<<<std::min(R, 16 * 152), 256, 0, st>>>(x, ldx, y, ldy, R, Cn);
+  const bool vec = Cn % 8 == 0 && ldx % 8 == 0 && ldy % 8 == 0 && mtp::aligned16(x) && mtp::aligned16(y);
+  if (vec) f32_to_bf16_kernel<true><<<std::min(R, 16 * 152), 128, 0, st>>>(x, ldx, y, ldy, R, Cn);
+  else f32_to_bf16_kernel<false><<<std::min(R, 16 * 152), 256, 0, st>>>(x, ldx, y, ldy, R, Cn);
   mtp::note_launch();
 }
 
 // SwiGLU backward from the recomputed pre-activations pq = [p | q] ([M, 2 ffn]
-// bf16) and dg ([M, ffn] fp32): g = silu(p) q, dp = dg q silu'(p), dq = dg silu(p)
+// bf16) and dg ([M, ffn] fp32): g = silu(p) q, dp = dg q silu'(p), dq = dg silu(p).
+// VEC: 8 columns per thread step with 16-byte accesses (ffn a multiple of 8,
+// 16-byte aligned bases).
+__device__ __forceinline__ void swiglu_bwd1(float p, float q, float dgv, float& g, float& dp, float& dq) {
+  const float sg = 1.0f / (1.0f + __expf(-p));
+  const float silu = p * sg;
+  g = silu * q;
+  dp = dgv * q * (sg * (1.0f + p * (1.0f - sg)));
+  dq = dgv * silu;
+}
+template <bool VEC>
 __global__ void swiglu_bwd_kernel(const __nv_bfloat16* __restrict__ pq, const float* __restrict__ dg,
                                   __nv_bfloat16* __restrict__ g, __nv_bfloat16* __restrict__ dpq, int M, int ffn) {
   mtp::pdl_trigger();  // a GEMM that follows may start its setup
@@ -1179,14 +1219,37 @@ __global__ void swiglu_bwd_kernel(const __nv_bfloat16* __restrict__ pq, const fl
     const float* dgr = dg + static_cast<size_t>(m) * ffn;
     __nv_bfloat16* gr = g + static_cast<size_t>(m) * ffn;
     __nv_bfloat16* dr = dpq + static_cast<size_t>(m) * 2 * ffn;
-    for (int j = threadIdx.x; j < ffn; j += blockDim.x) {
-      const float p = __bfloat162float(pr[j]), q = __bfloat162float(pr[ffn + j]);
-      const float sg = 1.0f / (1.0f + __expf(-p));
-      const float silu = p * sg;
-      const float dgv = dgr[j];
-      gr[j] = __float2bfloat16_rn(silu * q);
-      dr[j] = __float2bfloat16_rn(dgv * q * (sg * (1.0f + p * (1.0f - sg))));
-      dr[ffn + j] = __float2bfloat16_rn(dgv * silu);
+    if constexpr (VEC) {
+      for (int j = 8 * threadIdx.x; j < ffn; j += 8 * blockDim.x) {
+        const uint4 pv = *reinterpret_cast<const uint4*>(pr + j);
+        const uint4 qv = *reinterpret_cast<const uint4*>(pr + ffn + j);
+        const float4 d0 = *reinterpret_cast<const float4*>(dgr + j);
+        const float4 d1 = *reinterpret_cast<const float4*>(dgr + j + 4);
+        const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w}, qw[4] = {qv.x, qv.y, qv.z, qv.w};
+        const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+        uint32_t go[4], dpo[4], dqo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 p2 = mtp::unpack2_bf16(pw[i]), q2 = mtp::unpack2_bf16(qw[i]);
+          float g0, g1, dp0, dp1, dq0, dq1;
+          swiglu_bwd1(p2.x, q2.x, dv[2 * i], g0, dp0, dq0);
+          swiglu_bwd1(p2.y, q2.y, dv[2 * i + 1], g1, dp1, dq1);
+          go[i] = mtp::pack2_bf16(g0, g1);
+          dpo[i] = mtp::pack2_bf16(dp0, dp1);
+          dqo[i] = mtp::pack2_bf16(dq0, dq1);
+        }
+        *reinterpret_cast<uint4*>(gr + j) = make_uint4(go[0], go[1], go[2], go[3]);
+        *reinterpret_cast<uint4*>(dr + j) = make_uint4(dpo[0], dpo[1], dpo[2], dpo[3]);
+        *reinterpret_cast<uint4*>(dr + ffn + j) = make_uint4(dqo[0], dqo[1], dqo[2], dqo[3]);
+      }
+    } else {
+      for (int j = threadIdx.x; j < ffn; j += blockDim.x) {
+        float gv, dp, dq;
+        swiglu_bwd1(__bfloat162float(pr[j]), __bfloat162float(pr[ffn + j]), dgr[j], gv, dp, dq);
+        gr[j] = __float2bfloat16_rn(gv);
+        dr[j] = __float2bfloat16_rn(dp);
+        dr[ffn + j] = __float2bfloat16_rn(dq);
+      }
     }
   }
 }
@@ -1375,7 +1438,10 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
     TRY(mtp::gemm_bf16_launch(g, st));
   }
   TRY(gemm_acc(M, f, d, bb(B.dhb), d, false, wt(C.W.w_down), f, true, fb(B.dgf), f, st, true));
-  swiglu_bwd_kernel<<<std::min(M, 16 * 152), 256, 0, st>>>(bb(B.pq), fb(B.dgf), bb(B.gb), bb(B.dpq), M, f);
+  if (f % 8 == 0)  // workspace buffers start 16-byte aligned (256-byte offsets from an aligned base)
+    swiglu_bwd_kernel<true><<<std::min(M, 16 * 152), 128, 0, st>>>(bb(B.pq), fb(B.dgf), bb(B.gb), bb(B.dpq), M, f);
+  else
+    swiglu_bwd_kernel<false><<<std::min(M, 16 * 152), 256, 0, st>>>(bb(B.pq), fb(B.dgf), bb(B.gb), bb(B.dpq), M, f);
   mtp::note_launch();
   if (float* gwd = gp(G->w_down)) TRY(gemm_acc(d, f, M, bb(B.dhb), d, true, bb(B.gb), f, true, gwd, f, st));
   // g = silu(y Wg^T) (y Wu^T): dWg += dp^T y; dWu += dq^T y; dy = dp Wg + dq Wu
@@ -1498,7 +1564,7 @@ extern "C" mtp_status mtp_chain_loss_grad(const mtp_dims* dims, const mtp_weight
     TRY(block_backward(C, T, BL, k, h_prev, grads));
   }
   if (grads->h0) {
-    add_f32_kernel<<<2 * 152, 256, 0, stream>>>(grads->h0, C.buf<float>(T.dstate), Md);
+    add_f32_kernel<<<8 * 152, 256, 0, stream>>>(grads->h0, C.buf<float>(T.dstate), Md);
     mtp::note_launch();
   }
   MTP_LAUNCH_CHECK();
