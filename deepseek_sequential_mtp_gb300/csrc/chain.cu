@@ -1370,19 +1370,28 @@ mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, bool a
   g.b_mn = b_mn;
   g.out_f32 = out;
   g.ldo = ldo;
-  const int tiles = ((M + 127) / 128) * ((N + 255) / 256);
+  // K splits by a cost model: waves of (tile, split) units times the k-blocks of a unit
+  // (~655 cycles each on a 256 x 256 CTA-pair tile), plus the split-K atomics (the fp32
+  // output added once per split at ~680 B per cycle of L2 atomic throughput) and, for an
+  // overwrite, the zeroing memset.  Measured on GB300: the head's dX (8192 x 1024, K = 32000)
+  // took 345 us unsplit and 400 us in 4 splits although 4 splits balance the waves better.
+  const bool pair = M > 128;
+  const int units1 = (pair ? (M + 255) / 256 : (M + 127) / 128) * ((N + 255) / 256);
+  const int slots = pair ? sms / 2 : sms;
   const int nk = (K + 63) / 64;
   const int max_split = std::max(1, std::min(16, nk / 8));
+  const double out_bytes = 4.0 * M * N;
   int splits = 1;
-  double best = 0.0;
+  double best = 1e300;
   for (int sp = 1; sp <= max_split; ++sp) {
-    const long long units = static_cast<long long>(tiles) * sp;
-    const double eff = static_cast<double>(units) / (static_cast<double>(sms) * ((units + sms - 1) / sms));
-    if (eff > best + 1e-9) {
-      best = eff;
+    const long long units = static_cast<long long>(units1) * sp;
+    const double waves = static_cast<double>((units + slots - 1) / slots);
+    double cyc = waves * ((nk + sp - 1) / sp) * 655.0;
+    if (sp > 1) cyc += sp * out_bytes / 680.0 + (overwrite ? out_bytes / 3400.0 : 0.0);
+    if (cyc < best * 0.98) {  // a split must win by 2%
+      best = cyc;
       splits = sp;
     }
-    if (eff >= 0.9) break;
   }
   g.splits = splits;
   g.pdl = true;
