@@ -1122,7 +1122,7 @@ mtp::GemmDesc gdesc(int M, int N, int K, const __nv_bfloat16* A, int lda, const 
 // gradients through the shared head and the final norm of term t (state h_t):
 // per vocabulary chunk the logits are recomputed by one GEMM whose epilogue
 // writes dz = (softmax - onehot) dL/dl (the logits are never stored whole);
-// then dX += dz W_U[chunk] and, from dz^T (a transpose), d_head[chunk] +=
+// then dX += dz W_U[chunk] and, reading dz MN-major as dz^T, d_head[chunk] +=
 // dz^T X; finally the final RMSNorm's backward adds d h_t into dstate[t] and
 // accumulates d_out_norm.
 mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_bfloat16* h_t, float* d_head,
