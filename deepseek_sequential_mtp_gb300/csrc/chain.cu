@@ -1351,10 +1351,9 @@ SaveOff make_save_off(const mtp_dims& D) {
 
 // C += A B^T (C = A B^T with `overwrite`) into fp32; A is [M, K] (a_mn: stored [K, M]) and B is [N, K]
 // (b_mn: stored [K, N]), so transposes of row-major operands are read in
-// place.  K is split (partial tiles added with vector atomics)
-// when that fills the SMs' waves better: the smallest split whose work units
-// fill at least 90% of their last wave, else the best one (at most 16, and
-// at least 8 k-blocks per split).
+// place.  K is split (partial tiles added with vector atomics) when the cost
+// model below says the better-filled waves pay for the atomics (at most 16
+// splits, at least 8 k-blocks per split).
 mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, bool a_mn, const __nv_bfloat16* B, int ldb,
                     bool b_mn, float* out, int ldo, cudaStream_t st, bool overwrite) {
   static int sms = 0;
