@@ -86,7 +86,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait for the phase of `parity` to complete; false on abort or timeout.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = cycles_now();
   for (uint32_t it = 1;; ++it) {
@@ -182,6 +182,12 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "[%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+// Pull a tile of `map` at (x, y) into L2 (no shared-memory destination, no barrier).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
@@ -452,12 +458,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     for (int s = 0; s < S; ++s) { issued[s] = false; armed[s] = 0; }
     bool ok = true;
     const uint32_t full_leader0 = PAIR ? map_to_rank(full_bar(0), 0) : full_bar(0);
-    for (int u = u_first; ok && u < ntiles; u += u_step) {
-      const int t = splits == 1 ? u : u / splits, sp = splits == 1 ? 0 : u % splits;
-      int tm, tn;
+    // a unit's tile coordinates and the B map and row its copies use
+    auto unit_coords = [&](int u, int& tm, int& tn, int& sp, const CUtensorMap*& bmap, int& by) {
+      const int t = splits == 1 ? u : u / splits;
+      sp = splits == 1 ? 0 : u % splits;
       unit_tile(t, tm, tn);
-      const CUtensorMap* bmap = &tmB0;
-      int by;
+      bmap = &tmB0;
       if constexpr (EPI == EPI_SWIGLU) {
         by = tn * (BN / 2);
         if constexpr (PAIR) bmap = crank ? &tmB1 : &tmB0;  // the leader stages the gate rows, the peer the up rows
@@ -467,6 +473,42 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         by = n0 - seg * P.seg_rows;
         bmap = seg == 0 ? &tmB0 : (seg == 1 ? &tmB1 : &tmB2);
       }
+    };
+    // The first k-blocks of a new tile come from DRAM with a latency close to the ring's
+    // lead, so a tile boundary stalled the MMAs; the next unit's first k-blocks are pulled
+    // into L2 when this unit starts, one tile's time ahead.
+    constexpr int kPrefetchKb = 3;
+    auto prefetch_unit = [&](int u) {
+      int tm, tn, sp, by;
+      const CUtensorMap* bmap;
+      unit_coords(u, tm, tn, sp, bmap, by);
+      const int kb0 = kb_lo(sp), kb1 = min(kb_lo(sp + 1), kb0 + kPrefetchKb);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (tm * BM < P.M) {
+          if constexpr (MNF & 1) {
+#pragma unroll
+            for (int c = 0; c < BM / 64; ++c) tma_prefetch_2d(&tmA, tm * BM + 64 * c, kb * BK);
+          } else {
+            tma_prefetch_2d(&tmA, kb * BK, tm * BM);
+          }
+        }
+        if constexpr (MNF & 2) {
+          const int n0 = tn * BN + (PAIR ? static_cast<int>(crank) * (BN / 2) : 0);
+#pragma unroll
+          for (int c = 0; c < (PAIR ? BN / 2 : BN) / 64; ++c) tma_prefetch_2d(&tmB0, n0 + 64 * c, kb * BK);
+        } else if constexpr (EPI == EPI_SWIGLU && !PAIR) {
+          tma_prefetch_2d(&tmB0, kb * BK, by);
+          tma_prefetch_2d(&tmB1, kb * BK, by);
+        } else {
+          tma_prefetch_2d(bmap, kb * BK, by);
+        }
+      }
+    };
+    for (int u = u_first; ok && u < ntiles; u += u_step) {
+      int tm, tn, sp, by;
+      const CUtensorMap* bmap;
+      unit_coords(u, tm, tn, sp, bmap, by);
+      if (u + u_step < ntiles) prefetch_unit(u + u_step);
       const int kb_end = kb_lo(sp + 1);
       for (int kb = kb_lo(sp); kb < kb_end; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }

@@ -36,7 +36,7 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // Wait until the phase of parity `parity` has completed; false once the wait
 // limit has passed.  A parity wait cannot distinguish phase u+1 from u-1, so
 // callers must never wait more than one phase ahead of the barrier.
-static __device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+static __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
   if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = cycles_now();
   for (uint32_t it = 1;; ++it) {

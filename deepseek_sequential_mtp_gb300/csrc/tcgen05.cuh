@@ -24,7 +24,7 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 }
 // Wait for the phase of `parity`; false on abort or after the wait limit
 // (then the abort flag is raised and MTP_DEVERR_TIMEOUT or'ed into *err).
-static __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+static __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                                unsigned int* err) {
   if (mbar_try(bar, parity)) return true;
   const long long t0 = cycles_now();
