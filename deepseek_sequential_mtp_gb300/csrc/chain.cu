@@ -596,6 +596,7 @@ mtp_status gemm<__nv_bfloat16>(const Ctx& C, const __nv_bfloat16* A, int lda, co
   g.resid = resid;
   g.ldr = ldr;
   g.pdl = true;  // every forward-chain GEMM follows one of this library's kernels
+  g.b_early = true;  // B is a weight matrix
   if (epi == mtp::EPI_ROPE) {
     g.pos = C.pos;
     g.rope = C.buf<float2>(C.L.rope);
@@ -688,6 +689,7 @@ mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double
     g.ce_part = part;
     g.z_tgt = zt;
     g.pdl = true;  // follows the RMSNorm kernel
+    g.b_early = true;  // B = W_U
     mtp::prof_begin(MTP_KC_HEAD_CE_GEMM, C.st);
     TRY(mtp::gemm_bf16_launch(g, C.st));
     mtp::prof_end(MTP_KC_HEAD_CE_GEMM, C.st);
@@ -1150,6 +1152,7 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
     g.ce_scale = scale;
     g.ce_offset = v0;
     g.pdl = true;  // follows the RMSNorm kernel or the previous chunk's GEMM
+    g.b_early = true;  // B = W_U
     TRY(mtp::gemm_bf16_launch(g, C.st));
     // dX += dz W_U[v0 : v0 + vc] (W_U rows read as the MN-major B operand)
     TRY(gemm_acc(M, d, vc, dz, T.vc, false, WU + static_cast<size_t>(v0) * d, d, true, dx, d, C.st, v0 == 0));

@@ -283,6 +283,7 @@ struct Args {
   const float* lse;
   const float* ce_scale;
   int ce_offset;
+  int b_early;  // B is read-only for the stream's earlier kernels: prefetch it before pdl_wait
 };
 
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
@@ -427,13 +428,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t crank = PAIR ? cluster_ctarank() & 1u : 0u;  // 0: the leader of the pair
-  // setup above overlaps the previous kernel (programmatic dependent launch); every
-  // access to global memory below follows its completion.  This kernel releases its
-  // own dependents only by completing: with an explicit early release the backward
-  // pass's results came out wrong on GB300 (cause not identified), and the release
-  // bought no measurable time.
-  pdl_wait();
-
   // work units: (tile, K split); split s covers k-blocks [kb_lo(s), kb_lo(s+1)).  A pair
   // takes units of two M-tiles: 2 tm2 (leader) and 2 tm2 + 1 (peer) with the same N-tile.
   const int tiles_m_u = PAIR ? (P.tiles_m + 1) / 2 : P.tiles_m;
@@ -448,6 +442,61 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if constexpr (PAIR) tm = 2 * tm + static_cast<int>(crank);
   };
 
+  // a unit's tile coordinates and the B map and row its copies use
+  auto unit_coords = [&](int u, int& tm, int& tn, int& sp, const CUtensorMap*& bmap, int& by) {
+    const int t = splits == 1 ? u : u / splits;
+    sp = splits == 1 ? 0 : u % splits;
+    unit_tile(t, tm, tn);
+    bmap = &tmB0;
+    if constexpr (EPI == EPI_SWIGLU) {
+      by = tn * (BN / 2);
+      if constexpr (PAIR) bmap = crank ? &tmB1 : &tmB0;  // the leader stages the gate rows, the peer the up rows
+    } else {
+      const int n0 = tn * BN + (PAIR ? static_cast<int>(crank) * (BN / 2) : 0);  // a pair splits B's rows
+      const int seg = n0 < P.seg_rows ? 0 : (n0 < 2 * P.seg_rows ? 1 : 2);  // at most three segments
+      by = n0 - seg * P.seg_rows;
+      bmap = seg == 0 ? &tmB0 : (seg == 1 ? &tmB1 : &tmB2);
+    }
+  };
+  // The first k-blocks of a new tile come from DRAM with a latency close to the ring's
+  // lead, so a tile boundary stalled the MMAs; the next unit's first k-blocks are pulled
+  // into L2 when this unit starts, one tile's time ahead.
+  constexpr int kPrefetchKb = 3;
+  auto prefetch_unit = [&](int u, bool with_a) {
+    int tm, tn, sp, by;
+    const CUtensorMap* bmap;
+    unit_coords(u, tm, tn, sp, bmap, by);
+    const int kb0 = kb_lo(sp), kb1 = min(kb_lo(sp + 1), kb0 + kPrefetchKb);
+    for (int kb = kb0; kb < kb1; ++kb) {
+      if (with_a && tm * BM < P.M) {
+        if constexpr (MNF & 1) {
+#pragma unroll
+          for (int c = 0; c < BM / 64; ++c) tma_prefetch_2d(&tmA, tm * BM + 64 * c, kb * BK);
+        } else {
+          tma_prefetch_2d(&tmA, kb * BK, tm * BM);
+        }
+      }
+      if constexpr (MNF & 2) {
+        const int n0 = tn * BN + (PAIR ? static_cast<int>(crank) * (BN / 2) : 0);
+#pragma unroll
+        for (int c = 0; c < (PAIR ? BN / 2 : BN) / 64; ++c) tma_prefetch_2d(&tmB0, n0 + 64 * c, kb * BK);
+      } else if constexpr (EPI == EPI_SWIGLU && !PAIR) {
+        tma_prefetch_2d(&tmB0, kb * BK, by);
+        tma_prefetch_2d(&tmB1, kb * BK, by);
+      } else {
+        tma_prefetch_2d(bmap, kb * BK, by);
+      }
+    }
+  };
+  // Setup above overlaps the previous kernel (programmatic dependent launch); every access
+  // to memory an earlier kernel writes follows pdl_wait().  B marked b_early is a weight
+  // matrix that no kernel of the stream writes, so its first k-blocks are pulled into L2
+  // before the wait.  This kernel releases its own dependents only by completing: with
+  // an explicit early release the backward pass's results came out wrong on GB300 (cause
+  // not identified), and the release bought no measurable time.
+  if (P.b_early && threadIdx.x == 0 && u_first < ntiles) prefetch_unit(u_first, false);
+  pdl_wait();
+
   if (warp == 0 && lane == 0) {
     // ------------------------------ producer ------------------------------
     int stage = 0;
@@ -458,57 +507,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     for (int s = 0; s < S; ++s) { issued[s] = false; armed[s] = 0; }
     bool ok = true;
     const uint32_t full_leader0 = PAIR ? map_to_rank(full_bar(0), 0) : full_bar(0);
-    // a unit's tile coordinates and the B map and row its copies use
-    auto unit_coords = [&](int u, int& tm, int& tn, int& sp, const CUtensorMap*& bmap, int& by) {
-      const int t = splits == 1 ? u : u / splits;
-      sp = splits == 1 ? 0 : u % splits;
-      unit_tile(t, tm, tn);
-      bmap = &tmB0;
-      if constexpr (EPI == EPI_SWIGLU) {
-        by = tn * (BN / 2);
-        if constexpr (PAIR) bmap = crank ? &tmB1 : &tmB0;  // the leader stages the gate rows, the peer the up rows
-      } else {
-        const int n0 = tn * BN + (PAIR ? static_cast<int>(crank) * (BN / 2) : 0);  // a pair splits B's rows
-        const int seg = n0 < P.seg_rows ? 0 : (n0 < 2 * P.seg_rows ? 1 : 2);  // at most three segments
-        by = n0 - seg * P.seg_rows;
-        bmap = seg == 0 ? &tmB0 : (seg == 1 ? &tmB1 : &tmB2);
-      }
-    };
-    // The first k-blocks of a new tile come from DRAM with a latency close to the ring's
-    // lead, so a tile boundary stalled the MMAs; the next unit's first k-blocks are pulled
-    // into L2 when this unit starts, one tile's time ahead.
-    constexpr int kPrefetchKb = 3;
-    auto prefetch_unit = [&](int u) {
-      int tm, tn, sp, by;
-      const CUtensorMap* bmap;
-      unit_coords(u, tm, tn, sp, bmap, by);
-      const int kb0 = kb_lo(sp), kb1 = min(kb_lo(sp + 1), kb0 + kPrefetchKb);
-      for (int kb = kb0; kb < kb1; ++kb) {
-        if (tm * BM < P.M) {
-          if constexpr (MNF & 1) {
-#pragma unroll
-            for (int c = 0; c < BM / 64; ++c) tma_prefetch_2d(&tmA, tm * BM + 64 * c, kb * BK);
-          } else {
-            tma_prefetch_2d(&tmA, kb * BK, tm * BM);
-          }
-        }
-        if constexpr (MNF & 2) {
-          const int n0 = tn * BN + (PAIR ? static_cast<int>(crank) * (BN / 2) : 0);
-#pragma unroll
-          for (int c = 0; c < (PAIR ? BN / 2 : BN) / 64; ++c) tma_prefetch_2d(&tmB0, n0 + 64 * c, kb * BK);
-        } else if constexpr (EPI == EPI_SWIGLU && !PAIR) {
-          tma_prefetch_2d(&tmB0, kb * BK, by);
-          tma_prefetch_2d(&tmB1, kb * BK, by);
-        } else {
-          tma_prefetch_2d(bmap, kb * BK, by);
-        }
-      }
-    };
     for (int u = u_first; ok && u < ntiles; u += u_step) {
       int tm, tn, sp, by;
       const CUtensorMap* bmap;
       unit_coords(u, tm, tn, sp, bmap, by);
-      if (u + u_step < ntiles) prefetch_unit(u + u_step);
+      if (u + u_step < ntiles) prefetch_unit(u + u_step, true);
       const int kb_end = kb_lo(sp + 1);
       for (int kb = kb_lo(sp); kb < kb_end; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
@@ -1066,6 +1069,7 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
   a.lse = g.lse;
   a.ce_scale = g.ce_scale;
   a.ce_offset = g.ce_offset;
+  a.b_early = g.b_early ? 1 : 0;
   if constexpr (PAIR) {  // clusters of two CTAs, one pair per two SMs
     const int units = ((a.tiles_m + 1) / 2) * a.tiles_n * a.splits;
     const int pairs = units < num_sms() / 2 ? units : num_sms() / 2;
