@@ -1397,6 +1397,7 @@ mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, bool a
   }
   g.splits = splits;
   g.pdl = true;
+  g.b_early = true;  // an L2 prefetch is coherent with later writes, so any B may be fetched early
   if (overwrite) {  // out = A B^T: one split stores directly, several add into a zeroed output
     if (splits == 1) {
       g.f32_overwrite = true;
@@ -1441,12 +1442,14 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
     g.out = bb(B.pq);
     g.ldo = 2 * f;
     g.pdl = true;  // follows the conversion kernel
+    g.b_early = true;
     TRY(mtp::gemm_bf16_launch(g, st));
     g = gdesc(M, f, d, y, d, wt(C.W.w_up), d);
     g.epi = mtp::EPI_STORE;
     g.out = bb(B.pq) + f;
     g.ldo = 2 * f;
     g.pdl = true;
+    g.b_early = true;
     TRY(mtp::gemm_bf16_launch(g, st));
   }
   TRY(gemm_acc(M, f, d, bb(B.dhb), d, false, wt(C.W.w_down), f, true, fb(B.dgf), f, st, true));
@@ -1476,6 +1479,7 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
     g.out = bb(B.dob);
     g.ldo = d;
     g.pdl = true;  // follows a GEMM or the conversion kernel
+    g.b_early = true;
     TRY(mtp::gemm_bf16_launch(g, st));
   }
   // segment-causal attention backward (tensor cores), then RoPE backward

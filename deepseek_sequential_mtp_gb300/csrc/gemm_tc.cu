@@ -489,9 +489,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   };
   // Setup above overlaps the previous kernel (programmatic dependent launch); every access
-  // to memory an earlier kernel writes follows pdl_wait().  B marked b_early is a weight
-  // matrix that no kernel of the stream writes, so its first k-blocks are pulled into L2
-  // before the wait.  This kernel releases its own dependents only by completing: with
+  // to memory an earlier kernel writes follows pdl_wait().  With b_early, B's first k-blocks
+  // are pulled into L2 before the wait (a prefetch into L2 stays coherent with the writes
+  // that follow it; B is typically a weight matrix).  This kernel releases its own dependents
+  // only by completing: with
   // an explicit early release the backward pass's results came out wrong on GB300 (cause
   // not identified), and the release bought no measurable time.
   if (P.b_early && threadIdx.x == 0 && u_first < ntiles) prefetch_unit(u_first, false);

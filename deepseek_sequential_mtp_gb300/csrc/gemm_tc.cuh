@@ -54,8 +54,9 @@ struct GemmDesc {
   // programmatic dependent launch: the kernel's setup may overlap the stream's previous
   // kernel.  Only for launches whose stream predecessor is a kernel (not a memset or copy).
   bool pdl = false;
-  // B is a matrix no kernel of the stream writes (weights): with pdl, its first k-blocks are
-  // prefetched into L2 while the previous kernel still runs
+  // with pdl: B's first k-blocks are prefetched into L2 while the previous kernel still runs
+  // (an L2 prefetch stays coherent with writes that follow it, so this is safe for any B; it
+  // pays where B is not the previous kernel's output, e.g. weights)
   bool b_early = false;
   __nv_bfloat16* out = nullptr;
   int ldo = 0;
