@@ -57,7 +57,10 @@ struct Cfg {
   // per epilogue warp: two 32 x 64 bf16 boxes (4 KB each); none for the CE epilogue
   static constexpr int kBoxBytes = 32 * 64 * 2;
   static constexpr int kStagingBytes = epi_uses_staging(EPI) ? 4 * 2 * kBoxBytes : 0;
-  static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024 + 256;
+  // + 1024: alignment of the stage ring; + 512: mbarriers (8 B each, 2 S + 13 slots) and the
+  // TMEM address and abort flag after them (256 B did not cover the 10-stage configuration)
+  static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024 + 512;
+  static_assert(8 * (2 * kStages + 13) + 8 <= 512, "barrier area");
 };
 
 // ---------------------------------------------------------------------------
