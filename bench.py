@@ -124,11 +124,29 @@ def step_roofline(cfg, seg, supervised_rows, verify_bytes, step_ms, peaks):
                     "each term here is bound by one of the two"}
 
 
+def code_lines(text):
+    """The code of a C++/CUDA source: // comments, surrounding blanks and empty lines dropped
+    (so a comment edit does not count as a kernel change)."""
+    out = []
+    for line in text.splitlines():
+        i = line.find("//")
+        while i >= 0 and line.count('"', 0, i) % 2 == 1:  # a // inside a string literal
+            i = line.find("//", i + 2)
+        if i >= 0:
+            line = line[:i]
+        line = line.strip()
+        if line:
+            out.append(line)
+    return "\n".join(out)
+
+
 def gemm_source_hash():
+    """Hash of the GEMM core's code (gemm_tc.cu and .cuh, comments excluded): the key that ties
+    the committed ncu capture to the kernel it was taken on."""
     h = hashlib.sha256()
     for p in GEMM_SOURCES:
-        with open(p, "rb") as fh:
-            h.update(fh.read())
+        with open(p, encoding="utf-8") as fh:
+            h.update(code_lines(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -2,13 +2,15 @@
 // fp32 accumulation in tensor memory, fused epilogues.
 //
 // Persistent, warp-specialised CTA of 6 warps, one CTA per SM:
-//   warp 0     TMA producer: 128x64 A box and BNx64 B box (128-byte swizzle)
-//              per k-block into a STAGES-deep shared-memory ring (mbarriers
-//              with transaction counts).
+//   warp 0     TMA producer: 128x64 A box and BNx64 B box (128-byte swizzle;
+//              MN-major operands as 64x64 boxes) per k-block into a
+//              STAGES-deep shared-memory ring (mbarriers with transaction
+//              counts).  When a tile starts it pulls the next tile's first
+//              k-blocks into L2.
 //   warp 1     allocates 2*BN TMEM columns; one thread issues
-//              tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16) four
-//              times per k-block and tcgen05.commit's the smem slot back to
-//              the producer; a whole tile's accumulator is committed to the
+//              tcgen05.mma.kind::f16 (M=128, N=BN, K=16) four times per
+//              k-block and tcgen05.commit's the smem slot back to the
+//              producer; a whole tile's accumulator is committed to the
 //              epilogue.  Two accumulators alternate so the epilogue of tile
 //              i overlaps the MMAs of tile i+1.
 //   warps 2-5  epilogue: tcgen05.ld 32 lanes x 32 columns per load (warp w
@@ -19,10 +21,16 @@
 //              registers from global memory: the tile's first two 64-column
 //              pieces while its MMAs still run, later pieces two ahead.  The
 //              CE epilogue stores only per-row partials.
-// Every mbarrier wait is bounded: after ~1.5 s it sets MTP_DEVERR_TIMEOUT,
-// raises a CTA abort flag and every role drains out; the producer then waits
-// (bounded) for its in-flight copies and warp 1 for its MMAs before freeing
-// TMEM.
+// With more than one 128-row tile, 256-wide tiles run on CTA pairs (clusters of
+// two): 256x256 tiles with tcgen05.mma.cta_group::2 issued by the leader, each
+// CTA staging its 128 rows of A and half of B.
+// Launches may be programmatic dependents of the previous kernel: the setup
+// (barriers, TMEM, tensor-map prefetch, an optional L2 prefetch of B) runs
+// before griddepcontrol.wait.
+// Every mbarrier wait is bounded (and inlined: a call per wait cost ~10%):
+// after ~1.5 s it sets MTP_DEVERR_TIMEOUT, raises a CTA abort flag and every
+// role drains out; the producer then waits (bounded) for its in-flight copies
+// and warp 1 for its MMAs before freeing TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
