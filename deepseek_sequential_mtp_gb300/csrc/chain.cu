@@ -389,46 +389,49 @@ __global__ void head_ce_f32_kernel(const float* __restrict__ x, const float* __r
 // CE reduction and loss assembly
 // ---------------------------------------------------------------------------
 // ℓ_t = max + log Σ_tiles s_j exp(m_j - max) - z_label for supervised rows;
-// one warp per row, one (sum, count) atomic pair per block of 8 rows
+// one warp per row (rows strided over the grid), one (sum, count) atomic pair per block
 __global__ void ce_reduce_kernel(int M, int nvt, const float2* __restrict__ part, const float* __restrict__ zt,
                                  const int32_t* __restrict__ labels, float* __restrict__ row_loss,
                                  double* __restrict__ sum_count, float* __restrict__ lse_out) {
   mtp::pdl_trigger();  // a GEMM that follows may start its setup
-  __shared__ float s_loss[8];
-  __shared__ int s_sup[8];
+  __shared__ double s_sum[8];
+  __shared__ int s_cnt[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m = blockIdx.x * 8 + warp;
-  float loss = NAN;
-  const bool supervised = m < M && labels[m] >= 0;
-  if (supervised) {
-    const float2* p = part + static_cast<size_t>(m) * nvt;
-    float mx = -INFINITY;
-    for (int j = lane; j < nvt; j += 32) mx = fmaxf(mx, p[j].x);
-    mx = mtp::warp_max(mx);
-    float sum = 0.f;
-    for (int j = lane; j < nvt; j += 32) {
-      const float2 v = p[j];
-      sum += v.y * expf(v.x - mx);
+  double wsum = 0.0;
+  int wcnt = 0;
+  for (int m = blockIdx.x * 8 + warp; m < M; m += gridDim.x * 8) {
+    float loss = NAN;
+    if (labels[m] >= 0) {
+      const float2* p = part + static_cast<size_t>(m) * nvt;
+      float mx = -INFINITY;
+      for (int j = lane; j < nvt; j += 32) mx = fmaxf(mx, p[j].x);
+      mx = mtp::warp_max(mx);
+      float sum = 0.f;
+      for (int j = lane; j < nvt; j += 32) {
+        const float2 v = p[j];
+        sum += v.y * expf(v.x - mx);
+      }
+      sum = mtp::warp_sum(sum);
+      const float lse = mx + logf(sum);
+      loss = lse - zt[m];
+      if (lse_out && lane == 0) lse_out[m] = lse;
+      wsum += loss;
+      ++wcnt;
     }
-    sum = mtp::warp_sum(sum);
-    const float lse = mx + logf(sum);
-    loss = lse - zt[m];
-    if (lse_out && lane == 0) lse_out[m] = lse;
+    if (lane == 0 && row_loss) row_loss[m] = loss;
   }
   if (lane == 0) {
-    if (m < M && row_loss) row_loss[m] = loss;
-    s_loss[warp] = loss;
-    s_sup[warp] = supervised;
+    s_sum[warp] = wsum;
+    s_cnt[warp] = wcnt;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     double a = 0.0;
     int c = 0;
-    for (int w = 0; w < 8; ++w)
-      if (s_sup[w]) {
-        a += s_loss[w];
-        ++c;
-      }
+    for (int w = 0; w < 8; ++w) {
+      a += s_sum[w];
+      c += s_cnt[w];
+    }
     if (c) {
       atomicAdd(sum_count, a);
       atomicAdd(sum_count + 1, static_cast<double>(c));
@@ -698,7 +701,7 @@ mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double
                                                              part, zt, C.L.nvt);
     mtp::note_launch();
   }
-  ce_reduce_kernel<<<(C.M + 7) / 8, 256, 0, C.st>>>(
+  ce_reduce_kernel<<<std::min((C.M + 7) / 8, 256), 256, 0, C.st>>>(
       C.M, C.L.nvt, part, zt, labels, row_loss_term, sum_count,
       C.lse_save ? C.lse_save + static_cast<size_t>(k) * C.M : nullptr);
   mtp::note_launch();
