@@ -873,9 +873,10 @@ int sm_count() {
   return n;
 }
 
-// out[R, ldo] (fp32, columns [col0, col0 + features)) += X[R, K] · W[features, K]^T
+// out[R, ldo] (fp32) = X[R, K] · W[features, K]^T: the swap-AB tcgen05 GEMM (weights on the
+// 128-row side, the <= 32 tokens as N, the logits stored transposed)
 mtp_status skinny_gemm(const __nv_bfloat16* W, int features, int K, const __nv_bfloat16* X, int R, float* out,
-                       int ldo, cudaStream_t st, bool store = false) {
+                       int ldo, cudaStream_t st) {
   mtp::GemmDesc g;
   g.M = features;
   g.N = R;
@@ -888,15 +889,8 @@ mtp_status skinny_gemm(const __nv_bfloat16* W, int features, int K, const __nv_b
   g.seg_rows = R;
   g.out_f32 = out;
   g.ldo = ldo;
-  const int tiles = (features + 127) / 128;
-  const int nk = (K + 63) / 64;
-  int splits = 1;
-  if (!store) {
-    splits = (3 * sm_count() + tiles - 1) / tiles;
-    splits = std::max(1, std::min(splits, nk / 4 > 0 ? nk / 4 : 1));
-  }
-  g.splits = splits;
-  g.epi = store ? mtp::EPI_T_STORE : mtp::EPI_T_ATOMIC;
+  g.splits = 1;
+  g.epi = mtp::EPI_T_STORE;
   return mtp::gemm_bf16_launch(g, st);
 }
 
@@ -1040,7 +1034,7 @@ mtp_status draft_one_step(const mtp_dims& D, const mtp_weights* w, const mtp_blo
   // logits into q, then softmax and the draw
   mtp::prof_begin(MTP_KC_HEAD_CE_GEMM, st);
   if (ldq > 0x7FFFFFFFull) return MTP_ERR_UNSUPPORTED;
-  TRY(skinny_gemm(static_cast<const __nv_bfloat16*>(w->head), V, d, x, R, q_s, static_cast<int>(ldq), st, true));
+  TRY(skinny_gemm(static_cast<const __nv_bfloat16*>(w->head), V, d, x, R, q_s, static_cast<int>(ldq), st));
   mtp::prof_end(MTP_KC_HEAD_CE_GEMM, st);
   softmax_sample_kernel<<<R * kSampleCluster, kSampleThreads, 0, st>>>(
       q_s, V, ldq, key, static_cast<uint32_t>(step), static_cast<uint32_t>(offset & 0xFFFFFFFFu),

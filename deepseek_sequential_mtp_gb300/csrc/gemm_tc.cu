@@ -796,7 +796,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
           ship(box, col0, row0w);
         }
-      } else if constexpr (EPI == EPI_T_STORE || EPI == EPI_T_ATOMIC) {
+      } else if constexpr (EPI == EPI_T_STORE) {
         // row = feature; TMEM columns = tokens; for a fixed token the warp's
         // 32 lanes write 32 consecutive features (128 bytes)
         float v[32];
@@ -806,8 +806,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           for (int j = 0; j < 32; ++j) {
             if (j < P.N) {
               float* dst = P.out_f32 + static_cast<size_t>(j) * P.ldo + row;
-              if constexpr (EPI == EPI_T_ATOMIC) atomicAdd(dst, v[j]);
-              else *dst = v[j];
+              *dst = v[j];
             }
           }
         }
@@ -825,32 +824,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               v[i] = fmaf(exp2f(fmaf(v[i], 1.4426950408889634f, -lse2)), sc, i == off ? -sc : 0.f);
-            box_write32(box, lane, half, v);
-          }
-          ship(box, col0, row0w);
-        }
-      } else if constexpr (EPI == EPI_CE_GRAD_T) {
-        // rows = vocabulary entries, columns = tokens: lane i fetches token
-        // (col + i)'s label and lse, shuffles hand them to every row's lane
-        const float sc = *P.ce_scale;
-        const int vocab = P.ce_offset + row;
-#pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
-          const int col0 = tn * BN + c * 64;
-          uint8_t* box = claim();
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int tok = col0 + half * 32 + lane;
-            const int my_lab = tok < P.N ? P.labels[tok] : -1;
-            const float my_lse = my_lab >= 0 ? P.lse[tok] : 0.f;
-            float v[32];
-            tmem_ld32(taddr + c * 64 + half * 32, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int lab = __shfl_sync(0xffffffffu, my_lab, i);
-              const float lse = __shfl_sync(0xffffffffu, my_lse, i);
-              v[i] = lab >= 0 ? (__expf(v[i] - lse) - (vocab == lab ? 1.f : 0.f)) * sc : 0.f;
-            }
             box_write32(box, lane, half, v);
           }
           ship(box, col0, row0w);
@@ -1195,11 +1168,8 @@ mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream) {
       if (!g.labels || !g.ce_part || !g.z_tgt) return MTP_ERR_INVALID_ARG;
       return g.M > BM ? launch<256, EPI_CE, 0, true>(g, stream) : launch<256, EPI_CE>(g, stream);
     case EPI_CE_GRAD:
-    case EPI_CE_GRAD_T:
       if (!g.labels || !g.lse || !g.ce_scale) return MTP_ERR_INVALID_ARG;
-      if (g.epi == EPI_CE_GRAD)
-        return g.M > BM ? launch<256, EPI_CE_GRAD, 0, true>(g, stream) : launch<256, EPI_CE_GRAD>(g, stream);
-      return launch<256, EPI_CE_GRAD_T>(g, stream);
+      return g.M > BM ? launch<256, EPI_CE_GRAD, 0, true>(g, stream) : launch<256, EPI_CE_GRAD>(g, stream);
     case EPI_F32_ACC: {
       if (!g.out_f32 || g.ldo % 4 || !aligned16(g.out_f32)) return MTP_ERR_INVALID_ARG;
       const int nk = (g.K + BK - 1) / BK;
@@ -1212,12 +1182,9 @@ mtp_status gemm_bf16_launch(const GemmDesc& g, cudaStream_t stream) {
       }
     }
     case EPI_T_STORE:
-    case EPI_T_ATOMIC: {
       if (g.N > 32 || !g.out_f32 || g.nseg != 1) return MTP_ERR_UNSUPPORTED;
-      const int nk = (g.K + BK - 1) / BK;
-      if (g.splits < 1 || g.splits > nk || (g.epi == EPI_T_STORE && g.splits != 1)) return MTP_ERR_INVALID_ARG;
-      return g.epi == EPI_T_STORE ? launch<32, EPI_T_STORE>(g, stream) : launch<32, EPI_T_ATOMIC>(g, stream);
-    }
+      if (g.splits != 1) return MTP_ERR_INVALID_ARG;
+      return launch<32, EPI_T_STORE>(g, stream);
     default:
       return MTP_ERR_INVALID_ARG;
   }

@@ -17,20 +17,16 @@ enum GemmEpilogue : int {
   // 128-row side, B = activations [tokens <= 32, K]; the accumulator tile is
   // [128 features, 32 tokens] and is written transposed, out[token, feature]
   EPI_T_STORE = 5,  // out_f32[token * ldo + feature] = acc (no split-K)
-  EPI_T_ATOMIC = 6,  // out_f32[token * ldo + feature] += acc (split-K partials; out zeroed first)
   // cross-entropy backward from recomputed logits z (rows = tokens, columns =
   // vocabulary entries ce_offset + col): out = bf16((exp(z - lse[row]) -
   // [ce_offset + col == labels[row]]) * ce_scale[0]), 0 for rows without a label
   EPI_CE_GRAD = 7,
-  // the same with rows = vocabulary entries ce_offset + row and columns = tokens
-  EPI_CE_GRAD_T = 8,
   EPI_F32_ACC = 9  // out_f32[row * ldo + col] += acc (read-modify-write; with split-K, vector atomics)
 };
 
 // Epilogues that write bf16 boxes through the shared-memory staging buffers.
 constexpr bool epi_uses_staging(int epi) {
-  return epi == EPI_STORE || epi == EPI_RESID || epi == EPI_ROPE || epi == EPI_SWIGLU || epi == EPI_CE_GRAD ||
-         epi == EPI_CE_GRAD_T;
+  return epi == EPI_STORE || epi == EPI_RESID || epi == EPI_ROPE || epi == EPI_SWIGLU || epi == EPI_CE_GRAD;
 }
 
 // C-side description of one GEMM  acc[M, N] = A[M, K] · B[N, K]^T  (bf16 in,
