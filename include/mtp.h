@@ -44,7 +44,7 @@ typedef enum mtp_status {
   MTP_ERR_WORKSPACE = 4,    /* workspace smaller than the query returned     */
   MTP_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed             */
   MTP_ERR_DEVICE = 6,       /* a kernel set the device error word           */
-  MTP_ERR_UNSUPPORTED = 7   /* a shape/dtype combination this build lacks   */
+  MTP_ERR_UNSUPPORTED = 7   /* a shape/dtype combination not implemented  */
 } mtp_status;
 
 typedef enum mtp_dtype { MTP_F32 = 0, MTP_BF16 = 1 } mtp_dtype;
