@@ -15,7 +15,11 @@
  *     allocates nothing and keeps no state besides one device error word per
  *     translation unit (read with mtp_check_errors) and the tensor-map
  *     encoder entry point resolved on first use.
- *   - Calls are asynchronous on `stream`.  Argument errors are detected on the
+ *   - Calls are asynchronous on `stream`.  Inside one call, a GEMM may be
+ *     launched as a programmatic dependent of the call's previous kernel (its
+ *     setup overlaps that kernel; it reads nothing before it completes); the
+ *     first kernel of every call is an ordinary launch, so a call is ordered
+ *     after all earlier work on `stream`.  Argument errors are detected on the
  *     host, return a status and launch nothing.  Data-dependent errors (token
  *     id out of range, a kernel wait that ran out of time) set bits of the
  *     device error word (MTP_DEVERR_*) and never trap; spec_verify reports
