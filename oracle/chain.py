@@ -10,7 +10,7 @@ Forcing, and Speculative Runtime":
 * §0x03 / §0x04B: shared head p = softmax(W_U Norm_out(h^k)), the state handed
   to the next depth being the pre-final-norm h^k;
 * §0x04C / §0x06A: the rows of each depth are compiled first
-  (``oracle.rows.compile_mtp_rows``), previous states are gathered by
+  (``oracle.rows.depth_states``), previous states are gathered by
   physical row, attention is restricted to the same segment and to earlier
   bases;
 * §0x05: per-depth loss with the fixed denominator or the masked mean, and
@@ -41,7 +41,7 @@ from dataclasses import dataclass
 import numpy as np
 
 from .bf16 import round_bf16
-from .rows import compile_all_depths, label_owned
+from .rows import label_owned, states_all_depths
 
 
 @dataclass(frozen=True)
@@ -200,22 +200,22 @@ def chain_forward_loss(tokens, seg, pos, h0, W, dims: Dims, precision="f64",
                 row_loss[0, b, main_rows] = row_cross_entropy(
                     x0, [tok[t + 1] for t in main_rows], W, dims, rnd)
         state = _f64(h0[b])
-        for k, rows in enumerate(compile_all_depths(tok, sg, active, D)):
+        for k, rows in enumerate(states_all_depths(sg, active, D)):
             if not rows:
                 state = state[:0]
                 continue
-            prev = state[[r.previous_depth_row for r in rows]]
-            shifted = [tok[r.shifted_token_index] for r in rows]
+            prev = state[[r.parent for r in rows]]
+            shifted = [tok[r.input_at] for r in rows]
             bases = [r.base for r in rows]
-            h = mtp_module(prev, shifted, W, k, pos[b][[r.position for r in rows]],
+            h = mtp_module(prev, shifted, W, k, pos[b][bases],
                            [r.segment for r in rows], bases, dims, rnd)
             state = h
             h_out[k, b, bases] = h
             if with_loss:
-                sup = [j for j, r in enumerate(rows) if r.loss_valid]
+                sup = [j for j, r in enumerate(rows) if r.supervised]
                 if sup:
                     row_loss[k + 1, b, [rows[j].base for j in sup]] = row_cross_entropy(
-                        h[sup], [tok[rows[j].label_index] for j in sup], W, dims, rnd)
+                        h[sup], [tok[rows[j].label_at] for j in sup], W, dims, rnd)
 
     out = {"h": h_out, "row_loss": row_loss}
     if not with_loss:

@@ -27,7 +27,7 @@ import numpy as np
 import torch
 
 from .chain import Dims, assemble_loss
-from .rows import compile_all_depths, label_owned
+from .rows import label_owned, states_all_depths
 
 _F = torch.float64
 PER_DEPTH = ("hnorm", "enorm", "eh_proj", "attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up",
@@ -114,17 +114,17 @@ def chain_loss_grads(tokens, seg, pos, h0, W, dims: Dims, lam=0.3, den="fixed", 
                 sums[0] = sums[0] + ell.sum()
                 counts[0] += len(main_rows)
         state = h0_t[b]
-        for k, rows in enumerate(compile_all_depths(tok, sg, active, D)):
+        for k, rows in enumerate(states_all_depths(sg, active, D)):
             if not rows:
                 state = state[:0]
                 continue
-            prev = state[[r.previous_depth_row for r in rows]]
-            h = _module(prev, [tok[r.shifted_token_index] for r in rows], P, k,
-                        pos[b][[r.position for r in rows]], [r.segment for r in rows], [r.base for r in rows], dims)
+            prev = state[[r.parent for r in rows]]
+            h = _module(prev, [tok[r.input_at] for r in rows], P, k,
+                        pos[b][[r.base for r in rows]], [r.segment for r in rows], [r.base for r in rows], dims)
             state = h
-            sup = [j for j, r in enumerate(rows) if r.loss_valid]
+            sup = [j for j, r in enumerate(rows) if r.supervised]
             if sup:
-                ell = _row_ce(h[sup], [tok[rows[j].label_index] for j in sup], P, dims)
+                ell = _row_ce(h[sup], [tok[rows[j].label_at] for j in sup], P, dims)
                 sums[k + 1] = sums[k + 1] + ell.sum()
                 counts[k + 1] += len(sup)
 

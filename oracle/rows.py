@@ -1,9 +1,23 @@
-"""Semantic rows and label ownership -- oracle, test infrastructure only.
+"""Semantic state rows and label ownership -- oracle, test infrastructure only.
 
-Follows "M7.6 - DeepSeek MTP: Sequential Modules, Teacher Forcing, and
-Speculative Runtime" §0x04C (compile semantic rows before gathering tensors),
-§0x05A (label counts) and "M7.4 - Multi-Token Prediction Foundations" §0x01A /
-§0x03A (label ownership on padded, packed batches).
+Written from the rule stated in prose by "M7.6 - DeepSeek MTP: Sequential
+Modules, Teacher Forcing, and Speculative Runtime" §0x04C (compile the rows
+of a depth before gathering any tensor), with the counts of §0x05A and the
+label ownership of "M7.4 - Multi-Token Prediction Foundations" §0x01A /
+§0x03A (padded, packed batches).
+
+The rule, restated.  Depth k gives a packed position i (its *base*) a state
+when the k+1 teacher-forced inputs x_i, ..., x_{i+k} are all real tokens of
+the segment that holds i.  The state is *supervised* when x_{i+k+1} is a real
+token of that same segment as well; a state without a label is still kept,
+because the next depth may need it.  The state of depth k is built from the
+state of the same base at depth k-1, which must exist: it is looked up by
+base and never replaced by a neighbouring row.
+
+This module evaluates the rule through run lengths: for every position j,
+``run[j]`` counts the consecutive real tokens j, j+1, ... that share j's
+segment.  Base i then has a depth-k state iff run[i] >= k+1 and a label iff
+run[i] >= k+2.
 """
 from __future__ import annotations
 
@@ -12,89 +26,89 @@ from typing import Optional, Sequence
 
 
 @dataclass(frozen=True)
-class MTPRow:
-    """One state row of depth k (M7.6 §0x04C).
+class StateRow:
+    """A depth-k state (M7.6 §0x04C).
 
-    ``base`` is the semantic address i of the row in the packed stream;
-    ``previous_depth_row`` is the physical row of the same base in the
-    previous depth's tensor; the row reads token x_{i+k}
-    (``shifted_token_index``) and, when ``loss_valid``, is supervised by
-    x_{i+k+1} (``label_index``)."""
+    ``base``: packed position i the state belongs to; ``parent``: index of
+    the same base in the previous depth's list of states (the physical row
+    gathered as h^{k-1}); ``input_at``: i+k, the position whose token the
+    depth embeds; ``label_at``: i+k+1 when that token supervises the state,
+    else None; ``segment``: the segment id of i."""
 
     base: int
-    previous_depth_row: int
-    shifted_token_index: int
-    label_index: Optional[int]
-    loss_valid: bool
-    position: int
+    parent: int
+    input_at: int
+    label_at: Optional[int]
     segment: int
 
+    @property
+    def supervised(self) -> bool:
+        return self.label_at is not None
 
-def _is_int(v) -> bool:
+
+def _whole_number(v) -> bool:
     return isinstance(v, int) and not isinstance(v, bool)
 
 
-def compile_mtp_rows(tokens: Sequence[int], segment_ids: Sequence[int],
-                     valid: Sequence[bool], depth: int,
-                     previous_bases: Sequence[int]) -> list[MTPRow]:
-    """State rows of one packed stream at ``depth`` (M7.6 §0x04C).
-
-    A base i has state support at depth k when every teacher-forced input
-    i, i+1, ..., i+k is active and lies in the segment of i.  Such a row keeps
-    its state even without a label; it is supervised only if x_{i+k+1} exists,
-    is active and belongs to the same segment.  The predecessor state must be
-    present among ``previous_bases``; a missing one is an error, never a
-    fallback to another row.  Raises ``ValueError`` on misaligned inputs, a
-    non-positive depth, out-of-range or duplicate previous bases.
-    """
-    n = len(tokens)
-    if len(segment_ids) != n or len(valid) != n:
-        raise ValueError("unaligned packed inputs")
-    if not _is_int(depth) or depth < 1:
-        raise ValueError("depth must be positive")
-    for b in previous_bases:
-        if not _is_int(b) or b < 0 or b >= n:
-            raise ValueError("invalid previous base")
-    physical_row_of = {}
-    for row, b in enumerate(previous_bases):
-        if b in physical_row_of:
-            raise ValueError("duplicate previous base")
-        physical_row_of[b] = row
-
-    out: list[MTPRow] = []
-    for base in range(n):
-        shifted = base + depth
-        if shifted >= n:
+def same_segment_runs(segment: Sequence[int], active: Sequence[bool]) -> list[int]:
+    """run[j] = length of the stretch j, j+1, ... of real tokens that share
+    the segment of j (0 when j itself is padding), computed right to left."""
+    n = len(segment)
+    run = [0] * n
+    for j in reversed(range(n)):
+        if not active[j]:
             continue
-        own_segment = segment_ids[base]
-        supported = True
-        for j in range(base, shifted + 1):
-            if not valid[j] or segment_ids[j] != own_segment:
-                supported = False
-                break
-        if not supported:
+        joins_next = j + 1 < n and active[j + 1] and segment[j + 1] == segment[j]
+        run[j] = run[j + 1] + 1 if joins_next else 1
+    return run
+
+
+def depth_states(segment: Sequence[int], active: Sequence[bool], depth: int,
+                 parent_bases: Sequence[int]) -> list[StateRow]:
+    """States of one packed stream at ``depth``, in base order (M7.6 §0x04C).
+
+    ``parent_bases`` lists, in row order, the bases that hold a state at
+    depth-1 (every position for depth 1, where h^0 covers the stream).
+    Raises ValueError when the two per-position lists differ in length, when
+    the depth is not an integer >= 1, when a parent base lies outside the
+    stream or is listed twice, and when a base with support at this depth has
+    no parent state (the page's rule forbids substituting another row)."""
+    n = len(segment)
+    if len(active) != n:
+        raise ValueError("segment ids and activity flags must cover the same positions")
+    if not _whole_number(depth) or depth < 1:
+        raise ValueError(f"depth must be an integer >= 1, got {depth!r}")
+    row_of_base: dict[int, int] = {}
+    for row, b in enumerate(parent_bases):
+        if not _whole_number(b) or not 0 <= b < n:
+            raise ValueError(f"parent base {b!r} is not a position of the stream")
+        if b in row_of_base:
+            raise ValueError(f"parent base {b} appears more than once")
+        row_of_base[b] = row
+
+    run = same_segment_runs(segment, active)
+    states = []
+    for i, length in enumerate(run):
+        if length <= depth:  # x_i..x_{i+depth} are not all in i's segment
             continue
-        if base not in physical_row_of:
-            raise ValueError("required predecessor state is missing")
-        label = shifted + 1
-        has_label = label < n and bool(valid[label]) and segment_ids[label] == own_segment
-        out.append(MTPRow(base=base, previous_depth_row=physical_row_of[base],
-                          shifted_token_index=shifted,
-                          label_index=label if has_label else None,
-                          loss_valid=has_label, position=base, segment=own_segment))
-    return out
+        if i not in row_of_base:
+            raise ValueError(f"base {i} has support at depth {depth} but no state at depth {depth - 1}")
+        label = i + depth + 1 if length >= depth + 2 else None
+        states.append(StateRow(base=i, parent=row_of_base[i], input_at=i + depth,
+                               label_at=label, segment=int(segment[i])))
+    return states
 
 
-def compile_all_depths(tokens, segment_ids, valid, D: int) -> list[list[MTPRow]]:
-    """Rows of depths 1..D, carrying each depth's bases forward as the next
-    depth's ``previous_bases`` (M7.6 §0x04C, §0x06A)."""
-    bases = list(range(len(tokens)))
-    per_depth = []
+def states_all_depths(segment: Sequence[int], active: Sequence[bool], D: int) -> list[list[StateRow]]:
+    """States of depths 1..D; each depth's bases are the next depth's parents
+    (M7.6 §0x04C, §0x06A: compile, gather, run, repeat)."""
+    parents = list(range(len(segment)))
+    out = []
     for k in range(1, D + 1):
-        rows = compile_mtp_rows(tokens, segment_ids, valid, k, bases)
-        per_depth.append(rows)
-        bases = [r.base for r in rows]
-    return per_depth
+        states = depth_states(segment, active, k, parents)
+        out.append(states)
+        parents = [s.base for s in states]
+    return out
 
 
 def label_owned(active: Sequence[bool], segment: Sequence[int], t: int, k: int) -> bool:

@@ -15,7 +15,7 @@ import torch
 
 from deepseek_sequential_mtp_gb300 import lib, synth
 from oracle import chain as oc
-from oracle.rows import compile_all_depths, label_owned
+from oracle.rows import label_owned, states_all_depths
 
 pytestmark = pytest.mark.gpu
 
@@ -167,15 +167,13 @@ def test_mid_config_sampled_windows():
             checked += 1
     assert checked >= 3
     # counts over the whole batch equal the row compiler's, exactly
-    tok = inp["tokens"].numpy()
-    n_state = np.zeros(cfg.D, int)
     n_loss = np.zeros(cfg.D, int)
     n_main = 0
     for b in range(cfg.B):
         act = [s != -1 for s in seg[b]]
         n_main += sum(label_owned(act, list(seg[b]), t, 1) for t in range(cfg.T))
-        for k, rows in enumerate(compile_all_depths(list(tok[b]), list(seg[b]), act, cfg.D)):
-            n_loss[k] += sum(r_.loss_valid for r_ in rows)
+        for k, rows in enumerate(states_all_depths(list(seg[b]), act, cfg.D)):
+            n_loss[k] += sum(r_.supervised for r_ in rows)
     assert list(g["sums_counts"][1::2]) == [float(n_main)] + [float(c) for c in n_loss]
     # the reported terms are the reported row losses reduced by the policy
     rl = g["row_loss"]

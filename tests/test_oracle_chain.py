@@ -114,6 +114,49 @@ def test_projection_coordinate_expansion():
             assert math.isclose(got[i, r], u_r, rel_tol=1e-9, abs_tol=1e-12)
 
 
+def test_block_tail_swiglu_coordinates():
+    """FFN of the block (M7.6 §0x03C with the dense stand-in
+    h = a + (silu(y W_g^T) * (y W_u^T)) W_d^T, y = Norm_f(a)): with one-hot
+    rows in W_g and W_u and W_d an injection of the ffn coordinates into the
+    d outputs, h - a is silu(y_i) * y_j at the coordinate W_d sends the pair
+    to and zero elsewhere.  The pairs are asymmetric and W_d is not square,
+    so a swapped gate/up, a silu on the up branch or a transposed W_d fails.
+    The output projection is checked the same way: with W_d = 0 and W_o a
+    cyclic permutation, h = u + o W_o^T picks o at the permuted coordinate."""
+    d, ffn = 6, 4
+    cfg = synth.ChainConfig(name="t", B=1, T=3, d=d, n_heads=1, head_dim=d, ffn=ffn, V=9,
+                            D=1, dtype="f32", w_std=0.5, gain_std=0.3)
+    W = _tiny_weights(cfg, 7)
+    dims = oc.Dims(n_heads=1, head_dim=d, D=1)
+    rng = np.random.default_rng(8)
+    u = rng.standard_normal((3, d)) * 2.0
+    o = rng.standard_normal((3, d))
+    gate_src, up_src, dest = [1, 4, 0, 5], [3, 2, 5, 1], [3, 0, 5, 1]
+    W["wo"][0][:] = 0.0
+    W["w_gate"][0][:] = 0.0
+    W["w_up"][0][:] = 0.0
+    W["w_down"][0][:] = 0.0
+    for m in range(ffn):
+        W["w_gate"][0][m, gate_src[m]] = 1.0
+        W["w_up"][0][m, up_src[m]] = 1.0
+        W["w_down"][0][dest[m], m] = 1.0
+    h = oc.block_tail(u, o, W, 0, dims, lambda a: a)
+    g = W["ffn_norm"][0].astype(np.float64)
+    for i in range(3):
+        y = g * u[i] / math.sqrt(np.mean(u[i] ** 2) + 1e-6)
+        want = np.zeros(d)
+        for m in range(ffn):
+            want[dest[m]] = y[gate_src[m]] * scipy.special.expit(y[gate_src[m]]) * y[up_src[m]]
+        np.testing.assert_allclose(h[i] - u[i], want, rtol=1e-12, atol=1e-14)
+    # the output projection's orientation: W_o[r, perm[r]] = 1
+    perm = [2, 0, 4, 1, 5, 3]
+    W["w_down"][0][:] = 0.0
+    for r in range(d):
+        W["wo"][0][r, perm[r]] = 1.0
+    h = oc.block_tail(u, o, W, 0, dims, lambda a: a)
+    np.testing.assert_allclose(h, u + o[:, perm], rtol=1e-14)
+
+
 def _run(cfg, batch, h0, W, **kw):
     dims = oc.Dims(n_heads=cfg.n_heads, head_dim=cfg.head_dim, D=cfg.D)
     return oc.chain_forward_loss(batch["tokens"], batch["seg"], batch["pos"], h0, W, dims, **kw)

@@ -6,8 +6,8 @@ import numpy as np
 import pytest
 
 from conftest import read_golden
-from oracle.rows import (compile_all_depths, compile_mtp_rows, horizon_counts,
-                         label_owned, single_sequence_label_counts)
+from oracle.rows import (depth_states, horizon_counts, label_owned, same_segment_runs,
+                         single_sequence_label_counts, states_all_depths)
 
 
 def ints(vals):
@@ -18,15 +18,14 @@ def test_two_segment_fixture():
     f, _ = read_golden("rows_two_segments.txt")
     seg = ints(f["segments"])
     n = len(seg)
-    tokens = list(range(100, 100 + n))
     valid = [True] * n
-    d1 = compile_mtp_rows(tokens, seg, valid, 1, list(range(n)))
+    d1 = depth_states(seg, valid, 1, list(range(n)))
     assert [r.base for r in d1] == ints(f["depth1_state_bases"])
-    assert [r.base for r in d1 if r.loss_valid] == ints(f["depth1_supervised_bases"])
-    d2 = compile_mtp_rows(tokens, seg, valid, 2, [r.base for r in d1])
+    assert [r.base for r in d1 if r.supervised] == ints(f["depth1_supervised_bases"])
+    d2 = depth_states(seg, valid, 2, [r.base for r in d1])
     assert [r.base for r in d2] == ints(f["depth2_state_bases"])
-    assert [r.previous_depth_row for r in d2] == ints(f["depth2_previous_physical_rows"])
-    assert [r.base for r in d2 if r.loss_valid] == ints(f["depth2_supervised_bases"])
+    assert [r.parent for r in d2] == ints(f["depth2_previous_physical_rows"])
+    assert [r.base for r in d2 if r.supervised] == ints(f["depth2_supervised_bases"])
 
 
 def test_packed_label_ownership_counts():
@@ -38,12 +37,11 @@ def test_packed_label_ownership_counts():
     S = len(seg_rows[0])
     assert [len(seg_rows) * (S - k) for k in (1, 2, 3)] == ints(f["shape_only_counts_h1_h2_h3"])
     # MTP depth k is supervised at horizon k+1 and has state at horizon k.
-    toks = [ints(f["tokens_row0"]), ints(f["tokens_row1"])]
     n_state, n_loss = [0, 0], [0, 0]
-    for tok, seg, act in zip(toks, seg_rows, act_rows):
-        for k, rows in enumerate(compile_all_depths(tok, seg, act, 2)):
+    for seg, act in zip(seg_rows, act_rows):
+        for k, rows in enumerate(states_all_depths(seg, act, 2)):
             n_state[k] += len(rows)
-            n_loss[k] += sum(r.loss_valid for r in rows)
+            n_loss[k] += sum(r.supervised for r in rows)
     assert n_state == [9, 6]
     assert n_loss == [6, 3]
 
@@ -53,12 +51,12 @@ def test_single_sequence_counts_and_polynomial():
     T, D = int(f["T"][0]), int(f["D"][0])
     assert single_sequence_label_counts(T, D) == ints(f["counts"])
     assert D * (T - 1) - D * (D + 1) // 2 == int(f["unrestricted_polynomial"][0])
-    per_depth = compile_all_depths(list(range(T)), [0] * T, [True] * T, D)
-    assert [sum(r.loss_valid for r in rows) for rows in per_depth] == ints(f["counts"])
+    per_depth = states_all_depths([0] * T, [True] * T, D)
+    assert [sum(r.supervised for r in rows) for rows in per_depth] == ints(f["counts"])
     for T in range(2, 12):
         for D in range(1, T):
-            per_depth = compile_all_depths(list(range(T)), [0] * T, [True] * T, D)
-            n = sum(sum(r.loss_valid for r in rows) for rows in per_depth)
+            per_depth = states_all_depths([0] * T, [True] * T, D)
+            n = sum(sum(r.supervised for r in rows) for rows in per_depth)
             assert n == D * (T - 1) - D * (D + 1) // 2
 
 
@@ -66,11 +64,11 @@ def test_depth_two_rows_A_to_F():
     f, _ = read_golden("depth_two_rows_AF.txt")
     names = f["tokens"]
     n = len(names)
-    per_depth = compile_all_depths(list(range(n)), [0] * n, [True] * n, 2)
+    per_depth = states_all_depths([0] * n, [True] * n, 2)
     for k, key in enumerate(("depth1", "depth2")):
         want = [tuple(t.split(",")) for t in f[key]]
-        got = [(names[r.base], names[r.shifted_token_index], names[r.label_index])
-               for r in per_depth[k] if r.loss_valid]
+        got = [(names[r.base], names[r.input_at], names[r.label_at])
+               for r in per_depth[k] if r.supervised]
         assert got == want
 
 
@@ -82,9 +80,9 @@ def test_tiny_config_counts():
     assert horizon_counts(act_rows, seg_rows, 1) == [24]
     n_state = n_loss = 0
     for seg, act in zip(seg_rows, act_rows):
-        rows = compile_mtp_rows([0] * 16, seg, act, 1, list(range(16)))
+        rows = depth_states(seg, act, 1, list(range(16)))
         n_state += len(rows)
-        n_loss += sum(r.loss_valid for r in rows)
+        n_loss += sum(r.supervised for r in rows)
     assert (n_state, n_loss) == (24, 21)
 
 
@@ -108,27 +106,58 @@ def test_compiler_matches_label_ownership(seed):
     n = int(rng.integers(1, 25))
     seg = brute_force_segments(rng, n)
     act = [s != -1 for s in seg]
-    per_depth = compile_all_depths([0] * n, seg, act, 4)
+    per_depth = states_all_depths(seg, act, 4)
     for k, rows in enumerate(per_depth, start=1):
         state = {r.base for r in rows}
-        loss = {r.base for r in rows if r.loss_valid}
+        loss = {r.base for r in rows if r.supervised}
         assert state == {t for t in range(n) if label_owned(act, seg, t, k)}
         assert loss == {t for t in range(n) if label_owned(act, seg, t, k + 1)}
         for r in rows:  # physical row of the same base one depth up
-            assert r.shifted_token_index == r.base + k
-            if r.loss_valid:
-                assert r.label_index == r.base + k + 1
+            assert r.input_at == r.base + k
+            if r.supervised:
+                assert r.label_at == r.base + k + 1
+
+
+def brute_force_states(seg, act, k):
+    """Direct reading of the rule: every input i..i+k real and in i's segment."""
+    n = len(seg)
+    return [i for i in range(n - k)
+            if all(act[j] and seg[j] == seg[i] for j in range(i, i + k + 1))]
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_runs_match_direct_rule(seed):
+    """The run-length evaluation equals the rule read literally (all inputs
+    base..base+k present in the base's segment), including streams whose
+    segment ids repeat after padding or another segment."""
+    rng = np.random.default_rng(100 + seed)
+    n = int(rng.integers(1, 30))
+    seg = [int(v) for v in rng.integers(0, 3, n)]
+    act = [bool(v) for v in rng.random(n) > 0.15]
+    run = same_segment_runs(seg, act)
+    for j in range(n):
+        want = 0
+        while j + want < n and act[j + want] and seg[j + want] == seg[j]:
+            want += 1
+        assert run[j] == want
+    parents = list(range(n))
+    for k in range(1, 5):
+        rows = depth_states(seg, act, k, parents)
+        assert [r.base for r in rows] == brute_force_states(seg, act, k)
+        assert [r.base for r in rows if r.supervised] == brute_force_states(seg, act, k + 1)
+        assert all(parents[r.parent] == r.base for r in rows)
+        parents = [r.base for r in rows]
 
 
 def test_compiler_errors():
     with pytest.raises(ValueError):
-        compile_mtp_rows([1, 2], [0], [True, True], 1, [0, 1])
+        depth_states([0], [True, True], 1, [0, 1])
     for bad in (0, -1, True, 1.0):
         with pytest.raises(ValueError):
-            compile_mtp_rows([1, 2, 3], [0, 0, 0], [True] * 3, bad, [0, 1, 2])
+            depth_states([0, 0, 0], [True] * 3, bad, [0, 1, 2])
     with pytest.raises(ValueError):
-        compile_mtp_rows([1, 2, 3], [0, 0, 0], [True] * 3, 1, [0, 0])
+        depth_states([0, 0, 0], [True] * 3, 1, [0, 0])
     with pytest.raises(ValueError):
-        compile_mtp_rows([1, 2, 3], [0, 0, 0], [True] * 3, 1, [0, 3])
+        depth_states([0, 0, 0], [True] * 3, 1, [0, 3])
     with pytest.raises(ValueError):  # base 1 has support but no predecessor
-        compile_mtp_rows([1, 2, 3], [0, 0, 0], [True] * 3, 1, [0])
+        depth_states([0, 0, 0], [True] * 3, 1, [0])
