@@ -553,13 +553,8 @@ mtp_status attn_launch(int dtype, const void* qkv, void* out, const int32_t* seg
       mtp::note_launch();
     } else if (hd == 128) {
       constexpr int smem = (kBQ + 4 * kBK) * 128 * 2;
-      static bool attr = false;
-      if (!attr) {
-        if (cudaFuncSetAttribute(flash_attn_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
-          return MTP_ERR_CUDA;
-        attr = true;
-      }
+      static PerDevice attr;
+      if (!smem_limit(attr, flash_attn_bf16_kernel<128>, smem)) return MTP_ERR_CUDA;
       flash_attn_bf16_kernel<128><<<grid, kThreads, smem, stream>>>(
           static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out), seg_start, T, H, scale_log2,
           lse2_out);
@@ -571,13 +566,8 @@ mtp_status attn_launch(int dtype, const void* qkv, void* out, const int32_t* seg
     const int warps = 4;
     const size_t smem = static_cast<size_t>(warps) * T * sizeof(float);
     if (smem > 200 * 1024) return MTP_ERR_UNSUPPORTED;
-    static bool attr = false;
-    if (!attr) {
-      if (cudaFuncSetAttribute(attn_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
-          cudaSuccess)
-        return MTP_ERR_CUDA;
-      attr = true;
-    }
+    static PerDevice attr;
+    if (!smem_limit(attr, attn_f32_kernel, 200 * 1024)) return MTP_ERR_CUDA;
     const int items = B * T * H;
     attn_f32_kernel<<<(items + warps - 1) / warps, warps * 32, smem, stream>>>(
         static_cast<const float*>(qkv), static_cast<float*>(out), seg_start, B * T, T, H, hd,
@@ -602,25 +592,15 @@ mtp_status attn_bwd_launch(const __nv_bfloat16* qkv, const __nv_bfloat16* o, con
   if (hd == 64) {
     attn_dsum_kernel<64><<<(items + 7) / 8, 256, 0, stream>>>(o, dO, dsum, items, H);
     constexpr int smem = (6 * kBK * 64 + kBK * kBQ) * 2 + 2 * kBQ * 12 + 64;
-    static bool attr = false;
-    if (!attr) {
-      if (cudaFuncSetAttribute(flash_attn_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-          cudaSuccess)
-        return MTP_ERR_CUDA;
-      attr = true;
-    }
+    static PerDevice attr;
+    if (!smem_limit(attr, flash_attn_bwd_kernel<64>, smem)) return MTP_ERR_CUDA;
     flash_attn_bwd_kernel<64><<<grid, kThreads, smem, stream>>>(qkv, dO, lse2, dsum, seg_start, seg_end, dqkv, T, H,
                                                                 scale_log2, scale);
   } else if (hd == 128) {
     attn_dsum_kernel<128><<<(items + 7) / 8, 256, 0, stream>>>(o, dO, dsum, items, H);
     constexpr int smem = (6 * kBK * 128 + kBK * kBQ) * 2 + 2 * kBQ * 12 + 64;
-    static bool attr = false;
-    if (!attr) {
-      if (cudaFuncSetAttribute(flash_attn_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-          cudaSuccess)
-        return MTP_ERR_CUDA;
-      attr = true;
-    }
+    static PerDevice attr;
+    if (!smem_limit(attr, flash_attn_bwd_kernel<128>, smem)) return MTP_ERR_CUDA;
     flash_attn_bwd_kernel<128><<<grid, kThreads, smem, stream>>>(qkv, dO, lse2, dsum, seg_start, seg_end, dqkv, T,
                                                                  H, scale_log2, scale);
   } else {

@@ -1362,13 +1362,7 @@ SaveOff make_save_off(const mtp_dims& D) {
 // splits, at least 8 k-blocks per split).
 mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, bool a_mn, const __nv_bfloat16* B, int ldb,
                     bool b_mn, float* out, int ldo, cudaStream_t st, bool overwrite) {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
-  }
+  const int sms = mtp::sm_count_current();
   mtp::GemmDesc g = gdesc(M, N, K, A, lda, B, ldb);
   g.epi = mtp::EPI_F32_ACC;
   g.a_mn = a_mn;

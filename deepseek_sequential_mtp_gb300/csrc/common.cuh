@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/mtp.h"
 
 #define MTP_CUDA_TRY(expr)                                \
@@ -42,6 +44,44 @@ void prof_begin(int kernel_class, cudaStream_t stream);
 void prof_end(int kernel_class, cudaStream_t stream);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch attributes (the dynamic shared-memory limit of a kernel) and device
+// properties belong to one device, so a process that drives several GPUs
+// keeps one entry per device ordinal.  Objects of static storage duration
+// start zeroed; concurrent first calls may both set an attribute, which is
+// harmless.
+constexpr int kMaxDevices = 64;
+struct PerDevice {
+  std::atomic<int> v[kMaxDevices];
+};
+inline int current_device() {
+  int d = -1;
+  return cudaGetDevice(&d) == cudaSuccess ? d : -1;
+}
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device.
+template <typename Kernel>
+inline bool smem_limit(PerDevice& done, Kernel* kernel, int bytes) {
+  const int dev = current_device();
+  if (dev < 0) return false;
+  if (dev < kMaxDevices && done.v[dev].load(std::memory_order_acquire)) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  if (dev < kMaxDevices) done.v[dev].store(1, std::memory_order_release);
+  return true;
+}
+// Streaming multiprocessors of the current device (cached per device).
+inline int sm_count_current() {
+  static PerDevice cache;
+  const int dev = current_device();
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = cache.v[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (dev < 0 || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev >= 0 && dev < kMaxDevices) cache.v[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
 
 // Bounded waits count SM clock cycles (clock64 is monotonic per SM; the
 // global nanosecond timer can step when it is resynchronised with the host).

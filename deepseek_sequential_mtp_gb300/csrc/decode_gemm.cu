@@ -236,14 +236,7 @@ dgemm_bf16_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constan
 }
 
 int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
+  return sm_count_current();
 }
 
 }  // namespace
@@ -276,11 +269,8 @@ mtp_status dgemm_bf16_launch(const DecSeg* segs, int nseg, int K, const __nv_bfl
   for (int i = nseg; i < 3; ++i) tw[i] = tw[0];
   if (!tensor_map_bf16_2d(&tx, x, R, K, K, kBK, kTok, true)) return MTP_ERR_CUDA;
   P.total = static_cast<int>(total);
-  static bool attr = false;
-  if (!attr) {
-    MTP_CUDA_TRY(cudaFuncSetAttribute(dgemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
-    attr = true;
-  }
+  static PerDevice attr;
+  if (!smem_limit(attr, dgemm_bf16_kernel, kSmemBytes)) return MTP_ERR_CUDA;
   const int grid = static_cast<int>(total < sm_count() ? total : sm_count());
   dgemm_bf16_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tw[0], tw[1], tw[2], tx, P);
   note_launch();

@@ -863,14 +863,7 @@ bool draft_dims_ok(const mtp_dims& D) {
 }
 
 int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
+  return mtp::sm_count_current();
 }
 
 // out[R, ldo] (fp32) = X[R, K] · W[features, K]^T: the swap-AB tcgen05 GEMM (weights on the
@@ -988,24 +981,16 @@ mtp_status draft_one_step(const mtp_dims& D, const mtp_weights* w, const mtp_blo
     return MTP_ERR_CUDA;
   mtp::prof_begin(MTP_KC_ATTENTION, st);
   if (hd == 128) {
-    static bool attr = false;
-    if (!attr) {
-      MTP_CUDA_TRY(cudaFuncSetAttribute(decode_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        AttnCfg<128>::kSmemBytes));
-      attr = true;
-    }
+    static mtp::PerDevice attr;
+    if (!mtp::smem_limit(attr, decode_attn_kernel<128>, AttnCfg<128>::kSmemBytes)) return MTP_ERR_CUDA;
     decode_attn_kernel<128><<<agrid, kAttnThreads, AttnCfg<128>::kSmemBytes, st>>>(
         tmk, tmv, qkv, ctx_len, part, H, D.T, n_split, split_keys, n_units, scale);
     mtp::note_launch();
     decode_attn_combine_kernel<128><<<(R * H + 7) / 8, 256, 0, st>>>(qkv, sk, sv, gamma, step + 1, part, o, R, H,
                                                                      n_split, scale);
   } else {
-    static bool attr = false;
-    if (!attr) {
-      MTP_CUDA_TRY(cudaFuncSetAttribute(decode_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        AttnCfg<64>::kSmemBytes));
-      attr = true;
-    }
+    static mtp::PerDevice attr;
+    if (!mtp::smem_limit(attr, decode_attn_kernel<64>, AttnCfg<64>::kSmemBytes)) return MTP_ERR_CUDA;
     decode_attn_kernel<64><<<agrid, kAttnThreads, AttnCfg<64>::kSmemBytes, st>>>(
         tmk, tmv, qkv, ctx_len, part, H, D.T, n_split, split_keys, n_units, scale);
     mtp::note_launch();

@@ -335,14 +335,7 @@ __global__ void __launch_bounds__(256) split_act_kernel(const __nv_bfloat16* __r
 }
 
 int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
+  return sm_count_current();
 }
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
@@ -392,11 +385,8 @@ mtp_status fp8w_gemm_launch(const Fp8Seg* segs, int nseg, int K, const __nv_bflo
   for (int i = nseg; i < 3; ++i) tw[i] = tw[0];
   if (!tensor_map_u8_2d(&ta, a, 2 * kTok, K, K, kKb, 2 * kTok)) return MTP_ERR_CUDA;
   P.total = static_cast<int>(total);
-  static bool attr = false;
-  if (!attr) {
-    MTP_CUDA_TRY(cudaFuncSetAttribute(fp8w_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
-    attr = true;
-  }
+  static PerDevice attr;
+  if (!smem_limit(attr, fp8w_gemm_kernel, kSmemBytes)) return MTP_ERR_CUDA;
   const int warps = kTok * P.nkb;
   split_act_kernel<<<(warps + 7) / 8, 256, 0, stream>>>(x, R, K, P.nkb, a, xs);
   note_launch();

@@ -992,26 +992,14 @@ bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int ld, int b
 }
 
 int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
+  return sm_count_current();
 }
 
 template <int BN, int EPI, int MNF = 0, bool PAIR = false>
 mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
   using C = Cfg<BN, EPI, PAIR>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, MNF, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes) != cudaSuccess)
-      return MTP_ERR_CUDA;
-    attr_done = true;
-  }
+  static PerDevice attr;
+  if (!smem_limit(attr, gemm_tc_kernel<BN, EPI, MNF, PAIR>, C::kSmemBytes)) return MTP_ERR_CUDA;
   CUtensorMap ta, tb[3];
   const int box_b = (EPI == EPI_SWIGLU || PAIR) ? BN / 2 : BN;  // a pair stages half of B per CTA
   // MN-major operands are [K rows][M or N] in memory, loaded as [64 x 64] boxes

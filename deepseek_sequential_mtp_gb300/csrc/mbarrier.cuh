@@ -36,13 +36,14 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // Wait until the phase of parity `parity` has completed; false once the wait
 // limit has passed.  A parity wait cannot distinguish phase u+1 from u-1, so
 // callers must never wait more than one phase ahead of the barrier.
-static __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+static __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                        long long limit_cycles = kWaitLimitCycles) {
   if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = cycles_now();
   for (uint32_t it = 1;; ++it) {
     if (mbar_test_wait(bar, parity)) return true;
     if (it > 64) __nanosleep(32);
-    if ((it & 31u) == 0 && cycles_now() - t0 > kWaitLimitCycles) return false;
+    if ((it & 31u) == 0 && cycles_now() - t0 > limit_cycles) return false;
   }
 }
 __device__ __forceinline__ uint32_t cluster_addr(uint32_t a, uint32_t rank) {

@@ -10,7 +10,10 @@
 // cudaMalloc, cudaFree or allocating library routine.  All calls share the
 // one array, so calls that overlap on the GPU (other streams, other threads)
 // race on it; the chain rewrites every scratch element it reads, so no part
-// of the array has to start at zero.
+// of the array has to start at zero.  The cached address belongs to the
+// device's primary context: after cudaDeviceReset (or anything else that
+// destroys that context) it is stale, so a process that resets a device must
+// not call this entry point on that device again.
 #include <mutex>
 
 #include "common.cuh"
@@ -18,18 +21,17 @@
 namespace {
 
 constexpr size_t kScratchBytes = MTP_NOALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_setup_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+void* g_scratch_ptr[mtp::kMaxDevices] = {};
 
 // Device address of the scratch array on the current device (looked up once).
 mtp_status scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MTP_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return MTP_ERR_UNSUPPORTED;
+  if (dev < 0 || dev >= mtp::kMaxDevices) return MTP_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   if (!g_scratch_ptr[dev]) {
     void* ptr = nullptr;
@@ -51,7 +53,11 @@ extern "C" mtp_status mtp_chain_loss_noalloc(const mtp_dims* dims, const mtp_wei
                                              float* row_loss, void* h_out, cudaStream_t stream) {
   if (!dims) return MTP_ERR_INVALID_ARG;
   const size_t need = mtp_chain_workspace_bytes(dims);
-  if (need == 0) return MTP_ERR_SHAPE;
+  // invalid or unsupported dimensions: the workspace entry point's own checks
+  // give the status (they fail before any launch)
+  if (need == 0)
+    return mtp_chain_loss(dims, w, tokens, seg, pos, h0, lambda, den, with_main, sums_counts, losses, row_loss,
+                          h_out, nullptr, 0, stream);
   if (need > kScratchBytes) return MTP_ERR_WORKSPACE;
   void* scratch = nullptr;
   const mtp_status st = scratch_for_current_device(&scratch);

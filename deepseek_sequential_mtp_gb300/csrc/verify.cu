@@ -119,15 +119,20 @@ using mtp::mbar_arrive_cnt;
 using mtp::mbar_expect_tx;
 using mtp::mbar_init;
 using mtp::smem_u32;
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) { return mtp::mbar_wait_bounded(bar, parity); }
-
-template <bool kVec4>
+// kStarve (failure-path test only): the producer issues no copy, so every
+// consumer's first ring wait runs out after `wait_limit` cycles with nothing
+// in flight; the request then ends with MTP_VERIFY_DEVICE_TIMEOUT and the
+// error word's MTP_DEVERR_TIMEOUT, as a real stall would.
+template <bool kVec4, bool kStarve>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* __restrict__ q,
                    const int32_t* __restrict__ draft, uint2 key, uint32_t off_lo, uint32_t off_hi,
                    const int32_t* __restrict__ eos, const int32_t* __restrict__ remaining,
                    int32_t* __restrict__ accepted, int32_t* __restrict__ next_token,
-                   int32_t* __restrict__ n_emit, int32_t* __restrict__ status) {
+                   int32_t* __restrict__ n_emit, int32_t* __restrict__ status, long long wait_limit) {
+  auto mbar_wait = [wait_limit](uint32_t bar, uint32_t parity) {
+    return mtp::mbar_wait_bounded(bar, parity, wait_limit);
+  };
   extern __shared__ __align__(128) uint8_t ring[];   // kRing stages of p and q chunks
   __shared__ float2 s_all[kMaxChunks];  // CTA 0: (hi, lo) sum of every chunk of the request
   __shared__ float s_w[kChunk];
@@ -227,7 +232,7 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
   bool bad = false;
   float2* all0 = cluster.map_shared_rank(s_all, 0);  // rank 0's chunk table
   if constexpr (kVec4) {
-    const int n_stages = (n_local + kStageChunks - 1) / kStageChunks;
+    const int n_stages = kStarve ? 0 : (n_local + kStageChunks - 1) / kStageChunks;
     if (warp == kConsumerWarps) {
       // producer warp: every lane waits, lane 0 issues the copies
       int issued_last = -1;
@@ -449,13 +454,11 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
   }
 }
 
-}  // namespace
-
-extern "C" mtp_status spec_verify(int R, int gamma, int V, const float* p, const float* q,
-                                  const int32_t* draft, uint64_t seed, uint64_t offset,
-                                  const int32_t* eos, const int32_t* remaining,
-                                  int32_t* accepted, int32_t* next_token, int32_t* n_emit,
-                                  int32_t* status, cudaStream_t stream) {
+template <bool kStarve>
+mtp_status verify_launch(int R, int gamma, int V, const float* p, const float* q, const int32_t* draft,
+                         uint64_t seed, uint64_t offset, const int32_t* eos, const int32_t* remaining,
+                         int32_t* accepted, int32_t* next_token, int32_t* n_emit, int32_t* status,
+                         long long wait_limit, cudaStream_t stream) {
   if (R < 0 || gamma < 0 || V <= 0) return MTP_ERR_INVALID_ARG;
   if (gamma > kMaxGamma || V > kMaxChunks * kChunk) return MTP_ERR_UNSUPPORTED;
   if (R == 0) return MTP_OK;
@@ -463,25 +466,39 @@ extern "C" mtp_status spec_verify(int R, int gamma, int V, const float* p, const
   if (gamma > 0 && !q) return MTP_ERR_INVALID_ARG;
   const uint2 key = make_uint2((uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32));
   const uint32_t olo = (uint32_t)(offset & 0xFFFFFFFFu), ohi = (uint32_t)(offset >> 32);
-  mtp::prof_begin(MTP_KC_SPEC_VERIFY, stream);
   const bool vec = (V % 4 == 0) && mtp::aligned16(p) && (gamma == 0 || mtp::aligned16(q));
-  if (vec) {
-    static bool attr = false;
-    if (!attr) {
-      if (cudaFuncSetAttribute(spec_verify_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes) !=
-          cudaSuccess)
-        return MTP_ERR_CUDA;
-      attr = true;
-    }
-  }
+  if (kStarve && !vec) return MTP_ERR_UNSUPPORTED;  // the ring exists only on the bulk-copy path
+  static mtp::PerDevice attr;
+  if (vec && !mtp::smem_limit(attr, spec_verify_kernel<true, kStarve>, kRingBytes)) return MTP_ERR_CUDA;
+  if (!kStarve) mtp::prof_begin(MTP_KC_SPEC_VERIFY, stream);
   if (vec)
-    spec_verify_kernel<true><<<R * kCluster, kThreads, kRingBytes, stream>>>(gamma, V, p, q, draft, key, olo, ohi, eos,
-                                                          remaining, accepted, next_token, n_emit, status);
+    spec_verify_kernel<true, kStarve><<<R * kCluster, kThreads, kRingBytes, stream>>>(
+        gamma, V, p, q, draft, key, olo, ohi, eos, remaining, accepted, next_token, n_emit, status, wait_limit);
   else
-    spec_verify_kernel<false><<<R * kCluster, kThreads, 0, stream>>>(gamma, V, p, q, draft, key, olo, ohi, eos,
-                                                           remaining, accepted, next_token, n_emit, status);
+    spec_verify_kernel<false, false><<<R * kCluster, kThreads, 0, stream>>>(
+        gamma, V, p, q, draft, key, olo, ohi, eos, remaining, accepted, next_token, n_emit, status, wait_limit);
   mtp::note_launch();
-  mtp::prof_end(MTP_KC_SPEC_VERIFY, stream);
+  if (!kStarve) mtp::prof_end(MTP_KC_SPEC_VERIFY, stream);
   MTP_LAUNCH_CHECK();
   return MTP_OK;
+}
+
+}  // namespace
+
+extern "C" mtp_status spec_verify(int R, int gamma, int V, const float* p, const float* q,
+                                  const int32_t* draft, uint64_t seed, uint64_t offset,
+                                  const int32_t* eos, const int32_t* remaining,
+                                  int32_t* accepted, int32_t* next_token, int32_t* n_emit,
+                                  int32_t* status, cudaStream_t stream) {
+  return verify_launch<false>(R, gamma, V, p, q, draft, seed, offset, eos, remaining, accepted, next_token, n_emit,
+                              status, mtp::kWaitLimitCycles, stream);
+}
+
+extern "C" mtp_status mtp_diag_verify_starved(int R, int gamma, int V, const float* p, const float* q,
+                                              const int32_t* draft, uint64_t seed, uint64_t offset,
+                                              int32_t* accepted, int32_t* next_token, int32_t* n_emit,
+                                              int32_t* status, long long wait_limit_cycles, cudaStream_t stream) {
+  if (wait_limit_cycles <= 0 || wait_limit_cycles > mtp::kWaitLimitCycles) return MTP_ERR_INVALID_ARG;
+  return verify_launch<true>(R, gamma, V, p, q, draft, seed, offset, nullptr, nullptr, accepted, next_token,
+                             n_emit, status, wait_limit_cycles, stream);
 }

@@ -124,6 +124,9 @@ def load() -> ctypes.CDLL:
     lib.mtp_chain_loss_grad.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Weights), vp, vp, vp, vp,
                                         ctypes.c_float, i32, i32, ctypes.POINTER(ctypes.c_float), vp, vp,
                                         ctypes.POINTER(Grads), vp, sz, vp]
+    lib.mtp_diag_verify_starved.restype = i32
+    lib.mtp_diag_verify_starved.argtypes = [i32, i32, i32, vp, vp, vp, u64, u64, vp, vp, vp, vp,
+                                            ctypes.c_longlong, vp]
     lib.mtp_kernel_launches.restype = ctypes.c_ulonglong
     lib.mtp_kernel_launches.argtypes = []
     _lib = lib
@@ -189,6 +192,25 @@ def spec_verify(p: torch.Tensor, q: torch.Tensor, draft: torch.Tensor, seed: int
                             _ptr(out["next_token"]), _ptr(out["n_emit"]), _ptr(out["status"]),
                             _stream(stream))
     _check(st, "spec_verify")
+    return out
+
+
+def verify_starved(p: torch.Tensor, q: torch.Tensor, draft: torch.Tensor, seed: int, offset: int,
+                   wait_limit_cycles: int, stream=None) -> dict:
+    """spec_verify with a producer that issues no copy, so every row sweep's
+    bounded wait runs out (include/mtp.h: mtp_diag_verify_starved)."""
+    R, gamma = draft.shape
+    V = p.shape[-1]
+    _need(p, "p", torch.float32)
+    _need(q, "q", torch.float32)
+    _need(draft, "draft", torch.int32)
+    out = {k: torch.empty(R, dtype=torch.int32, device=p.device)
+           for k in ("accepted", "next_token", "n_emit", "status")}
+    st = load().mtp_diag_verify_starved(R, gamma, V, _ptr(p), _ptr(q), _ptr(draft),
+                                        int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                                        _ptr(out["accepted"]), _ptr(out["next_token"]), _ptr(out["n_emit"]),
+                                        _ptr(out["status"]), int(wait_limit_cycles), _stream(stream))
+    _check(st, "mtp_diag_verify_starved")
     return out
 
 

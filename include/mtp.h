@@ -197,7 +197,9 @@ mtp_status mtp_chain_loss(const mtp_dims* dims, const mtp_weights* w,
  * exits.  Returns MTP_ERR_WORKSPACE, launching nothing, when
  * mtp_chain_workspace_bytes(dims) exceeds that size (small shapes only).  The
  * first call on a device looks up the array's device address with that device
- * current; make that first call before any stream capture.  Calls share the
+ * current; make that first call before any stream capture.  The address is
+ * kept for the life of the process: after cudaDeviceReset of a device, do not
+ * call this entry point on that device again.  Calls share the
  * one array: calls that overlap on the GPU race, so serialise them (one
  * stream, or events).  It allocates nothing itself. */
 #define MTP_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
@@ -415,6 +417,26 @@ mtp_status mtp_gemm_decode_bf16(int R, int N, int K, const void* x, const void* 
  * with fp32 atomics.  Leading dimensions % 8 == 0; pointers 16-byte aligned. */
 mtp_status mtp_gemm_f32acc(int M, int N, int K, const void* A, int lda, int a_mn, const void* B, int ldb, int b_mn,
                            float* out, int ldo, int splits, cudaStream_t stream);
+
+/* Failure-path diagnostic of spec_verify's bounded waits (the method has no
+ * counterpart; it exercises the failure detection every pipeline wait of
+ * this library relies on).  Runs spec_verify's bulk-copy kernel with the same
+ * arguments (no EOS, no budget) except that its producer issues no copy, so
+ * each request that reaches the row sweep (a rejection or a bonus draw)
+ * waits on a ring stage nothing will fill; that wait gives up after
+ * `wait_limit_cycles` SM clock cycles (1 .. the library's limit of 3e9,
+ * ~1.5 s) with no copy in flight.  Such requests end with status
+ * MTP_VERIFY_DEVICE_TIMEOUT, accepted = the accept prefix, next_token = -1,
+ * and the device error word gets MTP_DEVERR_TIMEOUT | MTP_DEVERR_FROM_VERIFY
+ * (read and cleared by mtp_check_errors); requests that end in the accept
+ * phase (invalid draft) report as spec_verify would.  The kernel returns
+ * normally and the stream stays usable.  Requires V % 4 == 0 and 16-byte
+ * aligned p and q (else MTP_ERR_UNSUPPORTED); other argument errors as
+ * spec_verify, plus MTP_ERR_INVALID_ARG for a limit out of range. */
+mtp_status mtp_diag_verify_starved(int R, int gamma, int V, const float* p, const float* q,
+                                   const int32_t* draft, uint64_t seed, uint64_t offset,
+                                   int32_t* accepted, int32_t* next_token, int32_t* n_emit,
+                                   int32_t* status, long long wait_limit_cycles, cudaStream_t stream);
 
 /* Kernel classes for mtp_profile_kernel. */
 enum {

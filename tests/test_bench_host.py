@@ -21,13 +21,15 @@ def test_step_roofline_counts_state_rows_and_visible_pairs():
     # t = 0, 1 (next token in the same segment) and t = 3; t = 2 and t = 4 end their segments.
     seg = np.array([[0, 0, 0, 1, 1, -1]], dtype=np.int32)
     cfg = _Cfg()
-    peaks = {"bf16_tflops_sustained": 1.0, "hbm_gbs": 1.0}  # 1e12 FLOP/s, 1e9 B/s
+    peaks = {"bf16_tflops": 1.0, "hbm_gbs": 1.0}  # 1e12 FLOP/s, 1e9 B/s
     r = bench.step_roofline(cfg, seg, [5.0, 2.0], 1000.0, 1.0, peaks)
     rows, pairs = 3, 1 + 2 + 1  # keys from the segment start to t: 1, 2 and 1
     d, f, V = cfg.d, cfg.ffn, cfg.V
     t = r["terms_ms"]
     assert np.isclose(t["gemm_block"], rows * (12 * d * d + 6 * d * f) / 1e12 * 1e3)
-    assert np.isclose(t["attention"], 4 * d * pairs / 1e12 * 1e3)
+    # attention: the larger of its FLOPs (4 d per visible pair) and its bytes (q, k, v read and
+    # o written in bf16 per row with state)
+    assert np.isclose(t["attention"], max(4 * d * pairs / 1e12, rows * 8 * d / 1e9) * 1e3)
     assert np.isclose(t["head_ce"], 2 * d * V * 7.0 / 1e12 * 1e3)
     assert np.isclose(t["norms_prologue"], rows * (8 * d + 8 * d) / 1e9 * 1e3)
     assert np.isclose(t["head_norms"], 4 * d * 7.0 / 1e9 * 1e3)
@@ -40,12 +42,12 @@ def test_step_roofline_depth_two_drops_segment_tails():
     # depth 2 needs t + 2 in t's segment: in a 4-token segment that is t = 0, 1 only
     seg = np.array([[7, 7, 7, 7]], dtype=np.int32)
     cfg = _Cfg(D=2)
-    peaks = {"bf16_tflops_sustained": 1.0, "hbm_gbs": 1.0}
+    peaks = {"bf16_tflops": 1.0, "hbm_gbs": 1.0}
     r = bench.step_roofline(cfg, seg, [0.0, 0.0, 0.0], 0.0, 1.0, peaks)
     rows = 3 + 2  # depth 1: t = 0, 1, 2; depth 2: t = 0, 1
     pairs = (1 + 2 + 3) + (1 + 2)
     assert np.isclose(r["terms_ms"]["gemm_block"], rows * (12 * cfg.d ** 2 + 6 * cfg.d * cfg.ffn) / 1e9)
-    assert np.isclose(r["terms_ms"]["attention"], 4 * cfg.d * pairs / 1e9)
+    assert np.isclose(r["terms_ms"]["attention"], max(4 * cfg.d * pairs / 1e9, rows * 8 * cfg.d / 1e6))
 
 
 def test_code_lines_ignores_comments_and_blank_lines():

@@ -64,6 +64,8 @@ def compare_rows(cfg, g, r, window=None):
     assert np.all(np.isfinite(gh[mh]))
     err = np.abs(gh[mh] - rh[mh])
     assert np.all(err <= atol + rtol * np.abs(rh[mh])), f"h max err {err.max()}"
+    if cfg.dtype == "bf16":  # beyond the pure 2e-2 bar only where one bf16 ulp exceeds it
+        assert (err > atol).mean() <= 1e-3, f"share of h beyond {atol}: {(err > atol).mean()}"
     ml = np.isfinite(rl)
     assert np.array_equal(np.isfinite(gl[ml]), np.ones(ml.sum(), bool))
     lerr = np.abs(gl[ml] - rl[ml]) / np.abs(rl[ml])
@@ -195,3 +197,56 @@ def test_dsv3_width_sampled_windows():
         r = run_oracle(cfg, inp, W=W, window=(0, s0, s1), lam=cfg.lam)
         compare_rows(cfg, g, r, window=(0, s0, s1))
     assert list(g["sums_counts"][1::2]) == [4094.0, 4092.0]
+
+
+LONG_SEGMENTS = [
+    synth.ChainConfig(name="long_hd64", B=1, T=4096, d=256, n_heads=4, head_dim=64, ffn=704,
+                      V=1000, D=1, dtype="bf16", w_std=0.05, gain_std=0.1, tokens="zipf",
+                      layout="split", split_at=2048),
+    synth.ChainConfig(name="long_hd128", B=1, T=4096, d=256, n_heads=2, head_dim=128, ffn=704,
+                      V=1000, D=1, dtype="bf16", w_std=0.05, gain_std=0.1, tokens="zipf",
+                      layout="split", split_at=2048),
+]
+
+
+@pytest.mark.parametrize("cfg", LONG_SEGMENTS, ids=lambda c: c.name)
+def test_long_segments_whole(cfg):
+    """Two 2048-token segments in one 4096-row stream (the DeepSeek-V3-width
+    workload's packing at a small width): the oracle runs each whole segment,
+    so every query row is compared, including those whose keys span all 32
+    key blocks of 64 and the online-softmax rescales along them (M7.6 §0x04C
+    segment rule).  One depth, as in that workload: a second depth adds
+    nothing to the attention path and, with these weights, compounds the
+    first depth's bf16 rounding flips through cancellations (h = a + FFN with
+    |a| ~ 2-4 and |h| ~ 0.4) to ~2 ulps of a on isolated elements."""
+    inp = synth.make_chain_inputs(cfg, seed=21)
+    g = run_gpu(cfg, to_dev(inp))
+    W = oc.weights_to_numpy(inp["weights"])
+    for (s0, s1) in ((0, 2048), (2048, 4096)):
+        r = run_oracle(cfg, inp, W=W, window=(0, s0, s1), lam=cfg.lam)
+        compare_rows(cfg, g, r, window=(0, s0, s1))
+    assert list(g["sums_counts"][1::2]) == [4094.0] + [4092.0 - 2 * k for k in range(cfg.D)]
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "small_bf16_D2", "small_bf16_hd128"])
+def test_chain_forward(name):
+    """mtp_chain_forward: h^1..h^D on every state row against the oracle, and
+    bit-identical to the states the loss entry point writes."""
+    cfg = synth.CHAIN_CONFIGS[name]
+    inp = synth.make_chain_inputs(cfg, seed=13)
+    dev = to_dev(inp)
+    chain = lib.Chain(cfg, dev["weights"])
+    dt = synth.torch_dtype(cfg.dtype)
+    h = torch.full((cfg.D, cfg.B, cfg.T, cfg.d), float("nan"), dtype=dt, device="cuda")
+    chain.forward(dev["tokens"], dev["seg"], dev["pos"], dev["h0"], h_out=h)
+    lib.check_errors()
+    r = run_oracle(cfg, inp, with_loss=False)
+    rh = r["h"]
+    mh = np.isfinite(rh)
+    gh = h.float().cpu().numpy()
+    assert mh.any() and np.all(np.isfinite(gh[mh]))
+    atol, rtol, _ = tolerances(cfg)
+    err = np.abs(gh[mh] - rh[mh])
+    assert np.all(err <= atol + rtol * np.abs(rh[mh])), f"h max err {err.max()}"
+    g = run_gpu(cfg, dev)
+    assert np.array_equal(g["h"][mh], gh[mh])

@@ -7,6 +7,7 @@ running sum lies within 1e-7 (relative to the row's mass) of the draw point:
 the kernel forms each residual in fp32 (one rounding, at most 2^-24 of the
 element) and sums those with error-free compensated steps, so its running
 sums agree with the exact fp64 sums to 2^-24 = 6e-8 of their value."""
+import ctypes
 import math
 
 import numpy as np
@@ -111,6 +112,59 @@ def test_expected_emitted_monte_carlo(V):
         assert abs(n.mean() - want) < 4 * se, (n.mean(), want, se)
 
 
+def test_config4_monte_carlo_expected_emitted():
+    """E[N_emit] on the verify workload itself (R=64, γ=4, V=129280) over
+    10^4 rounds per request, each round with fresh drafts y_j ~ q_j (host
+    inverse CDF) and fresh uniforms (offset = round).  Position j of request
+    r accepts with probability α_{r,j} = Σ_v min(p_{r,j,v}, q_{r,j,v}) (the
+    speculative-decoding page's acceptance mass), so with neither EOS nor a
+    budget E[N_emit | r] = Σ_{j=0..γ} Π_{i<j} α_{r,i}, which is the closed
+    form (1 - α^{γ+1}) / (1 - α) when every α_{r,j} equals α.  The α_{r,j} of
+    this workload spread over ~0.58..0.94 around α̂ = 0.700, which puts the
+    closed form at α̂ (2.774) 0.014 above the exact mean (2.759): more than
+    four standard errors of 6.4e5 rounds, so the mean is held to the exact
+    per-request expectation and the closed form is checked at α̂ only to
+    that heterogeneity gap."""
+    cfg = synth.VERIFY_C4
+    case = synth.make_verify_inputs(cfg, seed=1)
+    R, gamma, V = cfg.R, cfg.gamma, cfg.V
+    p64, q64 = case["p"].double(), case["q"].double()
+    alpha = torch.minimum(p64[:, :gamma], q64).sum(-1).numpy()
+    exact = 1.0 + np.cumprod(alpha, axis=1).sum(axis=1)
+    a_hat = alpha.mean()
+    assert abs(a_hat - 0.70) < 0.005
+    closed = (1 - a_hat ** (gamma + 1)) / (1 - a_hat)
+    assert abs(closed - exact.mean()) < 0.03
+
+    rounds = 10000
+    rng = np.random.default_rng(2024)
+    drafts = np.empty((rounds, R, gamma), dtype=np.int32)
+    qn = case["q"].numpy()
+    for r in range(R):
+        for j in range(gamma):
+            cdf = np.cumsum(qn[r, j].astype(np.float64))
+            x = rng.random(rounds) * cdf[-1]
+            drafts[:, r, j] = np.minimum(np.searchsorted(cdf, x, side="right"), V - 1)
+    dev = "cuda"
+    p, q = case["p"].to(dev), case["q"].to(dev)
+    y = torch.from_numpy(drafts).to(dev)
+    out = torch.empty((rounds, 4, R), dtype=torch.int32, device=dev)
+    for i in range(rounds):
+        o = out[i]
+        lib.spec_verify(p, q, y[i], seed=31, offset=i,
+                        out={"accepted": o[0], "next_token": o[1], "n_emit": o[2], "status": o[3]})
+    assert lib.check_errors() == 0
+    res = out.cpu().numpy()
+    assert np.all(res[:, 3] == 0)
+    n_emit = res[:, 2].astype(np.float64)          # [rounds, R]
+    assert np.array_equal(n_emit, res[:, 0] + 1.0)  # no EOS, no budget: N = A + 1
+    per_req = n_emit.mean(axis=0)
+    se_req = n_emit.std(axis=0, ddof=1) / math.sqrt(rounds)
+    assert np.all(np.abs(per_req - exact) < 5 * se_req), np.max(np.abs(per_req - exact) / se_req)
+    se = math.sqrt((se_req ** 2).sum()) / R
+    assert abs(per_req.mean() - exact.mean()) < 4 * se, (per_req.mean(), exact.mean(), se)
+
+
 def test_worked_example_correction_is_index_zero():
     p = torch.tensor([[0.6, 0.3, 0.1], [0.6, 0.3, 0.1]]).expand(4000, 2, 3).contiguous()
     q = torch.tensor([[0.4, 0.4, 0.2]]).expand(4000, 1, 3).contiguous()
@@ -145,3 +199,35 @@ def test_ring_with_cold_cache_is_deterministic():
         res[mode] = out.cpu()
     assert torch.equal(res["flushed"], res["warm"])
     assert int((res["warm"][:, 3] != 0).sum()) == 0
+
+
+def test_bounded_wait_expiry_is_reported_and_recoverable():
+    """Failure detection (bounded waits, no trap): spec_verify's kernel with a
+    producer that issues no copy.  Every request that reaches the row sweep
+    waits on a ring stage nothing fills; the wait gives up after ~10 ms
+    (2e7 cycles) with nothing in flight, the request reports
+    MTP_VERIFY_DEVICE_TIMEOUT with its accept prefix, the error word carries
+    MTP_DEVERR_TIMEOUT from the verify kernels only, and the next ordinary
+    call on the same stream is exact again."""
+    case = synth.make_small_verify_case(6, R=16, gamma=3, V=4096)
+    dev = "cuda"
+    p, q, y = case["p"].to(dev), case["q"].to(dev), case["draft"].to(dev)
+    y[0, 0] = 4096  # ends in the accept phase: reported without waiting
+    lib.check_errors()
+    out = lib.verify_starved(p, q, y, seed=3, offset=0, wait_limit_cycles=20_000_000)
+    flags = ctypes.c_uint(0)
+    st = lib.load().mtp_check_errors(None, ctypes.byref(flags))
+    assert st == 6  # MTP_ERR_DEVICE
+    assert flags.value == (2 | (1 << 11))  # MTP_DEVERR_TIMEOUT | MTP_DEVERR_FROM_VERIFY
+    r = ov.spec_verify(case["p"].numpy(), case["q"].numpy(), y.cpu().numpy(), 3, 0)
+    g = {k: v.cpu().numpy() for k, v in out.items()}
+    swept = r["status"] != ov.STATUS_INVALID_DRAFT
+    assert not swept[0] and swept.sum() >= 12
+    assert np.all(g["status"][swept] == 5)  # MTP_VERIFY_DEVICE_TIMEOUT
+    np.testing.assert_array_equal(g["accepted"][swept], r["accepted"][swept])
+    assert np.all(g["next_token"][swept] == -1)
+    np.testing.assert_array_equal(g["n_emit"][swept], g["accepted"][swept])
+    assert g["status"][0] == ov.STATUS_INVALID_DRAFT
+    assert lib.check_errors() == 0  # the word was cleared
+    g2, r2 = run_both({"p": case["p"], "q": case["q"], "draft": y.cpu()}, 3, 0)
+    assert_parity(g2, r2)
