@@ -66,6 +66,8 @@ def parse_args():
     ap.add_argument("--draft-gamma", type=int, default=4, help="steps of the recurrent draft round (<= 1: off)")
     ap.add_argument("--no-draft-fp8", dest="draft_fp8", action="store_false",
                     help="skip the draft step with FP8 block-scaled module weights")
+    ap.add_argument("--only-c3", action="store_true",
+                    help="run only the DeepSeek-V3-width section (profiling its kernels) and print its record")
     ap.add_argument("--draft-requests", type=int, default=32,
                     help="requests of the draft-step section (32 = the measured workload; fewer for profiling)")
     return ap.parse_args()
@@ -418,6 +420,11 @@ def run_ours(args):
     mtp_build.build()
     dev = torch.device("cuda", local_rank if world > 1 else 0)
     torch.cuda.set_device(dev)
+    if args.only_c3:
+        res = measure_dsv3(args, dev, rank, load_peaks()[0])
+        if rank == 0:
+            print(json.dumps({"dsv3_width": res}), flush=True)
+        return
     cfg = synth.MID_BF16
     vcfg = synth.VERIFY_C4
     seed = 1 + 1000 * rank
