@@ -5,10 +5,10 @@
 // s in [seg_start(t), t] only.  q, k, v come from the fused QKV GEMM as one
 // [B*T, 3d] bf16 tensor (head h occupies columns h*hd.. of each third).
 //
-// bf16 forward: persistent tcgen05 kernel (attn_tc_kernel below): 128-query
-// tiles, 128-key blocks fed by TMA, S = Q K^T and O += P V accumulated in
-// TMEM, softmax warps reading S with tcgen05.ld; P is rounded to bf16 for
-// the P V product.
+// bf16 forward: persistent tcgen05 kernel (attn_tc2_kernel below): work items
+// of two 128-query tiles sharing 128-key blocks fed by TMA, S = Q K^T and
+// O += P V accumulated in TMEM, softmax warps reading S with tcgen05.ld and
+// writing P back into TMEM as bf16 for the P V product.
 // bf16 backward: flash-attention-2 form on mma.sync (flash_attn_bwd_kernel).
 // f32 path (small shapes): one warp per (query row, head), scores staged in
 // shared memory, fp32 throughout.
@@ -367,70 +367,9 @@ __global__ void attn_f32_kernel(const float* __restrict__ qkv, float* __restrict
   }
 }
 
-// ---------------------------------------------------------------------------
-// Forward on the tcgen05 tensor cores (bf16, head_dim 64 or 128).
-//
-// Persistent: one CTA per SM walks work items (128-query tile, head, packed
-// row), the tiles nearest a row's end first (they see the most keys).  Six
-// warps:
-//   warp 4     TMA producer.  Lane 0 loads the Q tile ([128 rows x 64 cols]
-//              boxes) and, per 128-key block, the K tile (same boxes) into a
-//              ring of K stages; lane 1 loads the V tile as [64 keys x 64 cols]
-//              boxes (the MN-major operand of P V) into its own ring.  K is
-//              released as soon as S has been computed and V only after P V,
-//              so K loads run further ahead than a shared K/V stage allows.
-//   warp 5     allocates 512 TMEM columns (S double buffer at 0 and 128, O at
-//              256); one thread issues S_j = Q K_j^T (M = 128, N = 128,
-//              K = head_dim) into S buffer j % 2 and, once the softmax warps
-//              have written P_j, O += P_j V_j (N = head_dim, K = 128 keys).
-//              The order S_0, S_1, PV_0, S_2, PV_1, ... lets the softmax of
-//              block j run while S_{j+1} and PV_{j-1} execute.
-//   warps 0-3  softmax, one query row per thread (= TMEM lane): read S_j with
-//              tcgen05.ld, apply the segment-causal mask and the scale (log2
-//              domain), keep a running maximum m, write P = 2^(s - m) as bf16
-//              into a 128-byte-swizzled K-major tile in shared memory, and sum
-//              P in fp32.  m is replaced only when a block's maximum exceeds it
-//              by more than 2^8 (P then stays <= 256); O, which lives in TMEM,
-//              is rescaled by those rows' factor after the previous P V has
-//              completed.  At the end of a tile O / l is written as bf16 (and
-//              m + log2 l for the backward).
-// The mask and the skipped blocks follow the segment rule: query t sees keys
-// [seg_start(t), t]; a tile needs key blocks from seg_start(first query) to
-// its last query.  Every wait is bounded (MTP_DEVERR_TIMEOUT, abort flag,
-// drain of in-flight copies and MMAs before TMEM is freed).
-// ---------------------------------------------------------------------------
-constexpr int kTcQ = 128;
-constexpr int kTcKeys = 128;
-constexpr int kTcThreads = 192;
-constexpr float kStaleMaxLog2 = 8.0f;
-
-template <int HD>
-struct TcAttn {
-  static constexpr int kChunks = HD / 64;       // 64-column (128-byte) pieces of a row
-  static constexpr int kTileBytes = 128 * 128;  // one [128 rows x 128 B] swizzled piece
-  static constexpr int kQBytes = kTcQ * HD * 2;
-  static constexpr int kKBytes = kTcKeys * HD * 2;
-  static constexpr int kVBytes = kTcKeys * HD * 2;
-  static constexpr int kPBytes = kTcQ * kTcKeys * 2;
-  // one CTA per SM (512 TMEM columns: S double-buffered); head_dim 128 fits
-  // one Q buffer and one P buffer in shared memory, head_dim 64 two of each
-  static constexpr int kCtasPerSm = 1;
-  static constexpr int kSBufs = 2;
-  static constexpr int kQBufs = HD == 64 ? 2 : 1;
-  static constexpr int kKStages = HD == 64 ? 4 : 3;
-  static constexpr int kVStages = HD == 64 ? 3 : 2;
-  static constexpr int kPBufs = HD == 64 ? 2 : 1;
-  static constexpr int kOffK = kQBufs * kQBytes;
-  static constexpr int kOffV = kOffK + kKStages * kKBytes;
-  static constexpr int kOffP = kOffV + kVStages * kVBytes;
-  static constexpr int kOffBar = kOffP + kPBufs * kPBytes;
-  // q full/empty, k full/empty, v full/empty, s_full[2], p_full[2], pv_done[2], o_free, drain
-  static constexpr int kNumBars = 2 * (kQBufs + kKStages + kVStages) + 8;
-  // the dynamic shared memory starts 1024-byte aligned (no static shared memory; checked at run time)
-  static constexpr int kSmemBytes = kOffBar + 8 * kNumBars + 16;
-  static constexpr uint32_t kColS = 0, kColO = kSBufs * kTcKeys;
-  static constexpr uint32_t kTmemCols = kSBufs == 1 ? 256 : 512;
-};
+constexpr int kTcQ = 128;     // queries per tile (MMA M, TMEM lanes)
+constexpr int kTcKeys = 128;  // keys per block (N of S = Q K^T, K of O += P V)
+constexpr float kStaleMaxLog2 = 8.0f;  // a running maximum is replaced only when exceeded by 2^8
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -438,21 +377,65 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// ---------------------------------------------------------------------------
+// Forward on the tcgen05 tensor cores: two query tiles per work item.
+//
+// A work item is 256 consecutive queries of one (packed row, head): tile A =
+// queries q0..q0+127, tile B = q0+128..q0+255 (absent past T).  Both tiles
+// share every K/V block they need, which halves the K/V traffic per FLOP, and
+// their softmax warpgroups alternate on the tensor pipe: while warps 0-3
+// turn S_A into P_A, the MMA thread runs P_B V and S_B, and the reverse.
+//   warps 0-3 / 4-7  softmax of tile A / B, one query row per thread (TMEM
+//              lane = row): S read with tcgen05.ld, segment-causal mask,
+//              stale-by-up-to-2^8 running maximum, P = 2^(s - m) written back
+//              as bf16 pairs into the first 64 columns of the tile's own S
+//              (tcgen05.st), where the P V product reads it as its A operand.
+//   warp 8     TMA: lane 0 loads Q_A, Q_B and the K blocks, lane 1 the V
+//              blocks (MN-major [64 keys x 64 cols] boxes), each into a ring.
+//   warp 9     allocates 512 TMEM columns (S_A, S_B at 0 and 128; O_A, O_B
+//              at 256 and 256 + HD); one thread issues, per key block j,
+//              P_A(j) V_j, S_A(j+1), P_B(j) V_j, S_B(j+1) (S of the first
+//              block up front), skipping a tile outside its key range.
+// Tile A needs key blocks [seg_start(q0) / 128, q0 / 128], tile B
+// [seg_start(q0 + 128) / 128, (q0 + 128) / 128]: A's range is a prefix of the
+// union, B's a suffix.  Every wait is bounded.
+// ---------------------------------------------------------------------------
+constexpr int kT2Threads = 320;
+
 template <int HD>
-__global__ void __launch_bounds__(kTcThreads, TcAttn<HD>::kCtasPerSm)
-attn_tc_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant__ CUtensorMap tm64,
-               __nv_bfloat16* __restrict__ out, const int32_t* __restrict__ seg_start, int B, int T, int H,
-               float scale_log2, float* __restrict__ lse2_out) {
-  using C = TcAttn<HD>;
+struct Tc2Attn {
+  static constexpr int kChunks = HD / 64;
+  static constexpr int kTileBytes = 128 * 128;  // one [128 rows x 128 B] swizzled piece
+  static constexpr int kQBytes = kTcQ * HD * 2;  // one tile's Q
+  static constexpr int kKBytes = kTcKeys * HD * 2;
+  static constexpr int kVBytes = kTcKeys * HD * 2;
+  static constexpr int kQBufs = HD == 64 ? 2 : 1;  // Q of the next item loads early when it fits
+  static constexpr int kKStages = HD == 64 ? 4 : 3;
+  static constexpr int kVStages = HD == 64 ? 4 : 2;
+  static constexpr int kOffK = kQBufs * 2 * kQBytes;
+  static constexpr int kOffV = kOffK + kKStages * kKBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kVBytes;
+  // q full/empty, k full/empty, v full/empty; per tile s_full, p_full, pv_done, o_free; drain
+  static constexpr int kNumBars = 2 * (kQBufs + kKStages + kVStages) + 8 + 1;
+  static constexpr int kSmemBytes = kOffBar + 8 * kNumBars + 16;
+  static constexpr uint32_t kColO0 = 256;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kT2Threads, 1)
+attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant__ CUtensorMap tm64,
+                __nv_bfloat16* __restrict__ out, const int32_t* __restrict__ seg_start, int B, int T, int H,
+                float scale_log2, float* __restrict__ lse2_out) {
+  using C = Tc2Attn<HD>;
   pdl_trigger();  // the output projection that follows may start its setup
-  extern __shared__ __align__(1024) uint8_t attn_smem[];
-  uint8_t* smem = attn_smem;
+  extern __shared__ __align__(1024) uint8_t attn2_smem[];
+  uint8_t* smem = attn2_smem;
   const uint32_t s0 = mtp::smem_u32(smem);
   if (s0 & 1023u) {  // the swizzled tiles need 1024-byte alignment
     if (threadIdx.x == 0) atomicOr(&g_mtp_error_word, MTP_DEVERR_TIMEOUT);
     return;
   }
-  const uint32_t sQ = s0, sK = s0 + C::kOffK, sV = s0 + C::kOffV, sP = s0 + C::kOffP;
+  const uint32_t sQ = s0, sK = s0 + C::kOffK, sV = s0 + C::kOffV;
   const uint32_t bar0 = s0 + C::kOffBar;
   auto q_full = [&](int i) { return bar0 + 8u * i; };
   auto q_empty = [&](int i) { return bar0 + 8u * (C::kQBufs + i); };
@@ -463,18 +446,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant_
   auto v_full = [&](int i) { return barv + 8u * i; };
   auto v_empty = [&](int i) { return barv + 8u * (C::kVStages + i); };
   const uint32_t barx = barv + 16u * C::kVStages;
-  auto s_full = [&](uint32_t b) { return barx + 8u * b; };
-  auto p_full = [&](uint32_t b) { return barx + 16u + 8u * b; };
-  auto pv_done = [&](uint32_t b) { return barx + 32u + 8u * b; };
-  const uint32_t o_free = barx + 48u, drain_bar = barx + 56u;
+  auto s_full = [&](int x) { return barx + 8u * x; };
+  auto p_full = [&](int x) { return barx + 16u + 8u * x; };
+  auto pv_done = [&](int x) { return barx + 32u + 8u * x; };
+  auto o_free = [&](int x) { return barx + 48u + 8u * x; };
+  const uint32_t drain_bar = barx + 64u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + 8 * C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   unsigned int* err = &g_mtp_error_word;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = H * HD;
-  const int n_qb = (T + kTcQ - 1) / kTcQ;
-  const int per_qb = H * B;
-  const int n_tiles = n_qb * per_qb;
+  const int n_pairs = (T + 2 * kTcQ - 1) / (2 * kTcQ);
+  const int per_qp = H * B;
+  const int n_items = n_pairs * per_qp;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kQBufs; ++i) {
@@ -489,51 +473,64 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant_
       mtp::mbar_init(v_full(i), 1);
       mtp::mbar_init(v_empty(i), 1);
     }
-    for (uint32_t b = 0; b < 2; ++b) {
-      mtp::mbar_init(s_full(b), 1);
-      mtp::mbar_init(p_full(b), kTcQ);
-      mtp::mbar_init(pv_done(b), 1);
+    for (int x = 0; x < 2; ++x) {
+      mtp::mbar_init(s_full(x), 1);
+      mtp::mbar_init(p_full(x), kTcQ);
+      mtp::mbar_init(pv_done(x), 1);
+      mtp::mbar_init(o_free(x), kTcQ);
     }
-    mtp::mbar_init(o_free, kTcQ);
     mtp::mbar_init(drain_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm128)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm64)) : "memory");
   }
-  if (warp == 5) mtp::tmem_alloc_cols(mtp::smem_u32(tmem_slot), C::kTmemCols);
+  if (warp == 9) mtp::tmem_alloc_cols(mtp::smem_u32(tmem_slot), 512);
   mtp::tc_fence_before();
   __syncthreads();
   mtp::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // work item t: query tile qb (last tiles first), head h, packed row b
+  // work item t: query pair qp (last pairs first), head h, packed row b
   auto coords = [&](int t, int& b, int& h, int& q0) {
-    const int qb = n_qb - 1 - t / per_qb;
-    const int r = t - (t / per_qb) * per_qb;
+    const int qp = n_pairs - 1 - t / per_qp;
+    const int r = t - (t / per_qp) * per_qp;
     h = r % H;
     b = r / H;
-    q0 = qb * kTcQ;
+    q0 = qp * 2 * kTcQ;
   };
-  // segment start of the tile's first query (its first key), loaded one work item ahead
-  auto first_key = [&](int t) {
-    if (t >= n_tiles) return 0;
+  // segment starts of both tiles' first queries (loaded one work item ahead)
+  auto first_keys = [&](int t) {
+    if (t >= n_items) return make_int2(0, 0);
     int b, h, q0;
     coords(t, b, h, q0);
-    return static_cast<int>(seg_start[static_cast<size_t>(b) * T + q0]);
+    const int32_t* ss = seg_start + static_cast<size_t>(b) * T;
+    return make_int2(ss[q0], q0 + kTcQ < T ? ss[q0 + kTcQ] : 0);
   };
-  // key blocks [kb0, kb0 + nb) of work item t, given its first key
-  auto decode = [&](int t, int key_first, int& b, int& h, int& q0, int& kb0, int& nb) {
-    coords(t, b, h, q0);
-    kb0 = key_first / kTcKeys;
-    nb = min(q0 + kTcQ - 1, T - 1) / kTcKeys - kb0 + 1;
+  // key-block ranges: tile x covers blocks [lo[x], hi[x]] (empty when hi < lo); union [lo[0], u_hi]
+  struct Ranges {
+    int lo[2], hi[2], u_hi;
+  };
+  auto ranges = [&](int q0, int2 keys) {
+    Ranges R;
+    R.lo[0] = keys.x / kTcKeys;
+    R.hi[0] = min(q0 + kTcQ - 1, T - 1) / kTcKeys;
+    if (q0 + kTcQ < T) {
+      R.lo[1] = keys.y / kTcKeys;
+      R.hi[1] = min(q0 + 2 * kTcQ - 1, T - 1) / kTcKeys;
+    } else {
+      R.lo[1] = 1;
+      R.hi[1] = 0;
+    }
+    R.u_hi = max(R.hi[0], R.hi[1]);
+    return R;
   };
   auto wait = [&](uint32_t bar, uint32_t parity) { return mtp::wait_phase(bar, parity, abort_flag, err); };
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------- TMA producers: lane 0 Q and K, lane 1 V ----------------
     if (lane < 2) {
       const bool kside = lane == 0;
@@ -541,25 +538,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant_
       uint32_t g = 0, issued = 0;
       int tl = 0, q_loads = 0;
       bool ok = true;
-      int key_next = first_key(blockIdx.x);
-      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++tl) {
-        const int key_first = key_next;
-        key_next = first_key(t + gridDim.x);
-        int b, h, q0, kb0, nb;
-        decode(t, key_first, b, h, q0, kb0, nb);
+      int2 key_next = first_keys(blockIdx.x);
+      for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x, ++tl) {
+        const int2 keys = key_next;
+        key_next = first_keys(t + gridDim.x);
+        int b, h, q0;
+        coords(t, b, h, q0);
+        const Ranges R = ranges(q0, keys);
         if (kside) {
           const int qi = tl % C::kQBufs, qu = tl / C::kQBufs;
           if (qu > 0 && !wait(q_empty(qi), (qu - 1) & 1)) { ok = false; break; }
-          mtp::mbar_expect_tx(q_full(qi), C::kQBytes);
-          for (int c = 0; c < C::kChunks; ++c)
-            mtp::tma_tile_2d(sQ + qi * C::kQBytes + c * C::kTileBytes, &tm128, h * HD + 64 * c, b * T + q0,
-                             q_full(qi));
+          const bool has_b = R.hi[1] >= R.lo[1];
+          mtp::mbar_expect_tx(q_full(qi), (has_b ? 2 : 1) * C::kQBytes);
+          for (int x = 0; x < (has_b ? 2 : 1); ++x)
+            for (int c = 0; c < C::kChunks; ++c)
+              mtp::tma_tile_2d(sQ + (qi * 2 + x) * C::kQBytes + c * C::kTileBytes, &tm128, h * HD + 64 * c,
+                               b * T + q0 + x * kTcQ, q_full(qi));
           ++q_loads;
         }
-        for (int j = 0; j < nb; ++j, ++g) {
+        for (int j = R.lo[0]; j <= R.u_hi; ++j, ++g) {
           const int st = static_cast<int>(g % stages);
           const uint32_t use = g / stages;
-          const int row0 = b * T + (kb0 + j) * kTcKeys;
+          const int row0 = b * T + j * kTcKeys;
           if (kside) {
             if (use > 0 && !wait(k_empty(st), (use - 1) & 1)) { ok = false; break; }
             mtp::mbar_expect_tx(k_full(st), C::kKBytes);
@@ -583,67 +583,91 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant_
       for (int x = q_loads > C::kQBufs ? q_loads - C::kQBufs : 0; x < q_loads; ++x)
         mtp::wait_drain(q_full(x % C::kQBufs), (x / C::kQBufs) & 1, kWaitLimitCycles);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t idesc_s = mtp::idesc_bf16_f32(kTcQ, kTcKeys, 0);
-      constexpr uint32_t idesc_o = mtp::idesc_bf16_f32(kTcQ, HD, 2);  // V read MN-major
-      uint32_t g = 0;
+      constexpr uint32_t idesc_o = mtp::idesc_bf16_f32(kTcQ, HD, 2);  // V read MN-major, P from TMEM
+      uint32_t g = 0;                  // union key blocks consumed (K/V ring position)
+      uint32_t ns[2] = {0u, 0u};       // S products issued per tile (= P V products after the block)
+      uint32_t no[2] = {0u, 0u};       // work items per tile whose output the softmax has read
       int tl = 0;
       bool ok = true, any = false;
-      int key_next = first_key(blockIdx.x);
-      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++tl) {
-        const int key_first = key_next;
-        key_next = first_key(t + gridDim.x);
-        int b, h, q0, kb0, nb;
-        decode(t, key_first, b, h, q0, kb0, nb);
+      int2 key_next = first_keys(blockIdx.x);
+      for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x, ++tl) {
+        const int2 keys = key_next;
+        key_next = first_keys(t + gridDim.x);
+        int b, h, q0;
+        coords(t, b, h, q0);
+        const Ranges R = ranges(q0, keys);
+        auto active = [&](int x, int j) { return j >= R.lo[x] && j <= R.hi[x]; };
         const int qi = tl % C::kQBufs;
         if (!wait(q_full(qi), (tl / C::kQBufs) & 1)) { ok = false; break; }
-        const uint32_t sQt = sQ + qi * C::kQBytes;
-        for (int j = 0; j <= nb; ++j) {
-          if (j < nb) {  // S_j = Q K_j^T into S buffer j % 2
-            const uint32_t gs = g + j;
-            const int ks = static_cast<int>(gs % C::kKStages);
-            if (!wait(k_full(ks), (gs / C::kKStages) & 1)) { ok = false; break; }
-            // S buffer gs % kSBufs was last read by the softmax of block gs - kSBufs
-            if (gs >= static_cast<uint32_t>(C::kSBufs)) {
-              const uint32_t gr = gs - C::kSBufs;
-              if (!wait(p_full(gr & 1), (gr >> 1) & 1)) { ok = false; break; }
-            }
-            mtp::tc_fence_after();
-            const uint32_t sKt = sK + ks * C::kKBytes;
-            const uint32_t dS = tmem + C::kColS + (gs % C::kSBufs) * kTcKeys;
+        // S_x(j) = Q_x K_j^T into tile x's S columns; its previous P was read by a P V issued before
+        auto issue_s = [&](int x, uint32_t gu) -> bool {
+          if (ns[x] > 0 && !wait(p_full(x), (ns[x] - 1) & 1)) return false;
+          mtp::tc_fence_after();
+          const uint32_t sQt = sQ + (qi * 2 + x) * C::kQBytes;
+          const uint32_t sKt = sK + (gu % C::kKStages) * C::kKBytes;
 #pragma unroll
-            for (int k = 0; k < HD / 16; ++k) {
-              const uint32_t off = (k >> 2) * C::kTileBytes + (k & 3) * 32;
-              mtp::umma_bf16_ss(dS, mtp::sdesc_k_sw128(sQt + off), mtp::sdesc_k_sw128(sKt + off), idesc_s, k > 0);
-            }
-            mtp::umma_commit(s_full(gs % C::kSBufs));
-            mtp::umma_commit(k_empty(ks));
-            if (j == nb - 1) mtp::umma_commit(q_empty(qi));
-            any = true;
+          for (int k = 0; k < HD / 16; ++k) {
+            const uint32_t off = (k >> 2) * C::kTileBytes + (k & 3) * 32;
+            mtp::umma_bf16_ss(tmem + 128u * x, mtp::sdesc_k_sw128(sQt + off), mtp::sdesc_k_sw128(sKt + off), idesc_s,
+                              k > 0);
           }
-          if (j >= 1) {  // O (+)= P_{j-1} V_{j-1}
-            const uint32_t gp = g + j - 1;
-            const int vs = static_cast<int>(gp % C::kVStages);
-            if (!wait(v_full(vs), (gp / C::kVStages) & 1)) { ok = false; break; }
-            if (!wait(p_full(gp & 1), (gp >> 1) & 1)) { ok = false; break; }
-            if (j == 1 && tl > 0 && !wait(o_free, (tl - 1) & 1)) { ok = false; break; }
-            mtp::tc_fence_after();
-            const uint32_t pb = sP + (gp % C::kPBufs) * C::kPBytes;
-            const uint32_t sVt = sV + vs * C::kVBytes;
+          mtp::umma_commit(s_full(x));
+          ++ns[x];
+          any = true;
+          return true;
+        };
+        bool first_pv[2] = {true, true};
+        const uint32_t g0 = g;
+        // the first block's S products
+        if (!wait(k_full(g0 % C::kKStages), (g0 / C::kKStages) & 1)) { ok = false; break; }
+        for (int x = 0; x < 2 && ok; ++x)
+          if (active(x, R.lo[0]) && !issue_s(x, g0)) ok = false;
+        if (!ok) break;
+        mtp::umma_commit(k_empty(g0 % C::kKStages));
+        if (R.lo[0] == R.u_hi) mtp::umma_commit(q_empty(qi));
+        for (int j = R.lo[0]; j <= R.u_hi && ok; ++j) {
+          const uint32_t gu = g0 + static_cast<uint32_t>(j - R.lo[0]);
+          const int vs = static_cast<int>(gu % C::kVStages);
+          if (!wait(v_full(vs), (gu / C::kVStages) & 1)) { ok = false; break; }
+          bool k_next_ready = false;
+          for (int x = 0; x < 2; ++x) {
+            if (active(x, j)) {  // O_x (+)= P_x(j) V_j, P_x in tile x's S columns
+              const uint32_t n = ns[x] - 1;  // this block's S index of tile x
+              if (!wait(p_full(x), n & 1)) { ok = false; break; }
+              if (first_pv[x] && no[x] > 0 && !wait(o_free(x), (no[x] - 1) & 1)) { ok = false; break; }
+              mtp::tc_fence_after();
+              const uint32_t sVt = sV + vs * C::kVBytes;
 #pragma unroll
-            for (int k = 0; k < kTcKeys / 16; ++k) {
-              const uint32_t a = pb + (k >> 2) * C::kTileBytes + (k & 3) * 32;
-              const uint32_t bv = sVt + (k >> 2) * (C::kChunks * 8192) + (k & 3) * 2048;
-              mtp::umma_bf16_ss(tmem + C::kColO, mtp::sdesc_k_sw128(a), mtp::sdesc_mn_sw128(bv), idesc_o,
-                                (j > 1 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < kTcKeys / 16; ++k) {
+                const uint32_t bv = sVt + (k >> 2) * (C::kChunks * 8192) + (k & 3) * 2048;
+                mtp::umma_bf16_ts(tmem + C::kColO0 + HD * x, tmem + 128u * x + 8u * k, mtp::sdesc_mn_sw128(bv),
+                                  idesc_o, (!first_pv[x] || k > 0) ? 1u : 0u);
+              }
+              mtp::umma_commit(pv_done(x));
+              first_pv[x] = false;
             }
-            mtp::umma_commit(pv_done(gp & 1));
-            mtp::umma_commit(v_empty(vs));
+            if (j < R.u_hi && active(x, j + 1)) {  // S_x(j+1)
+              if (!k_next_ready) {
+                if (!wait(k_full((gu + 1) % C::kKStages), ((gu + 1) / C::kKStages) & 1)) { ok = false; break; }
+                k_next_ready = true;
+              }
+              if (!issue_s(x, gu + 1)) { ok = false; break; }
+            }
+          }
+          if (!ok) break;
+          mtp::umma_commit(v_empty(vs));
+          if (k_next_ready) {
+            mtp::umma_commit(k_empty((gu + 1) % C::kKStages));
+            if (j + 1 == R.u_hi) mtp::umma_commit(q_empty(qi));
           }
         }
-        g += nb;
+        g = g0 + static_cast<uint32_t>(R.u_hi - R.lo[0] + 1);
+        for (int x = 0; x < 2; ++x)
+          if (R.hi[x] >= R.lo[x]) ++no[x];
       }
       // every issued MMA has completed before TMEM is freed
       if (any) {
@@ -652,43 +676,47 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant_
       }
     }
   } else {
-    // ---------------- softmax warps: one query row per thread ----------------
-    const int row = threadIdx.x;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    // warp-uniform bounded wait: every lane waits, all must succeed
+    // ---------------- softmax warpgroups: tile x = warp / 4, one query row per thread ----------------
+    const int x = warp >> 2;
+    const int row = threadIdx.x - 128 * x;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t colS = 128u * x, colO = C::kColO0 + HD * x;
     auto wwait = [&](uint32_t bar, uint32_t parity) { return __all_sync(0xffffffffu, wait(bar, parity)); };
-    uint32_t g = 0;
-    // this row's segment start, loaded one work item ahead
+    uint32_t n = 0;  // S products of this tile consumed
+    // this row's segment start in work item t (loaded one item ahead)
     auto row_start = [&](int t) {
-      if (t >= n_tiles) return 0;
+      if (t >= n_items) return 0;
       int b, h, q0;
       coords(t, b, h, q0);
-      const int q = q0 + row;
+      const int q = q0 + kTcQ * x + row;
       return q < T ? static_cast<int>(seg_start[static_cast<size_t>(b) * T + q]) : q;
     };
-    int key_next = first_key(blockIdx.x), st_next = row_start(blockIdx.x);
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-      const int key_first = key_next, st_row = st_next;
-      key_next = first_key(t + gridDim.x);
+    int2 key_next = first_keys(blockIdx.x);
+    int st_next = row_start(blockIdx.x);
+    for (int t = blockIdx.x; t < n_items; t += gridDim.x) {
+      const int2 keys = key_next;
+      const int st_row = st_next;
+      key_next = first_keys(t + gridDim.x);
       st_next = row_start(t + gridDim.x);
-      int b, h, q0, kb0, nb;
-      decode(t, key_first, b, h, q0, kb0, nb);
-      const int q = q0 + row;
+      int b, h, q0;
+      coords(t, b, h, q0);
+      const Ranges R = ranges(q0, keys);
+      if (R.hi[x] < R.lo[x]) continue;  // tile B past the end of the row
+      const int q = q0 + kTcQ * x + row;
       const bool live = q < T;
       float m = -INFINITY, l = 0.f;
       bool ok = true;
-      for (int j = 0; j < nb; ++j) {
-        const uint32_t gs = g + j;
-        if (!wwait(s_full(gs % C::kSBufs), (gs / C::kSBufs) & 1)) { ok = false; break; }
+      for (int j = R.lo[x]; j <= R.hi[x]; ++j, ++n) {
+        if (!wwait(s_full(x), n & 1)) { ok = false; break; }
         mtp::tc_fence_after();
         float sc[kTcKeys];
         {
           float (&lo)[64] = *reinterpret_cast<float (*)[64]>(&sc[0]);
           float (&hi)[64] = *reinterpret_cast<float (*)[64]>(&sc[64]);
-          mtp::tmem_ld64(lane_base + C::kColS + (gs % C::kSBufs) * kTcKeys, lo);
-          mtp::tmem_ld64(lane_base + C::kColS + (gs % C::kSBufs) * kTcKeys + 64, hi);
+          mtp::tmem_ld64(lane_base + colS, lo);
+          mtp::tmem_ld64(lane_base + colS + 64, hi);
         }
-        const int key0 = (kb0 + j) * kTcKeys;
+        const int key0 = j * kTcKeys;
         if (!(key0 >= st_row && key0 + kTcKeys - 1 <= q)) {  // a block the row sees only in part
 #pragma unroll
           for (int i = 0; i < kTcKeys; ++i) {
@@ -696,7 +724,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant_
             if (!(key >= st_row && key <= q)) sc[i] = -INFINITY;
           }
         }
-        // row maximum of the raw scores (scale > 0), eight independent chains
         float mx8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx8[i] = sc[i];
@@ -708,56 +735,45 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant_
         const float m_new = mx > m + kStaleMaxLog2 ? mx : m;
         const bool rescale = m_new != m && m != -INFINITY;
         const float neg_use = m_new == -INFINITY ? 0.f : -m_new;
-        // P = 2^(s scale - m), rounded to bf16 (packed in place: sc[i] holds pair i)
         float rs8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
 #pragma unroll
-        for (int i = 0; i < kTcKeys / 2; ++i) {
+        for (int i = 0; i < kTcKeys / 2; ++i) {  // P pairs packed in place: sc[i] holds keys 2i, 2i+1
           const float a = ex2_approx(fmaf(sc[2 * i], scale_log2, neg_use));
           const float bb = ex2_approx(fmaf(sc[2 * i + 1], scale_log2, neg_use));
           rs8[i & 7] += a + bb;
           sc[i] = __uint_as_float(pack2_bf16(a, bb));
         }
-        if (__any_sync(0xffffffffu, rescale)) {  // O holds earlier blocks' P V: wait for the last one
-          if (!wwait(pv_done((gs - 1) & 1), ((gs - 1) >> 1) & 1)) { ok = false; break; }
+        if (__any_sync(0xffffffffu, rescale)) {  // O holds this item's earlier P V: wait for the last one
+          if (!wwait(pv_done(x), (n - 1) & 1)) { ok = false; break; }
           mtp::tc_fence_after();
           const float alpha = rescale ? ex2_approx(m - m_new) : 1.f;
 #pragma unroll
           for (int c = 0; c < HD / 32; ++c) {
             float o[32];
-            mtp::tmem_ld32(lane_base + C::kColO + 32 * c, o);
+            mtp::tmem_ld32(lane_base + colO + 32 * c, o);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            mtp::tmem_st32(lane_base + C::kColO + 32 * c, o);
+            mtp::tmem_st32(lane_base + colO + 32 * c, o);
           }
           l *= alpha;
         }
         m = m_new;
         l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-        // the P buffer was last read by the P V of block gs - kPBufs
-        if (gs >= static_cast<uint32_t>(C::kPBufs)) {
-          const uint32_t gr = gs - C::kPBufs;
-          if (!wwait(pv_done(gr & 1), (gr >> 1) & 1)) { ok = false; break; }
+        // P into the first 64 columns of this tile's S (the scores are in registers now; the
+        // previous block's P V completed before this block's S did)
+        {
+          float (&p0)[32] = *reinterpret_cast<float (*)[32]>(&sc[0]);
+          float (&p1)[32] = *reinterpret_cast<float (*)[32]>(&sc[32]);
+          mtp::tmem_st32(lane_base + colS, p0);
+          mtp::tmem_st32(lane_base + colS + 32, p1);
         }
-        uint8_t* prow = smem + C::kOffP + (gs % C::kPBufs) * C::kPBytes + row * 128;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-#pragma unroll
-          for (int k8 = 0; k8 < 8; ++k8) {
-            const int i0 = 32 * c + 4 * k8;
-            *reinterpret_cast<uint4*>(prow + c * C::kTileBytes + ((k8 ^ (row & 7)) << 4)) =
-                make_uint4(__float_as_uint(sc[i0]), __float_as_uint(sc[i0 + 1]), __float_as_uint(sc[i0 + 2]),
-                           __float_as_uint(sc[i0 + 3]));
-          }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P visible to the tensor cores
         mtp::tc_fence_before();
-        mtp::mbar_arrive1(p_full(gs & 1));
+        mtp::mbar_arrive1(p_full(x));
       }
       if (!ok) break;
-      const uint32_t gl = g + nb - 1;
-      if (!wwait(pv_done(gl & 1), (gl >> 1) & 1)) break;
+      if (!wwait(pv_done(x), (n - 1) & 1)) break;  // the item's last P V
       mtp::tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       if (live && lse2_out) lse2_out[(static_cast<size_t>(b) * T + q) * H + h] = m + log2f(l);
@@ -765,7 +781,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant_
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         float o[32];
-        mtp::tmem_ld32(lane_base + C::kColO + 32 * c, o);
+        mtp::tmem_ld32(lane_base + colO + 32 * c, o);
         if (live) {
 #pragma unroll
           for (int v = 0; v < 4; ++v)
@@ -777,22 +793,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant_
         }
       }
       mtp::tc_fence_before();
-      mtp::mbar_arrive1(o_free);
-      g += nb;
+      mtp::mbar_arrive1(o_free(x));
     }
   }
   mtp::tc_fence_before();
   __syncthreads();
   mtp::tc_fence_after();
-  if (warp == 5) mtp::tmem_free_cols(tmem, C::kTmemCols);
+  if (warp == 9) mtp::tmem_free_cols(tmem, 512);
 }
 
 template <int HD>
-mtp_status attn_tc_launch(const __nv_bfloat16* qkv, __nv_bfloat16* out, const int32_t* seg_start, int B, int T,
-                          int H, float scale_log2, float* lse2_out, cudaStream_t stream) {
-  using C = TcAttn<HD>;
+mtp_status attn_tc2_launch(const __nv_bfloat16* qkv, __nv_bfloat16* out, const int32_t* seg_start, int B, int T,
+                           int H, float scale_log2, float* lse2_out, cudaStream_t stream) {
+  using C = Tc2Attn<HD>;
   static PerDevice attr;
-  if (!smem_limit(attr, attn_tc_kernel<HD>, C::kSmemBytes)) return MTP_ERR_CUDA;
+  if (!smem_limit(attr, attn_tc2_kernel<HD>, C::kSmemBytes)) return MTP_ERR_CUDA;
   if (!aligned16(qkv) || !aligned16(out)) return MTP_ERR_ALIGNMENT;
   const int d = H * HD;
   const uint64_t rows = static_cast<uint64_t>(B) * T;
@@ -801,16 +816,17 @@ mtp_status attn_tc_launch(const __nv_bfloat16* qkv, __nv_bfloat16* out, const in
   if (!tensor_map_bf16_2d(&m128, qkv, rows, 3 * d, 3 * d, 64, 128, true) ||
       !tensor_map_bf16_2d(&m64, qkv, rows, 3 * d, 3 * d, 64, 64, true))
     return MTP_ERR_CUDA;
-  const long long n_tiles = static_cast<long long>((T + kTcQ - 1) / kTcQ) * H * B;
-  if (n_tiles > 0x7FFFFFFFll) return MTP_ERR_UNSUPPORTED;
-  const long long slots = static_cast<long long>(C::kCtasPerSm) * sm_count_current();
-  const int grid = static_cast<int>(n_tiles < slots ? n_tiles : slots);
-  attn_tc_kernel<HD><<<grid, kTcThreads, C::kSmemBytes, stream>>>(m128, m64, out, seg_start, B, T, H, scale_log2,
-                                                                 lse2_out);
+  const long long n_items = static_cast<long long>((T + 2 * kTcQ - 1) / (2 * kTcQ)) * H * B;
+  if (n_items > 0x7FFFFFFFll) return MTP_ERR_UNSUPPORTED;
+  const int sms = sm_count_current();
+  const int grid = static_cast<int>(n_items < sms ? n_items : sms);
+  attn_tc2_kernel<HD><<<grid, kT2Threads, C::kSmemBytes, stream>>>(m128, m64, out, seg_start, B, T, H, scale_log2,
+                                                                  lse2_out);
   note_launch();
   MTP_LAUNCH_CHECK();
   return MTP_OK;
 }
+
 
 }  // namespace
 
@@ -820,10 +836,10 @@ mtp_status attn_launch(int dtype, const void* qkv, void* out, const int32_t* seg
   if (dtype == MTP_BF16) {
     const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(hd));
     if (hd == 64)
-      return attn_tc_launch<64>(static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out), seg_start,
+      return attn_tc2_launch<64>(static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out), seg_start,
                                 B, T, H, scale_log2, lse2_out, stream);
     if (hd == 128)
-      return attn_tc_launch<128>(static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out),
+      return attn_tc2_launch<128>(static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out),
                                  seg_start, B, T, H, scale_log2, lse2_out, stream);
     return MTP_ERR_UNSUPPORTED;
   } else {
