@@ -647,13 +647,94 @@ mtp_status gemm<float>(const Ctx& C, const float* A, int lda, const float* const
 
 // RMSNorm launch; with `labels` it also writes term k's labels (bf16 fuses
 // them into the norm kernel, f32 uses a separate kernel).
+// Register-resident forms of the two bf16 row kernels for d = 256 * NPL: every
+// lane loads its NPL 16-byte chunks of the row at once, so a warp has the whole
+// row in flight and reads it once.  Same summation order as the looped kernels
+// (lane-strided chunks, then the warp sum), hence the same results bit for bit.
+template <int NPL>
+__global__ void rmsnorm_bf16_reg_kernel(const uint4* __restrict__ x, const uint4* __restrict__ g,
+                                        uint4* __restrict__ y, int M, float eps, const int32_t* __restrict__ tokens,
+                                        const int32_t* __restrict__ seg, const int32_t* __restrict__ seg_end,
+                                        int32_t* __restrict__ labels, int Tlen, int k, int V) {
+  mtp::pdl_trigger();  // a GEMM that follows may start its setup
+  constexpr int d8 = 32 * NPL;
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= M) return;
+  const uint4* xr = x + static_cast<size_t>(warp) * d8;
+  uint4 v[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) v[i] = xr[lane + 32 * i];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) ss += sumsq8(v[i]);
+  ss = mtp::warp_sum(ss);
+  const float r = 1.0f / sqrtf(ss / (8.0f * d8) + eps);
+  uint4* yr = y + static_cast<size_t>(warp) * d8;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) yr[lane + 32 * i] = norm8(v[i], g[lane + 32 * i], r);
+  if (labels && lane == 0) {
+    const int m = warp, t = m % Tlen;
+    const bool ok = seg[m] != -1 && t + k + 1 < seg_end[m];
+    labels[m] = ok ? clamp_token(tokens[m + k + 1], V) : -1;
+  }
+}
+
+template <int NPL>
+__global__ void prologue_bf16_reg_kernel(const uint4* __restrict__ h_prev, const int32_t* __restrict__ tokens,
+                                         const uint4* __restrict__ embed, const uint4* __restrict__ g_h,
+                                         const uint4* __restrict__ g_e, uint4* __restrict__ c, int M, int Tlen, int V,
+                                         int k, float eps) {
+  mtp::pdl_trigger();  // a GEMM that follows may start its setup
+  constexpr int d8 = 32 * NPL;
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= M) return;
+  const int m = warp;
+  const int t = m % Tlen;
+  const int tok = clamp_token(tokens[m - t + min(t + k, Tlen - 1)], V);
+  const uint4* h = h_prev + static_cast<size_t>(m) * d8;
+  const uint4* e = embed + static_cast<size_t>(tok) * d8;
+  uint4 hv[NPL], ev[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    hv[i] = h[lane + 32 * i];
+    ev[i] = e[lane + 32 * i];
+  }
+  float sh = 0.f, se = 0.f;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    sh += sumsq8(hv[i]);
+    se += sumsq8(ev[i]);
+  }
+  sh = mtp::warp_sum(sh);
+  se = mtp::warp_sum(se);
+  const float d = 8.0f * d8;
+  const float rh = 1.0f / sqrtf(sh / d + eps);
+  const float re = 1.0f / sqrtf(se / d + eps);
+  uint4* out = c + static_cast<size_t>(m) * 2 * d8;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    out[lane + 32 * i] = norm8(hv[i], g_h[lane + 32 * i], rh);
+    out[d8 + lane + 32 * i] = norm8(ev[i], g_e[lane + 32 * i], re);
+  }
+}
+
 template <typename T>
 void launch_rmsnorm(const Ctx& C, const T* x, const T* g, T* y, int32_t* labels = nullptr, int k = 0) {
   const mtp_dims& D = C.D;
   if constexpr (sizeof(T) == 2) {
-    rmsnorm_bf16_kernel<<<warp_blocks(C.M), 256, 0, C.st>>>(
-        reinterpret_cast<const uint4*>(x), reinterpret_cast<const uint4*>(g), reinterpret_cast<uint4*>(y), C.M,
-        D.d / 8, D.eps, C.tokens, C.seg, C.buf<int32_t>(C.L.seg_end), labels, D.T, k, D.V);
+    const uint4* xv = reinterpret_cast<const uint4*>(x);
+    const uint4* gv = reinterpret_cast<const uint4*>(g);
+    uint4* yv = reinterpret_cast<uint4*>(y);
+    const int32_t* se = C.buf<int32_t>(C.L.seg_end);
+    switch (D.d) {
+      case 256: rmsnorm_bf16_reg_kernel<1><<<warp_blocks(C.M), 256, 0, C.st>>>(xv, gv, yv, C.M, D.eps, C.tokens, C.seg, se, labels, D.T, k, D.V); break;
+      case 512: rmsnorm_bf16_reg_kernel<2><<<warp_blocks(C.M), 256, 0, C.st>>>(xv, gv, yv, C.M, D.eps, C.tokens, C.seg, se, labels, D.T, k, D.V); break;
+      case 1024: rmsnorm_bf16_reg_kernel<4><<<warp_blocks(C.M), 256, 0, C.st>>>(xv, gv, yv, C.M, D.eps, C.tokens, C.seg, se, labels, D.T, k, D.V); break;
+      case 2048: rmsnorm_bf16_reg_kernel<8><<<warp_blocks(C.M), 256, 0, C.st>>>(xv, gv, yv, C.M, D.eps, C.tokens, C.seg, se, labels, D.T, k, D.V); break;
+      default:
+        rmsnorm_bf16_kernel<<<warp_blocks(C.M), 256, 0, C.st>>>(xv, gv, yv, C.M, D.d / 8, D.eps, C.tokens, C.seg, se,
+                                                                labels, D.T, k, D.V);
+    }
     mtp::note_launch();
   } else {
     rmsnorm_kernel<T><<<warp_blocks(C.M), 256, 0, C.st>>>(x, g, y, C.M, D.d, D.eps);
@@ -759,10 +840,19 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
     auto wt = [&](const void* const* arr) { return static_cast<const T*>(arr[i]); };
     mtp::prof_begin(MTP_KC_PROLOGUE, C.st);
     if constexpr (sizeof(T) == 2) {
-      prologue_bf16_kernel<<<warp_blocks(M), 256, 0, C.st>>>(
-          reinterpret_cast<const uint4*>(h_prev), C.tokens, static_cast<const uint4*>(C.W.embed),
-          static_cast<const uint4*>(C.W.hnorm[i]), static_cast<const uint4*>(C.W.enorm[i]),
-          reinterpret_cast<uint4*>(c), M, D.T, d / 8, D.V, k, D.eps);
+      const uint4* hp = reinterpret_cast<const uint4*>(h_prev);
+      const uint4* ev = static_cast<const uint4*>(C.W.embed);
+      const uint4* gh = static_cast<const uint4*>(C.W.hnorm[i]);
+      const uint4* ge = static_cast<const uint4*>(C.W.enorm[i]);
+      uint4* cv = reinterpret_cast<uint4*>(c);
+      switch (d) {
+        case 256: prologue_bf16_reg_kernel<1><<<warp_blocks(M), 256, 0, C.st>>>(hp, C.tokens, ev, gh, ge, cv, M, D.T, D.V, k, D.eps); break;
+        case 512: prologue_bf16_reg_kernel<2><<<warp_blocks(M), 256, 0, C.st>>>(hp, C.tokens, ev, gh, ge, cv, M, D.T, D.V, k, D.eps); break;
+        case 1024: prologue_bf16_reg_kernel<4><<<warp_blocks(M), 256, 0, C.st>>>(hp, C.tokens, ev, gh, ge, cv, M, D.T, D.V, k, D.eps); break;
+        default:
+          prologue_bf16_kernel<<<warp_blocks(M), 256, 0, C.st>>>(hp, C.tokens, ev, gh, ge, cv, M, D.T, d / 8, D.V, k,
+                                                                 D.eps);
+      }
     } else {
       prologue_kernel<T><<<warp_blocks(M), 256, 0, C.st>>>(h_prev, C.tokens, static_cast<const T*>(C.W.embed),
                                                            wt(C.W.hnorm), wt(C.W.enorm), c, M, D.T, d, D.V, k, D.eps);
