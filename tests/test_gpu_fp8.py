@@ -2,7 +2,8 @@
 oracle (exact dequantisation W = e4m3(q) * scale per 128 x 128 block).
 
 GEMM (mtp_gemm_fp8w): out += x~ W^T, x~ the two-term e4m3 form of x (the
-oracle's split, bit for bit), within 2e-5 of Σ_k |x~||W| per entry -- the
+oracle's split, bit for bit), within 2e-5 of Σ_k |x~||W| per entry, and
+against the unsplit x W^T within that plus the split's exactness bound -- the
 kernel sums exact e4m3 x e4m3 products in fp32 per 128-wide k-block and adds
 the scaled partials in fp32, so its error is a few hundred fp32 roundings of
 that sum at most; any layout, split or scale-index mistake is O(1).  Shapes
@@ -58,8 +59,20 @@ def test_gemm_parity(R, N, K):
     W = of.dequantize(q, s)
     ref = out0.double().numpy() + xs @ W.T
     bound = np.abs(xs) @ np.abs(W).T
-    err = np.abs(out.cpu().double().numpy() - ref)
+    got = out.cpu().double().numpy()
+    err = np.abs(got - ref)
     assert np.all(err <= 2e-5 * bound + 1e-6 * np.abs(out0.double().numpy())), err.max()
+    # against the unsplit product x W^T as well: the two-term form moves an element by at most
+    # 2^-17 of its 128-wide k-tile's largest (the split's exactness bound, from the e4m3
+    # mantissas alone), so the difference is bounded without reference to the split itself
+    xd = x.double().numpy()
+    nkb = -(-K // 128)
+    tile_max = np.stack([np.abs(xd[:, i * 128:(i + 1) * 128]).max(axis=1) for i in range(nkb)], axis=1)
+    absW = np.abs(W)
+    wsum = np.stack([absW[:, i * 128:(i + 1) * 128].sum(axis=1) for i in range(nkb)], axis=1)  # [N, nkb]
+    split_bound = 2.0 ** -17 * tile_max @ wsum.T
+    err_u = np.abs(got - (out0.double().numpy() + xd @ W.T))
+    assert np.all(err_u <= 2e-5 * (np.abs(xd) @ absW.T) + split_bound + 1e-6 * np.abs(out0.double().numpy()))
 
 
 def test_gemm_argument_errors():
