@@ -439,6 +439,78 @@ __global__ void ce_reduce_kernel(int M, int nvt, const float2* __restrict__ part
   }
 }
 
+// ce_reduce_kernel with the partials of G rows held in registers (nvt <= 32 NPL): a warp
+// issues the loads of its G rows at once and reads each partial once.  Per row the same
+// lane-strided maximum and sum as ce_reduce_kernel, so the same results bit for bit.
+template <int NPL, int G>
+__global__ void ce_reduce_reg_kernel(int M, int nvt, const float2* __restrict__ part, const float* __restrict__ zt,
+                                     const int32_t* __restrict__ labels, float* __restrict__ row_loss,
+                                     double* __restrict__ sum_count, float* __restrict__ lse_out) {
+  mtp::pdl_trigger();  // a GEMM that follows may start its setup
+  __shared__ double s_sum[8];
+  __shared__ int s_cnt[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  double wsum = 0.0;
+  int wcnt = 0;
+  const int stride = gridDim.x * 8;
+  for (int m0 = blockIdx.x * 8 + warp; m0 < M; m0 += G * stride) {
+    float2 v[G][NPL];
+    int lab[G];
+#pragma unroll
+    for (int r = 0; r < G; ++r) {
+      const int m = m0 + r * stride;
+      lab[r] = m < M ? labels[m] : -1;
+      const float2* p = part + static_cast<size_t>(m < M ? m : 0) * nvt;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int j = lane + 32 * i;
+        v[r][i] = (lab[r] >= 0 && j < nvt) ? p[j] : make_float2(-INFINITY, 0.f);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < G; ++r) {
+      const int m = m0 + r * stride;
+      if (m >= M) continue;
+      float loss = NAN;
+      if (lab[r] >= 0) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i)
+          if (lane + 32 * i < nvt) mx = fmaxf(mx, v[r][i].x);
+        mx = mtp::warp_max(mx);
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i)
+          if (lane + 32 * i < nvt) sum += v[r][i].y * expf(v[r][i].x - mx);
+        sum = mtp::warp_sum(sum);
+        const float lse = mx + logf(sum);
+        loss = lse - zt[m];
+        if (lse_out && lane == 0) lse_out[m] = lse;
+        wsum += loss;
+        ++wcnt;
+      }
+      if (lane == 0 && row_loss) row_loss[m] = loss;
+    }
+  }
+  if (lane == 0) {
+    s_sum[warp] = wsum;
+    s_cnt[warp] = wcnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double a = 0.0;
+    int c = 0;
+    for (int w = 0; w < 8; ++w) {
+      a += s_sum[w];
+      c += s_cnt[w];
+    }
+    if (c) {
+      atomicAdd(sum_count, a);
+      atomicAdd(sum_count + 1, static_cast<double>(c));
+    }
+  }
+}
+
 __global__ void zero_f64_kernel(double* p, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) p[i] = 0.0;
@@ -782,9 +854,22 @@ mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double
                                                              part, zt, C.L.nvt);
     mtp::note_launch();
   }
-  ce_reduce_kernel<<<std::min((C.M + 7) / 8, 256), 256, 0, C.st>>>(
-      C.M, C.L.nvt, part, zt, labels, row_loss_term, sum_count,
-      C.lse_save ? C.lse_save + static_cast<size_t>(k) * C.M : nullptr);
+  {
+    const int grid = std::min((C.M + 7) / 8, 256);
+    float* lse_out = C.lse_save ? C.lse_save + static_cast<size_t>(k) * C.M : nullptr;
+    const int nvt = C.L.nvt;
+    if (nvt <= 128)
+      ce_reduce_reg_kernel<4, 4><<<grid, 256, 0, C.st>>>(C.M, nvt, part, zt, labels, row_loss_term, sum_count,
+                                                         lse_out);
+    else if (nvt <= 256)
+      ce_reduce_reg_kernel<8, 2><<<grid, 256, 0, C.st>>>(C.M, nvt, part, zt, labels, row_loss_term, sum_count,
+                                                         lse_out);
+    else if (nvt <= 512)
+      ce_reduce_reg_kernel<16, 1><<<grid, 256, 0, C.st>>>(C.M, nvt, part, zt, labels, row_loss_term, sum_count,
+                                                          lse_out);
+    else
+      ce_reduce_kernel<<<grid, 256, 0, C.st>>>(C.M, nvt, part, zt, labels, row_loss_term, sum_count, lse_out);
+  }
   mtp::note_launch();
   MTP_LAUNCH_CHECK();
   return MTP_OK;
