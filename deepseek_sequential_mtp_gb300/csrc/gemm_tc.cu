@@ -17,10 +17,12 @@
 //              reads TMEM lanes 32*(w%4)..+31 = tile rows), applies the fused
 //              operation and writes each 32-row x 64-column bf16 box into a
 //              128-byte-swizzled shared-memory buffer (two per warp) that one
-//              lane ships with a TMA store.  The residual is read into
-//              registers from global memory: the tile's first two 64-column
-//              pieces while its MMAs still run, later pieces two ahead.  The
-//              CE epilogue stores only per-row partials.
+//              lane ships with a TMA store.  The residual epilogue has one box
+//              per 64-column piece of the tile: the warp's 32 rows of the
+//              residual are loaded into them by TMA while the tile's MMAs
+//              still run, each thread adds its row's accumulator in place and
+//              the boxes go back out by TMA.  The CE epilogue stores only
+//              per-row partials.
 // With more than one 128-row tile, 256-wide tiles run on CTA pairs (clusters of
 // two): 256x256 tiles with tcgen05.mma.cta_group::2 issued by the leader, each
 // CTA staging its 128 rows of A and half of B.
@@ -57,14 +59,18 @@ struct Cfg {
   // MMAs of the next tile more: the head GEMM measured 3% slower with them.)
   static constexpr int kEpiWarps = 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
-  static constexpr int kStages = PAIR ? 6 : (BN == 256 ? 4 : (BN == 128 ? 6 : 10));
+  // the residual epilogue's boxes (a whole tile's worth) take the place of ring stages
+  static constexpr int kStages = EPI == EPI_RESID ? (PAIR ? 5 : (BN == 256 ? 3 : 6))
+                                                  : (PAIR ? 6 : (BN == 256 ? 4 : (BN == 128 ? 6 : 10)));
   static constexpr int kABytes = BM * BK * 2;
   static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
-  // per epilogue warp: two 32 x 64 bf16 boxes (4 KB each); none for the CE epilogue
+  // per epilogue warp: 32 x 64 bf16 boxes (4 KB each), two (one per 64-column piece of
+  // the tile for the residual epilogue); none for the CE epilogue
   static constexpr int kBoxBytes = 32 * 64 * 2;
-  static constexpr int kStagingBytes = epi_uses_staging(EPI) ? 4 * 2 * kBoxBytes : 0;
+  static constexpr int kBoxesPerWarp = EPI == EPI_RESID ? BN / 64 : 2;
+  static constexpr int kStagingBytes = epi_uses_staging(EPI) ? 4 * kBoxesPerWarp * kBoxBytes : 0;
   // + 1024: alignment of the stage ring; + 512: mbarriers (8 B each, 2 S + 13 slots) and the
   // TMEM address and abort flag after them (256 B did not cover the 10-stage configuration)
   static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024 + 512;
@@ -326,35 +332,14 @@ __device__ __forceinline__ void box_write32(uint8_t* box, int lane, int half, co
     *reinterpret_cast<uint4*>(box + lane * 128 + ((c ^ (lane & 7)) << 4)) = *reinterpret_cast<uint4*>(h);
   }
 }
-// 64 residual columns [col0, col0 + 64) of one row as 8 x (8 bf16); zero outside [0, M) x [0, N)
-// Fetch `bytes` (a multiple of 16, from a 16-byte aligned address) into L2 without waiting.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void load_res64(uint4 (&r)[8], const __nv_bfloat16* resid, int ldr, int M, int N, int row,
-                                           int col0) {
-  const __nv_bfloat16* src = resid + static_cast<size_t>(row) * ldr + col0;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int col = col0 + 8 * k;
-    r[k] = make_uint4(0u, 0u, 0u, 0u);
-    if (row < M && col + 8 <= N) {
-      r[k] = __ldg(reinterpret_cast<const uint4*>(src + 8 * k));
-    } else if (row < M && col < N) {  // ragged right edge: element by element
-      uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (col + i < N)
-          w[i >> 1] |= static_cast<uint32_t>(__bfloat16_as_ushort(src[8 * k + i])) << (16 * (i & 1));
-      r[k] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-  }
-}
-// v[i] += residual column 32*half + i (pieces 4*half .. 4*half + 3)
-__device__ __forceinline__ void add_res32(float (&v)[32], const uint4 (&r)[8], int half) {
+// v[i] += the residual at this lane's row, columns [32 half, 32 half + 32) of a box that TMA
+// loaded with the 128-byte swizzle (the positions box_write32 then overwrites)
+__device__ __forceinline__ void box_add_res32(const uint8_t* box, int lane, int half, float (&v)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r[4 * half + q]);
+    const int c = half * 4 + q;
+    const uint4 w = *reinterpret_cast<const uint4*>(box + lane * 128 + ((c ^ (lane & 7)) << 4));
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float2 f = __bfloat1622float2(h[i]);
@@ -386,7 +371,7 @@ template <int BN, int EPI, int MNF = 0, bool PAIR = false>
 __global__ void __launch_bounds__(Cfg<BN, EPI, PAIR>::kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
-               const __grid_constant__ CUtensorMap tmOut,
+               const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmRes,
                const Args P) {
   using C = Cfg<BN, EPI, PAIR>;
   constexpr int S = C::kStages;
@@ -404,6 +389,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
   const uint32_t final_bar = bar0 + 8u * (2 * S + 4);
+  auto res_bar = [&](int w) { return bar0 + 8u * (2 * S + 5 + w); };  // residual boxes of epilogue warp w
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -421,6 +407,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       mbar_init(tempty_bar(a), (PAIR ? 2 : 1) * 32 * C::kEpiWarps);  // a pair: both CTAs' epilogue threads
     }
     mbar_init(final_bar, 1);
+    for (int w = 0; w < 4; ++w) mbar_init(res_bar(w), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -625,10 +612,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // ------------------------------ epilogue ------------------------------
     const int quarter = warp & 3;  // TMEM lanes 32*quarter.. = tile rows
     const int ew = warp - 2;       // epilogue warp index: owns two staging boxes
-    uint8_t* boxes = staging + ew * 2 * C::kBoxBytes;
+    uint8_t* boxes = staging + ew * C::kBoxesPerWarp * C::kBoxBytes;
     int nb = 0;                        // next staging box
     int local = 0;
     bool both_pending = false;         // the last store group read both boxes
+    bool res_inflight = false;         // residual boxes requested and not yet waited for
     // claim staging box nb: the store issued from it two boxes ago has read it
     auto claim = [&]() -> uint8_t* {
       if (lane == 0) {
@@ -655,19 +643,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       unit_tile(t, tm, tn);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
-      // residual: the first two 64-column pieces of this lane's row are fetched while the
-      // tile's MMAs run; piece c + 2 is fetched while piece c is written
-      uint4 rq[2][8];
+      // residual: the warp's 32 rows of every 64-column piece of the tile are loaded by TMA into
+      // its boxes while the tile's MMAs run, once the previous tile's stores have read them
       if constexpr (EPI == EPI_RESID) {
-        const int rrow = tm * BM + quarter * 32 + lane;
-        // the whole row piece of the tile goes to L2 now, so that pieces 2 and 3, read during
-        // the epilogue, do not queue DRAM misses behind the next tile's operand loads
-        if (rrow < P.M) {
-          const uint32_t bytes = static_cast<uint32_t>(2 * min(BN, P.N - tn * BN)) & ~15u;
-          if (bytes) prefetch_l2_bulk(P.resid + static_cast<size_t>(rrow) * P.ldr + tn * BN, bytes);
+        if (lane == 0) {
+          bulk_wait_read0();
+          const int r0 = tm * BM + quarter * 32;
+          uint32_t bytes = 0;
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c)
+            if (r0 < P.M && tn * BN + 64 * c < P.N) bytes += C::kBoxBytes;
+          if (bytes) {
+            mbar_expect_tx(res_bar(ew), bytes);
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)
+              if (r0 < P.M && tn * BN + 64 * c < P.N)
+                tma_load_2d(smem_u32(boxes + c * C::kBoxBytes), &tmRes, tn * BN + 64 * c, r0, res_bar(ew));
+          } else {
+            mbar_arrive(res_bar(ew));
+          }
         }
-        load_res64(rq[0], P.resid, P.ldr, P.M, P.N, rrow, tn * BN);
-        load_res64(rq[1], P.resid, P.ldr, P.M, P.N, rrow, tn * BN + 64);
+        __syncwarp();
+        res_inflight = true;
       }
       // CE backward: the row's label, log-sum-exp and scale, fetched while the MMAs run
       // (log2 domain; a row without a label gets lse = +inf, so its exp is 0 and its scale 0)
@@ -703,20 +700,24 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           ship(box, col0, row0w);
         }
       } else if constexpr (EPI == EPI_RESID) {
-#pragma unroll
+        if (!mbar_wait(res_bar(ew), local & 1, abort_flag)) break;
+        res_inflight = false;
+#pragma unroll 1
         for (int c = 0; c < BN / 64; ++c) {
-          const int col0 = tn * BN + c * 64;
-          uint8_t* box = claim();
+          uint8_t* box = boxes + c * C::kBoxBytes;
           float v[32];
           tmem_ld32(taddr + c * 64, v);
-          add_res32(v, rq[c & 1], 0);
+          box_add_res32(box, lane, 0, v);
           box_write32(box, lane, 0, v);
           tmem_ld32(taddr + c * 64 + 32, v);
-          add_res32(v, rq[c & 1], 1);
+          box_add_res32(box, lane, 1, v);
           box_write32(box, lane, 1, v);
-          if (c + 2 < BN / 64) load_res64(rq[c & 1], P.resid, P.ldr, P.M, P.N, row, col0 + 128);
-          ship(box, col0, row0w);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0 && tn * BN + c * 64 < P.N && row0w < P.M)
+            tma_store_2d(&tmOut, tn * BN + c * 64, row0w, smem_u32(box));
         }
+        if (lane == 0) bulk_commit();
       } else if constexpr (EPI == EPI_ROPE) {
         const int tile_col0 = tn * BN;
         if (tile_col0 >= P.rope_cols) {
@@ -926,6 +927,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         mbar_arrive(tempty_bar(acc));
       }
     }
+    // after an abort: the residual boxes still being loaded land before the CTA leaves
+    if (EPI == EPI_RESID && res_inflight && lane == 0) mbar_wait_drain(res_bar(ew), local & 1, 40000000ll);
     if constexpr (EPI != EPI_CE) {
       if (lane == 0) {
         bulk_wait_all();  // every TMA store of this warp has completed
@@ -1015,6 +1018,8 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
   // output / residual boxes: 32 rows x 64 columns, 128-byte swizzle
   CUtensorMap tout = ta;
   if (epi_uses_staging(EPI) && !make_map(&tout, g.out, g.M, g.N, g.ldo, 32)) return MTP_ERR_INVALID_ARG;
+  CUtensorMap tres = tout;
+  if (EPI == EPI_RESID && !make_map(&tres, g.resid, g.M, g.N, g.ldr, 32)) return MTP_ERR_INVALID_ARG;
   Args a{};
   a.M = g.M;
   a.N = g.N;
@@ -1060,7 +1065,7 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = g.pdl ? 2 : 1;
-    MTP_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EPI, MNF, PAIR>, ta, tb[0], tb[1], tb[2], tout, a));
+    MTP_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EPI, MNF, PAIR>, ta, tb[0], tb[1], tb[2], tout, tres, a));
   } else {
     const int ntiles = a.tiles_m * a.tiles_n * a.splits;
     cudaLaunchConfig_t cfg{};
@@ -1073,7 +1078,7 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = g.pdl ? 1 : 0;
-    MTP_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EPI, MNF, PAIR>, ta, tb[0], tb[1], tb[2], tout, a));
+    MTP_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EPI, MNF, PAIR>, ta, tb[0], tb[1], tb[2], tout, tres, a));
   }
   mtp::note_launch();
   MTP_LAUNCH_CHECK();
