@@ -23,8 +23,9 @@ MTP_DEFINE_ERROR_WORD(mtp_take_errors_attn)
 
 namespace mtp {
 
+// work_ctr (bf16): a device int that is 0 on entry and is used up by the launch (one per launch)
 mtp_status attn_launch(int dtype, const void* qkv, void* out, const int32_t* seg_start, int B, int T,
-                       int H, int hd, cudaStream_t stream, float* lse2_out = nullptr);
+                       int H, int hd, cudaStream_t stream, float* lse2_out = nullptr, int* work_ctr = nullptr);
 mtp_status attn_bwd_launch(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16* dO,
                            const float* lse2, const int32_t* seg_start, const int32_t* seg_end, float* dqkv,
                            float* dsum, int B, int T, int H, int hd, cudaStream_t stream);
@@ -398,7 +399,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
 //              block up front), skipping a tile outside its key range.
 // Tile A needs key blocks [seg_start(q0) / 128, q0 / 128], tile B
 // [seg_start(q0 + 128) / 128, (q0 + 128) / 128]: A's range is a prefix of the
-// union, B's a suffix.  Every wait is bounded.
+// union, B's a suffix.  Work items run from the last query pairs (the longest
+// key ranges) to the first; a CTA starts with item blockIdx.x and claims each
+// further one from a global counter (atomicAdd) when that item's Q buffer
+// frees, so CTAs whose items were short take more of them.  The TMA lane that claims an item publishes it,
+// with its tiles' segment starts, in a shared-memory ring that the V lane, the
+// MMA thread and the softmax warps read in the same order.  Every wait is
+// bounded.
 // ---------------------------------------------------------------------------
 constexpr int kT2Threads = 320;
 
@@ -415,9 +422,14 @@ struct Tc2Attn {
   static constexpr int kOffK = kQBufs * 2 * kQBytes;
   static constexpr int kOffV = kOffK + kKStages * kKBytes;
   static constexpr int kOffBar = kOffV + kVStages * kVBytes;
-  // q full/empty, k full/empty, v full/empty; per tile s_full, p_full, pv_done, o_free; drain
-  static constexpr int kNumBars = 2 * (kQBufs + kKStages + kVStages) + 8 + 1;
-  static constexpr int kSmemBytes = kOffBar + 8 * kNumBars + 16;
+  static constexpr int kRing = 4;  // claimed work items published ahead of their consumers
+  // readers of a ring slot: the V lane, the MMA thread and one lane of each softmax warp
+  static constexpr int kItemReaders = 10;
+  // q full/empty, k full/empty, v full/empty; per tile s_full, p_full, pv_done, o_free; drain;
+  // item ring full/empty
+  static constexpr int kNumBars = 2 * (kQBufs + kKStages + kVStages) + 8 + 1 + 2 * kRing;
+  static constexpr int kOffItems = (kOffBar + 8 * kNumBars + 15) / 16 * 16;
+  static constexpr int kSmemBytes = kOffItems + 16 * kRing + 16;
   static constexpr uint32_t kColO0 = 256;
 };
 
@@ -425,7 +437,7 @@ template <int HD>
 __global__ void __launch_bounds__(kT2Threads, 1)
 attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant__ CUtensorMap tm64,
                 __nv_bfloat16* __restrict__ out, const int32_t* __restrict__ seg_start, int B, int T, int H,
-                float scale_log2, float* __restrict__ lse2_out) {
+                float scale_log2, float* __restrict__ lse2_out, int* __restrict__ work_ctr) {
   using C = Tc2Attn<HD>;
   pdl_trigger();  // the output projection that follows may start its setup
   extern __shared__ __align__(1024) uint8_t attn2_smem[];
@@ -451,7 +463,11 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
   auto pv_done = [&](int x) { return barx + 32u + 8u * x; };
   auto o_free = [&](int x) { return barx + 48u + 8u * x; };
   const uint32_t drain_bar = barx + 64u;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + 8 * C::kNumBars);
+  auto it_full = [&](int i) { return barx + 72u + 8u * i; };
+  auto it_empty = [&](int i) { return barx + 72u + 8u * (C::kRing + i); };
+  // ring slot: (item, segment start of tile A's first query, of tile B's first query); item -1 ends
+  int4* items = reinterpret_cast<int4*>(smem + C::kOffItems);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffItems + 16 * C::kRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   unsigned int* err = &g_mtp_error_word;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -480,6 +496,10 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
       mtp::mbar_init(o_free(x), kTcQ);
     }
     mtp::mbar_init(drain_bar, 1);
+    for (int i = 0; i < C::kRing; ++i) {
+      mtp::mbar_init(it_full(i), 1);
+      mtp::mbar_init(it_empty(i), C::kItemReaders);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -502,7 +522,7 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
     b = r / H;
     q0 = qp * 2 * kTcQ;
   };
-  // segment starts of both tiles' first queries (loaded one work item ahead)
+  // segment starts of both tiles' first queries
   auto first_keys = [&](int t) {
     if (t >= n_items) return make_int2(0, 0);
     int b, h, q0;
@@ -536,18 +556,43 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
       const bool kside = lane == 0;
       const int stages = kside ? C::kKStages : C::kVStages;
       uint32_t g = 0, issued = 0;
-      int tl = 0, q_loads = 0;
+      int q_loads = 0;
       bool ok = true;
-      int2 key_next = first_keys(blockIdx.x);
-      for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x, ++tl) {
-        const int2 keys = key_next;
-        key_next = first_keys(t + gridDim.x);
-        int b, h, q0;
-        coords(t, b, h, q0);
-        const Ranges R = ranges(q0, keys);
+      // lane 0 claims item tl: with two Q buffers when item tl - 2 has released its Q (a CTA
+      // then holds at most about one claimed item it has not started); with one, as soon as
+      // item tl - 1 is published (its Q load waits for the previous item, so a later claim
+      // would add the claim's latency to that wait)
+      int t_next = static_cast<int>(blockIdx.x);
+      for (int tl = 0; ok; ++tl) {
+        const int slot = tl % C::kRing;
+        const int qi = tl % C::kQBufs, qu = tl / C::kQBufs;
+        int4 it;
         if (kside) {
-          const int qi = tl % C::kQBufs, qu = tl / C::kQBufs;
-          if (qu > 0 && !wait(q_empty(qi), (qu - 1) & 1)) { ok = false; break; }
+          if (C::kQBufs > 1) {
+            if (qu > 0 && !wait(q_empty(qi), (qu - 1) & 1)) { ok = false; break; }
+            if (tl > 0) t_next = static_cast<int>(gridDim.x) + atomicAdd(work_ctr, 1);
+          }
+          const int t = t_next;
+          const int2 k2 = t < n_items ? first_keys(t) : make_int2(0, 0);
+          it = make_int4(t < n_items ? t : -1, k2.x, k2.y, 0);
+          if (tl >= C::kRing && !wait(it_empty(slot), (tl / C::kRing - 1) & 1)) { ok = false; break; }
+          items[slot] = it;
+          mtp::mbar_arrive1(it_full(slot));
+          if (it.x < 0) break;
+          if (C::kQBufs == 1) {
+            t_next = static_cast<int>(gridDim.x) + atomicAdd(work_ctr, 1);
+            if (qu > 0 && !wait(q_empty(qi), (qu - 1) & 1)) { ok = false; break; }
+          }
+        } else {
+          if (!wait(it_full(slot), (tl / C::kRing) & 1)) { ok = false; break; }
+          it = items[slot];
+          mtp::mbar_arrive1(it_empty(slot));
+          if (it.x < 0) break;
+        }
+        int b, h, q0;
+        coords(it.x, b, h, q0);
+        const Ranges R = ranges(q0, make_int2(it.y, it.z));
+        if (kside) {
           const bool has_b = R.hi[1] >= R.lo[1];
           mtp::mbar_expect_tx(q_full(qi), (has_b ? 2 : 1) * C::kQBytes);
           for (int x = 0; x < (has_b ? 2 : 1); ++x)
@@ -591,15 +636,16 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
       uint32_t g = 0;                  // union key blocks consumed (K/V ring position)
       uint32_t ns[2] = {0u, 0u};       // S products issued per tile (= P V products after the block)
       uint32_t no[2] = {0u, 0u};       // work items per tile whose output the softmax has read
-      int tl = 0;
       bool ok = true, any = false;
-      int2 key_next = first_keys(blockIdx.x);
-      for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x, ++tl) {
-        const int2 keys = key_next;
-        key_next = first_keys(t + gridDim.x);
+      for (int tl = 0; ok; ++tl) {
+        const int slot = tl % C::kRing;
+        if (!wait(it_full(slot), (tl / C::kRing) & 1)) { ok = false; break; }
+        const int4 it = items[slot];
+        mtp::mbar_arrive1(it_empty(slot));
+        if (it.x < 0) break;
         int b, h, q0;
-        coords(t, b, h, q0);
-        const Ranges R = ranges(q0, keys);
+        coords(it.x, b, h, q0);
+        const Ranges R = ranges(q0, make_int2(it.y, it.z));
         auto active = [&](int x, int j) { return j >= R.lo[x] && j <= R.hi[x]; };
         const int qi = tl % C::kQBufs;
         if (!wait(q_full(qi), (tl / C::kQBufs) & 1)) { ok = false; break; }
@@ -683,27 +729,21 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
     const uint32_t colS = 128u * x, colO = C::kColO0 + HD * x;
     auto wwait = [&](uint32_t bar, uint32_t parity) { return __all_sync(0xffffffffu, wait(bar, parity)); };
     uint32_t n = 0;  // S products of this tile consumed
-    // this row's segment start in work item t (loaded one item ahead)
-    auto row_start = [&](int t) {
-      if (t >= n_items) return 0;
+    for (int tl = 0;; ++tl) {
+      const int slot = tl % C::kRing;
+      if (!wwait(it_full(slot), (tl / C::kRing) & 1)) break;
+      const int4 it = items[slot];
+      __syncwarp();
+      if (lane == 0) mtp::mbar_arrive1(it_empty(slot));
+      if (it.x < 0) break;
       int b, h, q0;
-      coords(t, b, h, q0);
-      const int q = q0 + kTcQ * x + row;
-      return q < T ? static_cast<int>(seg_start[static_cast<size_t>(b) * T + q]) : q;
-    };
-    int2 key_next = first_keys(blockIdx.x);
-    int st_next = row_start(blockIdx.x);
-    for (int t = blockIdx.x; t < n_items; t += gridDim.x) {
-      const int2 keys = key_next;
-      const int st_row = st_next;
-      key_next = first_keys(t + gridDim.x);
-      st_next = row_start(t + gridDim.x);
-      int b, h, q0;
-      coords(t, b, h, q0);
-      const Ranges R = ranges(q0, keys);
+      coords(it.x, b, h, q0);
+      const Ranges R = ranges(q0, make_int2(it.y, it.z));
       if (R.hi[x] < R.lo[x]) continue;  // tile B past the end of the row
       const int q = q0 + kTcQ * x + row;
       const bool live = q < T;
+      // this row's segment start (first used after the item's first scores arrive)
+      const int st_row = live ? static_cast<int>(seg_start[static_cast<size_t>(b) * T + q]) : q;
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = R.lo[x]; j <= R.hi[x]; ++j, ++n) {
@@ -804,11 +844,12 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
 
 template <int HD>
 mtp_status attn_tc2_launch(const __nv_bfloat16* qkv, __nv_bfloat16* out, const int32_t* seg_start, int B, int T,
-                           int H, float scale_log2, float* lse2_out, cudaStream_t stream) {
+                           int H, float scale_log2, float* lse2_out, int* work_ctr, cudaStream_t stream) {
   using C = Tc2Attn<HD>;
   static PerDevice attr;
   if (!smem_limit(attr, attn_tc2_kernel<HD>, C::kSmemBytes)) return MTP_ERR_CUDA;
   if (!aligned16(qkv) || !aligned16(out)) return MTP_ERR_ALIGNMENT;
+  if (!work_ctr) return MTP_ERR_INVALID_ARG;
   const int d = H * HD;
   const uint64_t rows = static_cast<uint64_t>(B) * T;
   if (rows > 0x7FFFFFFFull) return MTP_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
@@ -821,7 +862,7 @@ mtp_status attn_tc2_launch(const __nv_bfloat16* qkv, __nv_bfloat16* out, const i
   const int sms = sm_count_current();
   const int grid = static_cast<int>(n_items < sms ? n_items : sms);
   attn_tc2_kernel<HD><<<grid, kT2Threads, C::kSmemBytes, stream>>>(m128, m64, out, seg_start, B, T, H, scale_log2,
-                                                                  lse2_out);
+                                                                  lse2_out, work_ctr);
   note_launch();
   MTP_LAUNCH_CHECK();
   return MTP_OK;
@@ -831,16 +872,16 @@ mtp_status attn_tc2_launch(const __nv_bfloat16* qkv, __nv_bfloat16* out, const i
 }  // namespace
 
 mtp_status attn_launch(int dtype, const void* qkv, void* out, const int32_t* seg_start, int B, int T, int H,
-                       int hd, cudaStream_t stream, float* lse2_out) {
+                       int hd, cudaStream_t stream, float* lse2_out, int* work_ctr) {
   if (B <= 0 || T <= 0) return MTP_OK;
   if (dtype == MTP_BF16) {
     const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(hd));
     if (hd == 64)
       return attn_tc2_launch<64>(static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out), seg_start,
-                                B, T, H, scale_log2, lse2_out, stream);
+                                B, T, H, scale_log2, lse2_out, work_ctr, stream);
     if (hd == 128)
       return attn_tc2_launch<128>(static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(out),
-                                 seg_start, B, T, H, scale_log2, lse2_out, stream);
+                                 seg_start, B, T, H, scale_log2, lse2_out, work_ctr, stream);
     return MTP_ERR_UNSUPPORTED;
   } else {
     const int warps = 4;

@@ -33,8 +33,9 @@ namespace mtp {
 mtp_status attn_bwd_launch(const __nv_bfloat16* qkv, const __nv_bfloat16* o, const __nv_bfloat16* dO,
                            const float* lse2, const int32_t* seg_start, const int32_t* seg_end, float* dqkv,
                            float* dsum, int B, int T, int H, int hd, cudaStream_t stream);
+// work_ctr (bf16): a device int that is 0 on entry and is used up by the launch (one per launch)
 mtp_status attn_launch(int dtype, const void* qkv, void* out, const int32_t* seg_start, int B, int T, int H,
-                       int hd, cudaStream_t stream, float* lse2_out = nullptr);
+                       int hd, cudaStream_t stream, float* lse2_out = nullptr, int* work_ctr = nullptr);
 }
 
 namespace {
@@ -64,9 +65,13 @@ __device__ int block_scan_max(int v, int* sh) {  // inclusive max-scan over thre
 
 __global__ void __launch_bounds__(kScanThreads)
 segments_kernel(const int32_t* __restrict__ seg, const int32_t* __restrict__ tokens, int T, int V,
-                int32_t* __restrict__ seg_start, int32_t* __restrict__ seg_end) {
+                int32_t* __restrict__ seg_start, int32_t* __restrict__ seg_end, int* __restrict__ work_ctrs,
+                int n_ctrs) {
   __shared__ int sh[kScanThreads];
   const int b = blockIdx.x;
+  // the attention launches of this call claim their work items from these counters
+  if (b == 0)
+    for (int i = threadIdx.x; i < n_ctrs; i += blockDim.x) work_ctrs[i] = 0;
   const int32_t* s = seg + static_cast<size_t>(b) * T;
   const int32_t* x = tokens + static_cast<size_t>(b) * T;
   int32_t* out_start = seg_start + static_cast<size_t>(b) * T;
@@ -565,7 +570,7 @@ inline bool valid_den(int den) { return den >= MTP_DEN_FIXED && den <= MTP_DEN_W
 inline size_t align_up(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-  size_t seg_start, seg_end, labels, c, u, x, qkv, o, a, g, g2, h0buf, h1buf, rope, ce_part, zt, total;
+  size_t seg_start, seg_end, labels, c, u, x, qkv, o, a, g, g2, h0buf, h1buf, rope, ce_part, zt, work_ctrs, total;
   int nvt;
 };
 
@@ -615,6 +620,7 @@ Layout make_layout(const mtp_dims& D) {
   L.rope = take(static_cast<size_t>(D.T) * (D.head_dim / 2) * sizeof(float2));
   L.ce_part = take(M * L.nvt * sizeof(float2));
   L.zt = take(M * 4);
+  L.work_ctrs = take(static_cast<size_t>(D.D) * sizeof(int));  // one per depth's attention launch
   L.total = off;
   return L;
 }
@@ -882,7 +888,7 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
   const int M = C.M, d = D.d;
   const size_t Md = static_cast<size_t>(M) * d;
   segments_kernel<<<D.B, kScanThreads, 0, C.st>>>(C.seg, C.tokens, D.T, D.V, C.buf<int32_t>(C.L.seg_start),
-                                                  C.buf<int32_t>(C.L.seg_end));
+                                                  C.buf<int32_t>(C.L.seg_end), C.buf<int>(C.L.work_ctrs), D.D);
   mtp::note_launch();
   const int half = D.head_dim / 2;
   if (D.rope_base > 0.f) {
@@ -957,7 +963,7 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
     mtp::prof_begin(MTP_KC_ATTENTION, C.st);
     float* lse2 = C.save ? reinterpret_cast<float*>(C.save + static_cast<size_t>(i) * C.so.bytes + C.so.lse2) : nullptr;
     TRY(mtp::attn_launch(D.dtype, qkv, o, C.buf<int32_t>(C.L.seg_start), D.B, D.T, D.n_heads, D.head_dim, C.st,
-                         lse2));
+                         lse2, C.buf<int>(C.L.work_ctrs) + i));
     mtp::prof_end(MTP_KC_ATTENTION, C.st);
     const T* wo[1] = {wt(C.W.wo)};
     mtp::prof_begin(MTP_KC_O_GEMM, C.st);
