@@ -513,6 +513,7 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
   __syncthreads();
   mtp::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // q/k/v come from the kernel before (this launch is its programmatic dependent)
 
   // work item t: query pair qp (last pairs first), head h, packed row b
   auto coords = [&](int t, int& b, int& h, int& q0) {
@@ -861,8 +862,9 @@ mtp_status attn_tc2_launch(const __nv_bfloat16* qkv, __nv_bfloat16* out, const i
   if (n_items > 0x7FFFFFFFll) return MTP_ERR_UNSUPPORTED;
   const int sms = sm_count_current();
   const int grid = static_cast<int>(n_items < sms ? n_items : sms);
-  attn_tc2_kernel<HD><<<grid, kT2Threads, C::kSmemBytes, stream>>>(m128, m64, out, seg_start, B, T, H, scale_log2,
-                                                                  lse2_out, work_ctr);
+  // the QKV projection before it releases this launch when its CTAs start their last tiles
+  MTP_CUDA_TRY(launch_pdl(attn_tc2_kernel<HD>, dim3(grid), dim3(kT2Threads), C::kSmemBytes, stream, m128, m64, out,
+                          seg_start, B, T, H, scale_log2, lse2_out, work_ctr));
   note_launch();
   MTP_LAUNCH_CHECK();
   return MTP_OK;

@@ -198,6 +198,7 @@ __global__ void prologue_bf16_kernel(const uint4* __restrict__ h_prev, const int
                                      const uint4* __restrict__ g_e, uint4* __restrict__ c, int M, int Tlen, int d8,
                                      int V, int k, float eps) {
   mtp::pdl_trigger();  // a GEMM that follows may start its setup
+  mtp::pdl_wait();     // launched as a dependent of the kernel before it
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= M) return;
   const int m = warp;
@@ -248,6 +249,7 @@ __global__ void rmsnorm_bf16_kernel(const uint4* __restrict__ x, const uint4* __
                                     const int32_t* __restrict__ seg, const int32_t* __restrict__ seg_end,
                                     int32_t* __restrict__ labels, int Tlen, int k, int V) {
   mtp::pdl_trigger();  // a GEMM that follows may start its setup
+  mtp::pdl_wait();     // launched as a dependent of the kernel before it
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= M) return;
   const uint4* xr = x + static_cast<size_t>(warp) * d8;
@@ -399,6 +401,7 @@ __global__ void ce_reduce_kernel(int M, int nvt, const float2* __restrict__ part
                                  const int32_t* __restrict__ labels, float* __restrict__ row_loss,
                                  double* __restrict__ sum_count, float* __restrict__ lse_out) {
   mtp::pdl_trigger();  // a GEMM that follows may start its setup
+  mtp::pdl_wait();     // launched as a dependent of the kernel before it
   __shared__ double s_sum[8];
   __shared__ int s_cnt[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -452,6 +455,7 @@ __global__ void ce_reduce_reg_kernel(int M, int nvt, const float2* __restrict__ 
                                      const int32_t* __restrict__ labels, float* __restrict__ row_loss,
                                      double* __restrict__ sum_count, float* __restrict__ lse_out) {
   mtp::pdl_trigger();  // a GEMM that follows may start its setup
+  mtp::pdl_wait();     // launched as a dependent of the kernel before it
   __shared__ double s_sum[8];
   __shared__ int s_cnt[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -678,6 +682,7 @@ mtp_status gemm<__nv_bfloat16>(const Ctx& C, const __nv_bfloat16* A, int lda, co
   g.ldr = ldr;
   g.pdl = true;  // every forward-chain GEMM follows one of this library's kernels
   g.b_early = true;  // B is a weight matrix
+  g.trigger_early = true;  // the next kernel of the chain is a programmatic dependent
   if (epi == mtp::EPI_ROPE) {
     g.pos = C.pos;
     g.rope = C.buf<float2>(C.L.rope);
@@ -735,6 +740,7 @@ __global__ void rmsnorm_bf16_reg_kernel(const uint4* __restrict__ x, const uint4
                                         const int32_t* __restrict__ seg, const int32_t* __restrict__ seg_end,
                                         int32_t* __restrict__ labels, int Tlen, int k, int V) {
   mtp::pdl_trigger();  // a GEMM that follows may start its setup
+  mtp::pdl_wait();     // launched as a dependent of the kernel before it
   constexpr int d8 = 32 * NPL;
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= M) return;
@@ -763,6 +769,7 @@ __global__ void prologue_bf16_reg_kernel(const uint4* __restrict__ h_prev, const
                                          const uint4* __restrict__ g_e, uint4* __restrict__ c, int M, int Tlen, int V,
                                          int k, float eps) {
   mtp::pdl_trigger();  // a GEMM that follows may start its setup
+  mtp::pdl_wait();     // launched as a dependent of the kernel before it
   constexpr int d8 = 32 * NPL;
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= M) return;
@@ -796,22 +803,35 @@ __global__ void prologue_bf16_reg_kernel(const uint4* __restrict__ h_prev, const
   }
 }
 
+// pdl: launch as a programmatic dependent (the stream's previous operation is a kernel)
 template <typename T>
-void launch_rmsnorm(const Ctx& C, const T* x, const T* g, T* y, int32_t* labels = nullptr, int k = 0) {
+void launch_rmsnorm(const Ctx& C, const T* x, const T* g, T* y, int32_t* labels = nullptr, int k = 0,
+                    bool pdl = false) {
   const mtp_dims& D = C.D;
   if constexpr (sizeof(T) == 2) {
     const uint4* xv = reinterpret_cast<const uint4*>(x);
     const uint4* gv = reinterpret_cast<const uint4*>(g);
     uint4* yv = reinterpret_cast<uint4*>(y);
     const int32_t* se = C.buf<int32_t>(C.L.seg_end);
+    const dim3 grid(warp_blocks(C.M)), block(256);
+    auto go = [&](auto kern) {
+      if (pdl)
+        mtp::launch_pdl(kern, grid, block, 0, C.st, xv, gv, yv, C.M, D.eps, C.tokens, C.seg, se, labels, D.T, k, D.V);
+      else
+        kern<<<grid, block, 0, C.st>>>(xv, gv, yv, C.M, D.eps, C.tokens, C.seg, se, labels, D.T, k, D.V);
+    };
     switch (D.d) {
-      case 256: rmsnorm_bf16_reg_kernel<1><<<warp_blocks(C.M), 256, 0, C.st>>>(xv, gv, yv, C.M, D.eps, C.tokens, C.seg, se, labels, D.T, k, D.V); break;
-      case 512: rmsnorm_bf16_reg_kernel<2><<<warp_blocks(C.M), 256, 0, C.st>>>(xv, gv, yv, C.M, D.eps, C.tokens, C.seg, se, labels, D.T, k, D.V); break;
-      case 1024: rmsnorm_bf16_reg_kernel<4><<<warp_blocks(C.M), 256, 0, C.st>>>(xv, gv, yv, C.M, D.eps, C.tokens, C.seg, se, labels, D.T, k, D.V); break;
-      case 2048: rmsnorm_bf16_reg_kernel<8><<<warp_blocks(C.M), 256, 0, C.st>>>(xv, gv, yv, C.M, D.eps, C.tokens, C.seg, se, labels, D.T, k, D.V); break;
+      case 256: go(rmsnorm_bf16_reg_kernel<1>); break;
+      case 512: go(rmsnorm_bf16_reg_kernel<2>); break;
+      case 1024: go(rmsnorm_bf16_reg_kernel<4>); break;
+      case 2048: go(rmsnorm_bf16_reg_kernel<8>); break;
       default:
-        rmsnorm_bf16_kernel<<<warp_blocks(C.M), 256, 0, C.st>>>(xv, gv, yv, C.M, D.d / 8, D.eps, C.tokens, C.seg, se,
-                                                                labels, D.T, k, D.V);
+        if (pdl)
+          mtp::launch_pdl(rmsnorm_bf16_kernel, grid, block, 0, C.st, xv, gv, yv, C.M, D.d / 8, D.eps, C.tokens, C.seg,
+                          se, labels, D.T, k, D.V);
+        else
+          rmsnorm_bf16_kernel<<<grid, block, 0, C.st>>>(xv, gv, yv, C.M, D.d / 8, D.eps, C.tokens, C.seg, se, labels,
+                                                        D.T, k, D.V);
     }
     mtp::note_launch();
   } else {
@@ -833,7 +853,8 @@ mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double
   int32_t* labels = C.buf<int32_t>(C.L.labels);
   float2* part = C.buf<float2>(C.L.ce_part);
   float* zt = C.buf<float>(C.L.zt);
-  launch_rmsnorm<T>(C, h, static_cast<const T*>(C.W.out_norm), x, labels, k);
+  // its predecessor is a kernel: the previous depth's down projection or the zeroing of the sums
+  launch_rmsnorm<T>(C, h, static_cast<const T*>(C.W.out_norm), x, labels, k, true);
   MTP_LAUNCH_CHECK();
   if constexpr (sizeof(T) == 2) {
     mtp::GemmDesc g;
@@ -852,6 +873,7 @@ mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double
     g.z_tgt = zt;
     g.pdl = true;  // follows the RMSNorm kernel
     g.b_early = true;  // B = W_U
+    g.trigger_early = true;  // the CE reduction that follows is a programmatic dependent
     mtp::prof_begin(MTP_KC_HEAD_CE_GEMM, C.st);
     TRY(mtp::gemm_bf16_launch(g, C.st));
     mtp::prof_end(MTP_KC_HEAD_CE_GEMM, C.st);
@@ -864,17 +886,19 @@ mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double
     const int grid = std::min((C.M + 7) / 8, 256);
     float* lse_out = C.lse_save ? C.lse_save + static_cast<size_t>(k) * C.M : nullptr;
     const int nvt = C.L.nvt;
+    // a programmatic dependent of the head GEMM (bf16) or of the f32 head kernel
+    auto go = [&](auto kern) {
+      mtp::launch_pdl(kern, dim3(grid), dim3(256), 0, C.st, C.M, nvt, part, zt, labels, row_loss_term, sum_count,
+                      lse_out);
+    };
     if (nvt <= 128)
-      ce_reduce_reg_kernel<4, 4><<<grid, 256, 0, C.st>>>(C.M, nvt, part, zt, labels, row_loss_term, sum_count,
-                                                         lse_out);
+      go(ce_reduce_reg_kernel<4, 4>);
     else if (nvt <= 256)
-      ce_reduce_reg_kernel<8, 2><<<grid, 256, 0, C.st>>>(C.M, nvt, part, zt, labels, row_loss_term, sum_count,
-                                                         lse_out);
+      go(ce_reduce_reg_kernel<8, 2>);
     else if (nvt <= 512)
-      ce_reduce_reg_kernel<16, 1><<<grid, 256, 0, C.st>>>(C.M, nvt, part, zt, labels, row_loss_term, sum_count,
-                                                          lse_out);
+      go(ce_reduce_reg_kernel<16, 1>);
     else
-      ce_reduce_kernel<<<grid, 256, 0, C.st>>>(C.M, nvt, part, zt, labels, row_loss_term, sum_count, lse_out);
+      go(ce_reduce_kernel);
   }
   mtp::note_launch();
   MTP_LAUNCH_CHECK();
@@ -936,10 +960,20 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
       const uint4* gh = static_cast<const uint4*>(C.W.hnorm[i]);
       const uint4* ge = static_cast<const uint4*>(C.W.enorm[i]);
       uint4* cv = reinterpret_cast<uint4*>(c);
+      // from the second depth on the previous operation is a kernel (the head's CE reduction
+      // or the down projection): launch as its programmatic dependent
+      const bool pdl = k > 1;
+      auto go = [&](auto kern) {
+        if (pdl)
+          mtp::launch_pdl(kern, dim3(warp_blocks(M)), dim3(256), 0, C.st, hp, C.tokens, ev, gh, ge, cv, M, D.T, D.V,
+                          k, D.eps);
+        else
+          kern<<<warp_blocks(M), 256, 0, C.st>>>(hp, C.tokens, ev, gh, ge, cv, M, D.T, D.V, k, D.eps);
+      };
       switch (d) {
-        case 256: prologue_bf16_reg_kernel<1><<<warp_blocks(M), 256, 0, C.st>>>(hp, C.tokens, ev, gh, ge, cv, M, D.T, D.V, k, D.eps); break;
-        case 512: prologue_bf16_reg_kernel<2><<<warp_blocks(M), 256, 0, C.st>>>(hp, C.tokens, ev, gh, ge, cv, M, D.T, D.V, k, D.eps); break;
-        case 1024: prologue_bf16_reg_kernel<4><<<warp_blocks(M), 256, 0, C.st>>>(hp, C.tokens, ev, gh, ge, cv, M, D.T, D.V, k, D.eps); break;
+        case 256: go(prologue_bf16_reg_kernel<1>); break;
+        case 512: go(prologue_bf16_reg_kernel<2>); break;
+        case 1024: go(prologue_bf16_reg_kernel<4>); break;
         default:
           prologue_bf16_kernel<<<warp_blocks(M), 256, 0, C.st>>>(hp, C.tokens, ev, gh, ge, cv, M, D.T, d / 8, D.V, k,
                                                                  D.eps);
@@ -955,7 +989,7 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
     mtp::prof_begin(MTP_KC_PROJ_GEMM, C.st);
     TRY(gemm<T>(C, c, 2 * d, proj, 1, d, 2 * d, d, u, d, mtp::EPI_STORE));
     mtp::prof_end(MTP_KC_PROJ_GEMM, C.st);
-    launch_rmsnorm<T>(C, u, wt(C.W.attn_norm), x);
+    launch_rmsnorm<T>(C, u, wt(C.W.attn_norm), x, nullptr, 0, true);
     const T* wqkv[3] = {wt(C.W.wq), wt(C.W.wk), wt(C.W.wv)};
     mtp::prof_begin(MTP_KC_QKV_GEMM, C.st);
     TRY(gemm<T>(C, x, d, wqkv, 3, d, d, 3 * d, qkv, 3 * d, D.rope_base > 0.f ? mtp::EPI_ROPE : mtp::EPI_STORE));
@@ -969,7 +1003,7 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
     mtp::prof_begin(MTP_KC_O_GEMM, C.st);
     TRY(gemm<T>(C, o, d, wo, 1, d, d, d, a, d, mtp::EPI_RESID, u, d));
     mtp::prof_end(MTP_KC_O_GEMM, C.st);
-    launch_rmsnorm<T>(C, a, wt(C.W.ffn_norm), y);
+    launch_rmsnorm<T>(C, a, wt(C.W.ffn_norm), y, nullptr, 0, true);
     const T* wg[1] = {wt(C.W.w_gate)};
     mtp::prof_begin(MTP_KC_GATE_UP_GEMM, C.st);
     TRY(gemm<T>(C, y, d, wg, 1, D.ffn, d, D.ffn, g, D.ffn, mtp::EPI_SWIGLU, nullptr, 0, wt(C.W.w_up)));

@@ -300,6 +300,7 @@ struct Args {
   const float* lse;
   const float* ce_scale;
   int ce_offset;
+  int trigger;  // release dependents when the last tile starts
   int b_early;  // B is read-only for the stream's earlier kernels: prefetch it before pdl_wait
 };
 
@@ -643,6 +644,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       unit_tile(t, tm, tn);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
+      if (P.trigger && u + u_step >= ntiles) pdl_trigger();  // this CTA's last tile
       // residual: the warp's 32 rows of every 64-column piece of the tile are loaded by TMA into
       // its boxes while the tile's MMAs run, once the previous tile's stores have read them
       if constexpr (EPI == EPI_RESID) {
@@ -936,6 +938,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       __syncwarp();
     }
   }
+  if (P.trigger && warp < 2) {  // the producer and MMA warps, once their elected lane is done
+    __syncwarp();
+    pdl_trigger();
+  }
 
   __syncthreads();
   if constexpr (PAIR) {
@@ -1048,6 +1054,7 @@ mtp_status launch(const GemmDesc& g, cudaStream_t stream) {
   a.ce_scale = g.ce_scale;
   a.ce_offset = g.ce_offset;
   a.b_early = g.b_early ? 1 : 0;
+  a.trigger = g.trigger_early ? 1 : 0;
   if constexpr (PAIR) {  // clusters of two CTAs, one pair per two SMs
     const int units = ((a.tiles_m + 1) / 2) * a.tiles_n * a.splits;
     const int pairs = units < num_sms() / 2 ? units : num_sms() / 2;

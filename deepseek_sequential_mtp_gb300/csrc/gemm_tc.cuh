@@ -54,6 +54,9 @@ struct GemmDesc {
   // (an L2 prefetch stays coherent with writes that follow it, so this is safe for any B; it
   // pays where B is not the previous kernel's output, e.g. weights)
   bool b_early = false;
+  // release the stream's next kernel (a programmatic dependent that waits with pdl_wait)
+  // when each CTA starts its last tile, so that its launch and setup overlap this one's tail
+  bool trigger_early = false;
   __nv_bfloat16* out = nullptr;
   int ldo = 0;
   const __nv_bfloat16* resid = nullptr;
