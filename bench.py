@@ -460,20 +460,20 @@ def run_ours(args):
     torch.cuda.synchronize()
     lib.check_errors()
 
-    # only the dominant kernel's event timer is armed in the timed loop: an event record between two
-    # kernels costs ~2 us of stream time and stops the next launch from overlapping its predecessor
+    # only the dominant kernel's event timer is armed in the timed loop, and only in a few evenly
+    # spaced steps: an event record between two kernels costs ~2 us of stream time and stops the
+    # next launch from starting while its predecessor drains (programmatic dependent launch)
     launches_per_step = (("head_ce_gemm", cfg.D + 1), ("gate_up_gemm", cfg.D), ("down_gemm", cfg.D),
                          ("qkv_gemm", cfg.D), ("o_gemm", cfg.D), ("proj_gemm", cfg.D), ("attention", cfg.D),
                          ("spec_verify", 1), ("prologue", cfg.D))
-    timers = {"head_ce_gemm": lib.KernelTimer("head_ce_gemm", (cfg.D + 1) * K)}
+    n_sampled = min(K, 4)
+    sampled = {(j * K) // n_sampled: lib.KernelTimer("head_ce_gemm", cfg.D + 1) for j in range(n_sampled)}
     torch.cuda.synchronize()
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    for t in timers.values():
-        t.arm()
     visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
     clocks = ClockSampler(visible[local_rank] if len(visible) > local_rank and visible[local_rank] else str(local_rank))
     clocks.start()
@@ -481,9 +481,13 @@ def run_ours(args):
     t_wall0 = time.perf_counter()
     for i in range(K):
         flush()
+        if i in sampled:
+            sampled[i].arm()
         ev0[i].record()
         step(W + i)
         ev1[i].record()
+        if i in sampled:
+            lib.KernelTimer.disarm_all()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -502,7 +506,7 @@ def run_ours(args):
     tokens_per_step = sum(cfg.B * (cfg.T - k) for k in range(1, cfg.D + 1))
     value = world * tokens_per_step / (step_ms_max / 1e3)
 
-    head_ms = timers["head_ce_gemm"].durations_ms()  # measured inside the timed region
+    head_ms = [x for t in sampled.values() for x in t.durations_ms()]  # inside the timed region
 
     # per-kernel breakdown: a separate pass of KB steps with every kernel class's timer armed
     btimers = {name: lib.KernelTimer(name, n * KB) for name, n in launches_per_step}
@@ -523,12 +527,12 @@ def run_ours(args):
     kern = {name: t.durations_ms() for name, t in btimers.items()}
     kern["head_ce_gemm"] = head_ms
     kern_steps = {name: KB for name in kern}
-    kern_steps["head_ce_gemm"] = K
+    kern_steps["head_ce_gemm"] = n_sampled
     counts = out["sums_counts"][1::2].cpu().numpy()  # supervised rows per term (same every step)
     peaks, peak_src = load_peaks()
     # algorithmic FLOPs of the head GEMM: 2 d V per supervised row, for main + each depth
     head_flops_step = 2.0 * cfg.d * cfg.V * float(counts.sum())
-    head_ms_step = sum(head_ms) / K
+    head_ms_step = sum(head_ms) / n_sampled
     head_launch_flops = head_flops_step / (cfg.D + 1)
     head_launch_ms = head_ms_step / (cfg.D + 1)
     achieved = head_launch_flops / (head_launch_ms / 1e3) / 1e12
