@@ -50,28 +50,74 @@ using mtp::load_f32;
 // ---------------------------------------------------------------------------
 constexpr int kScanThreads = 1024;
 
-__device__ int block_scan_max(int v, int* sh) {  // inclusive max-scan over threadIdx order
+// Inclusive max-scan over threadIdx order (blockDim a multiple of 32, at most 1024): within
+// each warp by shuffles, then over the warp totals; the result is also left in sh[threadIdx.x].
+__device__ int block_scan_max(int v, int* sh) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v = max(v, n);
+  }
+  if (lane == 31) sh[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    int t = lane < static_cast<int>(blockDim.x >> 5) ? sh[lane] : INT_MIN;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t = max(t, n);
+    }
+    sh[lane] = t;
+  }
+  __syncthreads();
+  if (w > 0) v = max(v, sh[w - 1]);
+  __syncthreads();
   sh[threadIdx.x] = v;
   __syncthreads();
-  for (int o = 1; o < blockDim.x; o <<= 1) {
-    const int n = threadIdx.x >= o ? sh[threadIdx.x - o] : INT_MIN;
-    __syncthreads();
-    v = max(v, n);
-    sh[threadIdx.x] = v;
-    __syncthreads();
-  }
   return v;
 }
 
+// (cos, sin) table entry i = p * half + j of the angle p * base^(-2j/hd) (rope_table_kernel)
+__device__ __forceinline__ float2 rope_entry(int p, double inv_freq) {
+  const double ang = static_cast<double>(p) * inv_freq;
+  const double two_pi = 6.283185307179586;
+  const double red = ang - rint(ang / two_pi) * two_pi;
+  float s, c;
+  sincosf(static_cast<float>(red), &s, &c);
+  return make_float2(c, s);
+}
+
+struct SetupArgs {
+  double* sums = nullptr;  // the loss (sum, count) pairs to zero (null: none)
+  int n_sums = 0;
+  float2* rope = nullptr;  // [T, half]
+  int half = 0, hd = 0;
+  double base = 0.0;       // 0: RoPE off, the table is zeroed
+};
+
+// The call's setup in one launch.  Blocks [0, B) find the segment bounds of packed row b
+// (block 0 also zeroes the loss sums and the attention work counters); the blocks after them
+// fill the RoPE table, each computing its frequencies base^(-2j/hd) once.
 __global__ void __launch_bounds__(kScanThreads)
 segments_kernel(const int32_t* __restrict__ seg, const int32_t* __restrict__ tokens, int T, int V,
                 int32_t* __restrict__ seg_start, int32_t* __restrict__ seg_end, int* __restrict__ work_ctrs,
-                int n_ctrs) {
+                int n_ctrs, int B, SetupArgs A) {
   __shared__ int sh[kScanThreads];
+  __shared__ double inv_freq[64];
   const int b = blockIdx.x;
-  // the attention launches of this call claim their work items from these counters
-  if (b == 0)
+  if (b >= B) {  // RoPE table
+    if (A.base > 0.0 && threadIdx.x < A.half) inv_freq[threadIdx.x] = exp2(-2.0 * threadIdx.x / A.hd * log2(A.base));
+    __syncthreads();
+    const int i = (b - B) * blockDim.x + threadIdx.x;
+    if (i < T * A.half) A.rope[i] = A.base > 0.0 ? rope_entry(i / A.half, inv_freq[i % A.half]) : make_float2(0.f, 0.f);
+    return;
+  }
+  if (b == 0) {
+    // the attention launches of this call claim their work items from these counters
     for (int i = threadIdx.x; i < n_ctrs; i += blockDim.x) work_ctrs[i] = 0;
+    for (int i = threadIdx.x; i < A.n_sums; i += blockDim.x) A.sums[i] = 0.0;
+  }
   const int32_t* s = seg + static_cast<size_t>(b) * T;
   const int32_t* x = tokens + static_cast<size_t>(b) * T;
   int32_t* out_start = seg_start + static_cast<size_t>(b) * T;
@@ -264,23 +310,6 @@ __global__ void rmsnorm_bf16_kernel(const uint4* __restrict__ x, const uint4* __
     const bool ok = seg[m] != -1 && t + k + 1 < seg_end[m];
     labels[m] = ok ? clamp_token(tokens[m + k + 1], V) : -1;
   }
-}
-
-// (cos, sin) of the angle p * base^(-2j/hd).  The angle is formed and
-// reduced modulo 2*pi in double (a handful of FP64 instructions), then the
-// fp32 sine and cosine of the reduced angle are taken.
-__global__ void rope_table_kernel(float2* __restrict__ tab, int T, int half, int hd, double base) {
-  mtp::pdl_trigger();  // a GEMM that follows may start its setup
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= T * half) return;
-  const int p = i / half, j = i % half;
-  const double inv_freq = exp2(-2.0 * j / hd * log2(base));
-  const double ang = static_cast<double>(p) * inv_freq;
-  const double two_pi = 6.283185307179586;
-  const double red = ang - rint(ang / two_pi) * two_pi;
-  float s, c;
-  sincosf(static_cast<float>(red), &s, &c);
-  tab[i] = make_float2(c, s);
 }
 
 // labels of term k (0 = main): x_{t+k+1} where t..t+k+1 lie in t's segment, else -1
@@ -520,11 +549,6 @@ __global__ void ce_reduce_reg_kernel(int M, int nvt, const float2* __restrict__ 
   }
 }
 
-__global__ void zero_f64_kernel(double* p, int n) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) p[i] = 0.0;
-}
-
 // losses = [L, L_main, L^(1..D)] from (sum, count) pairs
 // Per-depth weights of the loss assembly (uniform lambda/D unless given).
 constexpr int kMaxDepthWeights = 32;
@@ -538,6 +562,7 @@ struct DepthWeights {
 // include/mtp.h): sums_counts holds (S_k, N_k), k = 0 main, 1..D depths.
 __global__ void loss_assemble_kernel(const double* __restrict__ sc, float* __restrict__ losses, int D, double n_pos,
                                      DepthWeights W, int den, int with_main) {
+  mtp::pdl_wait();
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   auto weight = [&](int k) -> double {
     return W.uniform ? static_cast<double>(W.lambda) / D : static_cast<double>(W.w[k - 1]);
@@ -594,6 +619,7 @@ mtp_status supported(const mtp_dims& D) {
     if (D.head_dim > 128 || static_cast<size_t>(D.T) * 16 > 200 * 1024) return MTP_ERR_UNSUPPORTED;
   }
   if (static_cast<long long>(D.B) * D.T > (1ll << 30)) return MTP_ERR_UNSUPPORTED;
+  if (static_cast<long long>(D.T) * (D.head_dim / 2) > (1ll << 30)) return MTP_ERR_UNSUPPORTED;  // RoPE table
   return MTP_OK;
 }
 
@@ -911,21 +937,22 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
   const mtp_dims& D = C.D;
   const int M = C.M, d = D.d;
   const size_t Md = static_cast<size_t>(M) * d;
-  segments_kernel<<<D.B, kScanThreads, 0, C.st>>>(C.seg, C.tokens, D.T, D.V, C.buf<int32_t>(C.L.seg_start),
-                                                  C.buf<int32_t>(C.L.seg_end), C.buf<int>(C.L.work_ctrs), D.D);
-  mtp::note_launch();
   const int half = D.head_dim / 2;
-  if (D.rope_base > 0.f) {
-    rope_table_kernel<<<(D.T * half + 255) / 256, 256, 0, C.st>>>(C.buf<float2>(C.L.rope), D.T, half, D.head_dim,
-                                                                  static_cast<double>(D.rope_base));
-    mtp::note_launch();
-  } else {
-    cudaMemsetAsync(C.buf<float2>(C.L.rope), 0, static_cast<size_t>(D.T) * half * sizeof(float2), C.st);
-  }
+  SetupArgs sa;
+  sa.sums = with_loss ? sums_counts : nullptr;
+  sa.n_sums = with_loss ? 2 * (D.D + 1) : 0;
+  sa.rope = C.buf<float2>(C.L.rope);
+  sa.half = half;
+  sa.hd = D.head_dim;
+  sa.base = D.rope_base > 0.f ? static_cast<double>(D.rope_base) : 0.0;
+  const int rope_blocks = (D.T * half + kScanThreads - 1) / kScanThreads;
+  segments_kernel<<<D.B + rope_blocks, kScanThreads, 0, C.st>>>(C.seg, C.tokens, D.T, D.V,
+                                                                C.buf<int32_t>(C.L.seg_start),
+                                                                C.buf<int32_t>(C.L.seg_end),
+                                                                C.buf<int>(C.L.work_ctrs), D.D, D.B, sa);
+  mtp::note_launch();
   MTP_LAUNCH_CHECK();
   if (with_loss) {
-    zero_f64_kernel<<<1, 64, 0, C.st>>>(sums_counts, 2 * (D.D + 1));
-    mtp::note_launch();
     if (with_main) TRY(head_ce<T>(C, h0, 0, row_loss, sums_counts));
     else if (row_loss)
       cudaMemsetAsync(row_loss, 0xff, static_cast<size_t>(M) * sizeof(float), C.st);  // NaN
@@ -1020,7 +1047,9 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
     DepthWeights W{};
     W.lambda = lambda;
     W.uniform = 1;
-    loss_assemble_kernel<<<1, 32, 0, C.st>>>(sums_counts, losses, D.D, static_cast<double>(M), W, den, with_main);
+    // a programmatic dependent of the last head's CE reduction
+    mtp::launch_pdl(loss_assemble_kernel, dim3(1), dim3(32), 0, C.st, sums_counts, losses, D.D, static_cast<double>(M),
+                    W, den, with_main);
     mtp::note_launch();
     MTP_LAUNCH_CHECK();
   }
