@@ -92,6 +92,31 @@ def test_full_parity_small(name, den):
     np.testing.assert_allclose(g["sums_counts"][0::2], r["sums"], rtol=ltol)
 
 
+@pytest.mark.parametrize("name", ["small_bf16_D2", "small_f32_D3"])
+def test_rope_off_parity(name):
+    # rope_base = 0 disables the rotation (the QKV GEMM stores plainly, the table is zero)
+    cfg = synth.CHAIN_CONFIGS[name].with_(name=name + "_norope", rope_base=0.0)
+    inp = synth.make_chain_inputs(cfg, seed=13)
+    g = run_gpu(cfg, to_dev(inp))
+    r = run_oracle(cfg, inp, lam=cfg.lam, den="fixed")
+    assert np.array_equal(g["sums_counts"][1::2], r["counts"].astype(np.float64))
+    compare_rows(cfg, g, r)
+
+
+@pytest.mark.parametrize("name", ["small_bf16_D2", "small_bf16_hd128"])
+def test_no_main_term_parity(name):
+    # without the main term the first depth's prologue follows the row-loss fill directly
+    cfg = synth.CHAIN_CONFIGS[name]
+    inp = synth.make_chain_inputs(cfg, seed=17)
+    g = run_gpu(cfg, to_dev(inp), den="masked_mean", with_main=False)
+    r = run_oracle(cfg, inp, lam=cfg.lam, den="masked_mean", with_main=False)
+    assert np.all(np.isnan(g["row_loss"][0]))
+    assert np.array_equal(g["sums_counts"][3::2], r["counts"][1:].astype(np.float64))
+    compare_rows(cfg, {"h": g["h"], "row_loss": g["row_loss"][1:]}, {"h": r["h"], "row_loss": r["row_loss"][1:]})
+    _, _, ltol = tolerances(cfg)
+    np.testing.assert_allclose(g["losses"][2:], r["loss_mtp"], rtol=ltol * 5, atol=1e-7)
+
+
 def test_tiny_config_counts_and_no_main():
     cfg = synth.TINY_F32
     inp = synth.make_chain_inputs(cfg, seed=3)
