@@ -24,6 +24,7 @@
 // shapes) runs the same steps on SIMT kernels in fp32.
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "gemm_tc.cuh"
 
@@ -673,6 +674,11 @@ struct Ctx {
   float* lse_save = nullptr;  // training: per-term log-sum-exp of every supervised row, [(D+1), M]
   uint8_t* save = nullptr;     // training: depth i's activations at save + i * so.bytes
   SaveOff so{};
+  // loss calls: a second stream for the row kernels off the chain of blocks (the next depth's
+  // prologue, each term's CE reduction) and the events that order it against st (kEv*)
+  cudaStream_t side = nullptr;
+  cudaEvent_t* ev = nullptr;
+  mutable bool red_pending = false;  // a CE reduction was enqueued on `side` (kEvRed recorded)
   template <typename T>
   T* buf(size_t off) const {
     return reinterpret_cast<T*>(ws + off);
@@ -681,15 +687,48 @@ struct Ctx {
 
 inline int warp_blocks(int rows) { return (rows + 7) / 8; }  // 8 warps (256 threads) per block
 
+// Events of a loss call's second stream: the next prologue done, the head's norm enqueued (h^k
+// ready), a head GEMM done, a CE reduction done.
+enum { kEvPro = 0, kEvH, kEvHead, kEvRed, kSideEvents };
+struct SideStream {
+  std::mutex mu;
+  cudaStream_t s = nullptr;
+  cudaEvent_t ev[kSideEvents] = {};
+  bool ready = false;
+};
+SideStream g_side[mtp::kMaxDevices];
+
+// The current device's second stream, locked into `lock` for the call that enqueues on it
+// (concurrent calls on one device take turns); null if it cannot be created, in which case
+// the call runs on its own stream alone.
+SideStream* side_stream(std::unique_lock<std::mutex>& lock) {
+  const int dev = mtp::current_device();
+  if (dev < 0 || dev >= mtp::kMaxDevices) return nullptr;
+  SideStream& S = g_side[dev];
+  lock = std::unique_lock<std::mutex>(S.mu);
+  if (!S.ready) {
+    bool ok = cudaStreamCreateWithFlags(&S.s, cudaStreamNonBlocking) == cudaSuccess;
+    for (int i = 0; ok && i < kSideEvents; ++i) ok = cudaEventCreateWithFlags(&S.ev[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    S.ready = true;
+  }
+  return &S;
+}
+
+// pdl = false: the stream's previous operation is not a kernel (e.g. an event wait)
 template <typename T>
 mtp_status gemm(const Ctx& C, const T* A, int lda, const T* const* Bs, int nseg, int seg_rows, int K, int N,
-                T* out, int ldo, int epi, const T* resid = nullptr, int ldr = 0, const T* B2 = nullptr);
+                T* out, int ldo, int epi, const T* resid = nullptr, int ldr = 0, const T* B2 = nullptr,
+                bool pdl = true);
 
 // bf16: the tcgen05 core
 template <>
 mtp_status gemm<__nv_bfloat16>(const Ctx& C, const __nv_bfloat16* A, int lda, const __nv_bfloat16* const* Bs,
                                int nseg, int seg_rows, int K, int N, __nv_bfloat16* out, int ldo, int epi,
-                               const __nv_bfloat16* resid, int ldr, const __nv_bfloat16* B2) {
+                               const __nv_bfloat16* resid, int ldr, const __nv_bfloat16* B2, bool pdl) {
   mtp::GemmDesc g;
   g.M = C.M;
   g.N = N;
@@ -706,7 +745,7 @@ mtp_status gemm<__nv_bfloat16>(const Ctx& C, const __nv_bfloat16* A, int lda, co
   g.ldo = ldo;
   g.resid = resid;
   g.ldr = ldr;
-  g.pdl = true;  // every forward-chain GEMM follows one of this library's kernels
+  g.pdl = pdl;  // every forward-chain GEMM follows one of this library's kernels unless told otherwise
   g.b_early = true;  // B is a weight matrix
   g.trigger_early = true;  // the next kernel of the chain is a programmatic dependent
   if (epi == mtp::EPI_ROPE) {
@@ -722,7 +761,7 @@ mtp_status gemm<__nv_bfloat16>(const Ctx& C, const __nv_bfloat16* A, int lda, co
 // f32: SIMT tiles; RoPE and SwiGLU as separate elementwise kernels
 template <>
 mtp_status gemm<float>(const Ctx& C, const float* A, int lda, const float* const* Bs, int nseg, int seg_rows, int K,
-                       int N, float* out, int ldo, int epi, const float* resid, int ldr, const float* B2) {
+                       int N, float* out, int ldo, int epi, const float* resid, int ldr, const float* B2, bool) {
   auto run = [&](const float* B, float* o, int n, int ldo_, const float* R, int ldr_) {
     const dim3 grid((n + 63) / 64, (C.M + 63) / 64);
     gemm_f32_kernel<<<grid, 256, 0, C.st>>>(A, lda, B, K, o, ldo_, R, ldr_, C.M, n, K);
@@ -871,17 +910,37 @@ void launch_rmsnorm(const Ctx& C, const T* x, const T* g, T* y, int32_t* labels 
   }
 }
 
-// head + CE for term `k` (0 = main) on hidden state h
 template <typename T>
-mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double* sum_count) {
+void launch_prologue(const Ctx& C, const T* h_prev, int k, T* c, cudaStream_t st, bool pdl);
+
+// head + CE for term `k` (0 = main) on hidden state h.  With the second stream and next_c, the
+// prologue of depth k + 1 (which reads the same h) runs there beside this head's GEMM.
+template <typename T>
+mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double* sum_count, T* next_c = nullptr) {
   const mtp_dims& D = C.D;
   T* x = C.buf<T>(C.L.x);
   int32_t* labels = C.buf<int32_t>(C.L.labels);
   float2* part = C.buf<float2>(C.L.ce_part);
   float* zt = C.buf<float>(C.L.zt);
-  // its predecessor is a kernel: the previous depth's down projection or the zeroing of the sums
-  launch_rmsnorm<T>(C, h, static_cast<const T*>(C.W.out_norm), x, labels, k, true);
+  // its predecessor is a kernel (the previous depth's down projection or the setup kernel) unless
+  // the previous term's CE reduction, on the second stream, must first finish reading the labels,
+  // the partials and the target logits that this term overwrites
+  bool norm_pdl = true;
+  if (C.side && C.red_pending) {
+    cudaStreamWaitEvent(C.st, C.ev[kEvRed], 0);
+    norm_pdl = false;
+  }
+  launch_rmsnorm<T>(C, h, static_cast<const T*>(C.W.out_norm), x, labels, k, norm_pdl);
   MTP_LAUNCH_CHECK();
+  if (C.side && next_c) {  // after the norm, so that it shares the SMs with the head GEMM rather than the norm
+    cudaEventRecord(C.ev[kEvH], C.st);
+    cudaStreamWaitEvent(C.side, C.ev[kEvH], 0);
+    mtp::prof_begin(MTP_KC_PROLOGUE, C.side);
+    launch_prologue<T>(C, h, k + 1, next_c, C.side, false);
+    mtp::prof_end(MTP_KC_PROLOGUE, C.side);
+    cudaEventRecord(C.ev[kEvPro], C.side);
+    MTP_LAUNCH_CHECK();
+  }
   if constexpr (sizeof(T) == 2) {
     mtp::GemmDesc g;
     g.M = C.M;
@@ -912,10 +971,18 @@ mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double
     const int grid = std::min((C.M + 7) / 8, 256);
     float* lse_out = C.lse_save ? C.lse_save + static_cast<size_t>(k) * C.M : nullptr;
     const int nvt = C.L.nvt;
+    // on the second stream after the head (nothing on the chain of blocks reads its results), or
     // a programmatic dependent of the head GEMM (bf16) or of the f32 head kernel
+    if (C.side) {
+      cudaEventRecord(C.ev[kEvHead], C.st);
+      cudaStreamWaitEvent(C.side, C.ev[kEvHead], 0);
+    }
     auto go = [&](auto kern) {
-      mtp::launch_pdl(kern, dim3(grid), dim3(256), 0, C.st, C.M, nvt, part, zt, labels, row_loss_term, sum_count,
-                      lse_out);
+      if (C.side)
+        kern<<<grid, 256, 0, C.side>>>(C.M, nvt, part, zt, labels, row_loss_term, sum_count, lse_out);
+      else
+        mtp::launch_pdl(kern, dim3(grid), dim3(256), 0, C.st, C.M, nvt, part, zt, labels, row_loss_term, sum_count,
+                        lse_out);
     };
     if (nvt <= 128)
       go(ce_reduce_reg_kernel<4, 4>);
@@ -925,10 +992,50 @@ mtp_status head_ce(const Ctx& C, const T* h, int k, float* row_loss_term, double
       go(ce_reduce_reg_kernel<16, 1>);
     else
       go(ce_reduce_kernel);
+    if (C.side) {
+      cudaEventRecord(C.ev[kEvRed], C.side);
+      C.red_pending = true;
+    }
   }
   mtp::note_launch();
   MTP_LAUNCH_CHECK();
   return MTP_OK;
+}
+
+// prologue input c of depth k from h^(k-1): [RMSNorm_hnorm(h); RMSNorm_enorm(E[x_{t+k}])] on `st`
+// (pdl: the stream's previous operation is a kernel)
+template <typename T>
+void launch_prologue(const Ctx& C, const T* h_prev, int k, T* c, cudaStream_t st, bool pdl) {
+  const mtp_dims& D = C.D;
+  const int M = C.M, d = D.d, i = k - 1;
+  if constexpr (sizeof(T) == 2) {
+    const uint4* hp = reinterpret_cast<const uint4*>(h_prev);
+    const uint4* ev = static_cast<const uint4*>(C.W.embed);
+    const uint4* gh = static_cast<const uint4*>(C.W.hnorm[i]);
+    const uint4* ge = static_cast<const uint4*>(C.W.enorm[i]);
+    uint4* cv = reinterpret_cast<uint4*>(c);
+    auto go = [&](auto kern) {
+      if (pdl)
+        mtp::launch_pdl(kern, dim3(warp_blocks(M)), dim3(256), 0, st, hp, C.tokens, ev, gh, ge, cv, M, D.T, D.V, k,
+                        D.eps);
+      else
+        kern<<<warp_blocks(M), 256, 0, st>>>(hp, C.tokens, ev, gh, ge, cv, M, D.T, D.V, k, D.eps);
+    };
+    switch (d) {
+      case 256: go(prologue_bf16_reg_kernel<1>); break;
+      case 512: go(prologue_bf16_reg_kernel<2>); break;
+      case 1024: go(prologue_bf16_reg_kernel<4>); break;
+      default:
+        prologue_bf16_kernel<<<warp_blocks(M), 256, 0, st>>>(hp, C.tokens, ev, gh, ge, cv, M, D.T, d / 8, D.V, k,
+                                                             D.eps);
+    }
+  } else {
+    prologue_kernel<T><<<warp_blocks(M), 256, 0, st>>>(h_prev, C.tokens, static_cast<const T*>(C.W.embed),
+                                                       static_cast<const T*>(C.W.hnorm[i]),
+                                                       static_cast<const T*>(C.W.enorm[i]), c, M, D.T, d, D.V, k,
+                                                       D.eps);
+  }
+  mtp::note_launch();
 }
 
 template <typename T>
@@ -937,6 +1044,13 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
   const mtp_dims& D = C.D;
   const int M = C.M, d = D.d;
   const size_t Md = static_cast<size_t>(M) * d;
+  // loss calls with a second stream: depth k's prologue runs there beside the head GEMM of term
+  // k - 1 (it needs only h^(k-1) and the tokens), and each term's CE reduction after its head
+  const bool split = C.side != nullptr && with_loss;
+  auto c_buf = [&](int k) -> T* {
+    return C.save ? reinterpret_cast<T*>(C.save + static_cast<size_t>(k - 1) * C.so.bytes + C.so.c)
+                  : C.buf<T>(C.L.c);
+  };
   const int half = D.head_dim / 2;
   SetupArgs sa;
   sa.sums = with_loss ? sums_counts : nullptr;
@@ -953,7 +1067,7 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
   mtp::note_launch();
   MTP_LAUNCH_CHECK();
   if (with_loss) {
-    if (with_main) TRY(head_ce<T>(C, h0, 0, row_loss, sums_counts));
+    if (with_main) TRY(head_ce<T>(C, h0, 0, row_loss, sums_counts, split ? c_buf(1) : nullptr));
     else if (row_loss)
       cudaMemsetAsync(row_loss, 0xff, static_cast<size_t>(M) * sizeof(float), C.st);  // NaN
   }
@@ -980,41 +1094,21 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
     }
     T* h_k = h_out ? h_out + static_cast<size_t>(i) * Md : C.buf<T>((k & 1) ? C.L.h1buf : C.L.h0buf);
     auto wt = [&](const void* const* arr) { return static_cast<const T*>(arr[i]); };
-    mtp::prof_begin(MTP_KC_PROLOGUE, C.st);
-    if constexpr (sizeof(T) == 2) {
-      const uint4* hp = reinterpret_cast<const uint4*>(h_prev);
-      const uint4* ev = static_cast<const uint4*>(C.W.embed);
-      const uint4* gh = static_cast<const uint4*>(C.W.hnorm[i]);
-      const uint4* ge = static_cast<const uint4*>(C.W.enorm[i]);
-      uint4* cv = reinterpret_cast<uint4*>(c);
+    if (split && (k > 1 || with_main)) {
+      cudaStreamWaitEvent(C.st, C.ev[kEvPro], 0);  // this depth's c, from the second stream
+    } else {
       // from the second depth on the previous operation is a kernel (the head's CE reduction
       // or the down projection): launch as its programmatic dependent
-      const bool pdl = k > 1;
-      auto go = [&](auto kern) {
-        if (pdl)
-          mtp::launch_pdl(kern, dim3(warp_blocks(M)), dim3(256), 0, C.st, hp, C.tokens, ev, gh, ge, cv, M, D.T, D.V,
-                          k, D.eps);
-        else
-          kern<<<warp_blocks(M), 256, 0, C.st>>>(hp, C.tokens, ev, gh, ge, cv, M, D.T, D.V, k, D.eps);
-      };
-      switch (d) {
-        case 256: go(prologue_bf16_reg_kernel<1>); break;
-        case 512: go(prologue_bf16_reg_kernel<2>); break;
-        case 1024: go(prologue_bf16_reg_kernel<4>); break;
-        default:
-          prologue_bf16_kernel<<<warp_blocks(M), 256, 0, C.st>>>(hp, C.tokens, ev, gh, ge, cv, M, D.T, d / 8, D.V, k,
-                                                                 D.eps);
-      }
-    } else {
-      prologue_kernel<T><<<warp_blocks(M), 256, 0, C.st>>>(h_prev, C.tokens, static_cast<const T*>(C.W.embed),
-                                                           wt(C.W.hnorm), wt(C.W.enorm), c, M, D.T, d, D.V, k, D.eps);
+      mtp::prof_begin(MTP_KC_PROLOGUE, C.st);
+      // (the first depth's follows a kernel unless the main term's row losses were just filled)
+      launch_prologue<T>(C, h_prev, k, c, C.st, k > 1 || !(with_loss && !with_main && row_loss));
+      mtp::prof_end(MTP_KC_PROLOGUE, C.st);
     }
-    mtp::prof_end(MTP_KC_PROLOGUE, C.st);
-    mtp::note_launch();
     MTP_LAUNCH_CHECK();
     const T* proj[1] = {wt(C.W.eh_proj)};
     mtp::prof_begin(MTP_KC_PROJ_GEMM, C.st);
-    TRY(gemm<T>(C, c, 2 * d, proj, 1, d, 2 * d, d, u, d, mtp::EPI_STORE));
+    TRY(gemm<T>(C, c, 2 * d, proj, 1, d, 2 * d, d, u, d, mtp::EPI_STORE, nullptr, 0, nullptr,
+                !(split && (k > 1 || with_main))));
     mtp::prof_end(MTP_KC_PROJ_GEMM, C.st);
     launch_rmsnorm<T>(C, u, wt(C.W.attn_norm), x, nullptr, 0, true);
     const T* wqkv[3] = {wt(C.W.wq), wt(C.W.wk), wt(C.W.wv)};
@@ -1040,16 +1134,21 @@ mtp_status run_chain(const Ctx& C, const T* h0, T* h_out, bool with_loss, float 
     TRY(gemm<T>(C, g, D.ffn, wd, 1, d, D.ffn, d, h_k, d, mtp::EPI_RESID, a, d));
     mtp::prof_end(MTP_KC_DOWN_GEMM, C.st);
     if (with_loss)
-      TRY(head_ce<T>(C, h_k, k, row_loss ? row_loss + static_cast<size_t>(k) * M : nullptr, sums_counts + 2 * k));
+      TRY(head_ce<T>(C, h_k, k, row_loss ? row_loss + static_cast<size_t>(k) * M : nullptr, sums_counts + 2 * k,
+                     split && k < D.D ? c_buf(k + 1) : nullptr));
     h_prev = h_k;
   }
   if (with_loss) {
     DepthWeights W{};
     W.lambda = lambda;
     W.uniform = 1;
-    // a programmatic dependent of the last head's CE reduction
-    mtp::launch_pdl(loss_assemble_kernel, dim3(1), dim3(32), 0, C.st, sums_counts, losses, D.D, static_cast<double>(M),
-                    W, den, with_main);
+    if (split && C.red_pending) {  // every reduction on the second stream has finished
+      cudaStreamWaitEvent(C.st, C.ev[kEvRed], 0);
+      loss_assemble_kernel<<<1, 32, 0, C.st>>>(sums_counts, losses, D.D, static_cast<double>(M), W, den, with_main);
+    } else {  // a programmatic dependent of the last head's CE reduction
+      mtp::launch_pdl(loss_assemble_kernel, dim3(1), dim3(32), 0, C.st, sums_counts, losses, D.D,
+                      static_cast<double>(M), W, den, with_main);
+    }
     mtp::note_launch();
     MTP_LAUNCH_CHECK();
   }
@@ -1109,6 +1208,11 @@ extern "C" mtp_status mtp_chain_loss(const mtp_dims* dims, const mtp_weights* w,
   if (!valid_den(den)) return MTP_ERR_INVALID_ARG;
   if (h_out && !mtp::aligned16(h_out)) return MTP_ERR_ALIGNMENT;
   Ctx C{*dims, *w, tokens, seg, pos, static_cast<uint8_t*>(ws), make_layout(*dims), stream, dims->B * dims->T};
+  std::unique_lock<std::mutex> side_lock;
+  if (SideStream* S = side_stream(side_lock)) {
+    C.side = S->s;
+    C.ev = S->ev;
+  }
   if (dims->dtype == MTP_BF16)
     return run_chain<__nv_bfloat16>(C, static_cast<const __nv_bfloat16*>(h0), static_cast<__nv_bfloat16*>(h_out),
                                     true, lambda, den, with_main, sums_counts, losses, row_loss);
@@ -1792,6 +1896,11 @@ extern "C" mtp_status mtp_chain_loss_grad(const mtp_dims* dims, const mtp_weight
   const BwdLayout BL = make_bwd_layout(D, T.total, T.mp);
   if (ws_bytes < BL.total) return MTP_ERR_WORKSPACE;
   Ctx C{D, *w, tokens, seg, pos, static_cast<uint8_t*>(ws), make_layout(D), stream, D.B * D.T};
+  std::unique_lock<std::mutex> side_lock;
+  if (SideStream* S = side_stream(side_lock)) {
+    C.side = S->s;
+    C.ev = S->ev;
+  }
   C.lse_save = C.buf<float>(T.lse);
   C.save = C.buf<uint8_t>(T.save);
   C.so = make_save_off(D);
