@@ -6,31 +6,34 @@
 // truncation) generalised to gamma drafts by the left-to-right rule of the
 // speculative-decoding page.  Uniforms: Philox4x32-10 (Salmon et al., SC'11).
 //
-// Layout on the GPU: a cluster of 2 CTAs per request, one CTA per SM (544
-// threads: 16 consumer warps and one producer warp, 128 KB ring of four
-// 32 KB stages), so the 64
-// requests of a decode batch occupy 128 SMs in one wave.
+// Layout on the GPU: a cluster of 2 CTAs per request, one CTA per SM (416
+// threads: 12 consumer warps and one producer warp, 192 KB ring of six
+// 32 KB stages), so the 64 requests of a decode batch occupy 128 SMs in one
+// wave.
 //   phase A  warp 0 of every CTA: lane j evaluates draft position j (two
-//            scalar loads, one Philox block, one fp64 division); a ballot
-//            picks the first position that ends the round.  Both CTAs reach
-//            the same decision.
+//            scalar loads, one Philox block, an exact fp32 test of u*q < p);
+//            a ballot picks the first position that ends the round.  Both
+//            CTAs reach the same decision.
 //   phase B  CTA `rank` owns half of the chunks of the one row pair (or bonus
 //            row) the round samples from.  Its producer warp streams them
 //            with one-dimensional bulk copies into a ring of shared-memory
 //            stages (mbarrier-tracked); consumer warps form residuals in fp32
 //            and compensated (hi, lo) fp32 chunk sums.
-//   phase C  CTA 0 gathers the chunk sums through distributed shared memory,
-//            takes their fp64 prefix to find the chunk holding u' * mass, then
-//            rescans that one chunk in index order (staged in shared memory)
-//            to find the smallest index whose running sum exceeds it.
+//   phase C  CTA 0 gathers the chunk sums through distributed shared memory;
+//            its warp 0 takes their double-float prefix to find the chunk
+//            holding u' * mass, then rescans that one chunk in index order
+//            (staged, transposed, in the idle ring) to find the smallest index
+//            whose running sum exceeds it.  Nothing on phases A and C uses
+//            FP64: GB300 runs it at a small fraction of the FP32 rate, and a
+//            short chain of FP64 additions here cost microseconds.
 // The kernel is HBM-bound: it reads 2*V*4 bytes for a rejection, V*4 for a
 // bonus, plus 8*gamma bytes of scalars.
 // Ring invariant: a parity wait cannot tell phase u+1 from phase u-1, so no
 // waiter may reach a barrier more than one phase ahead of its last completed
-// phase.  With S chunks per stage, consumer warp w takes chunks w, w+16, ...,
-// i.e. stages w/S + (16/S) m; a ring of a multiple of 16/S stages keeps it on
-// the same slot(s), so it sees each slot's phases one after another (it
-// waited on use u-1 itself before waiting on use u).  The producer issues use
+// phase.  With S chunks per stage and W consumer warps, consumer warp w takes
+// chunks w, w+W, ..., i.e. stages w/S + (W/S) m; a ring of a multiple of W/S
+// stages keeps it on the same slot(s), so it sees each slot's phases one after
+// another (it waited on use u-1 itself before waiting on use u).  The producer issues use
 // u of a slot only after every consumer of use u-1 released it, and waits for
 // every copy it issued before it leaves.
 #include <cooperative_groups.h>
@@ -44,17 +47,20 @@ MTP_DEFINE_ERROR_WORD(mtp_take_errors_verify)
 
 namespace {
 
-constexpr int kThreads = 544;  // 16 consumer warps + 1 producer warp
+constexpr int kThreads = 416;  // 12 consumer warps + 1 producer warp
 constexpr int kCluster = 2;
-constexpr int kConsumerWarps = 16;
+constexpr int kConsumerWarps = 12;
 constexpr int kStageChunks = 4;  // chunks per ring stage: 16 KB bulk copies per row (a copy has a fixed cost)
-constexpr int kRing = 4;          // ring stages (4 x 4 KB x 2 rows each)
+constexpr int kRing = 6;          // ring stages of 4 chunks x 4 KB x 2 rows (192 KB: the deeper the ring, the more bytes in flight per SM)
 constexpr int kStageBytes = 2 * kStageChunks * 1024 * 4;
 constexpr int kRingBytes = kRing * kStageBytes;
 
 constexpr int kChunk = 1024;       // elements per chunk
 constexpr int kMaxChunks = 512;    // V <= 524288
 constexpr int kMaxGamma = 31;
+// phase C's transposed chunk (4 padding floats after every 32) reuses the ring's shared memory
+constexpr int kRescanBytes = (kChunk + kChunk / 32 * 4) * 4;
+static_assert(kRescanBytes <= kRingBytes, "the rescan staging must fit in the ring");
 // each consumer warp must revisit the same ring slot (see the ring invariant)
 static_assert(kRing % (kConsumerWarps / kStageChunks) == 0, "ring length must be a multiple of the warp stage stride");
 
@@ -74,8 +80,22 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
   return c;
 }
 
-__device__ __forceinline__ double uniform24(uint32_t w) {
-  return static_cast<double>(w >> 8) * (1.0 / 16777216.0);
+// u = (w >> 8) * 2^-24: a 24-bit integer times a power of two, exact in fp32
+__device__ __forceinline__ float uniform24(uint32_t w) {
+  return static_cast<float>(w >> 8) * (1.0f / 16777216.0f);
+}
+
+// u < min(1, p/q) for u in [0, 1) and q > 0 is u*q < p (when p >= q both hold
+// for every u < 1).  u has 24 significant bits, so u*q = hi + lo exactly with
+// hi = fl(u*q), lo = fma(u, q, -hi), and the test needs no division and no
+// FP64 (GB300 runs FP64 at a small fraction of the FP32 rate, and this
+// decision sits on the kernel's critical path).  It is the exact comparison;
+// a fp64 quotient rounded first can differ only for u within one rounding of
+// p/q.
+__device__ __forceinline__ bool accept_draft(float u, float pj, float qj) {
+  const float hi = u * qj;
+  const float lo = fmaf(u, qj, -hi);
+  return hi < pj || (hi == pj && lo < 0.0f);
 }
 
 __device__ __forceinline__ bool prob_ok(float v) { return isfinite(v) && v >= 0.0f; }
@@ -111,7 +131,51 @@ __device__ __forceinline__ void warp_two_sum(float& hi, float& lo) {
     lo = (lo + olo) + err;
   }
 }
-__device__ __forceinline__ double chunk_value(float2 v) { return (double)v.x + (double)v.y; }
+// Double-float values (hi + lo, |lo| <= ulp(hi)/2): the running sums of
+// phase C carry ~48 significant bits with FP32 instructions only.  Every
+// value here is a sum of non-negative weights.
+struct f2 {
+  float hi, lo;
+};
+// renormalise hi + lo with |hi| >= |lo| (fast two-sum)
+__device__ __forceinline__ f2 f2_norm(float hi, float lo) {
+  const float s = hi + lo;
+  return {s, lo - (s - hi)};
+}
+__device__ __forceinline__ f2 f2_add(f2 a, f2 b) {
+  float s, e;
+  two_sum(a.hi, b.hi, s, e);
+  return f2_norm(s, e + (a.lo + b.lo));
+}
+// a > b: the difference of the high parts is exact when they are within a
+// factor of two (Sterbenz) and has the right sign otherwise
+__device__ __forceinline__ bool f2_gt(f2 a, f2 b) { return (a.hi - b.hi) + (a.lo - b.lo) > 0.0f; }
+// u * m for a 24-bit u: the product of the high parts split exactly by FMA
+__device__ __forceinline__ f2 f2_scale(float u, f2 m) {
+  const float p = u * m.hi;
+  return f2_norm(p, fmaf(u, m.lo, fmaf(u, m.hi, -p)));
+}
+__device__ __forceinline__ f2 f2_shfl(f2 v, int src) {
+  return {__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+__device__ __forceinline__ f2 f2_shfl_up(f2 v, int d) {
+  return {__shfl_up_sync(0xffffffffu, v.hi, d), __shfl_up_sync(0xffffffffu, v.lo, d)};
+}
+__device__ __forceinline__ f2 warp_inclusive_scan_f2(f2 v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const f2 n = f2_shfl_up(v, o);
+    if (lane >= o) v = f2_add(v, n);
+  }
+  return v;
+}
+// exclusive prefix from an inclusive one (lane 0 gets zero)
+__device__ __forceinline__ f2 f2_exclusive(f2 incl) {
+  const f2 n = f2_shfl_up(incl, 1);
+  return (threadIdx.x & 31) ? n : f2{0.0f, 0.0f};
+}
+__device__ __forceinline__ f2 chunk_value(float2 v) { return f2_norm(v.x, v.y); }
 
 using mtp::bulk_load;
 using mtp::cluster_addr;
@@ -133,12 +197,11 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
   auto mbar_wait = [wait_limit](uint32_t bar, uint32_t parity) {
     return mtp::mbar_wait_bounded(bar, parity, wait_limit);
   };
-  extern __shared__ __align__(128) uint8_t ring[];   // kRing stages of p and q chunks
+  extern __shared__ __align__(128) uint8_t ring[];   // kRing stages of p and q chunks (kRescanBytes without the ring)
   __shared__ float2 s_all[kMaxChunks];  // CTA 0: (hi, lo) sum of every chunk of the request
-  __shared__ float s_w[kChunk];
   __shared__ __align__(8) uint64_t s_bars[2 * kRing];
-  __shared__ int s_jstar, s_event, s_bad, s_cstar, s_timeout;
-  __shared__ double s_u, s_before, s_target;
+  __shared__ int s_jstar, s_event, s_bad, s_timeout;
+  __shared__ float s_u;
   const uint32_t s_full_bar = smem_u32(s_bars), s_empty_bar = s_full_bar + 8u * kRing;
   auto ring_p = [&](int slot) { return smem_u32(ring + slot * kStageBytes); };
   auto ring_q = [&](int slot) { return smem_u32(ring + slot * kStageBytes + kStageChunks * kChunk * 4); };
@@ -167,8 +230,7 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
           ev = EV_INVALID_DRAFT;
         } else {
           const uint4 w = philox4x32_10(make_uint4((uint32_t)j, (uint32_t)r, off_lo, off_hi), key);
-          const double ratio = fmin(1.0, (double)pj / (double)qj);
-          if (!(uniform24(w.x) < ratio)) ev = EV_REJECT;
+          if (!accept_draft(uniform24(w.x), pj, qj)) ev = EV_REJECT;
           else if (j + 1 == budget || y == eos_id) ev = EV_STOP;
         }
       }
@@ -220,8 +282,8 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
   // the sum of the fp32 elements to ~2^-45 relative without FP64
   // instructions (GB300 issues FP64 warp instructions at a small fraction of
   // the FP32 rate).  With 16-byte-aligned rows a producer warp streams the
-  // rows with bulk copies into a ring of shared-memory stages (two chunks of
-  // p and of q per stage) and the eight consumer warps reduce them.
+  // rows with bulk copies into a ring of shared-memory stages (four chunks of
+  // p and of q per stage) and the consumer warps reduce them.
   const bool residual = (event == EV_REJECT);
   const float* prow = p + ((size_t)r * (gamma + 1) + jstar) * V;
   const float* qrow = residual ? q + ((size_t)r * gamma + jstar) * V : prow;
@@ -348,105 +410,130 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 
   // ---------------- phase C: locate u' * mass ----------------
-  if (warp == 0) {
-    int st = MTP_VERIFY_OK;
-    int cstar = -1;
-    double before = 0.0, target = 0.0;
-    if (s_timeout) {
-      st = MTP_VERIFY_DEVICE_TIMEOUT;
-    } else if (s_bad) {
-      st = MTP_VERIFY_INVALID_PROBS;
-    } else {
-      // lane l owns chunks [l*per, (l+1)*per)
-      const int per = (n_chunks + 31) / 32;
-      double own = 0.0;
-      for (int c = lane * per; c < min(n_chunks, (lane + 1) * per); ++c) own += chunk_value(s_all[c]);
-      const double incl = mtp::warp_inclusive_scan(own);
-      const double mass = __shfl_sync(0xffffffffu, incl, 31);
-      if (!(mass > 0.0)) {
-        st = MTP_VERIFY_ZERO_RESIDUAL;
-      } else {
-        target = s_u * mass;
-        // chunk holding the target (or the last chunk with mass if rounding overshoots)
-        const unsigned over = __ballot_sync(0xffffffffu, incl > target);
-        const unsigned has_mass = __ballot_sync(0xffffffffu, own > 0.0);
-        const int src = over ? __ffs(over) - 1 : 31 - __clz(has_mass);
-        if (lane == src) {
-          double run = incl - own;
-          int last_pos = -1;
-          double before_last = run;
-          for (int c = lane * per; c < min(n_chunks, (lane + 1) * per); ++c) {
-            const double cv = chunk_value(s_all[c]);
-            if (cv > 0.0) { last_pos = c; before_last = run; }
-            if (over && run + cv > target) { cstar = c; before = run; break; }
-            run += cv;
-          }
-          if (cstar < 0) { cstar = last_pos; before = before_last; }
-        }
-        cstar = __shfl_sync(0xffffffffu, cstar, src);
-        before = __shfl_sync(0xffffffffu, before, src);
-      }
-    }
-    if (lane == 0) {
-      s_event = st;
-      s_cstar = cstar;
-      s_before = before;
-      s_target = target;
-    }
-  }
-  __syncthreads();
-  if (s_event != MTP_VERIFY_OK) {
-    if (threadIdx.x == 0) {
-      accepted[r] = jstar; next_token[r] = -1; n_emit[r] = jstar; status[r] = s_event;
-    }
-    return;
-  }
-  // stage the chosen chunk's weights in shared memory
-  for (int i = threadIdx.x; i < kChunk; i += kThreads) {
-    const int e = s_cstar * kChunk + i;
-    s_w[i] = e < V ? weight_of(prow[e], residual ? qrow[e] : 0.0f, residual) : 0.0f;
-  }
-  __syncthreads();
+  // Warp 0 of CTA 0 alone, in double-float arithmetic (no FP64 on this
+  // latency-bound path: a chain of FP64 additions here took ~4.7 us on
+  // GB300): a prefix over the chunk sums finds the chunk holding the target,
+  // then that chunk is rescanned in index order (the row was just streamed,
+  // so its loads hit L2).
   if (warp != 0) return;
-  // lane l holds elements [32l, 32l+32) of the chunk: compensated fp32 lane
-  // sums, an fp64 scan over lanes, then a compensated scan of the chosen
-  // lane's 32 elements spread across the warp.
-  float lhi = 0.0f, llo = 0.0f;
-  for (int i = 0; i < 32; ++i) acc_add(lhi, llo, s_w[32 * lane + i]);
-  const double lane_sum = (double)lhi + (double)llo;
-  const double target = s_target;
-  const double lincl = mtp::warp_inclusive_scan(lane_sum) + s_before;
-  const unsigned lover = __ballot_sync(0xffffffffu, lincl > target);
-  const unsigned lpos = __ballot_sync(0xffffffffu, lane_sum > 0.0);
-  if (!lover && !lpos) {  // unreachable unless the two passes disagree on an empty chunk
+  int st = MTP_VERIFY_OK;
+  int cstar = -1;
+  f2 before = {0.0f, 0.0f}, target = {0.0f, 0.0f};
+  if (s_timeout) {
+    st = MTP_VERIFY_DEVICE_TIMEOUT;
+  } else if (s_bad) {
+    st = MTP_VERIFY_INVALID_PROBS;
+  } else {
+    // lane l owns chunks [l*per, (l+1)*per)
+    const int per = (n_chunks + 31) / 32;
+    const int c0 = lane * per, c1 = min(n_chunks, (lane + 1) * per);
+    f2 own = {0.0f, 0.0f};
+    for (int c = c0; c < c1; ++c) own = f2_add(own, chunk_value(s_all[c]));
+    const f2 incl = warp_inclusive_scan_f2(own);
+    const f2 excl = f2_exclusive(incl);
+    const f2 mass = f2_shfl(incl, 31);
+    if (!(mass.hi > 0.0f)) {
+      st = MTP_VERIFY_ZERO_RESIDUAL;
+    } else {
+      target = f2_scale(s_u, mass);
+      // chunk holding the target (or the last chunk with mass if rounding overshoots)
+      const unsigned over = __ballot_sync(0xffffffffu, f2_gt(incl, target));
+      const unsigned has_mass = __ballot_sync(0xffffffffu, own.hi > 0.0f);
+      const int src = over ? __ffs(over) - 1 : 31 - __clz(has_mass);
+      if (lane == src) {
+        f2 run = excl, before_last = excl;
+        int last_pos = -1;
+        for (int c = c0; c < c1; ++c) {
+          const f2 cv = chunk_value(s_all[c]);
+          const f2 next = f2_add(run, cv);
+          if (cv.hi > 0.0f) { last_pos = c; before_last = run; }
+          if (over && f2_gt(next, target)) { cstar = c; before = run; break; }
+          run = next;
+        }
+        if (cstar < 0) { cstar = last_pos; before = before_last; }
+      }
+      cstar = __shfl_sync(0xffffffffu, cstar, src);
+      before = f2_shfl(before, src);
+    }
+  }
+  if (st != MTP_VERIFY_OK) {
     if (lane == 0) {
-      accepted[r] = jstar; next_token[r] = -1; n_emit[r] = jstar; status[r] = MTP_VERIFY_ZERO_RESIDUAL;
+      accepted[r] = jstar; next_token[r] = -1; n_emit[r] = jstar; status[r] = st;
     }
     return;
   }
-  const int lsrc = lover ? __ffs(lover) - 1 : 31 - __clz(lpos);
-  // distance from the start of lane lsrc's elements to the target
-  const double delta = __shfl_sync(0xffffffffu, target - (lincl - lane_sum), lsrc);
-  const float wv = s_w[32 * lsrc + lane];
-  float phi = wv, plo = 0.0f;  // inclusive compensated scan of the 32 elements
+  // Rescan of chunk cstar: coalesced loads (lane l, group row k: elements
+  // 4(l + 32k) .. +3) into the ring, which is idle now (every copy into it
+  // has landed), transposed so that lane l holds elements 32l .. 32l + 31
+  // (4 padding floats after every 32 keep both 16-byte access patterns free
+  // of bank conflicts); one compensated lane sum and one warp scan pick the
+  // lane, a second warp scan over that lane's 32 elements picks the element.
+  const int cbase = cstar * kChunk;
+  float* s_w = reinterpret_cast<float*>(ring);
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float nhi = __shfl_up_sync(0xffffffffu, phi, o);
-    const float nlo = __shfl_up_sync(0xffffffffu, plo, o);
-    if (lane >= o) {
-      float sum, err;
-      two_sum(phi, nhi, sum, err);
-      phi = sum;
-      plo = (plo + nlo) + err;
+  for (int k = 0; k < 8; ++k) {
+    const int e = 4 * (lane + 32 * k);  // offset in the chunk
+    const int g = cbase + e;
+    float pv[4] = {0.f, 0.f, 0.f, 0.f}, qv[4] = {0.f, 0.f, 0.f, 0.f};
+    if (kVec4) {  // V % 4 == 0: a group is entirely inside the row or entirely past it
+      if (g < V) {
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(prow + g));
+        pv[0] = a.x; pv[1] = a.y; pv[2] = a.z; pv[3] = a.w;
+        if (residual) {
+          const float4 b = __ldcg(reinterpret_cast<const float4*>(qrow + g));
+          qv[0] = b.x; qv[1] = b.y; qv[2] = b.z; qv[3] = b.w;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (g + i < V) {
+          pv[i] = __ldcg(prow + g + i);
+          if (residual) qv[i] = __ldcg(qrow + g + i);
+        }
     }
+    float4 wv;
+    wv.x = (g + 0 < V) ? weight_of(pv[0], qv[0], residual) : 0.0f;
+    wv.y = (g + 1 < V) ? weight_of(pv[1], qv[1], residual) : 0.0f;
+    wv.z = (g + 2 < V) ? weight_of(pv[2], qv[2], residual) : 0.0f;
+    wv.w = (g + 3 < V) ? weight_of(pv[3], qv[3], residual) : 0.0f;
+    *reinterpret_cast<float4*>(s_w + e + (e >> 5) * 4) = wv;
   }
-  const unsigned eover = __ballot_sync(0xffffffffu, lover && ((double)phi + (double)plo) > delta);
-  const unsigned epos = __ballot_sync(0xffffffffu, wv > 0.0f);
+  __syncwarp();
+  float lhi = 0.0f, llo = 0.0f;
+  int lp = -1;  // last positive element of this lane
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float4 v = *reinterpret_cast<const float4*>(s_w + 36 * lane + 4 * k);
+    acc_add(lhi, llo, v.x);
+    acc_add(lhi, llo, v.y);
+    acc_add(lhi, llo, v.z);
+    acc_add(lhi, llo, v.w);
+    const int e = 32 * lane + 4 * k;
+    if (v.x > 0.0f) lp = e;
+    if (v.y > 0.0f) lp = e + 1;
+    if (v.z > 0.0f) lp = e + 2;
+    if (v.w > 0.0f) lp = e + 3;
+  }
+  const f2 lsum = f2_norm(lhi, llo);
+  const f2 lincl = f2_add(before, warp_inclusive_scan_f2(lsum));
+  const unsigned lover = __ballot_sync(0xffffffffu, f2_gt(lincl, target));
+  const unsigned lpos = __ballot_sync(0xffffffffu, lp >= 0);
+  int pick = -1, last_pos = -1;
+  if (lpos) last_pos = cbase + __shfl_sync(0xffffffffu, lp, 31 - __clz(lpos));
+  if (lover) {
+    const int src = __ffs(lover) - 1;
+    const f2 start = f2_shfl(f2_exclusive(lincl), src);  // running sum before lane src's elements
+    const f2 start0 = (src == 0) ? before : start;
+    const float wv = s_w[36 * src + lane];
+    const f2 cum = f2_add(start0, warp_inclusive_scan_f2(f2{wv, 0.0f}));
+    const unsigned eover = __ballot_sync(0xffffffffu, wv > 0.0f && f2_gt(cum, target));
+    const unsigned epos = __ballot_sync(0xffffffffu, wv > 0.0f);
+    if (eover) pick = cbase + 32 * src + __ffs(eover) - 1;
+    else if (epos) pick = cbase + 32 * src + 31 - __clz(epos);
+  }
+  if (pick < 0) pick = last_pos;
   if (lane == 0) {
-    const int base = s_cstar * kChunk + 32 * lsrc;
-    int pick = -1;
-    if (eover) pick = base + __ffs(eover) - 1;
-    else if (epos) pick = base + 31 - __clz(epos);
     accepted[r] = jstar;
     next_token[r] = pick;
     n_emit[r] = pick >= 0 ? jstar + 1 : jstar;
@@ -475,7 +562,7 @@ mtp_status verify_launch(int R, int gamma, int V, const float* p, const float* q
     spec_verify_kernel<true, kStarve><<<R * kCluster, kThreads, kRingBytes, stream>>>(
         gamma, V, p, q, draft, key, olo, ohi, eos, remaining, accepted, next_token, n_emit, status, wait_limit);
   else
-    spec_verify_kernel<false, false><<<R * kCluster, kThreads, 0, stream>>>(
+    spec_verify_kernel<false, false><<<R * kCluster, kThreads, kRescanBytes, stream>>>(
         gamma, V, p, q, draft, key, olo, ohi, eos, remaining, accepted, next_token, n_emit, status, wait_limit);
   mtp::note_launch();
   if (!kStarve) mtp::prof_end(MTP_KC_SPEC_VERIFY, stream);

@@ -227,7 +227,8 @@ mtp_status mtp_loss_assemble_weighted(int D, const double* sums_counts, double n
 /* Exact speculative verification of R requests with gamma drafts each
  * ([M7.6] §0x09 one-proposal selector, generalised to gamma by the
  * left-to-right rule of [SD]).  For j = 0..gamma-1: accept y_j iff
- * u_j < min(1, p_j[y_j] / q_j[y_j]) (fp64); the first rejection emits a
+ * u_j < min(1, p_j[y_j] / q_j[y_j]) (evaluated exactly as u_j q_j[y_j] <
+ * p_j[y_j]); the first rejection emits a
  * correction drawn from (p_j - q_j)+ / Σ(p_j - q_j)+ and ends the round; an
  * accepted y_j that equals eos, or that fills `remaining`, ends the round
  * with no further token; if all gamma are accepted a bonus is drawn from

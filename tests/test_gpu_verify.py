@@ -1,11 +1,14 @@
 """spec_verify on the GPU against the CPU oracle, through the C ABI.
 
 Bar: accepted length, emitted token, count and status bit-exact given the
-same Philox uniforms.  Accept decisions use the same fp64 division on both
-sides and are exact; a correction/bonus index is compared unless the oracle's
-running sum lies within 1e-7 (relative to the row's mass) of the draw point:
-the kernel forms each residual in fp32 (one rounding, at most 2^-24 of the
-element) and sums those with error-free compensated steps, so its running
+same Philox uniforms, except for draws within 1e-7 (relative) of a decision
+boundary.  The kernel decides acceptance by the exact test u*q < p (an exact
+fp32 two-product) where the oracle compares u with the fp64 quotient p/q: the
+two can differ only when u lies within one rounding of p/q.  A
+correction/bonus index is compared unless the oracle's running sum lies within
+1e-7 (relative to the row's mass) of the draw point: the kernel forms each
+residual in fp32 (one rounding, at most 2^-24 of the element) and sums those
+with error-free compensated steps and double-float prefixes, so its running
 sums agree with the exact fp64 sums to 2^-24 = 6e-8 of their value."""
 import ctypes
 import math
