@@ -99,6 +99,18 @@ __device__ __forceinline__ bool accept_draft(float u, float pj, float qj) {
 }
 
 __device__ __forceinline__ bool prob_ok(float v) { return isfinite(v) && v >= 0.0f; }
+// prob_ok over many values at two instructions each: nanchk accumulates
+// v * 0, which stays 0 for every finite v and turns NaN for a NaN or an
+// infinity (no overflow is possible), and mn tracks the minimum (fminf
+// ignores NaN, which nanchk catches).  Every value passed prob_ok iff
+// nanchk == 0 and mn >= 0 at the end (-0.0 passes both, as it does prob_ok).
+__device__ __forceinline__ void check_value4(float& nanchk, float& mn, float4 v) {
+  nanchk = fmaf(v.x, 0.0f, nanchk);
+  nanchk = fmaf(v.y, 0.0f, nanchk);
+  nanchk = fmaf(v.z, 0.0f, nanchk);
+  nanchk = fmaf(v.w, 0.0f, nanchk);
+  mn = fminf(mn, fminf(fminf(v.x, v.y), fminf(v.z, v.w)));
+}
 
 // weight of element v: residual max(p - q, 0) when q != nullptr, else p.
 __device__ __forceinline__ float weight_of(float pv, float qv, bool residual) {
@@ -348,21 +360,30 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
         const float* sp = reinterpret_cast<const float*>(ring + slot * kStageBytes) + i * kChunk;
         const float* sq = sp + kStageChunks * kChunk;
         const int base = (c_begin + li) * kChunk;
-        float hi = 0.0f, lo = 0.0f;
+        // four independent compensated sums per lane (one per vector
+        // component: a shorter dependent chain), merged after the loop
+        float h0 = 0.0f, l0 = 0.0f, h1 = 0.0f, l1 = 0.0f, h2 = 0.0f, l2 = 0.0f, h3 = 0.0f, l3 = 0.0f;
+        float nanchk = 0.0f, mn = 0.0f;  // see check_value
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int off = 4 * (lane + 32 * k);
           if (base + off < V) {
             const float4 pv = *reinterpret_cast<const float4*>(sp + off);
             const float4 qv = residual ? *reinterpret_cast<const float4*>(sq + off) : make_float4(0.f, 0.f, 0.f, 0.f);
-            bad |= !(prob_ok(pv.x) && prob_ok(pv.y) && prob_ok(pv.z) && prob_ok(pv.w));
-            if (residual) bad |= !(prob_ok(qv.x) && prob_ok(qv.y) && prob_ok(qv.z) && prob_ok(qv.w));
-            acc_add(hi, lo, weight_of(pv.x, qv.x, residual));
-            acc_add(hi, lo, weight_of(pv.y, qv.y, residual));
-            acc_add(hi, lo, weight_of(pv.z, qv.z, residual));
-            acc_add(hi, lo, weight_of(pv.w, qv.w, residual));
+            check_value4(nanchk, mn, pv);
+            if (residual) check_value4(nanchk, mn, qv);
+            acc_add(h0, l0, weight_of(pv.x, qv.x, residual));
+            acc_add(h1, l1, weight_of(pv.y, qv.y, residual));
+            acc_add(h2, l2, weight_of(pv.z, qv.z, residual));
+            acc_add(h3, l3, weight_of(pv.w, qv.w, residual));
           }
         }
+        bad |= !(nanchk == 0.0f) || mn < 0.0f;
+        float hi = h0, lo = l0;
+        acc_add(hi, lo, h1);
+        acc_add(hi, lo, h2);
+        acc_add(hi, lo, h3);
+        lo += (l1 + l2) + l3;
         warp_two_sum(hi, lo);
         __syncwarp();
         if (lane == 0) {

@@ -95,6 +95,37 @@ def test_error_statuses():
     assert g["status"][3] in (ov.STATUS_ZERO_RESIDUAL, ov.STATUS_INVALID_DRAFT)
 
 
+@pytest.mark.parametrize("V", [4096, 4097])
+def test_invalid_values_in_the_sampled_rows(V):
+    """NaN, infinities and negatives anywhere in the row pair (or bonus row) a
+    round samples from give INVALID_PROBS, as the oracle's row check does;
+    -0.0 and huge finite values are valid probabilities there.  Position 0 is
+    rejected for sure (p[y0] = 0 < q[y0]), so row pair 0 is the one scanned;
+    the bad value sits in a chunk other than the chosen one for half the
+    requests.  V = 4097 takes the scalar-load path."""
+    R = 12
+    case = synth.make_small_verify_case(9, R=R, gamma=2, V=V, overlap="none")
+    p, q, y = case["p"].clone(), case["q"].clone(), case["draft"].clone()
+    for r in range(R):
+        p[r, 0, y[r, 0]] = 0.0
+    far = [5, V - 3]  # first and last chunk of the row
+    bad = [("p", float("nan")), ("q", float("nan")), ("p", float("inf")), ("q", float("inf")),
+           ("p", -float("inf")), ("q", -1e-30), ("p", -0.0), ("p", 3.0e38)]
+    for r, (row, val) in enumerate(bad):
+        t = p if row == "p" else q
+        idx = far[r % 2]
+        if idx == int(y[r, 0]):
+            idx += 1
+        t[r, 0, idx] = val
+    g, ref = run_both({"p": p, "q": q, "draft": y}, 3, 0)
+    np.testing.assert_array_equal(g["status"], ref["status"])
+    np.testing.assert_array_equal(g["accepted"], ref["accepted"])
+    assert list(g["status"][:6]) == [ov.STATUS_INVALID_PROBS] * 6
+    assert g["status"][6] == ov.STATUS_OK and g["status"][7] == ov.STATUS_OK
+    keep = ref["margin"] > MARGIN
+    np.testing.assert_array_equal(g["next_token"][keep], ref["token"][keep])
+
+
 @pytest.mark.parametrize("V", [3, 4])
 def test_expected_emitted_monte_carlo(V):
     """E[N_emit] = (1 - α^{γ+1}) / (1 - α) at α = 0.7, γ = 3 and 4."""
