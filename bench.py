@@ -599,11 +599,26 @@ def run_ours(args):
         read_ms.append(c0.elapsed_time(c1))
     read_us = 1e3 * sorted(read_ms[2:])[len(read_ms[2:]) // 2]
     del src_buf
+    # what the same event pair reads around a kernel that does nothing (a one-element fill after
+    # the same flush): launch latency and event overhead that every timed launch carries
+    floor_ms = []
+    for _ in range(40):
+        flush()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record()
+        sink.fill_(0.0)
+        c1.record()
+        torch.cuda.synchronize()
+        floor_ms.append(c0.elapsed_time(c1))
+    floor_us = 1e3 * sorted(floor_ms[5:])[len(floor_ms[5:]) // 2]
+    net_us = 1e3 * v_ms_mean - floor_us
     verify = {"rows_per_s": world * vcfg.R * (vcfg.gamma + 1) / (v_ms_mean / 1e3),
               "same_size_read_us": read_us,
               "requests_per_s": world * vcfg.R / (v_ms_mean / 1e3), "us_per_call": 1e3 * v_ms_mean,
               "algorithmic_bytes_per_call": float(vbytes.mean()), "achieved_gbs": v_gbs, "peak_gbs": hbm_peak,
-              "frac": v_gbs / hbm_peak, "mean_accepted": float(acc.mean()), "status_nonzero": int((st != 0).sum())}
+              "frac": v_gbs / hbm_peak, "mean_accepted": float(acc.mean()), "status_nonzero": int((st != 0).sum()),
+              "event_floor_us": floor_us,
+              "frac_net_of_event_floor": (float(vbytes.mean()) / (net_us / 1e6) / 1e9 / hbm_peak) if net_us > 0 else None}
 
     # whole-step roofline (the metric's "% of roofline")
     step_rl = step_roofline(cfg, batch["seg"], counts, float(vbytes.mean()), step_ms_max, peaks)
