@@ -9,7 +9,9 @@
 // of two 128-query tiles sharing 128-key blocks fed by TMA, S = Q K^T and
 // O += P V accumulated in TMEM, softmax warps reading S with tcgen05.ld and
 // writing P back into TMEM as bf16 for the P V product.
-// bf16 backward: flash-attention-2 form on mma.sync (flash_attn_bwd_kernel).
+// bf16 backward: tcgen05 kernel (attn_bwd_tc_kernel below): one CTA per
+// 128-key block, S^T and dP^T in TMEM, dV and dK accumulated in TMEM, dQ
+// formed per query block in TMEM and added to global memory with atomics.
 // f32 path (small shapes): one warp per (query row, head), scores staged in
 // shared memory, fp32 throughout.
 #include <cuda.h>
@@ -32,78 +34,7 @@ mtp_status attn_bwd_launch(const __nv_bfloat16* qkv, const __nv_bfloat16* o, con
 
 namespace {
 
-constexpr int kBQ = 64;
-constexpr int kBK = 64;
-constexpr int kThreads = 128;
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// byte offset of element (row, col) in a [rows][HD] bf16 tile whose 16-byte
-// chunks are XOR-swizzled by (row & 7)
-template <int HD>
-__device__ __forceinline__ uint32_t swz(int row, int col) {
-  return static_cast<uint32_t>(row * HD * 2 + ((((col >> 3) ^ (row & 7))) << 4) + (col & 7) * 2);
-}
-
-// rows [row0, row0+64) of one head from the [B*T, 3d] qkv tensor (column
-// offset col0 selects q/k/v and the head); rows >= T are zero-filled.
-template <int HD>
-__device__ __forceinline__ void load_tile(uint32_t tile, const __nv_bfloat16* qkv, int b, int T, int ld3,
-                                          int row0, int col0) {
-  constexpr int kChunks = kBK * HD / 8;
-#pragma unroll
-  for (int i = threadIdx.x; i < kChunks; i += kThreads) {
-    const int r = i / (HD / 8), c = i % (HD / 8);
-    const int t = row0 + r;
-    const bool ok = t < T;
-    const __nv_bfloat16* src = qkv + (static_cast<size_t>(b) * T + (ok ? t : 0)) * ld3 + col0 + c * 8;
-    cp_async16(tile + swz<HD>(r, c * 8), src, ok);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Backward, flash-attention-2 form: one CTA per (64-key block, head, packed
-// row).  K and V of the block stay in shared memory; every 64-query block
-// that can see one of its keys streams through (Q and dO double-buffered
-// with cp.async).  Warp w owns keys 16w..16w+15:
-//   S^T = K_w Q^T, dP^T = V_w dO^T            (m16n8k16, K/V rows as A)
-//   P = exp2(S scale_log2 - lse2[q]) on visible (key, query) pairs
-//   dS^T = P (dP - D[q]),  D[q] = do_q . o_q
-//   dV_w += P^T dO,  dK_w += dS^T Q           (accumulated in registers)
-// dS^T goes to shared memory and each warp forms 16 rows of dQ = dS K,
-// added to the fp32 dq rows with atomics (every key block contributes).
-// P and dS are rounded to bf16 for the products.
-// ---------------------------------------------------------------------------
+// D[q] = dO_q . o_q for every (query row, head): one warp per item.
 template <int HD>
 __global__ void attn_dsum_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
                                  float* __restrict__ dsum, int items, int H) {
@@ -118,216 +49,6 @@ __global__ void attn_dsum_kernel(const __nv_bfloat16* __restrict__ o, const __nv
   for (int i = 0; i < KD; ++i) acc += __bfloat162float(o[base + i]) * __bfloat162float(dO[base + i]);
   acc = warp_sum(acc);
   if (lane == 0) dsum[item] = acc;
-}
-
-template <int HD>
-__global__ void __launch_bounds__(kThreads, 1)
-flash_attn_bwd_kernel(const __nv_bfloat16* __restrict__ qkv, const __nv_bfloat16* __restrict__ dO,
-                      const float* __restrict__ lse2, const float* __restrict__ dsum,
-                      const int32_t* __restrict__ seg_start, const int32_t* __restrict__ seg_end,
-                      float* __restrict__ dqkv, int T, int H, float scale_log2, float scale) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int kTile = kBK * HD * 2;
-  const uint32_t sK = smem_u32(smem);
-  const uint32_t sV = sK + kTile;
-  const uint32_t sQ0 = sV + kTile;
-  const uint32_t sdO0 = sQ0 + 2 * kTile;
-  const uint32_t sdS = sdO0 + 2 * kTile;  // [64 keys][64 queries] bf16, rows XOR-swizzled
-  uint8_t* sdS_ptr = smem + (sdS - sK);
-  float* s_lse = reinterpret_cast<float*>(sdS_ptr + kBK * kBQ * 2);  // [2][64]
-  float* s_D = s_lse + 2 * kBQ;
-  int* s_qss = reinterpret_cast<int*>(s_D + 2 * kBQ);
-  int* s_red = s_qss + 2 * kBQ;
-  const int kb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int d = H * HD, ld3 = 3 * d;
-  const int k0 = kb * kBK;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, tq = lane & 3;
-  const int32_t* ss = seg_start + static_cast<size_t>(b) * T;
-  const int32_t* se = seg_end + static_cast<size_t>(b) * T;
-
-  // the last query that sees one of the block's keys
-  int qhi = -1;
-  for (int i = threadIdx.x; i < kBK; i += kThreads) {
-    const int s = k0 + i;
-    if (s < T) qhi = max(qhi, max(se[s], s + 1) - 1);
-  }
-  qhi = __reduce_max_sync(0xffffffffu, qhi);
-  if (lane == 0) s_red[warp] = qhi;
-  __syncthreads();
-  qhi = max(max(s_red[0], s_red[1]), max(s_red[2], s_red[3]));
-  const int qb_first = kb, qb_last = qhi / kBQ;
-
-  auto load_params = [&](int buf, int qb) {
-    for (int i = threadIdx.x; i < kBQ; i += kThreads) {
-      const int q = qb * kBQ + i;
-      const bool ok = q < T;
-      const size_t item = (static_cast<size_t>(b) * T + (ok ? q : 0)) * H + h;
-      s_lse[buf * kBQ + i] = ok ? lse2[item] : INFINITY;
-      s_D[buf * kBQ + i] = ok ? dsum[item] : 0.f;
-      s_qss[buf * kBQ + i] = ok ? ss[q] : 0x7fffffff;
-    }
-  };
-  load_tile<HD>(sK, qkv, b, T, ld3, k0, d + h * HD);
-  load_tile<HD>(sV, qkv, b, T, ld3, k0, 2 * d + h * HD);
-  load_tile<HD>(sQ0, qkv, b, T, ld3, qb_first * kBQ, h * HD);
-  load_tile<HD>(sdO0, dO, b, T, d, qb_first * kBQ, h * HD);
-  cp_async_commit();
-  load_params(0, qb_first);
-
-  float dk[HD / 8][4], dv[HD / 8][4];
-#pragma unroll
-  for (int i = 0; i < HD / 8; ++i) {
-    dk[i][0] = dk[i][1] = dk[i][2] = dk[i][3] = 0.f;
-    dv[i][0] = dv[i][1] = dv[i][2] = dv[i][3] = 0.f;
-  }
-  const int key_a = k0 + warp * 16 + g, key_b = key_a + 8;
-
-  for (int qb = qb_first; qb <= qb_last; ++qb) {
-    const int buf = (qb - qb_first) & 1;
-    cp_async_wait_all();
-    __syncthreads();
-    if (qb < qb_last) {
-      const int nb = buf ^ 1;
-      load_tile<HD>(sQ0 + nb * kTile, qkv, b, T, ld3, (qb + 1) * kBQ, h * HD);
-      load_tile<HD>(sdO0 + nb * kTile, dO, b, T, d, (qb + 1) * kBQ, h * HD);
-      cp_async_commit();
-      load_params(nb, qb + 1);
-    }
-    const uint32_t sQ = sQ0 + buf * kTile, sdO = sdO0 + buf * kTile;
-    const float* lse_b = s_lse + buf * kBQ;
-    const float* D_b = s_D + buf * kBQ;
-    const int* qss_b = s_qss + buf * kBQ;
-
-    // S^T = K_w Q^T and dP^T = V_w dO^T: 16 keys x 64 queries per warp
-    float st[8][4], dp[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      st[nt][0] = st[nt][1] = st[nt][2] = st[nt][3] = 0.f;
-      dp[nt][0] = dp[nt][1] = dp[nt][2] = dp[nt][3] = 0.f;
-    }
-#pragma unroll
-    for (int kk = 0; kk < HD / 16; ++kk) {
-      uint32_t ka[4], va[4];
-      ldsm_x4(sK + swz<HD>(warp * 16 + (lane & 15), kk * 16 + (lane >> 4) * 8), ka[0], ka[1], ka[2], ka[3]);
-      ldsm_x4(sV + swz<HD>(warp * 16 + (lane & 15), kk * 16 + (lane >> 4) * 8), va[0], va[1], va[2], va[3]);
-#pragma unroll
-      for (int nt = 0; nt < 8; nt += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(sQ + swz<HD>(nt * 8 + (lane & 7) + ((lane >> 4) << 3), kk * 16 + ((lane >> 3) & 1) * 8), b0, b1,
-                b2, b3);
-        mma_bf16(st[nt], ka, b0, b1);
-        mma_bf16(st[nt + 1], ka, b2, b3);
-        ldsm_x4(sdO + swz<HD>(nt * 8 + (lane & 7) + ((lane >> 4) << 3), kk * 16 + ((lane >> 3) & 1) * 8), b0, b1,
-                b2, b3);
-        mma_bf16(dp[nt], va, b0, b1);
-        mma_bf16(dp[nt + 1], va, b2, b3);
-      }
-    }
-    // P^T (into st) and dS^T (into dp) on visible pairs: seg_start(q) <= key <= q
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int ql = nt * 8 + 2 * tq + e, q = qb * kBQ + ql;
-        const float lse = lse_b[ql], Dq = D_b[ql];
-        const int qss = qss_b[ql];
-        const bool va_ok = key_a < T && key_a >= qss && key_a <= q;
-        const bool vb_ok = key_b < T && key_b >= qss && key_b <= q;
-        const float pa = va_ok ? exp2f(st[nt][e] * scale_log2 - lse) : 0.f;
-        const float pb = vb_ok ? exp2f(st[nt][2 + e] * scale_log2 - lse) : 0.f;
-        st[nt][e] = pa;
-        st[nt][2 + e] = pb;
-        dp[nt][e] = pa * (dp[nt][e] - Dq);
-        dp[nt][2 + e] = pb * (dp[nt][2 + e] - Dq);
-      }
-    }
-    // dV_w += P^T dO and dK_w += dS^T Q (k-steps of 16 queries)
-#pragma unroll
-    for (int kt = 0; kt < 4; ++kt) {
-      uint32_t pa[4], da[4];
-      pa[0] = pack_bf16(st[2 * kt][0], st[2 * kt][1]);
-      pa[1] = pack_bf16(st[2 * kt][2], st[2 * kt][3]);
-      pa[2] = pack_bf16(st[2 * kt + 1][0], st[2 * kt + 1][1]);
-      pa[3] = pack_bf16(st[2 * kt + 1][2], st[2 * kt + 1][3]);
-      da[0] = pack_bf16(dp[2 * kt][0], dp[2 * kt][1]);
-      da[1] = pack_bf16(dp[2 * kt][2], dp[2 * kt][3]);
-      da[2] = pack_bf16(dp[2 * kt + 1][0], dp[2 * kt + 1][1]);
-      da[3] = pack_bf16(dp[2 * kt + 1][2], dp[2 * kt + 1][3]);
-#pragma unroll
-      for (int dt = 0; dt < HD / 8; dt += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sdO + swz<HD>(kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, dt * 8 + (lane >> 4) * 8), b0, b1, b2,
-                  b3);
-        mma_bf16(dv[dt], pa, b0, b1);
-        mma_bf16(dv[dt + 1], pa, b2, b3);
-        ldsm_x4_t(sQ + swz<HD>(kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, dt * 8 + (lane >> 4) * 8), b0, b1, b2,
-                  b3);
-        mma_bf16(dk[dt], da, b0, b1);
-        mma_bf16(dk[dt + 1], da, b2, b3);
-      }
-    }
-    // dS^T to shared memory (row = key, column = query)
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const int col = nt * 8 + 2 * tq;
-      *reinterpret_cast<uint32_t*>(sdS_ptr + swz<64>(warp * 16 + g, col)) = pack_bf16(dp[nt][0], dp[nt][1]);
-      *reinterpret_cast<uint32_t*>(sdS_ptr + swz<64>(warp * 16 + g + 8, col)) = pack_bf16(dp[nt][2], dp[nt][3]);
-    }
-    __syncthreads();
-    // dQ rows 16w..16w+15 of the query block: dS (A, read transposed) times K (B, read transposed)
-    float dq[HD / 8][4];
-#pragma unroll
-    for (int i = 0; i < HD / 8; ++i) dq[i][0] = dq[i][1] = dq[i][2] = dq[i][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < kBK / 16; ++kk) {
-      uint32_t a[4];
-      ldsm_x4_t(sdS + swz<64>(kk * 16 + (lane & 7) + ((lane >> 4) << 3), warp * 16 + ((lane >> 3) & 1) * 8), a[0],
-                a[1], a[2], a[3]);
-#pragma unroll
-      for (int dt = 0; dt < HD / 8; dt += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sK + swz<HD>(kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, dt * 8 + (lane >> 4) * 8), b0, b1, b2,
-                  b3);
-        mma_bf16(dq[dt], a, b0, b1);
-        mma_bf16(dq[dt + 1], a, b2, b3);
-      }
-    }
-    const int qa_row = qb * kBQ + warp * 16 + g, qb_row = qa_row + 8;
-#pragma unroll
-    for (int dt = 0; dt < HD / 8; ++dt) {
-      const int col = h * HD + dt * 8 + 2 * tq;
-      if (qa_row < T) {
-        float* dst = dqkv + (static_cast<size_t>(b) * T + qa_row) * ld3 + col;
-        atomicAdd(dst, dq[dt][0] * scale);
-        atomicAdd(dst + 1, dq[dt][1] * scale);
-      }
-      if (qb_row < T) {
-        float* dst = dqkv + (static_cast<size_t>(b) * T + qb_row) * ld3 + col;
-        atomicAdd(dst, dq[dt][2] * scale);
-        atomicAdd(dst + 1, dq[dt][3] * scale);
-      }
-    }
-  }
-  // dK (scaled) and dV of the warp's 16 keys
-#pragma unroll
-  for (int dt = 0; dt < HD / 8; ++dt) {
-    const int col = h * HD + dt * 8 + 2 * tq;
-    if (key_a < T) {
-      float* r = dqkv + (static_cast<size_t>(b) * T + key_a) * ld3;
-      r[d + col] = dk[dt][0] * scale;
-      r[d + col + 1] = dk[dt][1] * scale;
-      r[2 * d + col] = dv[dt][0];
-      r[2 * d + col + 1] = dv[dt][1];
-    }
-    if (key_b < T) {
-      float* r = dqkv + (static_cast<size_t>(b) * T + key_b) * ld3;
-      r[d + col] = dk[dt][2] * scale;
-      r[d + col + 1] = dk[dt][3] * scale;
-      r[2 * d + col] = dv[dt][2];
-      r[2 * d + col + 1] = dv[dt][3];
-    }
-  }
 }
 
 // f32: one warp per (row, head); scores of the row's keys staged in smem.
@@ -871,6 +592,441 @@ mtp_status attn_tc2_launch(const __nv_bfloat16* qkv, __nv_bfloat16* out, const i
 }
 
 
+// ---------------------------------------------------------------------------
+// Backward on the tcgen05 tensor cores (bf16, head_dim 64 or 128).
+//
+// One CTA per (128-key block j, head, packed row); every 128-query block i
+// that can see one of the block's keys streams through.  K_j and V_j stay in
+// shared memory (TMA, K-major with the 128-byte swizzle); Q_i and dO_i arrive
+// by TMA into a ring, beside each query's lse2 and D = rowsum(dO * O) staged
+// by the producer warp.  A key sees the queries key <= q < max(seg_end(key),
+// key + 1): the forward's rule seg_start(q) <= key <= q read from the key's
+// side (a pad sees only itself).  With one TMEM lane per key:
+//   S^T = K_j Q_i^T, dP^T = V_j dO_i^T          (TMEM columns 0 and 128)
+//   P^T = 2^(S^T scale_log2 - lse2) on the visible pairs, dS^T = P^T (dP^T - D)
+//                                               (warps 0-7: two warps per lane
+//                                               quadrant, one per 64 queries;
+//                                               P^T and dS^T go back into the
+//                                               first halves of their columns
+//                                               as bf16 pairs once both warps
+//                                               have read their scores, and
+//                                               dS^T into shared memory)
+//   dK_j += dS^T Q_i                            (A from TMEM; B = Q_i read
+//                                               MN-major from its tile)
+//   dQ_i = dS K_j                               (A = the staged dS^T read
+//                                               MN-major, B = K_j MN-major; into
+//                                               TMEM columns 128.., after dK
+//                                               has read dS^T there)
+//   dV_j += P^T dO_i                            (A from TMEM, B = dO_i MN-major)
+// As soon as dQ_i is formed, warps 0-7 read it (a query row per thread, half
+// the columns per warp group), pass it through shared memory so each access
+// covers four rows of 128 bytes, and add it, scaled, to the fp32 dq rows with
+// vector reductions (every key block of the segment contributes); at the end
+// they store dV_j and dK_j (scaled) the same way.  Warp 8 issues the TMA loads,
+// warp 9 allocates TMEM and issues the MMAs.  The MMAs of the one issuing
+// thread run in order, so a product may overwrite TMEM columns that an earlier
+// product read as its A operand.  P and dS are rounded to bf16 for the
+// products.  Every wait is bounded.
+// ---------------------------------------------------------------------------
+constexpr int kBwdThreads = 320;
+
+// two sets of 32 consecutive fp32 TMEM columns of this thread's lane, one wait
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&a)[32], float (&b)[32]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(ta), "r"(tb)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    a[i] = __uint_as_float(r[i]);
+    b[i] = __uint_as_float(r[32 + i]);
+  }
+}
+
+// A warp's 32 rows x 32 fp32 columns (a row per lane, as TMEM hands them out) go
+// through its own 4 KB of shared memory (16-byte chunks XOR-swizzled by row) so
+// that each global access of the warp covers 4 rows x 128 contiguous bytes.
+// Lane l writes row l; then lane l owns chunk l % 8 of rows l / 8 + 4k.
+__device__ __forceinline__ void stage_rows32(uint8_t* wbuf, int lane, const float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    *reinterpret_cast<float4*>(wbuf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+        make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+}
+__device__ __forceinline__ float4 staged_chunk(const uint8_t* wbuf, int row, int chunk) {
+  return *reinterpret_cast<const float4*>(wbuf + row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// *p += v element-wise (fp32, 16-byte aligned), without returning the old value
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+template <int HD>
+struct TcBwd {
+  static constexpr int kChunks = HD / 64;
+  static constexpr int kPiece = 128 * 128;         // one [128 rows x 64 bf16] swizzled piece (16 KB)
+  static constexpr int kTile = 128 * HD * 2;       // one [128 x HD] bf16 tile
+  static constexpr int kSlots = HD == 64 ? 2 : 1;  // Q/dO ring (the next block loads early when it fits)
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTile;
+  static constexpr int kOffQ = 2 * kTile;                 // + slot * kTile
+  static constexpr int kOffdO = kOffQ + kSlots * kTile;   // + slot * kTile
+  static constexpr int kOffdS = kOffdO + kSlots * kTile;  // two 64-query pieces of [128 keys x 128 B]
+  static constexpr int kOffPar = kOffdS + 2 * kPiece;     // per slot: lse2[128], D[128]
+  static constexpr int kParFloats = 2 * 128;
+  static constexpr int kOffBar = kOffPar + kSlots * kParFloats * 4;
+  // kv_full, qdo_full[slots], qdo_empty[slots], sd_full, p_full, dq_ready, dq_free, mma_done, drain,
+  // scores_read
+  static constexpr int kNumBars = 1 + 2 * kSlots + 7;
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // TMEM base, abort flag, 4 ints of scratch
+  static constexpr int kSmemBytes = kOffMisc + 32;
+  static constexpr uint32_t kColS = 0, kColdP = 128, kColdQ = 128, kColdV = 256, kColdK = 256 + HD;
+  static_assert(kColdK + HD <= 512, "TMEM columns");
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
+                   const float* __restrict__ lse2, const float* __restrict__ dsum,
+                   const int32_t* __restrict__ seg_end, float* __restrict__ dqkv, int T, int H, float scale_log2,
+                   float scale) {
+  using C = TcBwd<HD>;
+  extern __shared__ __align__(1024) uint8_t bwd_smem[];
+  const uint32_t s0 = mtp::smem_u32(bwd_smem);
+  if (s0 & 1023u) {  // the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) atomicOr(&g_mtp_error_word, MTP_DEVERR_TIMEOUT);
+    return;
+  }
+  const uint32_t sK = s0 + C::kOffK, sV = s0 + C::kOffV, sdS = s0 + C::kOffdS;
+  const uint32_t bar0 = s0 + C::kOffBar;
+  const uint32_t kv_full = bar0;
+  auto qdo_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto qdo_empty = [&](int s) { return bar0 + 8u * (1 + C::kSlots + s); };
+  const uint32_t sd_full = bar0 + 8u * (1 + 2 * C::kSlots);
+  const uint32_t p_full = sd_full + 8u, dq_ready = sd_full + 16u, dq_free = sd_full + 24u,
+                 mma_done = sd_full + 32u, drain_bar = sd_full + 40u, scores_read = sd_full + 48u;
+  float* par = reinterpret_cast<float*>(bwd_smem + C::kOffPar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bwd_smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* red = reinterpret_cast<int*>(tmem_slot + 2);
+  unsigned int* err = &g_mtp_error_word;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int d = H * HD;
+  const size_t ld3 = 3 * static_cast<size_t>(d);
+  const int k0 = kb * 128;
+  const int32_t* se = seg_end + static_cast<size_t>(b) * T;
+
+  // the last query that sees one of the block's keys (keys past T see none)
+  int qhi = -1;
+  if (threadIdx.x < 128) {
+    const int s = k0 + static_cast<int>(threadIdx.x);
+    if (s < T) qhi = max(static_cast<int>(se[s]), s + 1) - 1;
+  }
+  qhi = __reduce_max_sync(0xffffffffu, qhi);
+  if (lane == 0 && warp < 4) red[warp] = qhi;
+  if (threadIdx.x == 0) {
+    mtp::mbar_init(kv_full, 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mtp::mbar_init(qdo_full(s), 1);
+      mtp::mbar_init(qdo_empty(s), 1);
+    }
+    mtp::mbar_init(sd_full, 1);
+    mtp::mbar_init(p_full, 256);
+    mtp::mbar_init(dq_ready, 1);
+    mtp::mbar_init(dq_free, 256);
+    mtp::mbar_init(mma_done, 1);
+    mtp::mbar_init(drain_bar, 1);
+    mtp::mbar_init(scores_read, 256);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 8 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_qkv)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_do)) : "memory");
+  }
+  if (warp == 9) mtp::tmem_alloc_cols(mtp::smem_u32(tmem_slot), 512);
+  mtp::tc_fence_before();
+  __syncthreads();
+  mtp::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int q_last = max(max(red[0], red[1]), max(red[2], red[3]));
+  const int qb_first = kb;  // a key is seen only by queries at or after it
+  const int n_blocks = q_last >= k0 ? q_last / 128 - qb_first + 1 : 0;
+  auto wait = [&](uint32_t bar, uint32_t parity) { return mtp::wait_phase(bar, parity, abort_flag, err); };
+  auto wwait = [&](uint32_t bar, uint32_t parity) { return __all_sync(0xffffffffu, wait(bar, parity)); };
+
+  if (warp == 8) {
+    // ---------------- TMA producer and per-query values ----------------
+    int loads = 0;
+    if (lane == 0) {
+      mtp::mbar_expect_tx(kv_full, 2 * C::kTile);
+      for (int c = 0; c < C::kChunks; ++c) {
+        mtp::tma_tile_2d(sK + c * C::kPiece, &tm_qkv, d + h * HD + 64 * c, b * T + k0, kv_full);
+        mtp::tma_tile_2d(sV + c * C::kPiece, &tm_qkv, 2 * d + h * HD + 64 * c, b * T + k0, kv_full);
+      }
+    }
+    for (int i = 0; i < n_blocks; ++i) {
+      const int slot = i % C::kSlots, use = i / C::kSlots;
+      if (use > 0 && !wwait(qdo_empty(slot), (use - 1) & 1)) break;
+      const int q0 = (qb_first + i) * 128;
+      // the tiles first (the barrier counts their bytes before its one arrival), then the
+      // per-query values, published by lane 0's arrival after the warp's stores
+      if (lane == 0) {
+        const uint32_t sQ = s0 + C::kOffQ + slot * C::kTile, sdO = s0 + C::kOffdO + slot * C::kTile;
+        mtp::mbar_expect_tx_noarrive(qdo_full(slot), 2 * C::kTile);
+        for (int c = 0; c < C::kChunks; ++c) {
+          mtp::tma_tile_2d(sQ + c * C::kPiece, &tm_qkv, h * HD + 64 * c, b * T + q0, qdo_full(slot));
+          mtp::tma_tile_2d(sdO + c * C::kPiece, &tm_do, h * HD + 64 * c, b * T + q0, qdo_full(slot));
+        }
+      }
+      float* p = par + slot * C::kParFloats;
+      for (int r = lane; r < 128; r += 32) {
+        const int q = q0 + r;
+        const bool live = q < T;
+        const size_t item = (static_cast<size_t>(b) * T + (live ? q : 0)) * H + h;
+        p[r] = live ? lse2[item] : INFINITY;
+        p[128 + r] = live ? dsum[item] : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) mtp::mbar_arrive1(qdo_full(slot));
+      ++loads;
+    }
+    // no copy may still be landing when the CTA leaves (matters only after an abort)
+    if (lane == 0) {
+      mtp::wait_drain(kv_full, 0, kWaitLimitCycles);
+      for (int x = loads > C::kSlots ? loads - C::kSlots : 0; x < loads; ++x)
+        mtp::wait_drain(qdo_full(x % C::kSlots), (x / C::kSlots) & 1, kWaitLimitCycles);
+    }
+  } else if (warp == 9) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = mtp::idesc_bf16_f32(128, 128, 0);
+      constexpr uint32_t idesc_kv = mtp::idesc_bf16_f32(128, HD, 2);  // A from TMEM, B MN-major
+      constexpr uint32_t idesc_q = mtp::idesc_bf16_f32(128, HD, 3);   // A and B MN-major
+      constexpr uint32_t kLbo = C::kPiece;                            // MN pieces of the K-major tiles
+      bool ok = wait(kv_full, 0), any = false;
+      for (int i = 0; i < n_blocks && ok; ++i) {
+        const int slot = i % C::kSlots;
+        const uint32_t sQ = s0 + C::kOffQ + slot * C::kTile, sdO = s0 + C::kOffdO + slot * C::kTile;
+        if (!wait(qdo_full(slot), (i / C::kSlots) & 1)) { ok = false; break; }
+        mtp::tc_fence_after();
+        // S^T = K_j Q_i^T (the previous block's P^T was read by an earlier product)
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint32_t off = (k >> 2) * C::kPiece + (k & 3) * 32;
+          mtp::umma_bf16_ss(tmem + C::kColS, mtp::sdesc_k_sw128(sK + off), mtp::sdesc_k_sw128(sQ + off), idesc_s,
+                            k > 0);
+        }
+        any = true;
+        // dP^T = V_j dO_i^T into the columns of the previous block's dQ once that has been read
+        if (i > 0 && !wait(dq_free, (i - 1) & 1)) { ok = false; break; }
+        mtp::tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint32_t off = (k >> 2) * C::kPiece + (k & 3) * 32;
+          mtp::umma_bf16_ss(tmem + C::kColdP, mtp::sdesc_k_sw128(sV + off), mtp::sdesc_k_sw128(sdO + off), idesc_s,
+                            k > 0);
+        }
+        mtp::umma_commit(sd_full);
+        if (!wait(p_full, i & 1)) { ok = false; break; }
+        mtp::tc_fence_after();
+        // dK += dS^T Q over the block's 128 queries, then dQ = dS K over the 128 keys into
+        // the columns dK has just read dS^T from, then dV += P^T dO
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mtp::umma_bf16_ts(tmem + C::kColdK, tmem + C::kColdP + 8u * k, mtp::sdesc_mn_sw128_lbo(sQ + 2048 * k, kLbo),
+                            idesc_kv, (i > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mtp::umma_bf16_ss(tmem + C::kColdQ, mtp::sdesc_mn_sw128_lbo(sdS + 2048 * k, kLbo),
+                            mtp::sdesc_mn_sw128_lbo(sK + 2048 * k, kLbo), idesc_q, k > 0);
+        mtp::umma_commit(dq_ready);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mtp::umma_bf16_ts(tmem + C::kColdV, tmem + C::kColS + 8u * k, mtp::sdesc_mn_sw128_lbo(sdO + 2048 * k, kLbo),
+                            idesc_kv, (i > 0 || k > 0) ? 1u : 0u);
+        mtp::umma_commit(qdo_empty(slot));
+      }
+      if (ok && any) mtp::umma_commit(mma_done);  // dV and dK complete
+      // every issued MMA has completed before TMEM is freed
+      if (any) {
+        mtp::umma_commit(drain_bar);
+        mtp::wait_drain(drain_bar, 0, kWaitLimitCycles);
+      }
+    }
+  } else {
+    // ---------------- warps 0-7: P^T and dS^T, then dQ ----------------
+    // Warp w serves TMEM lane quadrant w % 4 (a key row per thread for P^T and dS^T, a query
+    // row per thread for dQ); warps 0-3 take queries 0-63 of each key row and columns
+    // 0..HD/2 of dQ, warps 4-7 queries 64-127 and the other dQ columns.
+    const int grp = warp >> 2;
+    const int kr = static_cast<int>(threadIdx.x) & 127;
+    const int key = k0 + kr;
+    // the queries that see this key: [key, q_end) (empty for a key past T)
+    const int q_end = key < T ? max(static_cast<int>(se[key]), key + 1) : key;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    uint8_t* sds_row = bwd_smem + C::kOffdS + grp * C::kPiece + (kr >> 3) * 1024 + (kr & 7) * 128;
+    uint8_t* wbuf = bwd_smem + C::kOffdS + warp * 4096;  // this warp's staging area (in the dS^T tile)
+    bool ok = true;
+    for (int i = 0; i < n_blocks; ++i) {
+      const int slot = i % C::kSlots;
+      const int q0 = (qb_first + i) * 128;
+      const float* p = par + slot * C::kParFloats;
+      if (!wwait(qdo_full(slot), (i / C::kSlots) & 1)) { ok = false; break; }  // per-query values
+      if (!wwait(sd_full, i & 1)) { ok = false; break; }
+      mtp::tc_fence_after();
+      uint32_t pk[2][16], dk[2][16];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {  // 32 queries per step
+        const int c = 2 * grp + cc;
+        const int qc = q0 + 32 * c;  // first query of the chunk
+        if (!__any_sync(0xffffffffu, qc < q_end && qc + 31 >= key)) {  // the warp's keys see none of them
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pk[cc][j] = dk[cc][j] = 0u;
+        } else {
+          float sv[32], dv[32];
+          tmem_ld32x2(lane_base + C::kColS + 32 * c, lane_base + C::kColdP + 32 * c, sv, dv);
+          // the queries' values four at a time (every lane reads the same 16 bytes)
+          const float4* lse4 = reinterpret_cast<const float4*>(p + 32 * c);
+          const float4* d4 = reinterpret_cast<const float4*>(p + 128 + 32 * c);
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const float4 l4 = lse4[g], dd4 = d4[g];
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {dd4.x, dd4.y, dd4.z, dd4.w};
+            float pp[4], dd[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int q = qc + 4 * g + t;
+              const float pv = (q >= key && q < q_end) ? ex2_approx(fmaf(sv[4 * g + t], scale_log2, -lv[t])) : 0.f;
+              pp[t] = pv;
+              dd[t] = pv * (dv[4 * g + t] - dvv[t]);
+            }
+            pk[cc][2 * g] = pack2_bf16(pp[0], pp[1]);
+            pk[cc][2 * g + 1] = pack2_bf16(pp[2], pp[3]);
+            dk[cc][2 * g] = pack2_bf16(dd[0], dd[1]);
+            dk[cc][2 * g + 1] = pack2_bf16(dd[2], dd[3]);
+          }
+        }
+        // dS^T row into shared memory: query piece grp, 16-byte chunks cc * 4 + m
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int chunk = cc * 4 + m;
+          *reinterpret_cast<uint4*>(sds_row + ((chunk ^ (kr & 7)) << 4)) =
+              make_uint4(dk[cc][4 * m], dk[cc][4 * m + 1], dk[cc][4 * m + 2], dk[cc][4 * m + 3]);
+        }
+      }
+      // both halves of every key row have read their scores before P^T and dS^T overwrite
+      // them (a bounded rendezvous of warps 0-7)
+      mtp::tc_fence_before();
+      mtp::mbar_arrive1(scores_read);
+      if (!wwait(scores_read, i & 1)) { ok = false; break; }
+      mtp::tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * grp + cc;
+        mtp::tmem_st16_nowait(lane_base + C::kColS + 16 * c, pk[cc]);
+        mtp::tmem_st16_nowait(lane_base + C::kColdP + 16 * c, dk[cc]);
+      }
+      mtp::tmem_wait_st();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // dS^T for the tensor pipe
+      mtp::tc_fence_before();
+      mtp::mbar_arrive1(p_full);
+      // dQ of this query block, half of its columns
+      if (!wwait(dq_ready, i & 1)) { ok = false; break; }
+      mtp::tc_fence_after();
+      // (the staged dS^T was read by the dQ product: its tile is free until the next block)
+#pragma unroll
+      for (int c = 0; c < HD / 64; ++c) {
+        const int col0 = grp * (HD / 2) + 32 * c;
+        float v[32];
+        mtp::tmem_ld32(lane_base + C::kColdQ + col0, v);
+        stage_rows32(wbuf, lane, v);
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int r = (lane >> 3) + 4 * k;  // row of the warp's 32
+          const int q = q0 + (warp & 3) * 32 + r;
+          const float4 x = staged_chunk(wbuf, r, lane & 7);
+          if (q < T)
+            red_add_v4(dqkv + (static_cast<size_t>(b) * T + q) * ld3 + h * HD + col0 + 4 * (lane & 7), x.x * scale,
+                       x.y * scale, x.z * scale, x.w * scale);
+        }
+        __syncwarp();
+      }
+      mtp::tc_fence_before();
+      mtp::mbar_arrive1(dq_free);
+    }
+    // dV_j (warps 0-3) and dK_j, scaled (warps 4-7), once every product has completed
+    if (ok && n_blocks > 0 && wwait(mma_done, 0)) {
+      mtp::tc_fence_after();
+      const uint32_t col = grp == 0 ? C::kColdV : C::kColdK;
+      const float f = grp == 0 ? 1.f : scale;
+      const size_t part = (grp == 0 ? 2 * static_cast<size_t>(d) : d) + h * HD;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        float v[32];
+        mtp::tmem_ld32(lane_base + col + 32 * c, v);
+        stage_rows32(wbuf, lane, v);
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int r = (lane >> 3) + 4 * k;
+          const int kk = k0 + (warp & 3) * 32 + r;  // the key of staged row r
+          const float4 x = staged_chunk(wbuf, r, lane & 7);
+          if (kk < T)
+            *reinterpret_cast<float4*>(dqkv + (static_cast<size_t>(b) * T + kk) * ld3 + part + 32 * c +
+                                       4 * (lane & 7)) = make_float4(x.x * f, x.y * f, x.z * f, x.w * f);
+        }
+        __syncwarp();
+      }
+    }
+  }
+  mtp::tc_fence_before();
+  __syncthreads();
+  mtp::tc_fence_after();
+  if (warp == 9) mtp::tmem_free_cols(tmem, 512);
+}
+
+template <int HD>
+mtp_status attn_bwd_tc_launch(const __nv_bfloat16* qkv, const __nv_bfloat16* dO, const float* lse2,
+                              const float* dsum, const int32_t* seg_end, float* dqkv, int B,
+                              int T, int H, float scale_log2, float scale, cudaStream_t stream) {
+  using C = TcBwd<HD>;
+  static PerDevice attr;
+  if (!smem_limit(attr, attn_bwd_tc_kernel<HD>, C::kSmemBytes)) return MTP_ERR_CUDA;
+  if (!aligned16(qkv) || !aligned16(dO) || !aligned16(dqkv)) return MTP_ERR_ALIGNMENT;
+  const int d = H * HD;
+  const uint64_t rows = static_cast<uint64_t>(B) * T;
+  if (rows > 0x7FFFFFFFull) return MTP_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
+  CUtensorMap mq, mdo;
+  if (!tensor_map_bf16_2d(&mq, qkv, rows, 3 * d, 3 * d, 64, 128, true) ||
+      !tensor_map_bf16_2d(&mdo, dO, rows, d, d, 64, 128, true))
+    return MTP_ERR_CUDA;
+  const dim3 grid((T + 127) / 128, H, B);
+  attn_bwd_tc_kernel<HD><<<grid, kBwdThreads, C::kSmemBytes, stream>>>(mq, mdo, lse2, dsum, seg_end, dqkv, T, H,
+                                                                      scale_log2, scale);
+  note_launch();
+  MTP_LAUNCH_CHECK();
+  return MTP_OK;
+}
+
+
 }  // namespace
 
 mtp_status attn_launch(int dtype, const void* qkv, void* out, const int32_t* seg_start, int B, int T, int H,
@@ -906,7 +1062,6 @@ mtp_status attn_bwd_launch(const __nv_bfloat16* qkv, const __nv_bfloat16* o, con
                            float* dsum, int B, int T, int H, int hd, cudaStream_t stream) {
   if (B <= 0 || T <= 0) return MTP_OK;
   const int items = B * T * H;
-  const dim3 grid((T + kBK - 1) / kBK, H, B);
   const float scale = 1.0f / sqrtf(static_cast<float>(hd));
   const float scale_log2 = 1.4426950408889634f * scale;
   // dq is accumulated with atomics by every key block: start from zero
@@ -914,25 +1069,15 @@ mtp_status attn_bwd_launch(const __nv_bfloat16* qkv, const __nv_bfloat16* o, con
     return MTP_ERR_CUDA;
   if (hd == 64) {
     attn_dsum_kernel<64><<<(items + 7) / 8, 256, 0, stream>>>(o, dO, dsum, items, H);
-    constexpr int smem = (6 * kBK * 64 + kBK * kBQ) * 2 + 2 * kBQ * 12 + 64;
-    static PerDevice attr;
-    if (!smem_limit(attr, flash_attn_bwd_kernel<64>, smem)) return MTP_ERR_CUDA;
-    flash_attn_bwd_kernel<64><<<grid, kThreads, smem, stream>>>(qkv, dO, lse2, dsum, seg_start, seg_end, dqkv, T, H,
-                                                                scale_log2, scale);
-  } else if (hd == 128) {
-    attn_dsum_kernel<128><<<(items + 7) / 8, 256, 0, stream>>>(o, dO, dsum, items, H);
-    constexpr int smem = (6 * kBK * 128 + kBK * kBQ) * 2 + 2 * kBQ * 12 + 64;
-    static PerDevice attr;
-    if (!smem_limit(attr, flash_attn_bwd_kernel<128>, smem)) return MTP_ERR_CUDA;
-    flash_attn_bwd_kernel<128><<<grid, kThreads, smem, stream>>>(qkv, dO, lse2, dsum, seg_start, seg_end, dqkv, T,
-                                                                 H, scale_log2, scale);
-  } else {
-    return MTP_ERR_UNSUPPORTED;
+    mtp::note_launch();
+    return attn_bwd_tc_launch<64>(qkv, dO, lse2, dsum, seg_end, dqkv, B, T, H, scale_log2, scale, stream);
   }
-  mtp::note_launch();
-  mtp::note_launch();
-  MTP_LAUNCH_CHECK();
-  return MTP_OK;
+  if (hd == 128) {
+    attn_dsum_kernel<128><<<(items + 7) / 8, 256, 0, stream>>>(o, dO, dsum, items, H);
+    mtp::note_launch();
+    return attn_bwd_tc_launch<128>(qkv, dO, lse2, dsum, seg_end, dqkv, B, T, H, scale_log2, scale, stream);
+  }
+  return MTP_ERR_UNSUPPORTED;
 }
 
 }  // namespace mtp

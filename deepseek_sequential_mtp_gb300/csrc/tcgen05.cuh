@@ -77,6 +77,15 @@ __device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr) {
          (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
          (static_cast<uint64_t>(2) << 61);
 }
+// The same MN-major layout with another distance between the 64-element MN
+// pieces: a [128 k rows x 64] piece loaded K-major by one 128-row TMA box
+// (16 KB) serves as an MN-major operand whose K runs over those 128 rows,
+// with the pieces lbo_bytes apart.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128_lbo(uint32_t saddr, uint32_t lbo_bytes) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(lbo_bytes >> 4) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
 // Instruction descriptor of tcgen05.mma kind::f16 with bf16 A and B and an
 // fp32 accumulator: D format at bits 4-5, A / B format at 7-9 / 10-12, A / B
 // MN-major flags at bits 15 / 16 (mn_major bit 0 / bit 1), N >> 3 at 17-22,
@@ -144,6 +153,17 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 #pragma unroll
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
+// store 16 32-bit values into 16 consecutive TMEM columns of this thread's
+// lane; the caller waits (tcgen05.wait::st) before the columns are read
+__device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // store 32 fp32 values into 32 consecutive TMEM columns of this thread's lane
 // and wait until the store has completed
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
