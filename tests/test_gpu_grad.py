@@ -147,6 +147,24 @@ def test_full_chain_gradients_mid_width():
     _check_all(cfg, grads, r)
 
 
+LONG_GRAD = [
+    synth.ChainConfig(name="long_grad_hd64", B=1, T=2048, d=256, n_heads=4, head_dim=64, ffn=512, V=1000, D=1,
+                      dtype="bf16", w_std=0.05, gain_std=0.1, tokens="zipf", layout="split", split_at=1024),
+    synth.ChainConfig(name="long_grad_hd128", B=1, T=2048, d=256, n_heads=2, head_dim=128, ffn=512, V=1000, D=1,
+                      dtype="bf16", w_std=0.05, gain_std=0.1, tokens="zipf", layout="split", split_at=1024),
+]
+
+
+@pytest.mark.parametrize("cfg", LONG_GRAD, ids=lambda c: c.name)
+def test_long_segment_gradients(cfg):
+    """Two 1024-token segments at both head widths: the attention backward of
+    a 128-key block streams up to eight query blocks (every ring phase and
+    the dq reductions of many key blocks into the same rows)."""
+    out, grads, r = _run_all(cfg, 12, 0.3, "fixed")
+    assert np.isclose(out["losses"][0].item(), r["loss_total"], rtol=2e-3)
+    _check_all(cfg, grads, r)
+
+
 def test_gradients_accumulate():
     """Two calls add their gradients into the same buffers."""
     cfg = synth.SMALL_BF16
