@@ -56,7 +56,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference", "cpu-one-core"], default="ours",
                     help="cpu-one-core: internal, the single-core oracle timing (run in a child process)")
-    ap.add_argument("--e2e-steps", type=int, default=40)
+    ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-max-len", type=int, default=256, help=argparse.SUPPRESS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
