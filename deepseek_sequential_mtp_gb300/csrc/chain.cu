@@ -1289,8 +1289,8 @@ constexpr int kNormBwdRows = 16;
 __global__ void __launch_bounds__(256)
 rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, int ld_h, const int32_t* __restrict__ h_rows,
                    const __nv_bfloat16* __restrict__ g, const float* __restrict__ dy, int ld_dy, float* __restrict__ dh,
-                   int ld_dh, const int32_t* __restrict__ dh_rows, float* __restrict__ dg_part, int M, int d,
-                   float eps) {
+                   int ld_dh, const int32_t* __restrict__ dh_rows, const float* __restrict__ dh_base,
+                   float* __restrict__ dg_part, int M, int d, float eps) {
   mtp::pdl_trigger();  // a GEMM that follows may start its setup
   __shared__ float s_r[kNormBwdRows], s_mean[kNormBwdRows];
   __shared__ int s_hrow[kNormBwdRows], s_dhrow[kNormBwdRows];
@@ -1350,7 +1350,9 @@ rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, int ld_h, const int32_t*
         if (dh_rows) {
           atomicAdd(dst, v);
         } else {
-          float4 o = *dst;
+          // dh = dh_base + v when a base is given (same layout as dh), else dh += v
+          float4 o = dh_base ? *reinterpret_cast<const float4*>(dh_base + static_cast<size_t>(s_dhrow[j]) * ld_dh + i)
+                             : *dst;
           o.x += v.x;
           o.y += v.y;
           o.z += v.z;
@@ -1387,10 +1389,10 @@ __global__ void __launch_bounds__(256) colsum_add_kernel(const float* __restrict
 
 void rmsnorm_bwd(const __nv_bfloat16* h, int ld_h, const int32_t* h_rows, const __nv_bfloat16* g, const float* dy,
                  int ld_dy, float* dh, int ld_dh, const int32_t* dh_rows, float* dg, float* dg_part, int M, int d,
-                 float eps, cudaStream_t st) {
+                 float eps, cudaStream_t st, const float* dh_base = nullptr) {
   const int nb = (M + kNormBwdRows - 1) / kNormBwdRows;
-  rmsnorm_bwd_kernel<<<nb, 256, 0, st>>>(h, ld_h, h_rows, g, dy, ld_dy, dh, ld_dh, dh_rows, dg ? dg_part : nullptr,
-                                         M, d, eps);
+  rmsnorm_bwd_kernel<<<nb, 256, 0, st>>>(h, ld_h, h_rows, g, dy, ld_dy, dh, ld_dh, dh_rows, dh_base,
+                                         dg ? dg_part : nullptr, M, d, eps);
   mtp::note_launch();
   if (dg) {
     colsum_add_kernel<<<(d + 31) / 32, 256, 0, st>>>(dg_part, nb, d, dg);
@@ -1810,10 +1812,9 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
   TRY(gemm_acc(M, d, f, bb(B.dpq), 2 * f, false, wt(C.W.w_gate), d, true, fb(B.dyf), d, st, true));
   TRY(gemm_acc(M, d, f, bb(B.dpq) + f, 2 * f, false, wt(C.W.w_up), d, true, fb(B.dyf), d, st));
   // y = RMSNorm_f(a): da = dh + RMSNorm backward
-  MTP_CUDA_TRY(cudaMemcpyAsync(fb(B.daf), dh, Md * 4, cudaMemcpyDeviceToDevice, st));
   float* dgp = fb(T.dgp);
   rmsnorm_bwd(a, d, nullptr, wt(C.W.ffn_norm), fb(B.dyf), d, fb(B.daf), d, nullptr, gp(G->ffn_norm), dgp, M, d, D.eps,
-              st);
+              st, dh);
   // a = u + o Wo^T: dWo += da^T o; do = da Wo; du = da (+ the attention path)
   f32_to_bf16(fb(B.daf), d, bb(B.dab), d, M, d, st);
   if (float* gwo = gp(G->wo)) TRY(gemm_acc(d, d, M, bb(B.dab), d, true, o, d, true, gwo, d, st));
@@ -1843,9 +1844,8 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
     TRY(gemm_acc(M, d, d, bb(B.dqkvb) + static_cast<size_t>(j) * d, 3 * d, false, wqkv[j], d, true, fb(B.dxf), d, st,
                  j == 0));
   // x = RMSNorm_a(u): du = da + RMSNorm backward
-  MTP_CUDA_TRY(cudaMemcpyAsync(fb(B.duf), fb(B.daf), Md * 4, cudaMemcpyDeviceToDevice, st));
   rmsnorm_bwd(u, d, nullptr, wt(C.W.attn_norm), fb(B.dxf), d, fb(B.duf), d, nullptr, gp(G->attn_norm), dgp, M, d, D.eps,
-              st);
+              st, fb(B.daf));
   // u = c M^T: dM += du^T c; dc = du M
   f32_to_bf16(fb(B.duf), d, bb(B.dub), d, M, d, st);
   if (float* gm = gp(G->eh_proj)) TRY(gemm_acc(d, 2 * d, M, bb(B.dub), d, true, c, 2 * d, true, gm, 2 * d, st));
