@@ -1290,7 +1290,7 @@ __global__ void __launch_bounds__(256)
 rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, int ld_h, const int32_t* __restrict__ h_rows,
                    const __nv_bfloat16* __restrict__ g, const float* __restrict__ dy, int ld_dy, float* __restrict__ dh,
                    int ld_dh, const int32_t* __restrict__ dh_rows, const float* __restrict__ dh_base,
-                   float* __restrict__ dg_part, int M, int d, float eps) {
+                   bool dh_store, float* __restrict__ dg_part, int M, int d, float eps) {
   mtp::pdl_trigger();  // a GEMM that follows may start its setup
   __shared__ float s_r[kNormBwdRows], s_mean[kNormBwdRows];
   __shared__ int s_hrow[kNormBwdRows], s_dhrow[kNormBwdRows];
@@ -1350,9 +1350,11 @@ rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, int ld_h, const int32_t*
         if (dh_rows) {
           atomicAdd(dst, v);
         } else {
-          // dh = dh_base + v when a base is given (same layout as dh), else dh += v
-          float4 o = dh_base ? *reinterpret_cast<const float4*>(dh_base + static_cast<size_t>(s_dhrow[j]) * ld_dh + i)
-                             : *dst;
+          // dh = dh_base + v when a base is given (same layout as dh), dh = v when dh_store
+          // (its first writer), else dh += v
+          float4 o = dh_base    ? *reinterpret_cast<const float4*>(dh_base + static_cast<size_t>(s_dhrow[j]) * ld_dh + i)
+                     : dh_store ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                : *dst;
           o.x += v.x;
           o.y += v.y;
           o.z += v.z;
@@ -1389,9 +1391,9 @@ __global__ void __launch_bounds__(256) colsum_add_kernel(const float* __restrict
 
 void rmsnorm_bwd(const __nv_bfloat16* h, int ld_h, const int32_t* h_rows, const __nv_bfloat16* g, const float* dy,
                  int ld_dy, float* dh, int ld_dh, const int32_t* dh_rows, float* dg, float* dg_part, int M, int d,
-                 float eps, cudaStream_t st, const float* dh_base = nullptr) {
+                 float eps, cudaStream_t st, const float* dh_base = nullptr, bool dh_store = false) {
   const int nb = (M + kNormBwdRows - 1) / kNormBwdRows;
-  rmsnorm_bwd_kernel<<<nb, 256, 0, st>>>(h, ld_h, h_rows, g, dy, ld_dy, dh, ld_dh, dh_rows, dh_base,
+  rmsnorm_bwd_kernel<<<nb, 256, 0, st>>>(h, ld_h, h_rows, g, dy, ld_dy, dh, ld_dh, dh_rows, dh_base, dh_store,
                                          dg ? dg_part : nullptr, M, d, eps);
   mtp::note_launch();
   if (dg) {
@@ -1478,8 +1480,9 @@ mtp::GemmDesc gdesc(int M, int N, int K, const __nv_bfloat16* A, int lda, const 
 // per vocabulary chunk the logits are recomputed by one GEMM whose epilogue
 // writes dz = (softmax - onehot) dL/dl (the logits are never stored whole);
 // then dX += dz W_U[chunk] and, reading dz MN-major as dz^T, d_head[chunk] +=
-// dz^T X; finally the final RMSNorm's backward adds d h_t into dstate[t] and
-// accumulates d_out_norm.
+// dz^T X; finally the final RMSNorm's backward writes d h_t into dstate[t] (its
+// first writer: the heads run before the blocks, whose backward then adds the
+// next depth's contribution) and accumulates d_out_norm.
 mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_bfloat16* h_t, float* d_head,
                          float* d_out_norm) {
   using bf = __nv_bfloat16;
@@ -1515,7 +1518,7 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
   }
   float* dstate_t = C.buf<float>(T.dstate) + static_cast<size_t>(t) * M * d;
   rmsnorm_bwd(h_t, d, nullptr, out_norm, dx, d, dstate_t, d, nullptr, d_out_norm, C.buf<float>(T.dgp), M, d, D.eps,
-              C.st);
+              C.st, nullptr, true);
   MTP_LAUNCH_CHECK();
   return MTP_OK;
 }
@@ -1919,7 +1922,9 @@ extern "C" mtp_status mtp_chain_loss_grad(const mtp_dims* dims, const mtp_weight
   term_scale_kernel<<<1, 32, 0, stream>>>(sums_counts, C.buf<float>(T.scale), D.D, static_cast<double>(M), W, den,
                                           with_main);
   mtp::note_launch();
-  MTP_CUDA_TRY(cudaMemsetAsync(C.buf<float>(T.dstate), 0, static_cast<size_t>(D.D + 1) * Md * 4, stream));
+  // every term's head backward writes its dstate slice before any block adds into it; only
+  // dL/dh^0 without the main term has no head to write it first
+  if (!with_main) MTP_CUDA_TRY(cudaMemsetAsync(C.buf<float>(T.dstate), 0, Md * 4, stream));
   for (int t = with_main ? 0 : 1; t <= D.D; ++t) {
     const bf* h_t = t == 0 ? static_cast<const bf*>(h0) : hs + static_cast<size_t>(t - 1) * Md;
     TRY(head_backward(C, T, t, h_t, grads->head, grads->out_norm));
