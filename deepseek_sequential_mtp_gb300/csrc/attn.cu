@@ -1064,8 +1064,11 @@ mtp_status attn_bwd_launch(const __nv_bfloat16* qkv, const __nv_bfloat16* o, con
   const int items = B * T * H;
   const float scale = 1.0f / sqrtf(static_cast<float>(hd));
   const float scale_log2 = 1.4426950408889634f * scale;
-  // dq is accumulated with atomics by every key block: start from zero
-  if (cudaMemsetAsync(dqkv, 0, static_cast<size_t>(B) * T * 3 * H * hd * sizeof(float), stream) != cudaSuccess)
+  // dq is accumulated with reductions by every key block: its third of each row starts from
+  // zero (the dk and dv thirds are stored once, by the CTA of their key block)
+  const size_t d = static_cast<size_t>(H) * hd;
+  if (cudaMemset2DAsync(dqkv, 3 * d * sizeof(float), 0, d * sizeof(float), static_cast<size_t>(B) * T, stream) !=
+      cudaSuccess)
     return MTP_ERR_CUDA;
   if (hd == 64) {
     attn_dsum_kernel<64><<<(items + 7) / 8, 256, 0, stream>>>(o, dO, dsum, items, H);

@@ -1290,7 +1290,8 @@ __global__ void __launch_bounds__(256)
 rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, int ld_h, const int32_t* __restrict__ h_rows,
                    const __nv_bfloat16* __restrict__ g, const float* __restrict__ dy, int ld_dy, float* __restrict__ dh,
                    int ld_dh, const int32_t* __restrict__ dh_rows, const float* __restrict__ dh_base,
-                   bool dh_store, float* __restrict__ dg_part, int M, int d, float eps) {
+                   bool dh_store, __nv_bfloat16* __restrict__ dh_bf16, float* __restrict__ dg_part, int M, int d,
+                   float eps) {
   mtp::pdl_trigger();  // a GEMM that follows may start its setup
   __shared__ float s_r[kNormBwdRows], s_mean[kNormBwdRows];
   __shared__ int s_hrow[kNormBwdRows], s_dhrow[kNormBwdRows];
@@ -1343,23 +1344,32 @@ rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ h, int ld_h, const int32_t*
       acc.y += dv.y * xh.y;
       acc.z += dv.z * xh.z;
       acc.w += dv.w * xh.w;
-      if (dh) {
+      if (dh || dh_bf16) {
         const float4 v = make_float4(r * (g01.x * dv.x - xh.x * mean), r * (g01.y * dv.y - xh.y * mean),
                                      r * (g23.x * dv.z - xh.z * mean), r * (g23.y * dv.w - xh.w * mean));
-        float4* dst = reinterpret_cast<float4*>(dh + static_cast<size_t>(s_dhrow[j]) * ld_dh + i);
+        float4* dst = dh ? reinterpret_cast<float4*>(dh + static_cast<size_t>(s_dhrow[j]) * ld_dh + i) : nullptr;
         if (dh_rows) {
           atomicAdd(dst, v);
         } else {
-          // dh = dh_base + v when a base is given (same layout as dh), dh = v when dh_store
-          // (its first writer), else dh += v
-          float4 o = dh_base    ? *reinterpret_cast<const float4*>(dh_base + static_cast<size_t>(s_dhrow[j]) * ld_dh + i)
-                     : dh_store ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                : *dst;
+          // dh = [dh +] [dh_base +] v: without dh_store (or without dh) the sum starts from
+          // dh's own value, with dh_store it is dh's first writer; dh_bf16 gets the result's
+          // bf16 copy ([M, d], the next GEMM's operand)
+          float4 o = (dh_store || !dh) ? make_float4(0.f, 0.f, 0.f, 0.f) : *dst;
+          if (dh_base) {
+            const float4 b = *reinterpret_cast<const float4*>(dh_base + static_cast<size_t>(s_dhrow[j]) * ld_dh + i);
+            o.x += b.x;
+            o.y += b.y;
+            o.z += b.z;
+            o.w += b.w;
+          }
           o.x += v.x;
           o.y += v.y;
           o.z += v.z;
           o.w += v.w;
-          *dst = o;
+          if (dh) *dst = o;
+          if (dh_bf16)
+            *reinterpret_cast<uint2*>(dh_bf16 + static_cast<size_t>(s_dhrow[j]) * d + i) =
+                make_uint2(mtp::pack2_bf16(o.x, o.y), mtp::pack2_bf16(o.z, o.w));
         }
       }
     }
@@ -1391,9 +1401,10 @@ __global__ void __launch_bounds__(256) colsum_add_kernel(const float* __restrict
 
 void rmsnorm_bwd(const __nv_bfloat16* h, int ld_h, const int32_t* h_rows, const __nv_bfloat16* g, const float* dy,
                  int ld_dy, float* dh, int ld_dh, const int32_t* dh_rows, float* dg, float* dg_part, int M, int d,
-                 float eps, cudaStream_t st, const float* dh_base = nullptr, bool dh_store = false) {
+                 float eps, cudaStream_t st, const float* dh_base = nullptr, bool dh_store = false,
+                 __nv_bfloat16* dh_bf16 = nullptr) {
   const int nb = (M + kNormBwdRows - 1) / kNormBwdRows;
-  rmsnorm_bwd_kernel<<<nb, 256, 0, st>>>(h, ld_h, h_rows, g, dy, ld_dy, dh, ld_dh, dh_rows, dh_base, dh_store,
+  rmsnorm_bwd_kernel<<<nb, 256, 0, st>>>(h, ld_h, h_rows, g, dy, ld_dy, dh, ld_dh, dh_rows, dh_base, dh_store, dh_bf16,
                                          dg ? dg_part : nullptr, M, d, eps);
   mtp::note_launch();
   if (dg) {
@@ -1402,24 +1413,6 @@ void rmsnorm_bwd(const __nv_bfloat16* h, int ld_h, const int32_t* h_rows, const 
   }
 }
 
-// a += b (fp32, n elements): 16-byte steps when both bases are 16-byte aligned,
-// the n % 4 tail (or everything, unaligned) element by element
-__global__ void add_f32_kernel(float* __restrict__ a, const float* __restrict__ b, size_t n) {
-  const size_t tid = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
-  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-  const bool vec = ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 15u) == 0;
-  const size_t n4 = vec ? n / 4 : 0;
-  for (size_t i = tid; i < n4; i += stride) {
-    float4 x = reinterpret_cast<float4*>(a)[i];
-    const float4 y = reinterpret_cast<const float4*>(b)[i];
-    x.x += y.x;
-    x.y += y.y;
-    x.z += y.z;
-    x.w += y.w;
-    reinterpret_cast<float4*>(a)[i] = x;
-  }
-  for (size_t i = 4 * n4 + tid; i < n; i += stride) a[i] += b[i];
-}
 
 inline int round_up8(int v) { return (v + 7) / 8 * 8; }
 
@@ -1482,9 +1475,10 @@ mtp::GemmDesc gdesc(int M, int N, int K, const __nv_bfloat16* A, int lda, const 
 // then dX += dz W_U[chunk] and, reading dz MN-major as dz^T, d_head[chunk] +=
 // dz^T X; finally the final RMSNorm's backward writes d h_t into dstate[t] (its
 // first writer: the heads run before the blocks, whose backward then adds the
-// next depth's contribution) and accumulates d_out_norm.
+// next depth's contribution), and its bf16 copy into dstate_bf16 when given, and
+// accumulates d_out_norm.
 mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_bfloat16* h_t, float* d_head,
-                         float* d_out_norm) {
+                         float* d_out_norm, __nv_bfloat16* dstate_bf16) {
   using bf = __nv_bfloat16;
   const mtp_dims& D = C.D;
   const int M = C.M, d = D.d, V = D.V;
@@ -1518,46 +1512,12 @@ mtp_status head_backward(const Ctx& C, const TrainLayout& T, int t, const __nv_b
   }
   float* dstate_t = C.buf<float>(T.dstate) + static_cast<size_t>(t) * M * d;
   rmsnorm_bwd(h_t, d, nullptr, out_norm, dx, d, dstate_t, d, nullptr, d_out_norm, C.buf<float>(T.dgp), M, d, D.eps,
-              C.st, nullptr, true);
+              C.st, nullptr, true, dstate_bf16);
   MTP_LAUNCH_CHECK();
   return MTP_OK;
 }
 
 // ---- block backward -------------------------------------------------------
-
-// y = bf16(x) for an fp32 [R, C] matrix (row strides ldx, ldy); block rows
-// stride over matrix rows, threads over columns (no per-element division).
-// VEC: 8 columns per thread step (two 16-byte loads, one 16-byte store), for
-// C, ldx and ldy multiples of 8 and 16-byte aligned bases.
-template <bool VEC>
-__global__ void f32_to_bf16_kernel(const float* __restrict__ x, int ldx, __nv_bfloat16* __restrict__ y, int ldy, int R,
-                                   int Cn) {
-  mtp::pdl_trigger();  // a GEMM that follows may start its setup
-  for (int r = blockIdx.x; r < R; r += gridDim.x) {
-    const float* xr = x + static_cast<size_t>(r) * ldx;
-    __nv_bfloat16* yr = y + static_cast<size_t>(r) * ldy;
-    if constexpr (VEC) {
-      for (int c = 8 * threadIdx.x; c < Cn; c += 8 * blockDim.x) {
-        const float4 a = *reinterpret_cast<const float4*>(xr + c);
-        const float4 b = *reinterpret_cast<const float4*>(xr + c + 4);
-        uint4 o;
-        o.x = mtp::pack2_bf16(a.x, a.y);
-        o.y = mtp::pack2_bf16(a.z, a.w);
-        o.z = mtp::pack2_bf16(b.x, b.y);
-        o.w = mtp::pack2_bf16(b.z, b.w);
-        *reinterpret_cast<uint4*>(yr + c) = o;
-      }
-    } else {
-      for (int c = threadIdx.x; c < Cn; c += blockDim.x) yr[c] = __float2bfloat16_rn(xr[c]);
-    }
-  }
-}
-void f32_to_bf16(const float* x, int ldx, __nv_bfloat16* y, int ldy, int R, int Cn, cudaStream_t st) {
-  const bool vec = Cn % 8 == 0 && ldx % 8 == 0 && ldy % 8 == 0 && mtp::aligned16(x) && mtp::aligned16(y);
-  if (vec) f32_to_bf16_kernel<true><<<std::min(R, 16 * 152), 128, 0, st>>>(x, ldx, y, ldy, R, Cn);
-  else f32_to_bf16_kernel<false><<<std::min(R, 16 * 152), 256, 0, st>>>(x, ldx, y, ldy, R, Cn);
-  mtp::note_launch();
-}
 
 // SwiGLU backward from the recomputed pre-activations pq = [p | q] ([M, 2 ffn]
 // bf16) and dg ([M, ffn] fp32): g = silu(p) q, dp = dg q silu'(p), dq = dg silu(p).
@@ -1763,7 +1723,7 @@ mtp_status gemm_acc(int M, int N, int K, const __nv_bfloat16* A, int lda, bool a
 // gradients into `grads` (those given), dL/dh_{k-1} added into dstate[k-1],
 // the embedding rows' gradient scattered into grads->embed.
 mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B, int k, const __nv_bfloat16* h_prev,
-                          const mtp_grads* G) {
+                          const mtp_grads* G, bool with_main) {
   using bf = __nv_bfloat16;
   const mtp_dims& D = C.D;
   const int M = C.M, d = D.d, f = D.ffn, H = D.n_heads, hd = D.head_dim, i = k - 1;
@@ -1784,14 +1744,15 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
   // MN-major B operand; weight gradients dW = dY^T X read both activations
   // as MN-major operands.  Nothing is transposed in memory.
 
-  // h = a + g W_d^T: dW_d += dh^T g; dg = dh W_d; da = dh (+ the FFN path below)
-  f32_to_bf16(dh, d, bb(B.dhb), d, M, d, st);
+  // h = a + g W_d^T: dW_d += dh^T g; dg = dh W_d; da = dh (+ the FFN path below).  dh's bf16
+  // copy (B.dhb) was written by the kernel that completed dh: the next depth's backward, or
+  // the last term's head backward for the deepest depth
   {  // recompute the gate and up pre-activations p = y Wg^T, q = y Wu^T into pq = [p | q]
     mtp::GemmDesc g = gdesc(M, f, d, y, d, wt(C.W.w_gate), d);
     g.epi = mtp::EPI_STORE;
     g.out = bb(B.pq);
     g.ldo = 2 * f;
-    g.pdl = true;  // follows the conversion kernel
+    g.pdl = true;  // follows a row kernel (RMSNorm or gain reduction)
     g.b_early = true;
     TRY(mtp::gemm_bf16_launch(g, st));
     g = gdesc(M, f, d, y, d, wt(C.W.w_up), d);
@@ -1814,12 +1775,11 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
   if (float* gu = gp(G->w_up)) TRY(gemm_acc(f, d, M, bb(B.dpq) + f, 2 * f, true, y, d, true, gu, d, st));
   TRY(gemm_acc(M, d, f, bb(B.dpq), 2 * f, false, wt(C.W.w_gate), d, true, fb(B.dyf), d, st, true));
   TRY(gemm_acc(M, d, f, bb(B.dpq) + f, 2 * f, false, wt(C.W.w_up), d, true, fb(B.dyf), d, st));
-  // y = RMSNorm_f(a): da = dh + RMSNorm backward
+  // y = RMSNorm_f(a): da = dh + RMSNorm backward (fp32, and its bf16 copy for the GEMMs)
   float* dgp = fb(T.dgp);
   rmsnorm_bwd(a, d, nullptr, wt(C.W.ffn_norm), fb(B.dyf), d, fb(B.daf), d, nullptr, gp(G->ffn_norm), dgp, M, d, D.eps,
-              st, dh);
+              st, dh, true, bb(B.dab));
   // a = u + o Wo^T: dWo += da^T o; do = da Wo; du = da (+ the attention path)
-  f32_to_bf16(fb(B.daf), d, bb(B.dab), d, M, d, st);
   if (float* gwo = gp(G->wo)) TRY(gemm_acc(d, d, M, bb(B.dab), d, true, o, d, true, gwo, d, st));
   {  // do = da Wo, written in bf16 straight from the accumulator (the attention backward's input)
     mtp::GemmDesc g = gdesc(M, d, d, bb(B.dab), d, wt(C.W.wo), d);
@@ -1827,7 +1787,7 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
     g.epi = mtp::EPI_STORE;
     g.out = bb(B.dob);
     g.ldo = d;
-    g.pdl = true;  // follows a GEMM or the conversion kernel
+    g.pdl = true;  // follows a GEMM or a row kernel
     g.b_early = true;
     TRY(mtp::gemm_bf16_launch(g, st));
   }
@@ -1846,16 +1806,20 @@ mtp_status block_backward(const Ctx& C, const TrainLayout& T, const BwdLayout& B
   for (int j = 0; j < 3; ++j)
     TRY(gemm_acc(M, d, d, bb(B.dqkvb) + static_cast<size_t>(j) * d, 3 * d, false, wqkv[j], d, true, fb(B.dxf), d, st,
                  j == 0));
-  // x = RMSNorm_a(u): du = da + RMSNorm backward
-  rmsnorm_bwd(u, d, nullptr, wt(C.W.attn_norm), fb(B.dxf), d, fb(B.duf), d, nullptr, gp(G->attn_norm), dgp, M, d, D.eps,
-              st, fb(B.daf));
+  // x = RMSNorm_a(u): du = da + RMSNorm backward (only its bf16 copy is used)
+  rmsnorm_bwd(u, d, nullptr, wt(C.W.attn_norm), fb(B.dxf), d, nullptr, d, nullptr, gp(G->attn_norm), dgp, M, d, D.eps,
+              st, fb(B.daf), true, bb(B.dub));
   // u = c M^T: dM += du^T c; dc = du M
-  f32_to_bf16(fb(B.duf), d, bb(B.dub), d, M, d, st);
   if (float* gm = gp(G->eh_proj)) TRY(gemm_acc(d, 2 * d, M, bb(B.dub), d, true, c, 2 * d, true, gm, 2 * d, st));
   TRY(gemm_acc(M, 2 * d, d, bb(B.dub), d, false, wt(C.W.eh_proj), 2 * d, true, fb(B.dcf), 2 * d, st, true));
   // c = [RMSNorm_h(h_{k-1}); RMSNorm_e(E[x_{t+k}])]: dh_{k-1} += ..., dE[x_{t+k}] += ...
-  rmsnorm_bwd(h_prev, d, nullptr, wt(C.W.hnorm), fb(B.dcf), 2 * d, dh_prev, d, nullptr, gp(G->hnorm), dgp, M, d, D.eps,
-              st);
+  if (k > 1) {  // dstate[k-1] is complete after this: its bf16 copy is the next backward's input
+    rmsnorm_bwd(h_prev, d, nullptr, wt(C.W.hnorm), fb(B.dcf), 2 * d, dh_prev, d, nullptr, gp(G->hnorm), dgp, M, d,
+                D.eps, st, nullptr, false, bb(B.dhb));
+  } else {  // dL/dh^0 = (the main term's head part, in dstate[0]) + this, added into the caller's h0 gradient
+    rmsnorm_bwd(h_prev, d, nullptr, wt(C.W.hnorm), fb(B.dcf), 2 * d, G->h0, d, nullptr, gp(G->hnorm), dgp, M, d, D.eps,
+                st, G->h0 && with_main ? dh_prev : nullptr, false);
+  }
   int32_t* tok = C.buf<int32_t>(B.tok);
   shifted_tokens_kernel<<<(M + 255) / 256, 256, 0, st>>>(C.tokens, tok, M, D.T, k, D.V);
   mtp::note_launch();
@@ -1922,21 +1886,18 @@ extern "C" mtp_status mtp_chain_loss_grad(const mtp_dims* dims, const mtp_weight
   term_scale_kernel<<<1, 32, 0, stream>>>(sums_counts, C.buf<float>(T.scale), D.D, static_cast<double>(M), W, den,
                                           with_main);
   mtp::note_launch();
-  // every term's head backward writes its dstate slice before any block adds into it; only
-  // dL/dh^0 without the main term has no head to write it first
-  if (!with_main) MTP_CUDA_TRY(cudaMemsetAsync(C.buf<float>(T.dstate), 0, Md * 4, stream));
+  // every term's head backward writes its dstate slice before any block adds into it (dstate[0]
+  // is read only with the main term, whose head writes it); the deepest term's head also writes
+  // the bf16 copy the deepest block's backward starts from
   for (int t = with_main ? 0 : 1; t <= D.D; ++t) {
     const bf* h_t = t == 0 ? static_cast<const bf*>(h0) : hs + static_cast<size_t>(t - 1) * Md;
-    TRY(head_backward(C, T, t, h_t, grads->head, grads->out_norm));
+    TRY(head_backward(C, T, t, h_t, grads->head, grads->out_norm, t == D.D ? C.buf<bf>(BL.dhb) : nullptr));
   }
-  // depths D..1: each depth's state gradient is complete once the deeper depth has run
+  // depths D..1: each depth's state gradient is complete once the deeper depth has run; depth 1
+  // adds dL/dh^0 into grads->h0
   for (int k = D.D; k >= 1; --k) {
     const bf* h_prev = k == 1 ? static_cast<const bf*>(h0) : hs + static_cast<size_t>(k - 2) * Md;
-    TRY(block_backward(C, T, BL, k, h_prev, grads));
-  }
-  if (grads->h0) {
-    add_f32_kernel<<<8 * 152, 256, 0, stream>>>(grads->h0, C.buf<float>(T.dstate), Md);
-    mtp::note_launch();
+    TRY(block_backward(C, T, BL, k, h_prev, grads, with_main != 0));
   }
   MTP_LAUNCH_CHECK();
   return MTP_OK;
