@@ -930,8 +930,9 @@ def measure_e2e(cfg, vcfg, chain, batch, x, vin, steps, dev, rank, world, tokens
     chain loss and spec_verify, and reads the losses and verify outputs back
     into pinned host memory.  Input copies are double-buffered on a second
     stream, so step i+1's copy overlaps step i's kernels, as an input pipeline
-    would; the wall clock covers all copies, kernels and read-backs of the
-    `steps` steps."""
+    would, and the results are read back on a third stream after an event, so
+    the next step's kernels do not queue behind those small copies; the wall
+    clock covers all copies, kernels and read-backs of the `steps` steps."""
     import torch
 
     from deepseek_sequential_mtp_gb300 import lib
@@ -948,8 +949,13 @@ def measure_e2e(cfg, vcfg, chain, batch, x, vin, steps, dev, rank, world, tokens
     d2h = res_l[0].numel() * 4 + res_v[0].numel() * 4
     comp = torch.cuda.current_stream()
     copy_stream = torch.cuda.Stream()
+    # step results are read back on a stream of their own, so the next step's kernels do not
+    # queue behind the small device-to-host copies
+    d2h_stream = torch.cuda.Stream()
     ready = [torch.cuda.Event() for _ in range(2)]
     free = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    outs = [None, None]  # device outputs of the step that last used each slot
 
     def issue_copy(i):
         b = i % 2
@@ -969,12 +975,20 @@ def measure_e2e(cfg, vcfg, chain, batch, x, vin, steps, dev, rank, world, tokens
             b = i % 2
             comp.wait_event(ready[b])
             dx, dv = bufs[b]
+            if outs[b] is not None:  # the read-back of this slot's previous outputs has finished
+                comp.wait_event(done[b])
             o = chain.loss(dx["tokens"], dx["seg"], dx["pos"], dx["h0"], den="fixed", with_main=True)
             v = lib.spec_verify(dv["p"], dv["q"], dv["draft"], seed=7 + rank, offset=base + i)
+            outs[b] = (o, v)
             free[b].record(comp)
-            res_l[i].copy_(o["losses"], non_blocking=True)
-            for j, kk in enumerate(("accepted", "next_token", "n_emit", "status")):
-                res_v[i][j].copy_(v[kk], non_blocking=True)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(free[b])
+                res_l[i].copy_(o["losses"], non_blocking=True)
+                o["losses"].record_stream(d2h_stream)
+                for j, kk in enumerate(("accepted", "next_token", "n_emit", "status")):
+                    res_v[i][j].copy_(v[kk], non_blocking=True)
+                    v[kk].record_stream(d2h_stream)
+                done[b].record(d2h_stream)
 
     run(min(2, n), 10 ** 6)  # warm-up
     torch.cuda.synchronize()
@@ -986,7 +1000,8 @@ def measure_e2e(cfg, vcfg, chain, batch, x, vin, steps, dev, rank, world, tokens
             "d2h_bytes_per_step": int(d2h), "ms_per_step": 1e3 * per, "steps": n,
             "note": "every step copies its chain inputs (tokens, seg, pos, h0) and verify inputs (p, q, drafts) "
                     "from pinned host memory and reads its losses and verify outputs back; input copies are "
-                    "double-buffered on a second stream so step i+1's copy overlaps step i's kernels"}
+                    "double-buffered on a second stream so step i+1's copy overlaps step i's kernels, and results "
+                    "are read back on a third stream so the next step's kernels do not wait for those copies"}
 
 
 def main():
