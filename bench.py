@@ -612,12 +612,48 @@ def run_ours(args):
         floor_ms.append(c0.elapsed_time(c1))
     floor_us = 1e3 * sorted(floor_ms[5:])[len(floor_ms[5:]) // 2]
     net_us = 1e3 * v_ms_mean - floor_us
+    # the same calls replayed from a CUDA graph (48 calls over four input sets of 298 MB each, so
+    # every call reads rows no recent call touched): per-call time without the launch and event
+    # overhead of an isolated call
+    gsets = [vin] + [synth.make_verify_inputs(vcfg, seed + 100 + s_, device=dev) for s_ in range(3)]
+    gouts = [{k: torch.empty(vcfg.R, dtype=torch.int32, device=dev)
+              for k in ("accepted", "next_token", "n_emit", "status")} for _ in gsets]
+    n_graph = 48
+
+    def graph_calls():
+        for i in range(n_graph):
+            v = gsets[i % len(gsets)]
+            lib.spec_verify(v["p"], v["q"], v["draft"], seed=7 + rank, offset=5000 + i, out=gouts[i % len(gsets)])
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up off the capture
+        graph_calls()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        graph_calls()
+    graph_ms = []
+    for _ in range(5):
+        flush()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record()
+        graph.replay()
+        c1.record()
+        torch.cuda.synchronize()
+        graph_ms.append(c0.elapsed_time(c1) / n_graph)
+    lib.check_errors()
+    graph_us = 1e3 * sorted(graph_ms)[len(graph_ms) // 2]
+    del graph, gsets, gouts
     verify = {"rows_per_s": world * vcfg.R * (vcfg.gamma + 1) / (v_ms_mean / 1e3),
               "same_size_read_us": read_us,
               "requests_per_s": world * vcfg.R / (v_ms_mean / 1e3), "us_per_call": 1e3 * v_ms_mean,
               "algorithmic_bytes_per_call": float(vbytes.mean()), "achieved_gbs": v_gbs, "peak_gbs": hbm_peak,
               "frac": v_gbs / hbm_peak, "mean_accepted": float(acc.mean()), "status_nonzero": int((st != 0).sum()),
               "event_floor_us": floor_us,
+              "us_per_call_graph": graph_us,
+              "frac_graph": float(vbytes.mean()) / (graph_us / 1e6) / 1e9 / hbm_peak,
               "frac_net_of_event_floor": (float(vbytes.mean()) / (net_us / 1e6) / 1e9 / hbm_peak) if net_us > 0 else None}
 
     # whole-step roofline (the metric's "% of roofline")
