@@ -95,6 +95,32 @@ def test_error_statuses():
     assert g["status"][3] in (ov.STATUS_ZERO_RESIDUAL, ov.STATUS_INVALID_DRAFT)
 
 
+def test_accept_test_exactly_at_the_boundary():
+    """The accept rule u < min(1, p/q) is strict.  With q[y] = 1/2 and p[y] = u/2
+    (exact: u has 24 significant bits) the draw sits exactly on the boundary
+    and must be rejected; one representable step above it, accepted.  The
+    kernel's exact two-product test and the oracle's fp64 quotient both decide
+    these cases without rounding doubt, so they are compared bit for bit with no
+    knife-edge exclusion."""
+    R, V, seed, offset = 32, 16, 123, 7
+    u = np.array([ov.verify_uniforms(seed, offset, r, 0)[0] for r in range(R)])
+    rng = np.random.default_rng(5)
+    p = rng.uniform(0.01, 0.05, size=(R, 2, V)).astype(np.float32)
+    q = rng.uniform(0.01, 0.05, size=(R, 1, V)).astype(np.float32)
+    y = np.full((R, 1), 3, dtype=np.int32)
+    q[:, 0, 3] = 0.5
+    on = np.float32(u * 0.5)  # exact
+    assert np.all(on.astype(np.float64) == u * 0.5)
+    above = np.nextafter(on, np.float32(np.inf))
+    p[:, 0, 3] = np.where(np.arange(R) % 2 == 0, on, above)
+    case = {"p": torch.from_numpy(p), "q": torch.from_numpy(q), "draft": torch.from_numpy(y)}
+    g, ref = run_both(case, seed, offset)
+    expect = (np.arange(R) % 2 == 1).astype(np.int64)  # accepted drafts: 1 above the boundary, 0 on it
+    np.testing.assert_array_equal(ref["accepted"], expect)
+    np.testing.assert_array_equal(g["accepted"], expect)
+    np.testing.assert_array_equal(g["status"], ref["status"])
+
+
 @pytest.mark.parametrize("V", [4096, 4097])
 def test_invalid_values_in_the_sampled_rows(V):
     """NaN, infinities and negatives anywhere in the row pair (or bonus row) a
