@@ -58,9 +58,9 @@ constexpr int kRingBytes = kRing * kStageBytes;
 constexpr int kChunk = 1024;       // elements per chunk
 constexpr int kMaxChunks = 512;    // V <= 524288
 constexpr int kMaxGamma = 31;
-// phase C's transposed chunk (4 padding floats after every 32) reuses the ring's shared memory
-constexpr int kRescanBytes = (kChunk + kChunk / 32 * 4) * 4;
-static_assert(kRescanBytes <= kRingBytes, "the rescan staging must fit in the ring");
+// per chunk of a CTA's half: 32 lane sums and the chunk's (hi, lo) sum
+constexpr int kTableBytesPerChunk = 32 * 4 + 8;
+__host__ __device__ constexpr int chunks_per_cta(int V) { return ((V + kChunk - 1) / kChunk + kCluster - 1) / kCluster; }
 // each consumer warp must revisit the same ring slot (see the ring invariant)
 static_assert(kRing % (kConsumerWarps / kStageChunks) == 0, "ring length must be a multiple of the warp stage stride");
 
@@ -209,8 +209,9 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
   auto mbar_wait = [wait_limit](uint32_t bar, uint32_t parity) {
     return mtp::mbar_wait_bounded(bar, parity, wait_limit);
   };
-  extern __shared__ __align__(128) uint8_t ring[];   // kRing stages of p and q chunks (kRescanBytes without the ring)
-  __shared__ float2 s_all[kMaxChunks];  // CTA 0: (hi, lo) sum of every chunk of the request
+  // kRing stages of p and q chunks (with kVec4), then this CTA's lane and chunk sums
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ float2 s_tot[kCluster];  // (hi, lo) sum of each CTA's half of the row
   __shared__ __align__(8) uint64_t s_bars[2 * kRing];
   __shared__ int s_jstar, s_event, s_bad, s_timeout;
   __shared__ float s_u;
@@ -300,11 +301,14 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
   const float* prow = p + ((size_t)r * (gamma + 1) + jstar) * V;
   const float* qrow = residual ? q + ((size_t)r * gamma + jstar) * V : prow;
   const int n_chunks = (V + kChunk - 1) / kChunk;
-  const int npc = (n_chunks + kCluster - 1) / kCluster;
+  const int npc = chunks_per_cta(V);
   const int c_begin = min(n_chunks, rank * npc);
   const int n_local = min(n_chunks, c_begin + npc) - c_begin;
   bool bad = false;
-  float2* all0 = cluster.map_shared_rank(s_all, 0);  // rank 0's chunk table
+  // this CTA's tables: for each of its chunks the 32 lanes' partial sums (lane l
+  // covers elements 32l .. 32l + 31 of the chunk) and the chunk's (hi, lo) sum
+  float* s_lane = reinterpret_cast<float*>(ring + (kVec4 ? kRingBytes : 0));
+  float2* s_chunk = reinterpret_cast<float2*>(s_lane + 32 * npc);
   if constexpr (kVec4) {
     const int n_stages = kStarve ? 0 : (n_local + kStageChunks - 1) / kStageChunks;
     if (warp == kConsumerWarps) {
@@ -360,13 +364,15 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
         const float* sp = reinterpret_cast<const float*>(ring + slot * kStageBytes) + i * kChunk;
         const float* sq = sp + kStageChunks * kChunk;
         const int base = (c_begin + li) * kChunk;
-        // four independent compensated sums per lane (one per vector
-        // component: a shorter dependent chain), merged after the loop
+        // lane l sums its 32 consecutive elements, their eight 16-byte groups taken
+        // in a rotated order (group (k + l) % 8 at step k) so that the eight lanes
+        // of a quarter-warp read distinct banks; four independent compensated sums
+        // per lane (one per vector component), merged after the loop
         float h0 = 0.0f, l0 = 0.0f, h1 = 0.0f, l1 = 0.0f, h2 = 0.0f, l2 = 0.0f, h3 = 0.0f, l3 = 0.0f;
         float nanchk = 0.0f, mn = 0.0f;  // see check_value
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const int off = 4 * (lane + 32 * k);
+          const int off = 32 * lane + 4 * ((k + lane) & 7);
           if (base + off < V) {
             const float4 pv = *reinterpret_cast<const float4*>(sp + off);
             const float4 qv = residual ? *reinterpret_cast<const float4*>(sq + off) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -384,10 +390,11 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
         acc_add(hi, lo, h2);
         acc_add(hi, lo, h3);
         lo += (l1 + l2) + l3;
+        s_lane[32 * li + lane] = hi + lo;
         warp_two_sum(hi, lo);
         __syncwarp();
         if (lane == 0) {
-          all0[c_begin + li] = make_float2(hi, lo);
+          s_chunk[li] = make_float2(hi, lo);
           // a stage expects kStageChunks arrivals; in a partial last stage the
           // consumer of its first chunk also supplies those of the missing chunks
           const int nch = min(kStageChunks, n_local - st * kStageChunks);
@@ -398,11 +405,11 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
   } else {
     if (warp < kConsumerWarps) {
       for (int li = warp; li < n_local; li += kConsumerWarps) {
-        const int base = (c_begin + li) * kChunk;
+        const int base = (c_begin + li) * kChunk + 32 * lane;  // this lane's 32 consecutive elements
         float hi = 0.0f, lo = 0.0f;
 #pragma unroll 4
-        for (int i = 0; i < kChunk / 32; ++i) {
-          const int e = base + lane + 32 * i;
+        for (int i = 0; i < 32; ++i) {
+          const int e = base + i;
           float pv = 0.f, qv = 0.f;
           if (e < V) {
             pv = prow[e];
@@ -411,149 +418,102 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
           bad |= !prob_ok(pv) || (residual && !prob_ok(qv));
           acc_add(hi, lo, weight_of(pv, qv, residual));
         }
+        s_lane[32 * li + lane] = hi + lo;
         warp_two_sum(hi, lo);
-        if (lane == 0) all0[c_begin + li] = make_float2(hi, lo);
+        if (lane == 0) s_chunk[li] = make_float2(hi, lo);
       }
     }
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&s_bad, 1);
-
-  // Every CTA has pushed its chunk sums into CTA 0's table; it now ORs its
-  // error flags into CTA 0's and arrives on the cluster barrier (release).
-  // CTA 0 waits (acquire) and continues alone; the others are done.
   __syncthreads();
-  if (rank != 0 && threadIdx.x == 0) {
-    if (s_bad) atomicOr(cluster.map_shared_rank(&s_bad, 0), 1);
-    if (s_timeout) atomicOr(cluster.map_shared_rank(&s_timeout, 0), 1);
-  }
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  if (rank != 0) return;
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 
   // ---------------- phase C: locate u' * mass ----------------
-  // Warp 0 of CTA 0 alone, in double-float arithmetic (no FP64 on this
-  // latency-bound path: a chain of FP64 additions here took ~4.7 us on
-  // GB300): a prefix over the chunk sums finds the chunk holding the target,
-  // then that chunk is rescanned in index order (the row was just streamed,
-  // so its loads hit L2).
-  if (warp != 0) return;
-  int st = MTP_VERIFY_OK;
-  int cstar = -1;
-  f2 before = {0.0f, 0.0f}, target = {0.0f, 0.0f};
-  if (s_timeout) {
-    st = MTP_VERIFY_DEVICE_TIMEOUT;
-  } else if (s_bad) {
-    st = MTP_VERIFY_INVALID_PROBS;
-  } else {
-    // lane l owns chunks [l*per, (l+1)*per)
-    const int per = (n_chunks + 31) / 32;
-    const int c0 = lane * per, c1 = min(n_chunks, (lane + 1) * per);
-    f2 own = {0.0f, 0.0f};
-    for (int c = c0; c < c1; ++c) own = f2_add(own, chunk_value(s_all[c]));
-    const f2 incl = warp_inclusive_scan_f2(own);
-    const f2 excl = f2_exclusive(incl);
-    const f2 mass = f2_shfl(incl, 31);
-    if (!(mass.hi > 0.0f)) {
-      st = MTP_VERIFY_ZERO_RESIDUAL;
-    } else {
-      target = f2_scale(s_u, mass);
-      // chunk holding the target (or the last chunk with mass if rounding overshoots)
-      const unsigned over = __ballot_sync(0xffffffffu, f2_gt(incl, target));
-      const unsigned has_mass = __ballot_sync(0xffffffffu, own.hi > 0.0f);
-      const int src = over ? __ffs(over) - 1 : 31 - __clz(has_mass);
-      if (lane == src) {
-        f2 run = excl, before_last = excl;
-        int last_pos = -1;
-        for (int c = c0; c < c1; ++c) {
-          const f2 cv = chunk_value(s_all[c]);
-          const f2 next = f2_add(run, cv);
-          if (cv.hi > 0.0f) { last_pos = c; before_last = run; }
-          if (over && f2_gt(next, target)) { cstar = c; before = run; break; }
-          run = next;
-        }
-        if (cstar < 0) { cstar = last_pos; before = before_last; }
-      }
-      cstar = __shfl_sync(0xffffffffu, cstar, src);
-      before = f2_shfl(before, src);
+  // In double-float arithmetic (no FP64 on this latency-bound path: a chain of
+  // FP64 additions here took ~4.7 us on GB300).  Warp 0 of each CTA takes the
+  // prefix over its own chunks and hands its total and error flags to the other
+  // CTA; after one cluster barrier both know the mass and the target, and the
+  // CTA whose half holds the target finds the chunk, the lane range of 32
+  // elements within it (from the staged lane sums) and, loading just those 32
+  // elements of p and q again (the row was just streamed: L2), the element.
+  const int per = (n_local + 31) / 32;  // lane l owns this CTA's chunks [l*per, (l+1)*per)
+  const int c0 = min(n_local, lane * per), c1 = min(n_local, (lane + 1) * per);
+  f2 own = {0.0f, 0.0f}, incl = {0.0f, 0.0f};
+  if (warp == 0) {
+    for (int c = c0; c < c1; ++c) own = f2_add(own, chunk_value(s_chunk[c]));
+    incl = warp_inclusive_scan_f2(own);
+    const f2 total = f2_shfl(incl, 31);
+    if (lane == 0) {
+      const uint32_t peer = static_cast<uint32_t>(rank ^ 1);
+      s_tot[rank] = make_float2(total.hi, total.lo);
+      *cluster.map_shared_rank(&s_tot[rank], peer) = make_float2(total.hi, total.lo);
+      if (s_bad) atomicOr(cluster.map_shared_rank(&s_bad, peer), 1);
+      if (s_timeout) atomicOr(cluster.map_shared_rank(&s_timeout, peer), 1);
     }
   }
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (warp != 0) return;
+  int st = MTP_VERIFY_OK;
+  const f2 S0 = chunk_value(s_tot[0]), S1 = chunk_value(s_tot[1]);
+  const f2 mass = f2_add(S0, S1);
+  if (s_timeout) st = MTP_VERIFY_DEVICE_TIMEOUT;
+  else if (s_bad) st = MTP_VERIFY_INVALID_PROBS;
+  else if (!(mass.hi > 0.0f)) st = MTP_VERIFY_ZERO_RESIDUAL;
   if (st != MTP_VERIFY_OK) {
-    if (lane == 0) {
+    if (rank == 0 && lane == 0) {
       accepted[r] = jstar; next_token[r] = -1; n_emit[r] = jstar; status[r] = st;
     }
     return;
   }
-  // Rescan of chunk cstar: coalesced loads (lane l, group row k: elements
-  // 4(l + 32k) .. +3) into the ring, which is idle now (every copy into it
-  // has landed), transposed so that lane l holds elements 32l .. 32l + 31
-  // (4 padding floats after every 32 keep both 16-byte access patterns free
-  // of bank conflicts); one compensated lane sum and one warp scan pick the
-  // lane, a second warp scan over that lane's 32 elements picks the element.
-  const int cbase = cstar * kChunk;
-  float* s_w = reinterpret_cast<float*>(ring);
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int e = 4 * (lane + 32 * k);  // offset in the chunk
-    const int g = cbase + e;
-    float pv[4] = {0.f, 0.f, 0.f, 0.f}, qv[4] = {0.f, 0.f, 0.f, 0.f};
-    if (kVec4) {  // V % 4 == 0: a group is entirely inside the row or entirely past it
-      if (g < V) {
-        const float4 a = __ldcg(reinterpret_cast<const float4*>(prow + g));
-        pv[0] = a.x; pv[1] = a.y; pv[2] = a.z; pv[3] = a.w;
-        if (residual) {
-          const float4 b = __ldcg(reinterpret_cast<const float4*>(qrow + g));
-          qv[0] = b.x; qv[1] = b.y; qv[2] = b.z; qv[3] = b.w;
-        }
+  const f2 target = f2_scale(s_u, mass);
+  // the half holding the target: CTA 0's when its sum exceeds it; else CTA 1's,
+  // which also takes the rounding overshoot (no running sum above the target:
+  // the last element with weight) unless it has no mass at all
+  const int owner = f2_gt(S0, target) ? 0 : (S1.hi > 0.0f ? 1 : 0);
+  if (rank != owner) return;
+  const f2 base = rank == 0 ? f2{0.0f, 0.0f} : S0;  // the mass before this CTA's chunks
+  int cstar = -1;  // local chunk index
+  f2 before = {0.0f, 0.0f};
+  {
+    const f2 cum = f2_add(base, incl);
+    const f2 cum_excl = f2_add(base, f2_exclusive(incl));
+    const unsigned over = __ballot_sync(0xffffffffu, f2_gt(cum, target));
+    const unsigned has_mass = __ballot_sync(0xffffffffu, own.hi > 0.0f);
+    const int src = over ? __ffs(over) - 1 : 31 - __clz(has_mass);
+    if (lane == src) {
+      f2 run = cum_excl, before_last = cum_excl;
+      int last_pos = -1;
+      for (int c = c0; c < c1; ++c) {
+        const f2 cv = chunk_value(s_chunk[c]);
+        const f2 next = f2_add(run, cv);
+        if (cv.hi > 0.0f) { last_pos = c; before_last = run; }
+        if (over && f2_gt(next, target)) { cstar = c; before = run; break; }
+        run = next;
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (g + i < V) {
-          pv[i] = __ldcg(prow + g + i);
-          if (residual) qv[i] = __ldcg(qrow + g + i);
-        }
+      if (cstar < 0) { cstar = last_pos; before = before_last; }
     }
-    float4 wv;
-    wv.x = (g + 0 < V) ? weight_of(pv[0], qv[0], residual) : 0.0f;
-    wv.y = (g + 1 < V) ? weight_of(pv[1], qv[1], residual) : 0.0f;
-    wv.z = (g + 2 < V) ? weight_of(pv[2], qv[2], residual) : 0.0f;
-    wv.w = (g + 3 < V) ? weight_of(pv[3], qv[3], residual) : 0.0f;
-    *reinterpret_cast<float4*>(s_w + e + (e >> 5) * 4) = wv;
+    cstar = __shfl_sync(0xffffffffu, cstar, src);
+    before = f2_shfl(before, src);
   }
-  __syncwarp();
-  float lhi = 0.0f, llo = 0.0f;
-  int lp = -1;  // last positive element of this lane
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float4 v = *reinterpret_cast<const float4*>(s_w + 36 * lane + 4 * k);
-    acc_add(lhi, llo, v.x);
-    acc_add(lhi, llo, v.y);
-    acc_add(lhi, llo, v.z);
-    acc_add(lhi, llo, v.w);
-    const int e = 32 * lane + 4 * k;
-    if (v.x > 0.0f) lp = e;
-    if (v.y > 0.0f) lp = e + 1;
-    if (v.z > 0.0f) lp = e + 2;
-    if (v.w > 0.0f) lp = e + 3;
-  }
-  const f2 lsum = f2_norm(lhi, llo);
-  const f2 lincl = f2_add(before, warp_inclusive_scan_f2(lsum));
+  // the lane range of 32 elements within chunk cstar
+  const float lp = s_lane[32 * cstar + lane];
+  const f2 lincl = f2_add(before, warp_inclusive_scan_f2(f2{lp, 0.0f}));
   const unsigned lover = __ballot_sync(0xffffffffu, f2_gt(lincl, target));
-  const unsigned lpos = __ballot_sync(0xffffffffu, lp >= 0);
-  int pick = -1, last_pos = -1;
-  if (lpos) last_pos = cbase + __shfl_sync(0xffffffffu, lp, 31 - __clz(lpos));
-  if (lover) {
-    const int src = __ffs(lover) - 1;
-    const f2 start = f2_shfl(f2_exclusive(lincl), src);  // running sum before lane src's elements
-    const f2 start0 = (src == 0) ? before : start;
-    const float wv = s_w[36 * src + lane];
-    const f2 cum = f2_add(start0, warp_inclusive_scan_f2(f2{wv, 0.0f}));
-    const unsigned eover = __ballot_sync(0xffffffffu, wv > 0.0f && f2_gt(cum, target));
-    const unsigned epos = __ballot_sync(0xffffffffu, wv > 0.0f);
-    if (eover) pick = cbase + 32 * src + __ffs(eover) - 1;
-    else if (epos) pick = cbase + 32 * src + 31 - __clz(epos);
+  const unsigned lpos = __ballot_sync(0xffffffffu, lp > 0.0f);
+  int pick = -1;
+  if (lover || lpos) {
+    const int lsrc = lover ? __ffs(lover) - 1 : 31 - __clz(lpos);
+    const f2 lexcl = f2_exclusive(lincl);
+    const f2 start = lsrc == 0 ? before : f2_shfl(lexcl, lsrc);  // running sum before the range
+    const int e0 = (c_begin + cstar) * kChunk + 32 * lsrc;
+    const int e = e0 + lane;
+    const float w = e < V ? weight_of(__ldcg(prow + e), residual ? __ldcg(qrow + e) : 0.0f, residual) : 0.0f;
+    const f2 cum = f2_add(start, warp_inclusive_scan_f2(f2{w, 0.0f}));
+    const unsigned eover = __ballot_sync(0xffffffffu, w > 0.0f && f2_gt(cum, target));
+    const unsigned epos = __ballot_sync(0xffffffffu, w > 0.0f);
+    if (eover) pick = e0 + __ffs(eover) - 1;
+    else if (epos) pick = e0 + 31 - __clz(epos);
   }
-  if (pick < 0) pick = last_pos;
   if (lane == 0) {
     accepted[r] = jstar;
     next_token[r] = pick;
@@ -577,13 +537,16 @@ mtp_status verify_launch(int R, int gamma, int V, const float* p, const float* q
   const bool vec = (V % 4 == 0) && mtp::aligned16(p) && (gamma == 0 || mtp::aligned16(q));
   if (kStarve && !vec) return MTP_ERR_UNSUPPORTED;  // the ring exists only on the bulk-copy path
   static mtp::PerDevice attr;
-  if (vec && !mtp::smem_limit(attr, spec_verify_kernel<true, kStarve>, kRingBytes)) return MTP_ERR_CUDA;
+  const size_t tables = static_cast<size_t>(chunks_per_cta(V)) * kTableBytesPerChunk;
+  // the attribute covers the largest V this kernel takes, so it is set once per device
+  constexpr size_t kMaxVecBytes = kRingBytes + static_cast<size_t>(kMaxChunks / kCluster) * kTableBytesPerChunk;
+  if (vec && !mtp::smem_limit(attr, spec_verify_kernel<true, kStarve>, kMaxVecBytes)) return MTP_ERR_CUDA;
   if (!kStarve) mtp::prof_begin(MTP_KC_SPEC_VERIFY, stream);
   if (vec)
-    spec_verify_kernel<true, kStarve><<<R * kCluster, kThreads, kRingBytes, stream>>>(
+    spec_verify_kernel<true, kStarve><<<R * kCluster, kThreads, kRingBytes + tables, stream>>>(
         gamma, V, p, q, draft, key, olo, ohi, eos, remaining, accepted, next_token, n_emit, status, wait_limit);
   else
-    spec_verify_kernel<false, false><<<R * kCluster, kThreads, kRescanBytes, stream>>>(
+    spec_verify_kernel<false, false><<<R * kCluster, kThreads, tables, stream>>>(
         gamma, V, p, q, draft, key, olo, ohi, eos, remaining, accepted, next_token, n_emit, status, wait_limit);
   mtp::note_launch();
   if (!kStarve) mtp::prof_end(MTP_KC_SPEC_VERIFY, stream);
