@@ -17,15 +17,19 @@
 //   phase B  CTA `rank` owns half of the chunks of the one row pair (or bonus
 //            row) the round samples from.  Its producer warp streams them
 //            with one-dimensional bulk copies into a ring of shared-memory
-//            stages (mbarrier-tracked); consumer warps form residuals in fp32
-//            and compensated (hi, lo) fp32 chunk sums.
-//   phase C  CTA 0 gathers the chunk sums through distributed shared memory;
-//            its warp 0 takes their double-float prefix to find the chunk
-//            holding u' * mass, then rescans that one chunk in index order
-//            (staged, transposed, in the idle ring) to find the smallest index
-//            whose running sum exceeds it.  Nothing on phases A and C uses
-//            FP64: GB300 runs it at a small fraction of the FP32 rate, and a
-//            short chain of FP64 additions here cost microseconds.
+//            stages (mbarrier-tracked); consumer warps form residuals in fp32,
+//            each lane summing 32 consecutive elements of a chunk with
+//            compensated (hi, lo) fp32 steps; the CTA keeps every chunk's 32
+//            lane sums and its (hi, lo) total in its own shared memory.
+//   phase C  warp 0 of each CTA takes the double-float prefix over its own
+//            chunks and hands its half's total (and its error flags) to the
+//            other CTA through distributed shared memory; after one cluster
+//            barrier both know the mass and u' * mass, and the CTA whose half
+//            holds it finds the chunk, then the lane's 32-element range from
+//            the staged lane sums, then the element, reloading only those 32
+//            elements (the row was just streamed: L2).  Nothing on phases A
+//            and C uses FP64: GB300 runs it at a small fraction of the FP32
+//            rate, and a short chain of FP64 additions here cost microseconds.
 // The kernel is HBM-bound: it reads 2*V*4 bytes for a rejection, V*4 for a
 // bonus, plus 8*gamma bytes of scalars.
 // Ring invariant: a parity wait cannot tell phase u+1 from phase u-1, so no
@@ -287,7 +291,7 @@ spec_verify_kernel(int gamma, int V, const float* __restrict__ p, const float* _
     return;
   }
 
-  // ---------------- phase B: chunk sums of the sampled weights ----------------
+  // ---------------- phase B: lane and chunk sums of the sampled weights ----------------
   // CTA `rank` owns the contiguous chunks [c_begin, c_end).  Residual elements
   // are formed in fp32 (one rounding each, at most 2^-24 of the element); a
   // chunk's sum is accumulated as an unevaluated pair (hi, lo) of fp32 values
