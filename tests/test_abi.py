@@ -50,6 +50,11 @@ def test_argument_errors_return_without_launching(lib):
                            None, None, None, None, None) == 7
     assert lib.spec_verify(0, 2, 10, None, None, None, 0, 0, None, None,
                            None, None, None, None, None) == 0
+    # one past the largest draft count (31) and vocabulary (512 chunks of 1024)
+    assert lib.spec_verify(4, 32, 10, None, None, None, 0, 0, None, None,
+                           None, None, None, None, None) == 7
+    assert lib.spec_verify(4, 2, 512 * 1024 + 1, None, None, None, 0, 0, None, None,
+                           None, None, None, None, None) == 7
 
 
 def _dims(binding, **kw):

@@ -137,6 +137,23 @@ def test_exhausted_depths_contribute_zero():
     np.testing.assert_allclose(g["losses"][:2], [r["loss_total"], r["loss_main"]], rtol=1e-5)
 
 
+@pytest.mark.parametrize("name", ["small_f32_D3", "small_bf16_D2"])
+def test_all_padding_batch(name):
+    """A batch with no active position (every segment id -1): no state-valid or
+    loss-valid row at any depth, so every sum and count is zero and every loss
+    is 0 under both denominators (an empty masked mean counts as 0)."""
+    cfg = synth.CHAIN_CONFIGS[name]
+    inp = synth.make_chain_inputs(cfg, seed=2)
+    inp["seg"][:] = -1
+    for den in ("fixed", "masked_mean"):
+        g = run_gpu(cfg, to_dev(inp), den=den)
+        r = run_oracle(cfg, inp, lam=cfg.lam, den=den)
+        assert np.all(r["counts"] == 0) and r["loss_total"] == 0.0
+        assert np.all(g["sums_counts"] == 0.0)
+        assert np.all(g["losses"] == 0.0)
+        assert np.all(np.isnan(g["row_loss"]))
+
+
 def test_packing_invariance_on_gpu():
     """A packed row equals its documents run in separate rows (segment rule
     applies to the attention graph)."""

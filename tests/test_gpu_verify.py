@@ -79,6 +79,22 @@ def test_eos_budget_and_gamma_zero():
     assert np.all(g["n_emit"] == 1)
 
 
+@pytest.mark.parametrize("V", [524288, 524287])
+def test_largest_supported_sizes(V):
+    """The largest vocabulary (512 chunks of 1024, and one element short of it:
+    the scalar path with a ragged last chunk) and the largest draft count
+    (gamma = 31, one accept lane per draft); request 0 has q = p at every
+    position, so all 31 drafts are accepted and the bonus is drawn from p_31."""
+    R, gamma = 3, 31
+    case = synth.make_small_verify_case(11, R=R, gamma=gamma, V=V)
+    case["q"][0] = case["p"][0, :gamma]
+    case["draft"][0] = torch.argmax(case["q"][0], dim=-1).to(torch.int32)
+    for offset in (0, 3):
+        g, r = run_both(case, 5, offset)
+        assert_parity(g, r, max_excluded=0.34)
+        assert g["accepted"][0] == gamma and g["n_emit"][0] == gamma + 1
+
+
 def test_error_statuses():
     case = synth.make_small_verify_case(5, R=6, gamma=2, V=128, overlap="none")
     p, q, y = case["p"].clone(), case["q"].clone(), case["draft"].clone()
