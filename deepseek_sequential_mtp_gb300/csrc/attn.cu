@@ -128,10 +128,12 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // MMA thread and the softmax warps read in the same order.  Every wait is
 // bounded.
 // ---------------------------------------------------------------------------
-constexpr int kT2Threads = 320;
-
 template <int HD>
 struct Tc2Attn {
+  // softmax threads per query row: at head_dim 64 two, each taking 64 of a block's 128 keys
+  static constexpr int kHalves = HD == 64 ? 2 : 1;
+  static constexpr int kSoftmaxWarps = 8 * kHalves;
+  static constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
   static constexpr int kChunks = HD / 64;
   static constexpr int kTileBytes = 128 * 128;  // one [128 rows x 128 B] swizzled piece
   static constexpr int kQBytes = kTcQ * HD * 2;  // one tile's Q
@@ -145,17 +147,21 @@ struct Tc2Attn {
   static constexpr int kOffBar = kOffV + kVStages * kVBytes;
   static constexpr int kRing = 4;  // claimed work items published ahead of their consumers
   // readers of a ring slot: the V lane, the MMA thread and one lane of each softmax warp
-  static constexpr int kItemReaders = 10;
+  static constexpr int kItemReaders = 2 + kSoftmaxWarps;
   // q full/empty, k full/empty, v full/empty; per tile s_full, p_full, pv_done, o_free; drain;
-  // item ring full/empty
-  static constexpr int kNumBars = 2 * (kQBufs + kKStages + kVStages) + 8 + 1 + 2 * kRing;
+  // item ring full/empty; with two halves per row, per tile the block-maximum and row-sum exchanges
+  static constexpr int kNumBars = 2 * (kQBufs + kKStages + kVStages) + 8 + 1 + 2 * kRing + (kHalves > 1 ? 4 : 0);
   static constexpr int kOffItems = (kOffBar + 8 * kNumBars + 15) / 16 * 16;
-  static constexpr int kSmemBytes = kOffItems + 16 * kRing + 16;
+  // exchange between the halves of a row: block maxima [block parity][tile][half][row], row sums
+  // [tile][half][row]
+  static constexpr int kOffXchg = kOffItems + 16 * kRing + 16;
+  static constexpr int kXchgBytes = kHalves > 1 ? 4 * (2 * 2 * kHalves * 128 + 2 * kHalves * 128) : 0;
+  static constexpr int kSmemBytes = kOffXchg + kXchgBytes;
   static constexpr uint32_t kColO0 = 256;
 };
 
 template <int HD>
-__global__ void __launch_bounds__(kT2Threads, 1)
+__global__ void __launch_bounds__(Tc2Attn<HD>::kThreads, 1)
 attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant__ CUtensorMap tm64,
                 __nv_bfloat16* __restrict__ out, const int32_t* __restrict__ seg_start, int B, int T, int H,
                 float scale_log2, float* __restrict__ lse2_out, int* __restrict__ work_ctr) {
@@ -186,6 +192,9 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
   const uint32_t drain_bar = barx + 64u;
   auto it_full = [&](int i) { return barx + 72u + 8u * i; };
   auto it_empty = [&](int i) { return barx + 72u + 8u * (C::kRing + i); };
+  const uint32_t barh = barx + 72u + 16u * C::kRing;
+  auto mx_bar = [&](int x) { return barh + 8u * x; };         // two halves: block maxima exchanged
+  auto sum_bar = [&](int x) { return barh + 16u + 8u * x; };  // two halves: row sums exchanged
   // ring slot: (item, segment start of tile A's first query, of tile B's first query); item -1 ends
   int4* items = reinterpret_cast<int4*>(smem + C::kOffItems);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffItems + 16 * C::kRing);
@@ -212,9 +221,13 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
     }
     for (int x = 0; x < 2; ++x) {
       mtp::mbar_init(s_full(x), 1);
-      mtp::mbar_init(p_full(x), kTcQ);
+      mtp::mbar_init(p_full(x), kTcQ * C::kHalves);
       mtp::mbar_init(pv_done(x), 1);
-      mtp::mbar_init(o_free(x), kTcQ);
+      mtp::mbar_init(o_free(x), kTcQ * C::kHalves);
+      if (C::kHalves > 1) {
+        mtp::mbar_init(mx_bar(x), kTcQ * C::kHalves);
+        mtp::mbar_init(sum_bar(x), kTcQ * C::kHalves);
+      }
     }
     mtp::mbar_init(drain_bar, 1);
     for (int i = 0; i < C::kRing; ++i) {
@@ -225,11 +238,12 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == 8 && lane == 0) {
+  constexpr int kTmaWarp = C::kSoftmaxWarps, kMmaWarp = C::kSoftmaxWarps + 1;
+  if (warp == kTmaWarp && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm128)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm64)) : "memory");
   }
-  if (warp == 9) mtp::tmem_alloc_cols(mtp::smem_u32(tmem_slot), 512);
+  if (warp == kMmaWarp) mtp::tmem_alloc_cols(mtp::smem_u32(tmem_slot), 512);
   mtp::tc_fence_before();
   __syncthreads();
   mtp::tc_fence_after();
@@ -272,7 +286,7 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
   };
   auto wait = [&](uint32_t bar, uint32_t parity) { return mtp::wait_phase(bar, parity, abort_flag, err); };
 
-  if (warp == 8) {
+  if (warp == kTmaWarp) {
     // ---------------- TMA producers: lane 0 Q and K, lane 1 V ----------------
     if (lane < 2) {
       const bool kside = lane == 0;
@@ -350,7 +364,7 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
       for (int x = q_loads > C::kQBufs ? q_loads - C::kQBufs : 0; x < q_loads; ++x)
         mtp::wait_drain(q_full(x % C::kQBufs), (x / C::kQBufs) & 1, kWaitLimitCycles);
     }
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t idesc_s = mtp::idesc_bf16_f32(kTcQ, kTcKeys, 0);
@@ -444,13 +458,24 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
       }
     }
   } else {
-    // ---------------- softmax warpgroups: tile x = warp / 4, one query row per thread ----------------
-    const int x = warp >> 2;
-    const int row = threadIdx.x - 128 * x;
+    // ---------------- softmax: one query row per thread of each half of tile x ----------------
+    // With two halves (head_dim 64) half hf takes keys 64 hf .. 64 hf + 63 of every block: the
+    // halves agree on each block's maximum through shared memory (both then take the same
+    // running maximum), each writes its keys' P, rescales and writes half of the row's output
+    // columns, and their row sums are added at the end of the item.
+    constexpr int kH = C::kHalves;
+    constexpr int kKeysPer = kTcKeys / kH;  // a block's scores per thread
+    constexpr int kOCols = HD / kH;         // output columns per thread
+    const int x = warp / (4 * kH);
+    const int hf = (warp >> 2) % kH;
+    const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t colS = 128u * x, colO = C::kColO0 + HD * x;
+    const uint32_t colS = 128u * x, colO = C::kColO0 + HD * x + kOCols * hf;
+    float* xmax = reinterpret_cast<float*>(smem + C::kOffXchg);
+    float* xsum = xmax + 2 * 2 * kH * kTcQ;
     auto wwait = [&](uint32_t bar, uint32_t parity) { return __all_sync(0xffffffffu, wait(bar, parity)); };
-    uint32_t n = 0;  // S products of this tile consumed
+    uint32_t n = 0;   // S products of this tile consumed
+    uint32_t ns = 0;  // row-sum exchanges of this tile
     for (int tl = 0;; ++tl) {
       const int slot = tl % C::kRing;
       if (!wwait(it_full(slot), (tl / C::kRing) & 1)) break;
@@ -471,17 +496,20 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
       for (int j = R.lo[x]; j <= R.hi[x]; ++j, ++n) {
         if (!wwait(s_full(x), n & 1)) { ok = false; break; }
         mtp::tc_fence_after();
-        float sc[kTcKeys];
-        {
+        float sc[kKeysPer];
+        if constexpr (kKeysPer == 128) {
           float (&lo)[64] = *reinterpret_cast<float (*)[64]>(&sc[0]);
           float (&hi)[64] = *reinterpret_cast<float (*)[64]>(&sc[64]);
           mtp::tmem_ld64(lane_base + colS, lo);
           mtp::tmem_ld64(lane_base + colS + 64, hi);
+        } else {
+          float (&v)[64] = *reinterpret_cast<float (*)[64]>(&sc[0]);
+          mtp::tmem_ld64(lane_base + colS + kKeysPer * hf, v);
         }
-        const int key0 = j * kTcKeys;
-        if (!(key0 >= st_row && key0 + kTcKeys - 1 <= q)) {  // a block the row sees only in part
+        const int key0 = j * kTcKeys + kKeysPer * hf;
+        if (!(key0 >= st_row && key0 + kKeysPer - 1 <= q)) {  // keys the row sees only in part
 #pragma unroll
-          for (int i = 0; i < kTcKeys; ++i) {
+          for (int i = 0; i < kKeysPer; ++i) {
             const int key = key0 + i;
             if (!(key >= st_row && key <= q)) sc[i] = -INFINITY;
           }
@@ -490,9 +518,20 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx8[i] = sc[i];
 #pragma unroll
-        for (int i = 8; i < kTcKeys; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sc[i]);
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * scale_log2;
+        for (int i = 8; i < kKeysPer; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sc[i]);
+        float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * scale_log2;
+        if constexpr (kH > 1) {
+          // the block maximum over both halves of the row; this half's scores are in registers
+          // before the other half may write its P over them
+          float* xm = xmax + ((n & 1) * 2 + x) * (kH * kTcQ);
+          xm[hf * kTcQ + row] = mx;
+          mtp::tc_fence_before();
+          mtp::mbar_arrive1(mx_bar(x));
+          if (!wwait(mx_bar(x), n & 1)) { ok = false; break; }
+          mtp::tc_fence_after();
+          mx = fmaxf(mx, xm[(hf ^ 1) * kTcQ + row]);
+        }
         // a new running maximum only when the block's exceeds the stale one by 2^8
         const float m_new = mx > m + kStaleMaxLog2 ? mx : m;
         const bool rescale = m_new != m && m != -INFINITY;
@@ -501,7 +540,7 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
 #pragma unroll
         for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
 #pragma unroll
-        for (int i = 0; i < kTcKeys / 2; ++i) {  // P pairs packed in place: sc[i] holds keys 2i, 2i+1
+        for (int i = 0; i < kKeysPer / 2; ++i) {  // P pairs packed in place: sc[i] holds keys 2i, 2i+1
           const float a = ex2_approx(fmaf(sc[2 * i], scale_log2, neg_use));
           const float bb = ex2_approx(fmaf(sc[2 * i + 1], scale_log2, neg_use));
           rs8[i & 7] += a + bb;
@@ -512,7 +551,7 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
           mtp::tc_fence_after();
           const float alpha = rescale ? ex2_approx(m - m_new) : 1.f;
 #pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
+          for (int c = 0; c < kOCols / 32; ++c) {
             float o[32];
             mtp::tmem_ld32(lane_base + colO + 32 * c, o);
 #pragma unroll
@@ -523,13 +562,13 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
         }
         m = m_new;
         l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-        // P into the first 64 columns of this tile's S (the scores are in registers now; the
-        // previous block's P V completed before this block's S did)
-        {
-          float (&p0)[32] = *reinterpret_cast<float (*)[32]>(&sc[0]);
-          float (&p1)[32] = *reinterpret_cast<float (*)[32]>(&sc[32]);
-          mtp::tmem_st32(lane_base + colS, p0);
-          mtp::tmem_st32(lane_base + colS + 32, p1);
+        // P into this tile's S columns (the pair of keys 2i, 2i + 1 of the block in column i; the
+        // scores are in registers now, and the previous block's P V completed before this
+        // block's S did)
+#pragma unroll
+        for (int c = 0; c < kKeysPer / 64; ++c) {
+          float (&p)[32] = *reinterpret_cast<float (*)[32]>(&sc[32 * c]);
+          mtp::tmem_st32(lane_base + colS + (kKeysPer / 2) * hf + 32 * c, p);
         }
         mtp::tc_fence_before();
         mtp::mbar_arrive1(p_full(x));
@@ -537,11 +576,20 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
       if (!ok) break;
       if (!wwait(pv_done(x), (n - 1) & 1)) break;  // the item's last P V
       mtp::tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      if (live && lse2_out) lse2_out[(static_cast<size_t>(b) * T + q) * H + h] = m + log2f(l);
-      __nv_bfloat16* orow = out + (static_cast<size_t>(b) * T + q) * d + h * HD;
+      float lt = l;
+      if constexpr (kH > 1) {  // the row sum over both halves (the same sum, added in either order)
+        float* xs = xsum + x * (kH * kTcQ);
+        xs[hf * kTcQ + row] = l;
+        mtp::mbar_arrive1(sum_bar(x));
+        if (!wwait(sum_bar(x), ns & 1)) break;
+        lt = l + xs[(hf ^ 1) * kTcQ + row];
+        ++ns;
+      }
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      if (live && lse2_out && hf == 0) lse2_out[(static_cast<size_t>(b) * T + q) * H + h] = m + log2f(lt);
+      __nv_bfloat16* orow = out + (static_cast<size_t>(b) * T + q) * d + h * HD + kOCols * hf;
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 0; c < kOCols / 32; ++c) {
         float o[32];
         mtp::tmem_ld32(lane_base + colO + 32 * c, o);
         if (live) {
@@ -561,7 +609,7 @@ attn_tc2_kernel(const __grid_constant__ CUtensorMap tm128, const __grid_constant
   mtp::tc_fence_before();
   __syncthreads();
   mtp::tc_fence_after();
-  if (warp == 9) mtp::tmem_free_cols(tmem, 512);
+  if (warp == kMmaWarp) mtp::tmem_free_cols(tmem, 512);
 }
 
 template <int HD>
@@ -584,7 +632,7 @@ mtp_status attn_tc2_launch(const __nv_bfloat16* qkv, __nv_bfloat16* out, const i
   const int sms = sm_count_current();
   const int grid = static_cast<int>(n_items < sms ? n_items : sms);
   // the QKV projection before it releases this launch when its CTAs start their last tiles
-  MTP_CUDA_TRY(launch_pdl(attn_tc2_kernel<HD>, dim3(grid), dim3(kT2Threads), C::kSmemBytes, stream, m128, m64, out,
+  MTP_CUDA_TRY(launch_pdl(attn_tc2_kernel<HD>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, m128, m64, out,
                           seg_start, B, T, H, scale_log2, lse2_out, work_ctr));
   note_launch();
   MTP_LAUNCH_CHECK();
