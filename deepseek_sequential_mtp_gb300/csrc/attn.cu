@@ -105,16 +105,20 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // A work item is 256 consecutive queries of one (packed row, head): tile A =
 // queries q0..q0+127, tile B = q0+128..q0+255 (absent past T).  Both tiles
 // share every K/V block they need, which halves the K/V traffic per FLOP, and
-// their softmax warpgroups alternate on the tensor pipe: while warps 0-3
-// turn S_A into P_A, the MMA thread runs P_B V and S_B, and the reverse.
-//   warps 0-3 / 4-7  softmax of tile A / B, one query row per thread (TMEM
-//              lane = row): S read with tcgen05.ld, segment-causal mask,
-//              stale-by-up-to-2^8 running maximum, P = 2^(s - m) written back
-//              as bf16 pairs into the first 64 columns of the tile's own S
-//              (tcgen05.st), where the P V product reads it as its A operand.
-//   warp 8     TMA: lane 0 loads Q_A, Q_B and the K blocks, lane 1 the V
-//              blocks (MN-major [64 keys x 64 cols] boxes), each into a ring.
-//   warp 9     allocates 512 TMEM columns (S_A, S_B at 0 and 128; O_A, O_B
+// their softmax warps alternate on the tensor pipe: while tile A's turn S_A
+// into P_A, the MMA thread runs P_B V and S_B, and the reverse.
+//   softmax    tile A's warps first, then tile B's: one query row per thread
+//              (TMEM lane = row) of each warpgroup; at head_dim 64 two
+//              warpgroups per tile, each taking 64 of a block's 128 keys and
+//              agreeing on the block maximum through shared memory.  S read
+//              with tcgen05.ld, segment-causal mask, stale-by-up-to-2^8
+//              running maximum, P = 2^(s - m) written back as bf16 pairs into
+//              the first 64 columns of the tile's own S (tcgen05.st), where
+//              the P V product reads it as its A operand.
+//   TMA warp   (after the softmax warps) lane 0 loads Q_A, Q_B and the K
+//              blocks, lane 1 the V blocks (MN-major [64 keys x 64 cols]
+//              boxes), each into a ring.
+//   MMA warp   (the last) allocates 512 TMEM columns (S_A, S_B at 0 and 128; O_A, O_B
 //              at 256 and 256 + HD); one thread issues, per key block j,
 //              P_A(j) V_j, S_A(j+1), P_B(j) V_j, S_B(j+1) (S of the first
 //              block up front), skipping a tile outside its key range.
