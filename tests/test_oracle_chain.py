@@ -51,6 +51,27 @@ def test_rope_properties():
     assert np.array_equal(oc.rope(x, np.arange(5), H, hd, 0.0), x)
 
 
+def test_rope_unit_vectors():
+    """Rotate-half RoPE at head_dim 4, base 10000: coordinate i pairs with
+    i + 2 and turns by pos * 10000^(-2i/4), i.e. by pos rad for i = 0 and by
+    pos / 100 rad for i = 1; a unit vector on coordinate i lands on
+    (cos, sin) of that angle in coordinates (i, i + 2) and nowhere else.  A
+    wrong frequency exponent, pairing (adjacent instead of halves) or sign of
+    the sine fails here."""
+    p = 3.0
+    e = np.eye(4)
+    y = oc.rope(e, np.full(4, p), 1, 4, 10000.0)
+    want = np.zeros((4, 4))
+    want[0, 0], want[0, 2] = np.cos(p), np.sin(p)            # x0 -> (x0, x2), angle p
+    want[2, 2], want[2, 0] = np.cos(p), -np.sin(p)           # x2 -> rotated by the same angle
+    want[1, 1], want[1, 3] = np.cos(p / 100), np.sin(p / 100)
+    want[3, 3], want[3, 1] = np.cos(p / 100), -np.sin(p / 100)
+    np.testing.assert_allclose(y, want, atol=1e-12)
+    # two heads rotate independently with the same per-head frequencies
+    y2 = oc.rope(np.tile(e[0], (1, 2)), [p], 2, 4, 10000.0)
+    np.testing.assert_allclose(y2[0], np.tile(want[0], 2), atol=1e-12)
+
+
 def test_attention_special_cases():
     rng = np.random.default_rng(2)
     n, H, hd = 6, 2, 4
